@@ -1,0 +1,177 @@
+"""CPU oracle for DiffKV-style differentiated KV-cache compaction.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg are the only callers.  The CUDA
+library never imports this package and shares no code with it.
+
+This module is a ctypes binding over ``dkv_oracle.cpp`` (a plain,
+single-threaded C++ restatement of the method; every reading of the source page
+is listed in that file's header) plus numpy-side page parsers used by the
+tests.  Building the oracle is ``oracle.build.build_oracle()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB_PATH, build_oracle
+
+OK = 0
+E_INVAL = -1
+E_NOMEM = -2
+E_RANGE = -3
+E_LENS = -7
+
+_lib = None
+
+
+class _Batch(ctypes.Structure):
+    _fields_ = [
+        ("L", ctypes.c_int32), ("R", ctypes.c_int32), ("Hq", ctypes.c_int32),
+        ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32), ("T", ctypes.c_int64),
+        ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("sig_sum", ctypes.c_void_p),
+        ("sig_cnt", ctypes.c_void_p), ("lens", ctypes.c_void_p), ("unit_base", ctypes.c_int64),
+    ]
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [
+        ("F", ctypes.c_int64), ("P", ctypes.c_int32), ("free_list", ctypes.c_void_p),
+        ("cursors", ctypes.c_void_p), ("rev_unit", ctypes.c_void_p),
+        ("rev_idx", ctypes.c_void_p), ("page_cls", ctypes.c_void_p), ("pages", ctypes.c_void_p),
+    ]
+
+
+class _Tables(ctypes.Structure):
+    _fields_ = [
+        ("fwd", ctypes.c_void_p), ("pmax", ctypes.c_int32), ("unit_hdr", ctypes.c_void_p),
+        ("classes", ctypes.c_void_p),
+    ]
+
+
+def lib():
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            build_oracle()
+        L = ctypes.CDLL(LIB_PATH)
+        L.oracle_fp16_rn.argtypes = [ctypes.c_float]
+        L.oracle_fp16_rn.restype = ctypes.c_uint16
+        L.oracle_fp16_to_f32.argtypes = [ctypes.c_uint16]
+        L.oracle_fp16_to_f32.restype = ctypes.c_float
+        L.oracle_fp16_rn_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+        L.oracle_fp16_rn_array.restype = None
+        L.oracle_quant_row.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_quant_row.restype = ctypes.c_int32
+        L.oracle_init_pool.argtypes = [ctypes.POINTER(_Pool)]
+        L.oracle_init_pool.restype = None
+        L.oracle_compact.argtypes = [ctypes.POINTER(_Batch), ctypes.c_float, ctypes.c_float,
+                                     ctypes.POINTER(_Pool), ctypes.POINTER(_Tables),
+                                     ctypes.c_void_p]
+        L.oracle_compact.restype = ctypes.c_int32
+        L.oracle_dequant_page.argtypes = [ctypes.POINTER(_Pool), ctypes.c_int32, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_dequant_page.restype = None
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def fp16_rn(x: np.ndarray) -> np.ndarray:
+    """fp32 -> fp16 bit patterns via the oracle's own IEEE conversion."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_fp16_rn_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def fp16_to_f32(h: int) -> float:
+    return float(lib().oracle_fp16_to_f32(int(h)))
+
+
+def quant_row(x_bf16_bits: np.ndarray, bits: int):
+    """Quantise one 128-element bf16 row; returns (status, codes, s16, z16)."""
+    x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+    assert x.size == 128
+    q = np.zeros(128, dtype=np.uint8)
+    s16 = ctypes.c_uint16(0)
+    z16 = ctypes.c_uint16(0)
+    st = lib().oracle_quant_row(_ptr(x), bits, _ptr(q), ctypes.byref(s16), ctypes.byref(z16))
+    return st, q, s16.value, z16.value
+
+
+class Pool:
+    """Host-side pool state for the oracle (numpy arrays)."""
+
+    def __init__(self, F: int, P: int, allocate_pages: bool = True):
+        self.F, self.P = int(F), int(P)
+        self.free_list = np.zeros(F, dtype=np.int32)
+        self.cursors = np.zeros(2, dtype=np.uint64)
+        self.rev_unit = np.zeros(F, dtype=np.int32)
+        self.rev_idx = np.zeros(F, dtype=np.int32)
+        self.page_cls = np.zeros(F, dtype=np.uint8)
+        # np.zeros is calloc-backed: untouched pages cost no memory.
+        self.pages = np.zeros((F, 216 * P), dtype=np.uint8)
+        self.init()
+
+    def _c(self):
+        return _Pool(self.F, self.P, _ptr(self.free_list), _ptr(self.cursors), _ptr(self.rev_unit),
+                     _ptr(self.rev_idx), _ptr(self.page_cls), _ptr(self.pages))
+
+    def init(self):
+        p = self._c()
+        lib().oracle_init_pool(ctypes.byref(p))
+
+
+class Tables:
+    def __init__(self, U: int, pmax: int, rows: int):
+        self.pmax = int(pmax)
+        self.fwd = np.full((U, pmax), -7, dtype=np.int32)
+        self.unit_hdr = np.zeros((U, 4), dtype=np.int32)
+        self.classes = np.full(rows, 0xEE, dtype=np.uint8)
+
+    def _c(self):
+        return _Tables(_ptr(self.fwd), self.pmax, _ptr(self.unit_hdr), _ptr(self.classes))
+
+
+def compact(inp: dict, alpha_h: float, alpha_l: float, pool: Pool, tables: Tables,
+            quant_mask: np.ndarray | None = None) -> int:
+    """Run the oracle's prefill compaction.
+
+    ``inp`` holds numpy arrays: k, v (uint16 bf16 bits [L][T][Hkv][128]),
+    sig_sum (float32 [L][T][Hq]), sig_cnt (int32 [T]), lens (int32 [R]), the
+    ints L, R, Hq, Hkv, T and optionally unit_base (global id of the first
+    unit, for layer-at-a-time calls).
+    """
+    k = np.ascontiguousarray(inp["k"])
+    v = np.ascontiguousarray(inp["v"])
+    sig = np.ascontiguousarray(inp["sig_sum"], dtype=np.float32)
+    cnt = np.ascontiguousarray(inp["sig_cnt"], dtype=np.int32)
+    lens = np.ascontiguousarray(inp["lens"], dtype=np.int32)
+    b = _Batch(int(inp["L"]), int(inp["R"]), int(inp["Hq"]), int(inp["Hkv"]), 128, int(inp["T"]),
+               _ptr(k), _ptr(v), _ptr(sig), _ptr(cnt), _ptr(lens), int(inp.get("unit_base", 0)))
+    p = pool._c()
+    t = tables._c()
+    mask = None if quant_mask is None else np.ascontiguousarray(quant_mask, dtype=np.uint8)
+    return int(lib().oracle_compact(ctypes.byref(b), float(alpha_h), float(alpha_l),
+                                     ctypes.byref(p), ctypes.byref(t), _ptr(mask)))
+
+
+def dequant_page(pool: Pool, page_id: int):
+    P = pool.P
+    k = np.zeros((2 * P, 128), dtype=np.float32)
+    v = np.zeros((2 * P, 128), dtype=np.float32)
+    pos = np.zeros(2 * P, dtype=np.int32)
+    p = pool._c()
+    lib().oracle_dequant_page(ctypes.byref(p), int(page_id), _ptr(k), _ptr(v), _ptr(pos))
+    return k, v, pos

@@ -1,0 +1,527 @@
+"""Pins for the CPU oracle (CPU only, no GPU).
+
+Each test ties the oracle to something other than itself: the IEEE binary16
+conversion as numpy implements it, an fp64 brute-force causal softmax, a
+closed form, the textbook per-token asymmetric quantizer of the special case
+alpha_h = alpha_l = 0, exact quantisation grids, the worked example printed in
+the DiffKV review, and allocator invariants checked from first principles.
+
+Source: DiffKV (arXiv 2412.03131), Pith review page: "What carries the
+argument", "Core claim", "Referee Report" (Summary; major comment 2 on
+Section 4 / Algorithm 1).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from differentiated_kv_cache_dkv_gb300 import workloads as W
+from tests.oracle_helpers import bf16_to_f32, f16, page_slots, run_oracle, unit_rows
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- fp16 --------
+
+def _check_fp16_block(bits):
+    x = bits.view(np.float32)
+    with np.errstate(over="ignore", invalid="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    got = oracle.fp16_rn(x)
+    nan = np.isnan(x)
+    if not np.array_equal(got[~nan], ref[~nan]):
+        bad = np.nonzero((got != ref) & ~nan)[0][:5]
+        raise AssertionError(f"fp16 mismatch at {[hex(int(bits[i])) for i in bad]}")
+    assert np.all((got[nan] & 0x7C00) == 0x7C00) and np.all((got[nan] & 0x3FF) != 0)
+
+
+def test_fp16_rn_against_numpy():
+    """The oracle's hand-written RNE binary32 -> binary16 conversion equals
+    numpy's binary16 cast: exhaustively over every fraction of every positive
+    exponent from 2^-31 to 2^19 (all rounding boundaries between 0 and
+    overflow, subnormals included), and on 2^24 random patterns of any sign
+    and exponent (NaNs compared as NaN).  DKV_EXHAUSTIVE=1 runs all 2^32."""
+    step = 1 << 23
+    for e in range(96, 147):
+        _check_fp16_block((np.arange(step, dtype=np.uint32) | np.uint32(e << 23)))
+    rng = np.random.default_rng(11)
+    _check_fp16_block(rng.integers(0, 1 << 32, size=1 << 24, dtype=np.uint64).astype(np.uint32))
+
+
+@pytest.mark.skipif(os.environ.get("DKV_EXHAUSTIVE") != "1", reason="set DKV_EXHAUSTIVE=1 (minutes)")
+def test_fp16_rn_exhaustive_against_numpy():
+    step = 1 << 24
+    for base in range(0, 1 << 32, step):
+        _check_fp16_block(np.arange(base, base + step, dtype=np.uint64).astype(np.uint32))
+
+
+def test_fp16_to_f32_all_patterns():
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = h.view(np.float16).astype(np.float32)
+    got = np.array([oracle.fp16_to_f32(int(x)) for x in h], dtype=np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+    assert np.all(np.isnan(got[nan]))
+
+
+# ---------------------------------------------------------- significance -----
+
+def _brute_force_classes(w, inp_t, alpha_h, alpha_l, rel=1e-6):
+    """fp64 classes straight from the causal softmax probabilities: average
+    over the N - i queries j >= i, max over the GQA group, compare alpha/N.
+    Returns (classes [T][Hkv], near-threshold mask)."""
+    G = w.Hq // w.Hkv
+    k = inp_t["k"][0].to(torch.float64)
+    q = W.make_queries(w, W.SEED_BASE, 0).to(torch.float64)
+    cls = np.zeros((w.T, w.Hkv), dtype=np.uint8)
+    near = np.zeros((w.T, w.Hkv), dtype=bool)
+    start = 0
+    for N in w.lens:
+        i = np.arange(N)
+        for h in range(w.Hkv):
+            best = np.full(N, -np.inf)
+            for g in range(G):
+                qh = h * G + g
+                logits = (q[start:start + N, qh] @ k[start:start + N, h].T) / math.sqrt(128)
+                mask = torch.tril(torch.ones((N, N), dtype=torch.bool))
+                p = torch.softmax(logits.masked_fill(~mask, float("-inf")), dim=1).numpy()
+                score = p.sum(axis=0) / (N - i)
+                best = np.maximum(best, score)
+            th, tl = alpha_h / N, alpha_l / N
+            c = np.where(best >= th, 2, np.where(best >= tl, 1, 0))
+            cls[start:start + N, h] = c
+            near[start:start + N, h] = (np.abs(best - th) <= rel * th) | (np.abs(best - tl) <= rel * tl)
+        start += N
+    return cls, near
+
+
+def test_significance_matches_fp64_causal_softmax_tiny():
+    w = W.get("tiny")
+    inp = W.make_inputs(w)
+    n = W.to_numpy(inp)
+    st, pool, tab = run_oracle(w, n)
+    assert st == oracle.OK
+    ref, near = _brute_force_classes(w, inp, w.alpha_h, w.alpha_l)
+    got = tab.classes.reshape(w.T, w.Hkv)
+    diff = (got != ref) & ~near
+    assert not diff.any(), f"{diff.sum()} classes differ from the fp64 brute force"
+    # the tiny workload exercises more than one tier
+    assert len(np.unique(got)) >= 2
+
+
+def test_significance_brute_force_with_pruning():
+    """Same brute force at thresholds that produce all three tiers."""
+    w = W.get("tiny")
+    inp = W.make_inputs(w)
+    n = W.to_numpy(inp)
+    st, pool, tab = run_oracle(w, n, alpha_h=1.5, alpha_l=0.9)
+    assert st == oracle.OK
+    ref, near = _brute_force_classes(w, inp, 1.5, 0.9)
+    got = tab.classes.reshape(w.T, w.Hkv)
+    assert not ((got != ref) & ~near).any()
+    assert set(np.unique(got)) == {0, 1, 2}
+
+
+def test_closed_form_zero_queries():
+    """Q = 0: p(j, i) = 1/(j+1), so score_i = (H_N - H_i)/(N - i) >= 1/N with
+    equality only for the last token.  At alpha_h = 1 every token is K8V4
+    (the last one only because the comparison is 'at or above')."""
+    w = W.get("tiny")
+    w.sig = "softmax_q0"
+    inp = W.make_inputs(w)
+    n = W.to_numpy(inp)
+    N = w.T
+    H = np.concatenate([[0.0], np.cumsum(1.0 / np.arange(1, N + 1))])
+    closed = (H[N] - H[np.arange(N)]) / (N - np.arange(N))
+    # the generator's sums agree with the harmonic closed form
+    sums = n["sig_sum"][0]
+    np.testing.assert_allclose(sums, (H[N] - H[np.arange(N)])[:, None].repeat(w.Hq, 1), rtol=1e-6)
+    st, pool, tab = run_oracle(w, n, alpha_h=1.0, alpha_l=0.2)
+    assert st == oracle.OK
+    assert np.all(tab.classes == 2)
+    # a threshold a little above 1 moves exactly the tokens the closed form says
+    ah = 1.001
+    st, pool, tab = run_oracle(w, n, alpha_h=ah, alpha_l=0.2)
+    expect = np.where(closed >= ah / N, 2, 1)
+    got = tab.classes.reshape(N, w.Hkv)
+    near = np.abs(closed - ah / N) <= 1e-6 * ah / N
+    for h in range(w.Hkv):
+        assert np.array_equal(got[~near, h], expect[~near])
+    assert got[N - 1, 0] == 1  # exactly 1/N < 1.001/N
+
+
+def test_zero_count_and_nan_scores():
+    """sig_cnt == 0 keeps a token K8V4; a NaN score is ignored inside the GQA
+    max; an all-NaN group prunes."""
+    w = W.small("edge", L=1, Hq=4, Hkv=2, lens=[40], P=16)
+    inp = W.to_numpy(W.make_inputs(w))
+    inp["sig_sum"] = inp["sig_sum"].copy()
+    inp["sig_cnt"] = inp["sig_cnt"].copy()
+    inp["sig_cnt"][3] = 0
+    inp["sig_sum"][0, 5, 0] = np.nan           # head 0, one of two q-heads NaN
+    inp["sig_sum"][0, 5, 1] = 10.0             # the other is large -> K8V4
+    inp["sig_sum"][0, 6, 2:4] = np.nan         # head 1 all NaN -> pruned
+    st, pool, tab = run_oracle(w, inp)
+    assert st == oracle.OK
+    c = tab.classes.reshape(w.T, w.Hkv)
+    assert c[3, 0] == 2 and c[3, 1] == 2
+    assert c[5, 0] == 2
+    assert c[6, 1] == 0
+
+
+# ------------------------------------------------------------- quantizer ----
+
+def _textbook_codes(x_bits, nbits):
+    """Per-token asymmetric uniform quantisation (KIVI-style; Jacob et al.):
+    fp16 scale (max-min)/(2^b-1) and zero = min, codes rint((x - zero)/scale)
+    in fp32, clamped.  numpy float32 / float16 arithmetic, ties to even."""
+    x = bf16_to_f32(x_bits)
+    n = np.float32((1 << nbits) - 1)
+    mn, mx = x.min(), x.max()
+    s16 = np.float16(np.float32(mx - mn) / n)
+    if mx > mn and s16 == 0:
+        s16 = np.float16(2.0 ** -24)
+    z16 = np.float16(mn)
+    s, z = np.float32(s16), np.float32(z16)
+    if s == 0:
+        q = np.zeros(128, dtype=np.uint8)
+    else:
+        q = np.clip(np.rint((x - z) / s), 0, n).astype(np.uint8)
+    return q, np.array([s16, z16], dtype=np.float16).view(np.uint16)
+
+
+def _stored_tokens(w, L, tab, pool, u):
+    """{position: (cls, k_codes, v_codes, meta, page, slot)} for unit u."""
+    out = {}
+    for k in range(tab.pmax):
+        pid = tab.fwd[u, k]
+        if pid < 0:
+            break
+        cls = pool.page_cls[pid]
+        for slot, (kc, vc, meta, pos) in enumerate(page_slots(pool.pages[pid], w.P, cls)):
+            if pos >= 0:
+                assert pos not in out, "token stored twice"
+                out[pos] = (cls, kc, vc, meta, pid, slot)
+    return out
+
+
+def test_alpha_zero_reduces_to_textbook_quantizer():
+    w = W.small("alpha0")
+    n = W.to_numpy(W.make_inputs(w))
+    st, pool, tab = run_oracle(w, n, alpha_h=0.0, alpha_l=0.0)
+    assert st == oracle.OK
+    assert np.all(tab.classes == 2)
+    for u in range(w.U):
+        l, r, h, start, N = unit_rows(w, n["L"], u)
+        stored = _stored_tokens(w, n["L"], tab, pool, u)
+        assert sorted(stored) == list(range(N))
+        for i in range(N):
+            cls, kc, vc, meta, pid, slot = stored[i]
+            assert slot == i % w.P and pid == tab.fwd[u, i // w.P]
+            qk, mk = _textbook_codes(n["k"][l, start + i, h], 8)
+            qv, mv = _textbook_codes(n["v"][l, start + i, h], 4)
+            assert np.array_equal(kc, qk) and np.array_equal(vc, qv)
+            assert np.array_equal(meta, np.concatenate([mk, mv]))
+
+
+def _grid_workload(N, rows_k, rows_v):
+    """A 1-layer, 1-request, 1-KV-head batch with explicit K and V rows."""
+    w = W.small("grid", L=1, Hq=2, Hkv=1, lens=[N], P=16)
+    inp = {"L": 1, "R": 1, "Hq": 2, "Hkv": 1, "T": N,
+           "k": np.ascontiguousarray(rows_k.reshape(1, N, 1, 128)),
+           "v": np.ascontiguousarray(rows_v.reshape(1, N, 1, 128)),
+           "sig_sum": np.ones((1, N, 2), dtype=np.float32),
+           "sig_cnt": np.ones(N, dtype=np.int32),
+           "lens": np.array([N], dtype=np.int32)}
+    return w, inp
+
+
+def _bf16_bits(x):
+    b = np.asarray(x, dtype=np.float32).view(np.uint32)
+    assert np.all((b & 0xFFFF) == 0), "grid value not exact in bf16"
+    return (b >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("tier", ["high", "low"])
+def test_exact_grid_rows(tier):
+    """Rows x = z + k*s with fp16-exact z and power-of-two s spanning the full
+    code range: codes equal k and dequantisation is exact."""
+    rng = np.random.default_rng(7)
+    N = 40
+    nk, nv = (255, 15) if tier == "high" else (15, 3)
+    kk = rng.integers(0, nk + 1, size=(N, 128))
+    kv = rng.integers(0, nv + 1, size=(N, 128))
+    kk[:, 0], kk[:, 1] = 0, nk
+    kv[:, 0], kv[:, 1] = 0, nv
+    zk, sk = -1.0, 1.0 / 16
+    zv, sv = -0.5, 1.0 / 8
+    xk = _bf16_bits(zk + kk * sk)
+    xv = _bf16_bits(zv + kv * sv)
+    w, inp = _grid_workload(N, xk, xv)
+    ah, al = (0.0, 0.0) if tier == "high" else (1e30, 0.0)
+    st, pool, tab = run_oracle(w, inp, alpha_h=ah, alpha_l=al)
+    assert st == oracle.OK
+    stored = _stored_tokens(w, 1, tab, pool, 0)
+    for i in range(N):
+        cls, kc, vc, meta, pid, slot = stored[i]
+        assert cls == (2 if tier == "high" else 1)
+        assert np.array_equal(kc, kk[i]) and np.array_equal(vc, kv[i])
+        assert np.array_equal(f16(meta), np.float32([sk, zk, sv, zv]))
+    for pid in set(tab.fwd[0][tab.fwd[0] >= 0]):
+        k, v, pos = oracle.dequant_page(pool, pid)
+        for s in range(2 * w.P):
+            if pos[s] >= 0:
+                assert np.array_equal(k[s], bf16_to_f32(xk[pos[s]]))
+                assert np.array_equal(v[s], bf16_to_f32(xv[pos[s]]))
+
+
+def test_constant_and_underflow_rows():
+    """Constant rows: scale 0, codes 0, exact dequantisation.  A row whose
+    span/255 underflows binary16 gets the smallest subnormal scale 2^-24."""
+    for c in [0.0, -3.5, 1.0, 2.0 ** -20, 57344.0]:
+        st, q, s16, z16 = oracle.quant_row(np.full(128, _bf16_bits([c])[0], dtype=np.uint16), 8)
+        assert st == oracle.OK and not q.any() and s16 == 0
+        assert oracle.fp16_to_f32(z16) == np.float32(np.float16(c))
+    base = np.float32(2.0 ** -12)
+    bits = np.full(128, _bf16_bits([base])[0], dtype=np.uint16)
+    bits[5] += 1  # next bf16 above 2^-12: span 2^-19, span/255 < 2^-25
+    st, q, s16, z16 = oracle.quant_row(bits, 8)
+    assert st == oracle.OK and s16 == 1
+    assert q[5] == np.clip(np.rint((bf16_to_f32(bits[5:6])[0] - f16([z16])[0]) / np.float32(2.0 ** -24)), 0, 255)
+
+
+def test_range_errors_in_quantizer():
+    row = np.full(128, _bf16_bits([1.0])[0], dtype=np.uint16)
+    for bad in [np.inf, -np.inf, 70144.0]:
+        r = row.copy()
+        r[9] = _bf16_bits([bad])[0]
+        assert oracle.quant_row(r, 8)[0] == oracle.E_RANGE
+    r = row.copy()
+    r[9] = 0x7FC0  # NaN
+    assert oracle.quant_row(r, 4)[0] == oracle.E_RANGE
+    r[9] = _bf16_bits([65280.0])[0]  # largest bf16 <= 65504
+    assert oracle.quant_row(r, 4)[0] == oracle.OK
+
+
+def test_dequant_error_bound():
+    """|x - (z + q*s)| <= s/2 + 1e-6 (evaluated in fp64).  fp32 rounding of
+    (x - z)/s next to a half-integer may add at most n*2^-23*s; such elements
+    are counted and held to that looser bound."""
+    w = W.small("bound", L=1, lens=[300, 129])
+    n = W.to_numpy(W.make_inputs(w))
+    st, pool, tab = run_oracle(w, n)
+    assert st == oracle.OK
+    loose = 0
+    for u in range(w.U):
+        l, r, h, start, N = unit_rows(w, 1, u)
+        for i, (cls, kc, vc, meta, pid, slot) in _stored_tokens(w, 1, tab, pool, u).items():
+            m = f16(meta).astype(np.float64)
+            for codes, x_bits, s, z, nb in ((kc, n["k"][l, start + i, h], m[0], m[1], 8 if cls == 2 else 4),
+                                            (vc, n["v"][l, start + i, h], m[2], m[3], 4 if cls == 2 else 2)):
+                x = bf16_to_f32(x_bits).astype(np.float64)
+                err = np.abs(x - (z + codes.astype(np.float64) * s))
+                strict = err <= 0.5 * s + 1e-6
+                loose += int((~strict).sum())
+                assert np.all(err <= s * (0.5 + ((1 << nb) - 1) * 2.0 ** -23) + 1e-6)
+    assert loose < 50
+
+
+# ------------------------------------------------------------- allocator ----
+
+def _check_allocation(w, L, n, pool, tab, head0, F):
+    """Allocator invariants from first principles (reading A1)."""
+    U = L * w.R * w.Hkv
+    cls = tab.classes.reshape(L, w.T, w.Hkv)
+    d = np.zeros(U, dtype=np.int64)
+    nhi = np.zeros(U, dtype=np.int64)
+    nlo = np.zeros(U, dtype=np.int64)
+    for u in range(U):
+        l, r, h, start, N = unit_rows(w, L, u)
+        c = cls[l, start:start + N, h]
+        nhi[u], nlo[u] = (c == 2).sum(), (c == 1).sum()
+        d[u] = -(-nhi[u] // w.P) + -(-nlo[u] // (2 * w.P))
+    off = np.concatenate([[0], np.cumsum(d)[:-1]])
+    assert np.array_equal(tab.unit_hdr[:, 0], nhi) and np.array_equal(tab.unit_hdr[:, 1], nlo)
+    assert np.array_equal(tab.unit_hdr[:, 2] + tab.unit_hdr[:, 3], d)
+    seen = set()
+    for u in range(U):
+        row = tab.fwd[u]
+        expect = (head0 + off[u] + np.arange(d[u])) % F  # identity free list
+        assert np.array_equal(row[:d[u]], expect)
+        assert np.all(row[d[u]:] == -1)
+        for k, pid in enumerate(row[:d[u]]):
+            assert pid not in seen
+            seen.add(int(pid))
+            assert pool.rev_unit[pid] == u and pool.rev_idx[pid] == k
+            assert pool.page_cls[pid] == (2 if k < tab.unit_hdr[u, 2] else 1)
+    free = np.setdiff1d(np.arange(F), np.array(sorted(seen), dtype=np.int64))
+    assert np.all(pool.rev_unit[free] == -1) and np.all(pool.page_cls[free] == 0)
+    assert int(pool.cursors[0]) == head0 + int(d.sum())
+    return d
+
+
+def test_allocation_invariants_ragged_with_wrap():
+    w = W.small("alloc")
+    n = W.to_numpy(W.make_inputs(w))
+    F = w.pool_pages
+    pool = oracle.Pool(F, w.P)
+    head0 = F - 5  # the run of slots wraps past the end of the ring
+    pool.cursors[:] = [head0, head0 + F]
+    st, pool, tab = run_oracle(w, n, pool=pool)
+    assert st == oracle.OK
+    d = _check_allocation(w, 2, n, pool, tab, head0, F)
+    assert d.sum() > 5
+    # every surviving token stored exactly once, in ascending slot order per tier
+    cls = tab.classes.reshape(2, w.T, w.Hkv)
+    for u in range(w.U):
+        l, r, h, start, N = unit_rows(w, 2, u)
+        stored = _stored_tokens(w, 2, tab, pool, u)
+        c = cls[l, start:start + N, h]
+        assert sorted(stored) == list(np.nonzero(c > 0)[0])
+        for tier in (2, 1):
+            toks = [i for i in sorted(stored) if stored[i][0] == tier]
+            assert all(stored[i][0] == c[i] for i in toks)
+            cap = w.P if tier == 2 else 2 * w.P
+            base = 0 if tier == 2 else tab.unit_hdr[u, 2]
+            for rank, i in enumerate(toks):
+                assert stored[i][4] == tab.fwd[u, base + rank // cap] and stored[i][5] == rank % cap
+        # unused slots: zero codes, zero metadata, position -1
+        for k in range(tab.unit_hdr[u, 2] + tab.unit_hdr[u, 3]):
+            pid = tab.fwd[u, k]
+            for kc, vc, meta, pos in page_slots(pool.pages[pid], w.P, pool.page_cls[pid]):
+                if pos < 0:
+                    assert not kc.any() and not vc.any() and not meta.any() and pos == -1
+            if pool.page_cls[pid] == 2:  # upper half of a K8V4 page is unused
+                page = pool.pages[pid]
+                assert not page[192 * w.P + 8 * w.P:208 * w.P].any()
+                assert np.all(page[208 * w.P + 4 * w.P:].view(np.int32) == -1)
+
+
+def test_all_pruned_changes_nothing():
+    w = W.small("pruned")
+    n = W.to_numpy(W.make_inputs(w))
+    st, pool, tab = run_oracle(w, n, alpha_h=1e30, alpha_l=1e30)
+    assert st == oracle.OK
+    assert np.all(tab.classes == 0) and int(pool.cursors[0]) == 0
+    assert np.all(tab.fwd == -1) and np.all(pool.page_cls == 0)
+
+
+def _snapshot(pool, tab):
+    return [a.copy() for a in (pool.free_list, pool.cursors, pool.rev_unit, pool.rev_idx,
+                               pool.page_cls, pool.pages, tab.fwd, tab.unit_hdr)]
+
+
+def test_out_of_memory_is_all_or_nothing():
+    w = W.small("nomem")
+    n = W.to_numpy(W.make_inputs(w))
+    st, pool, tab = run_oracle(w, n)
+    need = int(pool.cursors[0])
+    small_pool = oracle.Pool(need - 1, w.P)
+    tab2 = oracle.Tables(w.U, w.pmax, w.rows)
+    before = _snapshot(small_pool, tab2)
+    st = oracle.compact(n, w.alpha_h, w.alpha_l, small_pool, tab2)
+    assert st == oracle.E_NOMEM
+    for a, b in zip(before, _snapshot(small_pool, tab2)):
+        assert np.array_equal(a, b)
+    exact_pool = oracle.Pool(need, w.P)
+    assert oracle.compact(n, w.alpha_h, w.alpha_l, exact_pool, tab2) == oracle.OK
+    assert int(exact_pool.cursors[0]) == int(exact_pool.cursors[1])
+
+
+def test_range_error_is_all_or_nothing():
+    w = W.small("range")
+    n = W.to_numpy(W.make_inputs(w))
+    st, pool, tab = run_oracle(w, n)
+    cls = tab.classes.reshape(w.L, w.T, w.Hkv)
+    l, t, h = [int(x[0]) for x in np.nonzero(cls == 1)]
+    k = n["k"].copy()
+    k[l, t, h, 17] = 0x7F80  # +inf
+    bad = dict(n, k=k)
+    pool2 = oracle.Pool(w.pool_pages, w.P)
+    tab2 = oracle.Tables(w.U, w.pmax, w.rows)
+    before = _snapshot(pool2, tab2)
+    assert oracle.compact(bad, w.alpha_h, w.alpha_l, pool2, tab2) == oracle.E_RANGE
+    for a, b in zip(before, _snapshot(pool2, tab2)):
+        assert np.array_equal(a, b)
+    # an out-of-range value in a pruned row is never quantised
+    l, t, h = [int(x[0]) for x in np.nonzero(cls == 0)]
+    k = n["k"].copy()
+    k[l, t, h, 3] = 0x7F80
+    assert oracle.compact(dict(n, k=k), w.alpha_h, w.alpha_l, oracle.Pool(w.pool_pages, w.P),
+                          oracle.Tables(w.U, w.pmax, w.rows)) == oracle.OK
+
+
+def test_layer_split_equivalence():
+    """One L-layer call equals L successive one-layer calls on the same pool."""
+    w = W.small("split", L=3)
+    n = W.to_numpy(W.make_inputs(w))
+    st, pool_a, tab_a = run_oracle(w, n)
+    assert st == oracle.OK
+    pool_b = oracle.Pool(w.pool_pages, w.P)
+    Ul = w.R * w.Hkv
+    for l in range(w.L):
+        nl = dict(n, L=1, k=n["k"][l:l + 1], v=n["v"][l:l + 1], sig_sum=n["sig_sum"][l:l + 1],
+                  unit_base=l * Ul)
+        st, pool_b, tab_l = run_oracle(w, nl, pool=pool_b)
+        assert st == oracle.OK
+        assert np.array_equal(tab_l.fwd, tab_a.fwd[l * Ul:(l + 1) * Ul])
+        assert np.array_equal(tab_l.unit_hdr, tab_a.unit_hdr[l * Ul:(l + 1) * Ul])
+        assert np.array_equal(tab_l.classes, tab_a.classes.reshape(w.L, -1)[l])
+    for a, b in zip(_snapshot(pool_a, tab_a)[:6], _snapshot(pool_b, tab_a)[:6]):
+        assert np.array_equal(a, b)
+
+
+def test_argument_and_length_errors():
+    w = W.small("args")
+    n = W.to_numpy(W.make_inputs(w))
+    assert run_oracle(w, n, alpha_h=0.1, alpha_l=0.2)[0] == oracle.E_INVAL
+    assert run_oracle(w, n, alpha_h=1.0, alpha_l=-0.1)[0] == oracle.E_INVAL
+    bad = dict(n, lens=n["lens"] + np.array([1, 0, 0, 0, 0], dtype=np.int32))
+    assert run_oracle(w, bad)[0] == oracle.E_LENS
+    w_odd = W.small("args", P=15)
+    assert run_oracle(w_odd, n)[0] == oracle.E_INVAL
+
+
+# ------------------------------------------------- worked example (golden) ----
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = float(v)
+    return vals
+
+
+def test_memory_fraction_worked_example():
+    """The review's arithmetic: 46% K8V4 + 54% K4V2 tokens give a 27.4% KV
+    memory fraction of FP16.  The oracle's page layout must spend 12/32 and
+    6/32 of the FP16 bytes on the codes of a K8V4 and a K4V2 token, and a
+    unit with that mix must come out at the printed fraction."""
+    g = _read_golden("memory_fraction_worked_example.txt")
+    N = 100
+    n_hi, n_lo = int(round(g["high_fraction"] * N)), int(round(g["low_fraction"] * N))
+    rng = np.random.default_rng(3)
+    xk = _bf16_bits(np.float32(rng.integers(-64, 64, size=(N, 128)) / 16.0))
+    xv = _bf16_bits(np.float32(rng.integers(-64, 64, size=(N, 128)) / 16.0))
+    w, inp = _grid_workload(N, xk, xv)
+    sig = np.zeros((1, N, 2), dtype=np.float32)
+    sig[0, :n_hi] = 1.0       # score 1 >= 1/N        -> K8V4
+    sig[0, n_hi:] = 0.5 / N   # 0.2/N <= score < 1/N  -> K4V2
+    inp["sig_sum"] = sig
+    st, pool, tab = run_oracle(w, inp, alpha_h=1.0, alpha_l=0.2)
+    assert st == oracle.OK
+    assert tuple(tab.unit_hdr[0, :2]) == (n_hi, n_lo)
+    code_bytes = 0
+    for pos, (cls, kc, vc, meta, pid, slot) in _stored_tokens(w, 1, tab, pool, 0).items():
+        code_bytes += (128 * 8 + 128 * 4) // 8 if cls == 2 else (128 * 4 + 128 * 2) // 8
+    frac = code_bytes / (N * 2 * 128 * 2)
+    assert abs(frac - (12 * n_hi + 6 * n_lo) / (32 * N)) < 1e-12
+    assert round(frac, int(g["printed_decimals"])) == g["memory_fraction"]
