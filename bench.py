@@ -1,0 +1,320 @@
+#!/usr/bin/env python3
+"""Benchmark: differentiated KV-cache compaction throughput on GB300.
+
+One step = reset the page pool (dkv_init_pool) + one dkv_compact over the
+whole batch (significance reduce, classification, page scan, quantise +
+pack + scatter, table commit).  Default workload: Llama-3-8B-shaped prefill
+compaction (32 layers, 16 x 4096 tokens, 32 query / 8 KV heads, page 16).
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on
+the host cores instead (a bounded sample of the same workload per step).
+Multi-GPU (torchrun): every rank compacts its own batch on its own GPU (the
+units are independent: replicas, weak scaling); only the timing is reduced.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV tokens compacted/sec (token-rows: one token x one (layer, KV head))"
+UNIT = "token-rows/s"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="llama")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle ----
+
+def oracle_sample(w, seconds: float):
+    """Time the CPU oracle, as it stands, on layer 0 of the workload (repeated
+    until `seconds` of CPU work).  Returns (rows/s, reps, rows per rep)."""
+    import oracle
+    from differentiated_kv_cache_dkv_gb300 import workloads as W
+
+    inp = W.to_numpy(W.make_inputs(w, layers=[0]))
+    rows = w.T * w.Hkv
+    reps, t_total = 0, 0.0
+    while t_total < seconds or reps == 0:
+        pool = oracle.Pool(w.Hkv * sum(-(-n // w.P) + 1 for n in w.lens), w.P)
+        tab = oracle.Tables(w.R * w.Hkv, w.pmax, rows)
+        t = time.perf_counter()
+        st = oracle.compact(inp, w.alpha_h, w.alpha_l, pool, tab)
+        t_total += time.perf_counter() - t
+        assert st == oracle.OK, st
+        reps += 1
+    return rows * reps / t_total, reps, rows, t_total
+
+
+def run_reference(a):
+    """CPU oracle arm: each step compacts layer 0 of the workload on one host core."""
+    from differentiated_kv_cache_dkv_gb300 import workloads as W
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = W.get(a.workload)
+    for _ in range(a.warmup):
+        oracle_sample(w, 0.0)
+    times = []
+    rows = w.T * w.Hkv
+    for _ in range(a.steps):
+        r = oracle_sample(w, 0.0)
+        times.append(r[3])
+    total = sum(times)
+    value = rows * a.steps / total
+    sample = f"layer 0 of {a.workload} ({rows} token-rows) per step, single-threaded oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": 1000.0 * total / a.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": a.workload, "layers": w.L, "requests": w.R, "tokens": w.T, "Hq": w.Hq,
+                   "Hkv": w.Hkv, "page_tokens": w.P},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- native ----
+
+def run_native(a):
+    import torch
+    import torch.distributed as dist
+
+    from differentiated_kv_cache_dkv_gb300 import libdkv
+    from differentiated_kv_cache_dkv_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    libdkv.load()
+    w = W.get(a.workload)
+    dev = torch.device("cuda", local)
+    inp = W.make_inputs(w, seed=W.SEED_BASE + 1000 * rank, device=dev)
+    comp = libdkv.Compactor(w.L, w.R, w.Hq, w.Hkv, w.T, max(w.lens), w.P, w.pool_pages, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(profiler=None):
+        libdkv.dkv_init_pool(comp.pool)
+        comp.compact(inp, w.alpha_h, w.alpha_l, profiler=profiler)
+
+    for _ in range(a.warmup):
+        step()
+    assert libdkv.dkv_get_status(comp.pool) == libdkv.DKV_OK
+    torch.cuda.synchronize()
+
+    # per-step workload facts (identical every step)
+    rows = w.rows
+    classes = comp.classes[:rows]
+    n_pruned = int((classes == 0).sum())
+    n_surv = rows - n_pruned
+    pages = int(comp.pool.cursors[0])
+    hdr = comp.tables.unit_hdr
+    n_hi, n_lo = int(hdr[:, 0].sum()), int(hdr[:, 1].sum())
+
+    prof = libdkv.Profiler(a.steps)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(a.steps):
+        step(prof)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    assert libdkv.dkv_get_status(comp.pool) == libdkv.DKV_OK
+    kt = prof.read()
+    prof.close()
+    kernel_ms = {n: statistics.mean(c[i] for c in kt) for i, n in enumerate(libdkv.KERNEL_NAMES)}
+
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = world * rows * a.steps / (ms_max / 1000.0)
+
+    # roofline of the dominant kernel (k_pack): algorithmic bytes per launch
+    peak, peak_kind = _peaks()
+    U = w.U
+    ntiles = w.L * w.Hkv * sum(-(-n // 128) for n in w.lens)
+    pack_bytes = n_surv * 512 + pages * (216 * w.P + 4) + ntiles * 40 + U * 16
+    pack_ms = kernel_ms["k_pack"]
+    pack_gbs = pack_bytes / (pack_ms / 1000.0) / 1e9
+    step_read = n_surv * 512 + w.L * w.T * w.Hq * 4 + w.T * 4
+    step_write = rows + pages * (216 * w.P + 13) + U * (w.pmax * 4 + 16) + w.pool_pages * 13
+    step_gbs = (step_read + step_write) / (ms_max / a.steps / 1000.0) / 1e9
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if a.e2e_steps > 0:
+        host = {k: inp[k].to("cpu").pin_memory() for k in ("k", "v", "sig_sum", "sig_cnt", "lens")}
+        out_hdr = torch.empty_like(hdr, device="cpu").pin_memory()
+        out_cur = torch.empty(2, dtype=torch.int64).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_hdr.numel() * 4 + 16
+
+        def e2e_step():
+            for k_, t_ in host.items():
+                inp[k_].copy_(t_, non_blocking=True)
+            step()
+            out_hdr.copy_(hdr, non_blocking=True)
+            out_cur.copy_(comp.pool.cursors, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(a.e2e_steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        te = torch.tensor([s0.elapsed_time(s1)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * rows * a.e2e_steps / (float(te.item()) / 1000.0), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": a.e2e_steps}
+        del host
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        v, reps, rrows, tt = oracle_sample(w, a.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"layer 0 of {a.workload} ({rrows} token-rows) x {reps}, single-threaded, {tt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms_max / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": a.workload, "layers": w.L, "requests": w.R, "tokens_per_request": w.lens[0]
+                       if len(set(w.lens)) == 1 else "ragged", "Hq": w.Hq, "Hkv": w.Hkv, "page_tokens": w.P,
+                       "alpha_h": w.alpha_h, "alpha_l": w.alpha_l, "rows_per_step": rows,
+                       "l2": "inputs (%.1f GB) larger than L2" % ((rows * 512 + w.L * w.T * w.Hq * 4) / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "k_pack", "achieved": pack_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": pack_gbs / peak, "peak_kind": peak_kind, "traffic": None,
+                         "algorithmic_bytes": pack_bytes, "ms": pack_ms},
+            "step_hbm": {"achieved": step_gbs, "frac": step_gbs / peak, "bytes": step_read + step_write},
+            "kernels_ms": kernel_ms,
+            "request_tokens_per_s": value / (w.L * w.Hkv),
+            "classes": {"k8v4": n_hi / rows, "k4v2": n_lo / rows, "pruned": n_pruned / rows},
+            "pages_per_step": pages,
+            "payload_fraction": (12 * n_hi + 6 * n_lo) / (32 * rows),
+            "gpu_launches": a.steps * (1 + libdkv.DKV_PROFILE_KERNELS),
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_native(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,223 @@
+// alloc.cu -- page demand, parallel prefix sum over the circular free page
+// list (k_scan) and the commit of tables and cursors (k_commit).
+//
+// DiffKV (arXiv 2412.03131), Pith review, "What carries the argument": after
+// each attention head decides how many high- and low-precision pages it
+// needs, a parallel prefix sum over the circular free page list assigns every
+// head a disjoint contiguous region of page ids, so allocation happens on the
+// GPU in one coordinated step; "Core claim": unified pages, circular free
+// page list, bidirectional page table.
+//
+// The scan is a single pass: each block takes a ticket (its partition of
+// kScanUnits units, in ticket order so every predecessor is already running),
+// reduces its units' demands, publishes its aggregate, and looks back over
+// the predecessors' published aggregates / inclusive prefixes (the
+// decoupled look-back of Merrill and Garland, "Single-pass Parallel Prefix
+// Scan with Decoupled Look-back", 2016), the block-level pieces following the
+// work-efficient scan of Harris, Sengupta and Owens (GPU Gems 3, ch. 39),
+// which the DiffKV paper cites.  Every wait is bounded by spin_limit polls.
+#include <cuda_runtime.h>
+
+#include "dkv_internal.cuh"
+
+namespace dkv {
+
+namespace {
+
+constexpr int kScanThreads = 256;
+constexpr int kCommitThreads = 256;
+
+__device__ __forceinline__ void st_release(uint64_t *p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_acquire(const uint64_t *p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
+
+__global__ void __launch_bounds__(kScanThreads) k_scan(CompactArgs a) {
+  __shared__ int32_t nh_s[kScanUnits], nl_s[kScanUnits], d_s[kScanUnits], ex_s[kScanUnits];
+  __shared__ int32_t wsum_s[kScanUnits / 32];
+  __shared__ int32_t part_s, fail_s;
+  __shared__ int64_t prefix_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (a.ws->err != 0) return;  // lengths rejected by k_prep
+  if (tid == 0) {
+    part_s = atomicAdd(&a.ws->ticket, 1);
+    fail_s = 0;
+  }
+  __syncthreads();
+  const int32_t part = part_s;
+  const int32_t npart = a.ws->npart;
+  if (part >= npart) return;
+  const int32_t TR = a.ws->TR;
+  const int64_t u0 = static_cast<int64_t>(part) * kScanUnits;
+
+  // per unit: class counts of its tiles -> rank bases of every tile
+  for (int uu = warp; uu < kScanUnits; uu += kScanThreads / 32) {
+    const int64_t u = u0 + uu;
+    int32_t nh = 0, nl = 0;
+    if (u < a.U) {
+      const int32_t h = static_cast<int32_t>(u % a.Hkv);
+      const int64_t lr = u / a.Hkv;
+      const int32_t r = static_cast<int32_t>(lr % a.R);
+      const int64_t l = lr / a.R;
+      const int32_t tr0 = a.tile_off[r];
+      const int32_t nt = a.tile_off[r + 1] - tr0;
+      const int64_t tau0 = (l * TR + tr0) * a.Hkv + static_cast<int64_t>(h) * nt;
+      for (int jb = 0; jb < nt; jb += 32) {
+        const int j = jb + lane;
+        int32_t ch = 0, cl = 0;
+        if (j < nt) {
+          const uint4 *m = reinterpret_cast<const uint4 *>(a.mask + (tau0 + j) * (2 * kMaskWords));
+          const uint4 hw = m[0], lw = m[1];
+          ch = __popc(hw.x) + __popc(hw.y) + __popc(hw.z) + __popc(hw.w);
+          cl = __popc(lw.x) + __popc(lw.y) + __popc(lw.z) + __popc(lw.w);
+        }
+        int32_t ih = ch, il = cl;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int32_t xh = __shfl_up_sync(0xffffffffu, ih, o);
+          const int32_t xl = __shfl_up_sync(0xffffffffu, il, o);
+          if (lane >= o) {
+            ih += xh;
+            il += xl;
+          }
+        }
+        if (j < nt) a.base[tau0 + j] = make_int2(nh + ih - ch, nl + il - cl);
+        nh += __shfl_sync(0xffffffffu, ih, 31);
+        nl += __shfl_sync(0xffffffffu, il, 31);
+      }
+    }
+    if (lane == 0) {
+      nh_s[uu] = nh;
+      nl_s[uu] = nl;
+      d_s[uu] = ceil_div(nh, a.P) + ceil_div(nl, 2 * a.P);
+    }
+  }
+  __syncthreads();
+
+  // block-wide exclusive scan of the partition's page demands
+  int32_t incl = 0;
+  if (tid < kScanUnits) {
+    incl = d_s[tid];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    if (lane == 31) wsum_s[warp] = incl;
+  }
+  __syncthreads();
+  if (tid < kScanUnits) {
+    int32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += wsum_s[w];
+    ex_s[tid] = before + incl - d_s[tid];
+  }
+
+  // decoupled look-back over the preceding partitions (thread 0)
+  if (tid == 0) {
+    int64_t agg = 0;
+    for (int w = 0; w < kScanUnits / 32; ++w) agg += wsum_s[w];
+    int64_t prefix = 0;
+    bool fail = false;
+    if (part == 0) {
+      st_release(a.part, kFlagPrefix | static_cast<uint64_t>(agg));
+    } else {
+      st_release(a.part + part, kFlagAggregate | static_cast<uint64_t>(agg));
+      if (a.spin_limit == 0) {
+        fail = true;
+      } else {
+        int32_t pred = part - 1;
+        for (;;) {
+          uint64_t st = ld_acquire(a.part + pred);
+          int64_t spins = 0;
+          while ((st >> 62) == 0) {
+            if (++spins > a.spin_limit) {
+              fail = true;
+              break;
+            }
+            __nanosleep(64);
+            st = ld_acquire(a.part + pred);
+          }
+          if (fail) break;
+          prefix += static_cast<int64_t>(st & kValueMask);
+          if ((st & kFlagPrefix) != 0) break;
+          --pred;  // partition 0 always publishes a prefix, so pred stays >= 0
+        }
+      }
+      if (!fail) st_release(a.part + part, kFlagPrefix | static_cast<uint64_t>(prefix + agg));
+    }
+    if (fail) {
+      set_error(&a.ws->err, DKV_E_TIMEOUT);
+      fail_s = 1;
+    }
+    prefix_s = prefix;
+    if (!fail && part == npart - 1) {
+      const int64_t total = prefix + agg;
+      const uint64_t head = a.cursors[0], tail = a.cursors[1];
+      a.ws->total = total;
+      a.ws->head = head;
+      a.ws->head_mod = static_cast<int64_t>(head % static_cast<uint64_t>(a.F));
+      if (static_cast<uint64_t>(total) > tail - head) set_error(&a.ws->err, DKV_E_NOMEM);
+    }
+  }
+  __syncthreads();
+  if (fail_s) return;
+  if (tid < kScanUnits && u0 + tid < a.U) {
+    const int64_t off = prefix_s + ex_s[tid];
+    a.unit[u0 + tid] = UnitInfo{nh_s[tid], nl_s[tid], static_cast<int32_t>(off), ceil_div(nh_s[tid], a.P)};
+  }
+}
+
+__global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
+  const int32_t err = a.ws->err;
+  if (err != 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicCAS(a.status, 0, err);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t head_mod = a.ws->head_mod;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kCommitThreads / 32);
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * (kCommitThreads / 32) + (threadIdx.x >> 5); u < a.U;
+       u += nwarps) {
+    const UnitInfo inf = a.unit[u];
+    const int32_t p_lo = ceil_div(inf.n_lo, 2 * a.P);
+    const int32_t d = inf.p_hi + p_lo;
+    int64_t ring = head_mod + inf.off;
+    if (ring >= a.F) ring -= a.F;
+    int32_t *fw = a.fwd + u * a.pmax;
+    for (int k = lane; k < a.pmax; k += 32) {
+      int32_t id = -1;
+      if (k < d) {
+        int64_t idx = ring + k;
+        if (idx >= a.F) idx -= a.F;
+        id = a.free_list[idx];
+        a.rev_unit[id] = static_cast<int32_t>(a.unit_base + u);
+        a.rev_idx[id] = k;
+        a.page_cls[id] = k < inf.p_hi ? DKV_CLASS_K8V4 : DKV_CLASS_K4V2;
+      }
+      fw[k] = id;
+    }
+    if (lane == 0) reinterpret_cast<int4 *>(a.unit_hdr)[u] = make_int4(inf.n_hi, inf.n_lo, inf.p_hi, p_lo);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.cursors[0] = a.ws->head + static_cast<uint64_t>(a.ws->total);
+}
+
+}  // namespace
+
+cudaError_t launch_scan(const CompactArgs &a, int npart, cudaStream_t s) {
+  k_scan<<<npart, kScanThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_commit(const CompactArgs &a, int grid, cudaStream_t s) {
+  k_commit<<<grid, kCommitThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dkv

@@ -1,0 +1,238 @@
+// api.cu -- the libdkv C ABI: argument validation, workspace layout, kernel
+// launches, status and profiling.  Every entry point is declared, with its
+// argument meaning, layout, ownership and error behaviour, in include/dkv.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <new>
+#include <vector>
+
+#include "dkv_internal.cuh"
+
+namespace {
+
+using dkv::CompactArgs;
+
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+int g_pack_bps[kMaxDevices];
+
+bool device_info(int *sms, int *pack_bps) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (g_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return false;
+    g_pack_bps[dev] = dkv::pack_blocks_per_sm();
+    g_sms[dev] = n;
+  }
+  *sms = g_sms[dev];
+  *pack_bps = g_pack_bps[dev];
+  return true;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Profiler {
+  int32_t max_calls = 0;
+  int32_t next = 0;
+  std::vector<cudaEvent_t> ev;  // [max_calls][DKV_PROFILE_KERNELS + 1]
+};
+
+bool valid_pool(const dkv_pool *p) {
+  if (!p) return false;
+  if (p->F < 1 || p->F > INT32_MAX || p->P < 2 || (p->P & 1) || p->P > (1 << 16)) return false;
+  if (!p->free_list || !p->cursors || !p->rev_unit || !p->rev_idx || !p->page_cls || !p->pages || !p->status)
+    return false;
+  if (!aligned(p->pages, 16) || !aligned(p->cursors, 8) || !aligned(p->free_list, 4) || !aligned(p->rev_unit, 4) ||
+      !aligned(p->rev_idx, 4) || !aligned(p->status, 4))
+    return false;
+  return true;
+}
+
+bool valid_shape(const dkv_batch *b) {
+  if (!b) return false;
+  if (b->D != DKV_HEAD_DIM || b->L < 1 || b->R < 1 || b->Hkv < 1 || b->Hq < b->Hkv || b->Hq % b->Hkv != 0 ||
+      b->Hq > dkv::kMaxHq)
+    return false;
+  if (b->T < 0 || b->T > INT32_MAX || b->max_len < 0) return false;
+  const int64_t U = static_cast<int64_t>(b->L) * b->R * b->Hkv;
+  if (U > INT32_MAX || b->unit_base < 0 || b->unit_base + U > INT32_MAX) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dkv_version(void) { return 100; }
+
+const char *dkv_status_string(int32_t code) {
+  switch (code) {
+    case DKV_OK: return "ok";
+    case DKV_E_INVAL: return "invalid argument";
+    case DKV_E_NOMEM: return "page demand exceeds the free pages";
+    case DKV_E_RANGE: return "a value to quantise is non-finite or above 65504 in magnitude";
+    case DKV_E_TIMEOUT: return "a bounded wait of the page scan gave up";
+    case DKV_E_INTERNAL: return "internal consistency check failed";
+    case DKV_E_CUDA: return "a CUDA call failed";
+    case DKV_E_LENS: return "request lengths disagree with T or max_len";
+    default: return "unknown status";
+  }
+}
+
+int32_t dkv_workspace_size(const dkv_batch *b, size_t *bytes) {
+  if (!bytes || !valid_shape(b)) return DKV_E_INVAL;
+  *bytes = dkv::ws_layout(b->L, b->R, b->Hkv, b->T).bytes;
+  return DKV_OK;
+}
+
+int32_t dkv_init_pool(const dkv_pool *pool, void *stream) {
+  if (!valid_pool(pool)) return DKV_E_INVAL;
+  return dkv::launch_init_pool(*pool, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DKV_OK : DKV_E_CUDA;
+}
+
+int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *pool, const dkv_tables *t,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+  if (!valid_shape(b) || !p || !valid_pool(pool) || !t) return DKV_E_INVAL;
+  if (!b->k || !b->v || !b->sig_sum || !b->sig_cnt || !b->lens || !b->classes) return DKV_E_INVAL;
+  if (!aligned(b->k, 16) || !aligned(b->v, 16) || !aligned(b->sig_sum, 16) || !aligned(b->sig_cnt, 4) ||
+      !aligned(b->lens, 4))
+    return DKV_E_INVAL;
+  if (!(std::isfinite(p->alpha_h) && std::isfinite(p->alpha_l)) || !(p->alpha_l >= 0.0f) ||
+      !(p->alpha_h >= p->alpha_l) || p->reserved != 0)
+    return DKV_E_INVAL;
+  if (!t->fwd || !t->unit_hdr || !aligned(t->unit_hdr, 16) || !aligned(t->fwd, 4)) return DKV_E_INVAL;
+  const int64_t need_pmax = (static_cast<int64_t>(b->max_len) + pool->P - 1) / pool->P + 1;
+  if (t->pmax < need_pmax) return DKV_E_INVAL;
+  const dkv::WsLayout lay = dkv::ws_layout(b->L, b->R, b->Hkv, b->T);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.bytes) return DKV_E_INVAL;
+  int sms = 0, pack_bps = 0;
+  if (!device_info(&sms, &pack_bps)) return DKV_E_CUDA;
+
+  CompactArgs a{};
+  a.L = b->L; a.R = b->R; a.Hq = b->Hq; a.Hkv = b->Hkv; a.G = b->Hq / b->Hkv;
+  a.P = pool->P; a.pmax = t->pmax;
+  a.spin_limit = p->spin_limit < 0 ? (1 << 22) : p->spin_limit;
+  a.T = b->T; a.F = pool->F; a.U = static_cast<int64_t>(b->L) * b->R * b->Hkv; a.unit_base = b->unit_base;
+  a.max_len = b->max_len;
+  a.alpha_h = p->alpha_h; a.alpha_l = p->alpha_l;
+  a.k = static_cast<const uint16_t *>(b->k); a.v = static_cast<const uint16_t *>(b->v);
+  a.sig_sum = b->sig_sum; a.sig_cnt = b->sig_cnt; a.lens = b->lens; a.classes = b->classes;
+  a.free_list = pool->free_list; a.cursors = pool->cursors; a.rev_unit = pool->rev_unit; a.rev_idx = pool->rev_idx;
+  a.page_cls = pool->page_cls; a.pages = pool->pages; a.status = pool->status;
+  a.fwd = t->fwd; a.unit_hdr = t->unit_hdr;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  a.ws = reinterpret_cast<dkv::WsHeader *>(ws);
+  a.tok_off = reinterpret_cast<int64_t *>(ws + lay.tok_off);
+  a.tile_off = reinterpret_cast<int32_t *>(ws + lay.tile_off);
+  a.part = reinterpret_cast<uint64_t *>(ws + lay.part);
+  a.unit = reinterpret_cast<dkv::UnitInfo *>(ws + lay.unit);
+  a.mask = reinterpret_cast<uint32_t *>(ws + lay.mask);
+  a.base = reinterpret_cast<int2 *>(ws + lay.base);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Profiler *prof = static_cast<Profiler *>(p->profiler);
+  cudaEvent_t *ev = nullptr;
+  if (prof && prof->next < prof->max_calls) {
+    ev = prof->ev.data() + static_cast<size_t>(prof->next) * (DKV_PROFILE_KERNELS + 1);
+    prof->next++;
+  }
+  auto mark = [&](int i) {
+    if (ev) cudaEventRecord(ev[i], s);
+  };
+  const int64_t tr_max = b->T / dkv::kTileTokens + b->R;
+  const int64_t classify_items = static_cast<int64_t>(b->L) * tr_max;
+  const int classify_grid = static_cast<int>(std::min<int64_t>(classify_items, static_cast<int64_t>(sms) * 8));
+  const int pack_grid = sms * pack_bps;
+  const int commit_grid = static_cast<int>(std::min<int64_t>((a.U + 7) / 8, static_cast<int64_t>(sms) * 8));
+
+  mark(0);
+  if (dkv::launch_prep(a, s) != cudaSuccess) return DKV_E_CUDA;
+  mark(1);
+  if (dkv::launch_classify(a, std::max(classify_grid, 1), s) != cudaSuccess) return DKV_E_CUDA;
+  mark(2);
+  if (dkv::launch_scan(a, lay.npart, s) != cudaSuccess) return DKV_E_CUDA;
+  mark(3);
+  if (dkv::launch_pack(a, pack_grid, s) != cudaSuccess) return DKV_E_CUDA;
+  mark(4);
+  if (dkv::launch_commit(a, std::max(commit_grid, 1), s) != cudaSuccess) return DKV_E_CUDA;
+  mark(5);
+  return DKV_OK;
+}
+
+int32_t dkv_dequant_page(const dkv_pool *pool, int32_t page_id, float *k_out, float *v_out, int32_t *pos_out,
+                         void *stream) {
+  if (!valid_pool(pool) || page_id < 0 || page_id >= pool->F || !k_out || !v_out || !pos_out) return DKV_E_INVAL;
+  return dkv::launch_dequant(*pool, nullptr, page_id, 1, k_out, v_out, pos_out, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? DKV_OK
+             : DKV_E_CUDA;
+}
+
+int32_t dkv_dequant_pages(const dkv_pool *pool, const int32_t *page_ids, int32_t n, float *k_out, float *v_out,
+                          int32_t *pos_out, void *stream) {
+  if (!valid_pool(pool) || n < 0 || (n > 0 && (!page_ids || !k_out || !v_out || !pos_out))) return DKV_E_INVAL;
+  if (n == 0) return DKV_OK;
+  return dkv::launch_dequant(*pool, page_ids, 0, n, k_out, v_out, pos_out, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? DKV_OK
+             : DKV_E_CUDA;
+}
+
+int32_t dkv_get_status(const dkv_pool *pool, void *stream) {
+  if (!pool || !pool->status) return DKV_E_INVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t host = 0;
+  if (cudaMemcpyAsync(&host, pool->status, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess) return DKV_E_CUDA;
+  if (cudaMemsetAsync(pool->status, 0, sizeof(int32_t), s) != cudaSuccess) return DKV_E_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DKV_E_CUDA;
+  return host;
+}
+
+int32_t dkv_profiler_create(int32_t max_calls, void **profiler) {
+  if (!profiler || max_calls < 1) return DKV_E_INVAL;
+  Profiler *pr = new (std::nothrow) Profiler();
+  if (!pr) return DKV_E_CUDA;
+  pr->max_calls = max_calls;
+  pr->ev.resize(static_cast<size_t>(max_calls) * (DKV_PROFILE_KERNELS + 1));
+  for (auto &e : pr->ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+      dkv_profiler_destroy(pr);
+      return DKV_E_CUDA;
+    }
+  }
+  *profiler = pr;
+  return DKV_OK;
+}
+
+int32_t dkv_profiler_read(void *profiler, float *ms, int32_t capacity_calls) {
+  Profiler *pr = static_cast<Profiler *>(profiler);
+  if (!pr || (!ms && capacity_calls > 0)) return DKV_E_INVAL;
+  const int32_t n = pr->next < capacity_calls ? pr->next : capacity_calls;
+  for (int32_t c = 0; c < n; ++c) {
+    cudaEvent_t *ev = pr->ev.data() + static_cast<size_t>(c) * (DKV_PROFILE_KERNELS + 1);
+    if (cudaEventSynchronize(ev[DKV_PROFILE_KERNELS]) != cudaSuccess) return DKV_E_CUDA;
+    for (int k = 0; k < DKV_PROFILE_KERNELS; ++k) {
+      float t = 0.0f;
+      if (cudaEventElapsedTime(&t, ev[k], ev[k + 1]) != cudaSuccess) return DKV_E_CUDA;
+      ms[c * DKV_PROFILE_KERNELS + k] = t;
+    }
+  }
+  pr->next = 0;
+  return n;
+}
+
+int32_t dkv_profiler_destroy(void *profiler) {
+  Profiler *pr = static_cast<Profiler *>(profiler);
+  if (!pr) return DKV_E_INVAL;
+  for (auto &e : pr->ev)
+    if (e) cudaEventDestroy(e);
+  delete pr;
+  return DKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+// dkv_internal.cuh -- shared definitions of the libdkv kernels (device side).
+//
+// Work decomposition of one dkv_compact call
+//   unit      (layer l, request r, KV head h), u = (l * R + r) * Hkv + h
+//   tile      kTileTokens consecutive tokens of one request; a "unit tile" is
+//             a tile of one unit.  Unit tiles are numbered
+//             tau = (l * TR + tile_off[r]) * Hkv + h * nt_r + j,
+//             nt_r = ceil(N_r / kTileTokens), TR = sum_r nt_r.
+//
+// Kernels, in stream order (all bounded, none traps):
+//   k_prep      1 block: request prefix sums, length validation, resets
+//   k_classify  significance reduce + three-tier classification + per-tile
+//               class bitmasks (warp ballots)
+//   k_scan      per-unit page demand, block scan + decoupled look-back over
+//               partitions of units, capacity check
+//   k_pack      quantise + pack + scatter every surviving row into its page
+//               slot, fill unused slots
+//   k_commit    forward / reverse tables, page classes, head cursor, status
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/dkv.h"
+
+namespace dkv {
+
+constexpr int kTileTokens = 128;                 // tokens per tile
+constexpr int kMaskWords = kTileTokens / 32;     // 32-bit words per class mask
+constexpr int kScanUnits = 128;                  // units per scan partition
+constexpr int kMaxHq = 128;                      // query heads supported
+
+// Call-local state at the start of the workspace.
+struct WsHeader {
+  int32_t err;       // first device-side error of this call (0 = none)
+  int32_t ticket;    // scan partition ticket counter
+  int32_t TR;        // number of (request, tile) pairs
+  int32_t npart;     // scan partitions
+  int64_t total;     // sum of page demands
+  uint64_t head;     // free-list head when the call started
+  int64_t head_mod;  // head mod F
+  int64_t pad[3];
+};
+
+// Decoupled look-back status word: flag in the top two bits.
+constexpr uint64_t kFlagAggregate = 1ull << 62;
+constexpr uint64_t kFlagPrefix = 2ull << 62;
+constexpr uint64_t kValueMask = (1ull << 62) - 1;
+
+// Per-unit results of the scan: {n_k8v4, n_k4v2, page offset, pages_k8v4}.
+struct UnitInfo {
+  int32_t n_hi, n_lo, off, p_hi;
+};
+
+// Byte offsets of the workspace regions (all 256-byte aligned).
+struct WsLayout {
+  size_t tok_off;    // int64 [R + 1]
+  size_t tile_off;   // int32 [R + 1]
+  size_t part;       // uint64 [npart]
+  size_t unit;       // UnitInfo [U]
+  size_t mask;       // uint32 [NT][2 * kMaskWords]: K8V4 words then K4V2 words
+  size_t base;       // int2 [NT]: K8V4 and K4V2 rank of the tile's first row
+  size_t bytes;      // total
+  int64_t nt_max;    // unit tiles the layout has room for
+  int32_t npart;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int64_t L, int64_t R, int64_t Hkv, int64_t T) {
+  WsLayout w{};
+  const int64_t U = L * R * Hkv;
+  const int64_t tr_max = T / kTileTokens + R;  // >= sum_r ceil(N_r / tile)
+  w.nt_max = L * Hkv * tr_max;
+  w.npart = static_cast<int32_t>((U + kScanUnits - 1) / kScanUnits);
+  size_t o = align256(sizeof(WsHeader));
+  w.tok_off = o;  o = align256(o + sizeof(int64_t) * (R + 1));
+  w.tile_off = o; o = align256(o + sizeof(int32_t) * (R + 1));
+  w.part = o;     o = align256(o + sizeof(uint64_t) * w.npart);
+  w.unit = o;     o = align256(o + sizeof(UnitInfo) * U);
+  w.mask = o;     o = align256(o + sizeof(uint32_t) * 2 * kMaskWords * w.nt_max);
+  w.base = o;     o = align256(o + sizeof(int2) * w.nt_max);
+  w.bytes = o;
+  return w;
+}
+
+// Everything a kernel of dkv_compact needs, passed by value.
+struct CompactArgs {
+  int32_t L, R, Hq, Hkv, G, P, pmax, spin_limit;
+  int64_t T, F, U, unit_base;
+  int32_t max_len;
+  float alpha_h, alpha_l;
+  const uint16_t *k, *v;
+  const float *sig_sum;
+  const int32_t *sig_cnt, *lens;
+  uint8_t *classes;
+  int32_t *free_list;
+  uint64_t *cursors;
+  int32_t *rev_unit, *rev_idx;
+  uint8_t *page_cls, *pages;
+  int32_t *status;
+  int32_t *fwd, *unit_hdr;
+  // workspace
+  WsHeader *ws;
+  int64_t *tok_off;
+  int32_t *tile_off;
+  uint64_t *part;
+  UnitInfo *unit;
+  uint32_t *mask;
+  int2 *base;
+};
+
+__device__ __forceinline__ void set_error(int32_t *err, int32_t code) { atomicCAS(err, 0, code); }
+
+// Largest r in [0, n) with a[r] <= x (a non-decreasing, a[0] <= x).
+__device__ __forceinline__ int find_segment(const int32_t *a, int n, int64_t x, int64_t scale) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<int64_t>(__ldg(a + mid)) * scale <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace dkv
+
+// Launchers (defined in the kernel translation units).
+namespace dkv {
+cudaError_t launch_prep(const CompactArgs &a, cudaStream_t s);
+cudaError_t launch_classify(const CompactArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_scan(const CompactArgs &a, int npart, cudaStream_t s);
+cudaError_t launch_pack(const CompactArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_commit(const CompactArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_init_pool(const dkv_pool &p, cudaStream_t s);
+cudaError_t launch_dequant(const dkv_pool &p, const int32_t *ids, int32_t one_id, int32_t n,
+                           float *k_out, float *v_out, int32_t *pos_out, cudaStream_t s);
+int pack_blocks_per_sm();
+}  // namespace dkv

@@ -1,0 +1,252 @@
+"""Thin ctypes binding over libdkv.so (argument marshalling only).
+
+Every function here forwards to the C entry point of the same name declared
+in ``include/dkv.h``; all compute runs in the library's CUDA kernels.  PyTorch
+only provides device memory and the current stream.  There is no fallback:
+if ``libdkv.so`` has not been built, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libdkv.so")
+
+DKV_OK = 0
+DKV_E_INVAL = -1
+DKV_E_NOMEM = -2
+DKV_E_RANGE = -3
+DKV_E_TIMEOUT = -4
+DKV_E_INTERNAL = -5
+DKV_E_CUDA = -6
+DKV_E_LENS = -7
+DKV_PROFILE_KERNELS = 5
+KERNEL_NAMES = ("k_prep", "k_classify", "k_scan", "k_pack", "k_commit")
+
+_lib = None
+
+
+class DkvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+class dkv_batch(ctypes.Structure):
+    _fields_ = [
+        ("L", ctypes.c_int32), ("R", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+        ("D", ctypes.c_int32), ("max_len", ctypes.c_int32), ("T", ctypes.c_int64),
+        ("unit_base", ctypes.c_int64), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("sig_sum", ctypes.c_void_p), ("sig_cnt", ctypes.c_void_p), ("lens", ctypes.c_void_p),
+        ("classes", ctypes.c_void_p),
+    ]
+
+
+class dkv_params(ctypes.Structure):
+    _fields_ = [("alpha_h", ctypes.c_float), ("alpha_l", ctypes.c_float), ("spin_limit", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("profiler", ctypes.c_void_p)]
+
+
+class dkv_pool(ctypes.Structure):
+    _fields_ = [
+        ("F", ctypes.c_int64), ("P", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("free_list", ctypes.c_void_p), ("cursors", ctypes.c_void_p), ("rev_unit", ctypes.c_void_p),
+        ("rev_idx", ctypes.c_void_p), ("page_cls", ctypes.c_void_p), ("pages", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
+    ]
+
+
+class dkv_tables(ctypes.Structure):
+    _fields_ = [("fwd", ctypes.c_void_p), ("pmax", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("unit_hdr", ctypes.c_void_p)]
+
+
+def load():
+    """Load libdkv.so (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    sigs = {
+        "dkv_version": ([], i32),
+        "dkv_status_string": ([i32], ctypes.c_char_p),
+        "dkv_workspace_size": ([P(dkv_batch), P(ctypes.c_size_t)], i32),
+        "dkv_init_pool": ([P(dkv_pool), vp], i32),
+        "dkv_compact": ([P(dkv_batch), P(dkv_params), P(dkv_pool), P(dkv_tables), vp, ctypes.c_size_t, vp], i32),
+        "dkv_dequant_page": ([P(dkv_pool), i32, vp, vp, vp, vp], i32),
+        "dkv_dequant_pages": ([P(dkv_pool), vp, i32, vp, vp, vp, vp], i32),
+        "dkv_get_status": ([P(dkv_pool), vp], i32),
+        "dkv_profiler_create": ([i32, P(vp)], i32),
+        "dkv_profiler_read": ([vp, vp, i32], i32),
+        "dkv_profiler_destroy": ([vp], i32),
+    }
+    for name, (args, res) in sigs.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = L
+    return L
+
+
+def status_string(code: int) -> str:
+    return load().dkv_status_string(int(code)).decode()
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _p(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+class DevicePool:
+    """Pool state in device memory (torch tensors owned by this object)."""
+
+    def __init__(self, F: int, P: int, device="cuda"):
+        self.F, self.P = int(F), int(P)
+        d = torch.device(device)
+        self.free_list = torch.empty(self.F, dtype=torch.int32, device=d)
+        self.cursors = torch.zeros(2, dtype=torch.int64, device=d)   # uint64 bit patterns
+        self.rev_unit = torch.empty(self.F, dtype=torch.int32, device=d)
+        self.rev_idx = torch.empty(self.F, dtype=torch.int32, device=d)
+        self.page_cls = torch.empty(self.F, dtype=torch.uint8, device=d)
+        self.pages = torch.empty((self.F, 216 * self.P), dtype=torch.uint8, device=d)
+        self.status = torch.zeros(1, dtype=torch.int32, device=d)
+
+    def c(self) -> dkv_pool:
+        return dkv_pool(self.F, self.P, 0, _p(self.free_list), _p(self.cursors), _p(self.rev_unit),
+                        _p(self.rev_idx), _p(self.page_cls), _p(self.pages), _p(self.status))
+
+
+class DeviceTables:
+    def __init__(self, U: int, pmax: int, device="cuda"):
+        self.pmax = int(pmax)
+        self.fwd = torch.empty((U, self.pmax), dtype=torch.int32, device=device)
+        self.unit_hdr = torch.empty((U, 4), dtype=torch.int32, device=device)
+
+    def c(self) -> dkv_tables:
+        return dkv_tables(_p(self.fwd), self.pmax, 0, _p(self.unit_hdr))
+
+
+def make_batch(inp: dict, classes: torch.Tensor, max_len: int, unit_base: int = 0) -> dkv_batch:
+    return dkv_batch(int(inp["L"]), int(inp["R"]), int(inp["Hq"]), int(inp["Hkv"]), 128, int(max_len),
+                     int(inp["T"]), int(unit_base), _p(inp["k"]), _p(inp["v"]), _p(inp["sig_sum"]),
+                     _p(inp["sig_cnt"]), _p(inp["lens"]), _p(classes))
+
+
+def dkv_workspace_size(batch: dkv_batch) -> int:
+    n = ctypes.c_size_t(0)
+    rc = load().dkv_workspace_size(ctypes.byref(batch), ctypes.byref(n))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_workspace_size")
+    return int(n.value)
+
+
+def dkv_init_pool(pool: DevicePool, stream=None) -> None:
+    c = pool.c()
+    rc = load().dkv_init_pool(ctypes.byref(c), _stream(stream))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_init_pool")
+
+
+def dkv_compact(batch: dkv_batch, alpha_h: float, alpha_l: float, pool: DevicePool, tables: DeviceTables,
+                workspace: torch.Tensor, stream=None, spin_limit: int = -1, profiler=None) -> None:
+    """Enqueue one compaction; device-side errors are read with dkv_get_status."""
+    params = dkv_params(float(alpha_h), float(alpha_l), int(spin_limit), 0,
+                        None if profiler is None else profiler.handle)
+    pc, tc = pool.c(), tables.c()
+    rc = load().dkv_compact(ctypes.byref(batch), ctypes.byref(params), ctypes.byref(pc), ctypes.byref(tc),
+                            _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_compact")
+
+
+def dkv_get_status(pool: DevicePool, stream=None) -> int:
+    c = pool.c()
+    return int(load().dkv_get_status(ctypes.byref(c), _stream(stream)))
+
+
+def dkv_dequant_page(pool: DevicePool, page_id: int, stream=None):
+    P = pool.P
+    dev = pool.pages.device
+    k = torch.empty((2 * P, 128), dtype=torch.float32, device=dev)
+    v = torch.empty((2 * P, 128), dtype=torch.float32, device=dev)
+    pos = torch.empty(2 * P, dtype=torch.int32, device=dev)
+    c = pool.c()
+    rc = load().dkv_dequant_page(ctypes.byref(c), int(page_id), _p(k), _p(v), _p(pos), _stream(stream))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_dequant_page")
+    return k, v, pos
+
+
+def dkv_dequant_pages(pool: DevicePool, page_ids: torch.Tensor, stream=None):
+    P = pool.P
+    n = int(page_ids.numel())
+    dev = pool.pages.device
+    ids = page_ids.to(device=dev, dtype=torch.int32).contiguous()
+    k = torch.empty((n, 2 * P, 128), dtype=torch.float32, device=dev)
+    v = torch.empty((n, 2 * P, 128), dtype=torch.float32, device=dev)
+    pos = torch.empty((n, 2 * P), dtype=torch.int32, device=dev)
+    c = pool.c()
+    rc = load().dkv_dequant_pages(ctypes.byref(c), _p(ids), n, _p(k), _p(v), _p(pos), _stream(stream))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_dequant_pages")
+    return k, v, pos
+
+
+class Profiler:
+    """Per-kernel CUDA-event timing of dkv_compact calls (library-owned events)."""
+
+    def __init__(self, max_calls: int):
+        h = ctypes.c_void_p()
+        rc = load().dkv_profiler_create(int(max_calls), ctypes.byref(h))
+        if rc != DKV_OK:
+            raise DkvError(rc, "dkv_profiler_create")
+        self.handle = h.value
+        self.max_calls = int(max_calls)
+
+    def read(self):
+        """[(ms per kernel) for each recorded call], then starts a new recording."""
+        buf = (ctypes.c_float * (self.max_calls * DKV_PROFILE_KERNELS))()
+        n = load().dkv_profiler_read(self.handle, buf, self.max_calls)
+        if n < 0:
+            raise DkvError(n, "dkv_profiler_read")
+        return [list(buf[c * DKV_PROFILE_KERNELS:(c + 1) * DKV_PROFILE_KERNELS]) for c in range(n)]
+
+    def close(self):
+        if self.handle:
+            load().dkv_profiler_destroy(self.handle)
+            self.handle = None
+
+
+class Compactor:
+    """Convenience owner of pool, tables, classes and workspace for one shape."""
+
+    def __init__(self, L: int, R: int, Hq: int, Hkv: int, T: int, max_len: int, P: int, F: int, device="cuda"):
+        self.L, self.R, self.Hq, self.Hkv, self.T, self.max_len = L, R, Hq, Hkv, T, max_len
+        self.U = L * R * Hkv
+        self.pmax = -(-max_len // P) + 1
+        self.pool = DevicePool(F, P, device)
+        self.tables = DeviceTables(self.U, self.pmax, device)
+        self.classes = torch.empty(max(L * T * Hkv, 1), dtype=torch.uint8, device=device)
+        probe = dkv_batch(L, R, Hq, Hkv, 128, max_len, T, 0, None, None, None, None, None, None)
+        self.workspace = torch.empty(dkv_workspace_size(probe), dtype=torch.uint8, device=device)
+        dkv_init_pool(self.pool)
+
+    def batch(self, inp: dict, unit_base: int = 0) -> dkv_batch:
+        return make_batch(inp, self.classes, self.max_len, unit_base)
+
+    def compact(self, inp: dict, alpha_h: float, alpha_l: float, stream=None, spin_limit: int = -1,
+                profiler=None, unit_base: int = 0) -> None:
+        dkv_compact(self.batch(inp, unit_base), alpha_h, alpha_l, self.pool, self.tables, self.workspace,
+                    stream=stream, spin_limit=spin_limit, profiler=profiler)

@@ -1,0 +1,189 @@
+/*
+ * dkv.h -- libdkv: differentiated KV-cache compaction on one GB300 (sm_103a).
+ *
+ * Method: "DiffKV: Differentiated Memory Management for Large Language Models
+ * with Parallel KV Compaction" (arXiv 2412.03131), as summarised on its Pith
+ * review page.  For every (layer, request, KV head) -- a "unit" -- the library
+ *   1. scores each token by the average attention it has received from later
+ *      tokens, max-aggregated over the GQA query heads of the KV head
+ *      ("What carries the argument"; Referee Report, major comment 2 on
+ *      Section 4 / Algorithm 1);
+ *   2. classifies it against alpha_h/N and alpha_l/N into K8V4 (keys 8-bit,
+ *      values 4-bit), K4V2 or pruned ("Core claim");
+ *   3. hands every unit a disjoint contiguous run of page ids from a circular
+ *      free page list through a parallel prefix sum over the units' page
+ *      demands, and fills the bidirectional page table ("What carries the
+ *      argument"; abstract: "on-GPU memory manager that compacts fragmented
+ *      free memory list into contiguous regions in parallel");
+ *   4. quantises the surviving tokens per token (asymmetric min/max over the
+ *      128 channels of a head, fp16 scale and zero, fp32 round-half-to-even)
+ *      and packs them into unified pages ("Core claim": unified pages).
+ *
+ * Conventions shared by every call
+ *   - Every data pointer is a DEVICE pointer, allocated and owned by the
+ *     caller.  The library allocates no device memory; dkv_compact takes a
+ *     caller-provided workspace sized by dkv_workspace_size.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream unless stated.
+ *   - Return value: DKV_OK or a negative code.  A *synchronous* error (bad
+ *     argument: DKV_E_INVAL; a CUDA launch failure: DKV_E_CUDA) means nothing
+ *     was enqueued.  Conditions found on the device (DKV_E_NOMEM,
+ *     DKV_E_RANGE, DKV_E_TIMEOUT, DKV_E_LENS, DKV_E_INTERNAL) are recorded in
+ *     the pool's device status word and read with dkv_get_status.  A call
+ *     that ends in a device-side error changes neither the cursors, nor the
+ *     forward and reverse tables, nor any live page: it is all-or-nothing
+ *     (pages that were free may have been scribbled and stay free).
+ *   - Calls on one pool must be ordered on one stream (or synchronised by the
+ *     caller); two calls on one pool in flight at once race.
+ *
+ * Unit order is layer-major: u = (l * R + r) * Hkv + h.  One call over L
+ * layers gives bit-identical results to L one-layer calls made in layer
+ * order with unit_base = l * R * Hkv and tables offset by the same unit count.
+ *
+ * Unified page layout (216 * P bytes; P even).  A K8V4 page holds P tokens,
+ * a K4V2 page 2P tokens, so both spend 192 * P bytes on codes:
+ *     [0, 128P)        K codes: K8V4 slot s at 128*s (one byte per channel);
+ *                      K4V2 slot s at 64*s (two channels per byte)
+ *     [128P, 192P)     V codes: K8V4 slot s at 128P + 64*s (4-bit);
+ *                      K4V2 slot s at 128P + 32*s (2-bit)
+ *     [192P, 208P)     per slot s at 192P + 8*s: fp16 k_scale, k_zero,
+ *                      v_scale, v_zero
+ *     [208P, 216P)     per slot s at 208P + 4*s: int32 token position
+ * Sub-byte codes pack lowest channel in the lowest bits.  Slots fill in rank
+ * order (ascending position); unused slots, including slots P..2P-1 of a K8V4
+ * page, hold zero codes, zero metadata and position -1.
+ *
+ * Quantiser per token row x[0..127] and bit width b (n = 2^b - 1):
+ *     mn = min x, mx = max x (a zero extreme taken as +0); any non-finite x
+ *     or |x| > 65504 is DKV_E_RANGE
+ *     s16 = fp16_rn((mx - mn) / n), set to 2^-24 if it is 0 while mx > mn
+ *     z16 = fp16_rn(mn);  s = (float)s16, z = (float)z16
+ *     q   = s == 0 ? 0 : clamp(rint_even((x - z) / s), 0, n)   (fp32 ops)
+ *     x'  = fma((float)q, s, z)                               (dequantised)
+ */
+#ifndef DKV_H
+#define DKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DKV_OK 0
+#define DKV_E_INVAL (-1)    /* sync: invalid argument; nothing enqueued */
+#define DKV_E_NOMEM (-2)    /* device: total page demand > free pages */
+#define DKV_E_RANGE (-3)    /* device: a K/V value to quantise is non-finite or > 65504 */
+#define DKV_E_TIMEOUT (-4)  /* device: a bounded wait of the page scan gave up */
+#define DKV_E_INTERNAL (-5) /* device: an internal consistency check failed */
+#define DKV_E_CUDA (-6)     /* sync: a CUDA call failed while enqueuing */
+#define DKV_E_LENS (-7)     /* device: lens[] disagree with T or max_len */
+
+/* Token classes written to dkv_batch.classes and dkv_pool.page_cls. */
+#define DKV_CLASS_PRUNE 0
+#define DKV_CLASS_K4V2 1
+#define DKV_CLASS_K8V4 2
+
+#define DKV_HEAD_DIM 128
+
+/* One batch of prefill tokens.  T = sum(lens) tokens per layer and KV head. */
+typedef struct dkv_batch {
+  int32_t L, R, Hq, Hkv, D;  /* layers, requests, query heads, KV heads, D = 128 */
+  int32_t max_len;           /* host-side upper bound on every lens[r] */
+  int64_t T;                 /* total tokens of the batch (sum of lens) */
+  int64_t unit_base;         /* global id of unit 0 of this call, stored in rev_unit */
+  const void *k;             /* bf16 [L][T][Hkv][128], 16-byte aligned */
+  const void *v;             /* bf16 [L][T][Hkv][128], 16-byte aligned */
+  const float *sig_sum;      /* fp32 [L][T][Hq]: summed attention each token received */
+  const int32_t *sig_cnt;    /* int32 [T]: how many scores were summed (N - i in prefill) */
+  const int32_t *lens;       /* int32 [R]: tokens of each request, device memory */
+  uint8_t *classes;          /* out: uint8 [L][T][Hkv], DKV_CLASS_* per token row */
+} dkv_batch;
+
+typedef struct dkv_params {
+  float alpha_h;             /* K8V4 threshold alpha_h / N */
+  float alpha_l;             /* K4V2 threshold alpha_l / N; 0 <= alpha_l <= alpha_h */
+  int32_t spin_limit;        /* polls of one predecessor in the scan look-back before
+                                DKV_E_TIMEOUT; 0 gives up at once (any call with
+                                more than one scan partition then times out);
+                                negative = library default (about a second) */
+  int32_t reserved;          /* must be 0 */
+  void *profiler;            /* nullable dkv_profiler*: per-kernel event timing */
+} dkv_params;
+
+/* The page pool: circular free list, cursors, reverse table and pages. */
+typedef struct dkv_pool {
+  int64_t F;                 /* pages; 1 <= F <= 2^31 - 1 */
+  int32_t P;                 /* K8V4 tokens per page (K4V2 pages hold 2P); even */
+  int32_t reserved;
+  int32_t *free_list;        /* int32 [F]: ring of free page ids, slots [head, tail) mod F */
+  uint64_t *cursors;         /* uint64 [2]: {head, tail}, monotone; free = tail - head */
+  int32_t *rev_unit;         /* int32 [F]: owning global unit id, -1 if free */
+  int32_t *rev_idx;          /* int32 [F]: index in the owner's forward row, -1 if free */
+  uint8_t *page_cls;         /* uint8 [F]: 0 free, 1 K4V2 page, 2 K8V4 page */
+  uint8_t *pages;            /* uint8 [F][216 * P], 16-byte aligned */
+  int32_t *status;           /* int32 [1]: first device-side error since last read */
+} dkv_pool;
+
+/* Forward page table of the units of one call. */
+typedef struct dkv_tables {
+  int32_t *fwd;              /* int32 [U][pmax]: page ids, K8V4 pages first; -1 past demand */
+  int32_t pmax;              /* >= ceil(max_len / P) + 1 */
+  int32_t reserved;
+  int32_t *unit_hdr;         /* int32 [U][4]: {n_k8v4, n_k4v2, pages_k8v4, pages_k4v2} */
+} dkv_tables;
+
+/* Workspace bytes dkv_compact needs for this batch shape (host only; reads
+ * L, R, Hkv, T and max_len of `b`).  Returns DKV_OK or DKV_E_INVAL. */
+int32_t dkv_workspace_size(const dkv_batch *b, size_t *bytes);
+
+/* Reset a pool: free_list[i] = i, head = 0, tail = F, rev_* = -1,
+ * page_cls = 0, status = 0.  Page contents are left as they are. */
+int32_t dkv_init_pool(const dkv_pool *pool, void *stream);
+
+/* Prefill compaction of one batch (steps 1-4 above), asynchronous.
+ * workspace: device, 256-byte aligned, >= dkv_workspace_size bytes; its
+ * contents need no initialisation and are scratch after the call.
+ * On success: classes written; for every unit u, fwd[u][0 .. d_u) holds the
+ * page ids taken from free-list slots [head + off_u, head + off_u + d_u) mod F
+ * (off_u = exclusive prefix sum of d_u = ceil(n_k8v4 / P) + ceil(n_k4v2 / 2P)),
+ * rev_unit / rev_idx / page_cls describe those pages, the pages hold the
+ * packed tokens, and head advanced by sum(d_u). */
+int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *pool,
+                    const dkv_tables *t, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/* Dequantise one page: k_out, v_out fp32 [2P][128], pos_out int32 [2P]
+ * (device).  Slots the page class does not have, unused slots and free pages
+ * decode to 0 with position -1.  page_id outside [0, F) is DKV_E_INVAL. */
+int32_t dkv_dequant_page(const dkv_pool *pool, int32_t page_id, float *k_out, float *v_out,
+                         int32_t *pos_out, void *stream);
+
+/* Dequantise n pages whose ids are in device memory page_ids[n]; outputs are
+ * [n][2P][128] and [n][2P].  An id outside [0, F) decodes as a free page. */
+int32_t dkv_dequant_pages(const dkv_pool *pool, const int32_t *page_ids, int32_t n,
+                          float *k_out, float *v_out, int32_t *pos_out, void *stream);
+
+/* Synchronise `stream`, return the pool's device status word (DKV_OK or the
+ * first device-side error since the last read) and clear it. */
+int32_t dkv_get_status(const dkv_pool *pool, void *stream);
+
+/* Per-kernel timing of dkv_compact with CUDA events.  A profiler holds
+ * events for up to max_calls calls; every dkv_compact given it (through
+ * dkv_params.profiler) records its kernels into the next call slot.
+ * dkv_profiler_read synchronises and writes, for each recorded call c and
+ * kernel k, ms[c * DKV_PROFILE_KERNELS + k]; it returns the number of calls
+ * recorded and starts a new recording. */
+#define DKV_PROFILE_KERNELS 5 /* prep, classify, page scan, quantise+scatter, commit */
+int32_t dkv_profiler_create(int32_t max_calls, void **profiler);
+int32_t dkv_profiler_read(void *profiler, float *ms, int32_t capacity_calls);
+int32_t dkv_profiler_destroy(void *profiler);
+
+const char *dkv_status_string(int32_t code);
+int32_t dkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DKV_H */

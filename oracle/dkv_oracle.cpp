@@ -23,7 +23,8 @@
  *      (the review flags the 1/i wording as ambiguous; Algorithm 1 uses
  *      alpha/N).  thr = fp32(alpha / (float)N).  "At or above" is >= for both
  *      thresholds.  sig_cnt == 0 ("not yet observed") keeps the token K8V4.
- *  Q1  Quantizer per token row of 128 values and per tensor: mn, mx exact;
+ *  Q1  Quantizer per token row of 128 values and per tensor: mn, mx exact
+ *      (a zero extreme canonicalised to +0);
  *      any |x| > 65504 or non-finite x is a range error; s32 = (mx-mn)/n with
  *      n = 2^b - 1; s16 = fp16_rn(s32), bumped to 2^-24 if it underflows to 0
  *      while mx > mn; z16 = fp16_rn(mn); q = clamp(rint((x - z) / s), 0, n)
@@ -183,6 +184,10 @@ int32_t oracle_quant_row(const uint16_t *x, int32_t bits, uint8_t *q, uint16_t *
     if (xf[d] < mn) mn = xf[d];
     if (xf[d] > mx) mx = xf[d];
   }
+  /* reading Q1: a zero extreme is taken as +0 (IEEE min/max leave the sign
+   * of a zero result open when both zeros occur) */
+  mn = mn + 0.0f;
+  mx = mx + 0.0f;
   const int n = (1 << bits) - 1;
   const float span = mx - mn;
   const float s32 = span / static_cast<float>(n);
