@@ -68,13 +68,15 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(CompactArgs a) {
       const int64_t l = lr / a.R;
       const int32_t tr0 = a.tile_off[r];
       const int32_t nt = a.tile_off[r + 1] - tr0;
-      const int64_t tau0 = (l * TR + tr0) * a.Hkv + static_cast<int64_t>(h) * nt;
+      const int64_t tau0 = (l * a.Hkv + h) * TR + tr0;
       for (int jb = 0; jb < nt; jb += 32) {
         const int j = jb + lane;
         int32_t ch = 0, cl = 0;
+        uint4 hw = make_uint4(0, 0, 0, 0), lw = hw;
         if (j < nt) {
           const uint4 *m = reinterpret_cast<const uint4 *>(a.mask + (tau0 + j) * (2 * kMaskWords));
-          const uint4 hw = m[0], lw = m[1];
+          hw = m[0];
+          lw = m[1];
           ch = __popc(hw.x) + __popc(hw.y) + __popc(hw.z) + __popc(hw.w);
           cl = __popc(lw.x) + __popc(lw.y) + __popc(lw.z) + __popc(lw.w);
         }
@@ -88,7 +90,16 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(CompactArgs a) {
             il += xl;
           }
         }
-        if (j < nt) a.base[tau0 + j] = make_int2(nh + ih - ch, nl + il - cl);
+        if (j < nt) {
+          TileDesc &t = a.desc[tau0 + j];
+          t.hm = hw;
+          t.lm = lw;
+          t.base_hi = nh + ih - ch;
+          t.base_lo = nl + il - cl;
+          t.tok_row = static_cast<int32_t>(l * a.T + a.tok_off[r] + static_cast<int64_t>(j) * kTileTokens);
+          t.h = h;
+          t.pos0 = j * kTileTokens;
+        }
         nh += __shfl_sync(0xffffffffu, ih, 31);
         nl += __shfl_sync(0xffffffffu, il, 31);
       }
@@ -163,7 +174,8 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(CompactArgs a) {
       a.ws->total = total;
       a.ws->head = head;
       a.ws->head_mod = static_cast<int64_t>(head % static_cast<uint64_t>(a.F));
-      if (static_cast<uint64_t>(total) > tail - head) set_error(&a.ws->err, DKV_E_NOMEM);
+      // free pages are tail - head (never more than F for a consistent pool)
+      if (static_cast<uint64_t>(total) > tail - head || total > a.F) set_error(&a.ws->err, DKV_E_NOMEM);
     }
   }
   __syncthreads();
@@ -172,8 +184,39 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(CompactArgs a) {
     const int64_t off = prefix_s + ex_s[tid];
     a.unit[u0 + tid] = UnitInfo{nh_s[tid], nl_s[tid], static_cast<int32_t>(off), ceil_div(nh_s[tid], a.P)};
   }
+  // every tile of the partition's units learns where its unit's pages start
+  // in the free list (meaningful only when the call does not run out of pages)
+  const int64_t head_mod = static_cast<int64_t>(a.cursors[0] % static_cast<uint64_t>(a.F));
+  for (int uu = warp; uu < kScanUnits; uu += kScanThreads / 32) {
+    const int64_t u = u0 + uu;
+    if (u >= a.U) break;
+    const int32_t h = static_cast<int32_t>(u % a.Hkv);
+    const int64_t lr = u / a.Hkv;
+    const int32_t r = static_cast<int32_t>(lr % a.R);
+    const int64_t l = lr / a.R;
+    const int32_t tr0 = a.tile_off[r];
+    const int32_t nt = a.tile_off[r + 1] - tr0;
+    const int64_t tau0 = (l * a.Hkv + h) * TR + tr0;
+    int64_t ring = head_mod + (prefix_s + ex_s[uu]) % a.F;
+    if (ring >= a.F) ring -= a.F;
+    const int32_t p_hi = ceil_div(nh_s[uu], a.P);
+    for (int j = lane; j < nt; j += 32) {
+      a.desc[tau0 + j].ring = static_cast<int32_t>(ring);
+      a.desc[tau0 + j].p_hi = p_hi;
+    }
+  }
 }
 
+__device__ __forceinline__ void fill_words(uint8_t *p, int64_t nwords, uint32_t value, int lane) {
+  uint32_t *w = reinterpret_cast<uint32_t *>(p);
+  for (int64_t i = lane; i < nwords; i += 32) w[i] = value;
+}
+
+// Commit of a successful call: forward and reverse tables, page classes,
+// unit headers, the head cursor; and the unused slots of the new pages (zero
+// codes and metadata, position -1): slots P..2P-1 of every K8V4 page and the
+// tail of each unit's last K8V4 and K4V2 page.  A failed call only records
+// its error in the pool's status word.
 __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
   const int32_t err = a.ws->err;
   if (err != 0) {
@@ -182,6 +225,8 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
   }
   const int lane = threadIdx.x & 31;
   const int64_t head_mod = a.ws->head_mod;
+  const int64_t P = a.P;
+  const int64_t page_bytes = 216 * P;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kCommitThreads / 32);
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * (kCommitThreads / 32) + (threadIdx.x >> 5); u < a.U;
        u += nwarps) {
@@ -200,10 +245,40 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
         a.rev_unit[id] = static_cast<int32_t>(a.unit_base + u);
         a.rev_idx[id] = k;
         a.page_cls[id] = k < inf.p_hi ? DKV_CLASS_K8V4 : DKV_CLASS_K4V2;
+        if (k < inf.p_hi) {  // a K8V4 page has no slots P..2P-1
+          uint8_t *pg = a.pages + id * page_bytes;
+          uint4 *meta = reinterpret_cast<uint4 *>(pg + 200 * P);
+          int2 *pos = reinterpret_cast<int2 *>(pg + 212 * P);
+          for (int64_t i = 0; i < P / 2; ++i) {
+            meta[i] = make_uint4(0u, 0u, 0u, 0u);
+            pos[i] = make_int2(-1, -1);
+          }
+        }
       }
       fw[k] = id;
     }
     if (lane == 0) reinterpret_cast<int4 *>(a.unit_hdr)[u] = make_int4(inf.n_hi, inf.n_lo, inf.p_hi, p_lo);
+    // tails of the last K8V4 and the last K4V2 page
+    const int64_t sh = inf.n_hi % P;
+    if (sh != 0) {
+      int64_t idx = ring + inf.p_hi - 1;
+      if (idx >= a.F) idx -= a.F;
+      uint8_t *pg = a.pages + static_cast<int64_t>(a.free_list[idx]) * page_bytes;
+      fill_words(pg + 128 * sh, 32 * (P - sh), 0u, lane);
+      fill_words(pg + 128 * P + 64 * sh, 16 * (P - sh), 0u, lane);
+      fill_words(pg + 192 * P + 8 * sh, 2 * (P - sh), 0u, lane);
+      fill_words(pg + 208 * P + 4 * sh, P - sh, 0xffffffffu, lane);
+    }
+    const int64_t sl = inf.n_lo % (2 * P);
+    if (sl != 0) {
+      int64_t idx = ring + d - 1;
+      if (idx >= a.F) idx -= a.F;
+      uint8_t *pg = a.pages + static_cast<int64_t>(a.free_list[idx]) * page_bytes;
+      fill_words(pg + 64 * sl, 16 * (2 * P - sl), 0u, lane);
+      fill_words(pg + 128 * P + 32 * sl, 8 * (2 * P - sl), 0u, lane);
+      fill_words(pg + 192 * P + 8 * sl, 2 * (2 * P - sl), 0u, lane);
+      fill_words(pg + 208 * P + 4 * sl, 2 * P - sl, 0xffffffffu, lane);
+    }
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) a.cursors[0] = a.ws->head + static_cast<uint64_t>(a.ws->total);
 }

@@ -33,6 +33,15 @@ bool device_info(int *sms, int *pack_bps) {
   return true;
 }
 
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+// Map a CUDA status to DKV_OK / DKV_E_CUDA, remembering the CUDA error.
+int32_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DKV_OK;
+  g_last_cuda = e;
+  return DKV_E_CUDA;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 struct Profiler {
@@ -60,6 +69,8 @@ bool valid_shape(const dkv_batch *b) {
   if (b->T < 0 || b->T > INT32_MAX || b->max_len < 0) return false;
   const int64_t U = static_cast<int64_t>(b->L) * b->R * b->Hkv;
   if (U > INT32_MAX || b->unit_base < 0 || b->unit_base + U > INT32_MAX) return false;
+  // K / V rows are addressed with 32-bit TMA row coordinates
+  if (static_cast<int64_t>(b->L) * b->T * b->Hkv > INT32_MAX) return false;
   return true;
 }
 
@@ -68,6 +79,8 @@ bool valid_shape(const dkv_batch *b) {
 extern "C" {
 
 int32_t dkv_version(void) { return 100; }
+
+const char *dkv_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda); }
 
 const char *dkv_status_string(int32_t code) {
   switch (code) {
@@ -91,7 +104,7 @@ int32_t dkv_workspace_size(const dkv_batch *b, size_t *bytes) {
 
 int32_t dkv_init_pool(const dkv_pool *pool, void *stream) {
   if (!valid_pool(pool)) return DKV_E_INVAL;
-  return dkv::launch_init_pool(*pool, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DKV_OK : DKV_E_CUDA;
+  return cuda_status(dkv::launch_init_pool(*pool, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *pool, const dkv_tables *t,
@@ -110,7 +123,7 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
   const dkv::WsLayout lay = dkv::ws_layout(b->L, b->R, b->Hkv, b->T);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.bytes) return DKV_E_INVAL;
   int sms = 0, pack_bps = 0;
-  if (!device_info(&sms, &pack_bps)) return DKV_E_CUDA;
+  if (!device_info(&sms, &pack_bps)) return cuda_status(cudaErrorInvalidDevice);
 
   CompactArgs a{};
   a.L = b->L; a.R = b->R; a.Hq = b->Hq; a.Hkv = b->Hkv; a.G = b->Hq / b->Hkv;
@@ -128,10 +141,11 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
   a.ws = reinterpret_cast<dkv::WsHeader *>(ws);
   a.tok_off = reinterpret_cast<int64_t *>(ws + lay.tok_off);
   a.tile_off = reinterpret_cast<int32_t *>(ws + lay.tile_off);
+  a.tile_req = reinterpret_cast<int32_t *>(ws + lay.tile_req);
   a.part = reinterpret_cast<uint64_t *>(ws + lay.part);
   a.unit = reinterpret_cast<dkv::UnitInfo *>(ws + lay.unit);
   a.mask = reinterpret_cast<uint32_t *>(ws + lay.mask);
-  a.base = reinterpret_cast<int2 *>(ws + lay.base);
+  a.desc = reinterpret_cast<dkv::TileDesc *>(ws + lay.desc);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Profiler *prof = static_cast<Profiler *>(p->profiler);
@@ -150,15 +164,15 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
   const int commit_grid = static_cast<int>(std::min<int64_t>((a.U + 7) / 8, static_cast<int64_t>(sms) * 8));
 
   mark(0);
-  if (dkv::launch_prep(a, s) != cudaSuccess) return DKV_E_CUDA;
+  if (const int32_t rc = cuda_status(dkv::launch_prep(a, s))) return rc;
   mark(1);
-  if (dkv::launch_classify(a, std::max(classify_grid, 1), s) != cudaSuccess) return DKV_E_CUDA;
+  if (const int32_t rc = cuda_status(dkv::launch_classify(a, std::max(classify_grid, 1), s))) return rc;
   mark(2);
-  if (dkv::launch_scan(a, lay.npart, s) != cudaSuccess) return DKV_E_CUDA;
+  if (const int32_t rc = cuda_status(dkv::launch_scan(a, lay.npart, s))) return rc;
   mark(3);
-  if (dkv::launch_pack(a, pack_grid, s) != cudaSuccess) return DKV_E_CUDA;
+  if (const int32_t rc = cuda_status(dkv::launch_pack(a, pack_grid, s))) return rc;
   mark(4);
-  if (dkv::launch_commit(a, std::max(commit_grid, 1), s) != cudaSuccess) return DKV_E_CUDA;
+  if (const int32_t rc = cuda_status(dkv::launch_commit(a, std::max(commit_grid, 1), s))) return rc;
   mark(5);
   return DKV_OK;
 }
@@ -166,20 +180,16 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
 int32_t dkv_dequant_page(const dkv_pool *pool, int32_t page_id, float *k_out, float *v_out, int32_t *pos_out,
                          void *stream) {
   if (!valid_pool(pool) || page_id < 0 || page_id >= pool->F || !k_out || !v_out || !pos_out) return DKV_E_INVAL;
-  return dkv::launch_dequant(*pool, nullptr, page_id, 1, k_out, v_out, pos_out, static_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? DKV_OK
-             : DKV_E_CUDA;
+  return cuda_status(
+      dkv::launch_dequant(*pool, nullptr, page_id, 1, k_out, v_out, pos_out, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t dkv_dequant_pages(const dkv_pool *pool, const int32_t *page_ids, int32_t n, float *k_out, float *v_out,
                           int32_t *pos_out, void *stream) {
   if (!valid_pool(pool) || n < 0 || (n > 0 && (!page_ids || !k_out || !v_out || !pos_out))) return DKV_E_INVAL;
   if (n == 0) return DKV_OK;
-  return dkv::launch_dequant(*pool, page_ids, 0, n, k_out, v_out, pos_out, static_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? DKV_OK
-             : DKV_E_CUDA;
+  return cuda_status(
+      dkv::launch_dequant(*pool, page_ids, 0, n, k_out, v_out, pos_out, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t dkv_get_status(const dkv_pool *pool, void *stream) {

@@ -86,6 +86,10 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(CompactArgs a, int32_t np
     if (r < a.R) {
       a.tok_off[r] = before_tok + it - n;
       a.tile_off[r] = before_tile + il - nt;
+      // request of each of its tiles (bounded by the workspace's room)
+      const int64_t room = a.T / kTileTokens + a.R;
+      for (int32_t x = 0; x < nt; ++x)
+        if (before_tile + il - nt + x < room) a.tile_req[before_tile + il - nt + x] = static_cast<int32_t>(r);
     }
     __syncthreads();
     if (tid == blockDim.x - 1) {
@@ -111,8 +115,8 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(CompactArgs a, int32_t np
 template <bool kVec>
 __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  float *sig_s = reinterpret_cast<float *>(smem);                     // [tile][Hq]
-  int32_t *cnt_s = reinterpret_cast<int32_t *>(sig_s + kTileTokens * a.Hq);  // [tile]
+  float *sig_s = reinterpret_cast<float *>(smem);                     // [tile][Hq + 1]
+  int32_t *cnt_s = reinterpret_cast<int32_t *>(sig_s + kTileTokens * (a.Hq + 1));  // [tile]
   uint8_t *cls_s = reinterpret_cast<uint8_t *>(cnt_s + kTileTokens);  // [tile][Hkv]
   if (a.ws->err != 0) return;
   const int32_t TR = a.ws->TR;
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
   for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
     const int64_t l = item / TR;
     const int32_t rt = static_cast<int32_t>(item - l * TR);
-    const int r = find_segment(a.tile_off, a.R + 1, rt, 1);
+    const int r = __ldg(a.tile_req + rt);
     const int32_t tr0 = __ldg(a.tile_off + r);
     const int32_t nt = __ldg(a.tile_off + r + 1) - tr0;
     const int32_t j = rt - tr0;
@@ -134,20 +138,32 @@ __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
     const float thr_h = __fdiv_rn(a.alpha_h, static_cast<float>(N));
     const float thr_l = __fdiv_rn(a.alpha_l, static_cast<float>(N));
 
-    // stage the tile's summed scores [cnt][Hq] (contiguous) and counts
+    // stage the tile's summed scores [cnt][Hq] into rows padded to Hq + 1
+    // floats, so the per-token reads below hit 32 different banks
     const float *src = a.sig_sum + (l * a.T + t0) * a.Hq;
     const int nf = cnt * a.Hq;
+    const int ld = a.Hq + 1;
     if (kVec) {
       const float4 *s4 = reinterpret_cast<const float4 *>(src);
-      float4 *d4 = reinterpret_cast<float4 *>(sig_s);
-      for (int i = tid; i < (nf >> 2); i += blockDim.x) d4[i] = __ldcs(s4 + i);
+      for (int i = tid; i < (nf >> 2); i += blockDim.x) {
+        const float4 x = __ldcs(s4 + i);
+        const int k = (4 * i) / a.Hq;
+        float *d = sig_s + k * ld + (4 * i - k * a.Hq);
+        d[0] = x.x;
+        d[1] = x.y;
+        d[2] = x.z;
+        d[3] = x.w;
+      }
     } else {
-      for (int i = tid; i < nf; i += blockDim.x) sig_s[i] = __ldcs(src + i);
+      for (int i = tid; i < nf; i += blockDim.x) {
+        const int k = i / a.Hq;
+        sig_s[k * ld + (i - k * a.Hq)] = __ldcs(src + i);
+      }
     }
     for (int i = tid; i < cnt; i += blockDim.x) cnt_s[i] = __ldg(a.sig_cnt + t0 + i);
     __syncthreads();
 
-    const int64_t tau0 = (l * TR + tr0) * a.Hkv + j;
+    const int64_t tau0 = l * a.Hkv * TR + rt;  // unit tile of head 0
     for (int p = tid; p < a.Hkv * kTileTokens; p += blockDim.x) {
       const int h = p / kTileTokens;
       const int k = p % kTileTokens;
@@ -157,7 +173,7 @@ __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
         if (n == 0) {
           c = DKV_CLASS_K8V4;  // not yet observed: keep at high precision
         } else {
-          const float *row = sig_s + k * a.Hq + h * G;
+          const float *row = sig_s + k * (a.Hq + 1) + h * G;
           float m = row[0];
           if (n > 0) {
             for (int g = 1; g < G; ++g) m = fmaxf(m, row[g]);
@@ -172,7 +188,7 @@ __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
       const uint32_t hi = __ballot_sync(0xffffffffu, c == DKV_CLASS_K8V4);
       const uint32_t lo = __ballot_sync(0xffffffffu, c == DKV_CLASS_K4V2);
       if ((tid & 31) == 0) {
-        uint32_t *m = a.mask + (tau0 + static_cast<int64_t>(h) * nt) * (2 * kMaskWords);
+        uint32_t *m = a.mask + (tau0 + static_cast<int64_t>(h) * TR) * (2 * kMaskWords);
         m[k >> 5] = hi;
         m[kMaskWords + (k >> 5)] = lo;
       }
@@ -185,7 +201,7 @@ __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
 }
 
 size_t classify_smem(int Hq, int Hkv) {
-  return sizeof(float) * kTileTokens * Hq + sizeof(int32_t) * kTileTokens + kTileTokens * Hkv;
+  return sizeof(float) * kTileTokens * (Hq + 1) + sizeof(int32_t) * kTileTokens + kTileTokens * Hkv;
 }
 
 }  // namespace

@@ -2,10 +2,11 @@
 //
 // Work decomposition of one dkv_compact call
 //   unit      (layer l, request r, KV head h), u = (l * R + r) * Hkv + h
-//   tile      kTileTokens consecutive tokens of one request; a "unit tile" is
-//             a tile of one unit.  Unit tiles are numbered
-//             tau = (l * TR + tile_off[r]) * Hkv + h * nt_r + j,
-//             nt_r = ceil(N_r / kTileTokens), TR = sum_r nt_r.
+//   tile      kTileTokens consecutive tokens of one request; rt = tile_off[r] + j
+//             numbers the (request, tile) pairs, TR = sum_r ceil(N_r / tile).
+//             A "unit tile" is a tile of one unit, numbered
+//             tau = (l * Hkv + h) * TR + rt, so a unit's tiles are contiguous
+//             and tile_req[rt] = r decodes tau without a search.
 //
 // Kernels, in stream order (all bounded, none traps):
 //   k_prep      1 block: request prefix sums, length validation, resets
@@ -51,14 +52,29 @@ struct UnitInfo {
   int32_t n_hi, n_lo, off, p_hi;
 };
 
+// Everything the quantise + scatter kernel needs of one unit tile, written by
+// the scan (64 bytes, one load per tile).
+struct __align__(16) TileDesc {
+  uint4 hm, lm;       // K8V4 / K4V2 bitmasks of the tile's 128 tokens
+  int32_t base_hi;    // K8V4 rank of the tile's first K8V4 row within its unit
+  int32_t base_lo;    // K4V2 rank likewise
+  int32_t tok_row;    // l * T + first token of the tile
+  int32_t h;          // KV head
+  int32_t pos0;       // position of the tile's token 0 in its request
+  int32_t ring;       // free-list slot of the unit's first page, (head + off) mod F
+  int32_t p_hi;       // K8V4 pages of the unit
+  int32_t pad;
+};
+
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
   size_t tok_off;    // int64 [R + 1]
   size_t tile_off;   // int32 [R + 1]
+  size_t tile_req;   // int32 [tr_max]: request of each (request, tile) pair
   size_t part;       // uint64 [npart]
   size_t unit;       // UnitInfo [U]
   size_t mask;       // uint32 [NT][2 * kMaskWords]: K8V4 words then K4V2 words
-  size_t base;       // int2 [NT]: K8V4 and K4V2 rank of the tile's first row
+  size_t desc;       // TileDesc [NT]
   size_t bytes;      // total
   int64_t nt_max;    // unit tiles the layout has room for
   int32_t npart;
@@ -75,10 +91,11 @@ inline WsLayout ws_layout(int64_t L, int64_t R, int64_t Hkv, int64_t T) {
   size_t o = align256(sizeof(WsHeader));
   w.tok_off = o;  o = align256(o + sizeof(int64_t) * (R + 1));
   w.tile_off = o; o = align256(o + sizeof(int32_t) * (R + 1));
+  w.tile_req = o; o = align256(o + sizeof(int32_t) * tr_max);
   w.part = o;     o = align256(o + sizeof(uint64_t) * w.npart);
   w.unit = o;     o = align256(o + sizeof(UnitInfo) * U);
   w.mask = o;     o = align256(o + sizeof(uint32_t) * 2 * kMaskWords * w.nt_max);
-  w.base = o;     o = align256(o + sizeof(int2) * w.nt_max);
+  w.desc = o;     o = align256(o + sizeof(TileDesc) * w.nt_max);
   w.bytes = o;
   return w;
 }
@@ -103,10 +120,11 @@ struct CompactArgs {
   WsHeader *ws;
   int64_t *tok_off;
   int32_t *tile_off;
+  int32_t *tile_req;
   uint64_t *part;
   UnitInfo *unit;
   uint32_t *mask;
-  int2 *base;
+  TileDesc *desc;
 };
 
 __device__ __forceinline__ void set_error(int32_t *err, int32_t code) { atomicCAS(err, 0, code); }

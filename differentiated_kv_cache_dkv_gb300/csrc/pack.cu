@@ -10,31 +10,43 @@
 //
 // Exactness.  The reference result is q = rint(RN(RN(x - z) / s)) in fp32.
 // The kernel computes d = RN(x - z) exactly as the definition, then
-// y = RN(d * RN(1/s) + 1536) with one fused multiply-add.  y lies in
-// [1024, 2048), so it carries the quotient in fixed point with 13 fraction
-// bits: w = bits(y) - bits(1536).  The error of w * 2^-13 against RN(d / s)
-// is below 0.75 * 2^-13 (quotient <= 256: 2^-24 relative for the reciprocal,
-// half an ulp of y, 2^-24 relative for the reference's own rounding), so
-// (w + 4096) >> 13 equals the round-to-nearest-even code unless
-// w + 4096 is a multiple of 2^13 exactly -- only then can the quotient sit on
-// a tie or on the other side of one.  Those elements, and rows whose end
-// points would need clamping (checked exactly per row), are recomputed with
-// the IEEE division.  Codes are therefore bit-identical to the definition.
+// y = RN(d * RN(1/s) + 1536.5) with one fused multiply-add (packed two
+// channels at a time with sub.rn.f32x2 / fma.rn.f32x2, which round each half
+// like the scalar operation).  y lies in [1024, 2048), so it carries t + 0.5
+// in fixed point with 13 fraction bits.  The error of that fixed-point value
+// against RN(d / s) + 0.5 is below 0.75 * 2^-13 (quotient <= 256: 2^-24
+// relative for the reciprocal, half an ulp of y, 2^-24 relative for the
+// reference's own rounding), so bits(y) >> 13 carries the round-to-nearest-even
+// code in its low bits unless the 13 fraction bits are all zero -- only then
+// can the quotient sit on a tie or on the other side of one.  Those elements,
+// and rows whose end points would need clamping (checked exactly per row), are
+// recomputed with the IEEE division.  Codes are therefore bit-identical to
+// the definition.
 //
-// Work layout.  A block takes unit tiles (128 tokens of one (layer, request,
-// KV head)) in a grid-stride loop.  From the tile's two class bitmasks it
-// lists the surviving rows, K8V4 first, with their page id and slot (ranks
-// come from popcounts plus the tile's rank bases from the scan), so pruned
-// rows are never read and most warps see a single class.  A warp takes 16
-// list entries: 4 groups of 8 lanes, each group 4 rows, each lane 16 channels
-// (two 128-bit loads per tensor).  Row min / max are bf16x2 min / max
-// (NaN-propagating) reduced over the 8 lanes; the per-row scalar work (scale,
-// zero, reciprocal, end-point check, metadata store) is spread one job per
-// lane; codes are packed in registers and stored 4-16 bytes per lane, so the
-// four groups of a warp write neighbouring slots of a page.
+// Work layout (one CTA per SM, persistent over unit tiles = 128 tokens of one
+// (layer, request, KV head)), a warp-specialised pipeline over a ring of
+// kStages shared-memory stages:
+//   producer warp  issues two TMA tile loads per tile (cp.async.bulk.tensor
+//       3-D: the 128 consecutive token rows of one KV head, 32 KB of K and 32
+//       KB of V) into the stage, completing on its "full" mbarrier, then
+//       stores the list of surviving rows (K8V4 first, ranks by popcount of
+//       the class bitmasks) with page id (from the circular free list), slot
+//       and position, and arrives on it.  Tile descriptors are prefetched two
+//       tiles ahead and free-list lookups one tile ahead.
+//   consumer warps (16) take one row per 4-lane group, 8 rows per warp:
+//       bf16x2 min / max reduced over the group, one lane each computes the K
+//       and the V scale / zero / reciprocal and stores the slot's metadata and
+//       position, then every lane quantises its 32 K and 32 V channels and
+//       stores their packed codes; the stage is released on its "empty"
+//       mbarrier.
+// Unused slots of the pages are filled by k_commit, which walks every page.
+// Every mbarrier wait is bounded; on expiry the CTA records DKV_E_TIMEOUT,
+// drains its own copies in flight (again bounded) and leaves.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "dkv_internal.cuh"
 
@@ -42,14 +54,79 @@ namespace dkv {
 
 namespace {
 
-constexpr int kPackThreads = 256;
-constexpr int kPackWarps = kPackThreads / 32;
-constexpr int kRowsPerWarp = 16;
-static_assert(kPackWarps * kRowsPerWarp == kTileTokens, "one warp pass per tile");
+constexpr int kStages = 3;
+constexpr int kProducerWarps = 1;
+constexpr int kConsumerWarps = 16;
+constexpr int kRowsPerConsumerWarp = kTileTokens / kConsumerWarps;  // 8: one per 4-lane group
+constexpr int kPackThreads = 32 * (kConsumerWarps + kProducerWarps);
+constexpr int64_t kWaitLimit = 1ll << 24;  // polls of one mbarrier before giving up
+static_assert(kRowsPerConsumerWarp == 8, "8 groups of 4 lanes per consumer warp");
 
-constexpr float kMagic = 1536.0f;           // 1.5 * 2^10: y in [1024, 2048), ulp 2^-13
-constexpr uint32_t kMagicBits = 0x44C00000u;  // bits of 1536.0f
-constexpr uint32_t kBias = 4096u - kMagicBits;  // v = w + 4096 (mod 2^32)
+// 1536 = 1.5 * 2^10 puts y in [1024, 2048) (ulp 2^-13); the extra 0.5 turns
+// the floor of the 13-bit shift into round-to-nearest.  bits(1536) is a
+// multiple of 2^21, so bits(y) >> 13 carries the code in its low 8 bits and
+// bits(y) & 8191 is the fixed-point fraction of t + 0.5.
+constexpr float kMagicHalf = 1536.5f;
+
+struct __align__(128) Stage {
+  uint8_t k[kTileTokens][256];   // bf16 K rows of the tile's 128 tokens
+  uint8_t v[kTileTokens][256];   // bf16 V rows
+  int4 ent[kTileTokens];         // per listed row: page id, slot, position, token in tile
+  int32_t info[4];               // nsurv, nh_t
+};
+
+struct PackSmem {
+  Stage st[kStages];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+};
+constexpr size_t kPackSmemBytes = sizeof(PackSmem) + 128;  // + alignment slack
+
+// ------------------------------------------------------------ PTX helpers --
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  const uint32_t addr = smem_addr(bar);
+  for (int64_t i = 0; i < kWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+// TMA load of one box of a 3-D tensor map at coordinates (c0, c1, c2),
+// completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// -------------------------------------------------------------- numerics --
 
 __device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
   __nv_bfloat162 r = __hmin2_nan(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
@@ -64,197 +141,305 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Min and max over 16 bf16 channels (8 words), reduced over the 8 lanes of a
-// group.  Returns the pair packed as bf16x2 {min, -max}.
-__device__ __forceinline__ uint32_t row_minmax(const uint4 &a, const uint4 &b) {
-  uint32_t mn = bmin2(bmin2(bmin2(a.x, a.y), bmin2(a.z, a.w)), bmin2(bmin2(b.x, b.y), bmin2(b.z, b.w)));
-  uint32_t mx = bmax2(bmax2(bmax2(a.x, a.y), bmax2(a.z, a.w)), bmax2(bmax2(b.x, b.y), bmax2(b.z, b.w)));
-  // {min(lo, hi) of mn, min(lo, hi) of -mx}: pair (mn.lo, -mx.lo) vs (mn.hi, -mx.hi)
+// Min and max over the 32 bf16 channels a lane holds (16 words), reduced
+// over the 4 lanes of a group.  Returns the pair packed as bf16x2
+// {min, -max} (NaN propagates).
+__device__ __forceinline__ uint32_t row_minmax(const uint4 &a, const uint4 &b, const uint4 &c, const uint4 &d) {
+  const uint32_t m0 = bmin2(bmin2(bmin2(a.x, a.y), bmin2(a.z, a.w)), bmin2(bmin2(b.x, b.y), bmin2(b.z, b.w)));
+  const uint32_t m1 = bmin2(bmin2(bmin2(c.x, c.y), bmin2(c.z, c.w)), bmin2(bmin2(d.x, d.y), bmin2(d.z, d.w)));
+  const uint32_t x0 = bmax2(bmax2(bmax2(a.x, a.y), bmax2(a.z, a.w)), bmax2(bmax2(b.x, b.y), bmax2(b.z, b.w)));
+  const uint32_t x1 = bmax2(bmax2(bmax2(c.x, c.y), bmax2(c.z, c.w)), bmax2(bmax2(d.x, d.y), bmax2(d.z, d.w)));
+  const uint32_t mn = bmin2(m0, m1), mx = bmax2(x0, x1);
   const uint32_t p0 = __byte_perm(mn, mx, 0x5410) ^ 0x80000000u;  // {mn.lo, -mx.lo}
   const uint32_t p1 = __byte_perm(mn, mx, 0x7632) ^ 0x80000000u;  // {mn.hi, -mx.hi}
   uint32_t p = bmin2(p0, p1);
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1) p = bmin2(p, __shfl_xor_sync(0xffffffffu, p, o));
+  p = bmin2(p, __shfl_xor_sync(0xffffffffu, p, 1));
+  p = bmin2(p, __shfl_xor_sync(0xffffffffu, p, 2));
   return p;
 }
 
-// Fast code of one element (see the file header); `zero` accumulates the
-// minimum of the low 13 bits, 0 flags a possible tie.
-__device__ __forceinline__ uint32_t fast_code(float x, float z, float r, uint32_t &flag) {
-  const float d = __fsub_rn(x, z);
-  const float y = __fmaf_rn(d, r, kMagic);
-  const uint32_t v = __float_as_uint(y) + kBias;
-  flag = min(flag, v & 8191u);
-  return v >> 13;
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
 }
 
-__device__ __forceinline__ uint32_t exact_code(float x, float z, float s, float n) {
-  const float t = __fdiv_rn(__fsub_rn(x, z), s);
-  const float q = fminf(fmaxf(rintf(t), 0.0f), n);
-  return static_cast<uint32_t>(q);
+// Result bits of two channels held as one bf16x2 word, with packed fp32 math
+// (each half rounded exactly like the scalar IEEE operation):
+//   y = RN(RN(x - z) * r + 1536.5)
+__device__ __forceinline__ void fast_pair(uint32_t w, uint64_t zz, uint64_t rr, uint64_t mm, uint32_t &b0,
+                                          uint32_t &b1) {
+  const uint64_t x = pack2(bf_lo(w), bf_hi(w));
+  uint64_t d, y;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(zz));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(y) : "l"(d), "l"(rr), "l"(mm));
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(b0), "=r"(b1) : "l"(y));
 }
 
-// Codes of 16 channels held as 8 bf16x2 words.
-struct Codes16 {
-  uint32_t c[16];
+// Codes of 16 channels (a: channels 0-7, b: 8-15) with the exact division
+// wherever the fast code may differ from the definition, or everywhere for a
+// row that needs clamping (r < 0); one code per byte.  Rare, so out of line.
+__device__ __noinline__ uint4 exact16(uint4 a, uint4 b, float z, float r, float s, float n) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t out[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float x = (i & 1) ? bf_hi(w[i >> 1]) : bf_lo(w[i >> 1]);
+    const float d = __fsub_rn(x, z);
+    const uint32_t bits = __float_as_uint(__fmaf_rn(d, r, kMagicHalf));
+    uint32_t q = (bits >> 13) & 255u;
+    if (r < 0.0f || (bits & 8191u) == 0u) q = static_cast<uint32_t>(fminf(fmaxf(rintf(__fdiv_rn(d, s)), 0.0f), n));
+    out[i >> 2] |= q << (8 * (i & 3));
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// Per channel the bits of y; the code sits in bits [13, 13 + width).
+struct Bits16 {
+  uint32_t b[16];
 };
 
 __device__ __forceinline__ void quant16(const uint4 &a, const uint4 &b, float z, float r, float s, float n,
-                                        Codes16 &q) {
+                                        Bits16 &q) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const uint64_t zz = pack2(z, z), rr = pack2(r, r), mm = pack2(kMagicHalf, kMagicHalf);
   uint32_t flag = 0xffffffffu;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    q.c[2 * i] = fast_code(bf_lo(w[i]), z, r, flag);
-    q.c[2 * i + 1] = fast_code(bf_hi(w[i]), z, r, flag);
+    fast_pair(w[i], zz, rr, mm, q.b[2 * i], q.b[2 * i + 1]);
+    flag = min(flag, q.b[2 * i] & 8191u);
+    flag = min(flag, q.b[2 * i + 1] & 8191u);
   }
-  if (flag == 0u || r < 0.0f) {  // rare: a possible tie, or a row that needs clamping
+  if (flag == 0u || r < 0.0f) {
+    const uint4 e = exact16(a, b, z, r, s, n);
+    const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float x = (i & 1) ? bf_hi(w[i >> 1]) : bf_lo(w[i >> 1]);
-      const float y = __fmaf_rn(__fsub_rn(x, z), r, kMagic);
-      if (r < 0.0f || ((__float_as_uint(y) + kBias) & 8191u) == 0u) q.c[i] = exact_code(x, z, s, n);
-    }
+    for (int i = 0; i < 16; ++i) q.b[i] = ((ew[i >> 2] >> (8 * (i & 3))) & 255u) << 13;
   }
 }
 
-// Pack 16 codes of `bits` bits, lowest channel in the lowest bits.
-__device__ __forceinline__ uint32_t pack_word(const Codes16 &q, int first, int count, int bits) {
+// Pack `count` codes of `width` bits starting at channel `first`, lowest
+// channel in the lowest bits: one shift and one and-or per code.
+template <int kWidth, int kCount>
+__device__ __forceinline__ uint32_t pack_codes(const Bits16 &q, int first) {
   uint32_t w = 0;
 #pragma unroll
-  for (int i = count - 1; i >= 0; --i) w = (w << bits) | q.c[first + i];
+  for (int i = 0; i < kCount; ++i) {
+    const int sh = 13 - kWidth * i;
+    const uint32_t x = sh >= 0 ? (q.b[first + i] >> sh) : (q.b[first + i] << -sh);
+    w |= x & (((1u << kWidth) - 1u) << (kWidth * i));
+  }
   return w;
 }
 
-__device__ __forceinline__ void fill_words(uint8_t *p, int64_t nwords, uint32_t value, int tid) {
-  uint32_t *w = reinterpret_cast<uint32_t *>(p);
-  for (int64_t i = tid; i < nwords; i += kPackThreads) w[i] = value;
+// Quantise a lane's 32 K and 32 V channels of one row (chunks c = l4 + 4j,
+// channels 8c..8c+7) and store their packed codes into the row's slot.
+__device__ __forceinline__ void store_row(uint8_t *pg, int32_t P, int32_t slot_, bool high, int l4, const uint4 &k0,
+                                          const uint4 &k1, const uint4 &k2, const uint4 &k3, const uint4 &v0,
+                                          const uint4 &v1, const uint4 &v2, const uint4 &v3, float kz, float kq,
+                                          float ks, float vz, float vq, float vs) {
+  const int64_t slot = slot_;
+  const int c0 = l4, c1 = l4 + 4, c2 = l4 + 8, c3 = l4 + 12;
+  Bits16 q;
+  if (high) {
+    uint8_t *kd = pg + slot * 128;
+    uint8_t *vd = pg + 128 * static_cast<int64_t>(P) + slot * 64;
+    quant16(k0, k1, kz, kq, ks, 255.0f, q);
+    *reinterpret_cast<uint2 *>(kd + 8 * c0) = make_uint2(pack_codes<8, 4>(q, 0), pack_codes<8, 4>(q, 4));
+    *reinterpret_cast<uint2 *>(kd + 8 * c1) = make_uint2(pack_codes<8, 4>(q, 8), pack_codes<8, 4>(q, 12));
+    quant16(k2, k3, kz, kq, ks, 255.0f, q);
+    *reinterpret_cast<uint2 *>(kd + 8 * c2) = make_uint2(pack_codes<8, 4>(q, 0), pack_codes<8, 4>(q, 4));
+    *reinterpret_cast<uint2 *>(kd + 8 * c3) = make_uint2(pack_codes<8, 4>(q, 8), pack_codes<8, 4>(q, 12));
+    quant16(v0, v1, vz, vq, vs, 15.0f, q);
+    *reinterpret_cast<uint32_t *>(vd + 4 * c0) = pack_codes<4, 8>(q, 0);
+    *reinterpret_cast<uint32_t *>(vd + 4 * c1) = pack_codes<4, 8>(q, 8);
+    quant16(v2, v3, vz, vq, vs, 15.0f, q);
+    *reinterpret_cast<uint32_t *>(vd + 4 * c2) = pack_codes<4, 8>(q, 0);
+    *reinterpret_cast<uint32_t *>(vd + 4 * c3) = pack_codes<4, 8>(q, 8);
+  } else {
+    uint8_t *kd = pg + slot * 64;
+    uint8_t *vd = pg + 128 * static_cast<int64_t>(P) + slot * 32;
+    quant16(k0, k1, kz, kq, ks, 15.0f, q);
+    *reinterpret_cast<uint32_t *>(kd + 4 * c0) = pack_codes<4, 8>(q, 0);
+    *reinterpret_cast<uint32_t *>(kd + 4 * c1) = pack_codes<4, 8>(q, 8);
+    quant16(k2, k3, kz, kq, ks, 15.0f, q);
+    *reinterpret_cast<uint32_t *>(kd + 4 * c2) = pack_codes<4, 8>(q, 0);
+    *reinterpret_cast<uint32_t *>(kd + 4 * c3) = pack_codes<4, 8>(q, 8);
+    quant16(v0, v1, vz, vq, vs, 3.0f, q);
+    *reinterpret_cast<uint16_t *>(vd + 2 * c0) = static_cast<uint16_t>(pack_codes<2, 8>(q, 0));
+    *reinterpret_cast<uint16_t *>(vd + 2 * c1) = static_cast<uint16_t>(pack_codes<2, 8>(q, 8));
+    quant16(v2, v3, vz, vq, vs, 3.0f, q);
+    *reinterpret_cast<uint16_t *>(vd + 2 * c2) = static_cast<uint16_t>(pack_codes<2, 8>(q, 0));
+    *reinterpret_cast<uint16_t *>(vd + 2 * c3) = static_cast<uint16_t>(pack_codes<2, 8>(q, 8));
+  }
 }
 
-__global__ void __launch_bounds__(kPackThreads, 2) k_pack(CompactArgs a) {
-  __shared__ int32_t ent_tok[kTileTokens];
-  __shared__ int32_t ent_page[kTileTokens];
-  __shared__ int32_t ent_slot[kTileTokens];
-  if (a.ws->err != 0) return;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int grp = lane >> 3, l8 = lane & 7;
-  const int32_t TR = a.ws->TR;
-  const int64_t head_mod = a.ws->head_mod;
-  const int64_t per_layer = static_cast<int64_t>(TR) * a.Hkv;
-  const int64_t ntiles = per_layer * a.L;
-  const int64_t P = a.P;
-  const int64_t page_bytes = 216 * P;
+// ---------------------------------------------------------------- kernel --
 
-  for (int64_t tau = blockIdx.x; tau < ntiles; tau += gridDim.x) {
-    // ---- which unit tile
-    const int64_t l = tau / per_layer;
-    const int64_t rem = tau - l * per_layer;
-    const int r = find_segment(a.tile_off, a.R + 1, rem, a.Hkv);
-    const int32_t tr0 = __ldg(a.tile_off + r);
-    const int32_t nt = __ldg(a.tile_off + r + 1) - tr0;
-    const int32_t q = static_cast<int32_t>(rem - static_cast<int64_t>(tr0) * a.Hkv);
-    const int32_t h = q / nt;
-    const int32_t j = q - h * nt;
-    const int64_t u = (l * a.R + r) * a.Hkv + h;
-    const int64_t t0 = __ldg(a.tok_off + r) + static_cast<int64_t>(j) * kTileTokens;
+__device__ __forceinline__ TileDesc load_desc(const CompactArgs &a, int32_t tau) {
+  const uint4 *p = reinterpret_cast<const uint4 *>(a.desc + tau);
+  TileDesc d;
+  uint4 *q = reinterpret_cast<uint4 *>(&d);
+  q[0] = __ldg(p);
+  q[1] = __ldg(p + 1);
+  q[2] = __ldg(p + 2);
+  q[3] = __ldg(p + 3);
+  return d;
+}
 
-    const uint4 *mp = reinterpret_cast<const uint4 *>(a.mask + tau * (2 * kMaskWords));
-    const uint4 hm = mp[0], lm = mp[1];
-    const int2 base = a.base[tau];
-    const UnitInfo inf = a.unit[u];
-    const uint32_t hw[4] = {hm.x, hm.y, hm.z, hm.w};
-    const uint32_t lw[4] = {lm.x, lm.y, lm.z, lm.w};
-    const int nh_t = __popc(hw[0]) + __popc(hw[1]) + __popc(hw[2]) + __popc(hw[3]);
-    const int nl_t = __popc(lw[0]) + __popc(lw[1]) + __popc(lw[2]) + __popc(lw[3]);
-    const int nsurv = nh_t + nl_t;
-    int64_t ring = head_mod + inf.off;
-    if (ring >= a.F) ring -= a.F;
+__device__ __forceinline__ uint32_t word_of(const uint4 &m, int w) {
+  return w == 0 ? m.x : (w == 1 ? m.y : (w == 2 ? m.z : m.w));
+}
 
-    // ---- list the surviving rows: K8V4 first, each with page id and slot
-    if (tid < kTileTokens) {
-      const int k = tid, wi = k >> 5;
-      const uint32_t below = (1u << (k & 31)) - 1u;
-      int rh = __popc(hw[wi] & below), rl = __popc(lw[wi] & below);
+// The rows of one tile a producer lane owns (tokens lane + 32x): list entry
+// (K8V4 first, -1 if pruned), slot and page id (a load that may still be in
+// flight until the value is used).
+struct ProducerRows {
+  int ent[kMaskWords], slot[kMaskWords];
+  int32_t id[kMaskWords];
+  int nsurv, nh_t;
+};
+
+__device__ __forceinline__ void list_rows(const CompactArgs &a, const TileDesc &m, int lane, int32_t P,
+                                          ProducerRows &o) {
+  int nh_t = 0, nl_t = 0, pre_h[kMaskWords], pre_l[kMaskWords];
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
-        if (x < wi) {
-          rh += __popc(hw[x]);
-          rl += __popc(lw[x]);
-        }
-      const bool is_hi = (hw[wi] >> (k & 31)) & 1u;
-      const bool is_lo = (lw[wi] >> (k & 31)) & 1u;
-      if (is_hi || is_lo) {
-        int e;
-        int64_t pidx, slot;
-        if (is_hi) {
-          e = rh;
-          const int64_t rho = base.x + rh;
-          pidx = rho / P;
-          slot = rho - pidx * P;
-        } else {
-          e = nh_t + rl;
-          const int64_t rho = base.y + rl;
-          const int64_t pl = rho / (2 * P);
-          pidx = inf.p_hi + pl;
-          slot = rho - pl * 2 * P;
-        }
-        int64_t idx = ring + pidx;
-        if (idx >= a.F) idx -= a.F;
-        int32_t id = a.free_list[idx];
-        if (id < 0 || id >= a.F) {
-          set_error(&a.ws->err, DKV_E_INTERNAL);
-          id = -1;
-        }
-        ent_tok[e] = k;
-        ent_page[e] = id;
-        ent_slot[e] = static_cast<int32_t>(slot);
-      }
+  for (int x = 0; x < kMaskWords; ++x) {
+    pre_h[x] = nh_t;
+    pre_l[x] = nl_t;
+    nh_t += __popc(word_of(m.hm, x));
+    nl_t += __popc(word_of(m.lm, x));
+  }
+  const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+  for (int x = 0; x < kMaskWords; ++x) {
+    const uint32_t hw = word_of(m.hm, x), lw = word_of(m.lm, x);
+    const bool is_hi = (hw >> lane) & 1u;
+    const bool is_lo = (lw >> lane) & 1u;
+    int pidx = 0;
+    o.ent[x] = -1;
+    o.slot[x] = 0;
+    if (is_hi) {
+      o.ent[x] = pre_h[x] + __popc(hw & below);
+      const int32_t rho = m.base_hi + o.ent[x];
+      pidx = rho / P;
+      o.slot[x] = rho - pidx * P;
+    } else if (is_lo) {
+      const int rl = pre_l[x] + __popc(lw & below);
+      o.ent[x] = nh_t + rl;
+      const int32_t rho = m.base_lo + rl;
+      const int32_t pl = rho / (2 * P);
+      pidx = m.p_hi + pl;
+      o.slot[x] = rho - pl * 2 * P;
     }
-    __syncthreads();
+    int64_t idx = static_cast<int64_t>(m.ring) + pidx;
+    if (idx >= a.F) idx -= a.F;
+    o.id[x] = o.ent[x] >= 0 ? __ldg(a.free_list + idx) : 0;
+  }
+  o.nsurv = nh_t + nl_t;
+  o.nh_t = nh_t;
+}
 
-    // ---- quantise + pack + scatter: warp `warp` takes entries [16 warp, 16 warp + 16)
-    const int e0 = warp * kRowsPerWarp;
-    if (e0 < nsurv) {
-      uint4 kr[4][2], vr[4][2];
-      const uint16_t *kbase = a.k + ((l * a.T + t0) * a.Hkv + h) * 128 + 16 * l8;
-      const uint16_t *vbase = a.v + ((l * a.T + t0) * a.Hkv + h) * 128 + 16 * l8;
-      const int64_t tok_stride = static_cast<int64_t>(a.Hkv) * 128;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int e = e0 + grp + 4 * i;
-        if (e < nsurv) {
-          const int64_t off = ent_tok[e] * tok_stride;
-          const uint4 *kp = reinterpret_cast<const uint4 *>(kbase + off);
-          const uint4 *vp = reinterpret_cast<const uint4 *>(vbase + off);
-          kr[i][0] = __ldcs(kp);
-          kr[i][1] = __ldcs(kp + 1);
-          vr[i][0] = __ldcs(vp);
-          vr[i][1] = __ldcs(vp + 1);
-        } else {
-          kr[i][0] = kr[i][1] = vr[i][0] = vr[i][1] = make_uint4(0, 0, 0, 0);
-        }
+__global__ void __launch_bounds__(kPackThreads, 1)
+    k_pack(CompactArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+  extern __shared__ unsigned char smem_raw[];
+  PackSmem &sm = *reinterpret_cast<PackSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (a.ws->err != 0) return;
+
+  const int32_t TR = a.ws->TR;
+  const int32_t ntiles = TR * a.Hkv * a.L;  // < 2^31: rows are validated below 2^31
+  const int32_t P = a.P;
+  const int64_t page_bytes = 216 * static_cast<int64_t>(P);
+
+  if (warp >= kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    int64_t it = 0;
+    bool ok = true;
+    const int32_t g = gridDim.x;
+    const int32_t t0 = blockIdx.x;
+    TileDesc cur{}, nxt{}, nxt2{};
+    if (t0 < ntiles) cur = load_desc(a, t0);
+    if (t0 + g < ntiles) nxt = load_desc(a, t0 + g);
+    ProducerRows rows_cur, rows_nxt;
+    if (t0 < ntiles) list_rows(a, cur, lane, P, rows_cur);
+    for (int32_t tau = t0; tau < ntiles; tau += g, ++it) {
+      if (tau + 2 * g < ntiles) nxt2 = load_desc(a, tau + 2 * g);
+      const int s = static_cast<int>(it % kStages);
+      const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
+      if (it >= kStages && !mbar_wait(&sm.empty[s], ph ^ 1u)) {
+        ok = false;
+        break;
       }
-      // row min / max per (row, tensor), reduced over the 8 lanes of the group
-      uint32_t mm[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        mm[2 * i] = row_minmax(kr[i][0], kr[i][1]);
-        mm[2 * i + 1] = row_minmax(vr[i][0], vr[i][1]);
+      Stage &st = sm.st[s];
+      if (lane == 0) {
+        mbar_expect_tx(&sm.full[s], 2u * kTileTokens * 256u);
+        tma_load_3d(st.k, &kmap, 0, cur.h, cur.tok_row, &sm.full[s]);
+        tma_load_3d(st.v, &vmap, 0, cur.h, cur.tok_row, &sm.full[s]);
       }
-      // one scalar job per lane: row l8 >> 1, tensor l8 & 1
-      uint32_t mine = mm[0];
+      if (tau + g < ntiles) list_rows(a, nxt, lane, P, rows_nxt);
 #pragma unroll
-      for (int x = 1; x < 8; ++x) mine = (l8 == x) ? mm[x] : mine;
-      const int ji = l8 >> 1, jt = l8 & 1;
-      const int ej = e0 + grp + 4 * ji;
-      const bool jvalid = ej < nsurv;
-      const bool jhigh = ej < nh_t;
-      const int bits = jt == 0 ? (jhigh ? 8 : 4) : (jhigh ? 4 : 2);
-      const float nmax = static_cast<float>((1 << bits) - 1);
+      for (int x = 0; x < kMaskWords; ++x) {
+        if (rows_cur.ent[x] < 0) continue;
+        const int k = 32 * x + lane;
+        st.ent[rows_cur.ent[x]] = make_int4(rows_cur.id[x], rows_cur.slot[x], cur.pos0 + k, k);
+      }
+      if (lane == 0) {
+        st.info[0] = rows_cur.nsurv;
+        st.info[1] = rows_cur.nh_t;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.full[s]);
+      cur = nxt;
+      nxt = nxt2;
+      rows_cur = rows_nxt;
+    }
+    if (!ok) set_error(&a.ws->err, DKV_E_TIMEOUT);
+    for (int64_t q = (it > kStages ? it - kStages : 0); q < it; ++q)
+      mbar_wait(&sm.full[q % kStages], static_cast<uint32_t>((q / kStages) & 1));
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int grp = lane >> 2, l4 = lane & 3;
+  const int e = warp * kRowsPerConsumerWarp + grp;  // list row of this group
+  int64_t it = 0;
+  for (int32_t tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++it) {
+    const int s = static_cast<int>(it % kStages);
+    const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
+    if (!mbar_wait(&sm.full[s], ph)) {
+      set_error(&a.ws->err, DKV_E_TIMEOUT);
+      return;
+    }
+    const Stage &st = sm.st[s];
+    const int nsurv = st.info[0];
+    const int nh_t = st.info[1];
+    if (warp * kRowsPerConsumerWarp < nsurv) {
+      const bool valid = e < nsurv;
+      const int4 en = st.ent[valid ? e : 0];  // page id, slot, position, token in tile
+      // channels 8c..8c+7 for the chunks c = l4 + 4j, j = 0..3
+      const uint4 *kr = reinterpret_cast<const uint4 *>(st.k[en.w]);
+      const uint4 *vr = reinterpret_cast<const uint4 *>(st.v[en.w]);
+      const uint4 k0 = kr[l4], k1 = kr[l4 + 4], k2 = kr[l4 + 8], k3 = kr[l4 + 12];
+      const uint4 v0 = vr[l4], v1 = vr[l4 + 4], v2 = vr[l4 + 8], v3 = vr[l4 + 12];
+      const uint32_t kmm = row_minmax(k0, k1, k2, k3);
+      const uint32_t vmm = row_minmax(v0, v1, v2, v3);
+      const bool high = e < nh_t;
+      // scalar job: lane 0 of the group for K, lane 1 for V
+      const int jt = l4 & 1;
+      const uint32_t mine = jt ? vmm : kmm;
+      const float nmax = jt == 0 ? (high ? 255.0f : 15.0f) : (high ? 15.0f : 3.0f);
       // a zero extreme is +0 (min / max leave the sign of a zero open)
       const float mn = __fadd_rn(bf_lo(mine), 0.0f);
       const float mx = __fadd_rn(-bf_hi(mine), 0.0f);
-      if (jvalid && !(fabsf(mn) <= 65504.0f && fabsf(mx) <= 65504.0f)) set_error(&a.ws->err, DKV_E_RANGE);
       const float s32 = __fdiv_rn(__fsub_rn(mx, mn), nmax);
       __half hs = __float2half_rn(s32);
       if (mx > mn && __half_as_ushort(hs) == 0) hs = __ushort_as_half(1);  // 2^-24
@@ -264,113 +449,75 @@ __global__ void __launch_bounds__(kPackThreads, 2) k_pack(CompactArgs a) {
       float jr = 0.0f;
       if (js != 0.0f) {
         jr = __frcp_rn(js);
-        const float qlo = rintf(__fdiv_rn(__fsub_rn(mn, jz), js));
-        const float qhi = rintf(__fdiv_rn(__fsub_rn(mx, jz), js));
-        if (!(qlo >= 0.0f && qhi <= nmax)) jr = -1.0f;  // row needs clamping: exact path
-      }
-      if (jvalid) {
-        const int32_t pid = ent_page[ej];
-        if (pid >= 0) {
-          uint8_t *pg = a.pages + pid * page_bytes;
-          const int64_t slot = ent_slot[ej];
-          const uint32_t meta = static_cast<uint32_t>(__half_as_ushort(hs)) |
-                                (static_cast<uint32_t>(__half_as_ushort(hz)) << 16);
-          *reinterpret_cast<uint32_t *>(pg + 192 * P + 8 * slot + 4 * jt) = meta;
-          if (jt == 0)
-            *reinterpret_cast<int32_t *>(pg + 208 * P + 4 * slot) = j * kTileTokens + ent_tok[ej];
+        // Clamping can only be needed when the zero point is not the minimum
+        // itself or the scale lost precision as an fp16 subnormal; then check
+        // the end points exactly.
+        if (jz != mn || js < 6.103515625e-05f) {
+          const float qlo = rintf(__fdiv_rn(__fsub_rn(mn, jz), js));
+          const float qhi = rintf(__fdiv_rn(__fsub_rn(mx, jz), js));
+          if (!(qlo >= 0.0f && qhi <= nmax)) jr = -1.0f;  // row needs clamping: exact path
         }
       }
-      // codes, row by row
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int src = (grp << 3) + 2 * i;
-        const float kz = __shfl_sync(0xffffffffu, jz, src);
-        const float kq = __shfl_sync(0xffffffffu, jr, src);
-        const float ks = __shfl_sync(0xffffffffu, js, src);
-        const float vz = __shfl_sync(0xffffffffu, jz, src + 1);
-        const float vq = __shfl_sync(0xffffffffu, jr, src + 1);
-        const float vs = __shfl_sync(0xffffffffu, js, src + 1);
-        const int e = e0 + grp + 4 * i;
-        if (e >= nsurv) continue;
-        const int32_t pid = ent_page[e];
-        if (pid < 0) continue;
-        const int64_t slot = ent_slot[e];
-        uint8_t *pg = a.pages + pid * page_bytes;
-        const bool high = e < nh_t;
-        Codes16 ck, cv;
-        if (high) {
-          quant16(kr[i][0], kr[i][1], kz, kq, ks, 255.0f, ck);
-          quant16(vr[i][0], vr[i][1], vz, vq, vs, 15.0f, cv);
-          const uint4 kw = make_uint4(pack_word(ck, 0, 4, 8), pack_word(ck, 4, 4, 8), pack_word(ck, 8, 4, 8),
-                                      pack_word(ck, 12, 4, 8));
-          const uint2 vw = make_uint2(pack_word(cv, 0, 8, 4), pack_word(cv, 8, 8, 4));
-          *reinterpret_cast<uint4 *>(pg + slot * 128 + 16 * l8) = kw;
-          *reinterpret_cast<uint2 *>(pg + 128 * P + slot * 64 + 8 * l8) = vw;
-        } else {
-          quant16(kr[i][0], kr[i][1], kz, kq, ks, 15.0f, ck);
-          quant16(vr[i][0], vr[i][1], vz, vq, vs, 3.0f, cv);
-          const uint2 kw = make_uint2(pack_word(ck, 0, 8, 4), pack_word(ck, 8, 8, 4));
-          const uint32_t vw = pack_word(cv, 0, 16, 2);
-          *reinterpret_cast<uint2 *>(pg + slot * 64 + 8 * l8) = kw;
-          *reinterpret_cast<uint32_t *>(pg + 128 * P + slot * 32 + 4 * l8) = vw;
-        }
+      const bool pid_ok = en.x >= 0 && en.x < a.F;  // a corrupt free list is reported, not followed
+      if (valid && !pid_ok && l4 == 0) set_error(&a.ws->err, DKV_E_INTERNAL);
+      const bool write = valid && pid_ok;
+      uint8_t *pg = a.pages + static_cast<int64_t>(write ? en.x : 0) * page_bytes;
+      if (write && l4 < 2) {
+        if (!(fabsf(mn) <= 65504.0f && fabsf(mx) <= 65504.0f)) set_error(&a.ws->err, DKV_E_RANGE);
+        const uint32_t meta = static_cast<uint32_t>(__half_as_ushort(hs)) |
+                              (static_cast<uint32_t>(__half_as_ushort(hz)) << 16);
+        *reinterpret_cast<uint32_t *>(pg + 192 * P + 8 * static_cast<int64_t>(en.y) + 4 * jt) = meta;
+        if (jt == 0) *reinterpret_cast<int32_t *>(pg + 208 * P + 4 * static_cast<int64_t>(en.y)) = en.z;
       }
+      const int src = grp << 2;
+      const float kz = __shfl_sync(0xffffffffu, jz, src), kq = __shfl_sync(0xffffffffu, jr, src);
+      const float ks = __shfl_sync(0xffffffffu, js, src);
+      const float vz = __shfl_sync(0xffffffffu, jz, src + 1), vq = __shfl_sync(0xffffffffu, jr, src + 1);
+      const float vs = __shfl_sync(0xffffffffu, js, src + 1);
+      if (write) store_row(pg, P, en.y, high, l4, k0, k1, k2, k3, v0, v1, v2, v3, kz, kq, ks, vz, vq, vs);
     }
-
-    // ---- unused slots.  (a) every K8V4 page whose slot 0 is in this tile:
-    // metadata and positions of slots P..2P-1 (the page has no such slots).
-    {
-      const int64_t first = (base.x + P - 1) / P;         // first page starting at rank >= base.x
-      const int64_t last = (base.x + nh_t - 1) / P;       // page of the last rank in the tile
-      const int64_t npages = (nh_t > 0 && last >= first) ? last - first + 1 : 0;
-      const int64_t per_page = 3 * P;                      // 2P words of metadata, P of positions
-      for (int64_t w = tid; w < npages * per_page; w += kPackThreads) {
-        const int64_t pk = first + w / per_page;
-        const int64_t ww = w % per_page;
-        const int32_t pid = ent_page[pk * P - base.x];
-        if (pid < 0) continue;
-        uint8_t *pg = a.pages + pid * page_bytes;
-        if (ww < 2 * P) reinterpret_cast<uint32_t *>(pg + 200 * P)[ww] = 0u;
-        else reinterpret_cast<int32_t *>(pg + 212 * P)[ww - 2 * P] = -1;
-      }
-    }
-    // (b) tail of the unit's last K8V4 page, (c) tail of its last K4V2 page
-    if (nh_t > 0 && base.x + nh_t == inf.n_hi && (inf.n_hi % P) != 0) {
-      const int32_t pid = ent_page[nh_t - 1];
-      if (pid >= 0) {
-        uint8_t *pg = a.pages + pid * page_bytes;
-        const int64_t s0 = inf.n_hi % P;
-        fill_words(pg + 128 * s0, 32 * (P - s0), 0u, tid);
-        fill_words(pg + 128 * P + 64 * s0, 16 * (P - s0), 0u, tid);
-        fill_words(pg + 192 * P + 8 * s0, 2 * (P - s0), 0u, tid);
-        fill_words(pg + 208 * P + 4 * s0, P - s0, 0xffffffffu, tid);
-      }
-    }
-    if (nl_t > 0 && base.y + nl_t == inf.n_lo && (inf.n_lo % (2 * P)) != 0) {
-      const int32_t pid = ent_page[nsurv - 1];
-      if (pid >= 0) {
-        uint8_t *pg = a.pages + pid * page_bytes;
-        const int64_t s0 = inf.n_lo % (2 * P);
-        fill_words(pg + 64 * s0, 16 * (2 * P - s0), 0u, tid);
-        fill_words(pg + 128 * P + 32 * s0, 8 * (2 * P - s0), 0u, tid);
-        fill_words(pg + 192 * P + 8 * s0, 2 * (2 * P - s0), 0u, tid);
-        fill_words(pg + 208 * P + 4 * s0, 2 * P - s0, 0xffffffffu, tid);
-      }
-    }
-    __syncthreads();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
   }
+}
+
+// 3-D tensor map over a bf16 [L * T][Hkv][128] array whose box is the 128
+// channels of one KV head for 128 consecutive tokens.
+cudaError_t make_tile_map(CUtensorMap *map, const void *base, int64_t tokens, int32_t Hkv) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(tokens)};
+  const cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(Hkv) * 256};
+  const cuuint32_t box[3] = {128, 1, kTileTokens};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-int pack_blocks_per_sm() {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_pack, kPackThreads, 0) != cudaSuccess || n < 1) n = 1;
-  return n;
-}
+int pack_blocks_per_sm() { return 1; }
 
 cudaError_t launch_pack(const CompactArgs &a, int grid, cudaStream_t s) {
-  k_pack<<<grid, kPackThreads, 0, s>>>(a);
+  const int64_t tokens = static_cast<int64_t>(a.L) * a.T;
+  if (tokens < 1) return cudaSuccess;  // nothing can survive
+  alignas(64) CUtensorMap kmap, vmap;
+  cudaError_t e = make_tile_map(&kmap, a.k, tokens, a.Hkv);
+  if (e != cudaSuccess) return e;
+  e = make_tile_map(&vmap, a.v, tokens, a.Hkv);
+  if (e != cudaSuccess) return e;
+  const int smem = static_cast<int>(kPackSmemBytes);
+  e = cudaFuncSetAttribute(k_pack, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k_pack<<<grid, kPackThreads, smem, s>>>(a, kmap, vmap);
   return cudaGetLastError();
 }
 

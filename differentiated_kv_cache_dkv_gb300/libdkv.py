@@ -31,7 +31,8 @@ _lib = None
 
 class DkvError(RuntimeError):
     def __init__(self, code: int, what: str):
-        super().__init__(f"{what}: {status_string(code)} ({code})")
+        detail = f" [{load().dkv_last_cuda_error().decode()}]" if code == DKV_E_CUDA else ""
+        super().__init__(f"{what}: {status_string(code)} ({code}){detail}")
         self.code = code
 
 
@@ -77,6 +78,7 @@ def load():
     sigs = {
         "dkv_version": ([], i32),
         "dkv_status_string": ([i32], ctypes.c_char_p),
+        "dkv_last_cuda_error": ([], ctypes.c_char_p),
         "dkv_workspace_size": ([P(dkv_batch), P(ctypes.c_size_t)], i32),
         "dkv_init_pool": ([P(dkv_pool), vp], i32),
         "dkv_compact": ([P(dkv_batch), P(dkv_params), P(dkv_pool), P(dkv_tables), vp, ctypes.c_size_t, vp], i32),

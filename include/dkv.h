@@ -181,6 +181,10 @@ int32_t dkv_profiler_read(void *profiler, float *ms, int32_t capacity_calls);
 int32_t dkv_profiler_destroy(void *profiler);
 
 const char *dkv_status_string(int32_t code);
+
+/* Text of the CUDA error behind the calling thread's last DKV_E_CUDA
+ * ("no error" if there was none). */
+const char *dkv_last_cuda_error(void);
 int32_t dkv_version(void);
 
 #ifdef __cplusplus
