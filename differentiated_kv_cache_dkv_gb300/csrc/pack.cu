@@ -26,19 +26,21 @@
 // Work layout (one CTA per SM, persistent over unit tiles = 128 tokens of one
 // (layer, request, KV head)), a warp-specialised pipeline over a ring of
 // kStages shared-memory stages:
-//   producer warp  issues two TMA tile loads per tile (cp.async.bulk.tensor
+//   producer warps (2, alternate tiles) issue two TMA tile loads per tile
+//       (cp.async.bulk.tensor
 //       3-D: the 128 consecutive token rows of one KV head, 32 KB of K and 32
 //       KB of V) into the stage, completing on its "full" mbarrier, then
 //       stores the list of surviving rows (K8V4 first, ranks by popcount of
 //       the class bitmasks) with page id (from the circular free list), slot
-//       and position, and arrives on it.  Tile descriptors are prefetched two
-//       tiles ahead and free-list lookups one tile ahead.
-//   consumer warps (16) take one row per 4-lane group, 8 rows per warp:
-//       bf16x2 min / max reduced over the group, one lane each computes the K
-//       and the V scale / zero / reciprocal and stores the slot's metadata and
-//       position, then every lane quantises its 32 K and 32 V channels and
-//       stores their packed codes; the stage is released on its "empty"
-//       mbarrier.
+//       and position, and arrives on it.
+//   consumer warps (16) claim 8-row groups of a stage from a shared counter
+//       (K4V2 rows start at a multiple of 8, so a group is class-uniform),
+//       one row per 4-lane group: bf16x2 min / max reduced over the group,
+//       one lane each computes the K and the V scale / zero / reciprocal and
+//       stores the slot's metadata and position, then every lane quantises
+//       its 32 K and 32 V channels and stores their packed codes.  A warp
+//       that finds no group left arrives on the stage's "empty" mbarrier and
+//       moves on; the stage is refilled once all 16 have left it.
 // Unused slots of the pages are filled by k_commit, which walks every page.
 // Every mbarrier wait is bounded; on expiry the CTA records DKV_E_TIMEOUT,
 // drains its own copies in flight (again bounded) and leaves.
@@ -71,8 +73,9 @@ constexpr float kMagicHalf = 1536.5f;
 struct __align__(128) Stage {
   uint8_t k[kTileTokens][256];   // bf16 K rows of the tile's 128 tokens
   uint8_t v[kTileTokens][256];   // bf16 V rows
-  int4 ent[kTileTokens];         // per listed row: page id, slot, position, token in tile
-  int32_t info[4];               // nsurv, nh_t
+  int4 ent[kTileTokens + 8];     // per listed row: page id, slot, position, token in tile
+  int32_t info[4];               // entries spanned, K8V4 rows, first K4V2 entry, row groups
+  int32_t next_group;            // claim counter of the consumer warps
 };
 
 struct PackSmem {
@@ -291,9 +294,6 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &m, int w) {
   return w == 0 ? m.x : (w == 1 ? m.y : (w == 2 ? m.z : m.w));
 }
 
-// The rows of one tile a producer lane owns (tokens lane + 32x): list entry
-// (K8V4 first, -1 if pruned), slot and page id (a load that may still be in
-// flight until the value is used).
 struct ProducerRows {
   int ent[kMaskWords], slot[kMaskWords];
   int32_t id[kMaskWords];
@@ -310,6 +310,8 @@ __device__ __forceinline__ void list_rows(const CompactArgs &a, const TileDesc &
     nh_t += __popc(word_of(m.hm, x));
     nl_t += __popc(word_of(m.lm, x));
   }
+  // K4V2 entries start at a multiple of 8, so no 8-row group mixes classes
+  const int lo0 = (nh_t + 7) & ~7;
   const uint32_t below = (1u << lane) - 1u;
 #pragma unroll
   for (int x = 0; x < kMaskWords; ++x) {
@@ -326,7 +328,7 @@ __device__ __forceinline__ void list_rows(const CompactArgs &a, const TileDesc &
       o.slot[x] = rho - pidx * P;
     } else if (is_lo) {
       const int rl = pre_l[x] + __popc(lw & below);
-      o.ent[x] = nh_t + rl;
+      o.ent[x] = lo0 + rl;
       const int32_t rho = m.base_lo + rl;
       const int32_t pl = rho / (2 * P);
       pidx = m.p_hi + pl;
@@ -336,7 +338,7 @@ __device__ __forceinline__ void list_rows(const CompactArgs &a, const TileDesc &
     if (idx >= a.F) idx -= a.F;
     o.id[x] = o.ent[x] >= 0 ? __ldg(a.free_list + idx) : 0;
   }
-  o.nsurv = nh_t + nl_t;
+  o.nsurv = lo0 + nl_t;  // entries spanned
   o.nh_t = nh_t;
 }
 
@@ -361,7 +363,6 @@ __global__ void __launch_bounds__(kPackThreads, 1)
   const int64_t page_bytes = 216 * static_cast<int64_t>(P);
 
   if (warp >= kConsumerWarps) {
-    // ------------------------------------------------------------ producer
     int64_t it = 0;
     bool ok = true;
     const int32_t g = gridDim.x;
@@ -395,6 +396,9 @@ __global__ void __launch_bounds__(kPackThreads, 1)
       if (lane == 0) {
         st.info[0] = rows_cur.nsurv;
         st.info[1] = rows_cur.nh_t;
+        st.info[2] = (rows_cur.nh_t + 7) & ~7;
+        st.info[3] = (rows_cur.nsurv + 7) >> 3;
+        st.next_group = 0;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.full[s]);
@@ -409,8 +413,10 @@ __global__ void __launch_bounds__(kPackThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
+  // Warps claim 8-row groups of a stage from its shared counter, so a warp
+  // that is fast on one stage takes more groups or moves on; a stage is
+  // released once every warp has left it.
   const int grp = lane >> 2, l4 = lane & 3;
-  const int e = warp * kRowsPerConsumerWarp + grp;  // list row of this group
   int64_t it = 0;
   for (int32_t tau = blockIdx.x; tau < ntiles; tau += gridDim.x, ++it) {
     const int s = static_cast<int>(it % kStages);
@@ -419,11 +425,18 @@ __global__ void __launch_bounds__(kPackThreads, 1)
       set_error(&a.ws->err, DKV_E_TIMEOUT);
       return;
     }
-    const Stage &st = sm.st[s];
-    const int nsurv = st.info[0];
+    Stage &st = sm.st[s];
+    const int n_ent = st.info[0];
     const int nh_t = st.info[1];
-    if (warp * kRowsPerConsumerWarp < nsurv) {
-      const bool valid = e < nsurv;
+    const int lo0 = st.info[2];
+    const int ngroups = st.info[3];
+    for (;;) {
+      int g = 0;
+      if (lane == 0) g = atomicAdd(&st.next_group, 1);
+      g = __shfl_sync(0xffffffffu, g, 0);
+      if (g >= ngroups) break;
+      const int e = 8 * g + grp;
+      const bool valid = e < nh_t || (e >= lo0 && e < n_ent);  // entries [nh, lo0) are padding
       const int4 en = st.ent[valid ? e : 0];  // page id, slot, position, token in tile
       // channels 8c..8c+7 for the chunks c = l4 + 4j, j = 0..3
       const uint4 *kr = reinterpret_cast<const uint4 *>(st.k[en.w]);
@@ -432,7 +445,7 @@ __global__ void __launch_bounds__(kPackThreads, 1)
       const uint4 v0 = vr[l4], v1 = vr[l4 + 4], v2 = vr[l4 + 8], v3 = vr[l4 + 12];
       const uint32_t kmm = row_minmax(k0, k1, k2, k3);
       const uint32_t vmm = row_minmax(v0, v1, v2, v3);
-      const bool high = e < nh_t;
+      const bool high = 8 * g < nh_t;  // class-uniform group
       // scalar job: lane 0 of the group for K, lane 1 for V
       const int jt = l4 & 1;
       const uint32_t mine = jt ? vmm : kmm;
