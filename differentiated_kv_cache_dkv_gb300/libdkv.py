@@ -82,6 +82,7 @@ def load():
         "dkv_workspace_size": ([P(dkv_batch), P(ctypes.c_size_t)], i32),
         "dkv_init_pool": ([P(dkv_pool), vp], i32),
         "dkv_compact": ([P(dkv_batch), P(dkv_params), P(dkv_pool), P(dkv_tables), vp, ctypes.c_size_t, vp], i32),
+        "dkv_compact_noalloc": ([P(dkv_batch), P(dkv_params), P(dkv_pool), P(dkv_tables), vp], i32),
         "dkv_dequant_page": ([P(dkv_pool), i32, vp, vp, vp, vp], i32),
         "dkv_dequant_pages": ([P(dkv_pool), vp, i32, vp, vp, vp, vp], i32),
         "dkv_get_status": ([P(dkv_pool), vp], i32),
@@ -171,6 +172,17 @@ def dkv_compact(batch: dkv_batch, alpha_h: float, alpha_l: float, pool: DevicePo
                             _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != DKV_OK:
         raise DkvError(rc, "dkv_compact")
+
+
+def dkv_compact_noalloc(batch: dkv_batch, alpha_h: float, alpha_l: float, pool: DevicePool,
+                        tables: DeviceTables, stream=None, spin_limit: int = -1) -> None:
+    """dkv_compact with the library's built-in scratch instead of a workspace."""
+    params = dkv_params(float(alpha_h), float(alpha_l), int(spin_limit), 0, None)
+    pc, tc = pool.c(), tables.c()
+    rc = load().dkv_compact_noalloc(ctypes.byref(batch), ctypes.byref(params), ctypes.byref(pc), ctypes.byref(tc),
+                                    _stream(stream))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_compact_noalloc")
 
 
 def dkv_get_status(pool: DevicePool, stream=None) -> int:

@@ -154,6 +154,22 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
                     const dkv_tables *t, void *workspace, size_t workspace_bytes,
                     void *stream);
 
+/* dkv_compact without a caller workspace, for callers that cannot allocate
+ * device memory (no counterpart in the paper).  Same arguments, results and
+ * errors as dkv_compact; the scratch is a library-owned __device__ array of
+ * DKV_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
+ * process exit.  A batch whose dkv_workspace_size exceeds that limit is
+ * rejected with DKV_E_INVAL before anything is enqueued (the Llama-3-8B-shaped
+ * batch of 32 layers x 16 x 4096 tokens needs about 12.5 MiB).  The first call
+ * on a device resolves the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  The
+ * array is shared by all calls on a device and keeps the last call's contents
+ * (nothing in it needs to start at zero): calls that overlap on the GPU race,
+ * so order them on one stream.  Allocates nothing. */
+#define DKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+int32_t dkv_compact_noalloc(const dkv_batch *b, const dkv_params *p, const dkv_pool *pool,
+                            const dkv_tables *t, void *stream);
+
 /* Dequantise one page: k_out, v_out fp32 [2P][128], pos_out int32 [2P]
  * (device).  Slots the page class does not have, unused slots and free pages
  * decode to 0 with position -1.  page_id outside [0, F) is DKV_E_INVAL. */
