@@ -221,19 +221,21 @@ def _softmax_sig_layer(w: Workload, seed: int, layer: int, device, k_layer) -> t
 
 
 def make_inputs(w: Workload, seed: int | None = None, device="cpu", layers=None) -> dict:
-    """All inputs of the workload (or of the given layers) as torch tensors."""
+    """All inputs of the workload (or of the given layers) as torch tensors,
+    filled layer by layer into preallocated tensors."""
     seed = SEED_BASE if seed is None else seed
     layers = list(range(w.L)) if layers is None else list(layers)
-    ks, vs, sigs = [], [], []
-    for l in layers:
-        k = make_kv_layer(w, seed, l, 0, device)
-        v = make_kv_layer(w, seed, l, 1, device)
-        sigs.append(make_sig_layer(w, seed, l, device, k_layer=k))
-        ks.append(k)
-        vs.append(v)
+    n = len(layers)
+    k = torch.empty((n, w.T, w.Hkv, D), dtype=torch.bfloat16, device=device)
+    v = torch.empty((n, w.T, w.Hkv, D), dtype=torch.bfloat16, device=device)
+    sig = torch.empty((n, w.T, w.Hq), dtype=torch.float32, device=device)
+    for i, l in enumerate(layers):
+        k[i] = make_kv_layer(w, seed, l, 0, device)
+        v[i] = make_kv_layer(w, seed, l, 1, device)
+        sig[i] = make_sig_layer(w, seed, l, device, k_layer=k[i])
     return {
-        "L": len(layers), "R": w.R, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T,
-        "k": torch.stack(ks), "v": torch.stack(vs), "sig_sum": torch.stack(sigs),
+        "L": n, "R": w.R, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T,
+        "k": k, "v": v, "sig_sum": sig,
         "sig_cnt": sig_cnt_prefill(w, device),
         "lens": torch.tensor(w.lens, dtype=torch.int32, device=device),
     }
