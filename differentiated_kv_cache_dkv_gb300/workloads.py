@@ -250,3 +250,93 @@ def to_numpy(inp: dict) -> dict:
     out["sig_cnt"] = inp["sig_cnt"].detach().to("cpu").contiguous().numpy()
     out["lens"] = inp["lens"].detach().to("cpu").contiguous().numpy()
     return out
+
+
+# ------------------------------------------------------------- generation --
+
+ALPHA_MID = 0.5  # significance level the demotion updates move a token to (x alpha / N)
+
+
+def _i64(x: int) -> int:
+    """Two's-complement int64 value of x mod 2^64."""
+    x &= (1 << 64) - 1
+    return x - (1 << 64) if x >= (1 << 63) else x
+
+
+def _hash01(step: int, idx: torch.Tensor) -> torch.Tensor:
+    """Counter-based uniform [0, 1) from integer ids: the splitmix64 finaliser
+    (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
+    2014) of id * golden-gamma + step key, on int64 with wrap-around; the
+    same on any device."""
+    x = idx.to(torch.int64) * _i64(0x9E3779B97F4A7C15) + _i64((step + 1) * 0x632BE59BD9B4E019)
+    x = (x ^ ((x >> 30) & 0x3FFFFFFFF)) * _i64(0xBF58476D1CE4E5B9)
+    x = (x ^ ((x >> 27) & 0x1FFFFFFFFF)) * _i64(0x94D049BB133111EB)
+    x = x ^ ((x >> 31) & 0x1FFFFFFFF)
+    return ((x >> 11) & ((1 << 53) - 1)).to(torch.float64) / float(1 << 53)
+
+
+def decode_context(w: Workload, pre: dict, cap: int, device="cpu") -> dict:
+    """Decode-layout copies (capacity-strided context axis: position i of
+    request r at r * cap + i) of a prefill batch's significance sums and
+    counts; classes are filled in from the prefill result by the caller."""
+    lens = torch.tensor(w.lens, dtype=torch.int64, device=device)
+    req, pos = _positions(w, device)
+    dst = req * cap + pos
+    sig = torch.zeros((w.L, w.R * cap, w.Hq), dtype=torch.float32, device=device)
+    sig[:, dst] = pre["sig_sum"].to(device)
+    cnt = torch.zeros(w.R * cap, dtype=torch.int32, device=device)
+    cnt[dst] = pre["sig_cnt"].to(device)
+    return {"L": w.L, "R": w.R, "Hq": w.Hq, "Hkv": w.Hkv, "cap": cap, "sig_sum": sig, "sig_cnt": cnt,
+            "ctx_lens": lens.to(torch.int32), "dst": dst}
+
+
+def decode_update_inputs(w: Workload, ctx: dict, step: int, seed: int | None = None, device="cpu",
+                         p_prune: float = 0.005, p_demote: float = 0.005) -> dict:
+    """Advance the context by one generation step and draw the new tokens.
+
+    For every live position i < ctx_r of request r, layer l and KV head h a
+    counter hash u over (step, l, r, h, i) picks the update of the G query
+    heads of that KV head:
+    u < p_prune (0.5%): sig := 0 (the token stops being attended: it is
+              pruned);
+    u < p_prune + p_demote (1%): sig := (ALPHA_MID / N) * cnt with
+              N = ctx_r + 1 (demoted to the middle tier unless already there);
+    else:     sig += sig / cnt (its average stays as it was).
+    Every count then grows by one (the new query attends to every position).
+    The new token at position ctx_r gets count 1 and a log-normal(sigma)
+    self-attention weight with mean 1/N per query head; its K and V are drawn
+    like prefill rows.  fp32 division and multiplication as written, in place
+    on ctx."""
+    seed = SEED_BASE if seed is None else seed
+    L, R, Hq, Hkv, cap = w.L, w.R, w.Hq, w.Hkv, ctx["cap"]
+    G = Hq // Hkv
+    clen = ctx["ctx_lens"].to(torch.int64)
+    N = (clen + 1).to(torch.float32)
+    sig, cnt = ctx["sig_sum"], ctx["sig_cnt"]
+    pos_all = torch.arange(cap, device=device)
+    live = (pos_all[None, :] < clen[:, None]).reshape(-1)  # [R * cap]
+    tok = torch.nonzero(live).squeeze(1)
+    r_of = tok // cap
+    i_of = tok % cap
+    cntf = cnt[tok].to(torch.float32)[:, None, None]
+    mid = (torch.tensor(ALPHA_MID, dtype=torch.float32, device=device) / N[r_of])[:, None, None]
+    hh = torch.arange(Hkv, device=device)[None, :]
+    for l in range(L):
+        ids = ((l * R + r_of[:, None]) * Hkv + hh) * (cap + 1) + i_of[:, None]  # [n, Hkv]
+        u = _hash01(step, ids)[:, :, None]
+        s = sig[l, tok].view(-1, Hkv, G)
+        s = torch.where(u < p_prune, torch.zeros_like(s), torch.where(u < p_prune + p_demote, mid * cntf, s + s / cntf))
+        sig[l, tok] = s.view(-1, Hq)
+    cnt[tok] += 1
+    # the new token of every request
+    g = _gen(seed * 1000003 + 900000 + step, device)
+    newpos = torch.arange(R, device=device) * cap + clen
+    z = torch.randn((L, R, Hq), generator=g, device=device, dtype=torch.float64)
+    wt = torch.exp(w.sigma * z - w.sigma ** 2 / 2) / (clen + 1).to(torch.float64)[None, :, None]
+    sig[:, newpos] = wt.to(torch.float32)
+    cnt[newpos] = 1
+    kv = Workload(w.name, L=1, Hq=Hq, Hkv=Hkv, lens=[R], P=w.P, alpha_h=w.alpha_h, alpha_l=w.alpha_l,
+                  n_outlier=w.n_outlier, outlier_scale=w.outlier_scale)
+    k_new = torch.stack([make_kv_layer(kv, seed + 77 * step + 1, l, 0, device) for l in range(L)])
+    v_new = torch.stack([make_kv_layer(kv, seed + 77 * step + 1, l, 1, device) for l in range(L)])
+    return {"k_new": k_new, "v_new": v_new, "new_lens": torch.ones(R, dtype=torch.int32, device=device)}

@@ -23,6 +23,7 @@ E_INVAL = -1
 E_NOMEM = -2
 E_RANGE = -3
 E_LENS = -7
+E_INTERNAL = -5
 
 _lib = None
 
@@ -51,6 +52,16 @@ class _Tables(ctypes.Structure):
     ]
 
 
+class _DecodeBatch(ctypes.Structure):
+    _fields_ = [
+        ("L", ctypes.c_int32), ("R", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+        ("D", ctypes.c_int32), ("cap", ctypes.c_int32), ("unit_base", ctypes.c_int64),
+        ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("sig_sum", ctypes.c_void_p),
+        ("sig_cnt", ctypes.c_void_p), ("ctx_lens", ctypes.c_void_p), ("new_lens", ctypes.c_void_p),
+        ("classes", ctypes.c_void_p),
+    ]
+
+
 def lib():
     """Load (building first if needed) the oracle shared library."""
     global _lib
@@ -73,6 +84,9 @@ def lib():
                                      ctypes.POINTER(_Pool), ctypes.POINTER(_Tables),
                                      ctypes.c_void_p]
         L.oracle_compact.restype = ctypes.c_int32
+        L.oracle_decode_step.argtypes = [ctypes.POINTER(_DecodeBatch), ctypes.c_float, ctypes.c_float,
+                                         ctypes.POINTER(_Pool), ctypes.POINTER(_Tables)]
+        L.oracle_decode_step.restype = ctypes.c_int32
         L.oracle_dequant_page.argtypes = [ctypes.POINTER(_Pool), ctypes.c_int32, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_void_p]
         L.oracle_dequant_page.restype = None
@@ -165,6 +179,28 @@ def compact(inp: dict, alpha_h: float, alpha_l: float, pool: Pool, tables: Table
     mask = None if quant_mask is None else np.ascontiguousarray(quant_mask, dtype=np.uint8)
     return int(lib().oracle_compact(ctypes.byref(b), float(alpha_h), float(alpha_l),
                                      ctypes.byref(p), ctypes.byref(t), _ptr(mask)))
+
+
+def decode_step(dinp: dict, alpha_h: float, alpha_l: float, pool: Pool, tables: Tables) -> int:
+    """One generation step on the oracle's pool and tables (in place).
+
+    ``dinp`` holds numpy arrays: k_new, v_new (uint16 bf16 bits [L][R][Hkv][128]),
+    sig_sum (float32 [L][R*cap][Hq]), sig_cnt (int32 [R*cap]), ctx_lens, new_lens
+    (int32 [R]), classes (uint8 [L][R*cap][Hkv], updated in place), and the ints
+    L, R, Hq, Hkv, cap (and optionally unit_base).
+    """
+    arrs = {k: np.ascontiguousarray(dinp[k]) for k in ("k_new", "v_new", "sig_sum", "sig_cnt", "ctx_lens",
+                                                        "new_lens")}
+    cls = dinp["classes"]
+    assert cls.flags["C_CONTIGUOUS"] and cls.dtype == np.uint8
+    b = _DecodeBatch(int(dinp["L"]), int(dinp["R"]), int(dinp["Hq"]), int(dinp["Hkv"]), 128, int(dinp["cap"]),
+                     int(dinp.get("unit_base", 0)), _ptr(arrs["k_new"]), _ptr(arrs["v_new"]),
+                     _ptr(arrs["sig_sum"]), _ptr(arrs["sig_cnt"]), _ptr(arrs["ctx_lens"]), _ptr(arrs["new_lens"]),
+                     _ptr(cls))
+    p = pool._c()
+    t = tables._c()
+    return int(lib().oracle_decode_step(ctypes.byref(b), float(alpha_h), float(alpha_l), ctypes.byref(p),
+                                        ctypes.byref(t)))
 
 
 def dequant_page(pool: Pool, page_id: int):

@@ -42,12 +42,33 @@
  *      slots starting at head + offset (mod F); its K8V4 pages come first.
  *      head advances by the total; a total above tail - head is an
  *      out-of-memory error and the call changes nothing.
+ *  D   Generation step (the review's Algorithm 1 classifies tokens as they
+ *      age; here every live token is re-scored each step and, per the
+ *      review, demotion and pruning are irreversible): with N = ctx + new,
+ *      an old token's class becomes min(old class, classify(score, N)); the
+ *      new token is classified.  Per unit, each list (K8V4 slots, K4V2
+ *      slots) drops its removed tokens and is hole-filled: the survivors at
+ *      slots >= n' move, in ascending slot order, into the holes below n' in
+ *      ascending order (bytes copied unchanged).  Tokens demoted K8V4 -> K4V2
+ *      are appended to the K4V2 list in ascending position order,
+ *      requantised (Q1 with b = 4 for K, 2 for V) from their dequantised
+ *      fp32 values x = fma(q, s, z) (no range error: those values come from
+ *      finite fp16 scale and zero).  The new token is appended to its list.
+ *      Each list keeps its first min(have, need) pages, need = ceil(n / cap);
+ *      new pages come from the free list by the prefix sum of A1 (the unit's
+ *      new K8V4 pages first); surplus pages are freed after all allocation,
+ *      appended at the tail in (unit, list, page index) order.  Unused slots
+ *      of the lists' pages are cleared (zero codes and metadata, position
+ *      -1).  A step with new = 0 and no class change leaves everything as it
+ *      was.
  */
 #include "dkv_oracle.h"
 
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
+#include <utility>
 #include <vector>
 
 namespace {
@@ -213,6 +234,39 @@ int32_t oracle_quant_row(const uint16_t *x, int32_t bits, uint8_t *q, uint16_t *
   return ORACLE_OK;
 }
 
+/* Reading Q1 on fp32 inputs (used to requantise demoted tokens). */
+static void quant_row_f32(const float *xf, int32_t bits, uint8_t *q, uint16_t *s16_out, uint16_t *z16_out) {
+  float mn = xf[0], mx = xf[0];
+  for (int d = 1; d < 128; ++d) {
+    if (xf[d] < mn) mn = xf[d];
+    if (xf[d] > mx) mx = xf[d];
+  }
+  mn = mn + 0.0f;
+  mx = mx + 0.0f;
+  const int n = (1 << bits) - 1;
+  const float span = mx - mn;
+  const float s32 = span / static_cast<float>(n);
+  uint16_t s16 = oracle_fp16_rn(s32);
+  if (mx > mn && s16 == 0) s16 = 0x0001;
+  const uint16_t z16 = oracle_fp16_rn(mn);
+  const float s = oracle_fp16_to_f32(s16);
+  const float z = oracle_fp16_to_f32(z16);
+  for (int d = 0; d < 128; ++d) {
+    if (s == 0.0f) {
+      q[d] = 0;
+      continue;
+    }
+    const float diff = xf[d] - z;
+    const float t = diff / s;
+    float r = std::nearbyint(t);
+    if (r < 0.0f) r = 0.0f;
+    if (r > static_cast<float>(n)) r = static_cast<float>(n);
+    q[d] = static_cast<uint8_t>(r);
+  }
+  *s16_out = s16;
+  *z16_out = z16;
+}
+
 void oracle_init_pool(oracle_pool *pool) {
   for (int64_t i = 0; i < pool->F; ++i) {
     pool->free_list[i] = static_cast<int32_t>(i);
@@ -372,6 +426,292 @@ int32_t oracle_compact(const oracle_batch *b, float alpha_h, float alpha_l, orac
         }
       }
   pool->cursors[0] = head + static_cast<uint64_t>(total);
+  return ORACLE_OK;
+}
+
+
+namespace {
+
+/* One list of a unit: slot s lives in page pages[s / cap], slot s % cap. */
+struct ListRef {
+  bool high;
+  int64_t cap;
+  const int32_t *pages;
+};
+
+uint8_t *slot_k(uint8_t *pool_pages, const PageLayout &lay, const ListRef &lr, int64_t s) {
+  return pool_pages + static_cast<int64_t>(lr.pages[s / lr.cap]) * lay.bytes() + lay.k_off(lr.high, s % lr.cap);
+}
+
+void copy_slot(uint8_t *pp, const PageLayout &lay, const ListRef &lr, int64_t from, int64_t to) {
+  const int64_t kb = lr.high ? 128 : 64, vb = lr.high ? 64 : 32;
+  uint8_t *fp = pp + static_cast<int64_t>(lr.pages[from / lr.cap]) * lay.bytes();
+  uint8_t *tp = pp + static_cast<int64_t>(lr.pages[to / lr.cap]) * lay.bytes();
+  const int64_t fs = from % lr.cap, ts = to % lr.cap;
+  std::memcpy(tp + lay.k_off(lr.high, ts), fp + lay.k_off(lr.high, fs), static_cast<size_t>(kb));
+  std::memcpy(tp + lay.v_off(lr.high, ts), fp + lay.v_off(lr.high, fs), static_cast<size_t>(vb));
+  std::memcpy(tp + lay.meta_off(ts), fp + lay.meta_off(fs), 8);
+  std::memcpy(tp + lay.pos_off(ts), fp + lay.pos_off(fs), 4);
+}
+
+void clear_slot(uint8_t *pp, const PageLayout &lay, const ListRef &lr, int64_t s) {
+  const int64_t kb = lr.high ? 128 : 64, vb = lr.high ? 64 : 32;
+  uint8_t *pg = pp + static_cast<int64_t>(lr.pages[s / lr.cap]) * lay.bytes();
+  const int64_t ss = s % lr.cap;
+  std::memset(pg + lay.k_off(lr.high, ss), 0, static_cast<size_t>(kb));
+  std::memset(pg + lay.v_off(lr.high, ss), 0, static_cast<size_t>(vb));
+  std::memset(pg + lay.meta_off(ss), 0, 8);
+  put_i32(pg + lay.pos_off(ss), -1);
+}
+
+void write_slot(uint8_t *pp, const PageLayout &lay, const ListRef &lr, int64_t s, const uint8_t *qk, const uint8_t *qv,
+                uint16_t ks, uint16_t kz, uint16_t vs, uint16_t vz, int32_t pos) {
+  uint8_t *pg = pp + static_cast<int64_t>(lr.pages[s / lr.cap]) * lay.bytes();
+  const int64_t ss = s % lr.cap;
+  pack_codes(qk, lr.high ? 8 : 4, pg + lay.k_off(lr.high, ss));
+  pack_codes(qv, lr.high ? 4 : 2, pg + lay.v_off(lr.high, ss));
+  put_u16(pg + lay.meta_off(ss) + 0, ks);
+  put_u16(pg + lay.meta_off(ss) + 2, kz);
+  put_u16(pg + lay.meta_off(ss) + 4, vs);
+  put_u16(pg + lay.meta_off(ss) + 6, vz);
+  put_i32(pg + lay.pos_off(ss), pos);
+}
+
+/* Hole-fill of one list: survivors at slots >= n_keep move, in ascending
+ * order, into the holes below n_keep, in ascending order. */
+void hole_fill(uint8_t *pp, const PageLayout &lay, const ListRef &lr, const std::vector<uint8_t> &keep, int64_t n_keep) {
+  std::vector<int64_t> holes, movers;
+  for (int64_t s = 0; s < static_cast<int64_t>(keep.size()); ++s) {
+    if (s < n_keep && !keep[s]) holes.push_back(s);
+    if (s >= n_keep && keep[s]) movers.push_back(s);
+  }
+  for (size_t k = 0; k < holes.size(); ++k) copy_slot(pp, lay, lr, movers[k], holes[k]);
+}
+
+}  // namespace
+
+extern "C" int32_t oracle_decode_step(const oracle_decode_batch *b, float alpha_h, float alpha_l, oracle_pool *pool,
+                                      oracle_tables *t) {
+  if (b->D != 128 || b->L < 1 || b->R < 1 || b->Hkv < 1 || b->Hq < b->Hkv || b->Hq % b->Hkv != 0 || b->cap < 1)
+    return ORACLE_E_INVAL;
+  if (!(alpha_l >= 0.0f) || !(alpha_h >= alpha_l) || !std::isfinite(alpha_h)) return ORACLE_E_INVAL;
+  if (pool->P < 2 || pool->P % 2 != 0 || pool->F < 1 || t->pmax < 1) return ORACLE_E_INVAL;
+  const int64_t L = b->L, R = b->R, Hq = b->Hq, Hkv = b->Hkv, cap = b->cap, P = pool->P, F = pool->F;
+  const int64_t G = Hq / Hkv, U = L * R * Hkv, pmax = t->pmax;
+  for (int64_t r = 0; r < R; ++r) {
+    const int64_t c = b->ctx_lens[r], n = b->new_lens[r];
+    if (c < 0 || n < 0 || n > 1 || c + n > cap || c + n > (pmax - 1) * P) return ORACLE_E_LENS;
+  }
+  const PageLayout lay{P};
+  auto row_of = [&](int64_t l, int64_t r, int64_t i, int64_t h) { return ((l * R + r) * cap + i) * Hkv + h; };
+
+  /* classes after the step (readings S1-S3, D) */
+  std::vector<uint8_t> ncls(b->classes, b->classes + L * R * cap * Hkv);
+  for (int64_t l = 0; l < L; ++l)
+    for (int64_t r = 0; r < R; ++r) {
+      const int64_t N = b->ctx_lens[r] + b->new_lens[r];
+      if (N == 0) continue;
+      const float thr_h = alpha_h / static_cast<float>(N);
+      const float thr_l = alpha_l / static_cast<float>(N);
+      for (int64_t i = 0; i < N; ++i) {
+        const int64_t tok = r * cap + i;
+        const int32_t cnt = b->sig_cnt[tok];
+        for (int64_t h = 0; h < Hkv; ++h) {
+          uint8_t cls;
+          if (cnt == 0) {
+            cls = 2;
+          } else {
+            float s = NAN;
+            for (int64_t g = 0; g < G; ++g)
+              s = std::fmax(s, b->sig_sum[(l * R * cap + tok) * Hq + h * G + g] / static_cast<float>(cnt));
+            cls = (s >= thr_h) ? 2 : (s >= thr_l) ? 1 : 0;
+          }
+          const int64_t row = row_of(l, r, i, h);
+          if (i < b->ctx_lens[r] && b->classes[row] < cls) cls = b->classes[row];
+          ncls[row] = cls;
+        }
+      }
+    }
+
+  /* per-unit plan */
+  struct Plan {
+    int64_t keep_hi, keep_lo, dem, n_hi, n_lo, have_hi, have_lo, need_hi, need_lo, d, f;
+    int new_cls;
+  };
+  std::vector<Plan> plan(U);
+  std::vector<int64_t> off_d(U), off_f(U);
+  int64_t dsum = 0, fsum = 0;
+  for (int64_t l = 0; l < L; ++l)
+    for (int64_t r = 0; r < R; ++r)
+      for (int64_t h = 0; h < Hkv; ++h) {
+        const int64_t u = (l * R + r) * Hkv + h;
+        const int32_t *hdr = t->unit_hdr + u * 4;
+        const int32_t *fw = t->fwd + u * pmax;
+        Plan pl{};
+        const int64_t n_hi = hdr[0], n_lo = hdr[1];
+        pl.have_hi = hdr[2];
+        pl.have_lo = hdr[3];
+        if (pl.have_hi + pl.have_lo > pmax) return ORACLE_E_INVAL;
+        for (int64_t k = 0; k < pl.have_hi + pl.have_lo; ++k)
+          if (fw[k] < 0 || fw[k] >= F) return ORACLE_E_INVAL;
+        for (int64_t s = 0; s < n_hi; ++s) {
+          const uint8_t *pg = pool->pages + static_cast<int64_t>(fw[s / P]) * lay.bytes();
+          const int32_t pos = get_i32(pg + lay.pos_off(s % P));
+          if (pos < 0 || pos >= b->ctx_lens[r]) return ORACLE_E_INVAL;
+          const uint8_t c = ncls[row_of(l, r, pos, h)];
+          if (c == 2) ++pl.keep_hi;
+          if (c == 1) ++pl.dem;
+        }
+        for (int64_t s = 0; s < n_lo; ++s) {
+          const uint8_t *pg = pool->pages + static_cast<int64_t>(fw[pl.have_hi + s / (2 * P)]) * lay.bytes();
+          const int32_t pos = get_i32(pg + lay.pos_off(s % (2 * P)));
+          if (pos < 0 || pos >= b->ctx_lens[r]) return ORACLE_E_INVAL;
+          const uint8_t c = ncls[row_of(l, r, pos, h)];
+          if (c == 2) return ORACLE_E_INVAL;  /* a K4V2 token cannot climb back */
+          if (c == 1) ++pl.keep_lo;
+        }
+        pl.new_cls = b->new_lens[r] ? ncls[row_of(l, r, b->ctx_lens[r], h)] : 0;
+        if (pl.new_cls != 0) {
+          const int64_t nr = (l * R + r) * Hkv + h;
+          for (int d = 0; d < 128; ++d) {
+            const float kx = bf16_value(b->k_new[nr * 128 + d]);
+            const float vx = bf16_value(b->v_new[nr * 128 + d]);
+            if (!std::isfinite(kx) || std::fabs(kx) > 65504.0f) return ORACLE_E_RANGE;
+            if (!std::isfinite(vx) || std::fabs(vx) > 65504.0f) return ORACLE_E_RANGE;
+          }
+        }
+        pl.n_hi = pl.keep_hi + (pl.new_cls == 2);
+        pl.n_lo = pl.keep_lo + pl.dem + (pl.new_cls == 1);
+        pl.need_hi = ceil_div(pl.n_hi, P);
+        pl.need_lo = ceil_div(pl.n_lo, 2 * P);
+        if (pl.need_hi + pl.need_lo > pmax) return ORACLE_E_LENS;
+        pl.d = std::max<int64_t>(0, pl.need_hi - pl.have_hi) + std::max<int64_t>(0, pl.need_lo - pl.have_lo);
+        pl.f = std::max<int64_t>(0, pl.have_hi - pl.need_hi) + std::max<int64_t>(0, pl.have_lo - pl.need_lo);
+        off_d[u] = dsum;
+        off_f[u] = fsum;
+        dsum += pl.d;
+        fsum += pl.f;
+        plan[u] = pl;
+      }
+  const uint64_t head = pool->cursors[0], tail = pool->cursors[1];
+  if (static_cast<uint64_t>(dsum) > tail - head) return ORACLE_E_NOMEM;
+
+  /* apply, unit by unit */
+  std::vector<int32_t> freed;
+  for (int64_t l = 0; l < L; ++l)
+    for (int64_t r = 0; r < R; ++r)
+      for (int64_t h = 0; h < Hkv; ++h) {
+        const int64_t u = (l * R + r) * Hkv + h;
+        const Plan &pl = plan[u];
+        int32_t *hdr = t->unit_hdr + u * 4;
+        int32_t *fw = t->fwd + u * pmax;
+        const int64_t n_hi = hdr[0], n_lo = hdr[1];
+        std::vector<int32_t> old_hi(fw, fw + pl.have_hi), old_lo(fw + pl.have_hi, fw + pl.have_hi + pl.have_lo);
+        std::vector<int32_t> new_ids;
+        for (int64_t k = 0; k < pl.d; ++k)
+          new_ids.push_back(pool->free_list[(head + static_cast<uint64_t>(off_d[u] + k)) % static_cast<uint64_t>(F)]);
+        std::vector<int32_t> hi_pages(old_hi), lo_pages(old_lo);
+        size_t nx = 0;
+        std::vector<int32_t> created;
+        while (static_cast<int64_t>(hi_pages.size()) < pl.need_hi) {
+          hi_pages.push_back(new_ids[nx]);
+          created.push_back(new_ids[nx++]);
+        }
+        while (static_cast<int64_t>(lo_pages.size()) < pl.need_lo) {
+          lo_pages.push_back(new_ids[nx]);
+          created.push_back(new_ids[nx++]);
+        }
+        for (int32_t id : created) clear_page(pool->pages + static_cast<int64_t>(id) * lay.bytes(), lay);
+        const ListRef HI{true, P, hi_pages.data()}, LO{false, 2 * P, lo_pages.data()};
+        /* keep flags and demoted slots */
+        std::vector<uint8_t> keep_hi(n_hi), keep_lo(n_lo);
+        std::vector<std::pair<int32_t, int64_t>> dem_by_pos;  /* (position, K8V4 slot) */
+        for (int64_t s = 0; s < n_hi; ++s) {
+          const int32_t pos = get_i32(pool->pages + static_cast<int64_t>(HI.pages[s / P]) * lay.bytes() + lay.pos_off(s % P));
+          const uint8_t c = ncls[row_of(l, r, pos, h)];
+          keep_hi[s] = c == 2;
+          if (c == 1) dem_by_pos.emplace_back(pos, s);
+        }
+        std::sort(dem_by_pos.begin(), dem_by_pos.end());
+        std::vector<int64_t> demoted;
+        for (const auto &e : dem_by_pos) demoted.push_back(e.second);
+        for (int64_t s = 0; s < n_lo; ++s) {
+          const int32_t pos =
+              get_i32(pool->pages + static_cast<int64_t>(LO.pages[s / (2 * P)]) * lay.bytes() + lay.pos_off(s % (2 * P)));
+          keep_lo[s] = ncls[row_of(l, r, pos, h)] == 1;
+        }
+        /* K4V2 list first (its appends need the holes filled), then the
+         * demoted tokens, then the K8V4 list (after its demoted slots were
+         * read), then the new token */
+        hole_fill(pool->pages, lay, LO, keep_lo, pl.keep_lo);
+        for (size_t k = 0; k < demoted.size(); ++k) {
+          const int64_t s = demoted[k];
+          const uint8_t *pg = pool->pages + static_cast<int64_t>(HI.pages[s / P]) * lay.bytes();
+          const int64_t ss = s % P;
+          uint8_t qk[128], qv[128];
+          unpack_codes(pg + lay.k_off(true, ss), 8, qk);
+          unpack_codes(pg + lay.v_off(true, ss), 4, qv);
+          const uint8_t *meta = pg + lay.meta_off(ss);
+          const float ks = oracle_fp16_to_f32(get_u16(meta + 0)), kz = oracle_fp16_to_f32(get_u16(meta + 2));
+          const float vs = oracle_fp16_to_f32(get_u16(meta + 4)), vz = oracle_fp16_to_f32(get_u16(meta + 6));
+          float xk[128], xv[128];
+          for (int d = 0; d < 128; ++d) {
+            xk[d] = std::fma(static_cast<float>(qk[d]), ks, kz);
+            xv[d] = std::fma(static_cast<float>(qv[d]), vs, vz);
+          }
+          uint8_t nk[128], nv[128];
+          uint16_t s1, z1, s2, z2;
+          quant_row_f32(xk, 4, nk, &s1, &z1);
+          quant_row_f32(xv, 2, nv, &s2, &z2);
+          write_slot(pool->pages, lay, LO, pl.keep_lo + static_cast<int64_t>(k), nk, nv, s1, z1, s2, z2,
+                     get_i32(pg + lay.pos_off(ss)));
+        }
+        hole_fill(pool->pages, lay, HI, keep_hi, pl.keep_hi);
+        if (pl.new_cls != 0) {
+          const int64_t nr = (l * R + r) * Hkv + h;
+          const bool high = pl.new_cls == 2;
+          uint8_t qk[128], qv[128];
+          uint16_t ks, kz, vs, vz;
+          oracle_quant_row(b->k_new + nr * 128, high ? 8 : 4, qk, &ks, &kz);
+          oracle_quant_row(b->v_new + nr * 128, high ? 4 : 2, qv, &vs, &vz);
+          const int64_t slot = high ? pl.keep_hi : pl.keep_lo + pl.dem;
+          write_slot(pool->pages, lay, high ? HI : LO, slot, qk, qv, ks, kz, vs, vz,
+                     static_cast<int32_t>(b->ctx_lens[r]));
+        }
+        for (int64_t s = pl.n_hi; s < pl.need_hi * P; ++s) clear_slot(pool->pages, lay, HI, s);
+        for (int64_t s = pl.n_lo; s < pl.need_lo * 2 * P; ++s) clear_slot(pool->pages, lay, LO, s);
+        /* freed pages of this unit, in (list, page index) order */
+        for (int64_t k = pl.need_hi; k < pl.have_hi; ++k) freed.push_back(old_hi[k]);
+        for (int64_t k = pl.need_lo; k < pl.have_lo; ++k) freed.push_back(old_lo[k]);
+        /* tables */
+        for (int64_t k = 0; k < pmax; ++k) {
+          int32_t id = -1;
+          if (k < pl.need_hi) id = hi_pages[k];
+          else if (k < pl.need_hi + pl.need_lo) id = lo_pages[k - pl.need_hi];
+          fw[k] = id;
+          if (id >= 0) {
+            pool->rev_unit[id] = static_cast<int32_t>(b->unit_base + u);
+            pool->rev_idx[id] = static_cast<int32_t>(k);
+            pool->page_cls[id] = k < pl.need_hi ? 2 : 1;
+          }
+        }
+        hdr[0] = static_cast<int32_t>(pl.n_hi);
+        hdr[1] = static_cast<int32_t>(pl.n_lo);
+        hdr[2] = static_cast<int32_t>(pl.need_hi);
+        hdr[3] = static_cast<int32_t>(pl.need_lo);
+      }
+  /* frees after all allocation */
+  uint64_t tl = tail;
+  for (int32_t id : freed) {
+    pool->free_list[tl % static_cast<uint64_t>(F)] = id;
+    ++tl;
+    pool->rev_unit[id] = -1;
+    pool->rev_idx[id] = -1;
+    pool->page_cls[id] = 0;
+  }
+  pool->cursors[0] = head + static_cast<uint64_t>(dsum);
+  pool->cursors[1] = tl;
+  std::memcpy(b->classes, ncls.data(), ncls.size());
   return ORACLE_OK;
 }
 

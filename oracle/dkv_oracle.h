@@ -95,6 +95,27 @@ int32_t oracle_compact(const oracle_batch *b, float alpha_h, float alpha_l,
                        oracle_pool *pool, oracle_tables *t,
                        const uint8_t *quant_mask);
 
+/* One generation step on the pages a prefill (and earlier steps) left.
+ * The context axis is capacity-strided: position i of request r is token
+ * r * cap + i of sig_sum / sig_cnt / classes. */
+typedef struct oracle_decode_batch {
+  int32_t L, R, Hq, Hkv, D;
+  int32_t cap;             /* positions reserved per request */
+  int64_t unit_base;
+  const uint16_t *k_new;   /* bf16 [L][R][Hkv][D]: the new token of each request */
+  const uint16_t *v_new;
+  const float *sig_sum;    /* [L][R * cap][Hq] */
+  const int32_t *sig_cnt;  /* [R * cap] */
+  const int32_t *ctx_lens; /* [R] tokens before this step */
+  const int32_t *new_lens; /* [R] 0 or 1 */
+  uint8_t *classes;        /* in/out [L][R * cap][Hkv] */
+} oracle_decode_batch;
+
+/* Decode step (reading D in dkv_oracle.cpp).  t->fwd and t->unit_hdr are the
+ * unit tables the previous call left (in/out); t->classes is unused. */
+int32_t oracle_decode_step(const oracle_decode_batch *b, float alpha_h, float alpha_l,
+                           oracle_pool *pool, oracle_tables *t);
+
 /* Decode a page into fp32 K, V ([2P][128] each) and positions ([2P]). */
 void oracle_dequant_page(const oracle_pool *pool, int32_t page_id,
                          float *k_out, float *v_out, int32_t *pos_out);

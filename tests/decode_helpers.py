@@ -1,0 +1,149 @@
+"""Test-side helpers for the generation (decode) step: prefill-then-decode
+state on the host for the oracle, unit list parsing from raw page bytes, and
+the state invariants every step must keep.  No quantisation happens here."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from differentiated_kv_cache_dkv_gb300 import workloads as W
+from tests.oracle_helpers import unpack
+
+
+def decode_pmax(cap: int, P: int) -> int:
+    return -(-cap // P) + 1
+
+
+class HostDecode:
+    """Oracle-side decode state of a workload: pool, unit tables and the
+    capacity-strided context (sig, counts, classes) after an oracle prefill."""
+
+    def __init__(self, w: W.Workload, cap: int, F: int | None = None, seed: int | None = None, inp=None):
+        self.w, self.cap = w, cap
+        self.pmax = decode_pmax(cap, w.P)
+        inp = W.make_inputs(w, seed) if inp is None else inp
+        self.pool = oracle.Pool(F or w.pool_pages, w.P)
+        tab = oracle.Tables(w.U, self.pmax, w.rows)
+        st = oracle.compact(W.to_numpy(inp), w.alpha_h, w.alpha_l, self.pool, tab)
+        assert st == oracle.OK, st
+        self.tab = tab
+        self.ctx = W.decode_context(w, inp, cap)
+        dst = self.ctx["dst"].numpy()
+        self.classes = np.zeros((w.L, w.R * cap, w.Hkv), dtype=np.uint8)
+        self.classes[:, dst] = tab.classes.reshape(w.L, w.T, w.Hkv)
+        self.step_no = 0
+
+    @property
+    def ctx_lens(self) -> np.ndarray:
+        return self.ctx["ctx_lens"].numpy()
+
+    def dinp(self, upd: dict) -> dict:
+        w = self.w
+        return {"L": w.L, "R": w.R, "Hq": w.Hq, "Hkv": w.Hkv, "cap": self.cap,
+                "k_new": upd["k_new"].contiguous().view(torch.int16).numpy().view(np.uint16),
+                "v_new": upd["v_new"].contiguous().view(torch.int16).numpy().view(np.uint16),
+                "sig_sum": self.ctx["sig_sum"].numpy(), "sig_cnt": self.ctx["sig_cnt"].numpy(),
+                "ctx_lens": self.ctx["ctx_lens"].numpy(),
+                "new_lens": upd["new_lens"].numpy().astype(np.int32), "classes": self.classes}
+
+    def step(self, upd: dict | None = None, **kw) -> int:
+        """Draw this step's update (unless given) and run the oracle step."""
+        if upd is None:
+            upd = W.decode_update_inputs(self.w, self.ctx, self.step_no, **kw)
+        st = oracle.decode_step(self.dinp(upd), self.w.alpha_h, self.w.alpha_l, self.pool, self.tab)
+        if st == oracle.OK:
+            self.ctx["ctx_lens"] += upd["new_lens"]
+            self.step_no += 1
+        return st
+
+    def snapshot(self) -> dict:
+        p = self.pool
+        return {"free_list": p.free_list.copy(), "cursors": p.cursors.copy(), "rev_unit": p.rev_unit.copy(),
+                "rev_idx": p.rev_idx.copy(), "page_cls": p.page_cls.copy(), "pages": p.pages.copy(),
+                "fwd": self.tab.fwd.copy(), "unit_hdr": self.tab.unit_hdr.copy(), "classes": self.classes.copy()}
+
+
+def list_slots(pages: np.ndarray, fwd_row: np.ndarray, hdr, P: int):
+    """Raw bytes of a unit's two lists: for list 0 (K8V4) and 1 (K4V2), a
+    list of (K bytes, V bytes, metadata bytes, position) per slot, over every
+    slot of the list's pages (used slots first)."""
+    n_hi, n_lo, p_hi, p_lo = (int(x) for x in hdr)
+    out = []
+    for high, ids, per in ((True, fwd_row[:p_hi], P), (False, fwd_row[p_hi:p_hi + p_lo], 2 * P)):
+        kb, vb = (128, 64) if high else (64, 32)
+        slots = []
+        for pid in ids:
+            pg = pages[int(pid)]
+            for s in range(per):
+                k = pg[s * kb:(s + 1) * kb]
+                v = pg[128 * P + s * vb:128 * P + (s + 1) * vb]
+                meta = pg[192 * P + 8 * s:192 * P + 8 * s + 8]
+                pos = int(pg[208 * P + 4 * s:208 * P + 4 * s + 4].view(np.int32)[0])
+                slots.append((bytes(k), bytes(v), bytes(meta), pos))
+        out.append(slots)
+    return out
+
+
+def check_state(w: W.Workload, cap: int, pool, fwd: np.ndarray, unit_hdr: np.ndarray, classes: np.ndarray,
+                ctx_lens: np.ndarray, unit_base: int = 0, layers=None, check_ring: bool = True):
+    """Invariants of a decode state (raises AssertionError):
+    - every unit's header counts equal its K8V4 / K4V2 tokens in `classes`, its
+      page counts are ceil(n / capacity), its forward row lists those pages
+      then -1, and rev_unit / rev_idx / page_cls point back at it;
+    - the used slots of each list hold exactly the positions of that class,
+      each once, and every unused slot is clear (zero codes and metadata,
+      position -1), slots P..2P-1 of K8V4 pages included;
+    - the free ring [head, tail) and the owned pages partition the pool.
+    Returns {(unit, position): (list, slot bytes)} for the checked layers."""
+    P, F = pool.P, pool.F
+    Ul = w.R * w.Hkv
+    layers = range(w.L) if layers is None else layers
+    owned = []
+    where = {}
+    for l in layers:
+        for r in range(w.R):
+            c = int(ctx_lens[r])
+            for h in range(w.Hkv):
+                u = l * Ul + r * w.Hkv + h
+                n_hi, n_lo, p_hi, p_lo = (int(x) for x in unit_hdr[u])
+                col = classes[l, r * cap:r * cap + c, h]
+                assert n_hi == int((col == 2).sum()) and n_lo == int((col == 1).sum()), (u, n_hi, n_lo)
+                assert p_hi == -(-n_hi // P) and p_lo == -(-n_lo // (2 * P)), u
+                row = fwd[u]
+                ids = row[:p_hi + p_lo]
+                assert np.all(ids >= 0) and np.all(row[p_hi + p_lo:] == -1), u
+                for k, pid in enumerate(ids):
+                    assert pool.rev_unit[pid] == unit_base + u and pool.rev_idx[pid] == k, (u, k, pid)
+                    assert pool.page_cls[pid] == (2 if k < p_hi else 1), (u, k)
+                    if k < p_hi:
+                        pg = pool.pages[pid]
+                        assert not pg[192 * P + 8 * P:208 * P].any()
+                        assert np.all(pg[208 * P + 4 * P:216 * P].view(np.int32) == -1)
+                owned.extend(int(x) for x in ids)
+                lists = list_slots(pool.pages, row, unit_hdr[u], P)
+                for li, (n, cls) in enumerate(((n_hi, 2), (n_lo, 1))):
+                    slots = lists[li]
+                    got = [s[3] for s in slots[:n]]
+                    want = np.nonzero(col == cls)[0]
+                    assert sorted(got) == list(want), (u, li)
+                    for s in slots[n:]:
+                        assert s[3] == -1 and not any(s[0]) and not any(s[1]) and not any(s[2]), (u, li)
+                    for si, s in enumerate(slots[:n]):
+                        where[(u, s[3])] = (li, s[:3], si)
+    if check_ring:
+        head, tail = int(pool.cursors[0]), int(pool.cursors[1])
+        assert 0 <= tail - head <= F
+        ring = [int(pool.free_list[x % F]) for x in range(head, tail)]
+        assert all(pool.page_cls[p] == 0 and pool.rev_unit[p] == -1 for p in ring)
+        if len(list(layers)) == w.L:
+            assert sorted(ring + owned) == list(range(F))
+    return where
+
+
+def slot_codes(slot_bytes, high: bool):
+    """Unpacked (K codes, V codes, fp16 metadata) of a slot's raw bytes."""
+    k, v, meta = slot_bytes
+    kb, vb = (8, 4) if high else (4, 2)
+    return (unpack(np.frombuffer(k, np.uint8), kb), unpack(np.frombuffer(v, np.uint8), vb),
+            np.frombuffer(meta, np.uint16))
