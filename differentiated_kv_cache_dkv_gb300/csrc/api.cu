@@ -74,6 +74,54 @@ bool valid_shape(const dkv_batch *b) {
   return true;
 }
 
+bool valid_decode(const dkv_decode_batch *b) {
+  if (!b) return false;
+  if (b->D != DKV_HEAD_DIM || b->L < 1 || b->R < 1 || b->Hkv < 1 || b->Hq < b->Hkv || b->Hq % b->Hkv != 0 ||
+      b->Hq > dkv::kMaxHq || b->R > 65535 || b->L > 65535)
+    return false;
+  if (b->cap < 16 || (b->cap % 16) != 0) return false;
+  const int64_t U = static_cast<int64_t>(b->L) * b->R * b->Hkv;
+  if (U > INT32_MAX || b->unit_base < 0 || b->unit_base + U > INT32_MAX) return false;
+  return true;
+}
+
+bool decode_pointers(const dkv_decode_batch *b) {
+  return b->k_new && b->v_new && b->sig_sum && b->sig_cnt && b->ctx_lens && b->new_lens && b->classes &&
+         b->slot_of && aligned(b->k_new, 16) && aligned(b->v_new, 16) && aligned(b->sig_sum, 16) &&
+         aligned(b->sig_cnt, 4) && aligned(b->ctx_lens, 4) && aligned(b->new_lens, 4) && aligned(b->classes, 16) &&
+         aligned(b->slot_of, 4);
+}
+
+dkv::DecodeArgs decode_args(const dkv_decode_batch *b, const dkv_pool *pool, const dkv_tables *t) {
+  dkv::DecodeArgs a{};
+  a.L = b->L; a.R = b->R; a.Hq = b->Hq; a.Hkv = b->Hkv; a.G = b->Hq / b->Hkv;
+  a.P = pool->P; a.pmax = t->pmax; a.cap = b->cap;
+  a.F = pool->F; a.U = static_cast<int64_t>(b->L) * b->R * b->Hkv; a.unit_base = b->unit_base;
+  a.k_new = static_cast<const uint16_t *>(b->k_new); a.v_new = static_cast<const uint16_t *>(b->v_new);
+  a.sig_sum = b->sig_sum; a.sig_cnt = b->sig_cnt; a.ctx_lens = b->ctx_lens; a.new_lens = b->new_lens;
+  a.classes = b->classes; a.slot_of = b->slot_of;
+  a.free_list = pool->free_list; a.cursors = pool->cursors; a.rev_unit = pool->rev_unit; a.rev_idx = pool->rev_idx;
+  a.page_cls = pool->page_cls; a.pages = pool->pages; a.status = pool->status;
+  a.fwd = t->fwd; a.unit_hdr = t->unit_hdr;
+  return a;
+}
+
+bool valid_decode_tables(const dkv_decode_batch *b, const dkv_pool *pool, const dkv_tables *t) {
+  if (!t || !t->fwd || !t->unit_hdr || !aligned(t->unit_hdr, 16) || !aligned(t->fwd, 4) || t->pmax < 2) return false;
+  const int64_t U = static_cast<int64_t>(b->L) * b->R * b->Hkv;
+  // the scan packs two sums of at most U * pmax pages into 31 bits each
+  if (U * t->pmax >= (int64_t{1} << 31)) return false;
+  (void)pool;
+  return true;
+}
+
+// Largest head group per apply block whose shared memory fits; 0 if none.
+int32_t apply_heads(int32_t Hkv, int32_t words, int32_t pmax) {
+  int32_t hpc = Hkv < dkv::kMaxApplyWarps ? Hkv : dkv::kMaxApplyWarps;
+  while (hpc > 1 && dkv::apply_smem(hpc, words, pmax) > 96 * 1024) hpc = (hpc + 1) / 2;
+  return dkv::apply_smem(hpc, words, pmax) <= 200 * 1024 ? hpc : 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -173,6 +221,76 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
   if (const int32_t rc = cuda_status(dkv::launch_pack(a, pack_grid, s))) return rc;
   mark(4);
   if (const int32_t rc = cuda_status(dkv::launch_commit(a, std::max(commit_grid, 1), s))) return rc;
+  mark(5);
+  return DKV_OK;
+}
+
+int32_t dkv_decode_workspace_size(const dkv_decode_batch *b, size_t *bytes) {
+  if (!bytes || !valid_decode(b)) return DKV_E_INVAL;
+  *bytes = dkv::dec_ws_layout(static_cast<int64_t>(b->L) * b->R * b->Hkv).bytes;
+  return DKV_OK;
+}
+
+int32_t dkv_decode_index(const dkv_decode_batch *b, const dkv_pool *pool, const dkv_tables *t, void *stream) {
+  if (!valid_decode(b) || !valid_pool(pool) || !valid_decode_tables(b, pool, t)) return DKV_E_INVAL;
+  if (!b->ctx_lens || !b->classes || !b->slot_of || !aligned(b->ctx_lens, 4) || !aligned(b->slot_of, 4))
+    return DKV_E_INVAL;
+  int sms = 0, pack_bps = 0;
+  if (!device_info(&sms, &pack_bps)) return cuda_status(cudaErrorInvalidDevice);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(b->L) * b->R * b->cap * b->Hkv;
+  if (const int32_t rc = cuda_status(cudaMemsetAsync(b->classes, 0, rows, s))) return rc;
+  if (const int32_t rc = cuda_status(cudaMemsetAsync(b->slot_of, 0xff, rows * sizeof(int32_t), s))) return rc;
+  const dkv::DecodeArgs a = decode_args(b, pool, t);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((a.U + 7) / 8, int64_t{sms} * 8)));
+  return cuda_status(dkv::launch_index(a, grid, s));
+}
+
+int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dkv_pool *pool, const dkv_tables *t,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+  if (!valid_decode(b) || !p || !valid_pool(pool) || !decode_pointers(b) || !valid_decode_tables(b, pool, t))
+    return DKV_E_INVAL;
+  if (!(std::isfinite(p->alpha_h) && std::isfinite(p->alpha_l)) || !(p->alpha_l >= 0.0f) ||
+      !(p->alpha_h >= p->alpha_l) || p->reserved != 0)
+    return DKV_E_INVAL;
+  const int64_t U = static_cast<int64_t>(b->L) * b->R * b->Hkv;
+  const dkv::DecWsLayout lay = dkv::dec_ws_layout(U);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.bytes) return DKV_E_INVAL;
+  const int32_t words = (b->cap + 31) / 32;
+  const int32_t hpc = apply_heads(b->Hkv, words, t->pmax);
+  if (hpc == 0) return DKV_E_INVAL;
+  int sms = 0, pack_bps = 0;
+  if (!device_info(&sms, &pack_bps)) return cuda_status(cudaErrorInvalidDevice);
+
+  dkv::DecodeArgs a = decode_args(b, pool, t);
+  a.spin_limit = p->spin_limit < 0 ? (1 << 22) : p->spin_limit;
+  a.alpha_h = p->alpha_h;
+  a.alpha_l = p->alpha_l;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  a.ws = reinterpret_cast<dkv::DecWsHeader *>(ws);
+  a.ucnt = reinterpret_cast<int4 *>(ws + lay.ucnt);
+  a.part = reinterpret_cast<uint64_t *>(ws + lay.part);
+  a.plan = reinterpret_cast<dkv::DecPlan *>(ws + lay.plan);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Profiler *prof = static_cast<Profiler *>(p->profiler);
+  cudaEvent_t *ev = nullptr;
+  if (prof && prof->next < prof->max_calls) {
+    ev = prof->ev.data() + static_cast<size_t>(prof->next) * (DKV_PROFILE_KERNELS + 1);
+    prof->next++;
+  }
+  auto mark = [&](int i) {
+    if (ev) cudaEventRecord(ev[i], s);
+  };
+  mark(0);
+  if (const int32_t rc = cuda_status(cudaMemsetAsync(ws, 0, lay.reset, s))) return rc;
+  mark(1);
+  if (const int32_t rc = cuda_status(dkv::launch_reclass(a, s))) return rc;
+  mark(2);
+  if (const int32_t rc = cuda_status(dkv::launch_dscan(a, lay.npart, s))) return rc;
+  mark(3);
+  if (const int32_t rc = cuda_status(dkv::launch_apply(a, hpc, words, s))) return rc;
+  mark(4);
   mark(5);
   return DKV_OK;
 }

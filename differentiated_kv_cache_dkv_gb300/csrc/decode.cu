@@ -1,0 +1,890 @@
+// decode.cu -- one generation step on the unified pages (dkv_decode_step) and
+// the per-position index it keeps (dkv_decode_index).
+//
+// DiffKV (arXiv 2412.03131), Pith review: tokens are K8V4, K4V2 or pruned by
+// their significance against alpha_h/N and alpha_l/N ("What carries the
+// argument", "Core claim"); in the generation phase tokens are classified as
+// they age and demotion and pruning are irreversible (Referee Report, major
+// comment 2 on Section 4 / Algorithm 1); pages come from a circular free page
+// list through a parallel prefix sum and are tracked by a bidirectional page
+// table ("What carries the argument").
+//
+// Step semantics (with N = ctx + new for a request):
+//   - every live token's class becomes min(old, classify(score, N)); the new
+//     token is classified;
+//   - per unit (layer, request, KV head) each list (K8V4 slots, K4V2 slots)
+//     drops its removed tokens; the survivors in slots >= the survivor count
+//     move, ascending, into the holes below it, ascending (bytes copied);
+//   - tokens demoted K8V4 -> K4V2 are requantised (4-bit K, 2-bit V) from
+//     their dequantised fp32 values and appended to the K4V2 list in
+//     ascending position order; then the new token is appended to its list;
+//   - a list keeps its first min(have, need) pages, need = ceil(n / capacity);
+//     new pages come from the free-list head by an exclusive scan over units
+//     (a unit's new K8V4 pages first); surplus pages are freed to the tail in
+//     (unit, list, page) order; unused slots are cleared.
+//
+// Kernels, in stream order (after a memset of the call's counters):
+//   k_reclass  streams sig_sum / sig_cnt, reclassifies every live row and
+//              marks each changed class byte in place (0x80 | old << 2 | new;
+//              old = 3 for the new token) -- the step's only full pass over
+//              the significance sums, which dominate its bytes;
+//   k_dscan    per-unit plan (survivors, page needs, new and freed pages),
+//              block scan + decoupled look-back over partitions of units,
+//              capacity check;
+//   k_apply    one block per (layer, request, head group): turns the marks
+//              into final classes (or reverts them if the call failed),
+//              builds per-unit bitmaps of removed slots and demoted
+//              positions in shared memory, then one warp per unit clears new
+//              pages, hole-fills, requantises, appends, clears vacated slots
+//              and rewrites its tables.
+// All waits are bounded (look-back polls by spin_limit); nothing traps.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "dkv_internal.cuh"
+
+namespace dkv {
+
+namespace {
+
+constexpr int kReclassThreads = 512;
+constexpr int kReclassRows = 4;           // rows in flight per thread
+constexpr int kDScanThreads = 256;        // one unit per thread
+
+__device__ __forceinline__ void st_release(uint64_t *p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_acquire(const uint64_t *p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int32_t cdiv(int32_t a, int32_t b) { return (a + b - 1) / b; }
+
+// |x| > 65504 or non-finite for a bf16 bit pattern: bf16 0x477f is 65280, the
+// largest value not above 65504, and 0x4780 (65536) the next.
+__device__ __forceinline__ bool bf16_out_of_range(uint32_t h) { return (h & 0x7fffu) >= 0x4780u; }
+
+__device__ __forceinline__ bool words_out_of_range(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) bad |= bf16_out_of_range(w[i] & 0xffffu) | bf16_out_of_range(w[i] >> 16);
+  return bad;
+}
+
+// ---------------------------------------------------------------- k_reclass --
+
+template <int kV4>  // float4 loads per row (G / 4); 0 = scalar loads
+__global__ void __launch_bounds__(kReclassThreads) k_reclass(DecodeArgs a) {
+  __shared__ int32_t ev_s[kMaxHq * 3];  // per head: demoted, K8V4 pruned, K4V2 pruned
+  const int32_t r = blockIdx.y, l = blockIdx.z;
+  const int32_t i0 = blockIdx.x * kReclassChunk;
+  const int32_t ctx = __ldg(a.ctx_lens + r), nw = __ldg(a.new_lens + r);
+  const bool bad = ctx < 0 || nw < 0 || nw > 1 || static_cast<int64_t>(ctx) + nw > a.cap ||
+                   static_cast<int64_t>(ctx) + nw > static_cast<int64_t>(a.pmax - 1) * a.P;
+  if (bad) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(&a.ws->err, DKV_E_LENS);
+    return;
+  }
+  const int32_t N = ctx + nw;
+  if (i0 >= N) return;
+  const int32_t i1 = min(N, i0 + kReclassChunk);
+  const int Hkv = a.Hkv, G = a.G;
+  for (int t = threadIdx.x; t < Hkv * 3; t += blockDim.x) ev_s[t] = 0;
+  __syncthreads();
+  const float thr_h = __fdiv_rn(a.alpha_h, static_cast<float>(N));
+  const float thr_l = __fdiv_rn(a.alpha_l, static_cast<float>(N));
+  const int64_t tok0 = static_cast<int64_t>(r) * a.cap + i0;
+  const int64_t lrow = static_cast<int64_t>(l) * a.R * a.cap;  // first token row of the layer
+  uint8_t *cls = a.classes + (lrow + tok0) * Hkv;
+  const float *sig = a.sig_sum + (lrow + tok0) * a.Hq;
+  const int32_t *cnt = a.sig_cnt + tok0;
+  const int nrows = (i1 - i0) * Hkv;
+  const int64_t u0 = (static_cast<int64_t>(l) * a.R + r) * Hkv;
+
+  for (int jb = 0; jb < nrows; jb += kReclassRows * kReclassThreads) {
+    float m[kReclassRows];
+    int32_t c[kReclassRows];
+    uint32_t old[kReclassRows];
+#pragma unroll
+    for (int k = 0; k < kReclassRows; ++k) {
+      const int j = jb + k * kReclassThreads + threadIdx.x;
+      m[k] = 0.0f;
+      c[k] = 0;
+      old[k] = 0;
+      if (j < nrows) {
+        const int ii = j / Hkv;
+        c[k] = __ldg(cnt + ii);
+        old[k] = cls[j];
+        if (kV4 > 0) {
+          const float4 *p = reinterpret_cast<const float4 *>(sig + static_cast<int64_t>(j) * G);
+          const float4 x = __ldcs(p);
+          float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+          float mn = fminf(fminf(x.x, x.y), fminf(x.z, x.w));
+#pragma unroll
+          for (int q = 1; q < kV4; ++q) {
+            const float4 y = __ldcs(p + q);
+            mx = fmaxf(mx, fmaxf(fmaxf(y.x, y.y), fmaxf(y.z, y.w)));
+            mn = fminf(mn, fminf(fminf(y.x, y.y), fminf(y.z, y.w)));
+          }
+          m[k] = c[k] > 0 ? mx : mn;
+        } else {
+          const float *p = sig + static_cast<int64_t>(j) * G;
+          float mx = __ldcs(p), mn = mx;
+          for (int q = 1; q < G; ++q) {
+            const float y = __ldcs(p + q);
+            mx = fmaxf(mx, y);
+            mn = fminf(mn, y);
+          }
+          m[k] = c[k] > 0 ? mx : mn;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kReclassRows; ++k) {
+      const int j = jb + k * kReclassThreads + threadIdx.x;
+      if (j >= nrows) continue;
+      const int ii = j / Hkv, h = j - ii * Hkv;
+      uint32_t cn = DKV_CLASS_K8V4;  // a count of 0: not yet observed
+      if (c[k] != 0) {
+        // max over the group of the rounded quotients == rounded quotient
+        // of the max sum (min for a negative count): division is monotone
+        const float s = __fdiv_rn(m[k], static_cast<float>(c[k]));
+        cn = s >= thr_h ? DKV_CLASS_K8V4 : (s >= thr_l ? DKV_CLASS_K4V2 : DKV_CLASS_PRUNE);
+      }
+      if (i0 + ii < ctx) {
+        const uint32_t o = old[k];
+        if (o > DKV_CLASS_K8V4) {
+          set_error(&a.ws->err, DKV_E_INTERNAL);
+          continue;
+        }
+        if (cn < o) {
+          cls[j] = static_cast<uint8_t>(0x80u | (o << 2) | cn);
+          atomicAdd(&ev_s[h * 3 + (o == DKV_CLASS_K4V2 ? 2 : (cn == DKV_CLASS_K4V2 ? 0 : 1))], 1);
+        }
+      } else {  // the new token (position ctx)
+        cls[j] = static_cast<uint8_t>(0x80u | (3u << 2) | cn);
+        const int64_t u = u0 + h;
+        a.ucnt[u].w = static_cast<int32_t>(old[k] | (cn << 8) | (1u << 16));
+        if (cn != DKV_CLASS_PRUNE) {
+          const uint4 *kr = reinterpret_cast<const uint4 *>(a.k_new + u * DKV_HEAD_DIM);
+          const uint4 *vr = reinterpret_cast<const uint4 *>(a.v_new + u * DKV_HEAD_DIM);
+          bool oor = false;
+          for (int q = 0; q < DKV_HEAD_DIM / 8; ++q) oor |= words_out_of_range(__ldg(kr + q)) |
+                                                          words_out_of_range(__ldg(vr + q));
+          if (oor) set_error(&a.ws->err, DKV_E_RANGE);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < Hkv * 3; t += blockDim.x) {
+    const int32_t n = ev_s[t];
+    if (n == 0) continue;
+    int4 *uc = a.ucnt + u0 + t / 3;
+    int *dst = (t % 3 == 0) ? &uc->x : (t % 3 == 1 ? &uc->y : &uc->z);
+    atomicAdd(dst, n);
+  }
+}
+
+// ------------------------------------------------------------------ k_dscan --
+
+// 64-bit look-back word: flags in bits 62-63, new pages in bits 31-61, freed
+// pages in bits 0-30 (both sums stay below 2^31: units * pmax < 2^31).
+constexpr uint64_t kHalfMask = (1ull << 31) - 1;
+
+__global__ void __launch_bounds__(kDScanThreads) k_dscan(DecodeArgs a) {
+  __shared__ uint64_t wsum_s[kDScanThreads / 32];
+  __shared__ int32_t part_s, fail_s;
+  __shared__ uint64_t prefix_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    part_s = atomicAdd(&a.ws->ticket, 1);
+    fail_s = 0;
+  }
+  __syncthreads();
+  const int32_t part = part_s;
+  const int32_t npart = static_cast<int32_t>((a.U + kDScanThreads - 1) / kDScanThreads);
+  if (part >= npart) return;
+  const int64_t u = static_cast<int64_t>(part) * kDScanThreads + tid;
+
+  DecPlan pl{};
+  uint64_t v = 0;
+  if (u < a.U) {
+    const int4 hdr = reinterpret_cast<const int4 *>(a.unit_hdr)[u];
+    const int4 uc = a.ucnt[u];
+    pl.n_hi = hdr.x;
+    pl.n_lo = hdr.y;
+    pl.have_hi = hdr.z;
+    pl.have_lo = hdr.w;
+    pl.dem = uc.x;
+    pl.keep_hi = hdr.x - uc.x - uc.y;
+    pl.keep_lo = hdr.y - uc.z;
+    pl.new_cls = (uc.w & (1 << 16)) ? ((uc.w >> 8) & 3) : 0;
+    const int32_t n2_hi = pl.keep_hi + (pl.new_cls == DKV_CLASS_K8V4);
+    const int32_t n2_lo = pl.keep_lo + pl.dem + (pl.new_cls == DKV_CLASS_K4V2);
+    pl.need_hi = cdiv(n2_hi, a.P);
+    pl.need_lo = cdiv(n2_lo, 2 * a.P);
+    const int32_t ctx = __ldg(a.ctx_lens + (u / a.Hkv) % a.R);
+    if (pl.keep_hi < 0 || pl.keep_lo < 0 || pl.have_hi < 0 || pl.have_lo < 0 || hdr.x < 0 || hdr.y < 0 ||
+        pl.have_hi + pl.have_lo > a.pmax || static_cast<int64_t>(hdr.x) > static_cast<int64_t>(pl.have_hi) * a.P ||
+        static_cast<int64_t>(hdr.y) > static_cast<int64_t>(pl.have_lo) * 2 * a.P ||
+        static_cast<int64_t>(hdr.x) + hdr.y > ctx) {
+      set_error(&a.ws->err, DKV_E_INTERNAL);
+      pl.need_hi = pl.have_hi > 0 ? pl.have_hi : 0;
+      pl.need_lo = pl.have_lo > 0 ? pl.have_lo : 0;
+    } else if (pl.need_hi + pl.need_lo > a.pmax) {
+      set_error(&a.ws->err, DKV_E_LENS);
+      pl.need_hi = pl.have_hi;
+      pl.need_lo = pl.have_lo;
+    }
+    const int32_t d = max(0, pl.need_hi - pl.have_hi) + max(0, pl.need_lo - pl.have_lo);
+    const int32_t f = max(0, pl.have_hi - pl.need_hi) + max(0, pl.have_lo - pl.need_lo);
+    v = (static_cast<uint64_t>(d) << 31) | static_cast<uint64_t>(f);
+  }
+  // block-wide inclusive scan of the packed (new, freed) counts
+  uint64_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) wsum_s[warp] = incl;
+  __syncthreads();
+  uint64_t before = 0;
+  for (int w = 0; w < warp; ++w) before += wsum_s[w];
+  const uint64_t excl = before + incl - v;
+
+  if (tid == 0) {
+    uint64_t agg = 0;
+    for (int w = 0; w < kDScanThreads / 32; ++w) agg += wsum_s[w];
+    uint64_t prefix = 0;
+    bool fail = false;
+    if (part == 0) {
+      st_release(a.part, kFlagPrefix | agg);
+    } else {
+      st_release(a.part + part, kFlagAggregate | agg);
+      if (a.spin_limit == 0) {
+        fail = true;
+      } else {
+        int32_t pred = part - 1;
+        for (;;) {
+          uint64_t st = ld_acquire(a.part + pred);
+          int64_t spins = 0;
+          while ((st >> 62) == 0) {
+            if (++spins > a.spin_limit) {
+              fail = true;
+              break;
+            }
+            __nanosleep(64);
+            st = ld_acquire(a.part + pred);
+          }
+          if (fail) break;
+          prefix += st & kValueMask;
+          if ((st & kFlagPrefix) != 0) break;
+          --pred;  // partition 0 always publishes a prefix
+        }
+      }
+      if (!fail) st_release(a.part + part, kFlagPrefix | (prefix + agg));
+    }
+    if (fail) {
+      set_error(&a.ws->err, DKV_E_TIMEOUT);
+      fail_s = 1;
+    }
+    prefix_s = prefix;
+    if (!fail && part == npart - 1) {
+      const uint64_t tot = prefix + agg;
+      const int64_t dsum = static_cast<int64_t>(tot >> 31), fsum = static_cast<int64_t>(tot & kHalfMask);
+      const uint64_t head = a.cursors[0], tail = a.cursors[1];
+      a.ws->dsum = dsum;
+      a.ws->fsum = fsum;
+      a.ws->head = head;
+      a.ws->tail = tail;
+      if (tail - head > static_cast<uint64_t>(a.F) || static_cast<uint64_t>(dsum) > tail - head)
+        set_error(&a.ws->err, DKV_E_NOMEM);
+    }
+  }
+  __syncthreads();
+  if (fail_s || u >= a.U) return;
+  const uint64_t off = prefix_s + excl;
+  pl.off_d = static_cast<int32_t>(off >> 31);
+  pl.off_f = static_cast<int32_t>(off & kHalfMask);
+  a.plan[u] = pl;
+}
+
+// ------------------------------------------------------------------ k_apply --
+
+// Up to 32 next indices s in [cur, hi) whose bit in bm is `want`, ascending,
+// into buf[0..); advances cur past the last one taken.  Warp-collective.
+__device__ int next_bits(const uint32_t *bm, int32_t &cur, int32_t hi, bool want, int32_t *buf, int lane) {
+  int got = 0;
+  while (got < 32 && cur < hi) {
+    const int32_t w = (cur >> 5) + lane;
+    const int32_t s0 = w << 5;
+    uint32_t bits = 0;
+    if (s0 < hi) {
+      bits = want ? bm[w] : ~bm[w];
+      if (s0 < cur) bits &= ~0u << (cur - s0);
+      if (hi - s0 < 32) bits &= (1u << (hi - s0)) - 1u;
+    }
+    const int n = __popc(bits);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int room = 32 - got;
+    int rk = incl - n;
+    uint32_t b = bits;
+    while (b != 0u && rk < room) {
+      const int j = __ffs(b) - 1;
+      b &= b - 1u;
+      buf[got + rk] = s0 + j;
+      ++rk;
+    }
+    __syncwarp();
+    if (total <= room) {
+      got += total;
+      const int32_t nxt = ((cur >> 5) + 32) << 5;
+      cur = nxt < hi ? nxt : hi;
+    } else {
+      got = 32;
+      cur = buf[31] + 1;
+    }
+  }
+  return got;
+}
+
+// Everything one warp needs about its unit.
+struct UnitView {
+  int64_t u;
+  int64_t row0;        // classes / slot_of index of (position 0, this head)
+  int32_t ctx;         // live positions before the step
+  int32_t Hkv;
+  const int32_t *fw;   // forward row (old contents until the table phase)
+  DecPlan p;
+  int64_t new_base;    // head + off_d (free-list cursor of the unit's first new page)
+  int32_t xh;          // new K8V4 pages
+};
+
+__device__ __forceinline__ int32_t new_page(const DecodeArgs &a, const UnitView &v, int32_t j) {
+  const uint64_t idx = static_cast<uint64_t>(v.new_base + j) % static_cast<uint64_t>(a.F);
+  return a.free_list[idx];
+}
+
+// Page id of page k of the unit's K8V4 (hi) or K4V2 list: the old pages
+// first, then the new ones.  -1 (and an error) for an id outside the pool.
+__device__ __forceinline__ int32_t list_page(const DecodeArgs &a, const UnitView &v, bool hi, int32_t k) {
+  int32_t id;
+  if (hi) id = k < v.p.have_hi ? v.fw[k] : new_page(a, v, k - v.p.have_hi);
+  else id = k < v.p.have_lo ? v.fw[v.p.have_hi + k] : new_page(a, v, v.xh + k - v.p.have_lo);
+  if (id < 0 || id >= a.F) {
+    atomicCAS(a.status, 0, DKV_E_INTERNAL);
+    return -1;
+  }
+  return id;
+}
+
+struct SlotAddr {
+  uint8_t *k, *v, *meta, *pos;
+};
+
+__device__ __forceinline__ bool slot_addr(const DecodeArgs &a, const UnitView &v, bool hi, int32_t s, SlotAddr &o) {
+  const int32_t per = hi ? a.P : 2 * a.P;
+  const int32_t id = list_page(a, v, hi, s / per);
+  if (id < 0) return false;
+  const int64_t P = a.P;
+  const int64_t ss = s % per;
+  uint8_t *pg = a.pages + static_cast<int64_t>(id) * 216 * P;
+  o.k = pg + ss * (hi ? 128 : 64);
+  o.v = pg + 128 * P + ss * (hi ? 64 : 32);
+  o.meta = pg + 192 * P + 8 * ss;
+  o.pos = pg + 208 * P + 4 * ss;
+  return true;
+}
+
+// Copy one slot of a list to another slot of the same list (codes, metadata,
+// position); returns the moved token's position.
+__device__ __forceinline__ int32_t copy_slot(const SlotAddr &f, const SlotAddr &t, bool hi) {
+  const uint4 *fk = reinterpret_cast<const uint4 *>(f.k);
+  const uint4 *fv = reinterpret_cast<const uint4 *>(f.v);
+  uint4 *tk = reinterpret_cast<uint4 *>(t.k);
+  uint4 *tv = reinterpret_cast<uint4 *>(t.v);
+  if (hi) {
+    uint4 k[8], vv[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) k[i] = fk[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vv[i] = fv[i];
+    const uint2 m = *reinterpret_cast<const uint2 *>(f.meta);
+    const int32_t pos = *reinterpret_cast<const int32_t *>(f.pos);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tk[i] = k[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tv[i] = vv[i];
+    *reinterpret_cast<uint2 *>(t.meta) = m;
+    *reinterpret_cast<int32_t *>(t.pos) = pos;
+    return pos;
+  }
+  uint4 k[4], vv[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) k[i] = fk[i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) vv[i] = fv[i];
+  const uint2 m = *reinterpret_cast<const uint2 *>(f.meta);
+  const int32_t pos = *reinterpret_cast<const int32_t *>(f.pos);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) tk[i] = k[i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) tv[i] = vv[i];
+  *reinterpret_cast<uint2 *>(t.meta) = m;
+  *reinterpret_cast<int32_t *>(t.pos) = pos;
+  return pos;
+}
+
+__device__ __forceinline__ void clear_slot(const SlotAddr &t, bool hi) {
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  uint4 *tk = reinterpret_cast<uint4 *>(t.k);
+  uint4 *tv = reinterpret_cast<uint4 *>(t.v);
+  for (int i = 0; i < (hi ? 8 : 4); ++i) tk[i] = z;
+  for (int i = 0; i < (hi ? 4 : 2); ++i) tv[i] = z;
+  *reinterpret_cast<uint2 *>(t.meta) = make_uint2(0u, 0u);
+  *reinterpret_cast<int32_t *>(t.pos) = -1;
+}
+
+// Hole-fill of one list: survivors in slots >= keep move, ascending, into the
+// removed slots below keep, ascending; the moved tokens' index entries follow.
+__device__ void hole_fill(const DecodeArgs &a, const UnitView &v, bool hi, const uint32_t *rm, int32_t keep,
+                          int32_t n, int32_t *buf, int lane) {
+  int32_t hc = 0, mc = keep;
+  for (;;) {
+    const int nh = next_bits(rm, hc, keep, true, buf, lane);
+    if (nh == 0) break;
+    int32_t hole = lane < nh ? buf[lane] : 0;
+    __syncwarp();
+    const int nm = next_bits(rm, mc, n, false, buf, lane);
+    int32_t mover = lane < nm ? buf[lane] : 0;
+    __syncwarp();
+    if (nm != nh) {
+      if (lane == 0) atomicCAS(a.status, 0, DKV_E_INTERNAL);
+      return;
+    }
+    if (lane < nh) {
+      SlotAddr f, t;
+      if (slot_addr(a, v, hi, mover, f) && slot_addr(a, v, hi, hole, t)) {
+        const int32_t pos = copy_slot(f, t, hi);
+        if (pos >= 0 && pos < v.ctx) a.slot_of[v.row0 + static_cast<int64_t>(pos) * v.Hkv] = hole;
+        else atomicCAS(a.status, 0, DKV_E_INTERNAL);
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// The per-token quantiser on fp32 values spread over `lanes` lanes (each
+// holding 4 or 16 channels): exact min / max (a zero extreme taken as +0),
+// fp16 scale and zero, codes by IEEE division and round-half-to-even.
+template <int kPer, int kGroup>
+__device__ __forceinline__ void quant_vals(const float (&x)[kPer], int nmax, uint32_t (&q)[kPer], uint16_t &s16o,
+                                           uint16_t &z16o) {
+  float mn = x[0], mx = x[0];
+#pragma unroll
+  for (int i = 1; i < kPer; ++i) {
+    mn = fminf(mn, x[i]);
+    mx = fmaxf(mx, x[i]);
+  }
+#pragma unroll
+  for (int o = 1; o < kGroup; o <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  mn = __fadd_rn(mn, 0.0f);
+  mx = __fadd_rn(mx, 0.0f);
+  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(nmax));
+  uint16_t s16 = __half_as_ushort(__float2half_rn(s32));
+  if (mx > mn && s16 == 0) s16 = 1;
+  const uint16_t z16 = __half_as_ushort(__float2half_rn(mn));
+  const float s = __half2float(__ushort_as_half(s16));
+  const float z = __half2float(__ushort_as_half(z16));
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    q[i] = 0u;
+    if (s != 0.0f) {
+      const float t = rintf(__fdiv_rn(__fsub_rn(x[i], z), s));
+      q[i] = static_cast<uint32_t>(fminf(fmaxf(t, 0.0f), static_cast<float>(nmax)));
+    }
+  }
+  s16o = s16;
+  z16o = z16;
+}
+
+template <int kPer>
+__device__ __forceinline__ uint64_t pack_bits(const uint32_t (&q)[kPer], int width) {
+  uint64_t w = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) w |= static_cast<uint64_t>(q[i]) << (width * i);
+  return w;
+}
+
+// Requantise the demoted tokens (K8V4 -> K4V2) into K4V2 slots keep_lo + k in
+// ascending position order.  Eight lanes per token (16 channels each), four
+// tokens per pass.
+__device__ void demote(const DecodeArgs &a, const UnitView &v, const uint32_t *dem, int32_t *buf, int lane) {
+  int32_t cur = 0, k = 0;
+  const int grp = lane >> 3, t = lane & 7;
+  const int64_t P = a.P;
+  for (;;) {
+    const int nd = next_bits(dem, cur, v.ctx, true, buf, lane);
+    if (nd == 0) break;
+    for (int g = 0; g < nd; g += 4) {
+      const int j = g + grp;
+      const bool act = j < nd;
+      int32_t pos = 0, hs = -1;
+      SlotAddr src{}, dst{};
+      bool ok = false;
+      if (act) {
+        pos = buf[j];
+        hs = a.slot_of[v.row0 + static_cast<int64_t>(pos) * v.Hkv];
+        ok = hs >= 0 && hs < v.p.n_hi && slot_addr(a, v, true, hs, src) &&
+             slot_addr(a, v, false, v.p.keep_lo + k + j, dst);
+        if (ok && *reinterpret_cast<const int32_t *>(src.pos) != pos) ok = false;
+        if (!ok && t == 0) atomicCAS(a.status, 0, DKV_E_INTERNAL);
+      }
+      uint4 kc = make_uint4(0u, 0u, 0u, 0u);
+      uint2 vc = make_uint2(0u, 0u);
+      uint2 meta = make_uint2(0u, 0u);
+      if (ok) {
+        kc = reinterpret_cast<const uint4 *>(src.k)[t];  // channels 16t .. 16t+15, 8-bit
+        vc = reinterpret_cast<const uint2 *>(src.v)[t];  // channels 16t .. 16t+15, 4-bit
+        meta = *reinterpret_cast<const uint2 *>(src.meta);
+      }
+      const float ks = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.x & 0xffffu)));
+      const float kz = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.x >> 16)));
+      const float vs = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.y & 0xffffu)));
+      const float vz = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.y >> 16)));
+      float xk[16], xv[16];
+      const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
+      const uint32_t vw[2] = {vc.x, vc.y};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        xk[i] = __fmaf_rn(static_cast<float>((kw[i >> 2] >> (8 * (i & 3))) & 255u), ks, kz);
+        xv[i] = __fmaf_rn(static_cast<float>((vw[i >> 3] >> (4 * (i & 7))) & 15u), vs, vz);
+      }
+      uint32_t qk[16], qv[16];
+      uint16_t ks2, kz2, vs2, vz2;
+      quant_vals<16, 8>(xk, 15, qk, ks2, kz2);
+      quant_vals<16, 8>(xv, 3, qv, vs2, vz2);
+      if (ok) {
+        reinterpret_cast<uint2 *>(dst.k)[t] = make_uint2(static_cast<uint32_t>(pack_bits<16>(qk, 4)),
+                                                         static_cast<uint32_t>(pack_bits<16>(qk, 4) >> 32));
+        reinterpret_cast<uint32_t *>(dst.v)[t] = static_cast<uint32_t>(pack_bits<16>(qv, 2));
+        if (t == 0) {
+          *reinterpret_cast<uint2 *>(dst.meta) =
+              make_uint2(static_cast<uint32_t>(ks2) | (static_cast<uint32_t>(kz2) << 16),
+                         static_cast<uint32_t>(vs2) | (static_cast<uint32_t>(vz2) << 16));
+          *reinterpret_cast<int32_t *>(dst.pos) = pos;
+          a.slot_of[v.row0 + static_cast<int64_t>(pos) * v.Hkv] = v.p.keep_lo + k + j;
+        }
+      }
+    }
+    k += nd;
+    __syncwarp();
+  }
+  (void)P;
+}
+
+// Quantise and store the new token (bf16 row of 128 channels, 4 per lane).
+__device__ void append_new(const DecodeArgs &a, const UnitView &v, int lane) {
+  const bool hi = v.p.new_cls == DKV_CLASS_K8V4;
+  const int32_t slot = hi ? v.p.keep_hi : v.p.keep_lo + v.p.dem;
+  SlotAddr d;
+  if (!slot_addr(a, v, hi, slot, d)) return;
+  const uint2 kr = reinterpret_cast<const uint2 *>(a.k_new + v.u * DKV_HEAD_DIM)[lane];
+  const uint2 vr = reinterpret_cast<const uint2 *>(a.v_new + v.u * DKV_HEAD_DIM)[lane];
+  float xk[4] = {__uint_as_float(kr.x << 16), __uint_as_float(kr.x & 0xffff0000u), __uint_as_float(kr.y << 16),
+                 __uint_as_float(kr.y & 0xffff0000u)};
+  float xv[4] = {__uint_as_float(vr.x << 16), __uint_as_float(vr.x & 0xffff0000u), __uint_as_float(vr.y << 16),
+                 __uint_as_float(vr.y & 0xffff0000u)};
+  uint32_t qk[4], qv[4];
+  uint16_t ks, kz, vs, vz;
+  quant_vals<4, 32>(xk, hi ? 255 : 15, qk, ks, kz);
+  quant_vals<4, 32>(xv, hi ? 15 : 3, qv, vs, vz);
+  if (hi) {
+    reinterpret_cast<uint32_t *>(d.k)[lane] = static_cast<uint32_t>(pack_bits<4>(qk, 8));
+    reinterpret_cast<uint16_t *>(d.v)[lane] = static_cast<uint16_t>(pack_bits<4>(qv, 4));
+  } else {
+    reinterpret_cast<uint16_t *>(d.k)[lane] = static_cast<uint16_t>(pack_bits<4>(qk, 4));
+    d.v[lane] = static_cast<uint8_t>(pack_bits<4>(qv, 2));
+  }
+  if (lane == 0) {
+    *reinterpret_cast<uint2 *>(d.meta) = make_uint2(static_cast<uint32_t>(ks) | (static_cast<uint32_t>(kz) << 16),
+                                                    static_cast<uint32_t>(vs) | (static_cast<uint32_t>(vz) << 16));
+    *reinterpret_cast<int32_t *>(d.pos) = v.ctx;
+    a.slot_of[v.row0 + static_cast<int64_t>(v.ctx) * v.Hkv] = slot;
+  }
+}
+
+// Zero codes and metadata, position -1, over a whole new page.
+__device__ void clear_page(const DecodeArgs &a, int32_t id, int lane) {
+  const int64_t P = a.P;
+  uint4 *pg = reinterpret_cast<uint4 *>(a.pages + static_cast<int64_t>(id) * 216 * P);
+  const int64_t nz = 13 * P, nall = (216 * P) / 16;  // [0, 208P) zero, [208P, 216P) all ones
+  for (int64_t i = lane; i < nall; i += 32)
+    pg[i] = i < nz ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(~0u, ~0u, ~0u, ~0u);
+}
+
+__device__ void apply_unit(const DecodeArgs &a, UnitView &v, uint32_t *rh, uint32_t *rl, uint32_t *dem,
+                           int32_t *buf, int32_t *stage, int lane) {
+  const DecPlan &p = v.p;
+  const int32_t n2_hi = p.keep_hi + (p.new_cls == DKV_CLASS_K8V4);
+  const int32_t n2_lo = p.keep_lo + p.dem + (p.new_cls == DKV_CLASS_K4V2);
+  // new pages start clear
+  for (int32_t k = p.have_hi; k < p.need_hi; ++k) {
+    const int32_t id = list_page(a, v, true, k);
+    if (id >= 0) clear_page(a, id, lane);
+  }
+  for (int32_t k = p.have_lo; k < p.need_lo; ++k) {
+    const int32_t id = list_page(a, v, false, k);
+    if (id >= 0) clear_page(a, id, lane);
+  }
+  __syncwarp();
+  hole_fill(a, v, false, rl, p.keep_lo, p.n_lo, buf, lane);   // K4V2 list
+  demote(a, v, dem, buf, lane);                               // appended after its survivors
+  __syncwarp();
+  hole_fill(a, v, true, rh, p.keep_hi, p.n_hi, buf, lane);    // K8V4 list (demoted slots read)
+  if (p.new_cls != DKV_CLASS_PRUNE) append_new(a, v, lane);
+  __syncwarp();
+  // vacated slots of the pages the lists keep
+  {
+    const int32_t end_hi = min(p.n_hi, p.need_hi * a.P);
+    for (int32_t s = n2_hi + lane; s < end_hi; s += 32) {
+      SlotAddr t;
+      if (slot_addr(a, v, true, s, t)) clear_slot(t, true);
+    }
+    const int32_t end_lo = min(p.n_lo, p.need_lo * 2 * a.P);
+    for (int32_t s = n2_lo + lane; s < end_lo; s += 32) {
+      SlotAddr t;
+      if (slot_addr(a, v, false, s, t)) clear_slot(t, false);
+    }
+  }
+  // tables: stage the kept K4V2 page ids, free the surplus, rewrite the row
+  const int32_t keep_lo_pages = min(p.have_lo, p.need_lo);
+  for (int32_t k = lane; k < keep_lo_pages; k += 32) stage[k] = v.fw[p.have_hi + k];
+  int32_t fj = 0;
+  const uint64_t tail = a.ws->tail + static_cast<uint64_t>(p.off_f);
+  for (int32_t k = p.need_hi + lane; k < p.have_hi; k += 32) {
+    const int32_t id = v.fw[k];
+    const int32_t j = fj + (k - p.need_hi);
+    if (id >= 0 && id < a.F) {
+      a.free_list[(tail + j) % static_cast<uint64_t>(a.F)] = id;
+      a.rev_unit[id] = -1;
+      a.rev_idx[id] = -1;
+      a.page_cls[id] = DKV_CLASS_PRUNE;
+    }
+  }
+  fj += max(0, p.have_hi - p.need_hi);
+  for (int32_t k = p.need_lo + lane; k < p.have_lo; k += 32) {
+    const int32_t id = v.fw[p.have_hi + k];
+    const int32_t j = fj + (k - p.need_lo);
+    if (id >= 0 && id < a.F) {
+      a.free_list[(tail + j) % static_cast<uint64_t>(a.F)] = id;
+      a.rev_unit[id] = -1;
+      a.rev_idx[id] = -1;
+      a.page_cls[id] = DKV_CLASS_PRUNE;
+    }
+  }
+  __syncwarp();
+  const int32_t old_tot = p.have_hi + p.have_lo, new_tot = p.need_hi + p.need_lo;
+  const int32_t k0 = p.need_hi == p.have_hi ? p.need_hi + keep_lo_pages : min(p.have_hi, p.need_hi);
+  const int32_t k1 = max(old_tot, new_tot);
+  int32_t *fw = a.fwd + v.u * a.pmax;
+  const int32_t unit_id = static_cast<int32_t>(a.unit_base + v.u);
+  for (int32_t k = k0 + lane; k < k1; k += 32) {
+    int32_t id = -1;
+    if (k < p.need_hi) {
+      id = new_page(a, v, k - p.have_hi);  // k >= have_hi here: kept K8V4 entries are not rewritten
+    } else if (k < new_tot) {
+      const int32_t j = k - p.need_hi;
+      id = j < keep_lo_pages ? stage[j] : new_page(a, v, v.xh + j - p.have_lo);
+    }
+    fw[k] = id;
+    if (id >= 0 && id < a.F) {
+      a.rev_unit[id] = unit_id;
+      a.rev_idx[id] = k;
+      a.page_cls[id] = k < p.need_hi ? DKV_CLASS_K8V4 : DKV_CLASS_K4V2;
+    }
+  }
+  if (lane == 0) reinterpret_cast<int4 *>(a.unit_hdr)[v.u] = make_int4(n2_hi, n2_lo, p.need_hi, p.need_lo);
+}
+
+__global__ void __launch_bounds__(32 * kMaxApplyWarps) k_apply(DecodeArgs a, int32_t hpc, int32_t words) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  DecPlan *plan_s = reinterpret_cast<DecPlan *>(smem);
+  uint32_t *bm = reinterpret_cast<uint32_t *>(plan_s + hpc);        // [hpc][3][words]
+  int32_t *buf = reinterpret_cast<int32_t *>(bm + 3 * hpc * words);  // [hpc][32]
+  int32_t *stage = buf + 32 * hpc;                                   // [hpc][pmax]
+  const int32_t r = blockIdx.y, l = blockIdx.z;
+  const int32_t h0 = blockIdx.x * hpc;
+  const int32_t nh = min(hpc, a.Hkv - h0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t err = *reinterpret_cast<volatile int32_t *>(&a.ws->err);
+  if (blockIdx.x == 0 && r == 0 && l == 0 && tid == 0) {
+    if (err != 0) {
+      atomicCAS(a.status, 0, err);
+    } else {
+      a.cursors[0] = a.ws->head + static_cast<uint64_t>(a.ws->dsum);
+      a.cursors[1] = a.ws->tail + static_cast<uint64_t>(a.ws->fsum);
+    }
+  }
+  int32_t ctx = a.ctx_lens[r], nw = a.new_lens[r];
+  ctx = min(max(ctx, 0), a.cap);
+  nw = min(max(nw, 0), a.cap - ctx);
+  const int32_t N = ctx + nw;
+  const int64_t u0 = (static_cast<int64_t>(l) * a.R + r) * a.Hkv;
+  if (err == 0) {
+    for (int i = tid; i < nh; i += blockDim.x) plan_s[i] = a.plan[u0 + h0 + i];
+    for (int i = tid; i < 3 * hpc * words; i += blockDim.x) bm[i] = 0u;
+  }
+  __syncthreads();
+
+  // marks -> final classes (or the old ones if the call failed), bitmaps
+  const int64_t blk = (static_cast<int64_t>(l) * a.R + r) * a.cap * a.Hkv;  // classes index of (l, r, 0, 0)
+  uint8_t *cls = a.classes + blk;
+  const int32_t nbytes = N * a.Hkv;
+  const int32_t nvec = (nbytes + 15) >> 4;
+  for (int32_t vi = tid; vi < nvec; vi += blockDim.x) {
+    const uint4 x = reinterpret_cast<const uint4 *>(cls)[vi];
+    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+    if (((x.x | x.y | x.z | x.w) & 0x80808080u) == 0u) continue;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const uint32_t b = (xw[q >> 2] >> (8 * (q & 3))) & 255u;
+      if ((b & 0x80u) == 0u) continue;
+      const int32_t idx = vi * 16 + q;
+      if (idx >= nbytes) continue;
+      const int32_t i = idx / a.Hkv, h = idx - i * a.Hkv;
+      if (h < h0 || h >= h0 + nh) continue;
+      const uint32_t old = (b >> 2) & 3u, cn = b & 3u;
+      const int64_t u = u0 + h;
+      if (err != 0) {  // revert
+        cls[idx] = static_cast<uint8_t>(old == 3u ? (a.ucnt[u].w & 0xff) : old);
+        continue;
+      }
+      cls[idx] = static_cast<uint8_t>(cn);
+      if (old == 3u) continue;  // the new token: handled from the plan
+      const DecPlan &p = plan_s[h - h0];
+      uint32_t *b3 = bm + 3 * (h - h0) * words;  // removed K8V4 slots, removed K4V2 slots, demoted positions
+      int32_t *so = a.slot_of + blk + idx;
+      const int32_t s = *so;
+      const int32_t n = old == DKV_CLASS_K8V4 ? p.n_hi : p.n_lo;
+      if (s < 0 || s >= n) {
+        atomicCAS(a.status, 0, DKV_E_INTERNAL);
+        continue;
+      }
+      atomicOr(b3 + (old == DKV_CLASS_K8V4 ? 0 : words) + (s >> 5), 1u << (s & 31));
+      if (cn == DKV_CLASS_K4V2) atomicOr(b3 + 2 * words + (i >> 5), 1u << (i & 31));
+      else *so = -1;  // pruned
+    }
+  }
+  __syncthreads();
+  if (err != 0 || warp >= nh) return;
+
+  UnitView v;
+  v.u = u0 + h0 + warp;
+  v.row0 = blk + h0 + warp;
+  v.ctx = ctx;
+  v.Hkv = a.Hkv;
+  v.fw = a.fwd + v.u * a.pmax;
+  v.p = plan_s[warp];
+  v.new_base = static_cast<int64_t>(a.ws->head % static_cast<uint64_t>(a.F)) + v.p.off_d;
+  v.xh = max(0, v.p.need_hi - v.p.have_hi);
+  uint32_t *b3 = bm + 3 * warp * words;
+  apply_unit(a, v, b3, b3 + words, b3 + 2 * words, buf + 32 * warp, stage + a.pmax * warp, lane);
+}
+
+// ------------------------------------------------------------------ k_index --
+
+// Classes and slot index of every position from the pages: one warp per unit.
+__global__ void __launch_bounds__(256) k_index(DecodeArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); u < a.U;
+       u += nwarps) {
+    const int32_t h = static_cast<int32_t>(u % a.Hkv);
+    const int64_t lr = u / a.Hkv;
+    const int32_t r = static_cast<int32_t>(lr % a.R);
+    const int32_t ctx = a.ctx_lens[r];
+    const int4 hdr = reinterpret_cast<const int4 *>(a.unit_hdr)[u];
+    const int32_t *fw = a.fwd + u * a.pmax;
+    const int64_t row0 = lr * a.cap * a.Hkv + h;
+    if (ctx < 0 || ctx > a.cap || hdr.z < 0 || hdr.w < 0 || hdr.z + hdr.w > a.pmax || hdr.x < 0 || hdr.y < 0 ||
+        hdr.x > hdr.z * a.P || hdr.y > hdr.w * 2 * a.P) {
+      if (lane == 0) atomicCAS(a.status, 0, DKV_E_INTERNAL);
+      continue;
+    }
+    for (int li = 0; li < 2; ++li) {
+      const bool hi = li == 0;
+      const int32_t n = hi ? hdr.x : hdr.y;
+      const int32_t per = hi ? a.P : 2 * a.P;
+      for (int32_t s = lane; s < n; s += 32) {
+        const int32_t id = fw[(hi ? 0 : hdr.z) + s / per];
+        if (id < 0 || id >= a.F) {
+          atomicCAS(a.status, 0, DKV_E_INTERNAL);
+          continue;
+        }
+        const int32_t pos = *reinterpret_cast<const int32_t *>(a.pages + static_cast<int64_t>(id) * 216 * a.P +
+                                                               208 * static_cast<int64_t>(a.P) + 4 * (s % per));
+        if (pos < 0 || pos >= ctx) {
+          atomicCAS(a.status, 0, DKV_E_INTERNAL);
+          continue;
+        }
+        a.classes[row0 + static_cast<int64_t>(pos) * a.Hkv] = hi ? DKV_CLASS_K8V4 : DKV_CLASS_K4V2;
+        a.slot_of[row0 + static_cast<int64_t>(pos) * a.Hkv] = s;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+size_t apply_smem(int32_t hpc, int32_t words, int32_t pmax) {
+  return sizeof(DecPlan) * hpc + sizeof(uint32_t) * 3 * hpc * words + sizeof(int32_t) * 32 * hpc +
+         sizeof(int32_t) * static_cast<size_t>(pmax) * hpc;
+}
+
+cudaError_t launch_reclass(const DecodeArgs &a, cudaStream_t s) {
+  const dim3 grid((a.cap + kReclassChunk - 1) / kReclassChunk, a.R, a.L);
+  if (a.G == 4) k_reclass<1><<<grid, kReclassThreads, 0, s>>>(a);
+  else if (a.G == 8) k_reclass<2><<<grid, kReclassThreads, 0, s>>>(a);
+  else k_reclass<0><<<grid, kReclassThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dscan(const DecodeArgs &a, int32_t npart, cudaStream_t s) {
+  k_dscan<<<npart, kDScanThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply(const DecodeArgs &a, int32_t hpc, int32_t words, cudaStream_t s) {
+  const size_t smem = apply_smem(hpc, words, a.pmax);
+  if (smem > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_apply, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid((a.Hkv + hpc - 1) / hpc, a.R, a.L);
+  k_apply<<<grid, 32 * hpc, smem, s>>>(a, hpc, words);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_index(const DecodeArgs &a, int grid, cudaStream_t s) {
+  k_index<<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dkv

@@ -139,6 +139,72 @@ __device__ __forceinline__ int find_segment(const int32_t *a, int n, int64_t x, 
   return lo;
 }
 
+// ---------------------------------------------------------------- decode --
+
+constexpr int kReclassChunk = 2048;   // positions per reclassification block
+constexpr int kMaxApplyWarps = 8;     // units (KV heads) per apply block, one warp each
+
+struct DecWsHeader {
+  int32_t err;       // first device-side error of this call (0 = none)
+  int32_t ticket;    // scan partition ticket counter
+  int32_t npart;     // scan partitions
+  int32_t pad0;
+  uint64_t head;     // free-list cursors when the call started
+  uint64_t tail;
+  int64_t dsum;      // new pages of the step
+  int64_t fsum;      // freed pages of the step
+  int64_t pad1[2];
+};
+
+// Per-unit plan of a generation step (48 bytes), written by the scan.
+struct __align__(16) DecPlan {
+  int32_t n_hi, n_lo, have_hi, have_lo;   // lists and pages before the step
+  int32_t keep_hi, keep_lo, dem, new_cls; // survivors, demoted count, class of the new token
+  int32_t need_hi, need_lo, off_d, off_f; // pages after the step, scan offsets (new, freed)
+};
+
+struct DecWsLayout {
+  size_t ucnt;   // int4 [U]: demoted, K8V4 pruned, K4V2 pruned, new-token word
+  size_t part;   // uint64 [npart]
+  size_t plan;   // DecPlan [U]
+  size_t reset;  // bytes zeroed at the start of a call (header, counters, partitions)
+  size_t bytes;
+  int32_t npart;
+};
+
+inline DecWsLayout dec_ws_layout(int64_t U) {
+  DecWsLayout w{};
+  w.npart = static_cast<int32_t>((U + 255) / 256);
+  size_t o = align256(sizeof(DecWsHeader));
+  w.ucnt = o; o = align256(o + 16 * static_cast<size_t>(U));
+  w.part = o; o = align256(o + sizeof(uint64_t) * w.npart);
+  w.reset = o;
+  w.plan = o; o = align256(o + sizeof(DecPlan) * static_cast<size_t>(U));
+  w.bytes = o;
+  return w;
+}
+
+struct DecodeArgs {
+  int32_t L, R, Hq, Hkv, G, P, pmax, cap, spin_limit;
+  int64_t F, U, unit_base;
+  float alpha_h, alpha_l;
+  const uint16_t *k_new, *v_new;
+  const float *sig_sum;
+  const int32_t *sig_cnt, *ctx_lens, *new_lens;
+  uint8_t *classes;
+  int32_t *slot_of;
+  int32_t *free_list;
+  uint64_t *cursors;
+  int32_t *rev_unit, *rev_idx;
+  uint8_t *page_cls, *pages;
+  int32_t *status;
+  int32_t *fwd, *unit_hdr;
+  DecWsHeader *ws;
+  int4 *ucnt;
+  uint64_t *part;
+  DecPlan *plan;
+};
+
 }  // namespace dkv
 
 // Launchers (defined in the kernel translation units).
@@ -152,4 +218,9 @@ cudaError_t launch_init_pool(const dkv_pool &p, cudaStream_t s);
 cudaError_t launch_dequant(const dkv_pool &p, const int32_t *ids, int32_t one_id, int32_t n,
                            float *k_out, float *v_out, int32_t *pos_out, cudaStream_t s);
 int pack_blocks_per_sm();
+cudaError_t launch_reclass(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_dscan(const DecodeArgs &a, int32_t npart, cudaStream_t s);
+cudaError_t launch_apply(const DecodeArgs &a, int32_t hpc, int32_t words, cudaStream_t s);
+cudaError_t launch_index(const DecodeArgs &a, int grid, cudaStream_t s);
+size_t apply_smem(int32_t hpc, int32_t words, int32_t pmax);
 }  // namespace dkv

@@ -65,6 +65,16 @@ class dkv_tables(ctypes.Structure):
                 ("unit_hdr", ctypes.c_void_p)]
 
 
+class dkv_decode_batch(ctypes.Structure):
+    _fields_ = [
+        ("L", ctypes.c_int32), ("R", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+        ("D", ctypes.c_int32), ("cap", ctypes.c_int32), ("unit_base", ctypes.c_int64),
+        ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("sig_sum", ctypes.c_void_p),
+        ("sig_cnt", ctypes.c_void_p), ("ctx_lens", ctypes.c_void_p), ("new_lens", ctypes.c_void_p),
+        ("classes", ctypes.c_void_p), ("slot_of", ctypes.c_void_p),
+    ]
+
+
 def load():
     """Load libdkv.so (raises if it was not built)."""
     global _lib
@@ -86,6 +96,10 @@ def load():
         "dkv_dequant_page": ([P(dkv_pool), i32, vp, vp, vp, vp], i32),
         "dkv_dequant_pages": ([P(dkv_pool), vp, i32, vp, vp, vp, vp], i32),
         "dkv_get_status": ([P(dkv_pool), vp], i32),
+        "dkv_decode_workspace_size": ([P(dkv_decode_batch), P(ctypes.c_size_t)], i32),
+        "dkv_decode_index": ([P(dkv_decode_batch), P(dkv_pool), P(dkv_tables), vp], i32),
+        "dkv_decode_step": ([P(dkv_decode_batch), P(dkv_params), P(dkv_pool), P(dkv_tables), vp, ctypes.c_size_t,
+                             vp], i32),
         "dkv_profiler_create": ([i32, P(vp)], i32),
         "dkv_profiler_read": ([vp, vp, i32], i32),
         "dkv_profiler_destroy": ([vp], i32),
@@ -264,3 +278,90 @@ class Compactor:
                 profiler=None, unit_base: int = 0) -> None:
         dkv_compact(self.batch(inp, unit_base), alpha_h, alpha_l, self.pool, self.tables, self.workspace,
                     stream=stream, spin_limit=spin_limit, profiler=profiler)
+
+
+# ------------------------------------------------------------------ decode --
+
+def dkv_decode_workspace_size(batch: dkv_decode_batch) -> int:
+    n = ctypes.c_size_t(0)
+    rc = load().dkv_decode_workspace_size(ctypes.byref(batch), ctypes.byref(n))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_decode_workspace_size")
+    return int(n.value)
+
+
+def dkv_decode_index(batch: dkv_decode_batch, pool: DevicePool, tables, stream=None) -> None:
+    pc, tc = pool.c(), tables.c()
+    rc = load().dkv_decode_index(ctypes.byref(batch), ctypes.byref(pc), ctypes.byref(tc), _stream(stream))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_decode_index")
+
+
+def dkv_decode_step(batch: dkv_decode_batch, alpha_h: float, alpha_l: float, pool: DevicePool, tables,
+                    workspace: torch.Tensor, stream=None, spin_limit: int = -1, profiler=None) -> None:
+    params = dkv_params(float(alpha_h), float(alpha_l), int(spin_limit), 0,
+                        None if profiler is None else profiler.handle)
+    pc, tc = pool.c(), tables.c()
+    rc = load().dkv_decode_step(ctypes.byref(batch), ctypes.byref(params), ctypes.byref(pc), ctypes.byref(tc),
+                                _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_decode_step")
+
+
+class _TableView:
+    """Tables of a contiguous run of units (pointer offsets into DeviceTables)."""
+
+    def __init__(self, t: DeviceTables, u0: int):
+        self.t, self.u0 = t, int(u0)
+
+    def c(self) -> dkv_tables:
+        return dkv_tables(_p(self.t.fwd) + 4 * self.u0 * self.t.pmax, self.t.pmax, 0,
+                          _p(self.t.unit_hdr) + 16 * self.u0)
+
+
+class Decoder:
+    """Device state of a generation workload: pool, unit tables (pmax =
+    ceil(cap / P) + 1), capacity-strided classes and slot index, workspace.
+    prefill_layer() fills one layer's units with dkv_compact; index() derives
+    classes and slot_of from the pages; step() runs dkv_decode_step."""
+
+    def __init__(self, L: int, R: int, Hq: int, Hkv: int, cap: int, P: int, F: int, device="cuda"):
+        self.L, self.R, self.Hq, self.Hkv, self.cap, self.P = L, R, Hq, Hkv, cap, P
+        self.U = L * R * Hkv
+        self.pmax = -(-cap // P) + 1
+        self.device = torch.device(device)
+        self.pool = DevicePool(F, P, device)
+        self.tables = DeviceTables(self.U, self.pmax, device)
+        rows = L * R * cap * Hkv
+        self.classes = torch.zeros(rows, dtype=torch.uint8, device=device)
+        self.slot_of = torch.full((rows,), -1, dtype=torch.int32, device=device)
+        self.workspace = torch.empty(dkv_decode_workspace_size(self.batch({})), dtype=torch.uint8, device=device)
+        dkv_init_pool(self.pool)
+        self._pre_ws = None
+
+    def batch(self, d: dict) -> dkv_decode_batch:
+        g = d.get
+        return dkv_decode_batch(self.L, self.R, self.Hq, self.Hkv, 128, self.cap, 0, _p(g("k_new")), _p(g("v_new")),
+                                _p(g("sig_sum")), _p(g("sig_cnt")), _p(g("ctx_lens")), _p(g("new_lens")),
+                                _p(self.classes), _p(self.slot_of))
+
+    def prefill_layer(self, inp: dict, layer: int, max_len: int, alpha_h: float, alpha_l: float,
+                      stream=None) -> None:
+        """dkv_compact of one layer's prefill inputs (L = 1) into this pool,
+        units of layer `layer` (unit_base and table rows offset)."""
+        T = int(inp["T"])
+        cls = torch.empty(max(T * self.Hkv, 1), dtype=torch.uint8, device=self.device)
+        b = make_batch(inp, cls, max_len, unit_base=layer * self.R * self.Hkv)
+        need = dkv_workspace_size(b)
+        if self._pre_ws is None or self._pre_ws.numel() < need:
+            self._pre_ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        dkv_compact(b, alpha_h, alpha_l, self.pool, _TableView(self.tables, layer * self.R * self.Hkv),
+                    self._pre_ws, stream=stream)
+
+    def index(self, ctx_lens: torch.Tensor, stream=None) -> None:
+        dkv_decode_index(self.batch({"ctx_lens": ctx_lens}), self.pool, self.tables, stream=stream)
+
+    def step(self, d: dict, alpha_h: float, alpha_l: float, stream=None, spin_limit: int = -1,
+             profiler=None) -> None:
+        dkv_decode_step(self.batch(d), alpha_h, alpha_l, self.pool, self.tables, self.workspace, stream=stream,
+                        spin_limit=spin_limit, profiler=profiler)

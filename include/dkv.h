@@ -181,6 +181,83 @@ int32_t dkv_dequant_page(const dkv_pool *pool, int32_t page_id, float *k_out, fl
 int32_t dkv_dequant_pages(const dkv_pool *pool, const int32_t *page_ids, int32_t n,
                           float *k_out, float *v_out, int32_t *pos_out, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Generation (decode) step.  DiffKV review, Referee Report, major comment 2
+ * (Algorithm 1 classifies tokens as they age in the generation phase;
+ * demotion and pruning are irreversible), with "What carries the argument"
+ * and "Core claim" for classes, unified pages and the page allocator.
+ *
+ * The context axis of a decode batch is capacity-strided: position i of
+ * request r is token row r * cap + i of sig_sum, sig_cnt, classes and
+ * slot_of.  Units, pages and tables are those of dkv_compact (a prefill with
+ * tables of the same pmax leaves a valid starting state).
+ *
+ * One step, with N = ctx_lens[r] + new_lens[r]:
+ *   - every live token's class becomes min(old class, classify(score, N));
+ *     the new token (position ctx_lens[r], when new_lens[r] = 1) is
+ *     classified as in prefill;
+ *   - per unit, each list (K8V4 slots, K4V2 slots) drops its removed tokens;
+ *     with `keep` survivors, those in slots >= keep move, in ascending slot
+ *     order, into the holes below keep, in ascending order (bytes copied);
+ *   - tokens demoted K8V4 -> K4V2 are appended to the K4V2 list in ascending
+ *     position order, requantised (4-bit K, 2-bit V, the quantiser above)
+ *     from their dequantised values x = fma(q, s, z); then the new token is
+ *     appended to its list (a pruned new token is dropped);
+ *   - each list keeps its first min(have, need) pages, need = ceil(n / P)
+ *     (K8V4) or ceil(n / 2P) (K4V2); new pages come from free-list slots
+ *     head + off_u + k (mod F), off_u the exclusive prefix sum over units of
+ *     their new pages, a unit's K8V4 pages first; surplus pages are appended
+ *     at the tail in (unit, list, page index) order with rev -1, class 0;
+ *   - unused slots of the kept pages are cleared; head and tail advance by
+ *     the new and freed page counts; fwd / rev / page_cls / unit_hdr follow.
+ * ------------------------------------------------------------------------ */
+typedef struct dkv_decode_batch {
+  int32_t L, R, Hq, Hkv, D;  /* as dkv_batch; D = 128 */
+  int32_t cap;               /* positions reserved per request; a multiple of 16 */
+  int64_t unit_base;         /* global id of unit 0 of this call */
+  const void *k_new;         /* bf16 [L][R][Hkv][128]: each request's new token (16-byte aligned) */
+  const void *v_new;         /* bf16 [L][R][Hkv][128] */
+  const float *sig_sum;      /* fp32 [L][R * cap][Hq] (16-byte aligned) */
+  const int32_t *sig_cnt;    /* int32 [R * cap]: scores summed for each position */
+  const int32_t *ctx_lens;   /* int32 [R]: positions 0 .. ctx-1 are held; device memory */
+  const int32_t *new_lens;   /* int32 [R]: 0 or 1 new token at position ctx */
+  uint8_t *classes;          /* in/out uint8 [L][R * cap][Hkv] (16-byte aligned): DKV_CLASS_* of
+                                positions < ctx (+ the new one after the step); other bytes are
+                                not read except the new position's, which the step overwrites */
+  int32_t *slot_of;          /* in/out int32 [L][R * cap][Hkv]: slot of each held token in its
+                                class list, -1 when pruned; built by dkv_decode_index and
+                                maintained by dkv_decode_step */
+} dkv_decode_batch;
+
+/* Workspace bytes of dkv_decode_step for this shape (host only). */
+int32_t dkv_decode_workspace_size(const dkv_decode_batch *b, size_t *bytes);
+
+/* Derive classes and slot_of of positions 0 .. ctx_lens[r]-1 from the pages
+ * and tables (after a prefill, or to rebuild them).  Reads the shape,
+ * ctx_lens, the tables and the pages; k_new, v_new, sig_sum, sig_cnt and
+ * new_lens are not used (may be NULL).  Every byte of classes
+ * and every entry of slot_of is first reset (0 and -1), then each used slot
+ * of each unit's lists writes its position's class and slot.  A position or
+ * page id out of range in the pages is reported as DKV_E_INTERNAL in the
+ * status word.  Asynchronous; allocates nothing. */
+int32_t dkv_decode_index(const dkv_decode_batch *b, const dkv_pool *pool, const dkv_tables *t,
+                         void *stream);
+
+/* One generation step (semantics above), asynchronous.  workspace: device,
+ * 256-byte aligned, >= dkv_decode_workspace_size bytes, scratch.  The caller
+ * advances ctx_lens by new_lens after a successful step.  Device-side errors
+ * (read with dkv_get_status): DKV_E_LENS (ctx + new > cap, new not 0 or 1, a
+ * list needing more than pmax pages), DKV_E_RANGE (a kept new token with a
+ * non-finite value or one above 65504), DKV_E_NOMEM (new pages > free
+ * pages), DKV_E_TIMEOUT (scan wait), DKV_E_INTERNAL (classes, headers,
+ * slot_of or pages contradict one another).  On LENS, RANGE, NOMEM and
+ * TIMEOUT, and on INTERNAL found before any page is touched, the step
+ * changes nothing (classes restored); INTERNAL found while moving slots
+ * leaves the state undefined.  With dkv_params.profiler the five intervals
+ * are: counter reset, reclassification, page scan, apply, (empty). */
+int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dkv_pool *pool,
+                        const dkv_tables *t, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Synchronise `stream`, return the pool's device status word (DKV_OK or the
  * first device-side error since the last read) and clear it. */
 int32_t dkv_get_status(const dkv_pool *pool, void *stream);

@@ -97,3 +97,39 @@ def test_compact_rejects_bad_arguments_without_launching(lib):
         assert call(**c) == libdkv.DKV_E_INVAL, c
     assert lib.dkv_dequant_page(ctypes.byref(_pool()), 64, 256, 256, 256, None) == libdkv.DKV_E_INVAL
     assert lib.dkv_init_pool(ctypes.byref(_pool(pages=8193)), None) == libdkv.DKV_E_INVAL
+
+
+def _dbatch(**kw):
+    b = dict(L=2, R=3, Hq=8, Hkv=2, D=128, cap=64, unit_base=0, k_new=256, v_new=512, sig_sum=1024,
+             sig_cnt=2048, ctx_lens=4096, new_lens=8192, classes=16384, slot_of=32768)
+    b.update(kw)
+    return libdkv.dkv_decode_batch(**b)
+
+
+def test_decode_rejects_bad_arguments_without_launching(lib):
+    assert libdkv.dkv_decode_workspace_size(_dbatch()) > 0
+    for bad in (dict(cap=60), dict(cap=0), dict(D=64), dict(Hq=7), dict(R=0)):
+        with pytest.raises(libdkv.DkvError):
+            libdkv.dkv_decode_workspace_size(_dbatch(**bad))
+    t = libdkv.dkv_tables(256, 6, 0, 512)
+    params = libdkv.dkv_params(1.0, 0.2, -1, 0, None)
+
+    def call(b=None, p=None, pool=None, tab=None, wsp=1 << 20, wsb=1 << 30):
+        return lib.dkv_decode_step(ctypes.byref(b or _dbatch()), ctypes.byref(p or params),
+                                   ctypes.byref(pool or _pool()), ctypes.byref(tab or t), wsp, wsb, None)
+
+    cases = [
+        dict(b=_dbatch(cap=40)),                                  # not a multiple of 16
+        dict(b=_dbatch(classes=16385)),                           # misaligned classes
+        dict(b=_dbatch(slot_of=None)),
+        dict(b=_dbatch(sig_sum=1028)),                            # misaligned sig_sum
+        dict(p=libdkv.dkv_params(0.1, 0.2, -1, 0, None)),
+        dict(pool=_pool(P=7)),
+        dict(tab=libdkv.dkv_tables(256, 1, 0, 512)),
+        dict(wsp=(1 << 20) + 8),
+        dict(wsb=64),
+    ]
+    for c in cases:
+        assert call(**c) == libdkv.DKV_E_INVAL, c
+    assert lib.dkv_decode_index(ctypes.byref(_dbatch(ctx_lens=None)), ctypes.byref(_pool()), ctypes.byref(t),
+                                None) == libdkv.DKV_E_INVAL
