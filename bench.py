@@ -327,12 +327,308 @@ def run_native(a):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- decode ----
+
+DECODE_SLACK = 1 << 16   # free pages between the head after prefill and the next wrap of the ring
+
+
+def decode_cap(w, steps: int) -> int:
+    return -(-(max(w.lens) + steps) // 16) * 16
+
+
+def decode_prefill(w, dec, dev, seed: int, cap: int, head_offset: int = 0):
+    """Per-layer prefill of the decode workload into dec's pool (dkv_compact,
+    one layer per call) and the capacity-strided significance sums and
+    counts the steps start from.  head_offset rotates the fresh ring (free
+    list slot i holds page i, cursors {head_offset, head_offset + F})."""
+    import torch
+    from differentiated_kv_cache_dkv_gb300 import libdkv
+    from differentiated_kv_cache_dkv_gb300 import workloads as W
+
+    libdkv.dkv_init_pool(dec.pool)
+    if head_offset:
+        dec.pool.cursors.copy_(torch.tensor([head_offset, head_offset + dec.pool.F], dtype=torch.int64))
+    req, pos = W._positions(w, dev)
+    dst = req * cap + pos
+    sig = torch.zeros((w.L, w.R * cap, w.Hq), dtype=torch.float32, device=dev)
+    cnt = torch.zeros(w.R * cap, dtype=torch.int32, device=dev)
+    cnt0 = W.sig_cnt_prefill(w, dev)
+    cnt[dst] = cnt0
+    lens = torch.tensor(w.lens, dtype=torch.int32, device=dev)
+    for l in range(w.L):
+        k = W.make_kv_layer(w, seed, l, 0, dev)[None]
+        v = W.make_kv_layer(w, seed, l, 1, dev)[None]
+        s = W.make_sig_layer(w, seed, l, dev)
+        sig[l, dst] = s
+        layer = {"L": 1, "R": w.R, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "k": k, "v": v, "sig_sum": s[None].contiguous(),
+                 "sig_cnt": cnt0, "lens": lens}
+        dec.prefill_layer(layer, l, max(w.lens), w.alpha_h, w.alpha_l)
+        del k, v, s, layer
+    st = libdkv.dkv_get_status(dec.pool)
+    assert st == libdkv.DKV_OK, libdkv.status_string(st)
+    ctx = {"L": w.L, "R": w.R, "Hq": w.Hq, "Hkv": w.Hkv, "cap": cap, "sig_sum": sig, "sig_cnt": cnt,
+           "ctx_lens": lens.clone()}
+    dec.index(ctx["ctx_lens"])
+    st = libdkv.dkv_get_status(dec.pool)
+    assert st == libdkv.DKV_OK, libdkv.status_string(st)
+    return ctx
+
+
+def decode_setup(w, dev, seed: int, total_steps: int):
+    """Decoder state after the prefill, with the pool sized so that the ring's
+    head wraps within the run: a first prefill in a worst-case pool measures
+    the pages it takes, the second starts the ring DECODE_SLACK pages before
+    its end."""
+    import torch
+    from differentiated_kv_cache_dkv_gb300 import libdkv
+
+    cap = decode_cap(w, total_steps)
+    dec = libdkv.Decoder(w.L, w.R, w.Hq, w.Hkv, cap, w.P, w.pool_pages, device=dev)
+    decode_prefill(w, dec, dev, seed, cap)
+    used = int(dec.pool.cursors[0])
+    F = dec.pool.F
+    offset = (F - used - DECODE_SLACK) % F
+    torch.cuda.empty_cache()
+    ctx = decode_prefill(w, dec, dev, seed, cap, head_offset=offset)
+    return dec, ctx, cap, used
+
+
+class DecodeOracleSample:
+    """The oracle's generation step on a bounded sample of the decode
+    workload: layer 0 of its first n_req requests, prefilled by the oracle
+    (untimed) and then stepped with the same seeded updates."""
+
+    def __init__(self, w, n_req: int = 16):
+        import dataclasses
+
+        self.w = dataclasses.replace(w, L=1, lens=list(w.lens[:n_req]))
+        self.max_steps = int(w.extra.get("steps", 100))  # the workload's own run length
+        self.steps = 0
+        self._fresh()
+
+    def _fresh(self):
+        from tests.decode_helpers import HostDecode
+
+        self.hd = HostDecode(self.w, decode_cap(self.w, self.max_steps))
+        self.local = 0
+
+    def step(self):
+        """One timed oracle step: (seconds, live token-rows).  Every
+        max_steps steps the sample starts again from its prefill (untimed)."""
+        from differentiated_kv_cache_dkv_gb300 import workloads as W
+
+        if self.local == self.max_steps:
+            self._fresh()
+        upd = W.decode_update_inputs(self.w, self.hd.ctx, self.local)
+        live = int((self.hd.ctx["ctx_lens"] + upd["new_lens"]).sum()) * self.w.Hkv
+        t = time.perf_counter()
+        st = self.hd.step(upd)
+        dt = time.perf_counter() - t
+        assert st == 0, st
+        self.steps += 1
+        self.local += 1
+        return dt, live
+
+
+def decode_oracle_sample(w, seconds: float):
+    """(live token-rows/s, steps, rows per step, seconds) of the oracle stepped
+    until `seconds` of step time."""
+    smp = DecodeOracleSample(w)
+    t_total, rows = 0.0, 0
+    while t_total < seconds or smp.steps == 0:
+        dt, live = smp.step()
+        t_total += dt
+        rows += live
+    return rows / t_total, smp.steps, rows / smp.steps, t_total
+
+
+def run_native_decode(a):
+    import torch
+
+    from differentiated_kv_cache_dkv_gb300 import libdkv
+    from differentiated_kv_cache_dkv_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    libdkv.load()
+    w = W.get(a.workload)
+    dev = torch.device("cuda", local)
+    total = a.warmup + a.steps + a.e2e_steps + 1
+    dec, ctx, cap, used = decode_setup(w, dev, W.SEED_BASE + 1000 * rank, total)
+    F = dec.pool.F
+    stream = torch.cuda.current_stream()
+    head0 = int(dec.pool.cursors[0])
+
+    def inputs(step):
+        upd = W.decode_update_inputs(w, ctx, step, device=dev)
+        return upd, {"k_new": upd["k_new"], "v_new": upd["v_new"], "sig_sum": ctx["sig_sum"],
+                     "sig_cnt": ctx["sig_cnt"], "ctx_lens": ctx["ctx_lens"], "new_lens": upd["new_lens"]}
+
+    step_no = 0
+    for _ in range(a.warmup):
+        upd, d = inputs(step_no)
+        dec.step(d, w.alpha_h, w.alpha_l)
+        ctx["ctx_lens"] += upd["new_lens"]
+        step_no += 1
+    assert libdkv.dkv_get_status(dec.pool) == libdkv.DKV_OK
+
+    prof = libdkv.Profiler(a.steps)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    live_rows, new_rows = 0, 0
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(a.steps):
+        upd, d = inputs(step_no)
+        live_rows += int((ctx["ctx_lens"] + upd["new_lens"]).sum()) * w.L * w.Hkv
+        new_rows += int(upd["new_lens"].sum()) * w.L * w.Hkv
+        evs[i][0].record(stream)
+        dec.step(d, w.alpha_h, w.alpha_l, profiler=prof)
+        evs[i][1].record(stream)
+        ctx["ctx_lens"] += upd["new_lens"]
+        step_no += 1
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    st = libdkv.dkv_get_status(dec.pool)
+    assert st == libdkv.DKV_OK, libdkv.status_string(st)
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
+    kt = prof.read()
+    prof.close()
+    names = ("reset", "k_reclass", "k_dscan", "k_apply")
+    kernel_ms = {n: statistics.mean(c[i] for c in kt) for i, n in enumerate(names)}
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = world * live_rows / (ms_max / 1000.0)
+
+    peak, peak_kind = _peaks()
+    tok_per_step = live_rows / a.steps / (w.L * w.Hkv)
+    rc_bytes = w.L * tok_per_step * (w.Hq * 4 + w.Hkv) + tok_per_step * 4
+    rc_ms = kernel_ms["k_reclass"]
+    rc_gbs = rc_bytes / (rc_ms / 1000.0) / 1e9
+    step_gbs = rc_bytes / (ms_max / a.steps / 1000.0) / 1e9
+
+    e2e = None
+    if a.e2e_steps > 0:
+        # end to end: this step's inputs (new K / V, significance sums and
+        # counts, lengths) copied from pinned host buffers, then the step, then
+        # the unit headers and cursors read back
+        upd, d = inputs(step_no)
+        host = {"k_new": upd["k_new"].cpu().pin_memory(), "v_new": upd["v_new"].cpu().pin_memory(),
+                "sig_sum": ctx["sig_sum"].cpu().pin_memory(), "sig_cnt": ctx["sig_cnt"].cpu().pin_memory(),
+                "ctx_lens": ctx["ctx_lens"].cpu().pin_memory(), "new_lens": upd["new_lens"].cpu().pin_memory()}
+        out_hdr = torch.empty(dec.tables.unit_hdr.shape, dtype=torch.int32).pin_memory()
+        out_cur = torch.empty(2, dtype=torch.int64).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in host.values())
+        d2h = out_hdr.numel() * 4 + 16
+        te = 0.0
+        e_rows = 0
+        for i in range(a.e2e_steps):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            s0.record(stream)
+            for k_, x in host.items():
+                d[k_].copy_(x, non_blocking=True)
+            dec.step(d, w.alpha_h, w.alpha_l)
+            out_hdr.copy_(dec.tables.unit_hdr, non_blocking=True)
+            out_cur.copy_(dec.pool.cursors, non_blocking=True)
+            s1.record(stream)
+            torch.cuda.synchronize()
+            te += s0.elapsed_time(s1)
+            e_rows += int((ctx["ctx_lens"] + upd["new_lens"]).sum()) * w.L * w.Hkv
+            ctx["ctx_lens"] += upd["new_lens"]
+            step_no += 1
+            if i + 1 < a.e2e_steps:
+                upd, d = inputs(step_no)
+                for k_ in host:
+                    host[k_].copy_(d[k_])
+        assert libdkv.dkv_get_status(dec.pool) == libdkv.DKV_OK
+        e2e = {"value": world * e_rows / (te / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": a.e2e_steps}
+        del host
+    head1 = int(dec.pool.cursors[0])
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        v, nsteps, rrows, tt = decode_oracle_sample(w, a.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"layer 0 of the first 16 requests of {a.workload} ({rrows:.0f} live token-rows per "
+                         f"step) x {nsteps} steps, single-threaded, {tt:.1f} s"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms_max / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": a.workload, "layers": w.L, "requests": w.R, "context": "uniform 2048..8192",
+                       "Hq": w.Hq, "Hkv": w.Hkv, "page_tokens": w.P, "alpha_h": w.alpha_h, "alpha_l": w.alpha_l,
+                       "cap": cap, "updates": "0.5% pruned + 0.5% demoted per (layer, request, KV head, token)",
+                       "timed": "dkv_decode_step only (significance updates between steps untimed)",
+                       "l2": "significance sums (%.1f GB) larger than L2" % (w.L * w.R * cap * w.Hq * 4 / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "k_reclass", "achieved": rc_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": rc_gbs / peak, "peak_kind": peak_kind, "traffic": None,
+                         "algorithmic_bytes": rc_bytes, "ms": rc_ms},
+            "step_hbm": {"achieved": step_gbs, "frac": step_gbs / peak, "bytes": rc_bytes},
+            "kernels_ms": kernel_ms,
+            "new_token_rows_per_s": world * new_rows / (ms_max / 1000.0),
+            "pool": {"F": F, "prefill_pages": used, "head_start": head0, "head_end": head1,
+                     "wraps": head1 // F - head0 // F},
+            "gpu_launches": a.steps * 4,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference_decode(a):
+    """CPU oracle arm of the decode workload: each step is one oracle
+    generation step on layer 0 of the first 16 requests."""
+    from differentiated_kv_cache_dkv_gb300 import workloads as W
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    w = W.get(a.workload)
+    smp = DecodeOracleSample(w)
+    for _ in range(a.warmup):
+        smp.step()
+    total, rows = 0.0, 0
+    for _ in range(a.steps):
+        dt, live = smp.step()
+        total += dt
+        rows += live
+    value = rows / total
+    sample = "one generation step on layer 0 of the first 16 requests per step, single-threaded oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": 1000.0 * total / a.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": a.workload, "layers": w.L, "requests": w.R, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "page_tokens": w.P},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def main():
     a = _args()
+    decode = a.workload == "decode"
     if a.impl == "reference":
-        run_reference(a)
+        run_reference_decode(a) if decode else run_reference(a)
     else:
-        run_native(a)
+        run_native_decode(a) if decode else run_native(a)
 
 
 if __name__ == "__main__":

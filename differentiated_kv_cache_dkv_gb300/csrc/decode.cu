@@ -50,6 +50,7 @@ namespace {
 constexpr int kReclassThreads = 512;
 constexpr int kReclassRows = 4;           // rows in flight per thread
 constexpr int kDScanThreads = 256;        // one unit per thread
+constexpr int kMarkCap = 256;             // listed marks per unit in the apply block
 
 __device__ __forceinline__ void st_release(uint64_t *p, uint64_t v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -486,9 +487,17 @@ __device__ void hole_fill(const DecodeArgs &a, const UnitView &v, bool hi, const
   __syncwarp();
 }
 
-// The per-token quantiser on fp32 values spread over `lanes` lanes (each
-// holding 4 or 16 channels): exact min / max (a zero extreme taken as +0),
-// fp16 scale and zero, codes by IEEE division and round-half-to-even.
+// The per-token quantiser on fp32 values spread over kGroup lanes (kPer
+// channels each): exact min / max (a zero extreme taken as +0), fp16 scale
+// and zero, q = clamp(rint_even(RN(x - z) / s), 0, n).
+//
+// The code of an element is read from y = RN(d * RN(1/s) + 1536.5), d =
+// RN(x - z): y lies on a grid of 2^-13 and bits(y) >> 13 holds floor(t + 0.5)
+// for t = y - 1536.5.  |d * RN(1/s) - d / s| <= 2^-16 for codes below 256, far
+// inside half the grid step, so when y is not an integer (t not a
+// half-integer) floor(t + 0.5) is the rounded quotient of the definition;
+// an integer y (low 13 bits zero) is re-evaluated with the IEEE division, as
+// is every element of a row whose codes would need clamping.
 template <int kPer, int kGroup>
 __device__ __forceinline__ void quant_vals(const float (&x)[kPer], int nmax, uint32_t (&q)[kPer], uint16_t &s16o,
                                            uint16_t &z16o) {
@@ -505,22 +514,30 @@ __device__ __forceinline__ void quant_vals(const float (&x)[kPer], int nmax, uin
   }
   mn = __fadd_rn(mn, 0.0f);
   mx = __fadd_rn(mx, 0.0f);
-  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(nmax));
+  const float nf = static_cast<float>(nmax);
+  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), nf);
   uint16_t s16 = __half_as_ushort(__float2half_rn(s32));
   if (mx > mn && s16 == 0) s16 = 1;
   const uint16_t z16 = __half_as_ushort(__float2half_rn(mn));
   const float s = __half2float(__ushort_as_half(s16));
   const float z = __half2float(__ushort_as_half(z16));
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    q[i] = 0u;
-    if (s != 0.0f) {
-      const float t = rintf(__fdiv_rn(__fsub_rn(x[i], z), s));
-      q[i] = static_cast<uint32_t>(fminf(fmaxf(t, 0.0f), static_cast<float>(nmax)));
-    }
-  }
   s16o = s16;
   z16o = z16;
+  if (s == 0.0f) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) q[i] = 0u;
+    return;
+  }
+  const float r = __frcp_rn(s);
+  const bool clamp_row = __fmul_rn(__fsub_rn(mn, z), r) < -0.25f || __fmul_rn(__fsub_rn(mx, z), r) > nf + 0.25f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const float d = __fsub_rn(x[i], z);
+    const uint32_t bits = __float_as_uint(__fmaf_rn(d, r, 1536.5f));
+    q[i] = (bits >> 13) & 255u;
+    if (clamp_row || (bits & 8191u) == 0u)
+      q[i] = static_cast<uint32_t>(fminf(fmaxf(rintf(__fdiv_rn(d, s)), 0.0f), nf));
+  }
 }
 
 template <int kPer>
@@ -541,28 +558,38 @@ __device__ void demote(const DecodeArgs &a, const UnitView &v, const uint32_t *d
   for (;;) {
     const int nd = next_bits(dem, cur, v.ctx, true, buf, lane);
     if (nd == 0) break;
+    // one lane per demoted token: its K8V4 slot, then the ids of its source
+    // and destination pages (two rounds of loads for up to 32 tokens)
+    int32_t my_hs = -1, my_src = -1, my_dst = -1;
+    if (lane < nd) my_hs = a.slot_of[v.row0 + static_cast<int64_t>(buf[lane]) * v.Hkv];
+    if (lane < nd) {
+      if (my_hs >= 0 && my_hs < v.p.n_hi) my_src = list_page(a, v, true, my_hs / a.P);
+      my_dst = list_page(a, v, false, (v.p.keep_lo + k + lane) / (2 * a.P));
+    }
     for (int g = 0; g < nd; g += 4) {
       const int j = g + grp;
       const bool act = j < nd;
-      int32_t pos = 0, hs = -1;
-      SlotAddr src{}, dst{};
-      bool ok = false;
-      if (act) {
-        pos = buf[j];
-        hs = a.slot_of[v.row0 + static_cast<int64_t>(pos) * v.Hkv];
-        ok = hs >= 0 && hs < v.p.n_hi && slot_addr(a, v, true, hs, src) &&
-             slot_addr(a, v, false, v.p.keep_lo + k + j, dst);
-        if (ok && *reinterpret_cast<const int32_t *>(src.pos) != pos) ok = false;
-        if (!ok && t == 0) atomicCAS(a.status, 0, DKV_E_INTERNAL);
-      }
+      const int32_t hs = __shfl_sync(0xffffffffu, my_hs, j & 31);
+      const int32_t sid = __shfl_sync(0xffffffffu, my_src, j & 31);
+      const int32_t did = __shfl_sync(0xffffffffu, my_dst, j & 31);
+      const int32_t pos = act ? buf[j] : 0;
+      bool ok = act && hs >= 0 && hs < v.p.n_hi && sid >= 0 && did >= 0;
+      const int64_t ss = hs % P, ds = (v.p.keep_lo + k + j) % (2 * P);
+      const uint8_t *spg = a.pages + static_cast<int64_t>(sid) * 216 * P;
+      uint8_t *dpg = a.pages + static_cast<int64_t>(did) * 216 * P;
+      SlotAddr dst{dpg + 64 * ds, dpg + 128 * P + 32 * ds, dpg + 192 * P + 8 * ds, dpg + 208 * P + 4 * ds};
       uint4 kc = make_uint4(0u, 0u, 0u, 0u);
       uint2 vc = make_uint2(0u, 0u);
       uint2 meta = make_uint2(0u, 0u);
+      int32_t spos = -1;
       if (ok) {
-        kc = reinterpret_cast<const uint4 *>(src.k)[t];  // channels 16t .. 16t+15, 8-bit
-        vc = reinterpret_cast<const uint2 *>(src.v)[t];  // channels 16t .. 16t+15, 4-bit
-        meta = *reinterpret_cast<const uint2 *>(src.meta);
+        kc = reinterpret_cast<const uint4 *>(spg + 128 * ss)[t];            // channels 16t .. 16t+15, 8-bit
+        vc = reinterpret_cast<const uint2 *>(spg + 128 * P + 64 * ss)[t];   // channels 16t .. 16t+15, 4-bit
+        meta = *reinterpret_cast<const uint2 *>(spg + 192 * P + 8 * ss);
+        spos = *reinterpret_cast<const int32_t *>(spg + 208 * P + 4 * ss);
       }
+      if (ok && spos != pos) ok = false;
+      if (act && !ok && t == 0) atomicCAS(a.status, 0, DKV_E_INTERNAL);
       const float ks = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.x & 0xffffu)));
       const float kz = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.x >> 16)));
       const float vs = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.y & 0xffffu)));
@@ -722,12 +749,63 @@ __device__ void apply_unit(const DecodeArgs &a, UnitView &v, uint32_t *rh, uint3
   if (lane == 0) reinterpret_cast<int4 *>(a.unit_hdr)[v.u] = make_int4(n2_hi, n2_lo, p.need_hi, p.need_lo);
 }
 
-__global__ void __launch_bounds__(32 * kMaxApplyWarps) k_apply(DecodeArgs a, int32_t hpc, int32_t words) {
+// Bits of one removed token: its slot in the removed-slot bitmap of its list,
+// its position in the demoted bitmap, or its index entry cleared if pruned.
+// mark = position << 4 | old class << 2 | new class.
+__device__ __forceinline__ void mark_slot(const DecodeArgs &a, uint32_t mark, int64_t row0, const DecPlan &p,
+                                          uint32_t *b3, int32_t words) {
+  const int32_t i = static_cast<int32_t>(mark >> 4);
+  const uint32_t old = (mark >> 2) & 3u, cn = mark & 3u;
+  int32_t *so = a.slot_of + row0 + static_cast<int64_t>(i) * a.Hkv;
+  const int32_t s = *so;
+  const int32_t n = old == DKV_CLASS_K8V4 ? p.n_hi : p.n_lo;
+  if (s < 0 || s >= n) {
+    atomicCAS(a.status, 0, DKV_E_INTERNAL);
+    return;
+  }
+  atomicOr(b3 + (old == DKV_CLASS_K8V4 ? 0 : words) + (s >> 5), 1u << (s & 31));
+  if (cn == DKV_CLASS_K4V2) atomicOr(b3 + 2 * words + (i >> 5), 1u << (i & 31));
+  else *so = -1;  // pruned
+}
+
+// Marks of one 16-byte vector of class bytes: the final class (or the old one
+// when the call failed) is written back and each removed token is listed
+// for its unit's warp (or handled here if the list is full).  Rare, so out of
+// line.
+__device__ __noinline__ void take_marks(const DecodeArgs &a, uint4 x, int32_t vi, int32_t nbytes, int32_t h0,
+                                        int32_t nh, int32_t err, int64_t u0, int64_t blk, const DecPlan *plan_s,
+                                        uint32_t *bm, int32_t words, uint32_t *mk, int32_t *mk_n) {
+  uint8_t *cls = a.classes + blk;
+  const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+  for (int e = 0; e < 16; ++e) {
+    const uint32_t b = (xw[e >> 2] >> (8 * (e & 3))) & 255u;
+    if ((b & 0x80u) == 0u) continue;
+    const int32_t idx = vi * 16 + e;
+    if (idx >= nbytes) continue;
+    const int32_t i = idx / a.Hkv, h = idx - i * a.Hkv;
+    if (h < h0 || h >= h0 + nh) continue;
+    const uint32_t old = (b >> 2) & 3u, cn = b & 3u;
+    if (err != 0) {  // revert
+      cls[idx] = static_cast<uint8_t>(old == 3u ? (a.ucnt[u0 + h].w & 0xff) : old);
+      continue;
+    }
+    cls[idx] = static_cast<uint8_t>(cn);
+    if (old == 3u) continue;  // the new token: handled from the plan
+    const uint32_t mark = (static_cast<uint32_t>(i) << 4) | (old << 2) | cn;
+    const int32_t k = atomicAdd(&mk_n[h - h0], 1);
+    if (k < kMarkCap) mk[(h - h0) * kMarkCap + k] = mark;
+    else mark_slot(a, mark, blk + h, plan_s[h - h0], bm + 3 * (h - h0) * words, words);
+  }
+}
+
+__global__ void __launch_bounds__(32 * kMaxApplyWarps, 3) k_apply(DecodeArgs a, int32_t hpc, int32_t words) {
   extern __shared__ __align__(16) unsigned char smem[];
   DecPlan *plan_s = reinterpret_cast<DecPlan *>(smem);
   uint32_t *bm = reinterpret_cast<uint32_t *>(plan_s + hpc);        // [hpc][3][words]
   int32_t *buf = reinterpret_cast<int32_t *>(bm + 3 * hpc * words);  // [hpc][32]
   int32_t *stage = buf + 32 * hpc;                                   // [hpc][pmax]
+  uint32_t *mk = reinterpret_cast<uint32_t *>(stage + a.pmax * hpc);  // [hpc][kMarkCap] marks per unit
+  int32_t *mk_n = reinterpret_cast<int32_t *>(mk + kMarkCap * hpc);   // [hpc]
   const int32_t r = blockIdx.y, l = blockIdx.z;
   const int32_t h0 = blockIdx.x * hpc;
   const int32_t nh = min(hpc, a.Hkv - h0);
@@ -747,7 +825,10 @@ __global__ void __launch_bounds__(32 * kMaxApplyWarps) k_apply(DecodeArgs a, int
   const int32_t N = ctx + nw;
   const int64_t u0 = (static_cast<int64_t>(l) * a.R + r) * a.Hkv;
   if (err == 0) {
-    for (int i = tid; i < nh; i += blockDim.x) plan_s[i] = a.plan[u0 + h0 + i];
+    for (int i = tid; i < nh; i += blockDim.x) {
+      plan_s[i] = a.plan[u0 + h0 + i];
+      mk_n[i] = 0;
+    }
     for (int i = tid; i < 3 * hpc * words; i += blockDim.x) bm[i] = 0u;
   }
   __syncthreads();
@@ -757,42 +838,28 @@ __global__ void __launch_bounds__(32 * kMaxApplyWarps) k_apply(DecodeArgs a, int
   uint8_t *cls = a.classes + blk;
   const int32_t nbytes = N * a.Hkv;
   const int32_t nvec = (nbytes + 15) >> 4;
-  for (int32_t vi = tid; vi < nvec; vi += blockDim.x) {
-    const uint4 x = reinterpret_cast<const uint4 *>(cls)[vi];
-    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-    if (((x.x | x.y | x.z | x.w) & 0x80808080u) == 0u) continue;
+  // loads four vectors per thread at a time; the rare marked ones go out of line
+  for (int32_t vb = 0; vb < nvec; vb += 4 * blockDim.x) {
+    uint4 x[4];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const uint32_t b = (xw[q >> 2] >> (8 * (q & 3))) & 255u;
-      if ((b & 0x80u) == 0u) continue;
-      const int32_t idx = vi * 16 + q;
-      if (idx >= nbytes) continue;
-      const int32_t i = idx / a.Hkv, h = idx - i * a.Hkv;
-      if (h < h0 || h >= h0 + nh) continue;
-      const uint32_t old = (b >> 2) & 3u, cn = b & 3u;
-      const int64_t u = u0 + h;
-      if (err != 0) {  // revert
-        cls[idx] = static_cast<uint8_t>(old == 3u ? (a.ucnt[u].w & 0xff) : old);
-        continue;
-      }
-      cls[idx] = static_cast<uint8_t>(cn);
-      if (old == 3u) continue;  // the new token: handled from the plan
-      const DecPlan &p = plan_s[h - h0];
-      uint32_t *b3 = bm + 3 * (h - h0) * words;  // removed K8V4 slots, removed K4V2 slots, demoted positions
-      int32_t *so = a.slot_of + blk + idx;
-      const int32_t s = *so;
-      const int32_t n = old == DKV_CLASS_K8V4 ? p.n_hi : p.n_lo;
-      if (s < 0 || s >= n) {
-        atomicCAS(a.status, 0, DKV_E_INTERNAL);
-        continue;
-      }
-      atomicOr(b3 + (old == DKV_CLASS_K8V4 ? 0 : words) + (s >> 5), 1u << (s & 31));
-      if (cn == DKV_CLASS_K4V2) atomicOr(b3 + 2 * words + (i >> 5), 1u << (i & 31));
-      else *so = -1;  // pruned
+    for (int q = 0; q < 4; ++q) {
+      const int32_t vi = vb + q * blockDim.x + tid;
+      x[q] = vi < nvec ? reinterpret_cast<const uint4 *>(cls)[vi] : make_uint4(0u, 0u, 0u, 0u);
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (((x[q].x | x[q].y | x[q].z | x[q].w) & 0x80808080u) != 0u)
+        take_marks(a, x[q], vb + q * blockDim.x + tid, nbytes, h0, nh, err, u0, blk, plan_s, bm, words, mk, mk_n);
   }
   __syncthreads();
   if (err != 0 || warp >= nh) return;
+  // this unit's listed marks: slots of the removed tokens, 32 at a time
+  {
+    const int32_t n_mk = min(mk_n[warp], kMarkCap);
+    for (int32_t j = lane; j < n_mk; j += 32)
+      mark_slot(a, mk[warp * kMarkCap + j], blk + h0 + warp, plan_s[warp], bm + 3 * warp * words, words);
+  }
+  __syncwarp();
 
   UnitView v;
   v.u = u0 + h0 + warp;
@@ -854,7 +921,7 @@ __global__ void __launch_bounds__(256) k_index(DecodeArgs a) {
 
 size_t apply_smem(int32_t hpc, int32_t words, int32_t pmax) {
   return sizeof(DecPlan) * hpc + sizeof(uint32_t) * 3 * hpc * words + sizeof(int32_t) * 32 * hpc +
-         sizeof(int32_t) * static_cast<size_t>(pmax) * hpc;
+         sizeof(int32_t) * static_cast<size_t>(pmax) * hpc + sizeof(uint32_t) * kMarkCap * hpc + sizeof(int32_t) * hpc;
 }
 
 cudaError_t launch_reclass(const DecodeArgs &a, cudaStream_t s) {

@@ -303,7 +303,7 @@ def decode_update_inputs(w: Workload, ctx: dict, step: int, seed: int | None = N
               N = ctx_r + 1 (demoted to the middle tier unless already there);
     else:     sig += sig / cnt (its average stays as it was).
     Every count then grows by one (the new query attends to every position).
-    The new token at position ctx_r gets count 1 and a log-normal(sigma)
+    The new token at position ctx_r (none when ctx_r = cap) gets count 1 and a log-normal(sigma)
     self-attention weight with mean 1/N per query head; its K and V are drawn
     like prefill rows.  fp32 division and multiplication as written, in place
     on ctx."""
@@ -313,30 +313,30 @@ def decode_update_inputs(w: Workload, ctx: dict, step: int, seed: int | None = N
     clen = ctx["ctx_lens"].to(torch.int64)
     N = (clen + 1).to(torch.float32)
     sig, cnt = ctx["sig_sum"], ctx["sig_cnt"]
-    pos_all = torch.arange(cap, device=device)
-    live = (pos_all[None, :] < clen[:, None]).reshape(-1)  # [R * cap]
-    tok = torch.nonzero(live).squeeze(1)
-    r_of = tok // cap
-    i_of = tok % cap
-    cntf = cnt[tok].to(torch.float32)[:, None, None]
-    mid = (torch.tensor(ALPHA_MID, dtype=torch.float32, device=device) / N[r_of])[:, None, None]
-    hh = torch.arange(Hkv, device=device)[None, :]
+    pos = torch.arange(cap, device=device)
+    live = (pos[None, :] < clen[:, None])                                 # [R, cap]
+    cntf = cnt.view(R, cap).to(torch.float32)[:, :, None, None]
+    mid = (torch.tensor(ALPHA_MID, dtype=torch.float32, device=device) / N)[:, None, None, None]
+    rh = torch.arange(R, device=device)[:, None] * Hkv + torch.arange(Hkv, device=device)[None, :]  # [R, Hkv]
     for l in range(L):
-        ids = ((l * R + r_of[:, None]) * Hkv + hh) * (cap + 1) + i_of[:, None]  # [n, Hkv]
-        u = _hash01(step, ids)[:, :, None]
-        s = sig[l, tok].view(-1, Hkv, G)
-        s = torch.where(u < p_prune, torch.zeros_like(s), torch.where(u < p_prune + p_demote, mid * cntf, s + s / cntf))
-        sig[l, tok] = s.view(-1, Hq)
+        ids = (l * R * Hkv + rh)[:, None, :] * (cap + 1) + pos[None, :, None]   # [R, cap, Hkv]
+        u = _hash01(step, ids)[..., None]
+        s = sig[l].view(R, cap, Hkv, G)
+        upd = torch.where(u < p_prune, torch.zeros_like(s),
+                          torch.where(u < p_prune + p_demote, mid * cntf, s + s / cntf))
+        s.copy_(torch.where(live[:, :, None, None], upd, s))
+    tok = torch.nonzero(live.reshape(-1)).squeeze(1)
     cnt[tok] += 1
     # the new token of every request
     g = _gen(seed * 1000003 + 900000 + step, device)
-    newpos = torch.arange(R, device=device) * cap + clen
+    room = clen < cap                                   # a full request takes no new token
+    newpos = (torch.arange(R, device=device) * cap + clen)[room]
     z = torch.randn((L, R, Hq), generator=g, device=device, dtype=torch.float64)
     wt = torch.exp(w.sigma * z - w.sigma ** 2 / 2) / (clen + 1).to(torch.float64)[None, :, None]
-    sig[:, newpos] = wt.to(torch.float32)
+    sig[:, newpos] = wt[:, room].to(torch.float32)
     cnt[newpos] = 1
     kv = Workload(w.name, L=1, Hq=Hq, Hkv=Hkv, lens=[R], P=w.P, alpha_h=w.alpha_h, alpha_l=w.alpha_l,
                   n_outlier=w.n_outlier, outlier_scale=w.outlier_scale)
     k_new = torch.stack([make_kv_layer(kv, seed + 77 * step + 1, l, 0, device) for l in range(L)])
     v_new = torch.stack([make_kv_layer(kv, seed + 77 * step + 1, l, 1, device) for l in range(L)])
-    return {"k_new": k_new, "v_new": v_new, "new_lens": torch.ones(R, dtype=torch.int32, device=device)}
+    return {"k_new": k_new, "v_new": v_new, "new_lens": room.to(torch.int32)}
