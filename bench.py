@@ -39,7 +39,32 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="keep only this many layers (a reduced case for profiler captures; named in config)")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="keep only the first this-many requests (a reduced case; named in config)")
     return ap.parse_args()
+
+
+def workload(a):
+    """The named workload, cut to --layers / --requests when given."""
+    import dataclasses
+
+    from differentiated_kv_cache_dkv_gb300 import workloads as W
+
+    w = W.get(a.workload)
+    if a.layers:
+        w = dataclasses.replace(w, L=min(a.layers, w.L))
+    if a.requests:
+        w = dataclasses.replace(w, lens=list(w.lens[:a.requests]))
+    return w
+
+
+def workload_name(a) -> str:
+    name = a.workload
+    if a.layers or a.requests:
+        name += f" (reduced: {a.layers or 'all'} layers, {a.requests or 'all'} requests)"
+    return name
 
 
 # DRAM traffic of one full k_pack launch on the Llama-shaped workload, from one
@@ -68,6 +93,26 @@ def _peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- ranks -----
+
+def max_over_ranks(ms: float, device, world: int) -> float:
+    """The slowest rank's time: every rank times its own replica between two
+    barriers; the whole job took as long as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Units all ranks processed per second (replicas: every rank processes
+    the same number of units)."""
+    return world * units_per_rank / (ms_max / 1000.0)
 
 
 # ------------------------------------------------------------------ clocks --
@@ -157,7 +202,7 @@ def run_reference(a):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    w = W.get(a.workload)
+    w = workload(a)
     for _ in range(a.warmup):
         oracle_sample(w, 0.0)
     times = []
@@ -172,7 +217,7 @@ def run_reference(a):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": 1000.0 * total / a.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": a.workload, "layers": w.L, "requests": w.R, "tokens": w.T, "Hq": w.Hq,
+        "config": {"workload": workload_name(a), "layers": w.L, "requests": w.R, "tokens": w.T, "Hq": w.Hq,
                    "Hkv": w.Hkv, "page_tokens": w.P},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -196,7 +241,7 @@ def run_native(a):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     libdkv.load()
-    w = W.get(a.workload)
+    w = workload(a)
     dev = torch.device("cuda", local)
     inp = W.make_inputs(w, seed=W.SEED_BASE + 1000 * rank, device=dev)
     comp = libdkv.Compactor(w.L, w.R, w.Hq, w.Hkv, w.T, max(w.lens), w.P, w.pool_pages, device=dev)
@@ -242,11 +287,8 @@ def run_native(a):
     prof.close()
     kernel_ms = {n: statistics.mean(c[i] for c in kt) for i, n in enumerate(libdkv.KERNEL_NAMES)}
 
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = world * rows * a.steps / (ms_max / 1000.0)
+    ms_max = max_over_ranks(ms, dev, world)
+    value = whole_job_rate(rows * a.steps, world, ms_max)
 
     # roofline of the dominant kernel (k_pack): algorithmic bytes per launch
     peak, peak_kind = _peaks()
@@ -285,10 +327,8 @@ def run_native(a):
             e2e_step()
         s1.record(stream)
         torch.cuda.synchronize()
-        te = torch.tensor([s0.elapsed_time(s1)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * rows * a.e2e_steps / (float(te.item()) / 1000.0), "unit": UNIT,
+        te = max_over_ranks(s0.elapsed_time(s1), dev, world)
+        e2e = {"value": whole_job_rate(rows * a.e2e_steps, world, te), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": a.e2e_steps}
         del host
 
@@ -303,13 +343,13 @@ def run_native(a):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_max / a.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": a.workload, "layers": w.L, "requests": w.R, "tokens_per_request": w.lens[0]
+            "config": {"workload": workload_name(a), "layers": w.L, "requests": w.R, "tokens_per_request": w.lens[0]
                        if len(set(w.lens)) == 1 else "ragged", "Hq": w.Hq, "Hkv": w.Hkv, "page_tokens": w.P,
                        "alpha_h": w.alpha_h, "alpha_l": w.alpha_l, "rows_per_step": rows,
                        "l2": "inputs (%.1f GB) larger than L2" % ((rows * 512 + w.L * w.T * w.Hq * 4) / 1e9),
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "kernel": "k_pack", "achieved": pack_gbs, "peak": peak, "unit": "GB/s",
-                         "frac": pack_gbs / peak, "peak_kind": peak_kind, "traffic": _pack_traffic(a.workload),
+                         "frac": pack_gbs / peak, "peak_kind": peak_kind, "traffic": _pack_traffic(workload_name(a)),
                          "algorithmic_bytes": pack_bytes, "ms": pack_ms},
             "step_hbm": {"achieved": step_gbs, "frac": step_gbs / peak, "bytes": step_read + step_write},
             "kernels_ms": kernel_ms,
@@ -456,7 +496,7 @@ def run_native_decode(a):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     libdkv.load()
-    w = W.get(a.workload)
+    w = workload(a)
     dev = torch.device("cuda", local)
     total = a.warmup + a.steps + a.e2e_steps + 1
     dec, ctx, cap, used = decode_setup(w, dev, W.SEED_BASE + 1000 * rank, total)
@@ -506,11 +546,8 @@ def run_native_decode(a):
     prof.close()
     names = ("reset", "k_reclass", "k_dscan", "k_apply")
     kernel_ms = {n: statistics.mean(c[i] for c in kt) for i, n in enumerate(names)}
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = world * live_rows / (ms_max / 1000.0)
+    ms_max = max_over_ranks(ms, dev, world)
+    value = whole_job_rate(live_rows, world, ms_max)
 
     peak, peak_kind = _peaks()
     tok_per_step = live_rows / a.steps / (w.L * w.Hkv)
@@ -554,7 +591,8 @@ def run_native_decode(a):
                 for k_ in host:
                     host[k_].copy_(d[k_])
         assert libdkv.dkv_get_status(dec.pool) == libdkv.DKV_OK
-        e2e = {"value": world * e_rows / (te / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        te = max_over_ranks(te, dev, world)
+        e2e = {"value": whole_job_rate(e_rows, world, te), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": a.e2e_steps}
         del host
     head1 = int(dec.pool.cursors[0])
@@ -570,7 +608,7 @@ def run_native_decode(a):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_max / a.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": a.workload, "layers": w.L, "requests": w.R, "context": "uniform 2048..8192",
+            "config": {"workload": workload_name(a), "layers": w.L, "requests": w.R, "context": "uniform 2048..8192",
                        "Hq": w.Hq, "Hkv": w.Hkv, "page_tokens": w.P, "alpha_h": w.alpha_h, "alpha_l": w.alpha_l,
                        "cap": cap, "updates": "0.5% pruned + 0.5% demoted per (layer, request, KV head, token)",
                        "timed": "dkv_decode_step only (significance updates between steps untimed)",
@@ -581,7 +619,7 @@ def run_native_decode(a):
                          "algorithmic_bytes": rc_bytes, "ms": rc_ms},
             "step_hbm": {"achieved": step_gbs, "frac": step_gbs / peak, "bytes": rc_bytes},
             "kernels_ms": kernel_ms,
-            "new_token_rows_per_s": world * new_rows / (ms_max / 1000.0),
+            "new_token_rows_per_s": whole_job_rate(new_rows, world, ms_max),
             "pool": {"F": F, "prefill_pages": used, "head_start": head0, "head_end": head1,
                      "wraps": head1 // F - head0 // F},
             "gpu_launches": a.steps * 4,
@@ -601,7 +639,7 @@ def run_reference_decode(a):
 
     if int(os.environ.get("RANK", "0")) != 0:
         return
-    w = W.get(a.workload)
+    w = workload(a)
     smp = DecodeOracleSample(w)
     for _ in range(a.warmup):
         smp.step()
@@ -616,7 +654,7 @@ def run_reference_decode(a):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": 1000.0 * total / a.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": a.workload, "layers": w.L, "requests": w.R, "Hq": w.Hq, "Hkv": w.Hkv,
+        "config": {"workload": workload_name(a), "layers": w.L, "requests": w.R, "Hq": w.Hq, "Hkv": w.Hkv,
                    "page_tokens": w.P},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)

@@ -26,8 +26,7 @@
 // Work layout (one CTA per SM, persistent over unit tiles = 128 tokens of one
 // (layer, request, KV head)), a warp-specialised pipeline over a ring of
 // kStages shared-memory stages:
-//   producer warps (2, alternate tiles) issue two TMA tile loads per tile
-//       (cp.async.bulk.tensor
+//   one producer warp issues two TMA tile loads per tile (cp.async.bulk.tensor
 //       3-D: the 128 consecutive token rows of one KV head, 32 KB of K and 32
 //       KB of V) into the stage, completing on its "full" mbarrier, then
 //       stores the list of surviving rows (K8V4 first, ranks by popcount of
@@ -38,7 +37,12 @@
 //       one row per 4-lane group: bf16x2 min / max reduced over the group,
 //       one lane each computes the K and the V scale / zero / reciprocal and
 //       stores the slot's metadata and position, then every lane quantises
-//       its 32 K and 32 V channels and stores their packed codes.  A warp
+//       its 32 K and 32 V channels as four jobs of 16 channels through one
+//       quantiser body (a rolled loop: the consumer code stays small enough
+//       for the instruction cache, which bounded the unrolled form) and
+//       stores their packed codes.  A lane's 16-byte chunks are rotated by its
+//       group, so the 8 rows a warp reads at once (256 bytes apart) fall on
+//       all 32 shared-memory banks.  A warp
 //       that finds no group left arrives on the stage's "empty" mbarrier and
 //       moves on; the stage is refilled once all 16 have left it.
 // Unused slots of the pages are filled by k_commit, which walks every page.
@@ -167,15 +171,21 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
   return r;
 }
 
-// Result bits of two channels held as one bf16x2 word, with packed fp32 math
+// Result bits of two channels held as one bf16x2 word: the subtraction reads
+// each bf16 half directly (mixed precision, no integer unpacking), the
+// multiply-add is packed fp32 math
 // (each half rounded exactly like the scalar IEEE operation):
 //   y = RN(RN(x - z) * r + 1536.5)
-__device__ __forceinline__ void fast_pair(uint32_t w, uint64_t zz, uint64_t rr, uint64_t mm, uint32_t &b0,
+__device__ __forceinline__ void fast_pair(uint32_t w, float z, uint64_t rr, uint64_t mm, uint32_t &b0,
                                           uint32_t &b1) {
-  const uint64_t x = pack2(bf_lo(w), bf_hi(w));
-  uint64_t d, y;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(zz));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(y) : "l"(d), "l"(rr), "l"(mm));
+  // RN(x - z) straight from each bf16 half (mixed-precision subtract: the
+  // bf16 operand is widened exactly, the difference rounded once in fp32)
+  float d0, d1;
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; sub.rn.f32.bf16 %0, l, %3; sub.rn.f32.bf16 %1, h, %3; }"
+      : "=f"(d0), "=f"(d1)
+      : "r"(w), "f"(z));
+  uint64_t y;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(y) : "l"(pack2(d0, d1)), "l"(rr), "l"(mm));
   asm("mov.b64 {%0, %1}, %2;" : "=r"(b0), "=r"(b1) : "l"(y));
 }
 
@@ -205,13 +215,14 @@ struct Bits16 {
 __device__ __forceinline__ void quant16(const uint4 &a, const uint4 &b, float z, float r, float s, float n,
                                         Bits16 &q) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  const uint64_t zz = pack2(z, z), rr = pack2(r, r), mm = pack2(kMagicHalf, kMagicHalf);
+  const uint64_t rr = pack2(r, r), mm = pack2(kMagicHalf, kMagicHalf);
   uint32_t flag = 0xffffffffu;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    fast_pair(w[i], zz, rr, mm, q.b[2 * i], q.b[2 * i + 1]);
-    flag = min(flag, q.b[2 * i] & 8191u);
-    flag = min(flag, q.b[2 * i + 1] & 8191u);
+    fast_pair(w[i], z, rr, mm, q.b[2 * i], q.b[2 * i + 1]);
+    // zero iff either channel's 13 fraction bits are all zero (the product
+    // of two 13-bit values fits 26 bits)
+    flag = min(flag, (q.b[2 * i] & 8191u) * (q.b[2 * i + 1] & 8191u));
   }
   if (flag == 0u || r < 0.0f) {
     const uint4 e = exact16(a, b, z, r, s, n);
@@ -235,45 +246,38 @@ __device__ __forceinline__ uint32_t pack_codes(const Bits16 &q, int first) {
   return w;
 }
 
-// Quantise a lane's 32 K and 32 V channels of one row (chunks c = l4 + 4j,
-// channels 8c..8c+7) and store their packed codes into the row's slot.
-__device__ __forceinline__ void store_row(uint8_t *pg, int32_t P, int32_t slot_, bool high, int l4, const uint4 &k0,
-                                          const uint4 &k1, const uint4 &k2, const uint4 &k3, const uint4 &v0,
-                                          const uint4 &v1, const uint4 &v2, const uint4 &v3, float kz, float kq,
-                                          float ks, float vz, float vq, float vs) {
+// Quantise a lane's 32 K and 32 V channels of one row and store their packed
+// codes into the row's slot: four jobs of 16 channels (K chunks l4, l4+4;
+// K chunks l4+8, l4+12; the same for V), one quantiser body for all of them,
+// the operands re-read from the staged tile.
+__device__ __forceinline__ void store_row(uint8_t *pg, int32_t P, int32_t slot_, bool high, int l4,
+                                          const uint4 *kr, const uint4 *vr, float kz, float kq, float ks,
+                                          float vz, float vq, float vs) {
   const int64_t slot = slot_;
-  const int c0 = l4, c1 = l4 + 4, c2 = l4 + 8, c3 = l4 + 12;
-  Bits16 q;
-  if (high) {
-    uint8_t *kd = pg + slot * 128;
-    uint8_t *vd = pg + 128 * static_cast<int64_t>(P) + slot * 64;
-    quant16(k0, k1, kz, kq, ks, 255.0f, q);
-    *reinterpret_cast<uint2 *>(kd + 8 * c0) = make_uint2(pack_codes<8, 4>(q, 0), pack_codes<8, 4>(q, 4));
-    *reinterpret_cast<uint2 *>(kd + 8 * c1) = make_uint2(pack_codes<8, 4>(q, 8), pack_codes<8, 4>(q, 12));
-    quant16(k2, k3, kz, kq, ks, 255.0f, q);
-    *reinterpret_cast<uint2 *>(kd + 8 * c2) = make_uint2(pack_codes<8, 4>(q, 0), pack_codes<8, 4>(q, 4));
-    *reinterpret_cast<uint2 *>(kd + 8 * c3) = make_uint2(pack_codes<8, 4>(q, 8), pack_codes<8, 4>(q, 12));
-    quant16(v0, v1, vz, vq, vs, 15.0f, q);
-    *reinterpret_cast<uint32_t *>(vd + 4 * c0) = pack_codes<4, 8>(q, 0);
-    *reinterpret_cast<uint32_t *>(vd + 4 * c1) = pack_codes<4, 8>(q, 8);
-    quant16(v2, v3, vz, vq, vs, 15.0f, q);
-    *reinterpret_cast<uint32_t *>(vd + 4 * c2) = pack_codes<4, 8>(q, 0);
-    *reinterpret_cast<uint32_t *>(vd + 4 * c3) = pack_codes<4, 8>(q, 8);
-  } else {
-    uint8_t *kd = pg + slot * 64;
-    uint8_t *vd = pg + 128 * static_cast<int64_t>(P) + slot * 32;
-    quant16(k0, k1, kz, kq, ks, 15.0f, q);
-    *reinterpret_cast<uint32_t *>(kd + 4 * c0) = pack_codes<4, 8>(q, 0);
-    *reinterpret_cast<uint32_t *>(kd + 4 * c1) = pack_codes<4, 8>(q, 8);
-    quant16(k2, k3, kz, kq, ks, 15.0f, q);
-    *reinterpret_cast<uint32_t *>(kd + 4 * c2) = pack_codes<4, 8>(q, 0);
-    *reinterpret_cast<uint32_t *>(kd + 4 * c3) = pack_codes<4, 8>(q, 8);
-    quant16(v0, v1, vz, vq, vs, 3.0f, q);
-    *reinterpret_cast<uint16_t *>(vd + 2 * c0) = static_cast<uint16_t>(pack_codes<2, 8>(q, 0));
-    *reinterpret_cast<uint16_t *>(vd + 2 * c1) = static_cast<uint16_t>(pack_codes<2, 8>(q, 8));
-    quant16(v2, v3, vz, vq, vs, 3.0f, q);
-    *reinterpret_cast<uint16_t *>(vd + 2 * c2) = static_cast<uint16_t>(pack_codes<2, 8>(q, 0));
-    *reinterpret_cast<uint16_t *>(vd + 2 * c3) = static_cast<uint16_t>(pack_codes<2, 8>(q, 8));
+  uint8_t *kd = pg + slot * (high ? 128 : 64);
+  uint8_t *vd = pg + 128 * static_cast<int64_t>(P) + slot * (high ? 64 : 32);
+#pragma unroll 2
+  for (int j = 0; j < 4; ++j) {
+    const bool isv = j >= 2;
+    const int c = (l4 + 8 * (j & 1)) & 15;  // first chunk of the job; the second is c + 4 (mod 16)
+    const int c2 = (c + 4) & 15;
+    const uint4 *src = isv ? vr : kr;
+    const uint4 a = src[c], b = src[c2];
+    const float z = isv ? vz : kz, r = isv ? vq : kq, s = isv ? vs : ks;
+    const int width = high ? (isv ? 4 : 8) : (isv ? 2 : 4);
+    Bits16 q;
+    quant16(a, b, z, r, s, static_cast<float>((1 << width) - 1), q);
+    uint8_t *d = isv ? vd : kd;
+    if (width == 8) {
+      *reinterpret_cast<uint2 *>(d + 8 * c) = make_uint2(pack_codes<8, 4>(q, 0), pack_codes<8, 4>(q, 4));
+      *reinterpret_cast<uint2 *>(d + 8 * c2) = make_uint2(pack_codes<8, 4>(q, 8), pack_codes<8, 4>(q, 12));
+    } else if (width == 4) {
+      *reinterpret_cast<uint32_t *>(d + 4 * c) = pack_codes<4, 8>(q, 0);
+      *reinterpret_cast<uint32_t *>(d + 4 * c2) = pack_codes<4, 8>(q, 8);
+    } else {
+      *reinterpret_cast<uint16_t *>(d + 2 * c) = static_cast<uint16_t>(pack_codes<2, 8>(q, 0));
+      *reinterpret_cast<uint16_t *>(d + 2 * c2) = static_cast<uint16_t>(pack_codes<2, 8>(q, 8));
+    }
   }
 }
 
@@ -441,8 +445,12 @@ __global__ void __launch_bounds__(kPackThreads, 1)
       // channels 8c..8c+7 for the chunks c = l4 + 4j, j = 0..3
       const uint4 *kr = reinterpret_cast<const uint4 *>(st.k[en.w]);
       const uint4 *vr = reinterpret_cast<const uint4 *>(st.v[en.w]);
-      const uint4 k0 = kr[l4], k1 = kr[l4 + 4], k2 = kr[l4 + 8], k3 = kr[l4 + 12];
-      const uint4 v0 = vr[l4], v1 = vr[l4 + 4], v2 = vr[l4 + 8], v3 = vr[l4 + 12];
+      // the lane's chunks are cb, cb+4, cb+8, cb+12 (mod 16) with cb rotated by
+      // the group, so the 8 groups of a warp, reading 8 rows 256 bytes apart,
+      // spread their 16-byte loads over all 32 banks
+      const int cb = (l4 + grp) & 15;
+      const uint4 k0 = kr[cb], k1 = kr[(cb + 4) & 15], k2 = kr[(cb + 8) & 15], k3 = kr[(cb + 12) & 15];
+      const uint4 v0 = vr[cb], v1 = vr[(cb + 4) & 15], v2 = vr[(cb + 8) & 15], v3 = vr[(cb + 12) & 15];
       const uint32_t kmm = row_minmax(k0, k1, k2, k3);
       const uint32_t vmm = row_minmax(v0, v1, v2, v3);
       const bool high = 8 * g < nh_t;  // class-uniform group
@@ -487,7 +495,7 @@ __global__ void __launch_bounds__(kPackThreads, 1)
       const float ks = __shfl_sync(0xffffffffu, js, src);
       const float vz = __shfl_sync(0xffffffffu, jz, src + 1), vq = __shfl_sync(0xffffffffu, jr, src + 1);
       const float vs = __shfl_sync(0xffffffffu, js, src + 1);
-      if (write) store_row(pg, P, en.y, high, l4, k0, k1, k2, k3, v0, v1, v2, v3, kz, kq, ks, vz, vq, vs);
+      if (write) store_row(pg, P, en.y, high, cb, kr, vr, kz, kq, ks, vz, vq, vs);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);
