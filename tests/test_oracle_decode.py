@@ -293,4 +293,6 @@ def test_length_errors():
     w = _small()
     hd = HostDecode(w, cap=517)  # request 2 already fills its capacity
     upd = W.decode_update_inputs(w, hd.ctx, 0)
+    assert int(upd["new_lens"][2]) == 0
+    upd["new_lens"][2] = 1       # one more token than it can hold
     assert hd.step(upd) == oracle.E_LENS
