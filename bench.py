@@ -71,19 +71,34 @@ def workload_name(a) -> str:
 # ncu capture of the same kernel on 2 of its 32 layers scaled by the units
 # processed (profiles/k_pack_llama_prefill.md); valid only for the kernel
 # source it was measured on.
-PACK_TRAFFIC = {"workload": "llama", "source_sha1": "a241058dc819", "bytes": 16 * (537.706496 + 131.256832) * 1e6}
+PACK_TRAFFIC = {"workload": "llama", "source_sha1": "9105ef3e12a6", "bytes": 16 * (537.732352 + 130.510336) * 1e6}
+
+# DRAM traffic of k_reclass per algorithmic byte, from one ncu capture on 4
+# layers x 64 requests of the decode workload (181.0 MB for 176.2 MB; traffic
+# grows with the live rows) (profiles/decode_step.md); valid only for the
+# kernel source it was measured on.
+RECLASS_TRAFFIC = {"workload": "decode", "source_sha1": "560086cb1980", "per_byte": (177.175040 + 3.787776) / 176.177616}
+
+
+def _source_sha(name: str):
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "differentiated_kv_cache_dkv_gb300", "csrc", name), "rb") as f:
+            return hashlib.sha1(f.read()).hexdigest()[:12]
+    except OSError:
+        return None
 
 
 def _pack_traffic(workload: str):
-    import hashlib
-    try:
-        with open(os.path.join(ROOT, "differentiated_kv_cache_dkv_gb300", "csrc", "pack.cu"), "rb") as f:
-            sha = hashlib.sha1(f.read()).hexdigest()[:12]
-    except OSError:
-        return None
-    if workload != PACK_TRAFFIC["workload"] or sha != PACK_TRAFFIC["source_sha1"]:
+    if workload != PACK_TRAFFIC["workload"] or _source_sha("pack.cu") != PACK_TRAFFIC["source_sha1"]:
         return None
     return PACK_TRAFFIC["bytes"]
+
+
+def _reclass_traffic(workload: str, alg_bytes: float):
+    if workload != RECLASS_TRAFFIC["workload"] or _source_sha("decode.cu") != RECLASS_TRAFFIC["source_sha1"]:
+        return None
+    return RECLASS_TRAFFIC["per_byte"] * alg_bytes
 
 
 def _peaks():
@@ -369,68 +384,7 @@ def run_native(a):
 
 # ---------------------------------------------------------------- decode ----
 
-DECODE_SLACK = 1 << 16   # free pages between the head after prefill and the next wrap of the ring
-
-
-def decode_cap(w, steps: int) -> int:
-    return -(-(max(w.lens) + steps) // 16) * 16
-
-
-def decode_prefill(w, dec, dev, seed: int, cap: int, head_offset: int = 0):
-    """Per-layer prefill of the decode workload into dec's pool (dkv_compact,
-    one layer per call) and the capacity-strided significance sums and
-    counts the steps start from.  head_offset rotates the fresh ring (free
-    list slot i holds page i, cursors {head_offset, head_offset + F})."""
-    import torch
-    from differentiated_kv_cache_dkv_gb300 import libdkv
-    from differentiated_kv_cache_dkv_gb300 import workloads as W
-
-    libdkv.dkv_init_pool(dec.pool)
-    if head_offset:
-        dec.pool.cursors.copy_(torch.tensor([head_offset, head_offset + dec.pool.F], dtype=torch.int64))
-    req, pos = W._positions(w, dev)
-    dst = req * cap + pos
-    sig = torch.zeros((w.L, w.R * cap, w.Hq), dtype=torch.float32, device=dev)
-    cnt = torch.zeros(w.R * cap, dtype=torch.int32, device=dev)
-    cnt0 = W.sig_cnt_prefill(w, dev)
-    cnt[dst] = cnt0
-    lens = torch.tensor(w.lens, dtype=torch.int32, device=dev)
-    for l in range(w.L):
-        k = W.make_kv_layer(w, seed, l, 0, dev)[None]
-        v = W.make_kv_layer(w, seed, l, 1, dev)[None]
-        s = W.make_sig_layer(w, seed, l, dev)
-        sig[l, dst] = s
-        layer = {"L": 1, "R": w.R, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T, "k": k, "v": v, "sig_sum": s[None].contiguous(),
-                 "sig_cnt": cnt0, "lens": lens}
-        dec.prefill_layer(layer, l, max(w.lens), w.alpha_h, w.alpha_l)
-        del k, v, s, layer
-    st = libdkv.dkv_get_status(dec.pool)
-    assert st == libdkv.DKV_OK, libdkv.status_string(st)
-    ctx = {"L": w.L, "R": w.R, "Hq": w.Hq, "Hkv": w.Hkv, "cap": cap, "sig_sum": sig, "sig_cnt": cnt,
-           "ctx_lens": lens.clone()}
-    dec.index(ctx["ctx_lens"])
-    st = libdkv.dkv_get_status(dec.pool)
-    assert st == libdkv.DKV_OK, libdkv.status_string(st)
-    return ctx
-
-
-def decode_setup(w, dev, seed: int, total_steps: int):
-    """Decoder state after the prefill, with the pool sized so that the ring's
-    head wraps within the run: a first prefill in a worst-case pool measures
-    the pages it takes, the second starts the ring DECODE_SLACK pages before
-    its end."""
-    import torch
-    from differentiated_kv_cache_dkv_gb300 import libdkv
-
-    cap = decode_cap(w, total_steps)
-    dec = libdkv.Decoder(w.L, w.R, w.Hq, w.Hkv, cap, w.P, w.pool_pages, device=dev)
-    decode_prefill(w, dec, dev, seed, cap)
-    used = int(dec.pool.cursors[0])
-    F = dec.pool.F
-    offset = (F - used - DECODE_SLACK) % F
-    torch.cuda.empty_cache()
-    ctx = decode_prefill(w, dec, dev, seed, cap, head_offset=offset)
-    return dec, ctx, cap, used
+from differentiated_kv_cache_dkv_gb300.decode_setup import DECODE_SLACK, decode_cap, decode_prefill, decode_setup  # noqa: E402,F401
 
 
 class DecodeOracleSample:
@@ -615,7 +569,8 @@ def run_native_decode(a):
                        "l2": "significance sums (%.1f GB) larger than L2" % (w.L * w.R * cap * w.Hq * 4 / 1e9),
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "kernel": "k_reclass", "achieved": rc_gbs, "peak": peak, "unit": "GB/s",
-                         "frac": rc_gbs / peak, "peak_kind": peak_kind, "traffic": None,
+                         "frac": rc_gbs / peak, "peak_kind": peak_kind,
+                         "traffic": _reclass_traffic(workload_name(a), rc_bytes),
                          "algorithmic_bytes": rc_bytes, "ms": rc_ms},
             "step_hbm": {"achieved": step_gbs, "frac": step_gbs / peak, "bytes": rc_bytes},
             "kernels_ms": kernel_ms,
