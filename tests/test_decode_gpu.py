@@ -236,3 +236,12 @@ def test_identity_step_on_device():
     after = _snap(dec)
     for k in before:
         assert np.array_equal(before[k], after[k]), k
+
+
+@pytest.mark.parametrize("p_prune,p_demote", [(0.25, 0.35), (0.6, 0.3)])
+def test_decode_heavy_churn(p_prune, p_demote):
+    """Most of a unit's tokens change class in one step: the per-unit mark
+    lists overflow into the in-place path, demotions run to several batches
+    of 32, and lists shrink by many pages at once."""
+    w = W.small("dec_churn", lens=[700, 9, 520, 1, 333], L=2, Hq=8, Hkv=2)
+    _run(w, cap=720, steps=6, p_prune=p_prune, p_demote=p_demote, slot_check_every=1)
