@@ -48,7 +48,7 @@ namespace dkv {
 namespace {
 
 constexpr int kReclassThreads = 512;
-constexpr int kReclassRows = 4;           // rows in flight per thread
+constexpr int kReclassRows = 2;           // rows in flight per thread (4 blocks of 512 per SM)
 constexpr int kDScanThreads = 256;        // one unit per thread
 constexpr int kMarkCap = 256;             // listed marks per unit in the apply block
 
@@ -78,8 +78,22 @@ __device__ __forceinline__ bool words_out_of_range(uint4 v) {
 
 // ---------------------------------------------------------------- k_reclass --
 
+// The new token's class mark, its saved prior byte and class, and the range
+// check of a kept new token's K and V.  Once per unit, so out of line.
+__device__ __noinline__ void new_token(const DecodeArgs &a, uint8_t *c, int64_t u, uint32_t prior, uint32_t cn) {
+  *c = static_cast<uint8_t>(0x80u | (3u << 2) | cn);
+  a.ucnt[u].w = static_cast<int32_t>(prior | (cn << 8) | (1u << 16));
+  if (cn != DKV_CLASS_PRUNE) {
+    const uint4 *kr = reinterpret_cast<const uint4 *>(a.k_new + u * DKV_HEAD_DIM);
+    const uint4 *vr = reinterpret_cast<const uint4 *>(a.v_new + u * DKV_HEAD_DIM);
+    bool oor = false;
+    for (int q = 0; q < DKV_HEAD_DIM / 8; ++q) oor |= words_out_of_range(__ldg(kr + q)) | words_out_of_range(__ldg(vr + q));
+    if (oor) set_error(&a.ws->err, DKV_E_RANGE);
+  }
+}
+
 template <int kV4>  // float4 loads per row (G / 4); 0 = scalar loads
-__global__ void __launch_bounds__(kReclassThreads) k_reclass(DecodeArgs a) {
+__global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
   __shared__ int32_t ev_s[kMaxHq * 3];  // per head: demoted, K8V4 pruned, K4V2 pruned
   const int32_t r = blockIdx.y, l = blockIdx.z;
   const int32_t i0 = blockIdx.x * kReclassChunk;
@@ -98,6 +112,17 @@ __global__ void __launch_bounds__(kReclassThreads) k_reclass(DecodeArgs a) {
   __syncthreads();
   const float thr_h = __fdiv_rn(a.alpha_h, static_cast<float>(N));
   const float thr_l = __fdiv_rn(a.alpha_l, static_cast<float>(N));
+  // Reciprocal test: with rc the hardware reciprocal of c (within 1 ulp),
+  // y = RN(m * rc) is within 2^-22 (relative) of m / c, so y >= thr (1 + 2^-19)
+  // proves RN(m / c) >= thr and y <= thr (1 - 2^-19) proves RN(m / c) < thr
+  // (the margins, themselves rounded, stay far from 2^-22); in between, and for
+  // thresholds below 2^-100 where a tiny quotient could leave the relative
+  // bound, the IEEE division decides.  A NaN fails every test: pruned, as by
+  // the division.
+  const bool exact_only = !(thr_l >= 0x1p-100f);
+  const float hi_h = __fmul_rn(thr_h, 1.0f + 0x1p-19f), lo_h = __fmul_rn(thr_h, 1.0f - 0x1p-19f);
+  const float hi_l = __fmul_rn(thr_l, 1.0f + 0x1p-19f), lo_l = __fmul_rn(thr_l, 1.0f - 0x1p-19f);
+  const int sh = (Hkv & (Hkv - 1)) == 0 ? __ffs(Hkv) - 1 : -1;
   const int64_t tok0 = static_cast<int64_t>(r) * a.cap + i0;
   const int64_t lrow = static_cast<int64_t>(l) * a.R * a.cap;  // first token row of the layer
   uint8_t *cls = a.classes + (lrow + tok0) * Hkv;
@@ -117,7 +142,7 @@ __global__ void __launch_bounds__(kReclassThreads) k_reclass(DecodeArgs a) {
       c[k] = 0;
       old[k] = 0;
       if (j < nrows) {
-        const int ii = j / Hkv;
+        const int ii = sh >= 0 ? (j >> sh) : j / Hkv;
         c[k] = __ldg(cnt + ii);
         old[k] = cls[j];
         if (kV4 > 0) {
@@ -148,16 +173,31 @@ __global__ void __launch_bounds__(kReclassThreads) k_reclass(DecodeArgs a) {
     for (int k = 0; k < kReclassRows; ++k) {
       const int j = jb + k * kReclassThreads + threadIdx.x;
       if (j >= nrows) continue;
-      const int ii = j / Hkv, h = j - ii * Hkv;
+      const int ii = sh >= 0 ? (j >> sh) : j / Hkv;
+      const int h = j - ii * Hkv;
+      const bool is_new = i0 + ii >= ctx;
+      const uint32_t o = old[k];
+      if (!is_new && o == DKV_CLASS_PRUNE) continue;  // min(0, x) = 0: nothing can change
       uint32_t cn = DKV_CLASS_K8V4;  // a count of 0: not yet observed
       if (c[k] != 0) {
         // max over the group of the rounded quotients == rounded quotient
         // of the max sum (min for a negative count): division is monotone
-        const float s = __fdiv_rn(m[k], static_cast<float>(c[k]));
-        cn = s >= thr_h ? DKV_CLASS_K8V4 : (s >= thr_l ? DKV_CLASS_K4V2 : DKV_CLASS_PRUNE);
+        const float cf = static_cast<float>(c[k]);
+        float rc;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(cf));
+        const float y = __fmul_rn(m[k], rc);
+        if (!exact_only && y >= hi_h) {
+          cn = DKV_CLASS_K8V4;
+        } else if (!exact_only && !(y > lo_h) && y >= hi_l) {
+          cn = DKV_CLASS_K4V2;
+        } else if (!exact_only && !(y > lo_h) && !(y > lo_l)) {
+          cn = DKV_CLASS_PRUNE;
+        } else {
+          const float s = __fdiv_rn(m[k], cf);
+          cn = s >= thr_h ? DKV_CLASS_K8V4 : (s >= thr_l ? DKV_CLASS_K4V2 : DKV_CLASS_PRUNE);
+        }
       }
-      if (i0 + ii < ctx) {
-        const uint32_t o = old[k];
+      if (!is_new) {
         if (o > DKV_CLASS_K8V4) {
           set_error(&a.ws->err, DKV_E_INTERNAL);
           continue;
@@ -167,17 +207,7 @@ __global__ void __launch_bounds__(kReclassThreads) k_reclass(DecodeArgs a) {
           atomicAdd(&ev_s[h * 3 + (o == DKV_CLASS_K4V2 ? 2 : (cn == DKV_CLASS_K4V2 ? 0 : 1))], 1);
         }
       } else {  // the new token (position ctx)
-        cls[j] = static_cast<uint8_t>(0x80u | (3u << 2) | cn);
-        const int64_t u = u0 + h;
-        a.ucnt[u].w = static_cast<int32_t>(old[k] | (cn << 8) | (1u << 16));
-        if (cn != DKV_CLASS_PRUNE) {
-          const uint4 *kr = reinterpret_cast<const uint4 *>(a.k_new + u * DKV_HEAD_DIM);
-          const uint4 *vr = reinterpret_cast<const uint4 *>(a.v_new + u * DKV_HEAD_DIM);
-          bool oor = false;
-          for (int q = 0; q < DKV_HEAD_DIM / 8; ++q) oor |= words_out_of_range(__ldg(kr + q)) |
-                                                          words_out_of_range(__ldg(vr + q));
-          if (oor) set_error(&a.ws->err, DKV_E_RANGE);
-        }
+        new_token(a, cls + j, u0 + h, o, cn);
       }
     }
   }

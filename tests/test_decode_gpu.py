@@ -245,3 +245,10 @@ def test_decode_heavy_churn(p_prune, p_demote):
     of 32, and lists shrink by many pages at once."""
     w = W.small("dec_churn", lens=[700, 9, 520, 1, 333], L=2, Hq=8, Hkv=2)
     _run(w, cap=720, steps=6, p_prune=p_prune, p_demote=p_demote, slot_check_every=1)
+
+
+def test_decode_zero_low_threshold():
+    """alpha_l = 0: nothing is pruned by score and the threshold test takes the
+    IEEE division for every row."""
+    w = W.small("dec_a0", lens=[300, 77, 5], L=1, Hq=8, Hkv=2, alpha_h=0.7, alpha_l=0.0)
+    _run(w, cap=320, steps=5, p_prune=0.05, p_demote=0.1, slot_check_every=5)
