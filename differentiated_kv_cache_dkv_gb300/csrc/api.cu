@@ -227,7 +227,7 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
 
 int32_t dkv_decode_workspace_size(const dkv_decode_batch *b, size_t *bytes) {
   if (!bytes || !valid_decode(b)) return DKV_E_INVAL;
-  *bytes = dkv::dec_ws_layout(static_cast<int64_t>(b->L) * b->R * b->Hkv).bytes;
+  *bytes = dkv::dec_ws_layout(static_cast<int64_t>(b->L) * b->R * b->Hkv, static_cast<int64_t>(b->L) * b->R).bytes;
   return DKV_OK;
 }
 
@@ -254,7 +254,7 @@ int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dk
       !(p->alpha_h >= p->alpha_l) || p->reserved != 0)
     return DKV_E_INVAL;
   const int64_t U = static_cast<int64_t>(b->L) * b->R * b->Hkv;
-  const dkv::DecWsLayout lay = dkv::dec_ws_layout(U);
+  const dkv::DecWsLayout lay = dkv::dec_ws_layout(U, static_cast<int64_t>(b->L) * b->R);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.bytes) return DKV_E_INVAL;
   const int32_t words = (b->cap + 31) / 32;
   const int32_t hpc = apply_heads(b->Hkv, words, t->pmax);
@@ -271,6 +271,8 @@ int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dk
   a.ucnt = reinterpret_cast<int4 *>(ws + lay.ucnt);
   a.part = reinterpret_cast<uint64_t *>(ws + lay.part);
   a.plan = reinterpret_cast<dkv::DecPlan *>(ws + lay.plan);
+  a.lcnt = reinterpret_cast<int32_t *>(ws + lay.lcnt);
+  a.list = reinterpret_cast<uint32_t *>(ws + lay.list);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Profiler *prof = static_cast<Profiler *>(p->profiler);

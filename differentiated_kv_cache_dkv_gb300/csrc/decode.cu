@@ -95,6 +95,8 @@ __device__ __noinline__ void new_token(const DecodeArgs &a, uint8_t *c, int64_t 
 template <int kV4>  // float4 loads per row (G / 4); 0 = scalar loads
 __global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
   __shared__ int32_t ev_s[kMaxHq * 3];  // per head: demoted, K8V4 pruned, K4V2 pruned
+  __shared__ uint32_t mk_s[kMarkList];  // this block's changes, listed for the apply kernel
+  __shared__ int32_t mk_n, mk_base;
   const int32_t r = blockIdx.y, l = blockIdx.z;
   const int32_t i0 = blockIdx.x * kReclassChunk;
   const int32_t ctx = __ldg(a.ctx_lens + r), nw = __ldg(a.new_lens + r);
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
   const int32_t i1 = min(N, i0 + kReclassChunk);
   const int Hkv = a.Hkv, G = a.G;
   for (int t = threadIdx.x; t < Hkv * 3; t += blockDim.x) ev_s[t] = 0;
+  if (threadIdx.x == 0) mk_n = 0;
   __syncthreads();
   const float thr_h = __fdiv_rn(a.alpha_h, static_cast<float>(N));
   const float thr_l = __fdiv_rn(a.alpha_l, static_cast<float>(N));
@@ -205,13 +208,29 @@ __global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
         if (cn < o) {
           cls[j] = static_cast<uint8_t>(0x80u | (o << 2) | cn);
           atomicAdd(&ev_s[h * 3 + (o == DKV_CLASS_K4V2 ? 2 : (cn == DKV_CLASS_K4V2 ? 0 : 1))], 1);
+          const int32_t q = atomicAdd(&mk_n, 1);
+          if (q < kMarkList) mk_s[q] = (static_cast<uint32_t>(i0 + ii) << 11) | (h << 4) | (o << 2) | cn;
         }
       } else {  // the new token (position ctx)
         new_token(a, cls + j, u0 + h, o, cn);
+        const int32_t q = atomicAdd(&mk_n, 1);
+        if (q < kMarkList) mk_s[q] = (static_cast<uint32_t>(i0 + ii) << 11) | (h << 4) | (3u << 2) | cn;
       }
     }
   }
   __syncthreads();
+  // the block's changes join its (layer, request) list; a block with more
+  // than the buffer holds pushes the list past its capacity, so the apply
+  // kernel scans the class bytes of that (layer, request) instead
+  const int32_t nmk = mk_n;
+  if (threadIdx.x == 0 && nmk > 0)
+    mk_base = atomicAdd(a.lcnt + (static_cast<int64_t>(l) * a.R + r), nmk <= kMarkList ? nmk : (1 << 24));
+  __syncthreads();
+  if (nmk > 0 && nmk <= kMarkList) {
+    uint32_t *dst = a.list + (static_cast<int64_t>(l) * a.R + r) * kMarkList;
+    for (int q = threadIdx.x; q < nmk; q += blockDim.x)
+      if (mk_base + q < kMarkList) dst[mk_base + q] = mk_s[q];
+  }
   for (int t = threadIdx.x; t < Hkv * 3; t += blockDim.x) {
     const int32_t n = ev_s[t];
     if (n == 0) continue;
@@ -798,14 +817,31 @@ __device__ __forceinline__ void mark_slot(const DecodeArgs &a, uint32_t mark, in
   else *so = -1;  // pruned
 }
 
-// Marks of one 16-byte vector of class bytes: the final class (or the old one
-// when the call failed) is written back and each removed token is listed
-// for its unit's warp (or handled here if the list is full).  Rare, so out of
-// line.
+// One changed class byte (position i, head h; old class 3 = the new token):
+// the final class (or the old one when the call failed) is written back and a
+// removed token is listed for its unit's warp (or handled here if the list is
+// full).
+__device__ __forceinline__ void take_mark(const DecodeArgs &a, int32_t i, int32_t h, uint32_t old, uint32_t cn,
+                                          int32_t h0, int32_t err, int64_t u0, int64_t blk, const DecPlan *plan_s,
+                                          uint32_t *bm, int32_t words, uint32_t *mk, int32_t *mk_n) {
+  uint8_t *c = a.classes + blk + static_cast<int64_t>(i) * a.Hkv + h;
+  if (err != 0) {  // revert
+    *c = static_cast<uint8_t>(old == 3u ? (a.ucnt[u0 + h].w & 0xff) : old);
+    return;
+  }
+  *c = static_cast<uint8_t>(cn);
+  if (old == 3u) return;  // the new token: handled from the plan
+  const uint32_t mark = (static_cast<uint32_t>(i) << 4) | (old << 2) | cn;
+  const int32_t k = atomicAdd(&mk_n[h - h0], 1);
+  if (k < kMarkCap) mk[(h - h0) * kMarkCap + k] = mark;
+  else mark_slot(a, mark, blk + h, plan_s[h - h0], bm + 3 * (h - h0) * words, words);
+}
+
+// Marks of one 16-byte vector of class bytes (the scan path).  Rare, so out
+// of line.
 __device__ __noinline__ void take_marks(const DecodeArgs &a, uint4 x, int32_t vi, int32_t nbytes, int32_t h0,
                                         int32_t nh, int32_t err, int64_t u0, int64_t blk, const DecPlan *plan_s,
                                         uint32_t *bm, int32_t words, uint32_t *mk, int32_t *mk_n) {
-  uint8_t *cls = a.classes + blk;
   const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
   for (int e = 0; e < 16; ++e) {
     const uint32_t b = (xw[e >> 2] >> (8 * (e & 3))) & 255u;
@@ -814,17 +850,20 @@ __device__ __noinline__ void take_marks(const DecodeArgs &a, uint4 x, int32_t vi
     if (idx >= nbytes) continue;
     const int32_t i = idx / a.Hkv, h = idx - i * a.Hkv;
     if (h < h0 || h >= h0 + nh) continue;
-    const uint32_t old = (b >> 2) & 3u, cn = b & 3u;
-    if (err != 0) {  // revert
-      cls[idx] = static_cast<uint8_t>(old == 3u ? (a.ucnt[u0 + h].w & 0xff) : old);
-      continue;
-    }
-    cls[idx] = static_cast<uint8_t>(cn);
-    if (old == 3u) continue;  // the new token: handled from the plan
-    const uint32_t mark = (static_cast<uint32_t>(i) << 4) | (old << 2) | cn;
-    const int32_t k = atomicAdd(&mk_n[h - h0], 1);
-    if (k < kMarkCap) mk[(h - h0) * kMarkCap + k] = mark;
-    else mark_slot(a, mark, blk + h, plan_s[h - h0], bm + 3 * (h - h0) * words, words);
+    take_mark(a, i, h, (b >> 2) & 3u, b & 3u, h0, err, u0, blk, plan_s, bm, words, mk, mk_n);
+  }
+}
+
+// Listed changes of one (layer, request), when the list holds them all.
+__device__ __noinline__ void take_list(const DecodeArgs &a, const uint32_t *list, int32_t n, int32_t h0, int32_t nh,
+                                       int32_t err, int64_t u0, int64_t blk, const DecPlan *plan_s, uint32_t *bm,
+                                       int32_t words, uint32_t *mk, int32_t *mk_n) {
+  for (int32_t q = threadIdx.x; q < n; q += blockDim.x) {
+    const uint32_t e = list[q];
+    const int32_t h = static_cast<int32_t>((e >> 4) & 127u);
+    if (h < h0 || h >= h0 + nh) continue;
+    take_mark(a, static_cast<int32_t>(e >> 11), h, (e >> 2) & 3u, e & 3u, h0, err, u0, blk, plan_s, bm, words, mk,
+              mk_n);
   }
 }
 
@@ -868,7 +907,13 @@ __global__ void __launch_bounds__(32 * kMaxApplyWarps, 3) k_apply(DecodeArgs a, 
   uint8_t *cls = a.classes + blk;
   const int32_t nbytes = N * a.Hkv;
   const int32_t nvec = (nbytes + 15) >> 4;
-  // loads four vectors per thread at a time; the rare marked ones go out of line
+  const int64_t lr = static_cast<int64_t>(l) * a.R + r;
+  const int32_t n_list = a.lcnt[lr];
+  if (n_list <= kMarkList) {  // every change of this (layer, request) is listed
+    take_list(a, a.list + lr * kMarkList, n_list, h0, nh, err, u0, blk, plan_s, bm, words, mk, mk_n);
+  } else {
+  // otherwise scan the class bytes, four vectors per thread at a time; the
+  // rare marked ones go out of line
   for (int32_t vb = 0; vb < nvec; vb += 4 * blockDim.x) {
     uint4 x[4];
 #pragma unroll
@@ -880,6 +925,7 @@ __global__ void __launch_bounds__(32 * kMaxApplyWarps, 3) k_apply(DecodeArgs a, 
     for (int q = 0; q < 4; ++q)
       if (((x[q].x | x[q].y | x[q].z | x[q].w) & 0x80808080u) != 0u)
         take_marks(a, x[q], vb + q * blockDim.x + tid, nbytes, h0, nh, err, u0, blk, plan_s, bm, words, mk, mk_n);
+  }
   }
   __syncthreads();
   if (err != 0 || warp >= nh) return;

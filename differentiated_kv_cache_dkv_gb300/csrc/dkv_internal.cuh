@@ -163,23 +163,29 @@ struct __align__(16) DecPlan {
   int32_t need_hi, need_lo, off_d, off_f; // pages after the step, scan offsets (new, freed)
 };
 
+constexpr int kMarkList = 1024;       // listed changes per (layer, request); more fall back to a scan
+
 struct DecWsLayout {
   size_t ucnt;   // int4 [U]: demoted, K8V4 pruned, K4V2 pruned, new-token word
   size_t part;   // uint64 [npart]
+  size_t lcnt;   // int32 [L * R]: changes listed per (layer, request)
   size_t plan;   // DecPlan [U]
-  size_t reset;  // bytes zeroed at the start of a call (header, counters, partitions)
+  size_t list;   // uint32 [L * R][kMarkList]: position << 11 | head << 4 | old << 2 | new
+  size_t reset;  // bytes zeroed at the start of a call (header, counters, partitions, list counts)
   size_t bytes;
   int32_t npart;
 };
 
-inline DecWsLayout dec_ws_layout(int64_t U) {
+inline DecWsLayout dec_ws_layout(int64_t U, int64_t LR) {
   DecWsLayout w{};
   w.npart = static_cast<int32_t>((U + 255) / 256);
   size_t o = align256(sizeof(DecWsHeader));
   w.ucnt = o; o = align256(o + 16 * static_cast<size_t>(U));
   w.part = o; o = align256(o + sizeof(uint64_t) * w.npart);
+  w.lcnt = o; o = align256(o + sizeof(int32_t) * static_cast<size_t>(LR));
   w.reset = o;
   w.plan = o; o = align256(o + sizeof(DecPlan) * static_cast<size_t>(U));
+  w.list = o; o = align256(o + sizeof(uint32_t) * kMarkList * static_cast<size_t>(LR));
   w.bytes = o;
   return w;
 }
@@ -202,7 +208,9 @@ struct DecodeArgs {
   DecWsHeader *ws;
   int4 *ucnt;
   uint64_t *part;
+  int32_t *lcnt;
   DecPlan *plan;
+  uint32_t *list;
 };
 
 }  // namespace dkv
