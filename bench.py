@@ -498,7 +498,7 @@ def run_native_decode(a):
     ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
     kt = prof.read()
     prof.close()
-    names = ("reset", "k_reclass", "k_dscan", "k_apply")
+    names = ("reset", "k_reclass", "k_dscan", "k_apply", "k_demote")
     kernel_ms = {n: statistics.mean(c[i] for c in kt) for i, n in enumerate(names)}
     ms_max = max_over_ranks(ms, dev, world)
     value = whole_job_rate(live_rows, world, ms_max)
@@ -577,7 +577,7 @@ def run_native_decode(a):
             "new_token_rows_per_s": whole_job_rate(new_rows, world, ms_max),
             "pool": {"F": F, "prefill_pages": used, "head_start": head0, "head_end": head1,
                      "wraps": head1 // F - head0 // F},
-            "gpu_launches": a.steps * 4,
+            "gpu_launches": a.steps * 4,  # counter reset is a memset: k_reclass, k_dscan, k_apply, k_demote
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -227,7 +227,8 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
 
 int32_t dkv_decode_workspace_size(const dkv_decode_batch *b, size_t *bytes) {
   if (!bytes || !valid_decode(b)) return DKV_E_INVAL;
-  *bytes = dkv::dec_ws_layout(static_cast<int64_t>(b->L) * b->R * b->Hkv, static_cast<int64_t>(b->L) * b->R).bytes;
+  *bytes = dkv::dec_ws_layout(static_cast<int64_t>(b->L) * b->R * b->Hkv, static_cast<int64_t>(b->L) * b->R,
+                              static_cast<int64_t>(b->L) * b->R * b->cap * b->Hkv).bytes;
   return DKV_OK;
 }
 
@@ -254,7 +255,8 @@ int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dk
       !(p->alpha_h >= p->alpha_l) || p->reserved != 0)
     return DKV_E_INVAL;
   const int64_t U = static_cast<int64_t>(b->L) * b->R * b->Hkv;
-  const dkv::DecWsLayout lay = dkv::dec_ws_layout(U, static_cast<int64_t>(b->L) * b->R);
+  const dkv::DecWsLayout lay =
+      dkv::dec_ws_layout(U, static_cast<int64_t>(b->L) * b->R, static_cast<int64_t>(b->L) * b->R * b->cap * b->Hkv);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < lay.bytes) return DKV_E_INVAL;
   const int32_t words = (b->cap + 31) / 32;
   const int32_t hpc = apply_heads(b->Hkv, words, t->pmax);
@@ -273,6 +275,8 @@ int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dk
   a.plan = reinterpret_cast<dkv::DecPlan *>(ws + lay.plan);
   a.lcnt = reinterpret_cast<int32_t *>(ws + lay.lcnt);
   a.list = reinterpret_cast<uint32_t *>(ws + lay.list);
+  a.jobs = reinterpret_cast<dkv::DemJob *>(ws + lay.jobs);
+  a.njobs = lay.njobs;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Profiler *prof = static_cast<Profiler *>(p->profiler);
@@ -293,6 +297,7 @@ int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dk
   mark(3);
   if (const int32_t rc = cuda_status(dkv::launch_apply(a, hpc, words, s))) return rc;
   mark(4);
+  if (const int32_t rc = cuda_status(dkv::launch_demote(a, sms * 8, s))) return rc;
   mark(5);
   return DKV_OK;
 }

@@ -597,9 +597,51 @@ __device__ __forceinline__ uint64_t pack_bits(const uint32_t (&q)[kPer], int wid
   return w;
 }
 
-// Requantise the demoted tokens (K8V4 -> K4V2) into K4V2 slots keep_lo + k in
-// ascending position order.  Eight lanes per token (16 channels each), four
-// tokens per pass.
+// Requantise one demoted token, 8 lanes (lane t: channels 16t .. 16t+15):
+// dequantise its K8V4 codes (fma(q, s, z)), quantise 4-bit K and 2-bit V and
+// store them, with the metadata and position, into K4V2 slot ds of page dpg.
+// Every lane of the warp calls it (the reductions shuffle within 8 lanes).
+__device__ __forceinline__ void requant8(const DecodeArgs &a, uint4 kc, uint2 vc, uint2 meta, bool ok, uint8_t *dpg,
+                                         int64_t ds, int32_t pos, int t) {
+  const int64_t P = a.P;
+  float x[16];
+  uint32_t q[16];
+  uint16_t ks2, kz2, vs2, vz2;
+  {  // K then V, one 16-channel piece at a time (fewer live registers)
+    const float ks = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.x & 0xffffu)));
+    const float kz = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.x >> 16)));
+    const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = __fmaf_rn(static_cast<float>((kw[i >> 2] >> (8 * (i & 3))) & 255u), ks, kz);
+    quant_vals<16, 8>(x, 15, q, ks2, kz2);
+    if (ok) {
+      const uint64_t pk = pack_bits<16>(q, 4);
+      reinterpret_cast<uint2 *>(dpg + 64 * ds)[t] = make_uint2(static_cast<uint32_t>(pk), static_cast<uint32_t>(pk >> 32));
+    }
+  }
+  {
+    const float vs = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.y & 0xffffu)));
+    const float vz = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.y >> 16)));
+    const uint32_t vw[2] = {vc.x, vc.y};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = __fmaf_rn(static_cast<float>((vw[i >> 3] >> (4 * (i & 7))) & 15u), vs, vz);
+    quant_vals<16, 8>(x, 3, q, vs2, vz2);
+    if (ok) reinterpret_cast<uint32_t *>(dpg + 128 * P + 32 * ds)[t] = static_cast<uint32_t>(pack_bits<16>(q, 2));
+  }
+  if (ok && t == 0) {
+    *reinterpret_cast<uint2 *>(dpg + 192 * P + 8 * ds) =
+        make_uint2(static_cast<uint32_t>(ks2) | (static_cast<uint32_t>(kz2) << 16),
+                   static_cast<uint32_t>(vs2) | (static_cast<uint32_t>(vz2) << 16));
+    *reinterpret_cast<int32_t *>(dpg + 208 * P + 4 * ds) = pos;
+  }
+}
+
+// The demoted tokens (K8V4 -> K4V2) go to K4V2 slots keep_lo + k in ascending
+// position order.  Normally each token's K8V4 slot bytes are copied, one lane
+// per token, into a job for k_demote (the copy must happen before the K8V4
+// hole-fill may overwrite the slot; the requantisation runs later, spread over
+// the whole GPU); when the call's job buffer is full, this warp requantises
+// them in place, 8 lanes per token.
 __device__ void demote(const DecodeArgs &a, const UnitView &v, const uint32_t *dem, int32_t *buf, int lane) {
   int32_t cur = 0, k = 0;
   const int grp = lane >> 3, t = lane & 7;
@@ -615,63 +657,73 @@ __device__ void demote(const DecodeArgs &a, const UnitView &v, const uint32_t *d
       if (my_hs >= 0 && my_hs < v.p.n_hi) my_src = list_page(a, v, true, my_hs / a.P);
       my_dst = list_page(a, v, false, (v.p.keep_lo + k + lane) / (2 * a.P));
     }
-    for (int g = 0; g < nd; g += 4) {
-      const int j = g + grp;
-      const bool act = j < nd;
-      const int32_t hs = __shfl_sync(0xffffffffu, my_hs, j & 31);
-      const int32_t sid = __shfl_sync(0xffffffffu, my_src, j & 31);
-      const int32_t did = __shfl_sync(0xffffffffu, my_dst, j & 31);
-      const int32_t pos = act ? buf[j] : 0;
-      bool ok = act && hs >= 0 && hs < v.p.n_hi && sid >= 0 && did >= 0;
-      const int64_t ss = hs % P, ds = (v.p.keep_lo + k + j) % (2 * P);
-      const uint8_t *spg = a.pages + static_cast<int64_t>(sid) * 216 * P;
-      uint8_t *dpg = a.pages + static_cast<int64_t>(did) * 216 * P;
-      SlotAddr dst{dpg + 64 * ds, dpg + 128 * P + 32 * ds, dpg + 192 * P + 8 * ds, dpg + 208 * P + 4 * ds};
-      uint4 kc = make_uint4(0u, 0u, 0u, 0u);
-      uint2 vc = make_uint2(0u, 0u);
-      uint2 meta = make_uint2(0u, 0u);
-      int32_t spos = -1;
-      if (ok) {
-        kc = reinterpret_cast<const uint4 *>(spg + 128 * ss)[t];            // channels 16t .. 16t+15, 8-bit
-        vc = reinterpret_cast<const uint2 *>(spg + 128 * P + 64 * ss)[t];   // channels 16t .. 16t+15, 4-bit
-        meta = *reinterpret_cast<const uint2 *>(spg + 192 * P + 8 * ss);
-        spos = *reinterpret_cast<const int32_t *>(spg + 208 * P + 4 * ss);
-      }
-      if (ok && spos != pos) ok = false;
-      if (act && !ok && t == 0) atomicCAS(a.status, 0, DKV_E_INTERNAL);
-      const float ks = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.x & 0xffffu)));
-      const float kz = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.x >> 16)));
-      const float vs = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.y & 0xffffu)));
-      const float vz = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.y >> 16)));
-      float xk[16], xv[16];
-      const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
-      const uint32_t vw[2] = {vc.x, vc.y};
+    int32_t base = 0;
+    if (lane == 0) base = atomicAdd(&a.ws->job_n, nd);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (static_cast<int64_t>(base) + nd <= a.njobs) {
+      if (lane < nd) {
+        const int32_t pos = buf[lane];
+        DemJob &jb = a.jobs[base + lane];
+        bool ok = my_hs >= 0 && my_hs < v.p.n_hi && my_src >= 0 && my_dst >= 0;
+        if (ok) {
+          const int64_t ss = my_hs % P;
+          const uint8_t *spg = a.pages + static_cast<int64_t>(my_src) * 216 * P;
+          const uint4 *kk = reinterpret_cast<const uint4 *>(spg + 128 * ss);
+          const uint4 *vv = reinterpret_cast<const uint4 *>(spg + 128 * P + 64 * ss);
+          uint4 kw[8], vw[4];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        xk[i] = __fmaf_rn(static_cast<float>((kw[i >> 2] >> (8 * (i & 3))) & 255u), ks, kz);
-        xv[i] = __fmaf_rn(static_cast<float>((vw[i >> 3] >> (4 * (i & 7))) & 15u), vs, vz);
-      }
-      uint32_t qk[16], qv[16];
-      uint16_t ks2, kz2, vs2, vz2;
-      quant_vals<16, 8>(xk, 15, qk, ks2, kz2);
-      quant_vals<16, 8>(xv, 3, qv, vs2, vz2);
-      if (ok) {
-        reinterpret_cast<uint2 *>(dst.k)[t] = make_uint2(static_cast<uint32_t>(pack_bits<16>(qk, 4)),
-                                                         static_cast<uint32_t>(pack_bits<16>(qk, 4) >> 32));
-        reinterpret_cast<uint32_t *>(dst.v)[t] = static_cast<uint32_t>(pack_bits<16>(qv, 2));
-        if (t == 0) {
-          *reinterpret_cast<uint2 *>(dst.meta) =
-              make_uint2(static_cast<uint32_t>(ks2) | (static_cast<uint32_t>(kz2) << 16),
-                         static_cast<uint32_t>(vs2) | (static_cast<uint32_t>(vz2) << 16));
-          *reinterpret_cast<int32_t *>(dst.pos) = pos;
-          a.slot_of[v.row0 + static_cast<int64_t>(pos) * v.Hkv] = v.p.keep_lo + k + j;
+          for (int i = 0; i < 8; ++i) kw[i] = kk[i];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) vw[i] = vv[i];
+          const uint2 meta = *reinterpret_cast<const uint2 *>(spg + 192 * P + 8 * ss);
+          const int32_t spos = *reinterpret_cast<const int32_t *>(spg + 208 * P + 4 * ss);
+          ok = spos == pos;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) jb.k[i] = kw[i];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) jb.v[i] = vw[i];
+          jb.meta = meta;
         }
+        if (!ok) atomicCAS(a.status, 0, DKV_E_INTERNAL);
+        const int32_t slot = v.p.keep_lo + k + lane;
+        jb.dst_page = ok ? my_dst : -1;
+        jb.dst_slot = slot % (2 * a.P);
+        jb.pos = pos;
+        if (ok) a.slot_of[v.row0 + static_cast<int64_t>(pos) * v.Hkv] = slot;
+      }
+    } else {
+      // the reservation ran past the buffer: its entries inside the buffer
+      // are marked empty (k_demote reads every reserved entry below the end)
+      if (lane < nd && static_cast<int64_t>(base) + lane < a.njobs) a.jobs[base + lane].dst_page = -1;
+      for (int g = 0; g < nd; g += 4) {
+        const int j = g + grp;
+        const bool act = j < nd;
+        const int32_t hs = __shfl_sync(0xffffffffu, my_hs, j & 31);
+        const int32_t sid = __shfl_sync(0xffffffffu, my_src, j & 31);
+        const int32_t did = __shfl_sync(0xffffffffu, my_dst, j & 31);
+        const int32_t pos = act ? buf[j] : 0;
+        bool ok = act && hs >= 0 && hs < v.p.n_hi && sid >= 0 && did >= 0;
+        const int64_t ss = hs % P, ds = (v.p.keep_lo + k + j) % (2 * P);
+        const uint8_t *spg = a.pages + static_cast<int64_t>(sid) * 216 * P;
+        uint4 kc = make_uint4(0u, 0u, 0u, 0u);
+        uint2 vc = make_uint2(0u, 0u);
+        uint2 meta = make_uint2(0u, 0u);
+        int32_t spos = -1;
+        if (ok) {
+          kc = reinterpret_cast<const uint4 *>(spg + 128 * ss)[t];
+          vc = reinterpret_cast<const uint2 *>(spg + 128 * P + 64 * ss)[t];
+          meta = *reinterpret_cast<const uint2 *>(spg + 192 * P + 8 * ss);
+          spos = *reinterpret_cast<const int32_t *>(spg + 208 * P + 4 * ss);
+        }
+        if (ok && spos != pos) ok = false;
+        if (act && !ok && t == 0) atomicCAS(a.status, 0, DKV_E_INTERNAL);
+        requant8(a, kc, vc, meta, ok, a.pages + static_cast<int64_t>(did) * 216 * P, ds, pos, t);
+        if (ok && t == 0) a.slot_of[v.row0 + static_cast<int64_t>(pos) * v.Hkv] = v.p.keep_lo + k + j;
       }
     }
     k += nd;
     __syncwarp();
   }
-  (void)P;
 }
 
 // Quantise and store the new token (bf16 row of 128 channels, 4 per lane).
@@ -950,6 +1002,39 @@ __global__ void __launch_bounds__(32 * kMaxApplyWarps, 3) k_apply(DecodeArgs a, 
   apply_unit(a, v, b3, b3 + words, b3 + 2 * words, buf + 32 * warp, stage + a.pmax * warp, lane);
 }
 
+// ----------------------------------------------------------------- k_demote --
+
+// The staged demotions of the call, requantised across the whole GPU: each
+// 8-lane group takes one job (grid-stride).  Runs after k_apply, whose K4V2
+// hole-fill has emptied the destination slots and whose page clears came
+// first; a failed call staged nothing.
+__global__ void __launch_bounds__(256) k_demote(DecodeArgs a) {
+  if (*reinterpret_cast<volatile int32_t *>(&a.ws->err) != 0) return;
+  const int64_t n = min(static_cast<int64_t>(a.ws->job_n), a.njobs);
+  const int lane = threadIdx.x & 31, grp = lane >> 3, t = lane & 7;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t P = a.P;
+  for (int64_t b = gw * 4; b < n; b += nw * 4) {
+    const int64_t j = b + grp;
+    const bool act = j < n;
+    uint4 kc = make_uint4(0u, 0u, 0u, 0u);
+    uint2 vc = make_uint2(0u, 0u), meta = make_uint2(0u, 0u);
+    int32_t page = -1, slot = 0, pos = 0;
+    if (act) {
+      const DemJob &jb = a.jobs[j];
+      kc = jb.k[t];
+      vc = reinterpret_cast<const uint2 *>(jb.v)[t];
+      meta = jb.meta;
+      page = jb.dst_page;
+      slot = jb.dst_slot;
+      pos = jb.pos;
+    }
+    const bool ok = act && page >= 0 && page < a.F;
+    requant8(a, kc, vc, meta, ok, a.pages + static_cast<int64_t>(ok ? page : 0) * 216 * P, slot, pos, t);
+  }
+}
+
 // ------------------------------------------------------------------ k_index --
 
 // Classes and slot index of every position from the pages: one warp per unit.
@@ -1022,6 +1107,11 @@ cudaError_t launch_apply(const DecodeArgs &a, int32_t hpc, int32_t words, cudaSt
   }
   const dim3 grid((a.Hkv + hpc - 1) / hpc, a.R, a.L);
   k_apply<<<grid, 32 * hpc, smem, s>>>(a, hpc, words);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_demote(const DecodeArgs &a, int grid, cudaStream_t s) {
+  k_demote<<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

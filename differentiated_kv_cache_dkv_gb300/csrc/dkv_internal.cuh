@@ -148,7 +148,7 @@ struct DecWsHeader {
   int32_t err;       // first device-side error of this call (0 = none)
   int32_t ticket;    // scan partition ticket counter
   int32_t npart;     // scan partitions
-  int32_t pad0;
+  int32_t job_n;     // demotion jobs staged for k_demote
   uint64_t head;     // free-list cursors when the call started
   uint64_t tail;
   int64_t dsum;      // new pages of the step
@@ -164,6 +164,18 @@ struct __align__(16) DecPlan {
 };
 
 constexpr int kMarkList = 1024;       // listed changes per (layer, request); more fall back to a scan
+constexpr int64_t kDemoteJobs = 1 << 20;  // staged demotions per call at most; more are done in place
+
+// One staged demotion: the token's K8V4 slot bytes and where its K4V2 copy goes.
+struct __align__(16) DemJob {
+  uint4 k[8];          // 8-bit K codes
+  uint4 v[4];          // 4-bit V codes
+  uint2 meta;          // fp16 k_scale, k_zero, v_scale, v_zero
+  int32_t dst_page;    // -1: nothing to write
+  int32_t dst_slot;
+  int32_t pos;
+  int32_t pad[3];
+};
 
 struct DecWsLayout {
   size_t ucnt;   // int4 [U]: demoted, K8V4 pruned, K4V2 pruned, new-token word
@@ -171,13 +183,16 @@ struct DecWsLayout {
   size_t lcnt;   // int32 [L * R]: changes listed per (layer, request)
   size_t plan;   // DecPlan [U]
   size_t list;   // uint32 [L * R][kMarkList]: position << 11 | head << 4 | old << 2 | new
+  size_t jobs;   // DemJob [njobs]
+  int64_t njobs;
   size_t reset;  // bytes zeroed at the start of a call (header, counters, partitions, list counts)
   size_t bytes;
   int32_t npart;
 };
 
-inline DecWsLayout dec_ws_layout(int64_t U, int64_t LR) {
+inline DecWsLayout dec_ws_layout(int64_t U, int64_t LR, int64_t rows) {
   DecWsLayout w{};
+  w.njobs = rows < kDemoteJobs ? rows : kDemoteJobs;
   w.npart = static_cast<int32_t>((U + 255) / 256);
   size_t o = align256(sizeof(DecWsHeader));
   w.ucnt = o; o = align256(o + 16 * static_cast<size_t>(U));
@@ -186,6 +201,7 @@ inline DecWsLayout dec_ws_layout(int64_t U, int64_t LR) {
   w.reset = o;
   w.plan = o; o = align256(o + sizeof(DecPlan) * static_cast<size_t>(U));
   w.list = o; o = align256(o + sizeof(uint32_t) * kMarkList * static_cast<size_t>(LR));
+  w.jobs = o; o = align256(o + sizeof(DemJob) * static_cast<size_t>(w.njobs));
   w.bytes = o;
   return w;
 }
@@ -211,6 +227,8 @@ struct DecodeArgs {
   int32_t *lcnt;
   DecPlan *plan;
   uint32_t *list;
+  DemJob *jobs;
+  int64_t njobs;
 };
 
 }  // namespace dkv
@@ -229,6 +247,7 @@ int pack_blocks_per_sm();
 cudaError_t launch_reclass(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_dscan(const DecodeArgs &a, int32_t npart, cudaStream_t s);
 cudaError_t launch_apply(const DecodeArgs &a, int32_t hpc, int32_t words, cudaStream_t s);
+cudaError_t launch_demote(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_index(const DecodeArgs &a, int grid, cudaStream_t s);
 size_t apply_smem(int32_t hpc, int32_t words, int32_t pmax);
 }  // namespace dkv

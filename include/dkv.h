@@ -254,7 +254,8 @@ int32_t dkv_decode_index(const dkv_decode_batch *b, const dkv_pool *pool, const 
  * TIMEOUT, and on INTERNAL found before any page is touched, the step
  * changes nothing (classes restored); INTERNAL found while moving slots
  * leaves the state undefined.  With dkv_params.profiler the five intervals
- * are: counter reset, reclassification, page scan, apply, (empty). */
+ * are: counter reset, reclassification, page scan, apply, requantisation of
+ * the demoted tokens. */
 int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dkv_pool *pool,
                         const dkv_tables *t, void *workspace, size_t workspace_bytes, void *stream);
 
