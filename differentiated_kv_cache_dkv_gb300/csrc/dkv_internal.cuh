@@ -192,7 +192,10 @@ struct DecWsLayout {
 
 inline DecWsLayout dec_ws_layout(int64_t U, int64_t LR, int64_t rows) {
   DecWsLayout w{};
-  w.njobs = rows < kDemoteJobs ? rows : kDemoteJobs;
+  // room for demoting one held row in 16 per call (the seeded generation
+  // demotes about 1 in 200); a step that demotes more does the rest in place
+  const int64_t want = rows / 16 + 64;
+  w.njobs = want < kDemoteJobs ? want : kDemoteJobs;
   w.npart = static_cast<int32_t>((U + 255) / 256);
   size_t o = align256(sizeof(DecWsHeader));
   w.ucnt = o; o = align256(o + 16 * static_cast<size_t>(U));
