@@ -74,10 +74,10 @@ def workload_name(a) -> str:
 PACK_TRAFFIC = {"workload": "llama", "source_sha1": "9105ef3e12a6", "bytes": 16 * (537.732352 + 130.510336) * 1e6}
 
 # DRAM traffic of k_reclass per algorithmic byte, from one ncu capture on 4
-# layers x 64 requests of the decode workload (181.0 MB for 176.2 MB; traffic
+# layers x 64 requests of the decode workload (181.6 MB for 176.2 MB; traffic
 # grows with the live rows) (profiles/decode_step.md); valid only for the
 # kernel source it was measured on.
-RECLASS_TRAFFIC = {"workload": "decode", "source_sha1": "560086cb1980", "per_byte": (177.175040 + 3.787776) / 176.177616}
+RECLASS_TRAFFIC = {"workload": "decode", "source_sha1": "bc94787e4733", "per_byte": (177.162496 + 4.481536) / 176.177616}
 
 
 def _source_sha(name: str):
