@@ -58,7 +58,7 @@ class _DecodeBatch(ctypes.Structure):
         ("D", ctypes.c_int32), ("cap", ctypes.c_int32), ("unit_base", ctypes.c_int64),
         ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("sig_sum", ctypes.c_void_p),
         ("sig_cnt", ctypes.c_void_p), ("ctx_lens", ctypes.c_void_p), ("new_lens", ctypes.c_void_p),
-        ("classes", ctypes.c_void_p),
+        ("classes", ctypes.c_void_p), ("window", ctypes.c_int32), ("mode", ctypes.c_int32),
     ]
 
 
@@ -187,7 +187,9 @@ def decode_step(dinp: dict, alpha_h: float, alpha_l: float, pool: Pool, tables: 
     ``dinp`` holds numpy arrays: k_new, v_new (uint16 bf16 bits [L][R][Hkv][128]),
     sig_sum (float32 [L][R*cap][Hq]), sig_cnt (int32 [R*cap]), ctx_lens, new_lens
     (int32 [R]), classes (uint8 [L][R*cap][Hkv], updated in place), and the ints
-    L, R, Hq, Hkv, cap (and optionally unit_base).
+    L, R, Hq, Hkv, cap (and optionally unit_base, window and mode: the recent
+    window W and the candidate policy, 0 = re-score all older tokens, 1 = only
+    the token leaving the window).
     """
     arrs = {k: np.ascontiguousarray(dinp[k]) for k in ("k_new", "v_new", "sig_sum", "sig_cnt", "ctx_lens",
                                                         "new_lens")}
@@ -196,7 +198,7 @@ def decode_step(dinp: dict, alpha_h: float, alpha_l: float, pool: Pool, tables: 
     b = _DecodeBatch(int(dinp["L"]), int(dinp["R"]), int(dinp["Hq"]), int(dinp["Hkv"]), 128, int(dinp["cap"]),
                      int(dinp.get("unit_base", 0)), _ptr(arrs["k_new"]), _ptr(arrs["v_new"]),
                      _ptr(arrs["sig_sum"]), _ptr(arrs["sig_cnt"]), _ptr(arrs["ctx_lens"]), _ptr(arrs["new_lens"]),
-                     _ptr(cls))
+                     _ptr(cls), int(dinp.get("window", 0)), int(dinp.get("mode", 0)))
     p = pool._c()
     t = tables._c()
     return int(lib().oracle_decode_step(ctypes.byref(b), float(alpha_h), float(alpha_l), ctypes.byref(p),

@@ -61,6 +61,16 @@
  *      of the lists' pages are cleared (zero codes and metadata, position
  *      -1).  A step with new = 0 and no class change leaves everything as it
  *      was.
+ *  D9  Recent window and candidate policy (the review's Algorithm 1: a
+ *      window of the W most recent tokens stays at high precision, and a
+ *      candidate token is classified once, irreversibly, as it leaves the
+ *      window).  With window W >= 0 the window after the step is positions
+ *      [N - W, N).  The new token enters as K8V4 when W >= 1 and is
+ *      classified when W = 0.  Held tokens inside the window keep their
+ *      class.  Mode 0 re-scores every older held token as in D; mode 1
+ *      re-scores only the token the new one pushes out of the window,
+ *      position ctx - W (when there is a new token and W >= 1).  W = 0 with
+ *      mode 0 is D itself.
  */
 #include "dkv_oracle.h"
 
@@ -496,6 +506,7 @@ extern "C" int32_t oracle_decode_step(const oracle_decode_batch *b, float alpha_
     return ORACLE_E_INVAL;
   if (!(alpha_l >= 0.0f) || !(alpha_h >= alpha_l) || !std::isfinite(alpha_h)) return ORACLE_E_INVAL;
   if (pool->P < 2 || pool->P % 2 != 0 || pool->F < 1 || t->pmax < 1) return ORACLE_E_INVAL;
+  if (b->window < 0 || (b->mode != 0 && b->mode != 1)) return ORACLE_E_INVAL;
   const int64_t L = b->L, R = b->R, Hq = b->Hq, Hkv = b->Hkv, cap = b->cap, P = pool->P, F = pool->F;
   const int64_t G = Hq / Hkv, U = L * R * Hkv, pmax = t->pmax;
   for (int64_t r = 0; r < R; ++r) {
@@ -513,12 +524,21 @@ extern "C" int32_t oracle_decode_step(const oracle_decode_batch *b, float alpha_
       if (N == 0) continue;
       const float thr_h = alpha_h / static_cast<float>(N);
       const float thr_l = alpha_l / static_cast<float>(N);
+      const int64_t ctx = b->ctx_lens[r], W = b->window;
       for (int64_t i = 0; i < N; ++i) {
+        const bool is_new = i >= ctx;
+        /* reading D9: which positions are (re)classified this step */
+        if (!is_new) {
+          if (i >= N - W) continue;                               /* in the window: kept */
+          if (b->mode == 1 && !(b->new_lens[r] == 1 && W >= 1 && i == ctx - W)) continue;
+        }
         const int64_t tok = r * cap + i;
         const int32_t cnt = b->sig_cnt[tok];
         for (int64_t h = 0; h < Hkv; ++h) {
           uint8_t cls;
-          if (cnt == 0) {
+          if (is_new && W >= 1) {
+            cls = 2;                                               /* enters the window */
+          } else if (cnt == 0) {
             cls = 2;
           } else {
             float s = NAN;

@@ -109,6 +109,8 @@ typedef struct oracle_decode_batch {
   const int32_t *ctx_lens; /* [R] tokens before this step */
   const int32_t *new_lens; /* [R] 0 or 1 */
   uint8_t *classes;        /* in/out [L][R * cap][Hkv] */
+  int32_t window;          /* W: the last W positions are the recent window (reading D9) */
+  int32_t mode;            /* 0: re-score every older held token; 1: only the token leaving the window */
 } oracle_decode_batch;
 
 /* Decode step (reading D in dkv_oracle.cpp).  t->fwd and t->unit_hdr are the

@@ -19,8 +19,10 @@ class HostDecode:
     """Oracle-side decode state of a workload: pool, unit tables and the
     capacity-strided context (sig, counts, classes) after an oracle prefill."""
 
-    def __init__(self, w: W.Workload, cap: int, F: int | None = None, seed: int | None = None, inp=None):
+    def __init__(self, w: W.Workload, cap: int, F: int | None = None, seed: int | None = None, inp=None,
+                 window: int = 0, mode: int = 0):
         self.w, self.cap = w, cap
+        self.window, self.mode = window, mode
         self.pmax = decode_pmax(cap, w.P)
         inp = W.make_inputs(w, seed) if inp is None else inp
         self.pool = oracle.Pool(F or w.pool_pages, w.P)
@@ -45,7 +47,8 @@ class HostDecode:
                 "v_new": upd["v_new"].contiguous().view(torch.int16).numpy().view(np.uint16),
                 "sig_sum": self.ctx["sig_sum"].numpy(), "sig_cnt": self.ctx["sig_cnt"].numpy(),
                 "ctx_lens": self.ctx["ctx_lens"].numpy(),
-                "new_lens": upd["new_lens"].numpy().astype(np.int32), "classes": self.classes}
+                "new_lens": upd["new_lens"].numpy().astype(np.int32), "classes": self.classes,
+                "window": self.window, "mode": self.mode}
 
     def step(self, upd: dict | None = None, **kw) -> int:
         """Draw this step's update (unless given) and run the oracle step."""

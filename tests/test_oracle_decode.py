@@ -296,3 +296,76 @@ def test_length_errors():
     assert int(upd["new_lens"][2]) == 0
     upd["new_lens"][2] = 1       # one more token than it can hold
     assert hd.step(upd) == oracle.E_LENS
+
+
+# ------------------------------------------------------------ recent window --
+
+def _held_classes(hd: HostDecode):
+    out = {}
+    for r in range(hd.w.R):
+        c = int(hd.ctx_lens[r])
+        out[r] = hd.classes[:, r * hd.cap:r * hd.cap + c].copy()
+    return out
+
+
+def test_window_covering_everything_only_appends():
+    """Mode 0 with a window longer than every request: no held token is
+    re-scored, each new token enters as K8V4, and every held token keeps its
+    slot bytes; the appended token's codes are the textbook 8-bit / 4-bit
+    quantisation of its row."""
+    w = _small()
+    hd = HostDecode(w, cap=560, window=10_000, mode=0)
+    before = _state(hd)
+    held = _held_classes(hd)
+    upd = W.decode_update_inputs(w, hd.ctx, 0, p_prune=0.2, p_demote=0.2)
+    ctx0 = hd.ctx_lens.copy()
+    assert hd.step(upd) == oracle.OK
+    after = _state(hd)
+    for r in range(w.R):
+        assert np.array_equal(hd.classes[:, r * 560:r * 560 + int(ctx0[r])], held[r])
+    for key, val in before.items():
+        assert after[key] == val, key  # same list, same slot, same bytes
+    kb = upd["k_new"].view(torch.int16).numpy().view(np.uint16)
+    vb = upd["v_new"].view(torch.int16).numpy().view(np.uint16)
+    for u in range(w.U):
+        l, r, h = u // (w.R * w.Hkv), (u // w.Hkv) % w.R, u % w.Hkv
+        if int(upd["new_lens"][r]) == 0:
+            continue
+        li, raw, _ = after[(u, int(ctx0[r]))]
+        assert li == 0  # K8V4
+        kq, vq, meta = slot_codes(raw, high=True)
+        _, k8, ks, kz = oracle.quant_row(kb[l, r, h], 8)
+        _, v4, vs, vz = oracle.quant_row(vb[l, r, h], 4)
+        assert np.array_equal(kq, k8) and np.array_equal(vq, v4) and list(meta) == [ks, kz, vs, vz]
+
+
+@pytest.mark.parametrize("window", [0, 3, 40])
+def test_candidate_mode_reclassifies_only_the_leaving_token(window):
+    """Mode 1: per request only position ctx - W (the token the new one pushes
+    out of the window) may change class, never upward; with W = 0 that is the
+    new token itself, classified as in prefill."""
+    w = _small()
+    hd = HostDecode(w, cap=600, window=window, mode=1)
+    for s in range(4):
+        held = _held_classes(hd)
+        ctx0 = hd.ctx_lens.copy()
+        upd = W.decode_update_inputs(w, hd.ctx, s, p_prune=0.2, p_demote=0.2)
+        assert hd.step(upd) == oracle.OK
+        for r in range(w.R):
+            c = int(ctx0[r])
+            now = hd.classes[:, r * 600:r * 600 + c]
+            diff = np.nonzero((now != held[r]).any(axis=(0, 2)))[0]
+            assert all(i == c - window for i in diff) if window >= 1 else diff.size == 0, (s, r, diff)
+            assert np.all(now <= held[r])
+            if int(upd["new_lens"][r]) and window >= 1:
+                assert np.all(hd.classes[:, r * 600 + c] == 2)
+        _state(hd)
+
+
+def test_window_invariants_over_steps_both_modes():
+    w = _small()
+    for mode in (0, 1):
+        hd = HostDecode(w, cap=600, window=16, mode=mode)
+        for s in range(6):
+            assert hd.step(p_prune=0.05, p_demote=0.05) == oracle.OK
+            _state(hd)
