@@ -43,6 +43,10 @@ def _args():
                     help="keep only this many layers (a reduced case for profiler captures; named in config)")
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first this-many requests (a reduced case; named in config)")
+    ap.add_argument("--window", type=int, default=0,
+                    help="decode: recent window W (tokens kept at K8V4; 0 = none)")
+    ap.add_argument("--decode-mode", type=int, default=0, choices=[0, 1],
+                    help="decode: 0 re-scores every older token, 1 only the one leaving the window")
     return ap.parse_args()
 
 
@@ -62,6 +66,8 @@ def workload(a):
 
 def workload_name(a) -> str:
     name = a.workload
+    if getattr(a, "window", 0) or getattr(a, "decode_mode", 0):
+        name += f" (window {a.window}, {'single candidate' if a.decode_mode else 'every token re-scored'})"
     if a.layers or a.requests:
         name += f" (reduced: {a.layers or 'all'} layers, {a.requests or 'all'} requests)"
     return name
@@ -77,7 +83,7 @@ PACK_TRAFFIC = {"workload": "llama", "source_sha1": "9105ef3e12a6", "bytes": 16 
 # layers x 64 requests of the decode workload (181.6 MB for 176.2 MB; traffic
 # grows with the live rows) (profiles/decode_step.md); valid only for the
 # kernel source it was measured on.
-RECLASS_TRAFFIC = {"workload": "decode", "source_sha1": "bc94787e4733", "per_byte": (177.162496 + 4.481536) / 176.177616}
+RECLASS_TRAFFIC = {"workload": "decode", "source_sha1": "5faafed4d5b3", "per_byte": (177.165312 + 3.728128) / 176.177616}
 
 
 def _source_sha(name: str):
@@ -392,10 +398,11 @@ class DecodeOracleSample:
     workload: layer 0 of its first n_req requests, prefilled by the oracle
     (untimed) and then stepped with the same seeded updates."""
 
-    def __init__(self, w, n_req: int = 16):
+    def __init__(self, w, n_req: int = 16, window: int = 0, mode: int = 0):
         import dataclasses
 
         self.w = dataclasses.replace(w, L=1, lens=list(w.lens[:n_req]))
+        self.window, self.mode = window, mode
         self.max_steps = int(w.extra.get("steps", 100))  # the workload's own run length
         self.steps = 0
         self._fresh()
@@ -403,7 +410,7 @@ class DecodeOracleSample:
     def _fresh(self):
         from tests.decode_helpers import HostDecode
 
-        self.hd = HostDecode(self.w, decode_cap(self.w, self.max_steps))
+        self.hd = HostDecode(self.w, decode_cap(self.w, self.max_steps), window=self.window, mode=self.mode)
         self.local = 0
 
     def step(self):
@@ -424,10 +431,10 @@ class DecodeOracleSample:
         return dt, live
 
 
-def decode_oracle_sample(w, seconds: float):
+def decode_oracle_sample(w, seconds: float, window: int = 0, mode: int = 0):
     """(live token-rows/s, steps, rows per step, seconds) of the oracle stepped
     until `seconds` of step time."""
-    smp = DecodeOracleSample(w)
+    smp = DecodeOracleSample(w, window=window, mode=mode)
     t_total, rows = 0.0, 0
     while t_total < seconds or smp.steps == 0:
         dt, live = smp.step()
@@ -453,7 +460,8 @@ def run_native_decode(a):
     w = workload(a)
     dev = torch.device("cuda", local)
     total = a.warmup + a.steps + a.e2e_steps + 1
-    dec, ctx, cap, used = decode_setup(w, dev, W.SEED_BASE + 1000 * rank, total)
+    dec, ctx, cap, used = decode_setup(w, dev, W.SEED_BASE + 1000 * rank, total, window=a.window,
+                                       mode=a.decode_mode)
     F = dec.pool.F
     stream = torch.cuda.current_stream()
     head0 = int(dec.pool.cursors[0])
@@ -473,7 +481,7 @@ def run_native_decode(a):
 
     prof = libdkv.Profiler(a.steps)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
-    live_rows, new_rows = 0, 0
+    live_rows, new_rows, scored = 0, 0, 0
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -484,6 +492,13 @@ def run_native_decode(a):
         upd, d = inputs(step_no)
         live_rows += int((ctx["ctx_lens"] + upd["new_lens"]).sum()) * w.L * w.Hkv
         new_rows += int(upd["new_lens"].sum()) * w.L * w.Hkv
+        # tokens whose significance the step reads: outside the window (mode
+        # 0), or the one leaving it (mode 1), plus a classified new token
+        nl = ctx["ctx_lens"] + upd["new_lens"]
+        if a.decode_mode == 0:
+            scored += int((nl - a.window).clamp(min=0).sum())
+        else:
+            scored += int(((ctx["ctx_lens"] - a.window >= 0) & (upd["new_lens"] > 0)).sum())
         evs[i][0].record(stream)
         dec.step(d, w.alpha_h, w.alpha_l, profiler=prof)
         evs[i][1].record(stream)
@@ -498,15 +513,17 @@ def run_native_decode(a):
     ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
     kt = prof.read()
     prof.close()
-    names = ("reset", "k_reclass", "k_dscan", "k_apply", "k_demote")
+    names = ("reset", "k_candidate" if a.decode_mode else "k_reclass", "k_dscan", "k_apply", "k_demote")
     kernel_ms = {n: statistics.mean(c[i] for c in kt) for i, n in enumerate(names)}
     ms_max = max_over_ranks(ms, dev, world)
     value = whole_job_rate(live_rows, world, ms_max)
 
     peak, peak_kind = _peaks()
     tok_per_step = live_rows / a.steps / (w.L * w.Hkv)
-    rc_bytes = w.L * tok_per_step * (w.Hq * 4 + w.Hkv) + tok_per_step * 4
-    rc_ms = kernel_ms["k_reclass"]
+    sc_per_step = scored / a.steps
+    rc_bytes = w.L * sc_per_step * (w.Hq * 4 + w.Hkv) + sc_per_step * 4
+    rc_name = names[1]
+    rc_ms = kernel_ms[rc_name]
     rc_gbs = rc_bytes / (rc_ms / 1000.0) / 1e9
     step_gbs = rc_bytes / (ms_max / a.steps / 1000.0) / 1e9
 
@@ -553,7 +570,7 @@ def run_native_decode(a):
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        v, nsteps, rrows, tt = decode_oracle_sample(w, a.cpu_seconds)
+        v, nsteps, rrows, tt = decode_oracle_sample(w, a.cpu_seconds, a.window, a.decode_mode)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"layer 0 of the first 16 requests of {a.workload} ({rrows:.0f} live token-rows per "
                          f"step) x {nsteps} steps, single-threaded, {tt:.1f} s"}
@@ -568,9 +585,9 @@ def run_native_decode(a):
                        "timed": "dkv_decode_step only (significance updates between steps untimed)",
                        "l2": "significance sums (%.1f GB) larger than L2" % (w.L * w.R * cap * w.Hq * 4 / 1e9),
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "k_reclass", "achieved": rc_gbs, "peak": peak, "unit": "GB/s",
+            "roofline": {"bound": "hbm", "kernel": rc_name, "achieved": rc_gbs, "peak": peak, "unit": "GB/s",
                          "frac": rc_gbs / peak, "peak_kind": peak_kind,
-                         "traffic": _reclass_traffic(workload_name(a), rc_bytes),
+                         "traffic": _reclass_traffic(workload_name(a), rc_bytes) if rc_name == "k_reclass" else None,
                          "algorithmic_bytes": rc_bytes, "ms": rc_ms},
             "step_hbm": {"achieved": step_gbs, "frac": step_gbs / peak, "bytes": rc_bytes},
             "kernels_ms": kernel_ms,
@@ -595,7 +612,7 @@ def run_reference_decode(a):
     if int(os.environ.get("RANK", "0")) != 0:
         return
     w = workload(a)
-    smp = DecodeOracleSample(w)
+    smp = DecodeOracleSample(w, window=a.window, mode=a.decode_mode)
     for _ in range(a.warmup):
         smp.step()
     total, rows = 0.0, 0

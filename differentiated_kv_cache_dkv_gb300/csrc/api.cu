@@ -80,6 +80,7 @@ bool valid_decode(const dkv_decode_batch *b) {
       b->Hq > dkv::kMaxHq || b->R > 65535 || b->L > 65535)
     return false;
   if (b->cap < 16 || (b->cap % 16) != 0) return false;
+  if (b->window < 0 || (b->mode != 0 && b->mode != 1)) return false;
   const int64_t U = static_cast<int64_t>(b->L) * b->R * b->Hkv;
   if (U > INT32_MAX || b->unit_base < 0 || b->unit_base + U > INT32_MAX) return false;
   return true;
@@ -96,6 +97,7 @@ dkv::DecodeArgs decode_args(const dkv_decode_batch *b, const dkv_pool *pool, con
   dkv::DecodeArgs a{};
   a.L = b->L; a.R = b->R; a.Hq = b->Hq; a.Hkv = b->Hkv; a.G = b->Hq / b->Hkv;
   a.P = pool->P; a.pmax = t->pmax; a.cap = b->cap;
+  a.window = b->window; a.mode = b->mode;
   a.F = pool->F; a.U = static_cast<int64_t>(b->L) * b->R * b->Hkv; a.unit_base = b->unit_base;
   a.k_new = static_cast<const uint16_t *>(b->k_new); a.v_new = static_cast<const uint16_t *>(b->v_new);
   a.sig_sum = b->sig_sum; a.sig_cnt = b->sig_cnt; a.ctx_lens = b->ctx_lens; a.new_lens = b->new_lens;
@@ -291,7 +293,7 @@ int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dk
   mark(0);
   if (const int32_t rc = cuda_status(cudaMemsetAsync(ws, 0, lay.reset, s))) return rc;
   mark(1);
-  if (const int32_t rc = cuda_status(dkv::launch_reclass(a, s))) return rc;
+  if (const int32_t rc = cuda_status(a.mode == 1 ? dkv::launch_candidate(a, s) : dkv::launch_reclass(a, s))) return rc;
   mark(2);
   if (const int32_t rc = cuda_status(dkv::launch_dscan(a, lay.npart, s))) return rc;
   mark(3);

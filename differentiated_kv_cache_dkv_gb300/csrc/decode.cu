@@ -23,11 +23,18 @@
 //     (a unit's new K8V4 pages first); surplus pages are freed to the tail in
 //     (unit, list, page) order; unused slots are cleared.
 //
+// With a recent window W (the review's Algorithm 1) held tokens at positions
+// >= N - W keep their class and the new token enters as K8V4 (W >= 1); in the
+// single-candidate mode only the token leaving the window, position ctx - W,
+// is classified, instead of every older held token.
+//
 // Kernels, in stream order (after a memset of the call's counters):
 //   k_reclass  streams sig_sum / sig_cnt, reclassifies every live row and
 //              marks each changed class byte in place (0x80 | old << 2 | new;
 //              old = 3 for the new token) -- the step's only full pass over
-//              the significance sums, which dominate its bytes;
+//              the significance sums, which dominate its bytes (in the
+//              single-candidate mode k_candidate does the same for the
+//              candidate and new rows alone);
 //   k_dscan    per-unit plan (survivors, page needs, new and freed pages),
 //              block scan + decoupled look-back over partitions of units,
 //              capacity check;
@@ -49,6 +56,7 @@ namespace {
 
 constexpr int kReclassThreads = 512;
 constexpr int kReclassRows = 2;           // rows in flight per thread (4 blocks of 512 per SM)
+constexpr int kCandThreads = 64;          // candidate kernel: 2 Hkv rows per (layer, request)
 constexpr int kDScanThreads = 256;        // one unit per thread
 constexpr int kMarkCap = 256;             // listed marks per unit in the apply block
 
@@ -92,6 +100,32 @@ __device__ __noinline__ void new_token(const DecodeArgs &a, uint8_t *c, int64_t 
   }
 }
 
+__device__ __forceinline__ bool lens_bad(const DecodeArgs &a, int32_t ctx, int32_t nw) {
+  return ctx < 0 || nw < 0 || nw > 1 || static_cast<int64_t>(ctx) + nw > a.cap ||
+         static_cast<int64_t>(ctx) + nw > static_cast<int64_t>(a.pmax - 1) * a.P;
+}
+
+// With a recent window the new token enters as K8V4 without a score: its
+// class mark, saved prior byte and list entry, and the range check of its K
+// and V words (32 threads per KV head: 16 K words, 16 V words).
+__device__ __noinline__ void window_new_token(const DecodeArgs &a, int32_t r, int32_t l, int32_t ctx) {
+  const int Hkv = a.Hkv;
+  const int64_t lr = static_cast<int64_t>(l) * a.R + r;
+  const int64_t u0 = lr * Hkv;
+  for (int t = threadIdx.x; t < Hkv * 32; t += blockDim.x) {
+    const int h = t >> 5, q = t & 31;
+    const uint4 *src = reinterpret_cast<const uint4 *>((q < 16 ? a.k_new : a.v_new) + (u0 + h) * DKV_HEAD_DIM);
+    if (words_out_of_range(__ldg(src + (q & 15)))) set_error(&a.ws->err, DKV_E_RANGE);
+    if (q != 0) continue;
+    uint8_t *c = a.classes + (lr * a.cap + ctx) * Hkv + h;
+    a.ucnt[u0 + h].w = static_cast<int32_t>(*c | (DKV_CLASS_K8V4 << 8) | (1u << 16));
+    *c = static_cast<uint8_t>(0x80u | (3u << 2) | DKV_CLASS_K8V4);
+    const int32_t m = atomicAdd(a.lcnt + lr, 1);
+    if (m < kMarkList)
+      a.list[lr * kMarkList + m] = (static_cast<uint32_t>(ctx) << 11) | (h << 4) | (3u << 2) | DKV_CLASS_K8V4;
+  }
+}
+
 template <int kV4>  // float4 loads per row (G / 4); 0 = scalar loads
 __global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
   __shared__ int32_t ev_s[kMaxHq * 3];  // per head: demoted, K8V4 pruned, K4V2 pruned
@@ -100,15 +134,20 @@ __global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
   const int32_t r = blockIdx.y, l = blockIdx.z;
   const int32_t i0 = blockIdx.x * kReclassChunk;
   const int32_t ctx = __ldg(a.ctx_lens + r), nw = __ldg(a.new_lens + r);
-  const bool bad = ctx < 0 || nw < 0 || nw > 1 || static_cast<int64_t>(ctx) + nw > a.cap ||
-                   static_cast<int64_t>(ctx) + nw > static_cast<int64_t>(a.pmax - 1) * a.P;
-  if (bad) {
+  if (lens_bad(a, ctx, nw)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) set_error(&a.ws->err, DKV_E_LENS);
+    return;
+  }
+  if (a.window >= 1 && blockIdx.x == gridDim.x - 1) {  // a block of its own (code here makes the loop spill)
+    if (nw == 1) window_new_token(a, r, l, ctx);
     return;
   }
   const int32_t N = ctx + nw;
   if (i0 >= N) return;
   const int32_t i1 = min(N, i0 + kReclassChunk);
+  // With a recent window the scored rows end where it starts (N - W; the
+  // held rows in it keep their class, the new token enters as K8V4 below)
+  const int32_t is = a.window >= 1 ? max(i0, min(i1, N - a.window)) : i1;
   const int Hkv = a.Hkv, G = a.G;
   for (int t = threadIdx.x; t < Hkv * 3; t += blockDim.x) ev_s[t] = 0;
   if (threadIdx.x == 0) mk_n = 0;
@@ -131,9 +170,8 @@ __global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
   uint8_t *cls = a.classes + (lrow + tok0) * Hkv;
   const float *sig = a.sig_sum + (lrow + tok0) * a.Hq;
   const int32_t *cnt = a.sig_cnt + tok0;
-  const int nrows = (i1 - i0) * Hkv;
+  const int nrows = (is - i0) * Hkv;
   const int64_t u0 = (static_cast<int64_t>(l) * a.R + r) * Hkv;
-
   for (int jb = 0; jb < nrows; jb += kReclassRows * kReclassThreads) {
     float m[kReclassRows];
     int32_t c[kReclassRows];
@@ -237,6 +275,72 @@ __global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
     int4 *uc = a.ucnt + u0 + t / 3;
     int *dst = (t % 3 == 0) ? &uc->x : (t % 3 == 1 ? &uc->y : &uc->z);
     atomicAdd(dst, n);
+  }
+}
+
+// -------------------------------------------------------------- k_candidate --
+
+// The single-candidate policy of the review's Algorithm 1 (Referee Report,
+// major comment 2): per (layer, request) only the token that the new one
+// pushes out of the recent window, position ctx - W, is classified (its class
+// becomes min(old, classify)), and the new token enters as K8V4 (W >= 1) or
+// is classified (W = 0).  Every other class byte stays as it is, so this
+// replaces k_reclass's pass over the significance sums with 2 Hkv rows per
+// (layer, request); it leaves the same marks, counters and change lists.
+__global__ void __launch_bounds__(kCandThreads) k_candidate(DecodeArgs a) {
+  const int32_t r = blockIdx.x, l = blockIdx.y;
+  const int32_t ctx = __ldg(a.ctx_lens + r), nw = __ldg(a.new_lens + r);
+  if (lens_bad(a, ctx, nw)) {
+    if (threadIdx.x == 0) set_error(&a.ws->err, DKV_E_LENS);
+    return;
+  }
+  if (nw == 0) return;  // no new token: nothing leaves the window
+  const int32_t N = ctx + 1, W = a.window, pc = ctx - W;
+  const int Hkv = a.Hkv, G = a.G;
+  const float thr_h = __fdiv_rn(a.alpha_h, static_cast<float>(N));
+  const float thr_l = __fdiv_rn(a.alpha_l, static_cast<float>(N));
+  const int64_t lr = static_cast<int64_t>(l) * a.R + r;
+  const int64_t u0 = lr * Hkv;
+  for (int j = threadIdx.x; j < 2 * Hkv; j += blockDim.x) {
+    const bool is_new = j >= Hkv;
+    const int h = is_new ? j - Hkv : j;
+    if (!is_new && (W < 1 || pc < 0)) continue;  // no held token leaves the window
+    const int32_t i = is_new ? ctx : pc;
+    const int64_t row = lr * a.cap + i;
+    uint8_t *c = a.classes + row * Hkv + h;
+    const uint32_t o = *c;
+    if (!is_new && o == DKV_CLASS_PRUNE) continue;
+    uint32_t cn = DKV_CLASS_K8V4;
+    const int32_t cnt = __ldg(a.sig_cnt + static_cast<int64_t>(r) * a.cap + i);
+    if (cnt != 0 && !(is_new && W >= 1)) {
+      const float *p = a.sig_sum + row * a.Hq + h * G;
+      float mx = __ldg(p), mn = mx;
+      for (int q = 1; q < G; ++q) {
+        const float y = __ldg(p + q);
+        mx = fmaxf(mx, y);
+        mn = fminf(mn, y);
+      }
+      const float sc = __fdiv_rn(cnt > 0 ? mx : mn, static_cast<float>(cnt));
+      cn = sc >= thr_h ? DKV_CLASS_K8V4 : (sc >= thr_l ? DKV_CLASS_K4V2 : DKV_CLASS_PRUNE);
+    }
+    uint32_t e;
+    if (!is_new) {
+      if (o > DKV_CLASS_K8V4) {
+        set_error(&a.ws->err, DKV_E_INTERNAL);
+        continue;
+      }
+      if (cn >= o) continue;
+      *c = static_cast<uint8_t>(0x80u | (o << 2) | cn);
+      int4 *uc = a.ucnt + u0 + h;
+      atomicAdd(o == DKV_CLASS_K4V2 ? &uc->z : (cn == DKV_CLASS_K4V2 ? &uc->x : &uc->y), 1);
+      e = (static_cast<uint32_t>(i) << 11) | (h << 4) | (o << 2) | cn;
+    } else {
+      new_token(a, c, u0 + h, o, cn);
+      e = (static_cast<uint32_t>(i) << 11) | (h << 4) | (3u << 2) | cn;
+    }
+    // at most 2 Hkv <= 256 entries: the list never overflows
+    const int32_t q = atomicAdd(a.lcnt + lr, 1);
+    if (q < kMarkList) a.list[lr * kMarkList + q] = e;
   }
 }
 
@@ -1086,10 +1190,16 @@ size_t apply_smem(int32_t hpc, int32_t words, int32_t pmax) {
 }
 
 cudaError_t launch_reclass(const DecodeArgs &a, cudaStream_t s) {
-  const dim3 grid((a.cap + kReclassChunk - 1) / kReclassChunk, a.R, a.L);
+  // with a recent window one more block per (layer, request) takes the new token
+  const dim3 grid((a.cap + kReclassChunk - 1) / kReclassChunk + (a.window >= 1 ? 1 : 0), a.R, a.L);
   if (a.G == 4) k_reclass<1><<<grid, kReclassThreads, 0, s>>>(a);
   else if (a.G == 8) k_reclass<2><<<grid, kReclassThreads, 0, s>>>(a);
   else k_reclass<0><<<grid, kReclassThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_candidate(const DecodeArgs &a, cudaStream_t s) {
+  k_candidate<<<dim3(a.R, a.L), kCandThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

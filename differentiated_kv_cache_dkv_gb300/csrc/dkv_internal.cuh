@@ -211,6 +211,7 @@ inline DecWsLayout dec_ws_layout(int64_t U, int64_t LR, int64_t rows) {
 
 struct DecodeArgs {
   int32_t L, R, Hq, Hkv, G, P, pmax, cap, spin_limit;
+  int32_t window, mode;
   int64_t F, U, unit_base;
   float alpha_h, alpha_l;
   const uint16_t *k_new, *v_new;
@@ -248,6 +249,7 @@ cudaError_t launch_dequant(const dkv_pool &p, const int32_t *ids, int32_t one_id
                            float *k_out, float *v_out, int32_t *pos_out, cudaStream_t s);
 int pack_blocks_per_sm();
 cudaError_t launch_reclass(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_candidate(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_dscan(const DecodeArgs &a, int32_t npart, cudaStream_t s);
 cudaError_t launch_apply(const DecodeArgs &a, int32_t hpc, int32_t words, cudaStream_t s);
 cudaError_t launch_demote(const DecodeArgs &a, int grid, cudaStream_t s);

@@ -50,13 +50,13 @@ def decode_prefill(w, dec, dev, seed: int, cap: int, head_offset: int = 0):
     return ctx
 
 
-def decode_setup(w, dev, seed: int, total_steps: int):
+def decode_setup(w, dev, seed: int, total_steps: int, window: int = 0, mode: int = 0):
     """Decoder state after the prefill, with the pool sized so that the ring's
     head wraps within the run: a first prefill in a worst-case pool measures
     the pages it takes, the second starts the ring DECODE_SLACK pages before
     its end."""
     cap = decode_cap(w, total_steps)
-    dec = libdkv.Decoder(w.L, w.R, w.Hq, w.Hkv, cap, w.P, w.pool_pages, device=dev)
+    dec = libdkv.Decoder(w.L, w.R, w.Hq, w.Hkv, cap, w.P, w.pool_pages, device=dev, window=window, mode=mode)
     decode_prefill(w, dec, dev, seed, cap)
     used = int(dec.pool.cursors[0])
     F = dec.pool.F

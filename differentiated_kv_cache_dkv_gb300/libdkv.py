@@ -71,7 +71,8 @@ class dkv_decode_batch(ctypes.Structure):
         ("D", ctypes.c_int32), ("cap", ctypes.c_int32), ("unit_base", ctypes.c_int64),
         ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("sig_sum", ctypes.c_void_p),
         ("sig_cnt", ctypes.c_void_p), ("ctx_lens", ctypes.c_void_p), ("new_lens", ctypes.c_void_p),
-        ("classes", ctypes.c_void_p), ("slot_of", ctypes.c_void_p),
+        ("classes", ctypes.c_void_p), ("slot_of", ctypes.c_void_p), ("window", ctypes.c_int32),
+        ("mode", ctypes.c_int32),
     ]
 
 
@@ -325,8 +326,10 @@ class Decoder:
     prefill_layer() fills one layer's units with dkv_compact; index() derives
     classes and slot_of from the pages; step() runs dkv_decode_step."""
 
-    def __init__(self, L: int, R: int, Hq: int, Hkv: int, cap: int, P: int, F: int, device="cuda"):
+    def __init__(self, L: int, R: int, Hq: int, Hkv: int, cap: int, P: int, F: int, device="cuda",
+                 window: int = 0, mode: int = 0):
         self.L, self.R, self.Hq, self.Hkv, self.cap, self.P = L, R, Hq, Hkv, cap, P
+        self.window, self.mode = int(window), int(mode)
         self.U = L * R * Hkv
         self.pmax = -(-cap // P) + 1
         self.device = torch.device(device)
@@ -343,7 +346,7 @@ class Decoder:
         g = d.get
         return dkv_decode_batch(self.L, self.R, self.Hq, self.Hkv, 128, self.cap, 0, _p(g("k_new")), _p(g("v_new")),
                                 _p(g("sig_sum")), _p(g("sig_cnt")), _p(g("ctx_lens")), _p(g("new_lens")),
-                                _p(self.classes), _p(self.slot_of))
+                                _p(self.classes), _p(self.slot_of), self.window, self.mode)
 
     def prefill_layer(self, inp: dict, layer: int, max_len: int, alpha_h: float, alpha_l: float,
                       stream=None) -> None:

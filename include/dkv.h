@@ -227,6 +227,13 @@ typedef struct dkv_decode_batch {
   int32_t *slot_of;          /* in/out int32 [L][R * cap][Hkv]: slot of each held token in its
                                 class list, -1 when pruned; built by dkv_decode_index and
                                 maintained by dkv_decode_step */
+  int32_t window;            /* W >= 0: the recent window, positions [N - W, N) after the step
+                                (the review's Algorithm 1 keeps the W most recent tokens at high
+                                precision).  The new token enters as K8V4 when W >= 1 (and is
+                                classified when W = 0); held tokens in the window keep their class */
+  int32_t mode;              /* 0: every older held token is re-scored (the semantics above);
+                                1: only the token the new one pushes out of the window, position
+                                ctx - W, is classified, once (Algorithm 1's candidate) */
 } dkv_decode_batch;
 
 /* Workspace bytes of dkv_decode_step for this shape (host only). */
@@ -245,7 +252,9 @@ int32_t dkv_decode_index(const dkv_decode_batch *b, const dkv_pool *pool, const 
 
 /* One generation step (semantics above), asynchronous.  workspace: device,
  * 256-byte aligned, >= dkv_decode_workspace_size bytes, scratch.  The caller
- * advances ctx_lens by new_lens after a successful step.  Device-side errors
+ * advances ctx_lens by new_lens after a successful step.  A bad shape, cap
+ * not a multiple of 16, window < 0 or mode not 0 or 1 is DKV_E_INVAL before
+ * anything is enqueued.  Device-side errors
  * (read with dkv_get_status): DKV_E_LENS (ctx + new > cap, new not 0 or 1, a
  * list needing more than pmax pages), DKV_E_RANGE (a kept new token with a
  * non-finite value or one above 65504), DKV_E_NOMEM (new pages > free
@@ -254,8 +263,8 @@ int32_t dkv_decode_index(const dkv_decode_batch *b, const dkv_pool *pool, const 
  * TIMEOUT, and on INTERNAL found before any page is touched, the step
  * changes nothing (classes restored); INTERNAL found while moving slots
  * leaves the state undefined.  With dkv_params.profiler the five intervals
- * are: counter reset, reclassification, page scan, apply, requantisation of
- * the demoted tokens. */
+ * are: counter reset, reclassification (or the candidate kernel in mode 1),
+ * page scan, apply, requantisation of the demoted tokens. */
 int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dkv_pool *pool,
                         const dkv_tables *t, void *workspace, size_t workspace_bytes, void *stream);
 

@@ -28,7 +28,7 @@ def gpu_decoder(hd: HostDecode, inp_cpu: dict) -> libdkv.Decoder:
     """Device copy of the oracle's prefill: per-layer dkv_compact on the same
     inputs, then dkv_decode_index."""
     w = hd.w
-    dec = libdkv.Decoder(w.L, w.R, w.Hq, w.Hkv, hd.cap, w.P, hd.pool.F)
+    dec = libdkv.Decoder(w.L, w.R, w.Hq, w.Hkv, hd.cap, w.P, hd.pool.F, window=hd.window, mode=hd.mode)
     for l in range(w.L):
         layer = {"L": 1, "R": w.R, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T,
                  "k": _dev(inp_cpu["k"][l:l + 1]), "v": _dev(inp_cpu["v"][l:l + 1]),
@@ -97,15 +97,18 @@ def check_slot_index(g: dict, hd: HostDecode):
 
 
 def _run(w: W.Workload, cap: int, steps: int, p_prune: float, p_demote: float, F: int | None = None,
-         slot_check_every: int = 5):
+         slot_check_every: int = 5, window: int = 0, mode: int = 0):
     inp = W.make_inputs(w, 77)
-    hd = HostDecode(w, cap, F=F, inp=inp)
+    hd = HostDecode(w, cap, F=F, inp=inp, window=window, mode=mode)
     dec = gpu_decoder(hd, inp)
     g = gpu_state(dec)
     compare(g, hd, "after prefill + index:")
     check_slot_index(g, hd)
     heads = [int(hd.pool.cursors[0])]
+    hd.held_changes = 0  # class changes of tokens held before their step
     for s in range(steps):
+        held = (np.arange(cap)[None, :] < hd.ctx_lens[:, None]).reshape(-1)
+        before = hd.classes.copy()
         upd = W.decode_update_inputs(w, hd.ctx, s, p_prune=p_prune, p_demote=p_demote)
         d = {"k_new": _dev(upd["k_new"]), "v_new": _dev(upd["v_new"]), "sig_sum": _dev(hd.ctx["sig_sum"]),
              "sig_cnt": _dev(hd.ctx["sig_cnt"]), "ctx_lens": _dev(hd.ctx["ctx_lens"]),
@@ -114,6 +117,7 @@ def _run(w: W.Workload, cap: int, steps: int, p_prune: float, p_demote: float, F
         st = libdkv.dkv_get_status(dec.pool)
         assert hd.step(upd) == oracle.OK
         assert st == libdkv.DKV_OK, libdkv.status_string(st)
+        hd.held_changes += int(((before != hd.classes) & held[None, :, None]).sum())
         g = gpu_state(dec)
         compare(g, hd, f"step {s}:")
         if s % slot_check_every == slot_check_every - 1 or s == steps - 1:
@@ -252,3 +256,16 @@ def test_decode_zero_low_threshold():
     IEEE division for every row."""
     w = W.small("dec_a0", lens=[300, 77, 5], L=1, Hq=8, Hkv=2, alpha_h=0.7, alpha_l=0.0)
     _run(w, cap=320, steps=5, p_prune=0.05, p_demote=0.1, slot_check_every=5)
+
+
+@pytest.mark.parametrize("window,mode", [(0, 1), (3, 0), (3, 1), (64, 0), (64, 1), (600, 0)])
+def test_decode_recent_window_and_candidate(window, mode):
+    """Recent window W and the single-candidate policy (mode 1): same bytes as
+    the oracle after every step.  Heavy churn so that candidates do change;
+    request lengths below, at and above W; W = 600 covers every request."""
+    w = W.small("decw", lens=[300, 7, 517, 0, 129, 64, 3])
+    hd, dec, _ = _run(w, cap=560, steps=10, p_prune=0.3, p_demote=0.3, window=window, mode=mode)
+    if window == 600 or (window == 0 and mode == 1):
+        assert hd.held_changes == 0  # every token in the window; or only new tokens classified
+    else:
+        assert hd.held_changes > 0, "no held token changed class: the case tests nothing"
