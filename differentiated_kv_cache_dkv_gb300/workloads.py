@@ -340,3 +340,9 @@ def decode_update_inputs(w: Workload, ctx: dict, step: int, seed: int | None = N
     k_new = torch.stack([make_kv_layer(kv, seed + 77 * step + 1, l, 0, device) for l in range(L)])
     v_new = torch.stack([make_kv_layer(kv, seed + 77 * step + 1, l, 1, device) for l in range(L)])
     return {"k_new": k_new, "v_new": v_new, "new_lens": room.to(torch.int32)}
+
+
+def decode_queries(w: Workload, n_layers: int, seed: int, step: int = 0, device="cpu") -> torch.Tensor:
+    """bf16 [n_layers][R][Hq][D] queries of one generation step, N(0,1)."""
+    g = _gen(seed * 1000003 + 700000 + step, device)
+    return torch.randn((n_layers, w.R, w.Hq, D), generator=g, device=device).to(torch.bfloat16)

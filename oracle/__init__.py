@@ -62,6 +62,16 @@ class _DecodeBatch(ctypes.Structure):
     ]
 
 
+class _AttnBatch(ctypes.Structure):
+    _fields_ = [
+        ("L", ctypes.c_int32), ("R", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+        ("cap", ctypes.c_int32), ("layer0", ctypes.c_int32), ("n_layers", ctypes.c_int32),
+        ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+        ("new_lens", ctypes.c_void_p), ("ctx_lens", ctypes.c_void_p), ("scale", ctypes.c_double),
+        ("out", ctypes.c_void_p), ("p_out", ctypes.c_void_p),
+    ]
+
+
 def lib():
     """Load (building first if needed) the oracle shared library."""
     global _lib
@@ -87,6 +97,9 @@ def lib():
         L.oracle_decode_step.argtypes = [ctypes.POINTER(_DecodeBatch), ctypes.c_float, ctypes.c_float,
                                          ctypes.POINTER(_Pool), ctypes.POINTER(_Tables)]
         L.oracle_decode_step.restype = ctypes.c_int32
+        L.oracle_decode_attention.argtypes = [ctypes.POINTER(_AttnBatch), ctypes.POINTER(_Pool),
+                                              ctypes.POINTER(_Tables)]
+        L.oracle_decode_attention.restype = ctypes.c_int32
         L.oracle_dequant_page.argtypes = [ctypes.POINTER(_Pool), ctypes.c_int32, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_void_p]
         L.oracle_dequant_page.restype = None
@@ -213,3 +226,28 @@ def dequant_page(pool: Pool, page_id: int):
     p = pool._c()
     lib().oracle_dequant_page(ctypes.byref(p), int(page_id), _ptr(k), _ptr(v), _ptr(pos))
     return k, v, pos
+
+
+def decode_attention(a: dict, pool: Pool, tables: Tables, p_out: bool = True):
+    """Decode attention (reading M).  a: L, R, Hq, Hkv, cap, layer0, n_layers,
+    q (uint16 bf16 bits [n_layers, R, Hq, 128]), optional k_new / v_new
+    (uint16 [n_layers, R, Hkv, 128]) with new_lens, ctx_lens, scale.
+    Returns (status, out [n_layers, R, Hq, 128] float64, p [n_layers, R*cap, Hq]
+    float64 or None)."""
+    nl, R, Hq = int(a["n_layers"]), int(a["R"]), int(a["Hq"])
+    q = np.ascontiguousarray(a["q"], dtype=np.uint16)
+    kn = a.get("k_new")
+    kn = None if kn is None else np.ascontiguousarray(kn, dtype=np.uint16)
+    vn = a.get("v_new")
+    vn = None if vn is None else np.ascontiguousarray(vn, dtype=np.uint16)
+    nlens = a.get("new_lens")
+    nlens = None if nlens is None else np.ascontiguousarray(nlens, dtype=np.int32)
+    ctx = np.ascontiguousarray(a["ctx_lens"], dtype=np.int32)
+    out = np.zeros((nl, R, Hq, 128), dtype=np.float64)
+    p = np.zeros((nl, R * int(a["cap"]), Hq), dtype=np.float64) if p_out else None
+    b = _AttnBatch(int(a["L"]), R, Hq, int(a["Hkv"]), int(a["cap"]), int(a["layer0"]), nl, _ptr(q), _ptr(kn),
+                   _ptr(vn), _ptr(nlens), _ptr(ctx), float(a["scale"]), _ptr(out), _ptr(p))
+    pp = pool._c()
+    tt = tables._c()
+    st = int(lib().oracle_decode_attention(ctypes.byref(b), ctypes.byref(pp), ctypes.byref(tt)))
+    return st, out, p

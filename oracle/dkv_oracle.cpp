@@ -71,6 +71,19 @@
  *      re-scores only the token the new one pushes out of the window,
  *      position ctx - W (when there is a new token and W >= 1).  W = 0 with
  *      mode 0 is D itself.
+ *  M   Decode attention over the unified pages (DiffKV, Figure 7 and section
+ *      6.1: attention runs over the mixed-precision pages; the page never
+ *      prints the kernel, so this is plain scaled dot-product attention).
+ *      For query head q of request r in layer l, the attended set is every
+ *      used slot of the K8V4 and K4V2 lists of unit (l, r, q / G), plus the
+ *      step's new token (bf16 K and V, position ctx) when there is one.
+ *      k and v of a held token are its dequantised fp32 values fma(c, s, z)
+ *      (what oracle_dequant_page returns).  Logits scale * (q . k) with the
+ *      bf16 query, softmax and the weighted sum of v are taken in double.
+ *      An empty attended set gives a zero output.  The probability given to
+ *      each attended position is reported; it is the score that the
+ *      significance sum of that position accumulates (the average attention
+ *      a token receives, "What carries the argument").
  */
 #include "dkv_oracle.h"
 
@@ -737,6 +750,84 @@ extern "C" int32_t oracle_decode_step(const oracle_decode_batch *b, float alpha_
 
 /* Reading Q2: x' = fma(q, s, z) per element; slots a page does not have (the
  * upper half of a K8V4 page) and free pages decode to 0 with position -1. */
+int32_t oracle_decode_attention(const oracle_attn_batch *b, const oracle_pool *pool,
+                                const oracle_tables *t) {
+  if (!b || !pool || !t || b->R < 0 || b->Hkv <= 0 || b->Hq <= 0 || b->Hq % b->Hkv != 0 ||
+      b->layer0 < 0 || b->n_layers < 0 || b->layer0 + b->n_layers > b->L || !b->q || !b->out ||
+      !b->ctx_lens || (b->k_new && (!b->v_new || !b->new_lens)))
+    return ORACLE_E_INVAL;
+  const PageLayout lay{pool->P};
+  const int64_t P = pool->P, R = b->R, Hq = b->Hq, Hkv = b->Hkv, G = Hq / Hkv, cap = b->cap;
+  if (b->p_out)
+    std::fill(b->p_out, b->p_out + static_cast<int64_t>(b->n_layers) * R * cap * Hq, 0.0);
+  for (int64_t li = 0; li < b->n_layers; ++li) {
+    for (int64_t r = 0; r < R; ++r) {
+      for (int64_t h = 0; h < Hkv; ++h) {
+        const int64_t u = ((b->layer0 + li) * R + r) * Hkv + h;
+        const int32_t *hdr = t->unit_hdr + 4 * u;
+        const int32_t *fwd = t->fwd + u * t->pmax;
+        /* the attended tokens: dequantised K, V and positions */
+        std::vector<float> ks, vs;
+        std::vector<int64_t> pos;
+        for (int list = 0; list < 2; ++list) {
+          const bool high = (list == 0);
+          const int64_t n = hdr[list], per = high ? P : 2 * P, first = high ? 0 : hdr[2];
+          for (int64_t i = 0; i < n; ++i) {
+            const uint8_t *pg = pool->pages + static_cast<int64_t>(fwd[first + i / per]) * lay.bytes();
+            const int64_t sl = i % per;
+            uint8_t qk[128], qv[128];
+            unpack_codes(pg + lay.k_off(high, sl), high ? 8 : 4, qk);
+            unpack_codes(pg + lay.v_off(high, sl), high ? 4 : 2, qv);
+            const uint8_t *meta = pg + lay.meta_off(sl);
+            const float k_s = oracle_fp16_to_f32(get_u16(meta + 0)), k_z = oracle_fp16_to_f32(get_u16(meta + 2));
+            const float v_s = oracle_fp16_to_f32(get_u16(meta + 4)), v_z = oracle_fp16_to_f32(get_u16(meta + 6));
+            for (int d = 0; d < 128; ++d) {
+              ks.push_back(std::fma(static_cast<float>(qk[d]), k_s, k_z));
+              vs.push_back(std::fma(static_cast<float>(qv[d]), v_s, v_z));
+            }
+            pos.push_back(get_i32(pg + lay.pos_off(sl)));
+          }
+        }
+        if (b->k_new && b->new_lens[r] == 1) {
+          const int64_t row = ((li * R + r) * Hkv + h) * 128;
+          for (int d = 0; d < 128; ++d) {
+            ks.push_back(bf16_value(b->k_new[row + d]));
+            vs.push_back(bf16_value(b->v_new[row + d]));
+          }
+          pos.push_back(b->ctx_lens[r]);
+        }
+        const int64_t n = static_cast<int64_t>(pos.size());
+        for (int64_t g = 0; g < G; ++g) {
+          const int64_t qh = h * G + g;
+          const uint16_t *qrow = b->q + ((li * R + r) * Hq + qh) * 128;
+          double *o = b->out + ((li * R + r) * Hq + qh) * 128;
+          for (int d = 0; d < 128; ++d) o[d] = 0.0;
+          if (n == 0) continue;
+          std::vector<double> lg(n);
+          double mx = -INFINITY;
+          for (int64_t i = 0; i < n; ++i) {
+            double dot = 0.0;
+            for (int d = 0; d < 128; ++d) dot += static_cast<double>(bf16_value(qrow[d])) * ks[i * 128 + d];
+            lg[i] = b->scale * dot;
+            mx = std::max(mx, lg[i]);
+          }
+          double den = 0.0;
+          for (int64_t i = 0; i < n; ++i) {
+            lg[i] = std::exp(lg[i] - mx);
+            den += lg[i];
+          }
+          for (int64_t i = 0; i < n; ++i) {
+            const double p = lg[i] / den;
+            for (int d = 0; d < 128; ++d) o[d] += p * vs[i * 128 + d];
+            if (b->p_out) b->p_out[(li * R * cap + r * cap + pos[i]) * Hq + qh] = p;
+          }
+        }
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
 void oracle_dequant_page(const oracle_pool *pool, int32_t page_id, float *k_out, float *v_out,
                          int32_t *pos_out) {
   const PageLayout lay{pool->P};

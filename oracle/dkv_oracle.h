@@ -118,6 +118,26 @@ typedef struct oracle_decode_batch {
 int32_t oracle_decode_step(const oracle_decode_batch *b, float alpha_h, float alpha_l,
                            oracle_pool *pool, oracle_tables *t);
 
+/* Decode attention over the unified pages (reading M in dkv_oracle.cpp).
+ * Layers [layer0, layer0 + n_layers) of the unit tables; unit of (layer l,
+ * request r, KV head h) is (l * R + r) * Hkv + h. */
+typedef struct oracle_attn_batch {
+  int32_t L, R, Hq, Hkv, cap;
+  int32_t layer0, n_layers;
+  const uint16_t *q;       /* bf16 [n_layers][R][Hq][128] */
+  const uint16_t *k_new;   /* bf16 [n_layers][R][Hkv][128], or NULL: no new token */
+  const uint16_t *v_new;
+  const int32_t *new_lens; /* [R] 0 or 1 (ignored when k_new is NULL) */
+  const int32_t *ctx_lens; /* [R]: the new token's position */
+  double scale;            /* softmax scale */
+  double *out;             /* [n_layers][R][Hq][128] */
+  double *p_out;           /* NULL or [n_layers][R * cap][Hq]: each attended position's
+                              probability (0 elsewhere) */
+} oracle_attn_batch;
+
+int32_t oracle_decode_attention(const oracle_attn_batch *b, const oracle_pool *pool,
+                                const oracle_tables *t);
+
 /* Decode a page into fp32 K, V ([2P][128] each) and positions ([2P]). */
 void oracle_dequant_page(const oracle_pool *pool, int32_t page_id,
                          float *k_out, float *v_out, int32_t *pos_out);
