@@ -47,6 +47,8 @@ def _args():
                     help="decode: recent window W (tokens kept at K8V4; 0 = none)")
     ap.add_argument("--decode-mode", type=int, default=0, choices=[0, 1],
                     help="decode: 0 re-scores every older token, 1 only the one leaving the window")
+    ap.add_argument("--op", default="step", choices=["step", "attention"],
+                    help="decode: time the generation step, or the attention over the pages")
     return ap.parse_args()
 
 
@@ -66,6 +68,8 @@ def workload(a):
 
 def workload_name(a) -> str:
     name = a.workload
+    if getattr(a, "op", "step") == "attention":
+        name += " attention"
     if getattr(a, "window", 0) or getattr(a, "decode_mode", 0):
         name += f" (window {a.window}, {'single candidate' if a.decode_mode else 'every token re-scored'})"
     if a.layers or a.requests:
@@ -632,10 +636,210 @@ def run_reference_decode(a):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
 
 
+# ------------------------------------------------------------- attention ---
+
+ATTN_METRIC = "KV tokens attended/sec (token-rows: one held token x one (layer, KV head), its G query heads)"
+ATTN_SCALE = 0.08838834764831845  # 1 / sqrt(128)
+
+
+class AttentionOracleSample:
+    """The oracle's decode attention on a bounded sample of the decode
+    workload: layer 0 of its first n_req requests, prefilled by the oracle
+    (untimed)."""
+
+    def __init__(self, w, n_req: int = 4):
+        import dataclasses
+
+        import torch
+
+        from differentiated_kv_cache_dkv_gb300 import workloads as W
+        from tests.decode_helpers import HostDecode
+
+        self.w = dataclasses.replace(w, L=1, lens=list(w.lens[:n_req]))
+        self.cap = decode_cap(self.w, 1)
+        self.hd = HostDecode(self.w, self.cap)
+        q = W.decode_queries(self.w, 1, W.SEED_BASE)
+        upd = W.decode_update_inputs(self.w, {k: (v.clone() if torch.is_tensor(v) else v)
+                                              for k, v in self.hd.ctx.items()}, 0)
+        b16 = lambda t: t.contiguous().view(torch.int16).numpy().view("uint16")  # noqa: E731
+        self.a = {"L": 1, "R": self.w.R, "Hq": self.w.Hq, "Hkv": self.w.Hkv, "cap": self.cap, "layer0": 0,
+                  "n_layers": 1, "q": b16(q), "k_new": b16(upd["k_new"]), "v_new": b16(upd["v_new"]),
+                  "new_lens": upd["new_lens"].numpy().astype("int32"),
+                  "ctx_lens": self.hd.ctx["ctx_lens"].numpy(), "scale": ATTN_SCALE}
+        self.rows = (int(self.hd.tab.unit_hdr[:, :2].sum()) + int(upd["new_lens"].sum()) * self.w.Hkv)
+
+    def step(self):
+        import oracle
+
+        t = time.perf_counter()
+        st, _, _ = oracle.decode_attention(self.a, self.hd.pool, self.hd.tab)
+        dt = time.perf_counter() - t
+        assert st == 0, st
+        return dt, self.rows
+
+
+def run_native_attention(a):
+    import torch
+
+    from differentiated_kv_cache_dkv_gb300 import libdkv
+    from differentiated_kv_cache_dkv_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    libdkv.load()
+    w = workload(a)
+    dev = torch.device("cuda", local)
+    dec, ctx, cap, used = decode_setup(w, dev, W.SEED_BASE + 1000 * rank, 2)
+    stream = torch.cuda.current_stream()
+    q = W.decode_queries(w, w.L, W.SEED_BASE + rank, device=dev)
+    upd = W.decode_update_inputs(w, {k: (v.clone() if torch.is_tensor(v) else v) for k, v in ctx.items()}, 0,
+                                 device=dev)
+    k_new, v_new, new_lens = upd["k_new"], upd["v_new"], upd["new_lens"]
+    out = torch.empty((w.L, w.R, w.Hq, 128), dtype=torch.float32, device=dev)
+    sig = ctx["sig_sum"]
+    hdr = dec.tables.unit_hdr.long()
+    n_hi, n_lo = int(hdr[:, 0].sum()), int(hdr[:, 1].sum())
+    n_new = int(new_lens.sum()) * w.L * w.Hkv
+    rows = n_hi + n_lo + n_new
+    G = w.Hq // w.Hkv
+    # algorithmic bytes: every held slot's codes, metadata and position; the
+    # new tokens' K and V; queries and outputs; the forward rows and headers
+    # read; each attended position's G significance sums read and written
+    pages_used = int(hdr[:, 2].sum() + hdr[:, 3].sum())
+    alg = (n_hi * (128 + 64 + 8 + 4) + n_lo * (64 + 32 + 8 + 4) + n_new * 512 + w.L * w.R * w.Hq * (256 + 512)
+           + pages_used * 4 + w.U * 16 + rows * G * 8)
+
+    def call():
+        dec.attend(q, ctx["ctx_lens"], out, ATTN_SCALE, k_new=k_new, v_new=v_new, new_lens=new_lens, sig_sum=sig)
+
+    for _ in range(a.warmup):
+        call()
+    torch.cuda.synchronize()
+    assert libdkv.dkv_get_status(dec.pool) == libdkv.DKV_OK
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(a.steps):
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    st = libdkv.dkv_get_status(dec.pool)
+    assert st == libdkv.DKV_OK, libdkv.status_string(st)
+    per = [e0.elapsed_time(e1) for e0, e1 in evs]
+    ms = sum(per)
+    ms_max = max_over_ranks(ms, dev, world)
+    value = whole_job_rate(rows * a.steps, world, ms_max)
+    peak, peak_kind = _peaks()
+    att_ms = statistics.mean(per)
+    gbs = alg / (att_ms / 1000.0) / 1e9
+
+    e2e = None
+    if a.e2e_steps > 0:
+        # end to end: queries, new K / V and lengths from pinned host memory,
+        # the call, the outputs read back (significance stays on the device)
+        host = {"q": q.cpu().pin_memory(), "k_new": k_new.cpu().pin_memory(), "v_new": v_new.cpu().pin_memory(),
+                "ctx": ctx["ctx_lens"].cpu().pin_memory(), "new": new_lens.cpu().pin_memory()}
+        dst = {"q": q, "k_new": k_new, "v_new": v_new, "ctx": ctx["ctx_lens"], "new": new_lens}
+        out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in host.values())
+        d2h = out_h.numel() * 4
+        te = 0.0
+        for _ in range(a.e2e_steps):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            s0.record(stream)
+            for k_, x in host.items():
+                dst[k_].copy_(x, non_blocking=True)
+            call()
+            out_h.copy_(out, non_blocking=True)
+            s1.record(stream)
+            torch.cuda.synchronize()
+            te += s0.elapsed_time(s1)
+        te = max_over_ranks(te, dev, world)
+        e2e = {"value": whole_job_rate(rows * a.e2e_steps, world, te), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": a.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        smp = AttentionOracleSample(w)
+        tt, rr, n = 0.0, 0, 0
+        while tt < a.cpu_seconds or n == 0:
+            dt, r_ = smp.step()
+            tt += dt
+            rr += r_
+            n += 1
+        cpu = {"value": rr / tt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"layer 0 of the first 4 requests of {a.workload} ({smp.rows} token-rows per call) x {n} "
+                         f"calls, single-threaded, {tt:.1f} s"}
+    if rank == 0:
+        line = {
+            "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms_max / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload_name(a), "layers": w.L, "requests": w.R, "context": "uniform 2048..8192",
+                       "Hq": w.Hq, "Hkv": w.Hkv, "page_tokens": w.P, "cap": cap,
+                       "held": {"k8v4": n_hi, "k4v2": n_lo, "new": n_new},
+                       "timed": "one dkv_decode_attention over every layer (significance update included)",
+                       "l2": "pages (%.1f GB) larger than L2" % (pages_used * 216 * w.P / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "k_attend", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes": alg,
+                         "ms": att_ms},
+            "gpu_launches": a.steps,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference_attention(a):
+    """CPU oracle arm of decode attention: each step is one oracle attention
+    call on layer 0 of the first 4 requests."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    w = workload(a)
+    smp = AttentionOracleSample(w)
+    for _ in range(a.warmup):
+        smp.step()
+    total, rows = 0.0, 0
+    for _ in range(a.steps):
+        dt, r_ = smp.step()
+        total += dt
+        rows += r_
+    value = rows / total
+    sample = "one oracle attention call on layer 0 of the first 4 requests per step, single-threaded"
+    print(json.dumps({
+        "impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1000.0 * total / a.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(a), "layers": w.L, "requests": w.R, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "page_tokens": w.P},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def main():
     a = _args()
     decode = a.workload == "decode"
-    if a.impl == "reference":
+    if decode and a.op == "attention":
+        run_reference_attention(a) if a.impl == "reference" else run_native_attention(a)
+    elif a.impl == "reference":
         run_reference_decode(a) if decode else run_reference(a)
     else:
         run_native_decode(a) if decode else run_native(a)

@@ -304,6 +304,45 @@ int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dk
   return DKV_OK;
 }
 
+int32_t dkv_decode_attention(const dkv_attn_batch *b, const dkv_pool *pool, const dkv_tables *t, void *stream) {
+  if (!b || !valid_pool(pool) || !t || !t->fwd || !t->unit_hdr || !aligned(t->unit_hdr, 16) ||
+      !aligned(t->fwd, 4) || t->pmax < 2)
+    return DKV_E_INVAL;
+  if (b->L < 1 || b->R < 0 || b->Hkv < 1 || b->Hq < b->Hkv || b->Hq % b->Hkv != 0 ||
+      b->Hq / b->Hkv > dkv::kAttendMaxG || b->cap < 1 || b->layer0 < 0 || b->n_layers < 0 ||
+      b->layer0 + static_cast<int64_t>(b->n_layers) > b->L || !std::isfinite(b->scale))
+    return DKV_E_INVAL;
+  if (!b->q || !b->out || !b->ctx_lens || !aligned(b->q, 16) || !aligned(b->out, 4) || !aligned(b->ctx_lens, 4))
+    return DKV_E_INVAL;
+  if ((b->k_new == nullptr) != (b->v_new == nullptr)) return DKV_E_INVAL;
+  if (b->k_new && (!b->new_lens || !aligned(b->k_new, 16) || !aligned(b->v_new, 16) || !aligned(b->new_lens, 4)))
+    return DKV_E_INVAL;
+  if (b->sig_sum && !aligned(b->sig_sum, 4)) return DKV_E_INVAL;
+  const int64_t units = static_cast<int64_t>(b->n_layers) * b->R * b->Hkv;
+  // one cluster of S blocks per unit, the fewest whose shares of a unit's
+  // logits (at most cap + 1 tokens) fit one block's shared memory
+  const int32_t G = b->Hq / b->Hkv;
+  int32_t S = 0, cmax = 0;
+  for (int32_t s = 1; s <= 8 && S == 0; s *= 2) {
+    const int32_t c = static_cast<int32_t>((static_cast<int64_t>(b->cap) + 1 + s - 1) / s);
+    if (dkv::attend_layout(c, G, t->pmax, pool->P).bytes <= 220 * 1024) {
+      S = s;
+      cmax = c;
+    }
+  }
+  if (S == 0 || units * S > INT32_MAX) return DKV_E_INVAL;
+  dkv::AttnArgs a{};
+  a.L = b->L; a.R = b->R; a.Hq = b->Hq; a.Hkv = b->Hkv; a.G = G; a.P = pool->P; a.pmax = t->pmax;
+  a.cap = b->cap; a.layer0 = b->layer0; a.n_layers = b->n_layers; a.cmax = cmax;
+  a.F = pool->F; a.units = units; a.scale = b->scale;
+  a.q = static_cast<const uint16_t *>(b->q);
+  a.k_new = static_cast<const uint16_t *>(b->k_new);
+  a.v_new = static_cast<const uint16_t *>(b->v_new);
+  a.new_lens = b->new_lens; a.ctx_lens = b->ctx_lens; a.out = b->out; a.sig_sum = b->sig_sum;
+  a.fwd = t->fwd; a.unit_hdr = t->unit_hdr; a.pages = pool->pages; a.status = pool->status;
+  return cuda_status(dkv::launch_attend(a, S, static_cast<cudaStream_t>(stream)));
+}
+
 int32_t dkv_dequant_page(const dkv_pool *pool, int32_t page_id, float *k_out, float *v_out, int32_t *pos_out,
                          void *stream) {
   if (!valid_pool(pool) || page_id < 0 || page_id >= pool->F || !k_out || !v_out || !pos_out) return DKV_E_INVAL;

@@ -235,6 +235,56 @@ struct DecodeArgs {
   int64_t njobs;
 };
 
+// Decode attention (attend.cu): one cluster of S blocks per unit; every warp
+// streams whole pages through a private ring of kAttendStages buffers.
+constexpr int kAttendStages = 2;
+constexpr int kAttendMaxG = 8;
+
+// Warps per block: 12 for up to four query heads per KV head, 8 above (the
+// second group of four heads doubles the registers a lane holds).
+__host__ __device__ constexpr int attend_warps(int G) { return G <= 4 ? 12 : 8; }
+
+struct AttnArgs {
+  int32_t L, R, Hq, Hkv, G, P, pmax, cap, layer0, n_layers;
+  int32_t cmax;                 // tokens one block of a cluster holds at most
+  int64_t F, units;             // units = n_layers * R * Hkv
+  float scale;
+  const uint16_t *q, *k_new, *v_new;
+  const int32_t *new_lens, *ctx_lens;
+  float *out, *sig_sum;
+  const int32_t *fwd, *unit_hdr;
+  const uint8_t *pages;
+  int32_t *status;
+};
+
+// Byte offsets of the attention kernel's dynamic shared memory.
+struct AttnLayout {
+  size_t stage;   // [warps][stages][216 P] page buffers (warps = attend_warps(G))
+  size_t bar;     // [warps][stages] mbarriers
+  size_t lg;      // [cmax][G] logits
+  size_t ps;      // [cmax] positions
+  size_t fw;      // [pmax] forward row
+  size_t red;     // [warps][G][128] partial outputs
+  size_t st;      // statistics: [warps][8] max, [warps][8] sum, 4 x [8]
+  size_t bytes;
+};
+
+__host__ __device__ inline AttnLayout attend_layout(int32_t cmax, int32_t G, int32_t pmax, int32_t P) {
+  auto up = [](size_t x) { return (x + 127) / 128 * 128; };
+  const size_t W = static_cast<size_t>(attend_warps(G));
+  AttnLayout o{};
+  size_t x = 0;
+  o.stage = x; x = up(x + W * kAttendStages * 216 * static_cast<size_t>(P));
+  o.bar = x; x = up(x + 8 * W * kAttendStages);
+  o.lg = x; x = up(x + 4 * static_cast<size_t>(cmax) * G);
+  o.ps = x; x = up(x + 4 * static_cast<size_t>(cmax));
+  o.fw = x; x = up(x + 4 * static_cast<size_t>(pmax));
+  o.red = x; x = up(x + 4 * W * G * 128);
+  o.st = x; x = up(x + 4 * static_cast<size_t>(kAttendMaxG) * (2 * W + 4));
+  o.bytes = x;
+  return o;
+}
+
 }  // namespace dkv
 
 // Launchers (defined in the kernel translation units).
@@ -255,4 +305,5 @@ cudaError_t launch_apply(const DecodeArgs &a, int32_t hpc, int32_t words, cudaSt
 cudaError_t launch_demote(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_index(const DecodeArgs &a, int grid, cudaStream_t s);
 size_t apply_smem(int32_t hpc, int32_t words, int32_t pmax);
+cudaError_t launch_attend(const AttnArgs &a, int32_t S, cudaStream_t s);
 }  // namespace dkv

@@ -76,6 +76,16 @@ class dkv_decode_batch(ctypes.Structure):
     ]
 
 
+class dkv_attn_batch(ctypes.Structure):
+    _fields_ = [
+        ("L", ctypes.c_int32), ("R", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+        ("cap", ctypes.c_int32), ("layer0", ctypes.c_int32), ("n_layers", ctypes.c_int32),
+        ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+        ("new_lens", ctypes.c_void_p), ("ctx_lens", ctypes.c_void_p), ("scale", ctypes.c_float),
+        ("out", ctypes.c_void_p), ("sig_sum", ctypes.c_void_p),
+    ]
+
+
 def load():
     """Load libdkv.so (raises if it was not built)."""
     global _lib
@@ -101,6 +111,7 @@ def load():
         "dkv_decode_index": ([P(dkv_decode_batch), P(dkv_pool), P(dkv_tables), vp], i32),
         "dkv_decode_step": ([P(dkv_decode_batch), P(dkv_params), P(dkv_pool), P(dkv_tables), vp, ctypes.c_size_t,
                              vp], i32),
+        "dkv_decode_attention": ([P(dkv_attn_batch), P(dkv_pool), P(dkv_tables), vp], i32),
         "dkv_profiler_create": ([i32, P(vp)], i32),
         "dkv_profiler_read": ([vp, vp, i32], i32),
         "dkv_profiler_destroy": ([vp], i32),
@@ -309,6 +320,13 @@ def dkv_decode_step(batch: dkv_decode_batch, alpha_h: float, alpha_l: float, poo
         raise DkvError(rc, "dkv_decode_step")
 
 
+def dkv_decode_attention(batch: dkv_attn_batch, pool: DevicePool, tables, stream=None) -> None:
+    pc, tc = pool.c(), tables.c()
+    rc = load().dkv_decode_attention(ctypes.byref(batch), ctypes.byref(pc), ctypes.byref(tc), _stream(stream))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_decode_attention")
+
+
 class _TableView:
     """Tables of a contiguous run of units (pointer offsets into DeviceTables)."""
 
@@ -368,3 +386,11 @@ class Decoder:
              profiler=None) -> None:
         dkv_decode_step(self.batch(d), alpha_h, alpha_l, self.pool, self.tables, self.workspace, stream=stream,
                         spin_limit=spin_limit, profiler=profiler)
+
+    def attend(self, q: torch.Tensor, ctx_lens: torch.Tensor, out: torch.Tensor, scale: float, layer0: int = 0,
+               k_new: torch.Tensor | None = None, v_new: torch.Tensor | None = None,
+               new_lens: torch.Tensor | None = None, sig_sum: torch.Tensor | None = None, stream=None) -> None:
+        """dkv_decode_attention over layers [layer0, layer0 + q.shape[0])."""
+        b = dkv_attn_batch(self.L, self.R, self.Hq, self.Hkv, self.cap, int(layer0), int(q.shape[0]), _p(q),
+                           _p(k_new), _p(v_new), _p(new_lens), _p(ctx_lens), float(scale), _p(out), _p(sig_sum))
+        dkv_decode_attention(b, self.pool, self.tables, stream=stream)

@@ -268,6 +268,51 @@ int32_t dkv_decode_index(const dkv_decode_batch *b, const dkv_pool *pool, const 
 int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dkv_pool *pool,
                         const dkv_tables *t, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Decode attention over the unified pages.
+ *
+ * DiffKV (arXiv 2412.03131), Figure 7 and section 6.1: the generation step's
+ * attention reads the mixed-precision unified pages.  The pages do not print
+ * that kernel; this is plain scaled dot-product attention.  For query head q
+ * of request r in layer l (unit (l, r, q / G), G = Hq / Hkv) the attended
+ * tokens are every used slot of the unit's K8V4 and K4V2 lists, with K and V
+ * the dequantised values fma(code, scale, zero) that dkv_dequant_page gives,
+ * plus the step's new token (its bf16 K and V, position ctx_lens[r]) when
+ * k_new is given and new_lens[r] = 1:
+ *   out = sum_t p_t v_t,   p = softmax_t(scale * (q . k_t)).
+ * An empty attended set gives a zero output.  With sig_sum given, each
+ * attended held token's significance row receives its probability
+ * (sig_sum[l][r * cap + pos][q] += p_t) and the new token's row is set to
+ * its p; this is the score whose average decides the classes (Pith review,
+ * "What carries the argument").  Counts (sig_cnt) are the caller's: +1 for
+ * every held position, 1 for the new token.
+ * Computed in fp32 (logits from the codes: scale_k (q . c) + zero_k (sum q)).
+ * ------------------------------------------------------------------------ */
+typedef struct dkv_attn_batch {
+  int32_t L, R, Hq, Hkv;     /* the tables' shape, as in dkv_decode_batch; 1 <= Hq / Hkv <= 8 */
+  int32_t cap;               /* positions per request (sig_sum rows); ctx + new <= cap */
+  int32_t layer0, n_layers;  /* attend layers [layer0, layer0 + n_layers) of the tables */
+  const void *q;             /* bf16 [n_layers][R][Hq][128], 16-byte aligned */
+  const void *k_new;         /* bf16 [n_layers][R][Hkv][128] or NULL (no new token), 16-byte aligned */
+  const void *v_new;         /* bf16, as k_new (NULL exactly when k_new is) */
+  const int32_t *new_lens;   /* int32 [R], 0 or 1 (read only with k_new) */
+  const int32_t *ctx_lens;   /* int32 [R]: tokens held before the step (the new token's position) */
+  float scale;               /* softmax scale, finite */
+  float *out;                /* out fp32 [n_layers][R][Hq][128] */
+  float *sig_sum;            /* NULL, or in/out fp32 [L][R * cap][Hq] */
+} dkv_attn_batch;
+
+/* Decode attention (above), asynchronous; allocates nothing.  The pool and
+ * tables are read only.  Synchronous DKV_E_INVAL: a bad shape or pointer,
+ * G outside 1..8, or a shape whose per-block shared memory does not fit 220 KB
+ * even with a cluster of 8 blocks per unit (a block holds 2 page buffers per
+ * warp, 16 x 216 P bytes, plus its share of the unit's logits and positions,
+ * (cap + 1) (4 G + 4) / S bytes).  Device-side errors (pool status word): DKV_E_LENS (a new
+ * token at ctx >= cap: attended without it), DKV_E_INTERNAL (a unit header,
+ * page id or stored position that contradicts the tables: that unit or token
+ * is left out). */
+int32_t dkv_decode_attention(const dkv_attn_batch *b, const dkv_pool *pool, const dkv_tables *t, void *stream);
+
 /* Synchronise `stream`, return the pool's device status word (DKV_OK or the
  * first device-side error since the last read) and clear it. */
 int32_t dkv_get_status(const dkv_pool *pool, void *stream);

@@ -1,0 +1,76 @@
+"""Test-side helpers for decode attention: a vectorised parser of a unit's
+held tokens from raw page bytes (codes, fp16 scale / zero, positions), and the
+error bound the GPU's fp32 attention is held to against the oracle's double
+result.  No attention is computed here."""
+from __future__ import annotations
+
+import numpy as np
+
+from tests.oracle_helpers import unpack
+
+U = 2.0 ** -24  # fp32 unit roundoff
+
+
+def unit_tokens(pages: np.ndarray, fwd_row: np.ndarray, hdr, P: int):
+    """Held tokens of a unit in list order (K8V4 list, then K4V2 list):
+    (K codes [n,128], V codes [n,128], k_s, k_z, v_s, v_z [n] float64,
+    positions [n] int64).  `pages` is indexable by the forward row's ids."""
+    n_hi, n_lo, p_hi, p_lo = (int(x) for x in hdr)
+    parts = []
+    for n, ids, per, kb, vb in ((n_hi, fwd_row[:p_hi], P, 8, 4), (n_lo, fwd_row[p_hi:p_hi + p_lo], 2 * P, 4, 2)):
+        if n == 0:
+            continue
+        pg = np.stack([pages[int(i)] for i in ids])                     # [pages, 216P]
+        kbytes = 16 * kb
+        vbytes = 16 * vb
+        kc = pg[:, :per * kbytes].reshape(-1, kbytes)[:n]
+        vc = pg[:, 128 * P:128 * P + per * vbytes].reshape(-1, vbytes)[:n]
+        meta = pg[:, 192 * P:192 * P + 8 * per].reshape(-1, 8)[:n].copy().view(np.uint16)
+        pos = pg[:, 208 * P:208 * P + 4 * per].reshape(-1, 4)[:n].copy().view(np.int32)[:, 0]
+        kq = unpack(kc.reshape(-1), kb).reshape(n, 128)
+        vq = unpack(vc.reshape(-1), vb).reshape(n, 128)
+        m = meta.view(np.float16).astype(np.float64)
+        parts.append((kq, vq, m[:, 0], m[:, 1], m[:, 2], m[:, 3], pos.astype(np.int64)))
+    if not parts:
+        z = np.zeros((0, 128), np.uint8)
+        e = np.zeros(0)
+        return z, z, e, e, e, e, np.zeros(0, np.int64)
+    return tuple(np.concatenate([p[i] for p in parts]) for i in range(7))
+
+
+def attention_bounds(q: np.ndarray, scale: float, toks, new_kv, p: np.ndarray):
+    """Error bounds of the GPU's fp32 decode attention of one query head.
+
+    q: [128] float64 (the bf16 query); toks: unit_tokens(...) of its KV head;
+    new_kv: None or (k [128], v [128]) float64 of the new token (attended
+    last); p: the oracle's probabilities in the same order.
+    Returns (bound on |out - out_oracle| per channel [128], bound on
+    |p_gpu - p| per token [n]).
+
+    The model (u = 2^-24): a logit is a sum of at most 16 fused products per
+    lane, a butterfly of at most 4 additions, then s*(q.c) + z*(sum q) and the
+    scale, so |dl_t| <= 32 u scale sum_d |q_d| (c_td s_t + |z_t|) (|q_d||k_d|
+    for the new token); exp(l - M) adds u |l - M| + 2 ulp; the denominator and
+    the outputs are fp32 sums of at most n + 32 terms.  The relative error of
+    p_t is then rho_t = expm1(eta_t) + expm1(sum_s p_s eta_s) + (n + 16) u with
+    eta_t = |dl_t| + u |l_t - M| + 2^-19 (the exponential and up to six
+    rescalings of running sums by exponential factors), and the output error is
+    sum_t p_t (rho_t + (n + 32) u) (c_td s_vt + |z_vt|).  Both bounds are
+    doubled to cover second-order terms."""
+    kq, vq, ks, kz, vs, vz, _ = toks
+    qa = np.abs(q)
+    kabs = (kq.astype(np.float64) * ks[:, None] + np.abs(kz)[:, None]) @ qa
+    vabs = vq.astype(np.float64) * vs[:, None] + np.abs(vz)[:, None]
+    if new_kv is not None:
+        kabs = np.append(kabs, np.abs(new_kv[0]) @ qa)
+        vabs = np.vstack([vabs, np.abs(new_kv[1])[None]])
+    n = kabs.size
+    if n == 0:
+        return np.zeros(128), np.zeros(0)
+    dl = 32 * U * scale * kabs
+    with np.errstate(divide="ignore"):
+        lm = np.where(p > 0, -np.log(np.where(p > 0, p, 1.0) / p.max()), 200.0)
+    eta = dl + U * np.minimum(lm, 200.0) + 2.0 ** -19  # exp, and up to 6 rescales by exp factors
+    rho = np.expm1(eta) + np.expm1(float(p @ eta)) + (n + 16) * U
+    out_b = 2.0 * ((p * (rho + (n + 32) * U)) @ vabs)
+    return out_b, 2.0 * rho * p

@@ -128,8 +128,42 @@ def test_decode_rejects_bad_arguments_without_launching(lib):
         dict(tab=libdkv.dkv_tables(256, 1, 0, 512)),
         dict(wsp=(1 << 20) + 8),
         dict(wsb=64),
+        dict(b=_dbatch(window=-1)),                               # negative recent window
+        dict(b=_dbatch(mode=2)),                                  # no such decode mode
     ]
     for c in cases:
         assert call(**c) == libdkv.DKV_E_INVAL, c
     assert lib.dkv_decode_index(ctypes.byref(_dbatch(ctx_lens=None)), ctypes.byref(_pool()), ctypes.byref(t),
                                 None) == libdkv.DKV_E_INVAL
+
+
+def _abatch(**kw):
+    b = dict(L=2, R=3, Hq=8, Hkv=2, cap=64, layer0=0, n_layers=2, q=256, k_new=None, v_new=None, new_lens=None,
+             ctx_lens=4096, scale=0.088, out=8192, sig_sum=None)
+    b.update(kw)
+    return libdkv.dkv_attn_batch(**b)
+
+
+def test_attention_rejects_bad_arguments_without_launching(lib):
+    t = libdkv.dkv_tables(256, 6, 0, 512)
+    cases = [
+        _abatch(Hq=7),                                  # Hq not a multiple of Hkv
+        _abatch(Hq=32),                                 # G = 16 > 8
+        _abatch(layer0=1),                              # layers past L
+        _abatch(n_layers=-1),
+        _abatch(q=None), _abatch(q=264),                # missing / misaligned query
+        _abatch(out=None), _abatch(ctx_lens=None),
+        _abatch(k_new=256),                             # K without V
+        _abatch(k_new=256, v_new=512),                  # new token without new_lens
+        _abatch(k_new=264, v_new=512, new_lens=1024),   # misaligned new K
+        _abatch(sig_sum=1030),                          # misaligned significance sums
+        _abatch(scale=float("inf")),
+        _abatch(cap=0),
+        _abatch(cap=1 << 22),                           # a unit's logits do not fit one cluster
+    ]
+    for c in cases:
+        rc = lib.dkv_decode_attention(ctypes.byref(c), ctypes.byref(_pool()), ctypes.byref(t), None)
+        assert rc == libdkv.DKV_E_INVAL, c
+    bad_tab = libdkv.dkv_tables(256, 6, 0, 520)         # unit headers not 16-byte aligned
+    assert lib.dkv_decode_attention(ctypes.byref(_abatch()), ctypes.byref(_pool()), ctypes.byref(bad_tab),
+                                    None) == libdkv.DKV_E_INVAL
