@@ -322,12 +322,16 @@ int32_t dkv_decode_attention(const dkv_attn_batch *b, const dkv_pool *pool, cons
   // one cluster of S blocks per unit, the fewest whose shares of a unit's
   // logits (at most cap + 1 tokens) fit one block's shared memory
   const int32_t G = b->Hq / b->Hkv;
+  // (first asking for a size that lets attend_blocks_per_sm blocks share an SM)
   int32_t S = 0, cmax = 0;
-  for (int32_t s = 1; s <= 8 && S == 0; s *= 2) {
-    const int32_t c = static_cast<int32_t>((static_cast<int64_t>(b->cap) + 1 + s - 1) / s);
-    if (dkv::attend_layout(c, G, t->pmax, pool->P).bytes <= 220 * 1024) {
-      S = s;
-      cmax = c;
+  const size_t budgets[2] = {static_cast<size_t>(220 * 1024) / dkv::attend_blocks_per_sm(G) - 1024, 220 * 1024};
+  for (int pass = 0; pass < 2 && S == 0; ++pass) {
+    for (int32_t s = 1; s <= 8 && S == 0; s *= 2) {
+      const int32_t c = static_cast<int32_t>((static_cast<int64_t>(b->cap) + 1 + s - 1) / s);
+      if (dkv::attend_layout(c, G, t->pmax, pool->P).bytes <= budgets[pass]) {
+        S = s;
+        cmax = c;
+      }
     }
   }
   if (S == 0 || units * S > INT32_MAX) return DKV_E_INVAL;

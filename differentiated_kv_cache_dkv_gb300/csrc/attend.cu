@@ -12,7 +12,7 @@
 // a unit's logits fit one block's shared memory.  Block `rank` takes a
 // contiguous share of the unit's token sequence (the K8V4 list, then the
 // K4V2 list, then the new token) and the pages that hold it.  Each of its
-// warps takes every 8th of those pages and streams them through a private
+// warps takes its share of those pages, round robin, and streams them through a private
 // ring of page buffers (bulk async copies completing on mbarriers), so each
 // page is read from HBM once, whole and contiguous.  Per 16-slot tile of a
 // page the warp
@@ -187,7 +187,7 @@ __device__ __forceinline__ T unrot(const T (&z)[4], int t, int i) {
 }
 
 template <int NT>  // n-tiles of four query heads (G <= 4 NT)
-__global__ void __launch_bounds__(32 * attend_warps(4 * NT)) k_attend(AttnArgs a) {
+__global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_sm(4 * NT)) k_attend(AttnArgs a) {
   constexpr int kWarps = attend_warps(4 * NT);
   constexpr int kAttendThreads = 32 * kWarps;
   cg::cluster_group cluster = cg::this_cluster();
@@ -438,9 +438,14 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT)) k_attend(AttnArgs a
           const float lg1 = (v1 && hv) ? a.scale * fmaf(ks1, d1, kz1 * qsum[j]) : -INFINITY;
           if (v0 && hv) lg[(tok0 + s0 - c0) * G + hh] = lg0;
           if (v1 && hv) lg[(tok0 + s1 - c0) * G + hh] = lg1;
+          // the head's maximum over the tile is taken (a butterfly) only when
+          // some lane of the warp needs the reference to move
           float tmx = fmaxf(lg0, lg1);
+          const bool up = tmx > m[j] + kRescale || (m[j] == -INFINITY && tmx > -INFINITY);
+          if (__any_sync(kFull, up)) {
 #pragma unroll
-          for (int off = 4; off < 32; off <<= 1) tmx = fmaxf(tmx, __shfl_xor_sync(kFull, tmx, off));
+            for (int off = 4; off < 32; off <<= 1) tmx = fmaxf(tmx, __shfl_xor_sync(kFull, tmx, off));
+          }
           if (tmx > m[j] + kRescale || (m[j] == -INFINITY && tmx > -INFINITY)) {  // uniform per head
             const float f = m[j] == -INFINITY ? 0.0f : __expf(m[j] - tmx);
             l[j] *= f;
@@ -476,9 +481,13 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT)) k_attend(AttnArgs a
 #pragma unroll
         for (int k = 0; k < kChunkTiles; ++k)
           if (k < nt) wx = fmaxf(wx, fmaxf(w0[k][j], w1[k][j]));
+        int ex = wx > 0.0f ? min(static_cast<int>((__float_as_uint(wx) >> 23) & 0xff) - 127, 100) : -100;
+        if (__any_sync(kFull, ex > ew[j])) {  // rare: the head's largest exponent (a butterfly)
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) wx = fmaxf(wx, __shfl_xor_sync(kFull, wx, off));
-        const int ex = wx > 0.0f ? min(static_cast<int>((__float_as_uint(wx) >> 23) & 0xff) - 127, 100) : -100;
+          for (int off = 4; off < 32; off <<= 1) ex = max(ex, __shfl_xor_sync(kFull, ex, off));
+        } else {
+          ex = ew[j];
+        }
         if (ex > ew[j]) {  // uniform per head
           const float f = pow2f(max(ew[j] - ex, -126));
 #pragma unroll
@@ -677,9 +686,9 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT)) k_attend(AttnArgs a
 
   // ---- significance: add each token's probability to its row.  Thread
   // (t0, g) = (tid / G, tid % G) takes head g of tokens t0, t0 + T, ...
-  // (T = threads / G), so a warp's stores are consecutive; four in flight.
+  // (T = threads / G), so a warp's stores are consecutive; eight in flight.
   if (a.sig_sum != nullptr && !failed) {
-    constexpr int kB = 4;
+    constexpr int kB = 8;
     const int64_t row0 = (static_cast<int64_t>(a.layer0 + li) * a.R + r) * a.cap;
     const int32_t nloc = c1 - c0;
     const int T = kAttendThreads / G;

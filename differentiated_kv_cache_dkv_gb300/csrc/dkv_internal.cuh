@@ -240,9 +240,12 @@ struct DecodeArgs {
 constexpr int kAttendStages = 2;
 constexpr int kAttendMaxG = 8;
 
-// Warps per block: 12 for up to four query heads per KV head, 8 above (the
-// second group of four heads doubles the registers a lane holds).
-__host__ __device__ constexpr int attend_warps(int G) { return G <= 4 ? 12 : 8; }
+// Warps per block: 6 for up to four query heads per KV head (two blocks share
+// an SM, so one block's merges and significance updates overlap the other's
+// page streaming), 8 above (the second group of four heads doubles the
+// registers a lane holds: one block per SM).
+__host__ __device__ constexpr int attend_warps(int G) { return G <= 4 ? 6 : 8; }
+__host__ __device__ constexpr int attend_blocks_per_sm(int G) { return G <= 4 ? 2 : 1; }
 
 struct AttnArgs {
   int32_t L, R, Hq, Hkv, G, P, pmax, cap, layer0, n_layers;
