@@ -156,3 +156,45 @@ def test_attention_new_token_past_capacity_is_a_length_error():
                new_lens=_dev(torch.tensor([0, 1], dtype=torch.int32)))
     assert libdkv.dkv_get_status(dec.pool) == libdkv.DKV_OK
     assert torch.equal(out[0, 0], out2[0, 0])  # request 0 attended its held tokens only
+
+
+def test_attention_leaves_out_what_contradicts_the_tables():
+    """A unit header whose page counts do not match its token counts, or a
+    forward entry outside the pool, is reported (DKV_E_INTERNAL) and left out:
+    the kernel reads no page through it, and every other unit's output keeps
+    its bits (the kernel's reductions run in a fixed order)."""
+    w = W.small("attx", lens=[300, 7, 517, 0, 129], L=1)
+    hd, dec = _state(w, cap=560, steps=1)
+    q = _dev(W.decode_queries(w, 1, 4))
+    ctx = _dev(hd.ctx["ctx_lens"])
+
+    def run():
+        out = torch.zeros((1, w.R, w.Hq, 128), dtype=torch.float32, device="cuda")
+        dec.attend(q, ctx, out, 0.088)
+        return out, libdkv.dkv_get_status(dec.pool)
+
+    ref, st = run()
+    assert st == libdkv.DKV_OK
+    G = w.Hq // w.Hkv
+    u_bad = 2 * w.Hkv + 1  # request 2, KV head 1
+    keep = torch.ones(w.R * w.Hkv, dtype=torch.bool)
+    keep[u_bad] = False
+    keep = keep.view(w.R, w.Hkv).repeat_interleave(G, dim=1).cuda()  # [R, Hq]
+
+    saved = dec.tables.unit_hdr[u_bad].clone()
+    dec.tables.unit_hdr[u_bad, 0] += 1  # one more K8V4 token than its pages say
+    out, st = run()
+    dec.tables.unit_hdr[u_bad] = saved
+    assert st == libdkv.DKV_E_INTERNAL
+    assert torch.equal(out[0][keep], ref[0][keep])
+    assert not out[0, 2, G:2 * G].any()  # the rejected unit attends to nothing
+
+    saved = dec.tables.fwd[u_bad, 0].clone()
+    dec.tables.fwd[u_bad, 0] = dec.pool.F + 5  # a page id outside the pool
+    out, st = run()
+    dec.tables.fwd[u_bad, 0] = saved
+    assert st == libdkv.DKV_E_INTERNAL
+    assert torch.equal(out[0][keep], ref[0][keep])
+    assert torch.isfinite(out).all()
+    out, st = run()
+    assert st == libdkv.DKV_OK and torch.equal(out, ref)

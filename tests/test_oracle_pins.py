@@ -525,3 +525,29 @@ def test_memory_fraction_worked_example():
     frac = code_bytes / (N * 2 * 128 * 2)
     assert abs(frac - (12 * n_hi + 6 * n_lo) / (32 * N)) < 1e-12
     assert round(frac, int(g["printed_decimals"])) == g["memory_fraction"]
+
+
+def test_class_mix_matches_the_log_normal_closed_form():
+    """The input recipe, not parity: scores log-normal(sigma) with mean 1/N and
+    G independent query heads put a KV head at or above alpha/N with
+    probability 1 - (1 - Q((ln alpha + sigma^2 / 2) / sigma))^G (Q the normal
+    tail).  For sigma = 2, G = 4, alpha 1.0 / 0.2 that is about 49.9% K8V4,
+    39.0% K4V2 and 11.1% pruned; the oracle's classes of a seeded batch of
+    65,536 token-rows must match within 1% (about five standard deviations)."""
+    from scipy.stats import norm
+
+    w = W.small("mix", L=1, lens=[4096, 4096], Hq=32, Hkv=8, sigma=2.0, n_outlier=0)
+    st, pool, tab = run_oracle(w, W.to_numpy(W.make_inputs(w, 21)))
+    assert st == oracle.OK
+    cls = tab.classes
+    G = w.Hq // w.Hkv
+
+    def above(alpha):
+        q = norm.sf((np.log(alpha) + w.sigma ** 2 / 2) / w.sigma)
+        return 1.0 - (1.0 - q) ** G
+
+    hi, lo_or_hi = above(w.alpha_h), above(w.alpha_l)
+    assert abs(hi - 0.499) < 0.002 and abs(1.0 - lo_or_hi - 0.111) < 0.002  # the closed form itself
+    assert abs(float(np.mean(cls == 2)) - hi) < 0.01
+    assert abs(float(np.mean(cls == 1)) - (lo_or_hi - hi)) < 0.01
+    assert abs(float(np.mean(cls == 0)) - (1.0 - lo_or_hi)) < 0.01
