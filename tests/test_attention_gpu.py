@@ -182,7 +182,7 @@ def test_attention_leaves_out_what_contradicts_the_tables():
     keep = keep.view(w.R, w.Hkv).repeat_interleave(G, dim=1).cuda()  # [R, Hq]
 
     saved = dec.tables.unit_hdr[u_bad].clone()
-    dec.tables.unit_hdr[u_bad, 0] += 1  # one more K8V4 token than its pages say
+    dec.tables.unit_hdr[u_bad, 2] += 1  # one more K8V4 page than its tokens need
     out, st = run()
     dec.tables.unit_hdr[u_bad] = saved
     assert st == libdkv.DKV_E_INTERNAL
