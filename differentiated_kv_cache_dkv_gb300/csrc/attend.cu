@@ -175,9 +175,9 @@ __device__ __forceinline__ uint32_t sel_pair(int b) { return b | (b << 4) | ((4 
 //            mt / 2 of its 4 bytes.
 // fp32 inputs become two fp16 parts (nearest, then the remainder) in two
 // columns, so the products carry 22 bits of them; query heads are scaled by
-// a power of two into fp16 range, and the weights p s_v by a power of two
-// per group of up to four tiles.
-constexpr int kChunkTiles = 4;
+// a power of two into fp16 range, and the weights p s_v by the power of two
+// that puts the largest weight seen so far there.
+constexpr int kChunkTiles = 1;
 
 // Element (4 - t + i) & 3 of four words, i.e. undo the rotated load order.
 template <typename T>
@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
   float *wl = wm + kWarps * kAttendMaxG;                   // [warps][8] sums
   float *bM = wl + kWarps * kAttendMaxG, *bL = bM + kAttendMaxG;  // block max / sum (read remotely)
   float *gM = bL + kAttendMaxG, *gL = gM + kAttendMaxG;           // cluster max / sum
+  float *bF = gL + kAttendMaxG;  // [8 blocks][8 heads]: exp(block max - cluster max)
 
   __shared__ int failed;  // a warp gave up on a copy: the significance update is skipped
   if (threadIdx.x == 0) failed = 0;
@@ -592,14 +593,16 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
     }
   }
   __syncthreads();
-  if (threadIdx.x < G) {
+  if (threadIdx.x < G) {  // thread g owns column g of wm / wl: it turns maxima into factors
     const int g = threadIdx.x;
     float mx = -INFINITY;
     for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, wm[w * kAttendMaxG + g]);
     float sum = 0.0f;
     for (int w = 0; w < kWarps; ++w) {
       const float mw = wm[w * kAttendMaxG + g];
-      if (mw > -INFINITY) sum += wl[w * kAttendMaxG + g] * expf(mw - mx);
+      const float f = mw > -INFINITY ? expf(mw - mx) : 0.0f;
+      sum = fmaf(wl[w * kAttendMaxG + g], f, sum);
+      wm[w * kAttendMaxG + g] = f;
     }
     bM[g] = mx;
     bL[g] = sum;
@@ -607,12 +610,8 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
   __syncthreads();
   for (int e = threadIdx.x; e < G * 128; e += kAttendThreads) {
     const int g = e >> 7;
-    const float mx = bM[g];
     float sum = 0.0f;
-    for (int w = 0; w < kWarps; ++w) {
-      const float mw = wm[w * kAttendMaxG + g];
-      if (mw > -INFINITY) sum += red[w * G * 128 + e] * expf(mw - mx);
-    }
+    for (int w = 0; w < kWarps; ++w) sum = fmaf(red[w * G * 128 + e], wm[w * kAttendMaxG + g], sum);
     red[e] = sum;  // each e is read and written by this thread alone
   }
 
@@ -664,7 +663,9 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
     float sum = 0.0f;
     for (int q = 0; q < S; ++q) {
       const float mq = cluster.map_shared_rank(bM, q)[g];
-      if (mq > -INFINITY) sum += cluster.map_shared_rank(bL, q)[g] * expf(mq - mx);
+      const float f = mq > -INFINITY ? expf(mq - mx) : 0.0f;
+      sum = fmaf(cluster.map_shared_rank(bL, q)[g], f, sum);
+      bF[q * kAttendMaxG + g] = f;
     }
     gM[g] = mx;
     gL[g] = sum;
@@ -675,10 +676,7 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
     for (int e = threadIdx.x; e < G * 128; e += kAttendThreads) {
       const int g = e >> 7;
       float sum = 0.0f;
-      for (int q = 0; q < S; ++q) {
-        const float mq = cluster.map_shared_rank(bM, q)[g];
-        if (mq > -INFINITY) sum += cluster.map_shared_rank(red, q)[e] * expf(mq - gM[g]);
-      }
+      for (int q = 0; q < S; ++q) sum = fmaf(cluster.map_shared_rank(red, q)[e], bF[q * kAttendMaxG + g], sum);
       const float lsum = gL[g];
       out[e] = lsum > 0.0f ? __fdiv_rn(sum, lsum) : 0.0f;
     }

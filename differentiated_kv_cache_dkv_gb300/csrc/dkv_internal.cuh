@@ -268,7 +268,7 @@ struct AttnLayout {
   size_t ps;      // [cmax] positions
   size_t fw;      // [pmax] forward row
   size_t red;     // [warps][G][128] partial outputs
-  size_t st;      // statistics: [warps][8] max, [warps][8] sum, 4 x [8]
+  size_t st;      // statistics: [warps][8] max, [warps][8] sum, 4 x [8], [8][8] block factors
   size_t bytes;
 };
 
@@ -283,7 +283,7 @@ __host__ __device__ inline AttnLayout attend_layout(int32_t cmax, int32_t G, int
   o.ps = x; x = up(x + 4 * static_cast<size_t>(cmax));
   o.fw = x; x = up(x + 4 * static_cast<size_t>(pmax));
   o.red = x; x = up(x + 4 * W * G * 128);
-  o.st = x; x = up(x + 4 * static_cast<size_t>(kAttendMaxG) * (2 * W + 4));
+  o.st = x; x = up(x + 4 * static_cast<size_t>(kAttendMaxG) * (2 * W + 12));
   o.bytes = x;
   return o;
 }
