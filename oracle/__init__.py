@@ -72,6 +72,15 @@ class _AttnBatch(ctypes.Structure):
     ]
 
 
+class _PrefillBatch(ctypes.Structure):
+    _fields_ = [
+        ("L", ctypes.c_int32), ("R", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+        ("T", ctypes.c_int64), ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("lens", ctypes.c_void_p), ("scale", ctypes.c_double), ("out", ctypes.c_void_p),
+        ("sig_sum", ctypes.c_void_p), ("sig_cnt", ctypes.c_void_p),
+    ]
+
+
 def lib():
     """Load (building first if needed) the oracle shared library."""
     global _lib
@@ -100,6 +109,8 @@ def lib():
         L.oracle_decode_attention.argtypes = [ctypes.POINTER(_AttnBatch), ctypes.POINTER(_Pool),
                                               ctypes.POINTER(_Tables)]
         L.oracle_decode_attention.restype = ctypes.c_int32
+        L.oracle_prefill_attention.argtypes = [ctypes.POINTER(_PrefillBatch)]
+        L.oracle_prefill_attention.restype = ctypes.c_int32
         L.oracle_dequant_page.argtypes = [ctypes.POINTER(_Pool), ctypes.c_int32, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_void_p]
         L.oracle_dequant_page.restype = None
@@ -251,3 +262,21 @@ def decode_attention(a: dict, pool: Pool, tables: Tables, p_out: bool = True):
     tt = tables._c()
     st = int(lib().oracle_decode_attention(ctypes.byref(b), ctypes.byref(pp), ctypes.byref(tt)))
     return st, out, p
+
+
+def prefill_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, lens, scale: float):
+    """Prefill attention with significance accumulation (reading S).  q, k, v:
+    uint16 bf16 bits [L][T][Hq or Hkv][128].  Returns (status, out [L][T][Hq][128]
+    float64, sig_sum [L][T][Hq] float64, sig_cnt [T] int32)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    L, T, Hq = q.shape[0], q.shape[1], q.shape[2]
+    out = np.zeros((L, T, Hq, 128), dtype=np.float64)
+    sig = np.zeros((L, T, Hq), dtype=np.float64)
+    cnt = np.zeros(T, dtype=np.int32)
+    b = _PrefillBatch(L, lens.size, Hq, k.shape[2], T, _ptr(q), _ptr(k), _ptr(v), _ptr(lens), float(scale),
+                      _ptr(out), _ptr(sig), _ptr(cnt))
+    st = int(lib().oracle_prefill_attention(ctypes.byref(b)))
+    return st, out, sig, cnt

@@ -84,6 +84,15 @@
  *      each attended position is reported; it is the score that the
  *      significance sum of that position accumulates (the average attention
  *      a token receives, "What carries the argument").
+ *  S   Prefill attention and the significance it produces ("What carries the
+ *      argument": significance is the average attention a token receives
+ *      from the tokens after it; Referee Report, major comment 2: the average
+ *      is over the N - i scores token i receives).  Query i of a request
+ *      attends, with causal softmax(scale * q . k), over keys 0 .. i of its
+ *      request (query head q reads KV head q / G), with the bf16 K and V as
+ *      they are; out_i = sum_j p(i, j) v_j.  Key j's significance sum is
+ *      sum over i >= j of p(i, j), its count N - j (query j itself
+ *      included).  Taken in double.
  */
 #include "dkv_oracle.h"
 
@@ -826,6 +835,51 @@ int32_t oracle_decode_attention(const oracle_attn_batch *b, const oracle_pool *p
     }
   }
   return ORACLE_OK;
+}
+
+int32_t oracle_prefill_attention(const oracle_prefill_batch *b) {
+  if (!b || b->L < 1 || b->R < 0 || b->Hkv < 1 || b->Hq < b->Hkv || b->Hq % b->Hkv != 0 || !b->q || !b->k ||
+      !b->v || !b->lens || !b->out || !b->sig_sum || !b->sig_cnt)
+    return ORACLE_E_INVAL;
+  const int64_t T = b->T, Hq = b->Hq, Hkv = b->Hkv, G = Hq / Hkv;
+  int64_t start = 0;
+  for (int64_t r = 0; r < b->R; ++r) {
+    const int64_t n = b->lens[r];
+    for (int64_t i = 0; i < n; ++i) b->sig_cnt[start + i] = static_cast<int32_t>(n - i);
+    for (int64_t l = 0; l < b->L; ++l) {
+      for (int64_t qh = 0; qh < Hq; ++qh) {
+        const int64_t h = qh / G;
+        for (int64_t j = 0; j < n; ++j) b->sig_sum[(l * T + start + j) * Hq + qh] = 0.0;
+        std::vector<double> lg(static_cast<size_t>(n));
+        for (int64_t i = 0; i < n; ++i) {
+          const uint16_t *qi = b->q + ((l * T + start + i) * Hq + qh) * 128;
+          double mx = -INFINITY;
+          for (int64_t j = 0; j <= i; ++j) {
+            const uint16_t *kj = b->k + ((l * T + start + j) * Hkv + h) * 128;
+            double dot = 0.0;
+            for (int d = 0; d < 128; ++d) dot += static_cast<double>(bf16_value(qi[d])) * bf16_value(kj[d]);
+            lg[j] = b->scale * dot;
+            mx = std::max(mx, lg[j]);
+          }
+          double den = 0.0;
+          for (int64_t j = 0; j <= i; ++j) {
+            lg[j] = std::exp(lg[j] - mx);
+            den += lg[j];
+          }
+          double *o = b->out + ((l * T + start + i) * Hq + qh) * 128;
+          for (int d = 0; d < 128; ++d) o[d] = 0.0;
+          for (int64_t j = 0; j <= i; ++j) {
+            const double p = lg[j] / den;
+            const uint16_t *vj = b->v + ((l * T + start + j) * Hkv + h) * 128;
+            for (int d = 0; d < 128; ++d) o[d] += p * bf16_value(vj[d]);
+            b->sig_sum[(l * T + start + j) * Hq + qh] += p;
+          }
+        }
+      }
+    }
+    start += n;
+  }
+  return start == T ? ORACLE_OK : ORACLE_E_INVAL;
 }
 
 void oracle_dequant_page(const oracle_pool *pool, int32_t page_id, float *k_out, float *v_out,

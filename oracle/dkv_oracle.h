@@ -138,6 +138,24 @@ typedef struct oracle_attn_batch {
 int32_t oracle_decode_attention(const oracle_attn_batch *b, const oracle_pool *pool,
                                 const oracle_tables *t);
 
+/* Prefill attention with significance accumulation (reading S in
+ * dkv_oracle.cpp): causal softmax attention of every query head over the
+ * earlier tokens of its request, and the significance inputs of compaction. */
+typedef struct oracle_prefill_batch {
+  int32_t L, R, Hq, Hkv;
+  int64_t T;               /* sum of lens */
+  const uint16_t *q;       /* bf16 [L][T][Hq][128] */
+  const uint16_t *k;       /* bf16 [L][T][Hkv][128] */
+  const uint16_t *v;
+  const int32_t *lens;     /* [R] */
+  double scale;
+  double *out;             /* [L][T][Hq][128] */
+  double *sig_sum;         /* [L][T][Hq]: attention received, summed over the token's queries */
+  int32_t *sig_cnt;        /* [T]: that number of queries, N - i */
+} oracle_prefill_batch;
+
+int32_t oracle_prefill_attention(const oracle_prefill_batch *b);
+
 /* Decode a page into fp32 K, V ([2P][128] each) and positions ([2P]). */
 void oracle_dequant_page(const oracle_pool *pool, int32_t page_id,
                          float *k_out, float *v_out, int32_t *pos_out);
