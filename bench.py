@@ -47,8 +47,9 @@ def _args():
                     help="decode: recent window W (tokens kept at K8V4; 0 = none)")
     ap.add_argument("--decode-mode", type=int, default=0, choices=[0, 1],
                     help="decode: 0 re-scores every older token, 1 only the one leaving the window")
-    ap.add_argument("--op", default="step", choices=["step", "attention"],
-                    help="decode: time the generation step, or the attention over the pages")
+    ap.add_argument("--op", default="step", choices=["step", "attention", "prefill-attention"],
+                    help="decode: the generation step or the attention over the pages; prefill workloads: "
+                         "the compaction step or the prefill attention that produces its significance inputs")
     return ap.parse_args()
 
 
@@ -70,6 +71,8 @@ def workload_name(a) -> str:
     name = a.workload
     if getattr(a, "op", "step") == "attention":
         name += " attention"
+    if getattr(a, "op", "step") == "prefill-attention":
+        name += " prefill attention"
     if getattr(a, "window", 0) or getattr(a, "decode_mode", 0):
         name += f" (window {a.window}, {'single candidate' if a.decode_mode else 'every token re-scored'})"
     if a.layers or a.requests:
@@ -834,10 +837,207 @@ def run_reference_attention(a):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
 
 
+# ----------------------------------------------------- prefill attention ---
+
+PREFILL_METRIC = "KV tokens attended in prefill/sec (token-rows: one token x one (layer, KV head)), significance produced"
+
+
+def _prefill_pairs(lens) -> int:
+    return sum(n * (n + 1) // 2 for n in lens)
+
+
+class PrefillOracleSample:
+    """The oracle's prefill attention on a bounded sample: layer 0 of the first
+    request, its first two query heads (one KV head)."""
+
+    def __init__(self, w):
+        import dataclasses
+
+        import torch
+
+        from differentiated_kv_cache_dkv_gb300 import workloads as W
+
+        G = w.Hq // w.Hkv
+        nq = min(2, G)
+        self.w = dataclasses.replace(w, L=1, lens=[w.lens[0]], Hq=nq, Hkv=1)
+        b16 = lambda t: t.contiguous().view(torch.int16).numpy().view("uint16")  # noqa: E731
+        kv = dataclasses.replace(w, L=1, lens=[w.lens[0]])
+        self.k = b16(W.make_kv_layer(kv, W.SEED_BASE, 0, 0)[:, :1][None])
+        self.v = b16(W.make_kv_layer(kv, W.SEED_BASE, 0, 1)[:, :1][None])
+        self.q = b16(W.prefill_queries(self.w, W.SEED_BASE, 0)[None])
+        self.rows = w.lens[0]  # token-rows of one (layer, KV head), attended by nq of its G heads
+
+    def step(self):
+        import oracle
+
+        t = time.perf_counter()
+        st, _, _, _ = oracle.prefill_attention(self.q, self.k, self.v, self.w.lens, ATTN_SCALE)
+        dt = time.perf_counter() - t
+        assert st == 0, st
+        return dt, self.rows
+
+
+def run_native_prefill_attention(a):
+    import torch
+
+    from differentiated_kv_cache_dkv_gb300 import libdkv
+    from differentiated_kv_cache_dkv_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    libdkv.load()
+    w = workload(a)
+    dev = torch.device("cuda", local)
+    seed = W.SEED_BASE + 1000 * rank
+    k = torch.empty((w.L, w.T, w.Hkv, 128), dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k)
+    q = torch.empty((w.L, w.T, w.Hq, 128), dtype=torch.bfloat16, device=dev)
+    for l in range(w.L):
+        k[l] = W.make_kv_layer(w, seed, l, 0, dev)
+        v[l] = W.make_kv_layer(w, seed, l, 1, dev)
+        q[l] = W.prefill_queries(w, seed, l, dev)
+    lens = torch.tensor(w.lens, dtype=torch.int32, device=dev)
+    out = torch.empty((w.L, w.T, w.Hq, 128), dtype=torch.float32, device=dev)
+    sig = torch.empty((w.L, w.T, w.Hq), dtype=torch.float32, device=dev)
+    cnt = torch.empty((w.T,), dtype=torch.int32, device=dev)
+    pool = libdkv.DevicePool(1, 16, dev)
+    libdkv.dkv_init_pool(pool)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        libdkv.dkv_prefill_attention(q, k, v, lens, max(w.lens), ATTN_SCALE, out, sig, cnt, pool)
+
+    for _ in range(a.warmup):
+        call()
+    torch.cuda.synchronize()
+    assert libdkv.dkv_get_status(pool) == libdkv.DKV_OK
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(a.steps):
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    assert libdkv.dkv_get_status(pool) == libdkv.DKV_OK
+    per = [e0.elapsed_time(e1) for e0, e1 in evs]
+    ms_max = max_over_ranks(sum(per), dev, world)
+    rows = w.T * w.L * w.Hkv
+    value = whole_job_rate(rows * a.steps, world, ms_max)
+    # algorithmic flops: q . k and p v over the causal pairs, every query head
+    flops = 4.0 * 128 * _prefill_pairs(w.lens) * w.Hq * w.L
+    tf = flops / (statistics.mean(per) / 1000.0) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        peak, peak_kind = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), "measured (sustained bf16)"
+    except Exception:
+        peak, peak_kind = 1700.0, "fallback (sustained bf16)"
+
+    e2e = None
+    if a.e2e_steps > 0:
+        host = {"q": q.cpu().pin_memory(), "k": k.cpu().pin_memory(), "v": v.cpu().pin_memory()}
+        dst = {"q": q, "k": k, "v": v}
+        sig_h = torch.empty(sig.shape, dtype=torch.float32).pin_memory()
+        cnt_h = torch.empty(cnt.shape, dtype=torch.int32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in host.values())
+        d2h = sig_h.numel() * 4 + cnt_h.numel() * 4
+        te = 0.0
+        for _ in range(a.e2e_steps):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            s0.record(stream)
+            for k_, x in host.items():
+                dst[k_].copy_(x, non_blocking=True)
+            call()
+            sig_h.copy_(sig, non_blocking=True)
+            cnt_h.copy_(cnt, non_blocking=True)
+            s1.record(stream)
+            torch.cuda.synchronize()
+            te += s0.elapsed_time(s1)
+        te = max_over_ranks(te, dev, world)
+        e2e = {"value": whole_job_rate(rows * a.e2e_steps, world, te), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": a.e2e_steps,
+               "note": "outputs stay on the device; the significance sums and counts are read back"}
+        del host
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        smp = PrefillOracleSample(w)
+        tt, rr, nn = 0.0, 0, 0
+        while tt < a.cpu_seconds or nn == 0:
+            dt, r_ = smp.step()
+            tt += dt
+            rr += r_
+            nn += 1
+        G = w.Hq // w.Hkv
+        # the sample attends nq of a KV head's G query heads: scale its time to all G
+        cpu = {"value": rr / (tt * G / smp.w.Hq), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"layer 0, request 0 ({smp.rows} tokens), {smp.w.Hq} of the {G} query heads of KV "
+                         f"head 0, x {nn} calls, {tt:.1f} s single-threaded; time scaled to all {G} heads"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": PREFILL_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms_max / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_name(a), "layers": w.L, "requests": w.R, "tokens": w.T, "Hq": w.Hq,
+                       "Hkv": w.Hkv, "timed": "one dkv_prefill_attention over every layer (outputs, significance "
+                                              "sums and counts)",
+                       "l2": "inputs (%.1f GB) larger than L2" % ((q.numel() + 2 * k.numel()) * 2 / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "kernel": "k_prefill", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak, "peak_kind": peak_kind, "traffic": None, "algorithmic_flops": flops,
+                         "ms": statistics.mean(per)},
+            "gpu_launches": a.steps * 2,  # k_sigcnt, k_prefill (the zeroing is a memset)
+            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu}), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference_prefill_attention(a):
+    """CPU oracle arm of prefill attention: each step is one oracle call on the
+    bounded sample (layer 0, request 0, two query heads)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    w = workload(a)
+    smp = PrefillOracleSample(w)
+    for _ in range(a.warmup):
+        smp.step()
+    total, rows = 0.0, 0
+    for _ in range(a.steps):
+        dt, r_ = smp.step()
+        total += dt
+        rows += r_
+    G = w.Hq // w.Hkv
+    value = rows / (total * G / smp.w.Hq)
+    sample = "oracle prefill attention of layer 0, request 0, two query heads per step; time scaled to all G heads"
+    print(json.dumps({
+        "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1000.0 * total / a.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(a), "layers": w.L, "requests": w.R, "Hq": w.Hq, "Hkv": w.Hkv},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def main():
     a = _args()
     decode = a.workload == "decode"
-    if decode and a.op == "attention":
+    if a.op == "prefill-attention" and not decode:
+        run_reference_prefill_attention(a) if a.impl == "reference" else run_native_prefill_attention(a)
+    elif decode and a.op == "attention":
         run_reference_attention(a) if a.impl == "reference" else run_native_attention(a)
     elif a.impl == "reference":
         run_reference_decode(a) if decode else run_reference(a)

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "lib", "libdkv.so")
-SOURCES = ["api.cu", "classify.cu", "alloc.cu", "pack.cu", "pool.cu", "noalloc.cu", "decode.cu", "attend.cu"]
+SOURCES = ["api.cu", "classify.cu", "alloc.cu", "pack.cu", "pool.cu", "noalloc.cu", "decode.cu", "attend.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

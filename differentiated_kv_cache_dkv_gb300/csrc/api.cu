@@ -347,6 +347,30 @@ int32_t dkv_decode_attention(const dkv_attn_batch *b, const dkv_pool *pool, cons
   return cuda_status(dkv::launch_attend(a, S, static_cast<cudaStream_t>(stream)));
 }
 
+int32_t dkv_prefill_attention(const dkv_prefill_batch *b, const dkv_pool *pool, void *stream) {
+  if (!b || !pool || !pool->status || !aligned(pool->status, 4)) return DKV_E_INVAL;
+  if (b->L < 1 || b->R < 0 || b->Hkv < 1 || b->Hq < b->Hkv || b->Hq % b->Hkv != 0 || b->max_len < 0 ||
+      b->T < 0 || b->reserved != 0 || !std::isfinite(b->scale))
+    return DKV_E_INVAL;
+  if (b->R > 65535 || static_cast<int64_t>(b->L) * b->Hq > 65535) return DKV_E_INVAL;  // grid y and z
+  if (!b->q || !b->k || !b->v || !b->lens || !b->out || !b->sig_sum || !b->sig_cnt || !aligned(b->q, 16) ||
+      !aligned(b->k, 16) || !aligned(b->v, 16) || !aligned(b->lens, 4) || !aligned(b->out, 8) ||
+      !aligned(b->sig_sum, 4) || !aligned(b->sig_cnt, 4))
+    return DKV_E_INVAL;
+  dkv::PrefillArgs a{};
+  a.L = b->L; a.R = b->R; a.Hq = b->Hq; a.Hkv = b->Hkv; a.G = b->Hq / b->Hkv; a.max_len = b->max_len;
+  a.T = b->T; a.scale = b->scale;
+  a.q = static_cast<const uint16_t *>(b->q);
+  a.k = static_cast<const uint16_t *>(b->k);
+  a.v = static_cast<const uint16_t *>(b->v);
+  a.lens = b->lens; a.out = b->out; a.sig_sum = b->sig_sum; a.sig_cnt = b->sig_cnt; a.status = pool->status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t sig_bytes = sizeof(float) * static_cast<size_t>(b->L) * static_cast<size_t>(b->T) * b->Hq;
+  if (sig_bytes > 0)
+    if (const int32_t rc = cuda_status(cudaMemsetAsync(b->sig_sum, 0, sig_bytes, s))) return rc;
+  return cuda_status(dkv::launch_prefill(a, s));
+}
+
 int32_t dkv_dequant_page(const dkv_pool *pool, int32_t page_id, float *k_out, float *v_out, int32_t *pos_out,
                          void *stream) {
   if (!valid_pool(pool) || page_id < 0 || page_id >= pool->F || !k_out || !v_out || !pos_out) return DKV_E_INVAL;

@@ -288,6 +288,18 @@ __host__ __device__ inline AttnLayout attend_layout(int32_t cmax, int32_t G, int
   return o;
 }
 
+// Prefill attention with significance accumulation (prefill.cu).
+struct PrefillArgs {
+  int32_t L, R, Hq, Hkv, G, max_len;
+  int64_t T;
+  float scale;
+  const uint16_t *q, *k, *v;
+  const int32_t *lens;
+  float *out, *sig_sum;
+  int32_t *sig_cnt;
+  int32_t *status;
+};
+
 }  // namespace dkv
 
 // Launchers (defined in the kernel translation units).
@@ -309,4 +321,5 @@ cudaError_t launch_demote(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_index(const DecodeArgs &a, int grid, cudaStream_t s);
 size_t apply_smem(int32_t hpc, int32_t words, int32_t pmax);
 cudaError_t launch_attend(const AttnArgs &a, int32_t S, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);
 }  // namespace dkv

@@ -86,6 +86,16 @@ class dkv_attn_batch(ctypes.Structure):
     ]
 
 
+class dkv_prefill_batch(ctypes.Structure):
+    _fields_ = [
+        ("L", ctypes.c_int32), ("R", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+        ("max_len", ctypes.c_int32), ("reserved", ctypes.c_int32), ("T", ctypes.c_int64),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("lens", ctypes.c_void_p),
+        ("scale", ctypes.c_float), ("out", ctypes.c_void_p), ("sig_sum", ctypes.c_void_p),
+        ("sig_cnt", ctypes.c_void_p),
+    ]
+
+
 def load():
     """Load libdkv.so (raises if it was not built)."""
     global _lib
@@ -112,6 +122,7 @@ def load():
         "dkv_decode_step": ([P(dkv_decode_batch), P(dkv_params), P(dkv_pool), P(dkv_tables), vp, ctypes.c_size_t,
                              vp], i32),
         "dkv_decode_attention": ([P(dkv_attn_batch), P(dkv_pool), P(dkv_tables), vp], i32),
+        "dkv_prefill_attention": ([P(dkv_prefill_batch), P(dkv_pool), vp], i32),
         "dkv_profiler_create": ([i32, P(vp)], i32),
         "dkv_profiler_read": ([vp, vp, i32], i32),
         "dkv_profiler_destroy": ([vp], i32),
@@ -325,6 +336,20 @@ def dkv_decode_attention(batch: dkv_attn_batch, pool: DevicePool, tables, stream
     rc = load().dkv_decode_attention(ctypes.byref(batch), ctypes.byref(pc), ctypes.byref(tc), _stream(stream))
     if rc != DKV_OK:
         raise DkvError(rc, "dkv_decode_attention")
+
+
+def dkv_prefill_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lens: torch.Tensor, max_len: int,
+                          scale: float, out: torch.Tensor, sig_sum: torch.Tensor, sig_cnt: torch.Tensor,
+                          pool: DevicePool, stream=None) -> None:
+    """dkv_prefill_attention: q [L][T][Hq][128], k / v [L][T][Hkv][128] bf16;
+    out fp32 [L][T][Hq][128], sig_sum fp32 [L][T][Hq], sig_cnt int32 [T]."""
+    L, T, Hq = int(q.shape[0]), int(q.shape[1]), int(q.shape[2])
+    b = dkv_prefill_batch(L, int(lens.numel()), Hq, int(k.shape[2]), int(max_len), 0, T, _p(q), _p(k), _p(v),
+                          _p(lens), float(scale), _p(out), _p(sig_sum), _p(sig_cnt))
+    pc = pool.c()
+    rc = load().dkv_prefill_attention(ctypes.byref(b), ctypes.byref(pc), _stream(stream))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_prefill_attention")
 
 
 class _TableView:

@@ -346,3 +346,9 @@ def decode_queries(w: Workload, n_layers: int, seed: int, step: int = 0, device=
     """bf16 [n_layers][R][Hq][D] queries of one generation step, N(0,1)."""
     g = _gen(seed * 1000003 + 700000 + step, device)
     return torch.randn((n_layers, w.R, w.Hq, D), generator=g, device=device).to(torch.bfloat16)
+
+
+def prefill_queries(w: Workload, seed: int, layer: int, device="cpu") -> torch.Tensor:
+    """bf16 [T][Hq][D] prefill queries of one layer, N(0,1)."""
+    g = _gen(seed * 1000003 + 800000 + layer, device)
+    return torch.randn((w.T, w.Hq, D), generator=g, device=device).to(torch.bfloat16)

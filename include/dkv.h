@@ -313,6 +313,41 @@ typedef struct dkv_attn_batch {
  * is left out). */
 int32_t dkv_decode_attention(const dkv_attn_batch *b, const dkv_pool *pool, const dkv_tables *t, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Prefill attention that produces the significance inputs of compaction.
+ *
+ * DiffKV (arXiv 2412.03131), Pith review, "What carries the argument": a
+ * token's significance is the average attention it receives from the tokens
+ * after it; Referee Report, major comment 2: the average is over the N - i
+ * scores token i receives.  For every layer, request and query head q (KV head
+ * q / G), query i attends causally over keys 0 .. i of its request:
+ *   out_i = sum_{j <= i} p(i, j) v_j,   p(i, .) = softmax_j(scale * q_i . k_j),
+ * and the call writes sig_sum[l][t(j)][q] = sum_{i >= j} p(i, j) and
+ * sig_cnt[t(j)] = N - j: the inputs dkv_compact classifies.  Computed with
+ * bf16 x bf16 products exact, fp32 accumulation and p carried to 22 bits.
+ * ------------------------------------------------------------------------ */
+typedef struct dkv_prefill_batch {
+  int32_t L, R, Hq, Hkv;     /* 1 <= Hq / Hkv */
+  int32_t max_len;           /* >= every lens[r] */
+  int32_t reserved;
+  int64_t T;                 /* sum of lens */
+  const void *q;             /* bf16 [L][T][Hq][128], 16-byte aligned */
+  const void *k;             /* bf16 [L][T][Hkv][128], 16-byte aligned (the dkv_batch layout) */
+  const void *v;             /* bf16 [L][T][Hkv][128], 16-byte aligned; |v| <= 65504 */
+  const int32_t *lens;       /* int32 [R] */
+  float scale;               /* softmax scale, finite */
+  float *out;                /* out fp32 [L][T][Hq][128] */
+  float *sig_sum;            /* out fp32 [L][T][Hq] (overwritten) */
+  int32_t *sig_cnt;          /* out int32 [T] (overwritten) */
+} dkv_prefill_batch;
+
+/* Prefill attention (above), asynchronous; allocates nothing.  Synchronous
+ * DKV_E_INVAL for a bad shape or pointer.  Device-side (pool status word;
+ * only `pool->status` is used): DKV_E_LENS when the lens add up to more than
+ * T.  Significance sums are added across query tiles by fp32 atomics, so
+ * their last bits depend on the order. */
+int32_t dkv_prefill_attention(const dkv_prefill_batch *b, const dkv_pool *pool, void *stream);
+
 /* Synchronise `stream`, return the pool's device status word (DKV_OK or the
  * first device-side error since the last read) and clear it. */
 int32_t dkv_get_status(const dkv_pool *pool, void *stream);

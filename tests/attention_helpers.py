@@ -74,3 +74,34 @@ def attention_bounds(q: np.ndarray, scale: float, toks, new_kv, p: np.ndarray):
     rho = np.expm1(eta) + np.expm1(float(p @ eta)) + (n + 16) * U
     out_b = 2.0 * ((p * (rho + (n + 32) * U)) @ vabs)
     return out_b, 2.0 * rho * p
+
+
+def prefill_bounds(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
+    """Error bounds of the GPU's causal prefill attention of one (request,
+    query head): q [n][128], k, v [n][128] float64 (the bf16 values).
+
+    Products of bf16 values are exact; the logits are fp32 sums of 128 of them
+    on the tensor cores: |dl_ij| <= 64 u scale sum_d |q_id| |k_jd|.  The
+    probabilities then carry rho_ij as in attention_bounds (exponential,
+    normaliser, 22-bit fp16 parts); the outputs are fp32 sums over n keys of
+    p times v in fp16 (exact in the normal range, 2^-25 below it), and a
+    significance sum adds n probabilities in fp32 (atomics in any order).
+    Returns (bound on |out| errors [n][128], bound on |sig_sum| errors [n],
+    the probabilities p [n][n] in double)."""
+    n = q.shape[0]
+    if n == 0:
+        return np.zeros((0, 128)), np.zeros(0), np.zeros((0, 0))
+    lg = scale * (q @ k.T)
+    mask = np.tril(np.ones((n, n), dtype=bool))
+    lg = np.where(mask, lg, -np.inf)
+    mx = lg.max(1, keepdims=True)
+    e = np.exp(lg - mx)
+    p = e / e.sum(1, keepdims=True)
+    dl = 64 * U * scale * (np.abs(q) @ np.abs(k).T)
+    with np.errstate(invalid="ignore"):
+        eta = np.where(mask, dl + U * np.minimum(mx - lg, 200.0) + 2.0 ** -19, 0.0)
+    rho = np.expm1(eta) + np.expm1((p * eta).sum(1, keepdims=True)) + (n + 16) * U
+    rho = np.where(mask, rho, 0.0)
+    out_b = 2.0 * ((p * (rho + (n + 32) * U)) @ np.abs(v) + 2.0 ** -24)
+    sig_b = 2.0 * ((p * rho).sum(0) + (n + 8) * U * p.sum(0))
+    return out_b, sig_b, p
