@@ -32,7 +32,7 @@ namespace dkv {
 
 namespace {
 
-constexpr int kQ = 64;          // queries per block
+constexpr int kQ = 64;          // queries per block (16 per warp)
 constexpr int kK = 64;          // keys per tile
 constexpr int kWarpsP = 4;
 constexpr int kThreadsP = 32 * kWarpsP;
@@ -75,23 +75,25 @@ __device__ __forceinline__ void split2(float x, float y, uint32_t &hi, uint32_t 
 // transposed to fp16; keys at or past n are zero.
 __device__ __forceinline__ void stage(PrefillSmem &sm, const PrefillArgs &a, int64_t row0, int32_t h, int32_t kb,
                                      int32_t n, bool with_v) {
-  // 64 keys x 16 chunks of 16 bytes
+  // K: 64 keys x 16 chunks of 16 bytes, a key's chunks on consecutive threads
   for (int c = threadIdx.x; c < kK * 16; c += kThreadsP) {
     const int key = c >> 4, ch = c & 15;
-    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-    if (kb + key < n) {
-      const int64_t off = ((row0 + kb + key) * a.Hkv + h) * 128 + ch * 8;
-      kv = __ldg(reinterpret_cast<const uint4 *>(a.k + off));
-      if (with_v) vv = __ldg(reinterpret_cast<const uint4 *>(a.v + off));
-    }
+    uint4 kv = make_uint4(0, 0, 0, 0);
+    if (kb + key < n) kv = __ldg(reinterpret_cast<const uint4 *>(a.k + ((row0 + kb + key) * a.Hkv + h) * 128 + ch * 8));
     *reinterpret_cast<uint4 *>(&sm.k[key][ch * 8]) = kv;
-    if (with_v) {
-      const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+  }
+  if (!with_v) return;
+  // V transposed: consecutive threads take consecutive keys of one chunk, so
+  // their 2-byte stores into a V^T row are consecutive
+  for (int c = threadIdx.x; c < kK * 16; c += kThreadsP) {
+    const int key = c & (kK - 1), ch = c / kK;
+    uint4 vv = make_uint4(0, 0, 0, 0);
+    if (kb + key < n) vv = __ldg(reinterpret_cast<const uint4 *>(a.v + ((row0 + kb + key) * a.Hkv + h) * 128 + ch * 8));
+    const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t b = (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16);
-        sm.vt[ch * 8 + e][key] = __float2half_rn(__uint_as_float(b));
-      }
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t b = (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16);
+      sm.vt[ch * 8 + e][key] = __float2half_rn(__uint_as_float(b));
     }
   }
 }
@@ -242,7 +244,9 @@ __global__ void __launch_bounds__(kThreadsP) k_prefill(PrefillArgs a) {
     if (threadIdx.x < kK) {
       const int32_t key = kt * kK + threadIdx.x;
       if (key < n) {
-        const float s = sm.cs[0][threadIdx.x] + sm.cs[1][threadIdx.x] + sm.cs[2][threadIdx.x] + sm.cs[3][threadIdx.x];
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarpsP; ++w) s += sm.cs[w][threadIdx.x];
         if (s != 0.0f) atomicAdd(a.sig_sum + (row0 + key) * a.Hq + qh, s);
       }
     }
