@@ -167,3 +167,26 @@ def test_attention_rejects_bad_arguments_without_launching(lib):
     bad_tab = libdkv.dkv_tables(256, 6, 0, 520)         # unit headers not 16-byte aligned
     assert lib.dkv_decode_attention(ctypes.byref(_abatch()), ctypes.byref(_pool()), ctypes.byref(bad_tab),
                                     None) == libdkv.DKV_E_INVAL
+
+
+def _pbatch(**kw):
+    b = dict(L=2, R=3, Hq=8, Hkv=2, max_len=100, reserved=0, T=250, q=256, k=512, v=768, lens=1024, scale=0.088,
+             out=2048, sig_sum=4096, sig_cnt=8192)
+    b.update(kw)
+    return libdkv.dkv_prefill_batch(**b)
+
+
+def test_prefill_attention_rejects_bad_arguments_without_launching(lib):
+    cases = [
+        _pbatch(Hq=7),                      # Hq not a multiple of Hkv
+        _pbatch(L=0), _pbatch(T=-1), _pbatch(max_len=-1), _pbatch(reserved=1),
+        _pbatch(q=None), _pbatch(q=264),    # missing / misaligned query
+        _pbatch(k=520), _pbatch(v=None),
+        _pbatch(lens=None), _pbatch(out=2052), _pbatch(sig_sum=None), _pbatch(sig_cnt=8194),
+        _pbatch(scale=float("nan")),
+        _pbatch(R=70000),                   # more requests than a grid dimension holds
+    ]
+    for c in cases:
+        rc = lib.dkv_prefill_attention(ctypes.byref(c), ctypes.byref(_pool()), None)
+        assert rc == libdkv.DKV_E_INVAL, c
+    assert lib.dkv_prefill_attention(ctypes.byref(_pbatch()), None, None) == libdkv.DKV_E_INVAL
