@@ -305,9 +305,11 @@ typedef struct dkv_attn_batch {
 /* Decode attention (above), asynchronous; allocates nothing.  The pool and
  * tables are read only.  Synchronous DKV_E_INVAL: a bad shape or pointer,
  * G outside 1..8, or a shape whose per-block shared memory does not fit 220 KB
- * even with a cluster of 8 blocks per unit (a block holds 2 page buffers per
- * warp, 16 x 216 P bytes, plus its share of the unit's logits and positions,
- * (cap + 1) (4 G + 4) / S bytes).  Device-side errors (pool status word): DKV_E_LENS (a new
+ * even with a cluster of 8 blocks per unit (a block holds 2 page buffers of
+ * 216 P bytes per warp, 6 warps for G <= 4 and 8 above, plus its share of the
+ * unit's logits and positions, (cap + 1) (4 G + 4) / S bytes; S is the
+ * smallest cluster that fits, preferring two blocks per SM).  Device-side
+ * errors (pool status word): DKV_E_LENS (a new
  * token at ctx >= cap: attended without it), DKV_E_INTERNAL (a unit header,
  * page id or stored position that contradicts the tables: that unit or token
  * is left out). */
