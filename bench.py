@@ -415,7 +415,7 @@ class DecodeOracleSample:
         self._fresh()
 
     def _fresh(self):
-        from tests.decode_helpers import HostDecode
+        from oracle.host_decode import HostDecode
 
         self.hd = HostDecode(self.w, decode_cap(self.w, self.max_steps), window=self.window, mode=self.mode)
         self.local = 0
@@ -656,7 +656,7 @@ class AttentionOracleSample:
         import torch
 
         from differentiated_kv_cache_dkv_gb300 import workloads as W
-        from tests.decode_helpers import HostDecode
+        from oracle.host_decode import HostDecode
 
         self.w = dataclasses.replace(w, L=1, lens=list(w.lens[:n_req]))
         self.cap = decode_cap(self.w, 1)

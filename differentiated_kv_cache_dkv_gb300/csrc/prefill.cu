@@ -45,6 +45,7 @@ struct PrefillSmem {
   __half vt[128][kVStride];
   float cs[kWarpsP][kK];
   int64_t start;
+  int32_t lens_ok;
 };
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -69,6 +70,41 @@ __device__ __forceinline__ void split2(float x, float y, uint32_t &hi, uint32_t 
   const __half lx = __float2half_rn(x - __half2float(hx)), ly = __float2half_rn(y - __half2float(hy));
   hi = static_cast<uint32_t>(__half_as_ushort(hx)) | (static_cast<uint32_t>(__half_as_ushort(hy)) << 16);
   lo = static_cast<uint32_t>(__half_as_ushort(lx)) | (static_cast<uint32_t>(__half_as_ushort(ly)) << 16);
+}
+
+// Where request r starts in the token axis, from the lengths, validated by
+// warp 0 of the block before anything is read or written: every lens[q] must
+// lie in [0, max_len] and they must add up to T.  Returns false (after the
+// first failing block records DKV_E_LENS) when they do not.  Every thread of
+// the block must call it.
+__device__ __forceinline__ bool request_start(const PrefillArgs &a, int32_t r, int64_t *start_sm, int32_t *ok_sm,
+                                              int64_t &start) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int64_t before = 0, total = 0;
+    int bad = 0;
+    for (int32_t q = lane; q < a.R; q += 32) {
+      const int32_t n = __ldg(a.lens + q);
+      if (n < 0 || n > a.max_len) bad = 1;
+      total += n;
+      if (q < r) before += n;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+      total += __shfl_xor_sync(0xffffffffu, total, o);
+      bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    if (lane == 0) {
+      const bool ok = !bad && total == a.T;
+      *start_sm = before;
+      *ok_sm = ok ? 1 : 0;
+      if (!ok) set_error(a.status, DKV_E_LENS);
+    }
+  }
+  __syncthreads();
+  start = *start_sm;
+  return *ok_sm != 0;
 }
 
 // Stage key tile [kb, kb + kK) of (layer, KV head): K rows as they are, V
@@ -127,20 +163,12 @@ __global__ void __launch_bounds__(kThreadsP) k_prefill(PrefillArgs a) {
   const int32_t r = blockIdx.y;
   const int32_t l = static_cast<int32_t>(blockIdx.z / a.Hq), qh = static_cast<int32_t>(blockIdx.z % a.Hq);
   const int32_t h = qh / a.G;
-  const int32_t n = __ldg(a.lens + r);
   const int32_t qb = blockIdx.x * kQ;
-  if (n < 0 || qb >= n) return;  // no cluster or grid barrier: leaving early is safe
-  if (threadIdx.x == 0) {
-    int64_t s = 0;
-    for (int32_t q = 0; q < r; ++q) s += __ldg(a.lens + q);
-    sm.start = s;
-  }
-  __syncthreads();
-  const int64_t start = sm.start;
-  if (start + n > a.T) {
-    if (threadIdx.x == 0) set_error(a.status, DKV_E_LENS);
-    return;
-  }
+  int64_t start = 0;
+  // no cluster or grid barrier: leaving early is safe
+  if (!request_start(a, r, &sm.start, &sm.lens_ok, start)) return;
+  const int32_t n = __ldg(a.lens + r);
+  if (qb >= n) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
   const int32_t i0 = qb + 16 * warp;                  // this warp's first row
   const int64_t row0 = static_cast<int64_t>(l) * a.T + start;  // (layer, request) token row 0
@@ -265,11 +293,12 @@ __global__ void __launch_bounds__(kThreadsP) k_prefill(PrefillArgs a) {
 
 // sig_cnt[start_r + i] = N_r - i.
 __global__ void __launch_bounds__(256) k_sigcnt(PrefillArgs a) {
+  __shared__ int64_t start_sm;
+  __shared__ int32_t ok_sm;
   const int32_t r = blockIdx.y;
-  const int32_t n = __ldg(a.lens + r);
   int64_t start = 0;
-  for (int32_t q = 0; q < r; ++q) start += __ldg(a.lens + q);
-  if (n < 0 || start + n > a.T) return;  // reported by k_prefill
+  if (!request_start(a, r, &start_sm, &ok_sm, start)) return;
+  const int32_t n = __ldg(a.lens + r);
   for (int32_t i = blockIdx.x * 256 + threadIdx.x; i < n; i += gridDim.x * 256) a.sig_cnt[start + i] = n - i;
 }
 

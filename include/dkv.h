@@ -345,9 +345,12 @@ typedef struct dkv_prefill_batch {
 
 /* Prefill attention (above), asynchronous; allocates nothing.  Synchronous
  * DKV_E_INVAL for a bad shape or pointer.  Device-side (pool status word;
- * only `pool->status` is used): DKV_E_LENS when the lens add up to more than
- * T.  Significance sums are added across query tiles by fp32 atomics, so
- * their last bits depend on the order. */
+ * only `pool->status` is used): DKV_E_LENS when a length is negative or above
+ * max_len, or the lengths do not add up to T; every block checks all of them
+ * before it reads or writes anything, so out and sig_cnt are then left as
+ * they were (sig_sum is zeroed first, in any case).  Significance sums are
+ * added across query tiles by fp32 atomics, so their last bits depend on the
+ * order. */
 int32_t dkv_prefill_attention(const dkv_prefill_batch *b, const dkv_pool *pool, void *stream);
 
 /* Synchronise `stream`, return the pool's device status word (DKV_OK or the

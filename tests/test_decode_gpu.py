@@ -258,11 +258,13 @@ def test_decode_zero_low_threshold():
     _run(w, cap=320, steps=5, p_prune=0.05, p_demote=0.1, slot_check_every=5)
 
 
-@pytest.mark.parametrize("window,mode", [(0, 1), (3, 0), (3, 1), (64, 0), (64, 1), (600, 0)])
+@pytest.mark.parametrize("window,mode", [(0, 1), (3, 0), (3, 1), (64, 0), (64, 1), (600, 0), (600, 1)])
 def test_decode_recent_window_and_candidate(window, mode):
     """Recent window W and the single-candidate policy (mode 1): same bytes as
     the oracle after every step.  Heavy churn so that candidates do change;
-    request lengths below, at and above W; W = 600 covers every request."""
+    request lengths below, at and above W; W = 600 covers every request, so
+    in either mode nothing held changes class (in mode 1 no candidate leaves
+    the window)."""
     w = W.small("decw", lens=[300, 7, 517, 0, 129, 64, 3])
     hd, dec, _ = _run(w, cap=560, steps=10, p_prune=0.3, p_demote=0.3, window=window, mode=mode)
     if window == 600 or (window == 0 and mode == 1):

@@ -21,6 +21,7 @@ import torch
 
 import oracle
 from differentiated_kv_cache_dkv_gb300 import workloads as W
+from tests.edge_rows import dequant_bound
 from tests.oracle_helpers import bf16_to_f32, f16, page_slots, run_oracle, unit_rows
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -310,8 +311,10 @@ def test_range_errors_in_quantizer():
 
 def test_dequant_error_bound():
     """|x - (z + q*s)| <= s/2 + 1e-6 (evaluated in fp64).  fp32 rounding of
-    (x - z)/s next to a half-integer may add at most n*2^-23*s; such elements
-    are counted and held to that looser bound."""
+    x - z and of the quotient by s moves t = (x - z)/s by at most
+    (n + 1/2) 2^-23 next to a half-integer; such elements are counted and held
+    to that looser bound (tests/edge_rows.dequant_bound, which the GPU tests
+    use too)."""
     w = W.small("bound", L=1, lens=[300, 129])
     n = W.to_numpy(W.make_inputs(w))
     st, pool, tab = run_oracle(w, n)
@@ -327,7 +330,7 @@ def test_dequant_error_bound():
                 err = np.abs(x - (z + codes.astype(np.float64) * s))
                 strict = err <= 0.5 * s + 1e-6
                 loose += int((~strict).sum())
-                assert np.all(err <= s * (0.5 + ((1 << nb) - 1) * 2.0 ** -23) + 1e-6)
+                assert np.all(err <= dequant_bound(s, nb))
     assert loose < 50
 
 

@@ -15,7 +15,8 @@ import oracle
 from differentiated_kv_cache_dkv_gb300 import libdkv
 from differentiated_kv_cache_dkv_gb300 import workloads as W
 from tests.gpu_helpers import assert_same_state, fetch, make_compactor, oracle_state, to_device
-from tests.oracle_helpers import bf16_to_f32, run_oracle
+from tests.edge_rows import dequant_bound
+from tests.oracle_helpers import bf16_to_f32, f16, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -213,16 +214,18 @@ def test_dequant_matches_oracle_and_bound():
         assert np.array_equal(k[i].view(np.uint32), ko.view(np.uint32))
         assert np.array_equal(v[i].view(np.uint32), vo.view(np.uint32))
         assert np.array_equal(pos[i], po)
-        # bound against the bf16 input: |x - x'| <= s/2 (+ fp32 rounding slack)
+        # bound against the bf16 input, per element, with the slot's own scale
         u = int(pool.rev_unit[pid])
         h, r = u % w.Hkv, (u // w.Hkv) % w.R
         start = sum(w.lens[:r])
+        high = pool.page_cls[pid] == 2
+        meta = pool.pages[pid][192 * w.P:208 * w.P].view(np.uint16).reshape(2 * w.P, 4)
         for s in np.nonzero(po >= 0)[0]:
             t = start + po[s]
-            for x_bits, xq in ((n["k"][0, t, h], ko[s]), (n["v"][0, t, h], vo[s])):
+            ms = f16(meta[s]).astype(np.float64)
+            for x_bits, xq, sc, nb in ((n["k"][0, t, h], k[i][s], ms[0], 8 if high else 4),
+                                       (n["v"][0, t, h], v[i][s], ms[2], 4 if high else 2)):
                 x = bf16_to_f32(x_bits).astype(np.float64)
-                span = x.max() - x.min()
-                nb = 255 if xq is ko[s] and pool.page_cls[pid] == 2 else None
-                assert np.all(np.abs(x - xq) <= span / 2 + 1e-6 + 1e-3 * span)
+                assert np.all(np.abs(x - xq.astype(np.float64)) <= dequant_bound(sc, nb)), (pid, s)
     k1, v1, p1 = libdkv.dkv_dequant_page(comp.pool, int(live[0]))
     assert torch.equal(k1.cpu(), torch.from_numpy(k[0]))

@@ -108,3 +108,32 @@ def test_prefill_attention_feeds_compaction():
     near = (np.abs(score - w.alpha_h / N) < 1e-4 * w.alpha_h / N) | (np.abs(score - w.alpha_l / N) < 1e-4 * w.alpha_l / N)
     assert np.array_equal(got[~near], want[~near])
     assert (got == 2).any() and (got == 1).any() and (got == 0).any()
+
+
+@pytest.mark.parametrize("bad_lens,max_len", [
+    ([-5, 70, 10], 70),     # a negative earlier length: request 1 would start before the layer
+    ([20, 55, 0], 50),      # a length above max_len: its queries past the grid would go uncomputed
+    ([20, 30, 10], 64),     # lengths that do not add up to T
+])
+def test_prefill_attention_rejects_bad_lengths(bad_lens, max_len):
+    """Every length is validated before any access: DKV_E_LENS is recorded,
+    and neither the outputs nor the counts are written."""
+    T = 75
+    g = torch.Generator().manual_seed(4)
+    q = torch.randn((1, T, 4, 128), generator=g).to(torch.bfloat16).cuda()
+    k = torch.randn((1, T, 2, 128), generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn((1, T, 2, 128), generator=g).to(torch.bfloat16).cuda()
+    pool = libdkv.DevicePool(4, 16)
+    libdkv.dkv_init_pool(pool)
+    out = torch.full((1, T, 4, 128), 7.0, dtype=torch.float32, device="cuda")
+    sig = torch.empty((1, T, 4), dtype=torch.float32, device="cuda")
+    cnt = torch.full((T,), -5, dtype=torch.int32, device="cuda")
+    lens = torch.tensor(bad_lens, dtype=torch.int32, device="cuda")
+    libdkv.dkv_prefill_attention(q, k, v, lens, max_len, SCALE, out, sig, cnt, pool)
+    assert libdkv.dkv_get_status(pool) == libdkv.DKV_E_LENS
+    assert torch.all(out == 7.0) and torch.all(cnt == -5)
+    # the same buffers with valid lengths then work
+    lens = torch.tensor([20, 45, 10], dtype=torch.int32, device="cuda")
+    libdkv.dkv_prefill_attention(q, k, v, lens, 64, SCALE, out, sig, cnt, pool)
+    assert libdkv.dkv_get_status(pool) == libdkv.DKV_OK
+    assert cnt[0].item() == 20 and cnt[20].item() == 45
