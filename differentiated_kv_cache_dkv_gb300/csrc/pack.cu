@@ -46,8 +46,9 @@
 //       that finds no group left arrives on the stage's "empty" mbarrier and
 //       moves on; the stage is refilled once all 16 have left it.
 // Unused slots of the pages are filled by k_commit, which walks every page.
-// Every mbarrier wait is bounded; on expiry the CTA records DKV_E_TIMEOUT,
-// drains its own copies in flight (again bounded) and leaves.
+// Every mbarrier wait is bounded by the global timer (about a second); on
+// expiry the CTA records DKV_E_TIMEOUT, drains its own copies in flight
+// (again bounded) and leaves.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda.h>
@@ -65,7 +66,8 @@ constexpr int kProducerWarps = 1;
 constexpr int kConsumerWarps = 16;
 constexpr int kRowsPerConsumerWarp = kTileTokens / kConsumerWarps;  // 8: one per 4-lane group
 constexpr int kPackThreads = 32 * (kConsumerWarps + kProducerWarps);
-constexpr int64_t kWaitLimit = 1ll << 24;  // polls of one mbarrier before giving up
+constexpr uint64_t kWaitNs = 1000000000ull;  // an mbarrier wait gives up after about a second
+constexpr uint32_t kWaitPolls = 1u << 26;    // ... or after this many polls, whichever is first
 static_assert(kRowsPerConsumerWarp == 8, "8 groups of 4 lanes per consumer warp");
 
 // 1536 = 1.5 * 2^10 puts y in [1024, 2048) (ulp 2^-13); the extra 0.5 turns
@@ -103,10 +105,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase with the given parity to complete: false after
+// about kWaitNs of the global timer (or kWaitPolls polls, whichever first).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   const uint32_t addr = smem_addr(bar);
-  for (int64_t i = 0; i < kWaitLimit; ++i) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
     uint32_t done;
     asm volatile(
         "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
@@ -114,6 +124,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
         : "r"(addr), "r"(parity)
         : "memory");
     if (done) return true;
+    if ((i & 63) == 63) {
+      const uint64_t t = global_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > kWaitNs) return false;
+    }
   }
   return false;
 }

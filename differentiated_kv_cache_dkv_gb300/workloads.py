@@ -60,6 +60,7 @@ class Workload:
     recent: int = 0                  # last `recent` tokens boosted by recent_scale
     recent_scale: float = 10.0
     F: int = 0                       # pages in the pool; 0 = worst case
+    scheme: int = 0                  # precision scheme: 0 K8V4/K4V2, 1 K8V2/K4V1, 2 K4V8/K2V4
     extra: dict = field(default_factory=dict)
 
     @property

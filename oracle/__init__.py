@@ -39,7 +39,7 @@ class _Batch(ctypes.Structure):
 
 class _Pool(ctypes.Structure):
     _fields_ = [
-        ("F", ctypes.c_int64), ("P", ctypes.c_int32), ("free_list", ctypes.c_void_p),
+        ("F", ctypes.c_int64), ("P", ctypes.c_int32), ("scheme", ctypes.c_int32), ("free_list", ctypes.c_void_p),
         ("cursors", ctypes.c_void_p), ("rev_unit", ctypes.c_void_p),
         ("rev_idx", ctypes.c_void_p), ("page_cls", ctypes.c_void_p), ("pages", ctypes.c_void_p),
     ]
@@ -148,22 +148,32 @@ def quant_row(x_bf16_bits: np.ndarray, bits: int):
     return st, q, s16.value, z16.value
 
 
+# Precision schemes (reading F of dkv_oracle.cpp): (kh, vh) of the high
+# class; the low class has half of each.
+SCHEMES = {0: (8, 4), 1: (8, 2), 2: (4, 8)}
+
+
+def page_bytes(P: int, scheme: int = 0) -> int:
+    kh, vh = SCHEMES[scheme]
+    return (16 * (kh + vh) + 24) * int(P)
+
+
 class Pool:
     """Host-side pool state for the oracle (numpy arrays)."""
 
-    def __init__(self, F: int, P: int, allocate_pages: bool = True):
-        self.F, self.P = int(F), int(P)
+    def __init__(self, F: int, P: int, allocate_pages: bool = True, scheme: int = 0):
+        self.F, self.P, self.scheme = int(F), int(P), int(scheme)
         self.free_list = np.zeros(F, dtype=np.int32)
         self.cursors = np.zeros(2, dtype=np.uint64)
         self.rev_unit = np.zeros(F, dtype=np.int32)
         self.rev_idx = np.zeros(F, dtype=np.int32)
         self.page_cls = np.zeros(F, dtype=np.uint8)
         # np.zeros is calloc-backed: untouched pages cost no memory.
-        self.pages = np.zeros((F, 216 * P), dtype=np.uint8)
+        self.pages = np.zeros((F, page_bytes(P, scheme)), dtype=np.uint8)
         self.init()
 
     def _c(self):
-        return _Pool(self.F, self.P, _ptr(self.free_list), _ptr(self.cursors), _ptr(self.rev_unit),
+        return _Pool(self.F, self.P, self.scheme, _ptr(self.free_list), _ptr(self.cursors), _ptr(self.rev_unit),
                      _ptr(self.rev_idx), _ptr(self.page_cls), _ptr(self.pages))
 
     def init(self):

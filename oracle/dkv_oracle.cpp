@@ -35,7 +35,18 @@
  *      bytes either way).  K codes at [0, 128P), V codes at [128P, 192P),
  *      fp16 {k_scale, k_zero, v_scale, v_zero} per slot at 192P + 8*slot,
  *      int32 token position per slot at 208P + 4*slot.  Unused slots: zero
- *      codes and metadata, position -1.  Nibbles and crumbs pack low-first.
+ *      codes and metadata, position -1.  Sub-byte codes pack low-first.
+ *  F   Precision schemes (the review's free-parameter list: the scheme
+ *      K8V4-K4V2 was chosen by comparing K8V4, K4V8, K8V2, K4V2, K2V4 and
+ *      K4V1 in its Section 7.2).  A scheme pairs a high class (K at kh bits,
+ *      V at vh bits) with the low class at half of each: K8V4/K4V2 (scheme
+ *      0, the default and the one the method states), K8V2/K4V1 (1) and
+ *      K4V8/K2V4 (2).  A low token then takes exactly half the code bytes of
+ *      a high one, so P1 generalises: a page of 16 (kh + vh) P + 24 P bytes
+ *      holds P high or 2P low tokens; K codes at [0, 16 kh P), V codes at
+ *      [16 kh P, 16 (kh + vh) P), then the metadata and positions.  The
+ *      quantiser (Q1) runs at the class's widths; demotion requantises from
+ *      (kh, vh) to (kh/2, vh/2).
  *  A1  Page demand of a unit (layer, request, KV head):
  *      ceil(n_hi / P) + ceil(n_lo / 2P).  An exclusive prefix sum over units
  *      in layer-major order gives each unit a contiguous run of free-list
@@ -146,18 +157,34 @@ int32_t get_i32(const uint8_t *p) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-/* Byte offsets inside one unified page (reading P1). */
+/* Bit widths of the precision scheme (reading F): the high class stores K
+ * at kh and V at vh bits, the low class at half of each. */
+int scheme_kh(int32_t scheme) { return scheme == 2 ? 4 : 8; }
+int scheme_vh(int32_t scheme) { return scheme == 0 ? 4 : (scheme == 1 ? 2 : 8); }
+bool scheme_ok(int32_t scheme) { return scheme >= 0 && scheme <= 2; }
+
+/* Byte offsets inside one unified page (readings P1 and F): a high slot has
+ * 128 * kh / 8 bytes of K codes and 128 * vh / 8 of V codes, a low slot half
+ * of each, so the code region is 16 (kh + vh) P bytes for P high or 2P low
+ * tokens; then 8 bytes of fp16 metadata and 4 of position per slot. */
 struct PageLayout {
   int64_t P;
-  int64_t bytes() const { return 216 * P; }
-  int64_t k_off(bool high, int64_t slot) const { return slot * (high ? 128 : 64); }
-  int64_t v_off(bool high, int64_t slot) const { return 128 * P + slot * (high ? 64 : 32); }
-  int64_t meta_off(int64_t slot) const { return 192 * P + 8 * slot; }
-  int64_t pos_off(int64_t slot) const { return 208 * P + 4 * slot; }
+  int kh, vh;
+  PageLayout(int64_t P_, int32_t scheme) : P(P_), kh(scheme_kh(scheme)), vh(scheme_vh(scheme)) {}
+  int kbits(bool high) const { return high ? kh : kh / 2; }
+  int vbits(bool high) const { return high ? vh : vh / 2; }
+  int64_t kbytes(bool high) const { return 16 * kbits(high); }
+  int64_t vbytes(bool high) const { return 16 * vbits(high); }
+  int64_t codes() const { return 16 * (kh + vh) * P; }
+  int64_t bytes() const { return codes() + 24 * P; }
+  int64_t k_off(bool high, int64_t slot) const { return slot * kbytes(high); }
+  int64_t v_off(bool high, int64_t slot) const { return 16 * kh * P + slot * vbytes(high); }
+  int64_t meta_off(int64_t slot) const { return codes() + 8 * slot; }
+  int64_t pos_off(int64_t slot) const { return codes() + 16 * P + 4 * slot; }
 };
 
 void clear_page(uint8_t *page, const PageLayout &lay) {
-  std::memset(page, 0, static_cast<size_t>(208 * lay.P));
+  std::memset(page, 0, static_cast<size_t>(lay.codes() + 16 * lay.P));
   for (int64_t s = 0; s < 2 * lay.P; ++s) put_i32(page + lay.pos_off(s), -1);
 }
 
@@ -316,7 +343,8 @@ int32_t oracle_compact(const oracle_batch *b, float alpha_h, float alpha_l, orac
   if (b->D != 128 || b->L < 1 || b->R < 1 || b->Hkv < 1 || b->Hq < b->Hkv || b->Hq % b->Hkv != 0)
     return ORACLE_E_INVAL;
   if (!(alpha_l >= 0.0f) || !(alpha_h >= alpha_l) || !std::isfinite(alpha_h)) return ORACLE_E_INVAL;
-  if (pool->P < 2 || pool->P % 2 != 0 || pool->F < 1 || t->pmax < 1) return ORACLE_E_INVAL;
+  if (pool->P < 2 || pool->P % 2 != 0 || pool->F < 1 || t->pmax < 1 || !scheme_ok(pool->scheme))
+    return ORACLE_E_INVAL;
 
   const int64_t L = b->L, R = b->R, Hq = b->Hq, Hkv = b->Hkv, T = b->T, P = pool->P;
   const int64_t G = Hq / Hkv;
@@ -396,7 +424,7 @@ int32_t oracle_compact(const oracle_batch *b, float alpha_h, float alpha_l, orac
       }
 
   /* tables, page classes and page contents */
-  const PageLayout lay{P};
+  const PageLayout lay(P, pool->scheme);
   const int64_t F = pool->F;
   for (int64_t l = 0; l < L; ++l)
     for (int64_t r = 0; r < R; ++r)
@@ -444,11 +472,11 @@ int32_t oracle_compact(const oracle_batch *b, float alpha_h, float alpha_l, orac
           }
           uint8_t qk[128], qv[128];
           uint16_t ks, kz, vs, vz;
-          oracle_quant_row(b->k + row * 128, high ? 8 : 4, qk, &ks, &kz);
-          oracle_quant_row(b->v + row * 128, high ? 4 : 2, qv, &vs, &vz);
+          oracle_quant_row(b->k + row * 128, lay.kbits(high), qk, &ks, &kz);
+          oracle_quant_row(b->v + row * 128, lay.vbits(high), qv, &vs, &vz);
           uint8_t *page = pool->pages + static_cast<int64_t>(fwd[k_idx]) * lay.bytes();
-          pack_codes(qk, high ? 8 : 4, page + lay.k_off(high, slot));
-          pack_codes(qv, high ? 4 : 2, page + lay.v_off(high, slot));
+          pack_codes(qk, lay.kbits(high), page + lay.k_off(high, slot));
+          pack_codes(qv, lay.vbits(high), page + lay.v_off(high, slot));
           uint8_t *meta = page + lay.meta_off(slot);
           put_u16(meta + 0, ks);
           put_u16(meta + 2, kz);
@@ -476,7 +504,7 @@ uint8_t *slot_k(uint8_t *pool_pages, const PageLayout &lay, const ListRef &lr, i
 }
 
 void copy_slot(uint8_t *pp, const PageLayout &lay, const ListRef &lr, int64_t from, int64_t to) {
-  const int64_t kb = lr.high ? 128 : 64, vb = lr.high ? 64 : 32;
+  const int64_t kb = lay.kbytes(lr.high), vb = lay.vbytes(lr.high);
   uint8_t *fp = pp + static_cast<int64_t>(lr.pages[from / lr.cap]) * lay.bytes();
   uint8_t *tp = pp + static_cast<int64_t>(lr.pages[to / lr.cap]) * lay.bytes();
   const int64_t fs = from % lr.cap, ts = to % lr.cap;
@@ -487,7 +515,7 @@ void copy_slot(uint8_t *pp, const PageLayout &lay, const ListRef &lr, int64_t fr
 }
 
 void clear_slot(uint8_t *pp, const PageLayout &lay, const ListRef &lr, int64_t s) {
-  const int64_t kb = lr.high ? 128 : 64, vb = lr.high ? 64 : 32;
+  const int64_t kb = lay.kbytes(lr.high), vb = lay.vbytes(lr.high);
   uint8_t *pg = pp + static_cast<int64_t>(lr.pages[s / lr.cap]) * lay.bytes();
   const int64_t ss = s % lr.cap;
   std::memset(pg + lay.k_off(lr.high, ss), 0, static_cast<size_t>(kb));
@@ -500,8 +528,8 @@ void write_slot(uint8_t *pp, const PageLayout &lay, const ListRef &lr, int64_t s
                 uint16_t ks, uint16_t kz, uint16_t vs, uint16_t vz, int32_t pos) {
   uint8_t *pg = pp + static_cast<int64_t>(lr.pages[s / lr.cap]) * lay.bytes();
   const int64_t ss = s % lr.cap;
-  pack_codes(qk, lr.high ? 8 : 4, pg + lay.k_off(lr.high, ss));
-  pack_codes(qv, lr.high ? 4 : 2, pg + lay.v_off(lr.high, ss));
+  pack_codes(qk, lay.kbits(lr.high), pg + lay.k_off(lr.high, ss));
+  pack_codes(qv, lay.vbits(lr.high), pg + lay.v_off(lr.high, ss));
   put_u16(pg + lay.meta_off(ss) + 0, ks);
   put_u16(pg + lay.meta_off(ss) + 2, kz);
   put_u16(pg + lay.meta_off(ss) + 4, vs);
@@ -527,7 +555,8 @@ extern "C" int32_t oracle_decode_step(const oracle_decode_batch *b, float alpha_
   if (b->D != 128 || b->L < 1 || b->R < 1 || b->Hkv < 1 || b->Hq < b->Hkv || b->Hq % b->Hkv != 0 || b->cap < 1)
     return ORACLE_E_INVAL;
   if (!(alpha_l >= 0.0f) || !(alpha_h >= alpha_l) || !std::isfinite(alpha_h)) return ORACLE_E_INVAL;
-  if (pool->P < 2 || pool->P % 2 != 0 || pool->F < 1 || t->pmax < 1) return ORACLE_E_INVAL;
+  if (pool->P < 2 || pool->P % 2 != 0 || pool->F < 1 || t->pmax < 1 || !scheme_ok(pool->scheme))
+    return ORACLE_E_INVAL;
   if (b->window < 0 || (b->mode != 0 && b->mode != 1)) return ORACLE_E_INVAL;
   const int64_t L = b->L, R = b->R, Hq = b->Hq, Hkv = b->Hkv, cap = b->cap, P = pool->P, F = pool->F;
   const int64_t G = Hq / Hkv, U = L * R * Hkv, pmax = t->pmax;
@@ -535,7 +564,7 @@ extern "C" int32_t oracle_decode_step(const oracle_decode_batch *b, float alpha_
     const int64_t c = b->ctx_lens[r], n = b->new_lens[r];
     if (c < 0 || n < 0 || n > 1 || c + n > cap || c + n > (pmax - 1) * P) return ORACLE_E_LENS;
   }
-  const PageLayout lay{P};
+  const PageLayout lay(P, pool->scheme);
   auto row_of = [&](int64_t l, int64_t r, int64_t i, int64_t h) { return ((l * R + r) * cap + i) * Hkv + h; };
 
   /* classes after the step (readings S1-S3, D) */
@@ -691,8 +720,8 @@ extern "C" int32_t oracle_decode_step(const oracle_decode_batch *b, float alpha_
           const uint8_t *pg = pool->pages + static_cast<int64_t>(HI.pages[s / P]) * lay.bytes();
           const int64_t ss = s % P;
           uint8_t qk[128], qv[128];
-          unpack_codes(pg + lay.k_off(true, ss), 8, qk);
-          unpack_codes(pg + lay.v_off(true, ss), 4, qv);
+          unpack_codes(pg + lay.k_off(true, ss), lay.kbits(true), qk);
+          unpack_codes(pg + lay.v_off(true, ss), lay.vbits(true), qv);
           const uint8_t *meta = pg + lay.meta_off(ss);
           const float ks = oracle_fp16_to_f32(get_u16(meta + 0)), kz = oracle_fp16_to_f32(get_u16(meta + 2));
           const float vs = oracle_fp16_to_f32(get_u16(meta + 4)), vz = oracle_fp16_to_f32(get_u16(meta + 6));
@@ -703,8 +732,8 @@ extern "C" int32_t oracle_decode_step(const oracle_decode_batch *b, float alpha_
           }
           uint8_t nk[128], nv[128];
           uint16_t s1, z1, s2, z2;
-          quant_row_f32(xk, 4, nk, &s1, &z1);
-          quant_row_f32(xv, 2, nv, &s2, &z2);
+          quant_row_f32(xk, lay.kbits(false), nk, &s1, &z1);
+          quant_row_f32(xv, lay.vbits(false), nv, &s2, &z2);
           write_slot(pool->pages, lay, LO, pl.keep_lo + static_cast<int64_t>(k), nk, nv, s1, z1, s2, z2,
                      get_i32(pg + lay.pos_off(ss)));
         }
@@ -714,8 +743,8 @@ extern "C" int32_t oracle_decode_step(const oracle_decode_batch *b, float alpha_
           const bool high = pl.new_cls == 2;
           uint8_t qk[128], qv[128];
           uint16_t ks, kz, vs, vz;
-          oracle_quant_row(b->k_new + nr * 128, high ? 8 : 4, qk, &ks, &kz);
-          oracle_quant_row(b->v_new + nr * 128, high ? 4 : 2, qv, &vs, &vz);
+          oracle_quant_row(b->k_new + nr * 128, lay.kbits(high), qk, &ks, &kz);
+          oracle_quant_row(b->v_new + nr * 128, lay.vbits(high), qv, &vs, &vz);
           const int64_t slot = high ? pl.keep_hi : pl.keep_lo + pl.dem;
           write_slot(pool->pages, lay, high ? HI : LO, slot, qk, qv, ks, kz, vs, vz,
                      static_cast<int32_t>(b->ctx_lens[r]));
@@ -763,9 +792,9 @@ int32_t oracle_decode_attention(const oracle_attn_batch *b, const oracle_pool *p
                                 const oracle_tables *t) {
   if (!b || !pool || !t || b->R < 0 || b->Hkv <= 0 || b->Hq <= 0 || b->Hq % b->Hkv != 0 ||
       b->layer0 < 0 || b->n_layers < 0 || b->layer0 + b->n_layers > b->L || !b->q || !b->out ||
-      !b->ctx_lens || (b->k_new && (!b->v_new || !b->new_lens)))
+      !b->ctx_lens || (b->k_new && (!b->v_new || !b->new_lens)) || !scheme_ok(pool->scheme))
     return ORACLE_E_INVAL;
-  const PageLayout lay{pool->P};
+  const PageLayout lay(pool->P, pool->scheme);
   const int64_t P = pool->P, R = b->R, Hq = b->Hq, Hkv = b->Hkv, G = Hq / Hkv, cap = b->cap;
   if (b->p_out)
     std::fill(b->p_out, b->p_out + static_cast<int64_t>(b->n_layers) * R * cap * Hq, 0.0);
@@ -785,8 +814,8 @@ int32_t oracle_decode_attention(const oracle_attn_batch *b, const oracle_pool *p
             const uint8_t *pg = pool->pages + static_cast<int64_t>(fwd[first + i / per]) * lay.bytes();
             const int64_t sl = i % per;
             uint8_t qk[128], qv[128];
-            unpack_codes(pg + lay.k_off(high, sl), high ? 8 : 4, qk);
-            unpack_codes(pg + lay.v_off(high, sl), high ? 4 : 2, qv);
+            unpack_codes(pg + lay.k_off(high, sl), lay.kbits(high), qk);
+            unpack_codes(pg + lay.v_off(high, sl), lay.vbits(high), qv);
             const uint8_t *meta = pg + lay.meta_off(sl);
             const float k_s = oracle_fp16_to_f32(get_u16(meta + 0)), k_z = oracle_fp16_to_f32(get_u16(meta + 2));
             const float v_s = oracle_fp16_to_f32(get_u16(meta + 4)), v_z = oracle_fp16_to_f32(get_u16(meta + 6));
@@ -884,7 +913,7 @@ int32_t oracle_prefill_attention(const oracle_prefill_batch *b) {
 
 void oracle_dequant_page(const oracle_pool *pool, int32_t page_id, float *k_out, float *v_out,
                          int32_t *pos_out) {
-  const PageLayout lay{pool->P};
+  const PageLayout lay(pool->P, pool->scheme);
   const int64_t P = pool->P;
   const uint8_t cls = pool->page_cls[page_id];
   const uint8_t *page = pool->pages + static_cast<int64_t>(page_id) * lay.bytes();
@@ -899,8 +928,8 @@ void oracle_dequant_page(const oracle_pool *pool, int32_t page_id, float *k_out,
     }
     const bool high = (cls == 2);
     uint8_t qk[128], qv[128];
-    unpack_codes(page + lay.k_off(high, s), high ? 8 : 4, qk);
-    unpack_codes(page + lay.v_off(high, s), high ? 4 : 2, qv);
+    unpack_codes(page + lay.k_off(high, s), lay.kbits(high), qk);
+    unpack_codes(page + lay.v_off(high, s), lay.vbits(high), qv);
     const uint8_t *meta = page + lay.meta_off(s);
     const float ks = oracle_fp16_to_f32(get_u16(meta + 0));
     const float kz = oracle_fp16_to_f32(get_u16(meta + 2));

@@ -58,13 +58,14 @@ typedef struct oracle_batch {
 
 typedef struct oracle_pool {
   int64_t F;               /* pages in the pool */
-  int32_t P;               /* K8V4 tokens per page; a K4V2 page holds 2P */
+  int32_t P;               /* high-class tokens per page; a low-class page holds 2P */
+  int32_t scheme;          /* 0 K8V4/K4V2, 1 K8V2/K4V1, 2 K4V8/K2V4 (reading F) */
   int32_t *free_list;      /* [F] ring of free page ids */
   uint64_t *cursors;       /* [2] {head, tail}, monotone */
   int32_t *rev_unit;       /* [F] owning unit or -1 */
   int32_t *rev_idx;        /* [F] index in the owner's forward row or -1 */
   uint8_t *page_cls;       /* [F] 0 free, 1 K4V2 page, 2 K8V4 page */
-  uint8_t *pages;          /* [F][216*P] */
+  uint8_t *pages;          /* [F][page bytes]: 216*P for schemes 0 and 2, 184*P for scheme 1 */
 } oracle_pool;
 
 typedef struct oracle_tables {
@@ -79,7 +80,8 @@ uint16_t oracle_fp16_rn(float x);
 float oracle_fp16_to_f32(uint16_t h);
 void oracle_fp16_rn_array(const float *x, uint16_t *out, int64_t n);
 
-/* Per-token asymmetric quantizer of one row of 128 bf16 values to b bits.
+/* Per-token asymmetric quantizer of one row of 128 bf16 values to b bits
+ * (b = 1, 2, 4 or 8).
  * Writes q[128] (unpacked codes), *s16 and *z16 (fp16 bits).  Returns
  * ORACLE_OK or ORACLE_E_RANGE. */
 int32_t oracle_quant_row(const uint16_t *x, int32_t bits, uint8_t *q,

@@ -30,7 +30,7 @@ class HostDecode:
         self.window, self.mode = window, mode
         self.pmax = decode_pmax(cap, w.P)
         inp = W.make_inputs(w, seed) if inp is None else inp
-        self.pool = oracle.Pool(F or w.pool_pages, w.P)
+        self.pool = oracle.Pool(F or w.pool_pages, w.P, scheme=w.scheme)
         tab = oracle.Tables(w.U, self.pmax, w.rows)
         st = oracle.compact(W.to_numpy(inp), w.alpha_h, w.alpha_l, self.pool, tab)
         assert st == oracle.OK, st

@@ -8,25 +8,26 @@ import numpy as np
 
 from differentiated_kv_cache_dkv_gb300 import workloads as W
 from oracle.host_decode import HostDecode, decode_pmax  # noqa: F401  (re-exported for the tests)
-from tests.oracle_helpers import unpack
+from tests.oracle_helpers import Layout, unpack
 
 
-def list_slots(pages: np.ndarray, fwd_row: np.ndarray, hdr, P: int):
-    """Raw bytes of a unit's two lists: for list 0 (K8V4) and 1 (K4V2), a
-    list of (K bytes, V bytes, metadata bytes, position) per slot, over every
-    slot of the list's pages (used slots first)."""
+def list_slots(pages: np.ndarray, fwd_row: np.ndarray, hdr, P: int, scheme: int = 0):
+    """Raw bytes of a unit's two lists: for list 0 (high class) and 1 (low
+    class), a list of (K bytes, V bytes, metadata bytes, position) per slot,
+    over every slot of the list's pages (used slots first)."""
+    lay = Layout(P, scheme)
     n_hi, n_lo, p_hi, p_lo = (int(x) for x in hdr)
     out = []
     for high, ids, per in ((True, fwd_row[:p_hi], P), (False, fwd_row[p_hi:p_hi + p_lo], 2 * P)):
-        kb, vb = (128, 64) if high else (64, 32)
+        kb, vb = 16 * lay.kbits(high), 16 * lay.vbits(high)
         slots = []
         for pid in ids:
             pg = pages[int(pid)]
             for s in range(per):
-                k = pg[s * kb:(s + 1) * kb]
-                v = pg[128 * P + s * vb:128 * P + (s + 1) * vb]
-                meta = pg[192 * P + 8 * s:192 * P + 8 * s + 8]
-                pos = int(pg[208 * P + 4 * s:208 * P + 4 * s + 4].view(np.int32)[0])
+                k = pg[lay.k_off(high, s):lay.k_off(high, s) + kb]
+                v = pg[lay.v_off(high, s):lay.v_off(high, s) + vb]
+                meta = pg[lay.meta + 8 * s:lay.meta + 8 * s + 8]
+                pos = int(pg[lay.pos + 4 * s:lay.pos + 4 * s + 4].view(np.int32)[0])
                 slots.append((bytes(k), bytes(v), bytes(meta), pos))
         out.append(slots)
     return out
@@ -44,6 +45,7 @@ def check_state(w: W.Workload, cap: int, pool, fwd: np.ndarray, unit_hdr: np.nda
     - the free ring [head, tail) and the owned pages partition the pool.
     Returns {(unit, position): (list, slot bytes)} for the checked layers."""
     P, F = pool.P, pool.F
+    lay = Layout(P, getattr(pool, "scheme", 0))
     Ul = w.R * w.Hkv
     layers = range(w.L) if layers is None else layers
     owned = []
@@ -65,10 +67,10 @@ def check_state(w: W.Workload, cap: int, pool, fwd: np.ndarray, unit_hdr: np.nda
                     assert pool.page_cls[pid] == (2 if k < p_hi else 1), (u, k)
                     if k < p_hi:
                         pg = pool.pages[pid]
-                        assert not pg[192 * P + 8 * P:208 * P].any()
-                        assert np.all(pg[208 * P + 4 * P:216 * P].view(np.int32) == -1)
+                        assert not pg[lay.meta + 8 * P:lay.pos].any()
+                        assert np.all(pg[lay.pos + 4 * P:lay.bytes].view(np.int32) == -1)
                 owned.extend(int(x) for x in ids)
-                lists = list_slots(pool.pages, row, unit_hdr[u], P)
+                lists = list_slots(pool.pages, row, unit_hdr[u], P, lay.scheme)
                 for li, (n, cls) in enumerate(((n_hi, 2), (n_lo, 1))):
                     slots = lists[li]
                     got = [s[3] for s in slots[:n]]
@@ -88,9 +90,10 @@ def check_state(w: W.Workload, cap: int, pool, fwd: np.ndarray, unit_hdr: np.nda
     return where
 
 
-def slot_codes(slot_bytes, high: bool):
+def slot_codes(slot_bytes, high: bool, scheme: int = 0):
     """Unpacked (K codes, V codes, fp16 metadata) of a slot's raw bytes."""
     k, v, meta = slot_bytes
-    kb, vb = (8, 4) if high else (4, 2)
+    lay = Layout(2, scheme)
+    kb, vb = lay.kbits(high), lay.vbits(high)
     return (unpack(np.frombuffer(k, np.uint8), kb), unpack(np.frombuffer(v, np.uint8), vb),
             np.frombuffer(meta, np.uint16))
