@@ -47,6 +47,8 @@ def _args():
                     help="decode: recent window W (tokens kept at K8V4; 0 = none)")
     ap.add_argument("--decode-mode", type=int, default=0, choices=[0, 1],
                     help="decode: 0 re-scores every older token, 1 only the one leaving the window")
+    ap.add_argument("--scheme", type=int, default=0, choices=[0, 1, 2],
+                    help="precision scheme of the pool: 0 K8V4/K4V2, 1 K8V2/K4V1, 2 K4V8/K2V4 (prefill workloads)")
     ap.add_argument("--op", default="step", choices=["step", "attention", "prefill-attention"],
                     help="decode: the generation step or the attention over the pages; prefill workloads: "
                          "the compaction step or the prefill attention that produces its significance inputs")
@@ -60,6 +62,8 @@ def workload(a):
     from differentiated_kv_cache_dkv_gb300 import workloads as W
 
     w = W.get(a.workload)
+    if getattr(a, "scheme", 0):
+        w = dataclasses.replace(w, scheme=a.scheme)
     if a.layers:
         w = dataclasses.replace(w, L=min(a.layers, w.L))
     if a.requests:
@@ -75,9 +79,14 @@ def workload_name(a) -> str:
         name += " prefill attention"
     if getattr(a, "window", 0) or getattr(a, "decode_mode", 0):
         name += f" (window {a.window}, {'single candidate' if a.decode_mode else 'every token re-scored'})"
+    if getattr(a, "scheme", 0):
+        name += " " + SCHEME_NAMES[a.scheme]
     if a.layers or a.requests:
         name += f" (reduced: {a.layers or 'all'} layers, {a.requests or 'all'} requests)"
     return name
+
+
+SCHEME_NAMES = {0: "K8V4/K4V2", 1: "K8V2/K4V1", 2: "K4V8/K2V4"}
 
 
 # DRAM traffic of one full k_pack launch on the Llama-shaped workload, from one
@@ -112,6 +121,11 @@ def _reclass_traffic(workload: str, alg_bytes: float):
     if workload != RECLASS_TRAFFIC["workload"] or _source_sha("decode.cu") != RECLASS_TRAFFIC["source_sha1"]:
         return None
     return RECLASS_TRAFFIC["per_byte"] * alg_bytes
+
+
+def scheme_bits(scheme: int) -> int:
+    """K + V bits of the high class of a scheme (the low class has half)."""
+    return {0: 12, 1: 10, 2: 12}[scheme]
 
 
 def _peaks():
@@ -272,7 +286,8 @@ def run_native(a):
     w = workload(a)
     dev = torch.device("cuda", local)
     inp = W.make_inputs(w, seed=W.SEED_BASE + 1000 * rank, device=dev)
-    comp = libdkv.Compactor(w.L, w.R, w.Hq, w.Hkv, w.T, max(w.lens), w.P, w.pool_pages, device=dev)
+    comp = libdkv.Compactor(w.L, w.R, w.Hq, w.Hkv, w.T, max(w.lens), w.P, w.pool_pages, device=dev,
+                            scheme=w.scheme)
     stream = torch.cuda.current_stream()
 
     def step(profiler=None):
@@ -318,15 +333,27 @@ def run_native(a):
     ms_max = max_over_ranks(ms, dev, world)
     value = whole_job_rate(rows * a.steps, world, ms_max)
 
-    # roofline of the dominant kernel (k_pack): algorithmic bytes per launch
+    # roofline of the dominant kernel (k_pack): algorithmic bytes per launch,
+    # the per-row figure of the measurement spec (every K / V row of the batch
+    # read, as the kernel's tiles do) plus the pages it writes, the free-list
+    # ids, tile descriptors and unit headers it reads
     peak, peak_kind = _peaks()
     U = w.U
+    pb = libdkv.dkv_page_bytes(w.scheme, w.P)
     ntiles = w.L * w.Hkv * sum(-(-n // 128) for n in w.lens)
-    pack_bytes = n_surv * 512 + pages * (216 * w.P + 4) + ntiles * 40 + U * 16
+    pack_bytes = rows * 512 + pages * (pb + 4) + ntiles * 40 + U * 16
     pack_ms = kernel_ms["k_pack"]
     pack_gbs = pack_bytes / (pack_ms / 1000.0) / 1e9
+    # the whole step by the spec's count: read every K / V row, the sums and
+    # counts; write the pages, class bytes, unit headers and the fwd + rev
+    # entries of the allocated pages
+    spec_read = rows * 512 + w.L * w.T * w.Hq * 4 + w.T * 4
+    spec_write = pages * pb + rows + U * 16 + pages * (4 + 8)
+    spec_gbs = (spec_read + spec_write) / (ms_max / a.steps / 1000.0) / 1e9
+    # and with what the step touches besides: only surviving rows' K / V
+    # count as read, but the pool reset and the full forward rows do count
     step_read = n_surv * 512 + w.L * w.T * w.Hq * 4 + w.T * 4
-    step_write = rows + pages * (216 * w.P + 13) + U * (w.pmax * 4 + 16) + w.pool_pages * 13
+    step_write = rows + pages * (pb + 13) + U * (w.pmax * 4 + 16) + w.pool_pages * 13
     step_gbs = (step_read + step_write) / (ms_max / a.steps / 1000.0) / 1e9
 
     # end to end through the public API with host buffers
@@ -373,18 +400,23 @@ def run_native(a):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": workload_name(a), "layers": w.L, "requests": w.R, "tokens_per_request": w.lens[0]
                        if len(set(w.lens)) == 1 else "ragged", "Hq": w.Hq, "Hkv": w.Hkv, "page_tokens": w.P,
-                       "alpha_h": w.alpha_h, "alpha_l": w.alpha_l, "rows_per_step": rows,
+                       "alpha_h": w.alpha_h, "alpha_l": w.alpha_l, "scheme": SCHEME_NAMES[w.scheme],
+                       "rows_per_step": rows,
                        "l2": "inputs (%.1f GB) larger than L2" % ((rows * 512 + w.L * w.T * w.Hq * 4) / 1e9),
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "kernel": "k_pack", "achieved": pack_gbs, "peak": peak, "unit": "GB/s",
                          "frac": pack_gbs / peak, "peak_kind": peak_kind, "traffic": _pack_traffic(workload_name(a)),
                          "algorithmic_bytes": pack_bytes, "ms": pack_ms},
-            "step_hbm": {"achieved": step_gbs, "frac": step_gbs / peak, "bytes": step_read + step_write},
+            "step_hbm_spec": {"achieved": spec_gbs, "frac": spec_gbs / peak, "bytes": spec_read + spec_write,
+                              "counted": "all K/V rows, sums, counts read; pages, classes, headers, fwd+rev written"},
+            "step_hbm": {"achieved": step_gbs, "frac": step_gbs / peak, "bytes": step_read + step_write,
+                         "counted": "surviving K/V rows, sums, counts read; pool reset, pages, classes, full "
+                                    "forward rows written"},
             "kernels_ms": kernel_ms,
             "request_tokens_per_s": value / (w.L * w.Hkv),
             "classes": {"k8v4": n_hi / rows, "k4v2": n_lo / rows, "pruned": n_pruned / rows},
             "pages_per_step": pages,
-            "payload_fraction": (12 * n_hi + 6 * n_lo) / (32 * rows),
+            "payload_fraction": ((scheme_bits(w.scheme)) * (n_hi + 0.5 * n_lo)) / (32 * rows),
             "gpu_launches": a.steps * (1 + libdkv.DKV_PROFILE_KERNELS),
             "clocks": clk,
             "e2e": e2e,

@@ -214,8 +214,8 @@ __device__ __forceinline__ void fill_words(uint8_t *p, int64_t nwords, uint32_t 
 
 // Commit of a successful call: forward and reverse tables, page classes,
 // unit headers, the head cursor; and the unused slots of the new pages (zero
-// codes and metadata, position -1): slots P..2P-1 of every K8V4 page and the
-// tail of each unit's last K8V4 and K4V2 page.  A failed call only records
+// codes and metadata, position -1): slots P..2P-1 of every high page and the
+// tail of each unit's last high and low page.  A failed call only records
 // its error in the pool's status word.
 __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
   const int32_t err = a.ws->err;
@@ -226,7 +226,8 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t head_mod = a.ws->head_mod;
   const int64_t P = a.P;
-  const int64_t page_bytes = 216 * P;
+  const PageGeom &g = a.pg;
+  const int64_t page_bytes = g.bytes;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kCommitThreads / 32);
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * (kCommitThreads / 32) + (threadIdx.x >> 5); u < a.U;
        u += nwarps) {
@@ -245,10 +246,10 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
         a.rev_unit[id] = static_cast<int32_t>(a.unit_base + u);
         a.rev_idx[id] = k;
         a.page_cls[id] = k < inf.p_hi ? DKV_CLASS_K8V4 : DKV_CLASS_K4V2;
-        if (k < inf.p_hi) {  // a K8V4 page has no slots P..2P-1
+        if (k < inf.p_hi) {  // a high page has no slots P..2P-1
           uint8_t *pg = a.pages + id * page_bytes;
-          uint4 *meta = reinterpret_cast<uint4 *>(pg + 200 * P);
-          int2 *pos = reinterpret_cast<int2 *>(pg + 212 * P);
+          uint4 *meta = reinterpret_cast<uint4 *>(pg + g.meta + 8 * P);
+          int2 *pos = reinterpret_cast<int2 *>(pg + g.pos + 4 * P);
           for (int64_t i = 0; i < P / 2; ++i) {
             meta[i] = make_uint4(0u, 0u, 0u, 0u);
             pos[i] = make_int2(-1, -1);
@@ -264,20 +265,20 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
       int64_t idx = ring + inf.p_hi - 1;
       if (idx >= a.F) idx -= a.F;
       uint8_t *pg = a.pages + static_cast<int64_t>(a.free_list[idx]) * page_bytes;
-      fill_words(pg + 128 * sh, 32 * (P - sh), 0u, lane);
-      fill_words(pg + 128 * P + 64 * sh, 16 * (P - sh), 0u, lane);
-      fill_words(pg + 192 * P + 8 * sh, 2 * (P - sh), 0u, lane);
-      fill_words(pg + 208 * P + 4 * sh, P - sh, 0xffffffffu, lane);
+      fill_words(pg + 16 * g.kh * sh, 4 * g.kh * (P - sh), 0u, lane);
+      fill_words(pg + g.vbase + 16 * g.vh * sh, 4 * g.vh * (P - sh), 0u, lane);
+      fill_words(pg + g.meta + 8 * sh, 2 * (P - sh), 0u, lane);
+      fill_words(pg + g.pos + 4 * sh, P - sh, 0xffffffffu, lane);
     }
     const int64_t sl = inf.n_lo % (2 * P);
     if (sl != 0) {
       int64_t idx = ring + d - 1;
       if (idx >= a.F) idx -= a.F;
       uint8_t *pg = a.pages + static_cast<int64_t>(a.free_list[idx]) * page_bytes;
-      fill_words(pg + 64 * sl, 16 * (2 * P - sl), 0u, lane);
-      fill_words(pg + 128 * P + 32 * sl, 8 * (2 * P - sl), 0u, lane);
-      fill_words(pg + 192 * P + 8 * sl, 2 * (2 * P - sl), 0u, lane);
-      fill_words(pg + 208 * P + 4 * sl, 2 * P - sl, 0xffffffffu, lane);
+      fill_words(pg + 8 * g.kh * sl, 2 * g.kh * (2 * P - sl), 0u, lane);
+      fill_words(pg + g.vbase + 8 * g.vh * sl, 2 * g.vh * (2 * P - sl), 0u, lane);
+      fill_words(pg + g.meta + 8 * sl, 2 * (2 * P - sl), 0u, lane);
+      fill_words(pg + g.pos + 4 * sl, 2 * P - sl, 0xffffffffu, lane);
     }
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) a.cursors[0] = a.ws->head + static_cast<uint64_t>(a.ws->total);

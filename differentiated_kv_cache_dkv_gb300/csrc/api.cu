@@ -53,6 +53,7 @@ struct Profiler {
 bool valid_pool(const dkv_pool *p) {
   if (!p) return false;
   if (p->F < 1 || p->F > INT32_MAX || p->P < 2 || (p->P & 1) || p->P > (1 << 16)) return false;
+  if (p->scheme < 0 || p->scheme >= dkv::kSchemes) return false;
   if (!p->free_list || !p->cursors || !p->rev_unit || !p->rev_idx || !p->page_cls || !p->pages || !p->status)
     return false;
   if (!aligned(p->pages, 16) || !aligned(p->cursors, 8) || !aligned(p->free_list, 4) || !aligned(p->rev_unit, 4) ||
@@ -95,6 +96,7 @@ bool decode_pointers(const dkv_decode_batch *b) {
 
 dkv::DecodeArgs decode_args(const dkv_decode_batch *b, const dkv_pool *pool, const dkv_tables *t) {
   dkv::DecodeArgs a{};
+  a.pg = dkv::page_geom(pool->scheme, pool->P);
   a.L = b->L; a.R = b->R; a.Hq = b->Hq; a.Hkv = b->Hkv; a.G = b->Hq / b->Hkv;
   a.P = pool->P; a.pmax = t->pmax; a.cap = b->cap;
   a.window = b->window; a.mode = b->mode;
@@ -146,6 +148,12 @@ const char *dkv_status_string(int32_t code) {
   }
 }
 
+int32_t dkv_page_bytes(int32_t scheme, int32_t P, int64_t *bytes) {
+  if (!bytes || scheme < 0 || scheme >= dkv::kSchemes || P < 2 || (P & 1) || P > (1 << 16)) return DKV_E_INVAL;
+  *bytes = dkv::page_geom(scheme, P).bytes;
+  return DKV_OK;
+}
+
 int32_t dkv_workspace_size(const dkv_batch *b, size_t *bytes) {
   if (!bytes || !valid_shape(b)) return DKV_E_INVAL;
   *bytes = dkv::ws_layout(b->L, b->R, b->Hkv, b->T).bytes;
@@ -176,6 +184,7 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
   if (!device_info(&sms, &pack_bps)) return cuda_status(cudaErrorInvalidDevice);
 
   CompactArgs a{};
+  a.pg = dkv::page_geom(pool->scheme, pool->P);
   a.L = b->L; a.R = b->R; a.Hq = b->Hq; a.Hkv = b->Hkv; a.G = b->Hq / b->Hkv;
   a.P = pool->P; a.pmax = t->pmax;
   a.spin_limit = p->spin_limit < 0 ? (1 << 22) : p->spin_limit;
@@ -308,6 +317,7 @@ int32_t dkv_decode_attention(const dkv_attn_batch *b, const dkv_pool *pool, cons
   if (!b || !valid_pool(pool) || !t || !t->fwd || !t->unit_hdr || !aligned(t->unit_hdr, 16) ||
       !aligned(t->fwd, 4) || t->pmax < 2)
     return DKV_E_INVAL;
+  if (pool->scheme != DKV_SCHEME_K8V4_K4V2) return DKV_E_INVAL;  // the attention kernel reads K8V4/K4V2 pages
   if (b->L < 1 || b->R < 0 || b->Hkv < 1 || b->Hq < b->Hkv || b->Hq % b->Hkv != 0 ||
       b->Hq / b->Hkv > dkv::kAttendMaxG || b->cap < 1 || b->layer0 < 0 || b->n_layers < 0 ||
       b->layer0 + static_cast<int64_t>(b->n_layers) > b->L || !std::isfinite(b->scale))

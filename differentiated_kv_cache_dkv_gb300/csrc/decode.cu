@@ -552,67 +552,64 @@ __device__ __forceinline__ bool slot_addr(const DecodeArgs &a, const UnitView &v
   const int32_t per = hi ? a.P : 2 * a.P;
   const int32_t id = list_page(a, v, hi, s / per);
   if (id < 0) return false;
-  const int64_t P = a.P;
+  const PageGeom &g = a.pg;
   const int64_t ss = s % per;
-  uint8_t *pg = a.pages + static_cast<int64_t>(id) * 216 * P;
-  o.k = pg + ss * (hi ? 128 : 64);
-  o.v = pg + 128 * P + ss * (hi ? 64 : 32);
-  o.meta = pg + 192 * P + 8 * ss;
-  o.pos = pg + 208 * P + 4 * ss;
+  uint8_t *pg = a.pages + static_cast<int64_t>(id) * g.bytes;
+  o.k = pg + ss * 16 * (hi ? g.kh : g.kh >> 1);
+  o.v = pg + g.vbase + ss * 16 * (hi ? g.vh : g.vh >> 1);
+  o.meta = pg + g.meta + 8 * ss;
+  o.pos = pg + g.pos + 4 * ss;
   return true;
 }
 
+// 16-byte units of K and V codes in one slot of the high (hi) or low list of
+// scheme S (the bit widths of the high class).
+template <int S>
+__device__ __forceinline__ int k_units(bool hi) { return hi ? scheme_kh(S) : scheme_kh(S) >> 1; }
+template <int S>
+__device__ __forceinline__ int v_units(bool hi) { return hi ? scheme_vh(S) : scheme_vh(S) >> 1; }
+
 // Copy one slot of a list to another slot of the same list (codes, metadata,
-// position); returns the moved token's position.
-__device__ __forceinline__ int32_t copy_slot(const SlotAddr &f, const SlotAddr &t, bool hi) {
+// position); kn, vn: 16-byte units of K and V codes per slot.  Returns the
+// moved token's position.
+__device__ __forceinline__ int32_t copy_slot(const SlotAddr &f, const SlotAddr &t, int kn, int vn) {
   const uint4 *fk = reinterpret_cast<const uint4 *>(f.k);
   const uint4 *fv = reinterpret_cast<const uint4 *>(f.v);
   uint4 *tk = reinterpret_cast<uint4 *>(t.k);
   uint4 *tv = reinterpret_cast<uint4 *>(t.v);
-  if (hi) {
-    uint4 k[8], vv[4];
+  uint4 x[8];  // K, then V (distinct slots: no overlap)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) k[i] = fk[i];
+  for (int i = 0; i < 8; ++i)
+    if (i < kn) x[i] = fk[i];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) vv[i] = fv[i];
-    const uint2 m = *reinterpret_cast<const uint2 *>(f.meta);
-    const int32_t pos = *reinterpret_cast<const int32_t *>(f.pos);
+  for (int i = 0; i < 8; ++i)
+    if (i < kn) tk[i] = x[i];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) tk[i] = k[i];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) tv[i] = vv[i];
-    *reinterpret_cast<uint2 *>(t.meta) = m;
-    *reinterpret_cast<int32_t *>(t.pos) = pos;
-    return pos;
-  }
-  uint4 k[4], vv[2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) k[i] = fk[i];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) vv[i] = fv[i];
+  for (int i = 0; i < 8; ++i)
+    if (i < vn) x[i] = fv[i];
   const uint2 m = *reinterpret_cast<const uint2 *>(f.meta);
   const int32_t pos = *reinterpret_cast<const int32_t *>(f.pos);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) tk[i] = k[i];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) tv[i] = vv[i];
+  for (int i = 0; i < 8; ++i)
+    if (i < vn) tv[i] = x[i];
   *reinterpret_cast<uint2 *>(t.meta) = m;
   *reinterpret_cast<int32_t *>(t.pos) = pos;
   return pos;
 }
 
-__device__ __forceinline__ void clear_slot(const SlotAddr &t, bool hi) {
+__device__ __forceinline__ void clear_slot(const SlotAddr &t, int kn, int vn) {
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   uint4 *tk = reinterpret_cast<uint4 *>(t.k);
   uint4 *tv = reinterpret_cast<uint4 *>(t.v);
-  for (int i = 0; i < (hi ? 8 : 4); ++i) tk[i] = z;
-  for (int i = 0; i < (hi ? 4 : 2); ++i) tv[i] = z;
+  for (int i = 0; i < kn; ++i) tk[i] = z;
+  for (int i = 0; i < vn; ++i) tv[i] = z;
   *reinterpret_cast<uint2 *>(t.meta) = make_uint2(0u, 0u);
   *reinterpret_cast<int32_t *>(t.pos) = -1;
 }
 
 // Hole-fill of one list: survivors in slots >= keep move, ascending, into the
 // removed slots below keep, ascending; the moved tokens' index entries follow.
+template <int S>
 __device__ void hole_fill(const DecodeArgs &a, const UnitView &v, bool hi, const uint32_t *rm, int32_t keep,
                           int32_t n, int32_t *buf, int lane) {
   int32_t hc = 0, mc = keep;
@@ -631,7 +628,7 @@ __device__ void hole_fill(const DecodeArgs &a, const UnitView &v, bool hi, const
     if (lane < nh) {
       SlotAddr f, t;
       if (slot_addr(a, v, hi, mover, f) && slot_addr(a, v, hi, hole, t)) {
-        const int32_t pos = copy_slot(f, t, hi);
+        const int32_t pos = copy_slot(f, t, k_units<S>(hi), v_units<S>(hi));
         if (pos >= 0 && pos < v.ctx) a.slot_of[v.row0 + static_cast<int64_t>(pos) * v.Hkv] = hole;
         else atomicCAS(a.status, 0, DKV_E_INTERNAL);
       }
@@ -642,7 +639,8 @@ __device__ void hole_fill(const DecodeArgs &a, const UnitView &v, bool hi, const
 
 // The per-token quantiser on fp32 values spread over kGroup lanes (kPer
 // channels each): exact min / max (a zero extreme taken as +0), fp16 scale
-// and zero, q = clamp(rint_even(RN(x - z) / s), 0, n).
+// (raised to 2^-24 from 0, lowered to 65504 from infinity) and zero,
+// q = clamp(rint_even(RN(x - z) / s), 0, n).
 //
 // The code of an element is read from y = RN(d * RN(1/s) + 1536.5), d =
 // RN(x - z): y lies on a grid of 2^-13 and bits(y) >> 13 holds floor(t + 0.5)
@@ -671,6 +669,7 @@ __device__ __forceinline__ void quant_vals(const float (&x)[kPer], int nmax, uin
   const float s32 = __fdiv_rn(__fsub_rn(mx, mn), nf);
   uint16_t s16 = __half_as_ushort(__float2half_rn(s32));
   if (mx > mn && s16 == 0) s16 = 1;
+  if (s16 == 0x7c00u) s16 = 0x7bffu;  // 65504: 1-bit codes of a span above 65519 clamp
   const uint16_t z16 = __half_as_ushort(__float2half_rn(mn));
   const float s = __half2float(__ushort_as_half(s16));
   const float z = __half2float(__ushort_as_half(z16));
@@ -701,59 +700,86 @@ __device__ __forceinline__ uint64_t pack_bits(const uint32_t (&q)[kPer], int wid
   return w;
 }
 
+// Code i (of width w bits) of a run of packed codes held in a uint4.
+__device__ __forceinline__ uint32_t code_at(const uint4 &c, int i, int w) {
+  const int o = i * w;
+  const int wi = o >> 5;
+  const uint32_t word = wi == 0 ? c.x : (wi == 1 ? c.y : (wi == 2 ? c.z : c.w));
+  return (word >> (o & 31)) & ((1u << w) - 1u);
+}
+
+// n bytes (4, 8 or 16; 16-byte-aligned runs of them) into a uint4, the rest zero.
+__device__ __forceinline__ uint4 load_bytes(const uint8_t *p, int n) {
+  if (n == 16) return *reinterpret_cast<const uint4 *>(p);
+  if (n == 8) {
+    const uint2 x = *reinterpret_cast<const uint2 *>(p);
+    return make_uint4(x.x, x.y, 0u, 0u);
+  }
+  return make_uint4(*reinterpret_cast<const uint32_t *>(p), 0u, 0u, 0u);
+}
+
+// The low 2 w bytes of v (16 codes of w bits) at p (w = 1, 2 or 4).
+__device__ __forceinline__ void store_codes16(uint8_t *p, uint64_t v, int w) {
+  if (w == 4) *reinterpret_cast<uint2 *>(p) = make_uint2(static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32));
+  else if (w == 2) *reinterpret_cast<uint32_t *>(p) = static_cast<uint32_t>(v);
+  else *reinterpret_cast<uint16_t *>(p) = static_cast<uint16_t>(v);
+}
+
 // Requantise one demoted token, 8 lanes (lane t: channels 16t .. 16t+15):
-// dequantise its K8V4 codes (fma(q, s, z)), quantise 4-bit K and 2-bit V and
-// store them, with the metadata and position, into K4V2 slot ds of page dpg.
-// Every lane of the warp calls it (the reductions shuffle within 8 lanes).
-__device__ __forceinline__ void requant8(const DecodeArgs &a, uint4 kc, uint2 vc, uint2 meta, bool ok, uint8_t *dpg,
+// dequantise its high-class codes (fma(q, s, z)) at the scheme's (kh, vh)
+// widths, quantise them at (kh/2, vh/2) and store them, with the metadata and
+// position, into low-class slot ds of page dpg.  kc, vc: the lane's 2 kh and
+// 2 vh code bytes.  Every lane of the warp calls it (the reductions shuffle
+// within 8 lanes).
+template <int S>
+__device__ __forceinline__ void requant8(const DecodeArgs &a, uint4 kc, uint4 vc, uint2 meta, bool ok, uint8_t *dpg,
                                          int64_t ds, int32_t pos, int t) {
-  const int64_t P = a.P;
+  const PageGeom &g = a.pg;
+  constexpr int KH = scheme_kh(S), VH = scheme_vh(S), kl = KH >> 1, vl = VH >> 1;
   float x[16];
   uint32_t q[16];
   uint16_t ks2, kz2, vs2, vz2;
   {  // K then V, one 16-channel piece at a time (fewer live registers)
     const float ks = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.x & 0xffffu)));
     const float kz = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.x >> 16)));
-    const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = __fmaf_rn(static_cast<float>((kw[i >> 2] >> (8 * (i & 3))) & 255u), ks, kz);
-    quant_vals<16, 8>(x, 15, q, ks2, kz2);
-    if (ok) {
-      const uint64_t pk = pack_bits<16>(q, 4);
-      reinterpret_cast<uint2 *>(dpg + 64 * ds)[t] = make_uint2(static_cast<uint32_t>(pk), static_cast<uint32_t>(pk >> 32));
-    }
+    for (int i = 0; i < 16; ++i) x[i] = __fmaf_rn(static_cast<float>(code_at(kc, i, KH)), ks, kz);
+    quant_vals<16, 8>(x, (1 << kl) - 1, q, ks2, kz2);
+    if (ok) store_codes16(dpg + ds * 16 * kl + 2 * kl * t, pack_bits<16>(q, kl), kl);
   }
   {
     const float vs = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.y & 0xffffu)));
     const float vz = __half2float(__ushort_as_half(static_cast<uint16_t>(meta.y >> 16)));
-    const uint32_t vw[2] = {vc.x, vc.y};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = __fmaf_rn(static_cast<float>((vw[i >> 3] >> (4 * (i & 7))) & 15u), vs, vz);
-    quant_vals<16, 8>(x, 3, q, vs2, vz2);
-    if (ok) reinterpret_cast<uint32_t *>(dpg + 128 * P + 32 * ds)[t] = static_cast<uint32_t>(pack_bits<16>(q, 2));
+    for (int i = 0; i < 16; ++i) x[i] = __fmaf_rn(static_cast<float>(code_at(vc, i, VH)), vs, vz);
+    quant_vals<16, 8>(x, (1 << vl) - 1, q, vs2, vz2);
+    if (ok) store_codes16(dpg + g.vbase + ds * 16 * vl + 2 * vl * t, pack_bits<16>(q, vl), vl);
   }
   if (ok && t == 0) {
-    *reinterpret_cast<uint2 *>(dpg + 192 * P + 8 * ds) =
+    *reinterpret_cast<uint2 *>(dpg + g.meta + 8 * ds) =
         make_uint2(static_cast<uint32_t>(ks2) | (static_cast<uint32_t>(kz2) << 16),
                    static_cast<uint32_t>(vs2) | (static_cast<uint32_t>(vz2) << 16));
-    *reinterpret_cast<int32_t *>(dpg + 208 * P + 4 * ds) = pos;
+    *reinterpret_cast<int32_t *>(dpg + g.pos + 4 * ds) = pos;
   }
 }
 
-// The demoted tokens (K8V4 -> K4V2) go to K4V2 slots keep_lo + k in ascending
-// position order.  Normally each token's K8V4 slot bytes are copied, one lane
-// per token, into a job for k_demote (the copy must happen before the K8V4
-// hole-fill may overwrite the slot; the requantisation runs later, spread over
-// the whole GPU); when the call's job buffer is full, this warp requantises
-// them in place, 8 lanes per token.
+// The demoted tokens (high -> low class) go to low-class slots keep_lo + k in
+// ascending position order.  Normally each token's high slot bytes are
+// copied, one lane per token, into a job for k_demote (the copy must happen
+// before the high list's hole-fill may overwrite the slot; the
+// requantisation runs later, spread over the whole GPU); when the call's job
+// buffer is full, this warp requantises them in place, 8 lanes per token.
+template <int S>
 __device__ void demote(const DecodeArgs &a, const UnitView &v, const uint32_t *dem, int32_t *buf, int lane) {
   int32_t cur = 0, k = 0;
   const int grp = lane >> 3, t = lane & 7;
+  const PageGeom &g = a.pg;
+  constexpr int KH = scheme_kh(S), VH = scheme_vh(S);
   const int64_t P = a.P;
   for (;;) {
     const int nd = next_bits(dem, cur, v.ctx, true, buf, lane);
     if (nd == 0) break;
-    // one lane per demoted token: its K8V4 slot, then the ids of its source
+    // one lane per demoted token: its high slot, then the ids of its source
     // and destination pages (two rounds of loads for up to 32 tokens)
     int32_t my_hs = -1, my_src = -1, my_dst = -1;
     if (lane < nd) my_hs = a.slot_of[v.row0 + static_cast<int64_t>(buf[lane]) * v.Hkv];
@@ -771,21 +797,25 @@ __device__ void demote(const DecodeArgs &a, const UnitView &v, const uint32_t *d
         bool ok = my_hs >= 0 && my_hs < v.p.n_hi && my_src >= 0 && my_dst >= 0;
         if (ok) {
           const int64_t ss = my_hs % P;
-          const uint8_t *spg = a.pages + static_cast<int64_t>(my_src) * 216 * P;
-          const uint4 *kk = reinterpret_cast<const uint4 *>(spg + 128 * ss);
-          const uint4 *vv = reinterpret_cast<const uint4 *>(spg + 128 * P + 64 * ss);
-          uint4 kw[8], vw[4];
+          const uint8_t *spg = a.pages + static_cast<int64_t>(my_src) * g.bytes;
+          const uint4 *kk = reinterpret_cast<const uint4 *>(spg + 16 * KH * ss);
+          const uint4 *vv = reinterpret_cast<const uint4 *>(spg + g.vbase + 16 * VH * ss);
+          uint4 c[8];  // K codes, then V codes
 #pragma unroll
-          for (int i = 0; i < 8; ++i) kw[i] = kk[i];
+          for (int i = 0; i < 8; ++i)
+            if (i < KH) c[i] = kk[i];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) vw[i] = vv[i];
-          const uint2 meta = *reinterpret_cast<const uint2 *>(spg + 192 * P + 8 * ss);
-          const int32_t spos = *reinterpret_cast<const int32_t *>(spg + 208 * P + 4 * ss);
+          for (int i = 0; i < 8; ++i)
+            if (i < KH) jb.c[i] = c[i];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i < VH) c[i] = vv[i];
+          const uint2 meta = *reinterpret_cast<const uint2 *>(spg + g.meta + 8 * ss);
+          const int32_t spos = *reinterpret_cast<const int32_t *>(spg + g.pos + 4 * ss);
           ok = spos == pos;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) jb.k[i] = kw[i];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) jb.v[i] = vw[i];
+          for (int i = 0; i < 8; ++i)
+            if (i < VH) jb.c[KH + i] = c[i];
           jb.meta = meta;
         }
         if (!ok) atomicCAS(a.status, 0, DKV_E_INTERNAL);
@@ -799,8 +829,8 @@ __device__ void demote(const DecodeArgs &a, const UnitView &v, const uint32_t *d
       // the reservation ran past the buffer: its entries inside the buffer
       // are marked empty (k_demote reads every reserved entry below the end)
       if (lane < nd && static_cast<int64_t>(base) + lane < a.njobs) a.jobs[base + lane].dst_page = -1;
-      for (int g = 0; g < nd; g += 4) {
-        const int j = g + grp;
+      for (int gq = 0; gq < nd; gq += 4) {
+        const int j = gq + grp;
         const bool act = j < nd;
         const int32_t hs = __shfl_sync(0xffffffffu, my_hs, j & 31);
         const int32_t sid = __shfl_sync(0xffffffffu, my_src, j & 31);
@@ -808,20 +838,19 @@ __device__ void demote(const DecodeArgs &a, const UnitView &v, const uint32_t *d
         const int32_t pos = act ? buf[j] : 0;
         bool ok = act && hs >= 0 && hs < v.p.n_hi && sid >= 0 && did >= 0;
         const int64_t ss = hs % P, ds = (v.p.keep_lo + k + j) % (2 * P);
-        const uint8_t *spg = a.pages + static_cast<int64_t>(sid) * 216 * P;
-        uint4 kc = make_uint4(0u, 0u, 0u, 0u);
-        uint2 vc = make_uint2(0u, 0u);
+        const uint8_t *spg = a.pages + static_cast<int64_t>(sid) * g.bytes;
+        uint4 kc = make_uint4(0u, 0u, 0u, 0u), vc = kc;
         uint2 meta = make_uint2(0u, 0u);
         int32_t spos = -1;
         if (ok) {
-          kc = reinterpret_cast<const uint4 *>(spg + 128 * ss)[t];
-          vc = reinterpret_cast<const uint2 *>(spg + 128 * P + 64 * ss)[t];
-          meta = *reinterpret_cast<const uint2 *>(spg + 192 * P + 8 * ss);
-          spos = *reinterpret_cast<const int32_t *>(spg + 208 * P + 4 * ss);
+          kc = load_bytes(spg + 16 * KH * ss + 2 * KH * t, 2 * KH);
+          vc = load_bytes(spg + g.vbase + 16 * VH * ss + 2 * VH * t, 2 * VH);
+          meta = *reinterpret_cast<const uint2 *>(spg + g.meta + 8 * ss);
+          spos = *reinterpret_cast<const int32_t *>(spg + g.pos + 4 * ss);
         }
         if (ok && spos != pos) ok = false;
         if (act && !ok && t == 0) atomicCAS(a.status, 0, DKV_E_INTERNAL);
-        requant8(a, kc, vc, meta, ok, a.pages + static_cast<int64_t>(did) * 216 * P, ds, pos, t);
+        requant8<S>(a, kc, vc, meta, ok, a.pages + static_cast<int64_t>(did) * g.bytes, ds, pos, t);
         if (ok && t == 0) a.slot_of[v.row0 + static_cast<int64_t>(pos) * v.Hkv] = v.p.keep_lo + k + j;
       }
     }
@@ -830,12 +859,32 @@ __device__ void demote(const DecodeArgs &a, const UnitView &v, const uint32_t *d
   }
 }
 
+// Four codes of w bits per lane (channels 4 lane .. 4 lane + 3) packed into a
+// slot's code bytes at d: 32, 16 or 8 bits a lane, or, at 1 bit, the nibbles
+// of two lanes joined into one byte.  Every lane of the warp calls it.
+__device__ __forceinline__ void store_lane4(uint8_t *d, const uint32_t (&q)[4], int w, int lane, bool ok) {
+  const uint32_t bits = static_cast<uint32_t>(pack_bits<4>(q, w));
+  if (w == 8) {
+    if (ok) reinterpret_cast<uint32_t *>(d)[lane] = bits;
+  } else if (w == 4) {
+    if (ok) reinterpret_cast<uint16_t *>(d)[lane] = static_cast<uint16_t>(bits);
+  } else if (w == 2) {
+    if (ok) d[lane] = static_cast<uint8_t>(bits);
+  } else {
+    const uint32_t up = __shfl_down_sync(0xffffffffu, bits, 1);
+    if (ok && (lane & 1) == 0) d[lane >> 1] = static_cast<uint8_t>(bits | (up << 4));
+  }
+}
+
 // Quantise and store the new token (bf16 row of 128 channels, 4 per lane).
+template <int S>
 __device__ void append_new(const DecodeArgs &a, const UnitView &v, int lane) {
   const bool hi = v.p.new_cls == DKV_CLASS_K8V4;
   const int32_t slot = hi ? v.p.keep_hi : v.p.keep_lo + v.p.dem;
   SlotAddr d;
-  if (!slot_addr(a, v, hi, slot, d)) return;
+  const bool ok = slot_addr(a, v, hi, slot, d);  // warp-uniform
+  if (!ok) return;
+  const int kw = k_units<S>(hi), vw = v_units<S>(hi);  // widths in bits = 16-byte units per slot
   const uint2 kr = reinterpret_cast<const uint2 *>(a.k_new + v.u * DKV_HEAD_DIM)[lane];
   const uint2 vr = reinterpret_cast<const uint2 *>(a.v_new + v.u * DKV_HEAD_DIM)[lane];
   float xk[4] = {__uint_as_float(kr.x << 16), __uint_as_float(kr.x & 0xffff0000u), __uint_as_float(kr.y << 16),
@@ -844,15 +893,10 @@ __device__ void append_new(const DecodeArgs &a, const UnitView &v, int lane) {
                  __uint_as_float(vr.y & 0xffff0000u)};
   uint32_t qk[4], qv[4];
   uint16_t ks, kz, vs, vz;
-  quant_vals<4, 32>(xk, hi ? 255 : 15, qk, ks, kz);
-  quant_vals<4, 32>(xv, hi ? 15 : 3, qv, vs, vz);
-  if (hi) {
-    reinterpret_cast<uint32_t *>(d.k)[lane] = static_cast<uint32_t>(pack_bits<4>(qk, 8));
-    reinterpret_cast<uint16_t *>(d.v)[lane] = static_cast<uint16_t>(pack_bits<4>(qv, 4));
-  } else {
-    reinterpret_cast<uint16_t *>(d.k)[lane] = static_cast<uint16_t>(pack_bits<4>(qk, 4));
-    d.v[lane] = static_cast<uint8_t>(pack_bits<4>(qv, 2));
-  }
+  quant_vals<4, 32>(xk, (1 << kw) - 1, qk, ks, kz);
+  quant_vals<4, 32>(xv, (1 << vw) - 1, qv, vs, vz);
+  store_lane4(d.k, qk, kw, lane, true);
+  store_lane4(d.v, qv, vw, lane, true);
   if (lane == 0) {
     *reinterpret_cast<uint2 *>(d.meta) = make_uint2(static_cast<uint32_t>(ks) | (static_cast<uint32_t>(kz) << 16),
                                                     static_cast<uint32_t>(vs) | (static_cast<uint32_t>(vz) << 16));
@@ -863,13 +907,13 @@ __device__ void append_new(const DecodeArgs &a, const UnitView &v, int lane) {
 
 // Zero codes and metadata, position -1, over a whole new page.
 __device__ void clear_page(const DecodeArgs &a, int32_t id, int lane) {
-  const int64_t P = a.P;
-  uint4 *pg = reinterpret_cast<uint4 *>(a.pages + static_cast<int64_t>(id) * 216 * P);
-  const int64_t nz = 13 * P, nall = (216 * P) / 16;  // [0, 208P) zero, [208P, 216P) all ones
+  uint4 *pg = reinterpret_cast<uint4 *>(a.pages + static_cast<int64_t>(id) * a.pg.bytes);
+  const int64_t nz = a.pg.pos / 16, nall = a.pg.bytes / 16;  // [0, pos) zero, [pos, bytes) all ones
   for (int64_t i = lane; i < nall; i += 32)
     pg[i] = i < nz ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(~0u, ~0u, ~0u, ~0u);
 }
 
+template <int S>
 __device__ void apply_unit(const DecodeArgs &a, UnitView &v, uint32_t *rh, uint32_t *rl, uint32_t *dem,
                            int32_t *buf, int32_t *stage, int lane) {
   const DecPlan &p = v.p;
@@ -885,23 +929,23 @@ __device__ void apply_unit(const DecodeArgs &a, UnitView &v, uint32_t *rh, uint3
     if (id >= 0) clear_page(a, id, lane);
   }
   __syncwarp();
-  hole_fill(a, v, false, rl, p.keep_lo, p.n_lo, buf, lane);   // K4V2 list
-  demote(a, v, dem, buf, lane);                               // appended after its survivors
+  hole_fill<S>(a, v, false, rl, p.keep_lo, p.n_lo, buf, lane);   // K4V2 list
+  demote<S>(a, v, dem, buf, lane);                               // appended after its survivors
   __syncwarp();
-  hole_fill(a, v, true, rh, p.keep_hi, p.n_hi, buf, lane);    // K8V4 list (demoted slots read)
-  if (p.new_cls != DKV_CLASS_PRUNE) append_new(a, v, lane);
+  hole_fill<S>(a, v, true, rh, p.keep_hi, p.n_hi, buf, lane);    // K8V4 list (demoted slots read)
+  if (p.new_cls != DKV_CLASS_PRUNE) append_new<S>(a, v, lane);
   __syncwarp();
   // vacated slots of the pages the lists keep
   {
     const int32_t end_hi = min(p.n_hi, p.need_hi * a.P);
     for (int32_t s = n2_hi + lane; s < end_hi; s += 32) {
       SlotAddr t;
-      if (slot_addr(a, v, true, s, t)) clear_slot(t, true);
+      if (slot_addr(a, v, true, s, t)) clear_slot(t, k_units<S>(true), v_units<S>(true));
     }
     const int32_t end_lo = min(p.n_lo, p.need_lo * 2 * a.P);
     for (int32_t s = n2_lo + lane; s < end_lo; s += 32) {
       SlotAddr t;
-      if (slot_addr(a, v, false, s, t)) clear_slot(t, false);
+      if (slot_addr(a, v, false, s, t)) clear_slot(t, k_units<S>(false), v_units<S>(false));
     }
   }
   // tables: stage the kept K4V2 page ids, free the surplus, rewrite the row
@@ -1023,6 +1067,7 @@ __device__ __noinline__ void take_list(const DecodeArgs &a, const uint32_t *list
   }
 }
 
+template <int S>
 __global__ void __launch_bounds__(32 * kMaxApplyWarps, 3) k_apply(DecodeArgs a, int32_t hpc, int32_t words) {
   extern __shared__ __align__(16) unsigned char smem[];
   DecPlan *plan_s = reinterpret_cast<DecPlan *>(smem);
@@ -1103,7 +1148,7 @@ __global__ void __launch_bounds__(32 * kMaxApplyWarps, 3) k_apply(DecodeArgs a, 
   v.new_base = static_cast<int64_t>(a.ws->head % static_cast<uint64_t>(a.F)) + v.p.off_d;
   v.xh = max(0, v.p.need_hi - v.p.have_hi);
   uint32_t *b3 = bm + 3 * warp * words;
-  apply_unit(a, v, b3, b3 + words, b3 + 2 * words, buf + 32 * warp, stage + a.pmax * warp, lane);
+  apply_unit<S>(a, v, b3, b3 + words, b3 + 2 * words, buf + 32 * warp, stage + a.pmax * warp, lane);
 }
 
 // ----------------------------------------------------------------- k_demote --
@@ -1112,30 +1157,33 @@ __global__ void __launch_bounds__(32 * kMaxApplyWarps, 3) k_apply(DecodeArgs a, 
 // 8-lane group takes one job (grid-stride).  Runs after k_apply, whose K4V2
 // hole-fill has emptied the destination slots and whose page clears came
 // first; a failed call staged nothing.
+template <int S>
 __global__ void __launch_bounds__(256) k_demote(DecodeArgs a) {
   if (*reinterpret_cast<volatile int32_t *>(&a.ws->err) != 0) return;
   const int64_t n = min(static_cast<int64_t>(a.ws->job_n), a.njobs);
   const int lane = threadIdx.x & 31, grp = lane >> 3, t = lane & 7;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int64_t P = a.P;
+  const PageGeom &g = a.pg;
+  constexpr int KH = scheme_kh(S), VH = scheme_vh(S);
   for (int64_t b = gw * 4; b < n; b += nw * 4) {
     const int64_t j = b + grp;
     const bool act = j < n;
-    uint4 kc = make_uint4(0u, 0u, 0u, 0u);
-    uint2 vc = make_uint2(0u, 0u), meta = make_uint2(0u, 0u);
+    uint4 kc = make_uint4(0u, 0u, 0u, 0u), vc = kc;
+    uint2 meta = make_uint2(0u, 0u);
     int32_t page = -1, slot = 0, pos = 0;
     if (act) {
       const DemJob &jb = a.jobs[j];
-      kc = jb.k[t];
-      vc = reinterpret_cast<const uint2 *>(jb.v)[t];
+      const uint8_t *c = reinterpret_cast<const uint8_t *>(jb.c);
+      kc = load_bytes(c + 2 * KH * t, 2 * KH);
+      vc = load_bytes(c + 16 * KH + 2 * VH * t, 2 * VH);
       meta = jb.meta;
       page = jb.dst_page;
       slot = jb.dst_slot;
       pos = jb.pos;
     }
     const bool ok = act && page >= 0 && page < a.F;
-    requant8(a, kc, vc, meta, ok, a.pages + static_cast<int64_t>(ok ? page : 0) * 216 * P, slot, pos, t);
+    requant8<S>(a, kc, vc, meta, ok, a.pages + static_cast<int64_t>(ok ? page : 0) * g.bytes, slot, pos, t);
   }
 }
 
@@ -1169,8 +1217,8 @@ __global__ void __launch_bounds__(256) k_index(DecodeArgs a) {
           atomicCAS(a.status, 0, DKV_E_INTERNAL);
           continue;
         }
-        const int32_t pos = *reinterpret_cast<const int32_t *>(a.pages + static_cast<int64_t>(id) * 216 * a.P +
-                                                               208 * static_cast<int64_t>(a.P) + 4 * (s % per));
+        const int32_t pos =
+            *reinterpret_cast<const int32_t *>(a.pages + static_cast<int64_t>(id) * a.pg.bytes + a.pg.pos + 4 * (s % per));
         if (pos < 0 || pos >= ctx) {
           atomicCAS(a.status, 0, DKV_E_INTERNAL);
           continue;
@@ -1210,18 +1258,20 @@ cudaError_t launch_dscan(const DecodeArgs &a, int32_t npart, cudaStream_t s) {
 
 cudaError_t launch_apply(const DecodeArgs &a, int32_t hpc, int32_t words, cudaStream_t s) {
   const size_t smem = apply_smem(hpc, words, a.pmax);
+  void (*kern)(DecodeArgs, int32_t, int32_t) = a.pg.vh == 2 ? k_apply<1> : (a.pg.kh == 4 ? k_apply<2> : k_apply<0>);
   if (smem > 48 * 1024) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(k_apply, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
   const dim3 grid((a.Hkv + hpc - 1) / hpc, a.R, a.L);
-  k_apply<<<grid, 32 * hpc, smem, s>>>(a, hpc, words);
+  kern<<<grid, 32 * hpc, smem, s>>>(a, hpc, words);
   return cudaGetLastError();
 }
 
 cudaError_t launch_demote(const DecodeArgs &a, int grid, cudaStream_t s) {
-  k_demote<<<grid, 256, 0, s>>>(a);
+  static_assert(scheme_vh(1) == 2 && scheme_kh(2) == 4, "scheme dispatch");
+  void (*kern)(DecodeArgs) = a.pg.vh == 2 ? k_demote<1> : (a.pg.kh == 4 ? k_demote<2> : k_demote<0>);
+  kern<<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,36 @@
 
 namespace dkv {
 
+// Precision schemes (dkv_pool.scheme): bits of K and V in the high class;
+// the low class has half of each, so a low token takes exactly half a high
+// token's code bytes and a page holds P high or 2P low tokens.
+__host__ __device__ constexpr int scheme_kh(int s) { return s == 2 ? 4 : 8; }
+__host__ __device__ constexpr int scheme_vh(int s) { return s == 0 ? 4 : (s == 1 ? 2 : 8); }
+constexpr int kSchemes = 3;
+
+// Byte geometry of one unified page: K codes [0, vbase), V codes
+// [vbase, meta), fp16 {k_scale, k_zero, v_scale, v_zero} per slot at
+// meta + 8 s, int32 position per slot at pos + 4 s.
+struct PageGeom {
+  int32_t P, kh, vh, pad;
+  int64_t vbase;  // 16 kh P
+  int64_t meta;   // 16 (kh + vh) P
+  int64_t pos;    // meta + 16 P
+  int64_t bytes;  // meta + 24 P
+};
+
+__host__ __device__ inline PageGeom page_geom(int scheme, int32_t P) {
+  PageGeom g{};
+  g.P = P;
+  g.kh = scheme_kh(scheme);
+  g.vh = scheme_vh(scheme);
+  g.vbase = 16 * static_cast<int64_t>(g.kh) * P;
+  g.meta = 16 * static_cast<int64_t>(g.kh + g.vh) * P;
+  g.pos = g.meta + 16 * static_cast<int64_t>(P);
+  g.bytes = g.meta + 24 * static_cast<int64_t>(P);
+  return g;
+}
+
 constexpr int kTileTokens = 128;                 // tokens per tile
 constexpr int kMaskWords = kTileTokens / 32;     // 32-bit words per class mask
 constexpr int kScanUnits = 128;                  // units per scan partition
@@ -102,6 +132,7 @@ inline WsLayout ws_layout(int64_t L, int64_t R, int64_t Hkv, int64_t T) {
 
 // Everything a kernel of dkv_compact needs, passed by value.
 struct CompactArgs {
+  PageGeom pg;                    // page layout of the pool's scheme
   int32_t L, R, Hq, Hkv, G, P, pmax, spin_limit;
   int64_t T, F, U, unit_base;
   int32_t max_len;
@@ -166,10 +197,10 @@ struct __align__(16) DecPlan {
 constexpr int kMarkList = 1024;       // listed changes per (layer, request); more fall back to a scan
 constexpr int64_t kDemoteJobs = 1 << 20;  // staged demotions per call at most; more are done in place
 
-// One staged demotion: the token's K8V4 slot bytes and where its K4V2 copy goes.
+// One staged demotion: the token's high-class slot bytes and where its
+// low-class copy goes.
 struct __align__(16) DemJob {
-  uint4 k[8];          // 8-bit K codes
-  uint4 v[4];          // 4-bit V codes
+  uint4 c[12];         // the high slot's K codes (16 kh bytes), then its V codes (16 vh bytes)
   uint2 meta;          // fp16 k_scale, k_zero, v_scale, v_zero
   int32_t dst_page;    // -1: nothing to write
   int32_t dst_slot;
@@ -210,6 +241,7 @@ inline DecWsLayout dec_ws_layout(int64_t U, int64_t LR, int64_t rows) {
 }
 
 struct DecodeArgs {
+  PageGeom pg;                    // page layout of the pool's scheme
   int32_t L, R, Hq, Hkv, G, P, pmax, cap, spin_limit;
   int32_t window, mode;
   int64_t F, U, unit_base;

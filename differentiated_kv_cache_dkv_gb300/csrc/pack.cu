@@ -33,14 +33,15 @@
 //       the class bitmasks) with page id (from the circular free list), slot
 //       and position, and arrives on it.
 //   consumer warps (16) claim 8-row groups of a stage from a shared counter
-//       (K4V2 rows start at a multiple of 8, so a group is class-uniform),
+//       (low-class rows start at a multiple of 8, so a group is
+//       class-uniform: one pair of K / V widths of the pool's scheme),
 //       one row per 4-lane group: bf16x2 min / max reduced over the group,
 //       one lane each computes the K and the V scale / zero / reciprocal and
 //       stores the slot's metadata and position, then every lane quantises
 //       its 32 K and 32 V channels as four jobs of 16 channels through one
 //       quantiser body (a rolled loop: the consumer code stays small enough
 //       for the instruction cache, which bounded the unrolled form) and
-//       stores their packed codes.  A lane's 16-byte chunks are rotated by its
+//       stores their packed codes at the class's 8, 4, 2 or 1 bits.  A lane's 16-byte chunks are rotated by its
 //       group, so the 8 rows a warp reads at once (256 bytes apart) fall on
 //       all 32 shared-memory banks.  A warp
 //       that finds no group left arrives on the stage's "empty" mbarrier and
@@ -264,13 +265,18 @@ __device__ __forceinline__ uint32_t pack_codes(const Bits16 &q, int first) {
 // Quantise a lane's 32 K and 32 V channels of one row and store their packed
 // codes into the row's slot: four jobs of 16 channels (K chunks l4, l4+4;
 // K chunks l4+8, l4+12; the same for V), one quantiser body for all of them,
-// the operands re-read from the staged tile.
+// the operands re-read from the staged tile.  The class's K and V widths come
+// from the scheme's high widths (kKH, kVH), halved for the low class: 8, 4,
+// 2 or 1 bits (the 1-bit packing is compiled only for a scheme that has it).
+template <int kKH, int kVH>
 __device__ __forceinline__ void store_row(uint8_t *pg, int32_t P, int32_t slot_, bool high, int l4,
                                           const uint4 *kr, const uint4 *vr, float kz, float kq, float ks,
                                           float vz, float vq, float vs) {
+  constexpr bool kOneBit = kKH == 2 || kVH == 2;
   const int64_t slot = slot_;
-  uint8_t *kd = pg + slot * (high ? 128 : 64);
-  uint8_t *vd = pg + 128 * static_cast<int64_t>(P) + slot * (high ? 64 : 32);
+  const int kw = high ? kKH : kKH / 2, vw = high ? kVH : kVH / 2;
+  uint8_t *kd = pg + slot * 16 * kw;
+  uint8_t *vd = pg + static_cast<int64_t>(16 * kKH) * P + slot * 16 * vw;
 #pragma unroll 2
   for (int j = 0; j < 4; ++j) {
     const bool isv = j >= 2;
@@ -279,7 +285,7 @@ __device__ __forceinline__ void store_row(uint8_t *pg, int32_t P, int32_t slot_,
     const uint4 *src = isv ? vr : kr;
     const uint4 a = src[c], b = src[c2];
     const float z = isv ? vz : kz, r = isv ? vq : kq, s = isv ? vs : ks;
-    const int width = high ? (isv ? 4 : 8) : (isv ? 2 : 4);
+    const int width = isv ? vw : kw;
     Bits16 q;
     quant16(a, b, z, r, s, static_cast<float>((1 << width) - 1), q);
     uint8_t *d = isv ? vd : kd;
@@ -289,9 +295,12 @@ __device__ __forceinline__ void store_row(uint8_t *pg, int32_t P, int32_t slot_,
     } else if (width == 4) {
       *reinterpret_cast<uint32_t *>(d + 4 * c) = pack_codes<4, 8>(q, 0);
       *reinterpret_cast<uint32_t *>(d + 4 * c2) = pack_codes<4, 8>(q, 8);
-    } else {
+    } else if (!kOneBit || width == 2) {
       *reinterpret_cast<uint16_t *>(d + 2 * c) = static_cast<uint16_t>(pack_codes<2, 8>(q, 0));
       *reinterpret_cast<uint16_t *>(d + 2 * c2) = static_cast<uint16_t>(pack_codes<2, 8>(q, 8));
+    } else {
+      d[c] = static_cast<uint8_t>(pack_codes<1, 8>(q, 0));
+      d[c2] = static_cast<uint8_t>(pack_codes<1, 8>(q, 8));
     }
   }
 }
@@ -361,6 +370,8 @@ __device__ __forceinline__ void list_rows(const CompactArgs &a, const TileDesc &
   o.nh_t = nh_t;
 }
 
+// kS: the pool's precision scheme, so the class widths are constants.
+template <int kS>
 __global__ void __launch_bounds__(kPackThreads, 1)
     k_pack(CompactArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ unsigned char smem_raw[];
@@ -379,7 +390,10 @@ __global__ void __launch_bounds__(kPackThreads, 1)
   const int32_t TR = a.ws->TR;
   const int32_t ntiles = TR * a.Hkv * a.L;  // < 2^31: rows are validated below 2^31
   const int32_t P = a.P;
-  const int64_t page_bytes = 216 * static_cast<int64_t>(P);
+  constexpr int kh = scheme_kh(kS), vh = scheme_vh(kS);
+  const int64_t page_bytes = static_cast<int64_t>(16 * (kh + vh) + 24) * P;
+  const int64_t meta_off = static_cast<int64_t>(16 * (kh + vh)) * P;
+  const int64_t pos_off = meta_off + 16 * static_cast<int64_t>(P);
 
   if (warp >= kConsumerWarps) {
     int64_t it = 0;
@@ -472,13 +486,16 @@ __global__ void __launch_bounds__(kPackThreads, 1)
       // scalar job: lane 0 of the group for K, lane 1 for V
       const int jt = l4 & 1;
       const uint32_t mine = jt ? vmm : kmm;
-      const float nmax = jt == 0 ? (high ? 255.0f : 15.0f) : (high ? 15.0f : 3.0f);
+      constexpr float kNh = (1 << kh) - 1, kNl = (1 << (kh / 2)) - 1, vNh = (1 << vh) - 1, vNl = (1 << (vh / 2)) - 1;
+      const float nmax = jt == 0 ? (high ? kNh : kNl) : (high ? vNh : vNl);  // top code of the class's width
       // a zero extreme is +0 (min / max leave the sign of a zero open)
       const float mn = __fadd_rn(bf_lo(mine), 0.0f);
       const float mx = __fadd_rn(-bf_hi(mine), 0.0f);
       const float s32 = __fdiv_rn(__fsub_rn(mx, mn), nmax);
       __half hs = __float2half_rn(s32);
       if (mx > mn && __half_as_ushort(hs) == 0) hs = __ushort_as_half(1);  // 2^-24
+      const bool big = __half_as_ushort(hs) == 0x7c00u;  // 1-bit codes of a span above 65519
+      if (big) hs = __ushort_as_half(0x7bff);              // 65504: the top codes clamp
       const __half hz = __float2half_rn(mn);
       const float js = __half2float(hs);
       const float jz = __half2float(hz);
@@ -486,9 +503,9 @@ __global__ void __launch_bounds__(kPackThreads, 1)
       if (js != 0.0f) {
         jr = __frcp_rn(js);
         // Clamping can only be needed when the zero point is not the minimum
-        // itself or the scale lost precision as an fp16 subnormal; then check
-        // the end points exactly.
-        if (jz != mn || js < 6.103515625e-05f) {
+        // itself, the scale lost precision as an fp16 subnormal, or it was
+        // lowered from infinity; then check the end points exactly.
+        if (jz != mn || js < 6.103515625e-05f || big) {
           const float qlo = rintf(__fdiv_rn(__fsub_rn(mn, jz), js));
           const float qhi = rintf(__fdiv_rn(__fsub_rn(mx, jz), js));
           if (!(qlo >= 0.0f && qhi <= nmax)) jr = -1.0f;  // row needs clamping: exact path
@@ -502,15 +519,15 @@ __global__ void __launch_bounds__(kPackThreads, 1)
         if (!(fabsf(mn) <= 65504.0f && fabsf(mx) <= 65504.0f)) set_error(&a.ws->err, DKV_E_RANGE);
         const uint32_t meta = static_cast<uint32_t>(__half_as_ushort(hs)) |
                               (static_cast<uint32_t>(__half_as_ushort(hz)) << 16);
-        *reinterpret_cast<uint32_t *>(pg + 192 * P + 8 * static_cast<int64_t>(en.y) + 4 * jt) = meta;
-        if (jt == 0) *reinterpret_cast<int32_t *>(pg + 208 * P + 4 * static_cast<int64_t>(en.y)) = en.z;
+        *reinterpret_cast<uint32_t *>(pg + meta_off + 8 * static_cast<int64_t>(en.y) + 4 * jt) = meta;
+        if (jt == 0) *reinterpret_cast<int32_t *>(pg + pos_off + 4 * static_cast<int64_t>(en.y)) = en.z;
       }
       const int src = grp << 2;
       const float kz = __shfl_sync(0xffffffffu, jz, src), kq = __shfl_sync(0xffffffffu, jr, src);
       const float ks = __shfl_sync(0xffffffffu, js, src);
       const float vz = __shfl_sync(0xffffffffu, jz, src + 1), vq = __shfl_sync(0xffffffffu, jr, src + 1);
       const float vs = __shfl_sync(0xffffffffu, js, src + 1);
-      if (write) store_row(pg, P, en.y, high, cb, kr, vr, kz, kq, ks, vz, vq, vs);
+      if (write) store_row<kh, vh>(pg, P, en.y, high, cb, kr, vr, kz, kq, ks, vz, vq, vs);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);
@@ -551,9 +568,12 @@ cudaError_t launch_pack(const CompactArgs &a, int grid, cudaStream_t s) {
   e = make_tile_map(&vmap, a.v, tokens, a.Hkv);
   if (e != cudaSuccess) return e;
   const int smem = static_cast<int>(kPackSmemBytes);
-  e = cudaFuncSetAttribute(k_pack, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  void (*kern)(CompactArgs, const CUtensorMap, const CUtensorMap) =
+      a.pg.vh == 2 ? k_pack<1> : (a.pg.kh == 4 ? k_pack<2> : k_pack<0>);
+  static_assert(scheme_vh(1) == 2 && scheme_kh(2) == 4, "scheme dispatch");
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k_pack<<<grid, kPackThreads, smem, s>>>(a, kmap, vmap);
+  kern<<<grid, kPackThreads, smem, s>>>(a, kmap, vmap);
   return cudaGetLastError();
 }
 

@@ -36,8 +36,9 @@ __global__ void __launch_bounds__(kDequantThreads) k_dequant(dkv_pool p, const i
   const int64_t b = blockIdx.x;
   const int32_t id = ids ? ids[b] : one_id;
   const int64_t P = p.P;
+  const PageGeom g = page_geom(p.scheme, p.P);
   const int cls = (id >= 0 && id < p.F) ? p.page_cls[id] : 0;
-  const uint8_t *pg = p.pages + static_cast<int64_t>(id >= 0 && id < p.F ? id : 0) * 216 * P;
+  const uint8_t *pg = p.pages + static_cast<int64_t>(id >= 0 && id < p.F ? id : 0) * g.bytes;
   float *ko = k_out + b * 2 * P * 128;
   float *vo = v_out + b * 2 * P * 128;
   for (int64_t e = threadIdx.x; e < 2 * P * 128; e += blockDim.x) {
@@ -48,18 +49,14 @@ __global__ void __launch_bounds__(kDequantThreads) k_dequant(dkv_pool p, const i
     float kx = 0.0f, vx = 0.0f;
     int32_t pos = -1;
     if (exists) {
-      uint32_t qk, qv;
-      if (high) {
-        qk = pg[s * 128 + d];
-        qv = (pg[128 * P + s * 64 + (d >> 1)] >> (4 * (d & 1))) & 15u;
-      } else {
-        qk = (pg[s * 64 + (d >> 1)] >> (4 * (d & 1))) & 15u;
-        qv = (pg[128 * P + s * 32 + (d >> 2)] >> (2 * (d & 3))) & 3u;
-      }
-      const __half *meta = reinterpret_cast<const __half *>(pg + 192 * P + 8 * s);
+      // channel d of a slot at width w: bits [w (d mod 8/w), ...) of byte d w / 8
+      const int kw = high ? g.kh : g.kh >> 1, vw = high ? g.vh : g.vh >> 1;
+      const uint32_t qk = (pg[s * 16 * kw + (d * kw >> 3)] >> ((d * kw) & 7)) & ((1u << kw) - 1u);
+      const uint32_t qv = (pg[g.vbase + s * 16 * vw + (d * vw >> 3)] >> ((d * vw) & 7)) & ((1u << vw) - 1u);
+      const __half *meta = reinterpret_cast<const __half *>(pg + g.meta + 8 * s);
       kx = __fmaf_rn(static_cast<float>(qk), __half2float(meta[0]), __half2float(meta[1]));
       vx = __fmaf_rn(static_cast<float>(qv), __half2float(meta[2]), __half2float(meta[3]));
-      pos = *reinterpret_cast<const int32_t *>(pg + 208 * P + 4 * s);
+      pos = *reinterpret_cast<const int32_t *>(pg + g.pos + 4 * s);
     }
     ko[e] = kx;
     vo[e] = vx;

@@ -53,7 +53,7 @@ class dkv_params(ctypes.Structure):
 
 class dkv_pool(ctypes.Structure):
     _fields_ = [
-        ("F", ctypes.c_int64), ("P", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("F", ctypes.c_int64), ("P", ctypes.c_int32), ("scheme", ctypes.c_int32),
         ("free_list", ctypes.c_void_p), ("cursors", ctypes.c_void_p), ("rev_unit", ctypes.c_void_p),
         ("rev_idx", ctypes.c_void_p), ("page_cls", ctypes.c_void_p), ("pages", ctypes.c_void_p),
         ("status", ctypes.c_void_p),
@@ -110,6 +110,7 @@ def load():
         "dkv_version": ([], i32),
         "dkv_status_string": ([i32], ctypes.c_char_p),
         "dkv_last_cuda_error": ([], ctypes.c_char_p),
+        "dkv_page_bytes": ([i32, i32, P(ctypes.c_int64)], i32),
         "dkv_workspace_size": ([P(dkv_batch), P(ctypes.c_size_t)], i32),
         "dkv_init_pool": ([P(dkv_pool), vp], i32),
         "dkv_compact": ([P(dkv_batch), P(dkv_params), P(dkv_pool), P(dkv_tables), vp, ctypes.c_size_t, vp], i32),
@@ -139,6 +140,19 @@ def status_string(code: int) -> str:
     return load().dkv_status_string(int(code)).decode()
 
 
+DKV_SCHEME_K8V4_K4V2 = 0
+DKV_SCHEME_K8V2_K4V1 = 1
+DKV_SCHEME_K4V8_K2V4 = 2
+
+
+def dkv_page_bytes(scheme: int, P: int) -> int:
+    n = ctypes.c_int64(0)
+    rc = load().dkv_page_bytes(int(scheme), int(P), ctypes.byref(n))
+    if rc != DKV_OK:
+        raise DkvError(rc, "dkv_page_bytes")
+    return int(n.value)
+
+
 def _stream(stream=None) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -152,19 +166,19 @@ def _p(t) -> int | None:
 class DevicePool:
     """Pool state in device memory (torch tensors owned by this object)."""
 
-    def __init__(self, F: int, P: int, device="cuda"):
-        self.F, self.P = int(F), int(P)
+    def __init__(self, F: int, P: int, device="cuda", scheme: int = 0):
+        self.F, self.P, self.scheme = int(F), int(P), int(scheme)
         d = torch.device(device)
         self.free_list = torch.empty(self.F, dtype=torch.int32, device=d)
         self.cursors = torch.zeros(2, dtype=torch.int64, device=d)   # uint64 bit patterns
         self.rev_unit = torch.empty(self.F, dtype=torch.int32, device=d)
         self.rev_idx = torch.empty(self.F, dtype=torch.int32, device=d)
         self.page_cls = torch.empty(self.F, dtype=torch.uint8, device=d)
-        self.pages = torch.empty((self.F, 216 * self.P), dtype=torch.uint8, device=d)
+        self.pages = torch.empty((self.F, dkv_page_bytes(self.scheme, self.P)), dtype=torch.uint8, device=d)
         self.status = torch.zeros(1, dtype=torch.int32, device=d)
 
     def c(self) -> dkv_pool:
-        return dkv_pool(self.F, self.P, 0, _p(self.free_list), _p(self.cursors), _p(self.rev_unit),
+        return dkv_pool(self.F, self.P, self.scheme, _p(self.free_list), _p(self.cursors), _p(self.rev_unit),
                         _p(self.rev_idx), _p(self.page_cls), _p(self.pages), _p(self.status))
 
 
@@ -283,11 +297,12 @@ class Profiler:
 class Compactor:
     """Convenience owner of pool, tables, classes and workspace for one shape."""
 
-    def __init__(self, L: int, R: int, Hq: int, Hkv: int, T: int, max_len: int, P: int, F: int, device="cuda"):
+    def __init__(self, L: int, R: int, Hq: int, Hkv: int, T: int, max_len: int, P: int, F: int, device="cuda",
+                 scheme: int = 0):
         self.L, self.R, self.Hq, self.Hkv, self.T, self.max_len = L, R, Hq, Hkv, T, max_len
         self.U = L * R * Hkv
         self.pmax = -(-max_len // P) + 1
-        self.pool = DevicePool(F, P, device)
+        self.pool = DevicePool(F, P, device, scheme=scheme)
         self.tables = DeviceTables(self.U, self.pmax, device)
         self.classes = torch.empty(max(L * T * Hkv, 1), dtype=torch.uint8, device=device)
         probe = dkv_batch(L, R, Hq, Hkv, 128, max_len, T, 0, None, None, None, None, None, None)
@@ -370,13 +385,13 @@ class Decoder:
     classes and slot_of from the pages; step() runs dkv_decode_step."""
 
     def __init__(self, L: int, R: int, Hq: int, Hkv: int, cap: int, P: int, F: int, device="cuda",
-                 window: int = 0, mode: int = 0):
+                 window: int = 0, mode: int = 0, scheme: int = 0):
         self.L, self.R, self.Hq, self.Hkv, self.cap, self.P = L, R, Hq, Hkv, cap, P
         self.window, self.mode = int(window), int(mode)
         self.U = L * R * Hkv
         self.pmax = -(-cap // P) + 1
         self.device = torch.device(device)
-        self.pool = DevicePool(F, P, device)
+        self.pool = DevicePool(F, P, device, scheme=scheme)
         self.tables = DeviceTables(self.U, self.pmax, device)
         rows = L * R * cap * Hkv
         self.classes = torch.zeros(rows, dtype=torch.uint8, device=device)

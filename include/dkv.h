@@ -40,23 +40,37 @@
  * layers gives bit-identical results to L one-layer calls made in layer
  * order with unit_base = l * R * Hkv and tables offset by the same unit count.
  *
- * Unified page layout (216 * P bytes; P even).  A K8V4 page holds P tokens,
- * a K4V2 page 2P tokens, so both spend 192 * P bytes on codes:
- *     [0, 128P)        K codes: K8V4 slot s at 128*s (one byte per channel);
- *                      K4V2 slot s at 64*s (two channels per byte)
- *     [128P, 192P)     V codes: K8V4 slot s at 128P + 64*s (4-bit);
- *                      K4V2 slot s at 128P + 32*s (2-bit)
- *     [192P, 208P)     per slot s at 192P + 8*s: fp16 k_scale, k_zero,
- *                      v_scale, v_zero
- *     [208P, 216P)     per slot s at 208P + 4*s: int32 token position
- * Sub-byte codes pack lowest channel in the lowest bits.  Slots fill in rank
- * order (ascending position); unused slots, including slots P..2P-1 of a K8V4
- * page, hold zero codes, zero metadata and position -1.
+ * Precision schemes (dkv_pool.scheme).  The review's free-parameter list
+ * compares K8V4, K4V8, K8V2, K4V2, K2V4 and K4V1 (its Section 7.2) and keeps
+ * K8V4-K4V2.  A scheme pairs a high class (K at kh bits, V at vh bits) with a
+ * low class at half of each, so a low token takes exactly half a high
+ * token's code bytes:
+ *     DKV_SCHEME_K8V4_K4V2 (0, the default)   kh = 8, vh = 4
+ *     DKV_SCHEME_K8V2_K4V1 (1)                kh = 8, vh = 2
+ *     DKV_SCHEME_K4V8_K2V4 (2)                kh = 4, vh = 8
+ * DKV_CLASS_K8V4 / DKV_CLASS_K4V2 below name the high / low class of
+ * whichever scheme the pool uses.
+ *
+ * Unified page layout (P even; C = 16 (kh + vh) P bytes of codes; page bytes
+ * C + 24 P: 216 P for schemes 0 and 2, 184 P for scheme 1).  A high page
+ * holds P tokens, a low page 2P tokens:
+ *     [0, 16 kh P)     K codes: high slot s at 16 kh s, low slot s at 8 kh s
+ *     [16 kh P, C)     V codes: high slot s at 16 kh P + 16 vh s, low slot s
+ *                      at 16 kh P + 8 vh s
+ *     [C, C + 16P)     per slot s at C + 8 s: fp16 k_scale, k_zero, v_scale,
+ *                      v_zero
+ *     [C + 16P, C + 24P)  per slot s at C + 16P + 4 s: int32 token position
+ * For scheme 0 that is K codes [0, 128P), V codes [128P, 192P), metadata at
+ * 192P, positions at 208P.  Sub-byte codes pack lowest channel in the lowest
+ * bits.  Slots fill in rank order (ascending position); unused slots,
+ * including slots P..2P-1 of a high page, hold zero codes, zero metadata and
+ * position -1.
  *
  * Quantiser per token row x[0..127] and bit width b (n = 2^b - 1):
  *     mn = min x, mx = max x (a zero extreme taken as +0); any non-finite x
  *     or |x| > 65504 is DKV_E_RANGE
- *     s16 = fp16_rn((mx - mn) / n), set to 2^-24 if it is 0 while mx > mn
+ *     s16 = fp16_rn((mx - mn) / n), set to 2^-24 if it is 0 while mx > mn,
+ *           and to 65504 if it is infinite (1-bit codes of a span > 65519)
  *     z16 = fp16_rn(mn);  s = (float)s16, z = (float)z16
  *     q   = s == 0 ? 0 : clamp(rint_even((x - z) / s), 0, n)   (fp32 ops)
  *     x'  = fma((float)q, s, z)                               (dequantised)
@@ -80,10 +94,16 @@ extern "C" {
 #define DKV_E_CUDA (-6)     /* sync: a CUDA call failed while enqueuing */
 #define DKV_E_LENS (-7)     /* device: lens[] disagree with T or max_len */
 
-/* Token classes written to dkv_batch.classes and dkv_pool.page_cls. */
+/* Token classes written to dkv_batch.classes and dkv_pool.page_cls (high /
+ * low class of the pool's scheme; the names are those of scheme 0). */
 #define DKV_CLASS_PRUNE 0
 #define DKV_CLASS_K4V2 1
 #define DKV_CLASS_K8V4 2
+
+/* Precision schemes (dkv_pool.scheme). */
+#define DKV_SCHEME_K8V4_K4V2 0
+#define DKV_SCHEME_K8V2_K4V1 1
+#define DKV_SCHEME_K4V8_K2V4 2
 
 #define DKV_HEAD_DIM 128
 
@@ -115,14 +135,14 @@ typedef struct dkv_params {
 /* The page pool: circular free list, cursors, reverse table and pages. */
 typedef struct dkv_pool {
   int64_t F;                 /* pages; 1 <= F <= 2^31 - 1 */
-  int32_t P;                 /* K8V4 tokens per page (K4V2 pages hold 2P); even */
-  int32_t reserved;
+  int32_t P;                 /* high-class tokens per page (low-class pages hold 2P); even */
+  int32_t scheme;            /* DKV_SCHEME_*: bit widths and page layout (0 = K8V4/K4V2) */
   int32_t *free_list;        /* int32 [F]: ring of free page ids, slots [head, tail) mod F */
   uint64_t *cursors;         /* uint64 [2]: {head, tail}, monotone; free = tail - head */
   int32_t *rev_unit;         /* int32 [F]: owning global unit id, -1 if free */
   int32_t *rev_idx;          /* int32 [F]: index in the owner's forward row, -1 if free */
   uint8_t *page_cls;         /* uint8 [F]: 0 free, 1 K4V2 page, 2 K8V4 page */
-  uint8_t *pages;            /* uint8 [F][216 * P], 16-byte aligned */
+  uint8_t *pages;            /* uint8 [F][dkv_page_bytes], 16-byte aligned */
   int32_t *status;           /* int32 [1]: first device-side error since last read */
 } dkv_pool;
 
@@ -133,6 +153,11 @@ typedef struct dkv_tables {
   int32_t reserved;
   int32_t *unit_hdr;         /* int32 [U][4]: {n_k8v4, n_k4v2, pages_k8v4, pages_k4v2} */
 } dkv_tables;
+
+/* Bytes of one unified page of the given scheme and P (host only):
+ * (16 (kh + vh) + 24) P.  DKV_E_INVAL for an unknown scheme or P not even
+ * and positive. */
+int32_t dkv_page_bytes(int32_t scheme, int32_t P, int64_t *bytes);
 
 /* Workspace bytes dkv_compact needs for this batch shape (host only; reads
  * L, R, Hkv, T and max_len of `b`).  Returns DKV_OK or DKV_E_INVAL. */
@@ -303,7 +328,9 @@ typedef struct dkv_attn_batch {
 } dkv_attn_batch;
 
 /* Decode attention (above), asynchronous; allocates nothing.  The pool and
- * tables are read only.  Synchronous DKV_E_INVAL: a bad shape or pointer,
+ * tables are read only.  Synchronous DKV_E_INVAL: a pool whose scheme is not
+ * DKV_SCHEME_K8V4_K4V2 (the kernel reads 8/4-bit K and 4/2-bit V), a bad
+ * shape or pointer,
  * G outside 1..8, or a shape whose per-block shared memory does not fit 220 KB
  * even with a cluster of 8 blocks per unit (a block holds 2 page buffers of
  * 216 P bytes per warp, 6 warps for G <= 4 and 8 above, plus its share of the

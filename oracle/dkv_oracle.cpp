@@ -27,8 +27,11 @@
  *      (a zero extreme canonicalised to +0);
  *      any |x| > 65504 or non-finite x is a range error; s32 = (mx-mn)/n with
  *      n = 2^b - 1; s16 = fp16_rn(s32), bumped to 2^-24 if it underflows to 0
- *      while mx > mn; z16 = fp16_rn(mn); q = clamp(rint((x - z) / s), 0, n)
- *      with round-half-to-even, or 0 when s == 0.
+ *      while mx > mn, and lowered to 65504 (the largest finite binary16) if
+ *      it overflows to infinity -- possible only at b = 1, for a span above
+ *      65519 -- so that the top codes clamp instead of dequantising to NaN;
+ *      z16 = fp16_rn(mn); q = clamp(rint((x - z) / s), 0, n) with
+ *      round-half-to-even, or 0 when s == 0.
  *  Q2  Dequantisation x' = fma(q, s, z) in fp32.
  *  P1  Unified page of 216*P bytes: a K8V4 page holds P tokens, a K4V2 page
  *      2P tokens (K4V2 is half the bits of K8V4, so the code region is 192*P
@@ -273,6 +276,7 @@ int32_t oracle_quant_row(const uint16_t *x, int32_t bits, uint8_t *q, uint16_t *
   const float s32 = span / static_cast<float>(n);
   uint16_t s16 = oracle_fp16_rn(s32);
   if (mx > mn && s16 == 0) s16 = 0x0001; /* smallest subnormal, 2^-24 */
+  if (s16 == 0x7c00) s16 = 0x7bff;       /* reading Q1 step 3: largest finite, 65504 */
   const uint16_t z16 = oracle_fp16_rn(mn);
   const float s = oracle_fp16_to_f32(s16);
   const float z = oracle_fp16_to_f32(z16);
@@ -307,6 +311,7 @@ static void quant_row_f32(const float *xf, int32_t bits, uint8_t *q, uint16_t *s
   const float s32 = span / static_cast<float>(n);
   uint16_t s16 = oracle_fp16_rn(s32);
   if (mx > mn && s16 == 0) s16 = 0x0001;
+  if (s16 == 0x7c00) s16 = 0x7bff;
   const uint16_t z16 = oracle_fp16_rn(mn);
   const float s = oracle_fp16_to_f32(s16);
   const float z = oracle_fp16_to_f32(z16);

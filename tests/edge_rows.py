@@ -186,7 +186,7 @@ def new_token_rows(L: int, R: int, Hkv: int, seed: int) -> tuple:
     return to_t(kx), to_t(vx)
 
 
-def dequant_bound(s: np.ndarray, nbits: int) -> np.ndarray:
+def dequant_bound(s: np.ndarray, nbits: int, span=0.0) -> np.ndarray:
     """Largest |x - (z + q s)| the quantiser allows for a row of scale s
     (float64, elementwise), derived from its fp32 arithmetic:
       - rounding x - z and the quotient by s moves t = (x - z) / s by at most
@@ -195,9 +195,13 @@ def dequant_bound(s: np.ndarray, nbits: int) -> np.ndarray:
       - a binary16 subnormal scale (s < 2^-14) can round down from (max -
         min) / n by up to 2^-25, and a subnormal minimum can round by up to
         2^-25, so the top codes may clamp: up to (n + 1) 2^-25 more;
+      - a scale lowered from infinity to 65504 (1-bit codes of a span above
+        65519: `span` = max - min of the row) clamps the top codes: up to
+        span - n s more;
       - 1e-6 absolute, as the method states its bound.
     """
     n = (1 << nbits) - 1
     s = np.asarray(s, dtype=np.float64)
     b = s * (0.5 + (n + 0.5) * 2.0 ** -23) + 1e-6
+    b = b + np.maximum(0.0, np.asarray(span, dtype=np.float64) - n * s)
     return b + np.where(s < 2.0 ** -14, (n + 1) * 2.0 ** -25, 0.0)

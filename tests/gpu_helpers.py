@@ -19,7 +19,7 @@ def to_device(inp: dict, device="cuda") -> dict:
 def make_compactor(w: W.Workload, L: int | None = None, F: int | None = None) -> libdkv.Compactor:
     L = w.L if L is None else L
     return libdkv.Compactor(L, w.R, w.Hq, w.Hkv, w.T, max(w.lens + [0]), w.P,
-                            w.pool_pages if F is None else F)
+                            w.pool_pages if F is None else F, scheme=w.scheme)
 
 
 def fetch(comp: libdkv.Compactor, pages=True) -> dict:

@@ -16,6 +16,7 @@ import oracle
 from differentiated_kv_cache_dkv_gb300 import libdkv
 from differentiated_kv_cache_dkv_gb300 import workloads as W
 from tests.decode_helpers import HostDecode, check_state
+from tests.oracle_helpers import Layout
 
 pytestmark = pytest.mark.gpu
 
@@ -28,7 +29,8 @@ def gpu_decoder(hd: HostDecode, inp_cpu: dict) -> libdkv.Decoder:
     """Device copy of the oracle's prefill: per-layer dkv_compact on the same
     inputs, then dkv_decode_index."""
     w = hd.w
-    dec = libdkv.Decoder(w.L, w.R, w.Hq, w.Hkv, hd.cap, w.P, hd.pool.F, window=hd.window, mode=hd.mode)
+    dec = libdkv.Decoder(w.L, w.R, w.Hq, w.Hkv, hd.cap, w.P, hd.pool.F, window=hd.window, mode=hd.mode,
+                         scheme=w.scheme)
     for l in range(w.L):
         layer = {"L": 1, "R": w.R, "Hq": w.Hq, "Hkv": w.Hkv, "T": w.T,
                  "k": _dev(inp_cpu["k"][l:l + 1]), "v": _dev(inp_cpu["v"][l:l + 1]),
@@ -74,6 +76,7 @@ def check_slot_index(g: dict, hd: HostDecode):
     """slot_of of every held token points at the slot holding its position;
     -1 for pruned positions."""
     w, cap, P = hd.w, hd.cap, hd.w.P
+    lay = Layout(P, w.scheme)
     cls = g["classes"].reshape(w.L, w.R * cap, w.Hkv)
     so = g["slot_of"].reshape(w.L, w.R * cap, w.Hkv)
     pages = g["pages"]
@@ -92,7 +95,8 @@ def check_slot_index(g: dict, hd: HostDecode):
                         continue
                     per = P if k == 2 else 2 * P
                     pid = fw[(0 if k == 2 else p_hi) + s // per]
-                    pos = pages[pid][208 * P + 4 * (s % per):208 * P + 4 * (s % per) + 4].view(np.int32)[0]
+                    o = lay.pos + 4 * (s % per)
+                    pos = pages[pid][o:o + 4].view(np.int32)[0]
                     assert pos == i, (u, i, s, pos)
 
 

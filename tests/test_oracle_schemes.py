@@ -204,3 +204,18 @@ def test_demotion_on_exact_grids_equals_the_textbook_quantiser(scheme):
             assert list(meta) == list(np.concatenate([mk, mv]))
             seen += 1
     assert seen > 5
+
+
+def test_one_bit_scale_overflow_is_lowered_to_the_largest_binary16():
+    """Reading Q1 step 3: at 1 bit a span above 65519 would round the scale
+    to infinity; it becomes 65504 (0x7bff), so x = min + k 65504 dequantise
+    exactly and the top element clamps to code 1."""
+    x = np.full(128, -65280.0, dtype=np.float32)
+    x[1::4] = np.float32(-65280.0 + 65504.0)   # 224: min + one scale step, exact in bf16
+    x[2] = 65280.0                             # span 130560: t = 1.993, clamped to code 1
+    st, q, s16, z16 = oracle.quant_row(bf16_bits_exact(x), 1)
+    assert st == oracle.OK and s16 == 0x7BFF and f16([z16])[0] == -65280.0
+    assert np.array_equal(q, (x > -65280.0).astype(np.uint8))
+    for bits in (2, 4, 8):  # wider codes never overflow: 130560 / 3 < 65504
+        st, q, s16, z16 = oracle.quant_row(bf16_bits_exact(x), bits)
+        assert st == oracle.OK and np.isfinite(f16([s16])[0])

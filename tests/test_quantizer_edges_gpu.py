@@ -24,31 +24,33 @@ from differentiated_kv_cache_dkv_gb300 import workloads as W
 from tests import edge_rows as E
 from tests.decode_helpers import HostDecode, check_state
 from tests.gpu_helpers import assert_same_state, fetch, make_compactor, oracle_state, to_device
-from tests.oracle_helpers import bf16_to_f32, f16, run_oracle
+from tests.oracle_helpers import Layout, bf16_to_f32, f16, run_oracle
 from tests.test_decode_gpu import check_slot_index, compare, gpu_decoder, gpu_state
 
 pytestmark = pytest.mark.gpu
 
 
 def _check_bound(pages: np.ndarray, page_cls: np.ndarray, P: int, k_in: np.ndarray, v_in: np.ndarray,
-                 where, comp_pool):
+                 where, comp_pool, scheme: int = 0):
     """Dequantise every live page on the GPU and hold each element to the
     bound with the slot's own scale.  where(page, pos) -> (layer, token row,
     head) of the input row."""
+    lay = Layout(P, scheme)
     live = np.nonzero(page_cls)[0]
     k, v, pos = libdkv.dkv_dequant_pages(comp_pool, torch.tensor(live, dtype=torch.int32))
     k, v, pos = k.cpu().numpy(), v.cpu().numpy(), pos.cpu().numpy()
     checked = 0
     for i, pid in enumerate(live):
         high = page_cls[pid] == 2
-        meta = pages[pid][192 * P:208 * P].view(np.uint16).reshape(2 * P, 4)
+        meta = pages[pid][lay.meta:lay.pos].view(np.uint16).reshape(2 * P, 4)
         for s in np.nonzero(pos[i] >= 0)[0]:
             l, t, h = where(int(pid), int(pos[i][s]))
             ms = f16(meta[s]).astype(np.float64)
-            for x_bits, xq, sc, nb in ((k_in[l, t, h], k[i][s], ms[0], 8 if high else 4),
-                                       (v_in[l, t, h], v[i][s], ms[2], 4 if high else 2)):
+            for x_bits, xq, sc, nb in ((k_in[l, t, h], k[i][s], ms[0], lay.kbits(high)),
+                                       (v_in[l, t, h], v[i][s], ms[2], lay.vbits(high))):
                 x = bf16_to_f32(x_bits).astype(np.float64)
-                assert np.all(np.abs(x - xq.astype(np.float64)) <= E.dequant_bound(sc, nb)), (pid, s)
+                bound = E.dequant_bound(sc, nb, x.max() - x.min())
+                assert np.all(np.abs(x - xq.astype(np.float64)) <= bound), (pid, s)
             checked += 1
     return checked
 
