@@ -363,6 +363,7 @@ int32_t dkv_prefill_attention(const dkv_prefill_batch *b, const dkv_pool *pool, 
       b->T < 0 || b->reserved != 0 || !std::isfinite(b->scale))
     return DKV_E_INVAL;
   if (b->R > 65535 || static_cast<int64_t>(b->L) * b->Hq > 65535) return DKV_E_INVAL;  // grid y and z
+  if (static_cast<int64_t>(b->L) * b->T >= INT32_MAX) return DKV_E_INVAL;              // 32-bit TMA row coordinates
   if (!b->q || !b->k || !b->v || !b->lens || !b->out || !b->sig_sum || !b->sig_cnt || !aligned(b->q, 16) ||
       !aligned(b->k, 16) || !aligned(b->v, 16) || !aligned(b->lens, 4) || !aligned(b->out, 8) ||
       !aligned(b->sig_sum, 4) || !aligned(b->sig_cnt, 4))

@@ -352,8 +352,10 @@ int32_t dkv_decode_attention(const dkv_attn_batch *b, const dkv_pool *pool, cons
  * q / G), query i attends causally over keys 0 .. i of its request:
  *   out_i = sum_{j <= i} p(i, j) v_j,   p(i, .) = softmax_j(scale * q_i . k_j),
  * and the call writes sig_sum[l][t(j)][q] = sum_{i >= j} p(i, j) and
- * sig_cnt[t(j)] = N - j: the inputs dkv_compact classifies.  Computed with
- * bf16 x bf16 products exact, fp32 accumulation and p carried to 22 bits.
+ * sig_cnt[t(j)] = N - j: the inputs dkv_compact classifies.  Computed on the
+ * tensor cores (tcgen05): bf16 x bf16 products exact, fp32 accumulation; the
+ * significance sums add the fp32 probabilities, the outputs use p rounded to
+ * bf16 for the P V product.
  * ------------------------------------------------------------------------ */
 typedef struct dkv_prefill_batch {
   int32_t L, R, Hq, Hkv;     /* 1 <= Hq / Hkv */

@@ -83,9 +83,9 @@ def prefill_bounds(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
     Products of bf16 values are exact; the logits are fp32 sums of 128 of them
     on the tensor cores: |dl_ij| <= 64 u scale sum_d |q_id| |k_jd|.  The
     probabilities then carry rho_ij as in attention_bounds (exponential,
-    normaliser, 22-bit fp16 parts); the outputs are fp32 sums over n keys of
-    p times v in fp16 (exact in the normal range, 2^-25 below it), and a
-    significance sum adds n probabilities in fp32 (atomics in any order).
+    normaliser); the outputs are fp32 sums over n keys of p rounded to bf16
+    (relative error at most 2^-8 more) times the bf16 v, and a significance
+    sum adds n fp32 probabilities in fp32 (atomics in any order).
     Returns (bound on |out| errors [n][128], bound on |sig_sum| errors [n],
     the probabilities p [n][n] in double)."""
     n = q.shape[0]
@@ -102,6 +102,6 @@ def prefill_bounds(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
         eta = np.where(mask, dl + U * np.minimum(mx - lg, 200.0) + 2.0 ** -19, 0.0)
     rho = np.expm1(eta) + np.expm1((p * eta).sum(1, keepdims=True)) + (n + 16) * U
     rho = np.where(mask, rho, 0.0)
-    out_b = 2.0 * ((p * (rho + (n + 32) * U)) @ np.abs(v) + 2.0 ** -24)
+    out_b = 2.0 * ((p * (rho + (n + 32) * U + 2.0 ** -8)) @ np.abs(v) + 2.0 ** -24)
     sig_b = 2.0 * ((p * rho).sum(0) + (n + 8) * U * p.sum(0))
     return out_b, sig_b, p
