@@ -10,36 +10,34 @@
 // is also where sig_sum[j] = sum_{i >= j} p(i, j) and sig_cnt[j] = N - j are
 // produced; the compaction reads exactly these.
 //
-// One CTA of 8 warps per (128-query tile, request, layer x query head): warp
-// w reads tensor-memory lanes 32 (w mod 4) .. + 31 (the rows it owns) and
-// columns 64 (w div 4) .. + 63 of each row, so two threads share a row and
-// its row statistics meet once, after pass 1.  Key tiles are 128 keys.  Operands are staged by TMA with the 128-byte swizzle, 64 channels
-// (128 bytes) per box row, two boxes per 128-channel tile:
-//   S = Q K^T     tcgen05.mma kind::f16, A = Q (K-major, bf16), B = K
-//                 (K-major, bf16), D = 128 x 128 fp32 in tensor-memory
-//                 columns [0, 128); products exact, fp32 accumulation
-//   O += P V      A = P rounded to bf16, held in tensor memory over the S
-//                 columns already read (keys 0-63 in columns [0, 32), keys
-//                 64-127 in [64, 96), two probabilities per column), B = V as
-//                 it lies in memory (keys x channels: MN-major), D = O in
-//                 columns [128, 256)
-// Pass 1 runs S over the key tiles for each row's maximum and sum (online);
-// pass 2 runs S again, forms the exact probabilities p = exp(S - m) / l in
-// fp32 (one multiply-add into log2 units and ex2), adds their column sums
-// (fp32, through a per-warp shared-memory transpose, then one atomic per key
-// and tile) to the keys' significance sums, and accumulates O.  Rows are
-// processed in rolled chunks of 32 columns, which keeps the code within the
-// instruction cache and the registers at two CTAs per SM.  Two passes because a column sum needs the final
-// normaliser of every row it crosses.
-//
-// Early prefetch: in pass 1 the V buffer is a second K buffer and two K tiles
-// are in flight; in pass 2 the next K tile is requested as soon as the MMA
-// that read the current one has completed, the next V tile as soon as P V
-// has.  Two CTAs share an
-// SM (about 107 KB of shared memory and 256 tensor-memory columns each).
+// One CTA per (128-query tile, request, layer x query head), one per SM:
+// 16 softmax warps, an S-issuing warp, a P V-issuing warp and a copy warp.
+// Key tiles are 128 keys; Q, K and V tiles are staged by TMA with the
+// 128-byte swizzle, 64 channels per box row, two boxes per 128-channel tile,
+// K and V through a ring of four tile slots.  Two passes, because a key's
+// significance needs the final normaliser of every row it meets:
+//   pass 1  S = Q K^T (A = Q, B = K, both K-major; D = 128 x 128 fp32 in one
+//           of three tensor-memory buffers, so S of later tiles runs while
+//           this one is read): each row's maximum and sum, online, in log2
+//           units.
+//   pass 2  S^T = K Q^T (A = K, B = Q): one tensor-memory lane per KEY, so
+//           p = exp2(s scale log2e - m_q) / l_q is formed per key row with
+//           the queries' (m, 1 / l) broadcast from shared memory, and the
+//           key's significance is a plain row sum in fp32 (four column
+//           quarters per key, one atomic each per tile).  P^T, rounded to
+//           bf16, goes to shared memory as rows of keys with the queries
+//           contiguous, which is P in the MN-major A form: O += P V with
+//           A = P (MN-major), B = V as it lies in memory (keys x channels:
+//           MN-major), D = O (128 x 128 fp32) in its own tensor-memory
+//           columns.
+// Warp w of the softmax group reads tensor-memory lanes 32 (w mod 4) .. + 31
+// and columns 32 (w div 4) .. + 31 of a tile: four threads per row (pass 1)
+// or key (pass 2), whose row statistics meet once, after pass 1.  S and P V
+// are issued by separate warps, so P V of a tile never queues behind the
+// wait for a later K tile.
 // Every mbarrier wait is bounded by the global timer; a CTA that gives up
-// records DKV_E_TIMEOUT, waits (bounded) for its own copies and MMAs, frees its
-// tensor memory and leaves.
+// records DKV_E_TIMEOUT, the copy and MMA warps wait (bounded) for their own
+// copies and MMAs, and the tensor memory is freed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -52,30 +50,41 @@
 namespace dkv {
 
 namespace {
-
 constexpr int kTile = 128;                  // queries per CTA, keys per key tile
-constexpr int kThreadsP = 256;              // two threads per query row, 64 columns each
-constexpr uint32_t kTmemCols = 256;         // S in [0, 128), O in [128, 256)
-constexpr uint32_t kColO = 128;
-constexpr uint32_t kBoxBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16
-constexpr uint32_t kTileBytes = 2 * kBoxBytes;
+constexpr int kSoftmaxWarps = 16;           // four threads per row or key, 32 columns each
+constexpr int kSWarp = kSoftmaxWarps;       // issues S (or S^T)
+constexpr int kPvWarp = kSoftmaxWarps + 1;  // issues P V, adds the significance
+constexpr int kLoadWarp = kSoftmaxWarps + 2;  // the copy warp
+constexpr int kThreadsP = 32 * (kLoadWarp + 1);
+constexpr int kSBuf = 3;                    // S buffers in tensor memory
+constexpr uint32_t kTmemCols = 512;         // S buffers [0, 128), [128, 256), [256, 384); O [384, 512)
+constexpr uint32_t kColO = 384;
+constexpr uint32_t kBox = kTile * 128;      // one box: 128 rows x 64 bf16 (16 KB)
+constexpr uint32_t kTileBytes = 2 * kBox;
+constexpr int kSlots = 4;                   // K / V staging ring
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr uint32_t kWaitPolls = 1u << 26;
 
 struct __align__(1024) PrefillSmem {
-  uint8_t q[kTileBytes];       // Q tile: box 0 (channels 0-63), box 1 (64-127)
-  uint8_t k[kTileBytes];       // K tile
-  uint8_t v[kTileBytes];       // V tile (pass 2) or the second K buffer (pass 1)
-  float tr[8][32 * 8];         // per-warp transpose of 8 probability columns
-  float part[4][kTile];        // column sums of the key tile per row quarter
-  float2 stat[2][kTile];       // pass-1 (max, sum) of each row's two column halves
-  uint64_t bar_q, bar_k, bar_v, bar_mma;
-  uint32_t tmem;               // tensor-memory base address from tcgen05.alloc
-  int32_t abort;               // a bounded wait gave up: skip the rest
+  uint8_t q[kTileBytes];             // Q tile: box 0 (channels 0-63), box 1 (64-127)
+  uint8_t ring[kSlots][kTileBytes];  // K or V tiles, same two-box form
+  uint8_t pt[kTileBytes];            // P^T in bf16: [query half][128 keys][64 queries], 128-byte swizzle
+  float2 stat[4][kTile];             // pass-1 (max, sum) of each row's four column quarters
+  float4 mi[kTile / 2];              // per query pair: (m, m', 1 / l, 1 / l')
+  uint64_t bar_q;                    // Q landed
+  uint64_t full[kSlots], empty[kSlots];  // a ring slot landed / was read by its MMAs
+  uint64_t bar_s[kSBuf];             // S (or S^T) of a tile computed into buffer b
+  uint64_t bar_sfree[kSBuf];         // the softmax warps have read buffer b
+  uint64_t bar_pready;               // P^T of a pass-2 tile is in shared memory
+  uint64_t bar_o, bar_done;          // P V of a tile done; every P V done
+  uint64_t bar_sdone;                // every S done
+  uint32_t tmem;                     // tensor-memory base address from tcgen05.alloc
+  int32_t abort;                     // a bounded wait gave up: everyone winds down
   int64_t start;
   int32_t lens_ok;
 };
 constexpr size_t kPrefillSmem = sizeof(PrefillSmem) + 1024;  // + alignment slack
+static_assert(kPrefillSmem <= 227 * 1024, "shared memory");
 
 // ------------------------------------------------------------ PTX helpers --
 
@@ -98,8 +107,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                : "memory");
 }
 
-// Bounded wait for the phase of the given parity: false after about kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Bounded wait for the phase of the given parity: false after about kWaitNs,
+// or as soon as *abort (when given) is set by another thread.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int32_t *abort) {
   const uint32_t addr = saddr(bar);
   uint64_t t0 = 0;
   for (uint32_t i = 0; i < kWaitPolls; ++i) {
@@ -111,12 +121,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     if (done) return true;
     if ((i & 63) == 63) {
+      if (abort && *abort) return false;
       const uint64_t t = global_ns();
       if (t0 == 0) t0 = t;
       else if (t - t0 > kWaitNs) return false;
     }
   }
   return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(saddr(bar)) : "memory");
+}
+
+// Named barrier of the softmax warps only.
+__device__ __forceinline__ void softmax_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftmaxWarps) : "memory");
 }
 
 // TMA load of one box of a 3-D tensor map at (channel c0, head c1, row c2).
@@ -129,11 +149,11 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
-// One 128-row x 128-channel tile: both 64-channel boxes on one barrier.
+// One 128-row tile (both 64-channel boxes) on one barrier.
 __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, int head, int row, uint64_t *bar) {
   mbar_expect_tx(bar, kTileBytes);
   tma_load_3d(dst, map, 0, head, row, bar);
-  tma_load_3d(dst + kBoxBytes, map, 64, head, row, bar);
+  tma_load_3d(dst + kBox, map, 64, head, row, bar);
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -152,24 +172,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint
   return d;
 }
 
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A
-// K-major, B K-major (b_mn = false) or MN-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A and
+// B K-major or MN-major (a_mn, b_mn), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 
@@ -196,22 +209,73 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&x)[32]) {
   for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
 }
 
-// 16 consecutive 32-bit columns of this thread's lane.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-
 // 2^x by the special-function unit (relative error about 2^-22; results
 // below 2^-126 flush to zero, far below any probability that matters).
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed fp32 pairs (one instruction for two lanes of work, each rounded to
+// nearest like the scalar operation).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of 32 values as a tree of three-input maxima.
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+  float t[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) t[i] = max3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  t[10] = fmaxf(v[30], v[31]);
+  const float u0 = max3(t[0], t[1], t[2]), u1 = max3(t[3], t[4], t[5]), u2 = max3(t[6], t[7], t[8]);
+  return max3(max3(u0, u1, u2), t[9], t[10]);
+}
+
+// v[i] <- 2^(v[i] * sl2 - mo) for 32 values, in packed pairs; returns their
+// sum (a tree of packed additions).
+__device__ __forceinline__ float exp2_sum32(float (&v)[32], float sl2, float mo) {
+  const uint64_t s2 = f2_pack(sl2, sl2), m2 = f2_pack(-mo, -mo);
+  uint64_t e[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float a, b;
+    f2_unpack(f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), s2, m2), a, b);
+    e[i] = f2_pack(ex2(a), ex2(b));
+  }
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) e[i] = f2_add(e[i], e[i + w]);
+  float lo, hi;
+  f2_unpack(e[0], lo, hi);
+  return lo + hi;
 }
 
 // bf16 pair rounded to nearest even, the lower-indexed value in the low half.
@@ -256,47 +320,13 @@ __device__ __forceinline__ bool request_start(const PrefillArgs &a, int32_t r, i
   return *ok_sm != 0;
 }
 
-// Column sums of one 32-column chunk of this tile's probabilities over the
-// warp's 32 rows: four rounds of 8 columns through the warp's shared-memory
-// transpose, 8 words per row.  Row r keeps its two 4-column halves swapped
-// when bit 2 of r is set, so a quarter-warp's two 16-byte stores hit 32
-// distinct banks; lane (g, c) sums column c over rows 8g .. 8g + 7, group g
-// taking them in the order starting at row 8g + g, so the four groups' loads
-// hit distinct banks too.  off: this lane's word offsets, computed once
-// (two stores, then eight loads).  Lanes 0-7 end with the sums of a round's
-// columns, written to part[row quarter][column].
-__device__ __forceinline__ void chunk_column_sums(PrefillSmem &sm, const float (&p)[32], int col0,
-                                                  const int (&off)[10]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float *tr = sm.tr[warp];
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    *reinterpret_cast<float4 *>(tr + off[0]) = make_float4(p[8 * r], p[8 * r + 1], p[8 * r + 2], p[8 * r + 3]);
-    *reinterpret_cast<float4 *>(tr + off[1]) = make_float4(p[8 * r + 4], p[8 * r + 5], p[8 * r + 6], p[8 * r + 7]);
-    __syncwarp();
-    float s0 = tr[off[2]] + tr[off[3]], s1 = tr[off[4]] + tr[off[5]];
-    float s2 = tr[off[6]] + tr[off[7]], s3 = tr[off[8]] + tr[off[9]];
-    float s = (s0 + s1) + (s2 + s3);
-    s += __shfl_xor_sync(0xffffffffu, s, 8);
-    s += __shfl_xor_sync(0xffffffffu, s, 16);
-    if (lane < 8) sm.part[warp & 3][col0 + 8 * r + lane] = s;
-    __syncwarp();
-  }
-}
-
-// Word offset of (row, column) in the transpose above.
-__device__ __forceinline__ int tr_word(int row, int col) {
-  return 8 * row + 4 * ((col >> 2) ^ ((row >> 2) & 1)) + (col & 3);
-}
-
-__global__ void __launch_bounds__(kThreadsP, 2)
+__global__ void __launch_bounds__(kThreadsP, 1)
     k_prefill(PrefillArgs a, const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
               const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ unsigned char smem_raw[];
   PrefillSmem &sm =
       *reinterpret_cast<PrefillSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rq = warp & 3, ch = warp >> 2;  // row quarter (tensor-memory lanes), column half
   const int32_t r = blockIdx.y;
   const int32_t l = static_cast<int32_t>(blockIdx.z / a.Hq), qh = static_cast<int32_t>(blockIdx.z % a.Hq);
   const int32_t h = qh / a.G;
@@ -308,28 +338,24 @@ __global__ void __launch_bounds__(kThreadsP, 2)
   const int32_t qt = ntq - 1 - static_cast<int32_t>(blockIdx.x);  // longest rows first
   if (qt < 0) return;
   const int64_t row0 = static_cast<int64_t>(l) * a.T + start;    // (layer, request) token row 0
-  const int32_t nkt = qt + 1;                                      // key tiles the causal rows reach
-  const int row = 32 * rq + lane;                                  // this thread's row of the tile
-  const int32_t qrow = qt * kTile + row;                           // its query position
-  // a row past the request masks every key (qlim = -1); masks are applied
-  // per element only in the diagonal tile and in a tile with such rows
-  const int32_t qlim = qrow < n ? qrow : -1;
-  const bool ragged = (qt + 1) * kTile > n;
-  const float sl2 = a.scale * 1.44269504088896340736f;             // logits in log2 units
-  int tro[10];  // the column-sum transpose's word offsets for this lane
-  {
-    const int g = lane >> 3, c = lane & 7;
-    tro[0] = tr_word(lane, 0);
-    tro[1] = tr_word(lane, 4);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) tro[2 + k] = tr_word(8 * g + ((k + g) & 7), c);
-  }
+  const int32_t nk = qt + 1;                                       // key tiles the causal rows reach
+  const bool ragged = (qt + 1) * kTile > n;                        // rows past the request in this tile
+  volatile int32_t *abort = &sm.abort;
 
   if (tid == 0) {
     mbar_init(&sm.bar_q, 1);
-    mbar_init(&sm.bar_k, 1);
-    mbar_init(&sm.bar_v, 1);
-    mbar_init(&sm.bar_mma, 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], 1);
+    }
+    for (int i = 0; i < kSBuf; ++i) {
+      mbar_init(&sm.bar_s[i], 1);
+      mbar_init(&sm.bar_sfree[i], kSoftmaxWarps);
+    }
+    mbar_init(&sm.bar_pready, kSoftmaxWarps);
+    mbar_init(&sm.bar_o, 1);
+    mbar_init(&sm.bar_done, 1);
+    mbar_init(&sm.bar_sdone, 1);
     sm.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -343,221 +369,248 @@ __global__ void __launch_bounds__(kThreadsP, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * rq) << 16);  // this warp's lanes
-  const uint32_t s_cols = lane_base + 64 * ch;                                // its 64 columns of S
 
-  constexpr uint32_t idesc_s = idesc_bf16(128, 128, false);
-  constexpr uint32_t idesc_o = idesc_bf16(128, 128, true);
-  const uint32_t q_s = saddr(sm.q), k_s = saddr(sm.k), v_s = saddr(sm.v);
-
-  // Per barrier: phases issued (copies or MMA commits requested; every
-  // thread counts them, the decisions are uniform) and phases waited for
-  // (the parity of the next wait).
-  uint32_t iss_q = 0, iss_k = 0, iss_v = 0, iss_mma = 0;
-  uint32_t ph_q = 0, ph_k = 0, ph_v = 0, ph_mma = 0;
-  bool ok = true;
-  // every thread waits; a failure anywhere aborts the whole CTA (the phase
-  // stays counted as outstanding)
-  auto wait_all = [&](uint64_t *bar, uint32_t &ph) {
-    const bool w = mbar_wait(bar, ph & 1u);
-    if (w) ph++;
-    if (!w) {
-      sm.abort = 1;
+  // a wait that gives up records the timeout once and makes everyone stop
+  auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+    if (mbar_wait(bar, parity, abort)) return true;
+    if (!*abort) {
+      *abort = 1;
       set_error(a.status, DKV_E_TIMEOUT);
     }
-    __syncthreads();
-    ok = ok && sm.abort == 0;
+    return false;
   };
+  // Tiles g = 0 .. 2 nk - 1: pass 1 (g < nk) key tile g, pass 2 key tile
+  // g - nk; tile g is computed into tensor-memory buffer g mod 3.  Copies
+  // L = 0 .. 3 nk - 1 go to ring slot L mod kSlots: pass 1 K(L); pass 2 K(j)
+  // at nk + 2 j and V(j) at nk + 2 j + 1.
+  const int32_t n_loads = 3 * nk;
 
-  // S = Q K^T of the key tile staged at kbuf into columns [0, 128): eight
-  // K-steps of 16 channels, 32 bytes along the swizzled 128-byte rows, the
-  // second four in the second box
-  auto issue_s = [&](uint32_t kbuf) {
-    iss_mma++;
-    if (tid == 0) {
+  if (warp == kLoadWarp) {
+    // ================= copy warp: lane 0 issues; a slot is refilled once
+    // the MMAs that read it have completed
+    if (lane == 0) {
+      load_tile(sm.q, &qmap, qh, static_cast<int>(row0 + qt * kTile), &sm.bar_q);
+      int32_t L = 0;
+      for (; L < n_loads; ++L) {
+        const int s = L % kSlots;
+        if (L >= kSlots && !wait(&sm.empty[s], ((L / kSlots) - 1) & 1u)) break;
+        const bool is_v = L >= nk && ((L - nk) & 1);
+        const int32_t j = L < nk ? L : (L - nk) >> 1;
+        load_tile(sm.ring[s], is_v ? &vmap : &kmap, h, static_cast<int>(row0 + j * kTile), &sm.full[s]);
+      }
+      // every copy issued has landed before the CTA leaves (bounded)
+      mbar_wait(&sm.bar_q, 0, nullptr);
+      for (int32_t i = max(0, L - kSlots); i < L; ++i) mbar_wait(&sm.full[i % kSlots], (i / kSlots) & 1u, nullptr);
+    }
+  } else if (warp == kSWarp || warp == kPvWarp) {
+    // ================= MMA warps: lane 0 waits and issues.  The S warp runs
+    // S (pass 1) and S^T (pass 2) of tile g into buffer g mod 3 as soon as
+    // the softmax warps have read tile g - 3 and the K tile has landed; the
+    // P V warp runs O += P V of each pass-2 tile once its P^T is in shared
+    // memory.
+    const bool leader = lane == 0;
+    constexpr uint32_t kSlotStep = kTileBytes >> 4;
+    bool ok = true;
+    if (warp == kSWarp) {
+      if (leader) {
+        constexpr uint32_t idesc_s = idesc_bf16(kTile, kTile, false, false);
+        // descriptors at the operands' bases; a K-step adds its byte offset / 16
+        const uint64_t dq = sw128_desc(saddr(sm.q), 16, 1024);
+        const uint64_t dk = sw128_desc(saddr(sm.ring[0]), 16, 1024);  // K-major (K tiles)
+        ok = wait(&sm.bar_q, 0);
+        for (int32_t g = 0; g < 2 * nk && ok; ++g) {
+          const int b = g % kSBuf;
+          if (g >= kSBuf && !(ok = wait(&sm.bar_sfree[b], ((g / kSBuf) - 1) & 1u))) break;
+          const bool pass2 = g >= nk;
+          const int32_t Lk = pass2 ? nk + 2 * (g - nk) : g;
+          if (!(ok = wait(&sm.full[Lk % kSlots], (Lk / kSlots) & 1u))) break;
+          tc_fence_after();
+          const uint64_t dks = dk + (Lk % kSlots) * kSlotStep;
+          const uint64_t da = pass2 ? dks : dq, db = pass2 ? dq : dks;  // S = Q K^T, S^T = K Q^T
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // 16 channels a step: 32 bytes along the swizzled rows, then the next box
+            const uint32_t o = ((kk >> 2) * kBox + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + kTile * b, da + o, db + o, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&sm.bar_s[b]);
+          mma_commit(&sm.empty[Lk % kSlots]);
+        }
+        // every MMA of this warp done (also after an abort)
+        mma_commit(&sm.bar_sdone);
+        mbar_wait(&sm.bar_sdone, 0, nullptr);
+      }
+    } else {
+      constexpr uint32_t idesc_o = idesc_bf16(kTile, 128, true, true);
+      const uint64_t dv = sw128_desc(saddr(sm.ring[0]), kBox, 1024);  // MN-major (V tiles): boxes kBox apart
+      const uint64_t dp = sw128_desc(saddr(sm.pt), kBox, 1024);       // MN-major (P^T): query halves kBox apart
+      if (leader) {
+        for (int32_t j = 0; j < nk && ok; ++j) {
+          const int32_t Lv = nk + 2 * j + 1;
+          if (!(ok = wait(&sm.bar_pready, j & 1u) && wait(&sm.full[Lv % kSlots], (Lv / kSlots) & 1u))) break;
+          tc_fence_after();
+          const uint64_t dvs = dv + (Lv % kSlots) * kSlotStep;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // 16 keys a step: 16 rows (2048 bytes) of P^T and of V
+            mma_ss(tmem + kColO, dp + ((kk * 2048) >> 4), dvs + ((kk * 2048) >> 4), idesc_o,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&sm.bar_o);
+          mma_commit(&sm.empty[Lv % kSlots]);
+        }
+        // every MMA of this warp done (also after an abort)
+        mma_commit(&sm.bar_done);
+        mbar_wait(&sm.bar_done, 0, nullptr);
+      }
+    }
+  } else {
+    // ================= softmax warps: warp w reads lanes 32 (w mod 4) .. + 31
+    // and columns 32 (w div 4) .. + 31 of each tile
+    const int rq = warp & 3, cq = warp >> 2;
+    const int row = 32 * rq + lane;  // pass 1: query row; pass 2: key row of the tile
+    const int32_t qrow = qt * kTile + row;
+    // pass 1 masks: a row past the request masks every key (qlim = -1);
+    // masks are applied per element only in the diagonal tile and in a tile
+    // with such rows
+    const int32_t qlim = qrow < n ? qrow : -1;
+    const float sl2 = a.scale * 1.44269504088896340736f;  // logits in log2 units
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * rq) << 16);
+    bool ok = true;
+    int32_t g = 0;
+
+    // ---- pass 1: row maximum and sum over this thread's columns (log2
+    // units); the buffer is handed back as soon as it is read
+    float m = -INFINITY, lsum = 0.0f;
+    for (int32_t j = 0; j < nk; ++j, ++g) {
+      if (!(ok = wait(&sm.bar_s[g % kSBuf], (g / kSBuf) & 1u))) break;
       tc_fence_after();
+      float v[32];
+      tmem_ld32(lane_base + kTile * (g % kSBuf) + 32 * cq, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.bar_sfree[g % kSBuf]);
+      if (j == qt || ragged) {
+        const int32_t key0 = j * kTile + 32 * cq;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-        mma_ss(tmem, sw128_desc(q_s + off, 16, 1024), sw128_desc(kbuf + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        for (int i = 0; i < 32; ++i) v[i] = key0 + i <= qlim ? v[i] : -INFINITY;
       }
-      mma_commit(&sm.bar_mma);
-    }
-  };
-
-  // ---- prologue: Q and the first two K tiles
-  if (tid == 0) {
-    load_tile(sm.q, &qmap, qh, static_cast<int>(row0 + qt * kTile), &sm.bar_q);
-    load_tile(sm.k, &kmap, h, static_cast<int>(row0), &sm.bar_k);
-    if (nkt > 1) load_tile(sm.v, &kmap, h, static_cast<int>(row0 + kTile), &sm.bar_v);
-  }
-  iss_q = 1;
-  iss_k = 1;
-  iss_v = nkt > 1 ? 1 : 0;
-  wait_all(&sm.bar_q, ph_q);
-
-  // ---- pass 1: row maximum and sum of this thread's 64 columns (log2
-  // units).  Key tile kt sits in buffer kt & 1 (k, then v); two tiles are in
-  // flight: tile kt + 2 is requested into tile kt's buffer once S of tile kt
-  // is done.
-  float m = -INFINITY, lsum = 0.0f;
-  for (int32_t kt = 0; kt < nkt && ok; ++kt) {
-    uint64_t *bar = (kt & 1) ? &sm.bar_v : &sm.bar_k;
-    uint32_t &ph = (kt & 1) ? ph_v : ph_k;
-    wait_all(bar, ph);
-    if (!ok) break;
-    issue_s((kt & 1) ? v_s : k_s);
-    wait_all(&sm.bar_mma, ph_mma);
-    if (!ok) break;
-    if (kt + 2 < nkt) {
-      if (tid == 0)
-        load_tile((kt & 1) ? sm.v : sm.k, &kmap, h, static_cast<int>(row0 + (kt + 2) * kTile), bar);
-      if (kt & 1) iss_v++; else iss_k++;
-    }
-    tc_fence_after();
-    const bool masked = kt == qt || ragged;
-#pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      float x[32];
-      tmem_ld32(s_cols + 32 * c, x);
-      const int32_t key0 = kt * kTile + 64 * ch + 32 * c;
-      float mx = -INFINITY;
-      if (masked) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[i] = key0 + i <= qlim ? x[i] * sl2 : -INFINITY;
-          mx = fmaxf(mx, x[i]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[i] *= sl2;
-          mx = fmaxf(mx, x[i]);
-        }
-      }
-      const float mn = fmaxf(m, mx);
+      const float mn = fmaxf(m, max32(v) * sl2);  // scale > 0: the maximum commutes with it
       if (mn != -INFINITY) {
-        float t = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) t += ex2(x[i] - mn);
-        lsum = lsum * ex2(m - mn) + t;  // ex2(-inf) = 0 on the first chunk
+        const float t = exp2_sum32(v, sl2, mn);
+        lsum = lsum * ex2(m - mn) + t;  // ex2(-inf) = 0 on the first tile
         m = mn;
       }
     }
-    tc_fence_before();
-    __syncthreads();  // S is read: its columns may be overwritten
-  }
-  // the two column halves of a row meet: m = max, l = sum of rescaled sums
-  sm.stat[ch][row] = make_float2(m, lsum);
-  __syncthreads();
-  {
-    const float2 o = sm.stat[ch ^ 1][row];
-    const float mn = fmaxf(m, o.x);
-    if (mn != -INFINITY) {
-      lsum = lsum * ex2(m - mn) + o.y * ex2(o.x - mn);
-      m = mn;
-    }
-  }
-  const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;  // 0 for a row past the request
-
-  // ---- pass 2: probabilities, column sums, O += P V.  Tile kt + 1's K is
-  // requested after S of tile kt, its V after P V of tile kt.
-  if (ok) {
-    if (tid == 0) {
-      load_tile(sm.k, &kmap, h, static_cast<int>(row0), &sm.bar_k);
-      load_tile(sm.v, &vmap, h, static_cast<int>(row0), &sm.bar_v);
-    }
-    iss_k++;
-    iss_v++;
-  }
-  for (int32_t kt = 0; kt < nkt && ok; ++kt) {
-    wait_all(&sm.bar_k, ph_k);
-    if (!ok) break;
-    issue_s(k_s);
-    wait_all(&sm.bar_mma, ph_mma);
-    if (!ok) break;
-    if (kt + 1 < nkt) {
-      if (tid == 0) load_tile(sm.k, &kmap, h, static_cast<int>(row0 + (kt + 1) * kTile), &sm.bar_k);
-      iss_k++;
-    }
-    tc_fence_after();
-    const bool masked = kt == qt || ragged;
-#pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      float x[32];
-      tmem_ld32(s_cols + 32 * c, x);
-      const int32_t key0 = kt * kTile + 64 * ch + 32 * c;
-      if (masked) {
+    // the four column quarters of a row meet: m = max, l = sum of rescaled
+    // sums; then (m, 1 / l) of every row is published for pass 2 (a row
+    // past the request has l = 0 and 1 / l is taken as 0)
+    sm.stat[cq][row] = make_float2(m, lsum);
+    softmax_sync();
+    if (cq == 0) {
+      float2 st[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = key0 + i <= qlim ? ex2(__fmaf_rn(x[i], sl2, -m)) * inv : 0.0f;
-      } else {
+      for (int c = 0; c < 4; ++c) st[c] = sm.stat[c][row];
+      const float mx = fmaxf(fmaxf(st[0].x, st[1].x), fmaxf(st[2].x, st[3].x));
+      float ls = 0.0f;
+      if (mx != -INFINITY) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = ex2(__fmaf_rn(x[i], sl2, -m)) * inv;
+        for (int c = 0; c < 4; ++c) ls += st[c].y * ex2(st[c].x - mx);
       }
-      chunk_column_sums(sm, x, 64 * ch + 32 * c, tro);
-      // P (bf16 pairs) of keys 64 ch + 32 c .. + 31 into columns
-      // 64 ch + 16 c .. + 15: S columns this warp has already read, so no
-      // other warp's S is overwritten
+      float *mi = reinterpret_cast<float *>(&sm.mi[row >> 1]);
+      mi[row & 1] = mx == -INFINITY ? 0.0f : mx;
+      mi[2 + (row & 1)] = ls > 0.0f ? 1.0f / ls : 0.0f;
+    }
+    softmax_sync();
+    ok = ok && *abort == 0;
+
+    // ---- pass 2: S^T of key tile j: this thread's key row, queries
+    // q0 .. q0 + 31.  p = exp2(s sl2 - m_q) / l_q; valid where key <= q < n.
+    // The row sum is added to the key's significance (four atomics per key
+    // and tile, one per column quarter), P^T (bf16) goes to shared memory
+    // once P V of the previous tile has read it: key row `row` of query half cq / 2, 16-byte chunks
+    // 4 (cq mod 2) .. + 3, chunk c stored at c xor (row mod 8) (the 128-byte
+    // swizzle).
+    const int32_t q0 = qt * kTile + 32 * cq;
+    uint8_t *prow = sm.pt + (cq >> 1) * kBox + row * 128;
+    const uint64_t s2 = f2_pack(sl2, sl2);
+    for (int32_t j = 0; j < nk && ok; ++j, ++g) {
+      if (!(ok = wait(&sm.bar_s[g % kSBuf], (g / kSBuf) & 1u))) break;
+      tc_fence_after();
+      float v[32];
+      tmem_ld32(lane_base + kTile * (g % kSBuf) + 32 * cq, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.bar_sfree[g % kSBuf]);
+      uint64_t e[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 t = sm.mi[16 * cq + 2 * i];      // queries q0 + 4 i, + 1
+        const float4 u = sm.mi[16 * cq + 2 * i + 1];  // queries q0 + 4 i + 2, + 3
+        float x0, x1, x2, x3;
+        f2_unpack(f2_fma(f2_pack(v[4 * i], v[4 * i + 1]), s2, f2_pack(-t.x, -t.y)), x0, x1);
+        f2_unpack(f2_fma(f2_pack(v[4 * i + 2], v[4 * i + 3]), s2, f2_pack(-u.x, -u.y)), x2, x3);
+        e[2 * i] = f2_mul(f2_pack(ex2(x0), ex2(x1)), f2_pack(t.z, t.w));
+        e[2 * i + 1] = f2_mul(f2_pack(ex2(x2), ex2(x3)), f2_pack(u.z, u.w));
+      }
+      if (j == qt || ragged) {
+        const int32_t key = j * kTile + row;
+        const int32_t lo = key - q0, hi = n - q0;  // valid queries: lo <= i < hi
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float x0, x1;
+          f2_unpack(e[i], x0, x1);
+          x0 = (2 * i >= lo && 2 * i < hi) ? x0 : 0.0f;
+          x1 = (2 * i + 1 >= lo && 2 * i + 1 < hi) ? x1 : 0.0f;
+          e[i] = f2_pack(x0, x1);
+        }
+      }
       uint32_t w[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = bf16x2_rn(x[2 * i], x[2 * i + 1]);
-      tmem_st16(s_cols + 16 * c, w);
-    }
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-    tc_fence_before();
-    __syncthreads();
-    {  // every column's four row-quarter sums -> one atomic per key
-      const int32_t key = kt * kTile + tid;
-      if (tid < kTile && key < n) {
-        const float s = sm.part[0][tid] + sm.part[1][tid] + sm.part[2][tid] + sm.part[3][tid];
-        if (s != 0.0f) atomicAdd(a.sig_sum + (row0 + key) * a.Hq + qh, s);
+      for (int i = 0; i < 16; ++i) {
+        float x0, x1;
+        f2_unpack(e[i], x0, x1);
+        w[i] = bf16x2_rn(x0, x1);
       }
-    }
-    wait_all(&sm.bar_v, ph_v);  // (its barrier also keeps part[] until every sum is read)
-    if (!ok) break;
-    iss_mma++;
-    if (tid == 0) {
-      tc_fence_after();
+      {
+        uint64_t t[8];
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // keys 16 kk .. + 15: 8 columns of P (at 64 (kk / 4) + 8 (kk % 4)), 16 rows of V
-        mma_ts(tmem + kColO, tmem + 64 * (kk >> 2) + 8 * (kk & 3), sw128_desc(v_s + kk * 2048, kBoxBytes, 1024),
-               idesc_o, (kt > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(&sm.bar_mma);
+        for (int i = 0; i < 8; ++i) t[i] = f2_add(e[i], e[i + 8]);
+#pragma unroll
+        for (int wd = 4; wd >= 1; wd >>= 1)
+#pragma unroll
+          for (int i = 0; i < wd; ++i) t[i] = f2_add(t[i], t[i + wd]);
+        float lo_, hi_;
+        f2_unpack(t[0], lo_, hi_);
+        const float rs = lo_ + hi_;
+        const int32_t key = j * kTile + row;
+        if (key < n && rs != 0.0f) atomicAdd(a.sig_sum + (row0 + key) * a.Hq + qh, rs);
+      }
+      if (j > 0 && !(ok = wait(&sm.bar_o, (j - 1) & 1u))) break;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint4 *>(prow + 16 * ((4 * (cq & 1) + i) ^ (row & 7))) =
+            make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.bar_pready);
     }
-    wait_all(&sm.bar_mma, ph_mma);
-    if (!ok) break;
-    if (kt + 1 < nkt) {
-      if (tid == 0) load_tile(sm.v, &vmap, h, static_cast<int>(row0 + (kt + 1) * kTile), &sm.bar_v);
-      iss_v++;
-    }
-  }
 
-  // ---- outputs: this thread's 64 channels of its row of O (the loads are
-  // warp-collective, so every lane takes them; rows past the request store
-  // nothing)
-  if (ok) {
-    tc_fence_after();
-    float *dst = a.out + ((row0 + qrow) * a.Hq + qh) * 128 + 64 * ch;
-#pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      float x[32];
-      tmem_ld32(lane_base + kColO + 64 * ch + 32 * c, x);
+    // ---- outputs: this thread's 32 channels of its row of O (the loads are
+    // warp-collective, so every lane takes them; rows past the request store
+    // nothing)
+    if (ok && wait(&sm.bar_done, 0)) {
+      tc_fence_after();
+      float v[32];
+      tmem_ld32(lane_base + kColO + 32 * cq, v);
       if (qrow < n) {
+        float *dst = a.out + ((row0 + qrow) * a.Hq + qh) * 128 + 32 * cq;
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4 *>(dst + 32 * c + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+          *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
       }
     }
   }
 
-  // ---- teardown: after an abort, wait (bounded) for this CTA's own copies
-  // and MMAs, so none outlives it; then free the tensor memory
-  if (!ok && tid == 0) {
-    for (; ph_q < iss_q; ++ph_q) mbar_wait(&sm.bar_q, ph_q & 1u);
-    for (; ph_k < iss_k; ++ph_k) mbar_wait(&sm.bar_k, ph_k & 1u);
-    for (; ph_v < iss_v; ++ph_v) mbar_wait(&sm.bar_v, ph_v & 1u);
-    for (; ph_mma < iss_mma; ++ph_mma) mbar_wait(&sm.bar_mma, ph_mma & 1u);
-  }
+  // ---- teardown: the copy and MMA warps have waited (bounded) for this
+  // CTA's own copies and MMAs; free the tensor memory
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
