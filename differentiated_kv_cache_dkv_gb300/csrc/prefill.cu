@@ -68,15 +68,17 @@ constexpr uint32_t kWaitPolls = 1u << 26;
 struct __align__(1024) PrefillSmem {
   uint8_t q[kTileBytes];             // Q tile: box 0 (channels 0-63), box 1 (64-127)
   uint8_t ring[kSlots][kTileBytes];  // K or V tiles, same two-box form
-  uint8_t pt[kTileBytes];            // P^T in bf16: [query half][128 keys][64 queries], 128-byte swizzle
-  float2 stat[4][kTile];             // pass-1 (max, sum) of each row's four column quarters
+  // P^T in bf16, two buffers by key-tile parity: [query half][128 keys][64
+  // queries], 128-byte swizzle.  Before pass 2 the first holds the pass-1
+  // (max, sum) of each row's four column quarters (float2 [4][128]).
+  uint8_t pt[2][kTileBytes];
   float4 mi[kTile / 2];              // per query pair: (m, m', 1 / l, 1 / l')
   uint64_t bar_q;                    // Q landed
   uint64_t full[kSlots], empty[kSlots];  // a ring slot landed / was read by its MMAs
   uint64_t bar_s[kSBuf];             // S (or S^T) of a tile computed into buffer b
   uint64_t bar_sfree[kSBuf];         // the softmax warps have read buffer b
-  uint64_t bar_pready;               // P^T of a pass-2 tile is in shared memory
-  uint64_t bar_o, bar_done;          // P V of a tile done; every P V done
+  uint64_t bar_pready[2];            // P^T of a pass-2 tile is in shared-memory buffer b
+  uint64_t bar_o[2], bar_done;       // P V of a tile from buffer b done; every P V done
   uint64_t bar_sdone;                // every S done
   uint32_t tmem;                     // tensor-memory base address from tcgen05.alloc
   int32_t abort;                     // a bounded wait gave up: everyone winds down
@@ -352,8 +354,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       mbar_init(&sm.bar_s[i], 1);
       mbar_init(&sm.bar_sfree[i], kSoftmaxWarps);
     }
-    mbar_init(&sm.bar_pready, kSoftmaxWarps);
-    mbar_init(&sm.bar_o, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.bar_pready[i], kSoftmaxWarps);
+      mbar_init(&sm.bar_o[i], 1);
+    }
     mbar_init(&sm.bar_done, 1);
     mbar_init(&sm.bar_sdone, 1);
     sm.abort = 0;
@@ -442,18 +446,20 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     } else {
       constexpr uint32_t idesc_o = idesc_bf16(kTile, 128, true, true);
       const uint64_t dv = sw128_desc(saddr(sm.ring[0]), kBox, 1024);  // MN-major (V tiles): boxes kBox apart
-      const uint64_t dp = sw128_desc(saddr(sm.pt), kBox, 1024);       // MN-major (P^T): query halves kBox apart
+      const uint64_t dp = sw128_desc(saddr(sm.pt[0]), kBox, 1024);    // MN-major (P^T): query halves kBox apart
       if (leader) {
         for (int32_t j = 0; j < nk && ok; ++j) {
           const int32_t Lv = nk + 2 * j + 1;
-          if (!(ok = wait(&sm.bar_pready, j & 1u) && wait(&sm.full[Lv % kSlots], (Lv / kSlots) & 1u))) break;
+          if (!(ok = wait(&sm.bar_pready[j & 1], (j >> 1) & 1u) && wait(&sm.full[Lv % kSlots], (Lv / kSlots) & 1u)))
+            break;
           tc_fence_after();
           const uint64_t dvs = dv + (Lv % kSlots) * kSlotStep;
+          const uint64_t dps = dp + (j & 1) * kSlotStep;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // 16 keys a step: 16 rows (2048 bytes) of P^T and of V
-            mma_ss(tmem + kColO, dp + ((kk * 2048) >> 4), dvs + ((kk * 2048) >> 4), idesc_o,
+            mma_ss(tmem + kColO, dps + ((kk * 2048) >> 4), dvs + ((kk * 2048) >> 4), idesc_o,
                    (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&sm.bar_o);
+          mma_commit(&sm.bar_o[j & 1]);
           mma_commit(&sm.empty[Lv % kSlots]);
         }
         // every MMA of this warp done (also after an abort)
@@ -502,12 +508,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     // the four column quarters of a row meet: m = max, l = sum of rescaled
     // sums; then (m, 1 / l) of every row is published for pass 2 (a row
     // past the request has l = 0 and 1 / l is taken as 0)
-    sm.stat[cq][row] = make_float2(m, lsum);
+    float2(&stat)[4][kTile] = *reinterpret_cast<float2(*)[4][kTile]>(sm.pt[0]);
+    stat[cq][row] = make_float2(m, lsum);
     softmax_sync();
     if (cq == 0) {
       float2 st[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) st[c] = sm.stat[c][row];
+      for (int c = 0; c < 4; ++c) st[c] = stat[c][row];
       const float mx = fmaxf(fmaxf(st[0].x, st[1].x), fmaxf(st[2].x, st[3].x));
       float ls = 0.0f;
       if (mx != -INFINITY) {
@@ -529,7 +536,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     // 4 (cq mod 2) .. + 3, chunk c stored at c xor (row mod 8) (the 128-byte
     // swizzle).
     const int32_t q0 = qt * kTile + 32 * cq;
-    uint8_t *prow = sm.pt + (cq >> 1) * kBox + row * 128;
+    const uint32_t prow = (cq >> 1) * kBox + row * 128;  // this thread's row of a P^T buffer
     const uint64_t s2 = f2_pack(sl2, sl2);
     for (int32_t j = 0; j < nk && ok; ++j, ++g) {
       if (!(ok = wait(&sm.bar_s[g % kSBuf], (g / kSBuf) & 1u))) break;
@@ -583,14 +590,16 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         const int32_t key = j * kTile + row;
         if (key < n && rs != 0.0f) atomicAdd(a.sig_sum + (row0 + key) * a.Hq + qh, rs);
       }
-      if (j > 0 && !(ok = wait(&sm.bar_o, (j - 1) & 1u))) break;
+      // buffer j mod 2 is free once P V of tile j - 2 has read it
+      if (j > 1 && !(ok = wait(&sm.bar_o[j & 1], ((j - 2) >> 1) & 1u))) break;
+      uint8_t *pb = sm.pt[j & 1] + prow;
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<uint4 *>(prow + 16 * ((4 * (cq & 1) + i) ^ (row & 7))) =
+        *reinterpret_cast<uint4 *>(pb + 16 * ((4 * (cq & 1) + i) ^ (row & 7))) =
             make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.bar_pready);
+      if (lane == 0) mbar_arrive(&sm.bar_pready[j & 1]);
     }
 
     // ---- outputs: this thread's 32 channels of its row of O (the loads are
