@@ -242,7 +242,9 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
       if (k < d) {
         int64_t idx = ring + k;
         if (idx >= a.F) idx -= a.F;
+        if (!in_range(idx, a.F, a.status)) continue;
         id = a.free_list[idx];
+        if (!in_range(id, a.F, a.status)) continue;
         a.rev_unit[id] = static_cast<int32_t>(a.unit_base + u);
         a.rev_idx[id] = k;
         a.page_cls[id] = k < inf.p_hi ? DKV_CLASS_K8V4 : DKV_CLASS_K4V2;
@@ -261,9 +263,11 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
     if (lane == 0) reinterpret_cast<int4 *>(a.unit_hdr)[u] = make_int4(inf.n_hi, inf.n_lo, inf.p_hi, p_lo);
     // tails of the last K8V4 and the last K4V2 page
     const int64_t sh = inf.n_hi % P;
-    if (sh != 0) {
-      int64_t idx = ring + inf.p_hi - 1;
-      if (idx >= a.F) idx -= a.F;
+    int64_t ih = ring + inf.p_hi - 1, il = ring + d - 1;
+    if (ih >= a.F) ih -= a.F;
+    if (il >= a.F) il -= a.F;
+    if (sh != 0 && in_range(ih, a.F, a.status) && in_range(a.free_list[ih], a.F, a.status)) {
+      const int64_t idx = ih;
       uint8_t *pg = a.pages + static_cast<int64_t>(a.free_list[idx]) * page_bytes;
       fill_words(pg + 16 * g.kh * sh, 4 * g.kh * (P - sh), 0u, lane);
       fill_words(pg + g.vbase + 16 * g.vh * sh, 4 * g.vh * (P - sh), 0u, lane);
@@ -271,9 +275,8 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
       fill_words(pg + g.pos + 4 * sh, P - sh, 0xffffffffu, lane);
     }
     const int64_t sl = inf.n_lo % (2 * P);
-    if (sl != 0) {
-      int64_t idx = ring + d - 1;
-      if (idx >= a.F) idx -= a.F;
+    if (sl != 0 && in_range(il, a.F, a.status) && in_range(a.free_list[il], a.F, a.status)) {
+      const int64_t idx = il;
       uint8_t *pg = a.pages + static_cast<int64_t>(a.free_list[idx]) * page_bytes;
       fill_words(pg + 8 * g.kh * sl, 2 * g.kh * (2 * P - sl), 0u, lane);
       fill_words(pg + g.vbase + 8 * g.vh * sl, 2 * g.vh * (2 * P - sl), 0u, lane);

@@ -132,6 +132,8 @@ extern "C" {
 
 int32_t dkv_version(void) { return 100; }
 
+int32_t dkv_build_flags(void) { return dkv::kChecked ? DKV_BUILD_CHECKED : 0; }
+
 const char *dkv_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda); }
 
 const char *dkv_status_string(int32_t code) {

@@ -535,6 +535,7 @@ __device__ __forceinline__ int32_t new_page(const DecodeArgs &a, const UnitView 
 // first, then the new ones.  -1 (and an error) for an id outside the pool.
 __device__ __forceinline__ int32_t list_page(const DecodeArgs &a, const UnitView &v, bool hi, int32_t k) {
   int32_t id;
+  if (!in_range(k, hi ? max(v.p.have_hi, v.p.need_hi) : max(v.p.have_lo, v.p.need_lo), a.status)) return -1;
   if (hi) id = k < v.p.have_hi ? v.fw[k] : new_page(a, v, k - v.p.have_hi);
   else id = k < v.p.have_lo ? v.fw[v.p.have_hi + k] : new_page(a, v, v.xh + k - v.p.have_lo);
   if (id < 0 || id >= a.F) {

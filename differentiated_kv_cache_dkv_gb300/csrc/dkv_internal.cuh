@@ -160,6 +160,22 @@ struct CompactArgs {
 
 __device__ __forceinline__ void set_error(int32_t *err, int32_t code) { atomicCAS(err, 0, code); }
 
+// Bounds checks of the DKV_CHECKED build, the stand-in for a device memory
+// checker: there in_range() records DKV_E_INTERNAL and returns false when i
+// lies outside [0, n), and the caller skips the access (no trap).  In the
+// normal build it is the constant true and costs nothing.
+#ifdef DKV_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+__device__ __forceinline__ bool in_range(int64_t i, int64_t n, int32_t *status) {
+  if (!kChecked) return true;
+  if (i >= 0 && i < n) return true;
+  set_error(status, DKV_E_INTERNAL);
+  return false;
+}
+
 // Largest r in [0, n) with a[r] <= x (a non-decreasing, a[0] <= x).
 __device__ __forceinline__ int find_segment(const int32_t *a, int n, int64_t x, int64_t scale) {
   int lo = 0, hi = n - 1;

@@ -364,7 +364,7 @@ __device__ __forceinline__ void list_rows(const CompactArgs &a, const TileDesc &
     }
     int64_t idx = static_cast<int64_t>(m.ring) + pidx;
     if (idx >= a.F) idx -= a.F;
-    o.id[x] = o.ent[x] >= 0 ? __ldg(a.free_list + idx) : 0;
+    o.id[x] = o.ent[x] >= 0 ? (in_range(idx, a.F, &a.ws->err) ? __ldg(a.free_list + idx) : -1) : 0;
   }
   o.nsurv = lo0 + nl_t;  // entries spanned
   o.nh_t = nh_t;

@@ -13,7 +13,10 @@ import os
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "lib", "libdkv.so")
+# DKV_LIBRARY=checked selects the bounds-checked build (lib/libdkv_checked.so),
+# DKV_LIBRARY=sanitized the one with sanitized host code (lib/libdkv_san.so)
+LIB_PATH = os.path.join(HERE, "lib", {"checked": "libdkv_checked.so", "sanitized": "libdkv_san.so"}.get(
+    os.environ.get("DKV_LIBRARY", ""), "libdkv.so"))
 
 DKV_OK = 0
 DKV_E_INVAL = -1
@@ -108,6 +111,7 @@ def load():
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     sigs = {
         "dkv_version": ([], i32),
+        "dkv_build_flags": ([], i32),
         "dkv_status_string": ([i32], ctypes.c_char_p),
         "dkv_last_cuda_error": ([], ctypes.c_char_p),
         "dkv_page_bytes": ([i32, i32, P(ctypes.c_int64)], i32),

@@ -404,6 +404,17 @@ const char *dkv_status_string(int32_t code);
 const char *dkv_last_cuda_error(void);
 int32_t dkv_version(void);
 
+/* How the library was built: DKV_BUILD_CHECKED is set in the bounds-checked
+ * build (lib/libdkv_checked.so, compiled with -DDKV_CHECKED).  There every
+ * page id, free-list index and page-list index that a kernel takes from the
+ * tables is checked before it is used; a value outside its range records
+ * DKV_E_INTERNAL in the pool status and the access is skipped (the kernel
+ * does not trap).  The pool contents after such an error are unspecified.
+ * The normal build keeps the checks that cost nothing measurable (page ids
+ * read from the forward table or the free list before a page is touched). */
+#define DKV_BUILD_CHECKED 1
+int32_t dkv_build_flags(void);
+
 #ifdef __cplusplus
 }
 #endif

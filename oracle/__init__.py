@@ -16,7 +16,7 @@ import os
 
 import numpy as np
 
-from .build import LIB_PATH, build_oracle
+from .build import LIB_PATH, LIB_PATH_SAN, build_oracle
 
 OK = 0
 E_INVAL = -1
@@ -85,9 +85,11 @@ def lib():
     """Load (building first if needed) the oracle shared library."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            build_oracle()
-        L = ctypes.CDLL(LIB_PATH)
+        sanitized = os.environ.get("ORACLE_LIBRARY") == "sanitized"
+        path = LIB_PATH_SAN if sanitized else LIB_PATH
+        if not os.path.exists(path):
+            build_oracle(sanitize=sanitized)
+        L = ctypes.CDLL(path)
         L.oracle_fp16_rn.argtypes = [ctypes.c_float]
         L.oracle_fp16_rn.restype = ctypes.c_uint16
         L.oracle_fp16_to_f32.argtypes = [ctypes.c_uint16]
