@@ -12,7 +12,6 @@
 // This convenience has no counterpart in the DiffKV paper.
 #include <cuda_runtime.h>
 
-#include <mutex>
 
 #include "dkv_internal.cuh"
 
@@ -24,26 +23,16 @@ constexpr size_t kScratchBytes = DKV_NOALLOC_SCRATCH_BYTES;
 // all it relies on at the start of each call).
 __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices];
-std::mutex g_scratch_mutex;
-
-// Device address of g_scratch on the current device (host code cannot use the
-// symbol's own address: it names a host-side stand-in).  Resolved once per
-// device, with that device current.
+// Device address of g_scratch in the current context (host code cannot use
+// the symbol's own address: it names a host-side stand-in).  Resolved on every
+// call: after cudaDeviceReset, or in another context on the same device, the
+// module is loaded again and the address can change; the lookup is cheap next
+// to the launches it precedes.
 cudaError_t scratch_address(void **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_addr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
