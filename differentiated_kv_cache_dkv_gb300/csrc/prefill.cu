@@ -62,23 +62,24 @@ constexpr uint32_t kColO = 384;
 constexpr uint32_t kBox = kTile * 128;      // one box: 128 rows x 64 bf16 (16 KB)
 constexpr uint32_t kTileBytes = 2 * kBox;
 constexpr int kSlots = 4;                   // K / V staging ring
+constexpr int kPBuf = 2;                    // P^T buffers
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr uint32_t kWaitPolls = 1u << 26;
 
 struct __align__(1024) PrefillSmem {
   uint8_t q[kTileBytes];             // Q tile: box 0 (channels 0-63), box 1 (64-127)
   uint8_t ring[kSlots][kTileBytes];  // K or V tiles, same two-box form
-  // P^T in bf16, two buffers by key-tile parity: [query half][128 keys][64
+  // P^T in bf16, kPBuf buffers by key tile: [query half][128 keys][64
   // queries], 128-byte swizzle.  Before pass 2 the first holds the pass-1
   // (max, sum) of each row's four column quarters (float2 [4][128]).
-  uint8_t pt[2][kTileBytes];
+  uint8_t pt[kPBuf][kTileBytes];
   float4 mi[kTile / 2];              // per query pair: (m, m', 1 / l, 1 / l')
   uint64_t bar_q;                    // Q landed
   uint64_t full[kSlots], empty[kSlots];  // a ring slot landed / was read by its MMAs
   uint64_t bar_s[kSBuf];             // S (or S^T) of a tile computed into buffer b
   uint64_t bar_sfree[kSBuf];         // the softmax warps have read buffer b
-  uint64_t bar_pready[2];            // P^T of a pass-2 tile is in shared-memory buffer b
-  uint64_t bar_o[2], bar_done;       // P V of a tile from buffer b done; every P V done
+  uint64_t bar_pready[kPBuf];        // P^T of a pass-2 tile is in shared-memory buffer b
+  uint64_t bar_o[kPBuf], bar_done;   // P V of a tile from buffer b done; every P V done
   uint64_t bar_sdone;                // every S done
   uint32_t tmem;                     // tensor-memory base address from tcgen05.alloc
   int32_t abort;                     // a bounded wait gave up: everyone winds down
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       mbar_init(&sm.bar_s[i], 1);
       mbar_init(&sm.bar_sfree[i], kSoftmaxWarps);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kPBuf; ++i) {
       mbar_init(&sm.bar_pready[i], kSoftmaxWarps);
       mbar_init(&sm.bar_o[i], 1);
     }
@@ -450,16 +451,16 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       if (leader) {
         for (int32_t j = 0; j < nk && ok; ++j) {
           const int32_t Lv = nk + 2 * j + 1;
-          if (!(ok = wait(&sm.bar_pready[j & 1], (j >> 1) & 1u) && wait(&sm.full[Lv % kSlots], (Lv / kSlots) & 1u)))
+          if (!(ok = wait(&sm.bar_pready[j % kPBuf], (j / kPBuf) & 1u) && wait(&sm.full[Lv % kSlots], (Lv / kSlots) & 1u)))
             break;
           tc_fence_after();
           const uint64_t dvs = dv + (Lv % kSlots) * kSlotStep;
-          const uint64_t dps = dp + (j & 1) * kSlotStep;
+          const uint64_t dps = dp + (j % kPBuf) * kSlotStep;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // 16 keys a step: 16 rows (2048 bytes) of P^T and of V
             mma_ss(tmem + kColO, dps + ((kk * 2048) >> 4), dvs + ((kk * 2048) >> 4), idesc_o,
                    (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&sm.bar_o[j & 1]);
+          mma_commit(&sm.bar_o[j % kPBuf]);
           mma_commit(&sm.empty[Lv % kSlots]);
         }
         // every MMA of this warp done (also after an abort)
@@ -590,16 +591,16 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         const int32_t key = j * kTile + row;
         if (key < n && rs != 0.0f) atomicAdd(a.sig_sum + (row0 + key) * a.Hq + qh, rs);
       }
-      // buffer j mod 2 is free once P V of tile j - 2 has read it
-      if (j > 1 && !(ok = wait(&sm.bar_o[j & 1], ((j - 2) >> 1) & 1u))) break;
-      uint8_t *pb = sm.pt[j & 1] + prow;
+      // buffer j mod kPBuf is free once P V of tile j - kPBuf has read it
+      if (j >= kPBuf && !(ok = wait(&sm.bar_o[j % kPBuf], ((j - kPBuf) / kPBuf) & 1u))) break;
+      uint8_t *pb = sm.pt[j % kPBuf] + prow;
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         *reinterpret_cast<uint4 *>(pb + 16 * ((4 * (cq & 1) + i) ^ (row & 7))) =
             make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.bar_pready[j & 1]);
+      if (lane == 0) mbar_arrive(&sm.bar_pready[j % kPBuf]);
     }
 
     // ---- outputs: this thread's 32 channels of its row of O (the loads are
