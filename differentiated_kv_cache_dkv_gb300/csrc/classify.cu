@@ -112,6 +112,32 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(CompactArgs a, int32_t np
   for (int32_t i = tid; i < npart; i += blockDim.x) a.part[i] = 0;
 }
 
+// One tile of a layer: where its scores start and how many tokens it holds.
+struct ClassifyItem {
+  int64_t l, t0, N;
+  int32_t rt, cnt;
+};
+
+__device__ __forceinline__ ClassifyItem classify_item(const CompactArgs &a, int64_t item, int32_t TR) {
+  ClassifyItem it;
+  it.l = item / TR;
+  it.rt = static_cast<int32_t>(item - it.l * TR);
+  const int r = __ldg(a.tile_req + it.rt);
+  const int32_t tr0 = __ldg(a.tile_off + r);
+  const int32_t j = it.rt - tr0;
+  const int64_t tok0 = __ldg(a.tok_off + r);
+  it.N = __ldg(a.tok_off + r + 1) - tok0;
+  it.t0 = tok0 + static_cast<int64_t>(j) * kTileTokens;
+  const int64_t left = it.N - static_cast<int64_t>(j) * kTileTokens;
+  it.cnt = static_cast<int>(left < kTileTokens ? left : kTileTokens);
+  return it;
+}
+
+// Scores held in registers for the next tile (the first kPre float4 per
+// thread: every score of a tile when Hq <= 32), loaded while the current tile
+// is classified.
+constexpr int kPre = 4;
+
 template <bool kVec>
 __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -123,47 +149,91 @@ __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
   const int64_t items = static_cast<int64_t>(a.L) * TR;
   const int tid = threadIdx.x;
   const int G = a.G;
-  for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
-    const int64_t l = item / TR;
-    const int32_t rt = static_cast<int32_t>(item - l * TR);
-    const int r = __ldg(a.tile_req + rt);
-    const int32_t tr0 = __ldg(a.tile_off + r);
-    const int32_t nt = __ldg(a.tile_off + r + 1) - tr0;
-    const int32_t j = rt - tr0;
-    const int64_t tok0 = __ldg(a.tok_off + r);
-    const int64_t N = __ldg(a.tok_off + r + 1) - tok0;
-    const int64_t t0 = tok0 + static_cast<int64_t>(j) * kTileTokens;
-    const int64_t left = N - static_cast<int64_t>(j) * kTileTokens;
-    const int cnt = static_cast<int>(left < kTileTokens ? left : kTileTokens);
-    const float thr_h = __fdiv_rn(a.alpha_h, static_cast<float>(N));
-    const float thr_l = __fdiv_rn(a.alpha_l, static_cast<float>(N));
+  const int ld = a.Hq + 1;
+  // (4 i) / Hq by a multiply: exact for 4 i < 2^32 / Hq (4 i <= 128 Hq here)
+  const uint32_t inv_hq = static_cast<uint32_t>((0x100000000ull + a.Hq - 1) / a.Hq);
+
+  float4 pre[kPre];
+  int32_t pre_cnt = 0;
+  auto prefetch = [&](const ClassifyItem &it) {
+    const float4 *s4 = reinterpret_cast<const float4 *>(a.sig_sum + (it.l * a.T + it.t0) * a.Hq);
+    const int nv = (it.cnt * a.Hq) >> 2;
+#pragma unroll
+    for (int q = 0; q < kPre; ++q) {
+      const int i = tid + q * kClassifyThreads;
+      pre[q] = i < nv ? __ldcs(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pre_cnt = tid < it.cnt ? __ldg(a.sig_cnt + it.t0 + tid) : 0;
+  };
+
+  int64_t item = blockIdx.x;
+  ClassifyItem cur{};
+  if (kVec && item < items) {
+    cur = classify_item(a, item, TR);
+    prefetch(cur);
+  }
+  for (; item < items; item += gridDim.x) {
+    if (!kVec) cur = classify_item(a, item, TR);
+    const int cnt = cur.cnt;
+    const float thr_h = __fdiv_rn(a.alpha_h, static_cast<float>(cur.N));
+    const float thr_l = __fdiv_rn(a.alpha_l, static_cast<float>(cur.N));
+    // Reciprocal test: with rc the hardware reciprocal of n (within 1 ulp),
+    // y = RN(m * rc) is within 2^-22 (relative) of m / n, so y >= thr (1 + 2^-19)
+    // proves RN(m / n) >= thr and y <= thr (1 - 2^-19) proves RN(m / n) < thr
+    // (the margins, themselves rounded, stay far from 2^-22); in between, and
+    // for thresholds below 2^-100 where a tiny quotient could leave the
+    // relative bound, the IEEE division decides.  A NaN fails every test and
+    // goes to the division: pruned.
+    const bool exact_only = !(thr_l >= 0x1p-100f);
+    const float hi_h = __fmul_rn(thr_h, 1.0f + 0x1p-19f), lo_h = __fmul_rn(thr_h, 1.0f - 0x1p-19f);
+    const float hi_l = __fmul_rn(thr_l, 1.0f + 0x1p-19f), lo_l = __fmul_rn(thr_l, 1.0f - 0x1p-19f);
 
     // stage the tile's summed scores [cnt][Hq] into rows padded to Hq + 1
     // floats, so the per-token reads below hit 32 different banks
-    const float *src = a.sig_sum + (l * a.T + t0) * a.Hq;
+    const float *src = a.sig_sum + (cur.l * a.T + cur.t0) * a.Hq;
     const int nf = cnt * a.Hq;
-    const int ld = a.Hq + 1;
     if (kVec) {
       const float4 *s4 = reinterpret_cast<const float4 *>(src);
-      for (int i = tid; i < (nf >> 2); i += blockDim.x) {
+      const int nv = nf >> 2;
+#pragma unroll
+      for (int q = 0; q < kPre; ++q) {
+        const int i = tid + q * kClassifyThreads;
+        if (i < nv) {
+          const int k = static_cast<int>(__umulhi(static_cast<uint32_t>(4 * i), inv_hq));
+          float *d = sig_s + k * ld + (4 * i - k * a.Hq);
+          d[0] = pre[q].x;
+          d[1] = pre[q].y;
+          d[2] = pre[q].z;
+          d[3] = pre[q].w;
+        }
+      }
+      for (int i = tid + kPre * kClassifyThreads; i < nv; i += blockDim.x) {  // Hq > 32: the rest, now
         const float4 x = __ldcs(s4 + i);
-        const int k = (4 * i) / a.Hq;
+        const int k = static_cast<int>(__umulhi(static_cast<uint32_t>(4 * i), inv_hq));
         float *d = sig_s + k * ld + (4 * i - k * a.Hq);
         d[0] = x.x;
         d[1] = x.y;
         d[2] = x.z;
         d[3] = x.w;
       }
+      if (tid < cnt) cnt_s[tid] = pre_cnt;
     } else {
       for (int i = tid; i < nf; i += blockDim.x) {
         const int k = i / a.Hq;
         sig_s[k * ld + (i - k * a.Hq)] = __ldcs(src + i);
       }
+      for (int i = tid; i < cnt; i += blockDim.x) cnt_s[i] = __ldg(a.sig_cnt + cur.t0 + i);
     }
-    for (int i = tid; i < cnt; i += blockDim.x) cnt_s[i] = __ldg(a.sig_cnt + t0 + i);
     __syncthreads();
+    // the next tile's scores are loaded while this one is classified
+    const int64_t next = item + gridDim.x;
+    ClassifyItem nxt{};
+    if (kVec && next < items) {
+      nxt = classify_item(a, next, TR);
+      prefetch(nxt);
+    }
 
-    const int64_t tau0 = l * a.Hkv * TR + rt;  // unit tile of head 0
+    const int64_t tau0 = cur.l * a.Hkv * TR + cur.rt;  // unit tile of head 0
     for (int p = tid; p < a.Hkv * kTileTokens; p += blockDim.x) {
       const int h = p / kTileTokens;
       const int k = p % kTileTokens;
@@ -180,8 +250,20 @@ __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
           } else {
             for (int g = 1; g < G; ++g) m = fminf(m, row[g]);
           }
-          const float s = __fdiv_rn(m, static_cast<float>(n));
-          c = s >= thr_h ? DKV_CLASS_K8V4 : (s >= thr_l ? DKV_CLASS_K4V2 : DKV_CLASS_PRUNE);
+          const float cf = static_cast<float>(n);
+          float rc;
+          asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(cf));
+          const float y = __fmul_rn(m, rc);
+          if (!exact_only && y >= hi_h) {
+            c = DKV_CLASS_K8V4;
+          } else if (!exact_only && !(y > lo_h) && y >= hi_l) {
+            c = DKV_CLASS_K4V2;
+          } else if (!exact_only && !(y > lo_h) && !(y > lo_l)) {
+            c = DKV_CLASS_PRUNE;
+          } else {
+            const float s = __fdiv_rn(m, cf);
+            c = s >= thr_h ? DKV_CLASS_K8V4 : (s >= thr_l ? DKV_CLASS_K4V2 : DKV_CLASS_PRUNE);
+          }
         }
         cls_s[k * a.Hkv + h] = static_cast<uint8_t>(c);
       }
@@ -194,9 +276,17 @@ __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
       }
     }
     __syncthreads();
-    uint8_t *dst = a.classes + (l * a.T + t0) * a.Hkv;
-    for (int b = tid; b < cnt * a.Hkv; b += blockDim.x) dst[b] = cls_s[b];
+    uint8_t *dst = a.classes + (cur.l * a.T + cur.t0) * a.Hkv;
+    const int nb = cnt * a.Hkv;
+    if ((reinterpret_cast<uintptr_t>(dst) & 3) == 0) {  // whole words, then the tail
+      for (int b = tid; b < (nb >> 2); b += blockDim.x)
+        reinterpret_cast<uint32_t *>(dst)[b] = reinterpret_cast<const uint32_t *>(cls_s)[b];
+      for (int b = (nb & ~3) + tid; b < nb; b += blockDim.x) dst[b] = cls_s[b];
+    } else {
+      for (int b = tid; b < nb; b += blockDim.x) dst[b] = cls_s[b];
+    }
     __syncthreads();
+    cur = nxt;
   }
 }
 
