@@ -248,17 +248,27 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
         a.rev_unit[id] = static_cast<int32_t>(a.unit_base + u);
         a.rev_idx[id] = k;
         a.page_cls[id] = k < inf.p_hi ? DKV_CLASS_K8V4 : DKV_CLASS_K4V2;
-        if (k < inf.p_hi) {  // a high page has no slots P..2P-1
-          uint8_t *pg = a.pages + id * page_bytes;
-          uint4 *meta = reinterpret_cast<uint4 *>(pg + g.meta + 8 * P);
-          int2 *pos = reinterpret_cast<int2 *>(pg + g.pos + 4 * P);
-          for (int64_t i = 0; i < P / 2; ++i) {
-            meta[i] = make_uint4(0u, 0u, 0u, 0u);
-            pos[i] = make_int2(-1, -1);
-          }
-        }
       }
       fw[k] = id;
+    }
+    // a high page has no slots P..2P-1: their metadata (8P bytes: P/2 chunks
+    // of 16) and positions (4P bytes: P/2 chunks of 8; P is even) are
+    // cleared, the chunks spread over the lanes so that consecutive lanes
+    // write consecutive chunks of one page
+    {
+      const int64_t cm = P / 2, cp = P / 2;  // chunks of metadata, of positions
+      const int64_t per = cm + cp;
+      for (int64_t e = lane; e < inf.p_hi * per; e += 32) {
+        const int64_t k = e / per, c = e - k * per;
+        int64_t idx = ring + k;
+        if (idx >= a.F) idx -= a.F;
+        if (!in_range(idx, a.F, a.status)) continue;
+        const int64_t id = a.free_list[idx];
+        if (!in_range(id, a.F, a.status)) continue;
+        uint8_t *pg = a.pages + id * page_bytes;
+        if (c < cm) reinterpret_cast<uint4 *>(pg + g.meta + 8 * P)[c] = make_uint4(0u, 0u, 0u, 0u);
+        else reinterpret_cast<int2 *>(pg + g.pos + 4 * P)[c - cm] = make_int2(-1, -1);
+      }
     }
     if (lane == 0) reinterpret_cast<int4 *>(a.unit_hdr)[u] = make_int4(inf.n_hi, inf.n_lo, inf.p_hi, p_lo);
     // tails of the last K8V4 and the last K4V2 page
