@@ -21,8 +21,8 @@
 //           this one is read): each row's maximum and sum, online, in log2
 //           units.
 //   pass 2  S^T = K Q^T (A = K, B = Q): one tensor-memory lane per KEY, so
-//           p = exp2(s scale log2e - m_q) / l_q is formed per key row with
-//           the queries' (m, 1 / l) broadcast from shared memory, and the
+//           p = exp2(s scale log2e - m_q - log2 l_q) is formed per key row
+//           with the queries' m + log2 l broadcast from shared memory, and the
 //           key's significance is a plain row sum in fp32 (four column
 //           quarters per key, one atomic each per tile).  P^T, rounded to
 //           bf16, goes to shared memory as rows of keys with the queries
@@ -73,7 +73,7 @@ struct __align__(1024) PrefillSmem {
   // queries], 128-byte swizzle.  Before pass 2 the first holds the pass-1
   // (max, sum) of each row's four column quarters (float2 [4][128]).
   uint8_t pt[kPBuf][kTileBytes];
-  float4 mi[kTile / 2];              // per query pair: (m, m', 1 / l, 1 / l')
+  float nlse[kTile];                 // per query: -(m + log2 l), its normaliser in log2 units
   uint64_t bar_q;                    // Q landed
   uint64_t full[kSlots], empty[kSlots];  // a ring slot landed / was read by its MMAs
   uint64_t bar_s[kSBuf];             // S (or S^T) of a tile computed into buffer b
@@ -507,8 +507,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       }
     }
     // the four column quarters of a row meet: m = max, l = sum of rescaled
-    // sums; then (m, 1 / l) of every row is published for pass 2 (a row
-    // past the request has l = 0 and 1 / l is taken as 0)
+    // sums; then -(m + log2 l) of every row is published for pass 2 (a row
+    // past the request has l = 0 and gets -inf: its probabilities are 0)
     float2(&stat)[4][kTile] = *reinterpret_cast<float2(*)[4][kTile]>(sm.pt[0]);
     stat[cq][row] = make_float2(m, lsum);
     softmax_sync();
@@ -522,15 +522,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) ls += st[c].y * ex2(st[c].x - mx);
       }
-      float *mi = reinterpret_cast<float *>(&sm.mi[row >> 1]);
-      mi[row & 1] = mx == -INFINITY ? 0.0f : mx;
-      mi[2 + (row & 1)] = ls > 0.0f ? 1.0f / ls : 0.0f;
+      sm.nlse[row] = ls > 0.0f ? -(mx + log2f(ls)) : -INFINITY;  // a row past the request: p = 0
     }
     softmax_sync();
     ok = ok && *abort == 0;
 
     // ---- pass 2: S^T of key tile j: this thread's key row, queries
-    // q0 .. q0 + 31.  p = exp2(s sl2 - m_q) / l_q; valid where key <= q < n.
+    // q0 .. q0 + 31.  p = exp2(s sl2 - (m_q + log2 l_q)); valid where
+    // key <= q < n.
     // The row sum is added to the key's significance (four atomics per key
     // and tile, one per column quarter), P^T (bf16) goes to shared memory
     // once P V of the previous tile has read it: key row `row` of query half cq / 2, 16-byte chunks
@@ -550,13 +549,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       uint64_t e[16];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 t = sm.mi[16 * cq + 2 * i];      // queries q0 + 4 i, + 1
-        const float4 u = sm.mi[16 * cq + 2 * i + 1];  // queries q0 + 4 i + 2, + 3
+        const float4 t = reinterpret_cast<const float4 *>(sm.nlse)[8 * cq + i];  // queries q0 + 4 i .. + 3
         float x0, x1, x2, x3;
-        f2_unpack(f2_fma(f2_pack(v[4 * i], v[4 * i + 1]), s2, f2_pack(-t.x, -t.y)), x0, x1);
-        f2_unpack(f2_fma(f2_pack(v[4 * i + 2], v[4 * i + 3]), s2, f2_pack(-u.x, -u.y)), x2, x3);
-        e[2 * i] = f2_mul(f2_pack(ex2(x0), ex2(x1)), f2_pack(t.z, t.w));
-        e[2 * i + 1] = f2_mul(f2_pack(ex2(x2), ex2(x3)), f2_pack(u.z, u.w));
+        f2_unpack(f2_fma(f2_pack(v[4 * i], v[4 * i + 1]), s2, f2_pack(t.x, t.y)), x0, x1);
+        f2_unpack(f2_fma(f2_pack(v[4 * i + 2], v[4 * i + 3]), s2, f2_pack(t.z, t.w)), x2, x3);
+        e[2 * i] = f2_pack(ex2(x0), ex2(x1));
+        e[2 * i + 1] = f2_pack(ex2(x2), ex2(x3));
       }
       if (j == qt || ragged) {
         const int32_t key = j * kTile + row;

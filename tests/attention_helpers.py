@@ -82,8 +82,10 @@ def prefill_bounds(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
 
     Products of bf16 values are exact; the logits are fp32 sums of 128 of them
     on the tensor cores: |dl_ij| <= 64 u scale sum_d |q_id| |k_jd|.  The
-    probabilities then carry rho_ij as in attention_bounds (exponential,
-    normaliser); the outputs are fp32 sums over n keys of p rounded to bf16
+    kernel forms p = 2^(s scale log2e - (m_i + log2 l_i)) with one rounded
+    multiply-add: the exponent adds u |ln p_ij| + u |lse_i| + 2^-23 ln l_i
+    (lse_i = m_i + ln l_i, natural units).  The probabilities then carry
+    rho_ij as in attention_bounds (exponential, normaliser); the outputs are fp32 sums over n keys of p rounded to bf16
     (relative error at most 2^-8 more) times the bf16 v, and a significance
     sum adds n fp32 probabilities in fp32 (atomics in any order).
     Returns (bound on |out| errors [n][128], bound on |sig_sum| errors [n],
@@ -98,8 +100,13 @@ def prefill_bounds(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
     e = np.exp(lg - mx)
     p = e / e.sum(1, keepdims=True)
     dl = 64 * U * scale * (np.abs(q) @ np.abs(k).T)
-    with np.errstate(invalid="ignore"):
-        eta = np.where(mask, dl + U * np.minimum(mx - lg, 200.0) + 2.0 ** -19, 0.0)
+    lsum = e.sum(1, keepdims=True)
+    lse = mx + np.log(lsum)  # the row's normaliser, natural log
+    with np.errstate(invalid="ignore", divide="ignore"):
+        # the exponent s scale log2e - (m + log2 l): rounded once (u |ln p|),
+        # plus the rounding of m + log2 l (u |lse|) and of log2 l (2 ulp)
+        eta = np.where(mask, dl + U * np.minimum(lse - lg, 200.0) + U * np.abs(lse) + 2.0 ** -23 * np.log(lsum)
+                       + 2.0 ** -19, 0.0)
     rho = np.expm1(eta) + np.expm1((p * eta).sum(1, keepdims=True)) + (n + 16) * U
     rho = np.where(mask, rho, 0.0)
     out_b = 2.0 * ((p * (rho + (n + 32) * U + 2.0 ** -8)) @ np.abs(v) + 2.0 ** -24)
