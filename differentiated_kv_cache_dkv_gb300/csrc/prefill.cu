@@ -11,7 +11,7 @@
 // produced; the compaction reads exactly these.
 //
 // One CTA per (128-query tile, request, layer x query head), one per SM:
-// 16 softmax warps, an S-issuing warp, a P V-issuing warp and a copy warp.
+// 8 softmax warps, an S-issuing warp, a P V-issuing warp and a copy warp.
 // Key tiles are 128 keys; Q, K and V tiles are staged by TMA with the
 // 128-byte swizzle, 64 channels per box row, two boxes per 128-channel tile,
 // K and V through a ring of four tile slots.  Two passes, because a key's
@@ -23,15 +23,15 @@
 //   pass 2  S^T = K Q^T (A = K, B = Q): one tensor-memory lane per KEY, so
 //           p = exp2(s scale log2e - m_q - log2 l_q) is formed per key row
 //           with the queries' m + log2 l broadcast from shared memory, and the
-//           key's significance is a plain row sum in fp32 (four column
-//           quarters per key, one atomic each per tile).  P^T, rounded to
+//           key's significance is a plain row sum in fp32 (two column
+//           halves per key, one atomic each per tile).  P^T, rounded to
 //           bf16, goes to shared memory as rows of keys with the queries
 //           contiguous, which is P in the MN-major A form: O += P V with
 //           A = P (MN-major), B = V as it lies in memory (keys x channels:
 //           MN-major), D = O (128 x 128 fp32) in its own tensor-memory
 //           columns.
 // Warp w of the softmax group reads tensor-memory lanes 32 (w mod 4) .. + 31
-// and columns 32 (w div 4) .. + 31 of a tile: four threads per row (pass 1)
+// and columns 64 (w div 4) .. + 63 of a tile: two threads per row (pass 1)
 // or key (pass 2), whose row statistics meet once, after pass 1.  S and P V
 // are issued by separate warps, so P V of a tile never queues behind the
 // wait for a later K tile.
@@ -51,7 +51,10 @@ namespace dkv {
 
 namespace {
 constexpr int kTile = 128;                  // queries per CTA, keys per key tile
-constexpr int kSoftmaxWarps = 16;           // four threads per row or key, 32 columns each
+constexpr int kSoftmaxWarps = 8;            // two threads per row or key
+constexpr int kQuarters = kSoftmaxWarps / 4;  // column groups of a row (warp w: lanes of w mod 4, group w div 4)
+constexpr int kCols = 128 / kQuarters;      // columns of a tile per thread
+static_assert(kCols == 64, "the softmax code below handles 64 columns per thread");
 constexpr int kSWarp = kSoftmaxWarps;       // issues S (or S^T)
 constexpr int kPvWarp = kSoftmaxWarps + 1;  // issues P V, adds the significance
 constexpr int kLoadWarp = kSoftmaxWarps + 2;  // the copy warp
@@ -71,7 +74,7 @@ struct __align__(1024) PrefillSmem {
   uint8_t ring[kSlots][kTileBytes];  // K or V tiles, same two-box form
   // P^T in bf16, kPBuf buffers by key tile: [query half][128 keys][64
   // queries], 128-byte swizzle.  Before pass 2 the first holds the pass-1
-  // (max, sum) of each row's four column quarters (float2 [4][128]).
+  // (max, sum) of each row's column groups (float2 [kQuarters][128]).
   uint8_t pt[kPBuf][kTileBytes];
   float nlse[kTile];                 // per query: -(m + log2 l), its normaliser in log2 units
   uint64_t bar_q;                    // Q landed
@@ -210,6 +213,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&x)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+}
+
+// 64 consecutive fp32 columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, "
+      "%38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, "
+      "%60, %61, %62, %63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]),
+        "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]),
+        "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+        "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
+        "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(r[i]);
 }
 
 // 2^x by the special-function unit (relative error about 2^-22; results
@@ -470,7 +495,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     }
   } else {
     // ================= softmax warps: warp w reads lanes 32 (w mod 4) .. + 31
-    // and columns 32 (w div 4) .. + 31 of each tile
+    // and columns kCols (w div 4) .. + kCols - 1 of each tile
     const int rq = warp & 3, cq = warp >> 2;
     const int row = 32 * rq + lane;  // pass 1: query row; pass 2: key row of the tile
     const int32_t qrow = qt * kTile + row;
@@ -489,38 +514,43 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     for (int32_t j = 0; j < nk; ++j, ++g) {
       if (!(ok = wait(&sm.bar_s[g % kSBuf], (g / kSBuf) & 1u))) break;
       tc_fence_after();
-      float v[32];
-      tmem_ld32(lane_base + kTile * (g % kSBuf) + 32 * cq, v);
+      float v[kCols];
+      tmem_ld64(lane_base + kTile * (g % kSBuf) + kCols * cq, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.bar_sfree[g % kSBuf]);
       if (j == qt || ragged) {
-        const int32_t key0 = j * kTile + 32 * cq;
+        const int32_t key0 = j * kTile + kCols * cq;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = key0 + i <= qlim ? v[i] : -INFINITY;
+        for (int i = 0; i < kCols; ++i) v[i] = key0 + i <= qlim ? v[i] : -INFINITY;
       }
-      const float mn = fmaxf(m, max32(v) * sl2);  // scale > 0: the maximum commutes with it
+      float(&v0)[32] = *reinterpret_cast<float(*)[32]>(&v[0]);
+      float(&v1)[32] = *reinterpret_cast<float(*)[32]>(&v[32]);
+      const float mn = fmaxf(m, fmaxf(max32(v0), max32(v1)) * sl2);  // scale > 0: the maximum commutes with it
       if (mn != -INFINITY) {
-        const float t = exp2_sum32(v, sl2, mn);
+        const float t = exp2_sum32(v0, sl2, mn) + exp2_sum32(v1, sl2, mn);
         lsum = lsum * ex2(m - mn) + t;  // ex2(-inf) = 0 on the first tile
         m = mn;
       }
     }
-    // the four column quarters of a row meet: m = max, l = sum of rescaled
-    // sums; then -(m + log2 l) of every row is published for pass 2 (a row
-    // past the request has l = 0 and gets -inf: its probabilities are 0)
-    float2(&stat)[4][kTile] = *reinterpret_cast<float2(*)[4][kTile]>(sm.pt[0]);
+    // the column groups of a row meet: m = max, l = sum of rescaled sums;
+    // then -(m + log2 l) of every row is published for pass 2 (a row past
+    // the request has l = 0 and gets -inf: its probabilities are 0)
+    float2(&stat)[kQuarters][kTile] = *reinterpret_cast<float2(*)[kQuarters][kTile]>(sm.pt[0]);
     stat[cq][row] = make_float2(m, lsum);
     softmax_sync();
     if (cq == 0) {
-      float2 st[4];
+      float2 st[kQuarters];
+      float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) st[c] = stat[c][row];
-      const float mx = fmaxf(fmaxf(st[0].x, st[1].x), fmaxf(st[2].x, st[3].x));
+      for (int c = 0; c < kQuarters; ++c) {
+        st[c] = stat[c][row];
+        mx = fmaxf(mx, st[c].x);
+      }
       float ls = 0.0f;
       if (mx != -INFINITY) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ls += st[c].y * ex2(st[c].x - mx);
+        for (int c = 0; c < kQuarters; ++c) ls += st[c].y * ex2(st[c].x - mx);
       }
       sm.nlse[row] = ls > 0.0f ? -(mx + log2f(ls)) : -INFINITY;  // a row past the request: p = 0
     }
@@ -528,54 +558,57 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     ok = ok && *abort == 0;
 
     // ---- pass 2: S^T of key tile j: this thread's key row, queries
-    // q0 .. q0 + 31.  p = exp2(s sl2 - (m_q + log2 l_q)); valid where
-    // key <= q < n.
-    // The row sum is added to the key's significance (four atomics per key
-    // and tile, one per column quarter), P^T (bf16) goes to shared memory
-    // once P V of the previous tile has read it: key row `row` of query half cq / 2, 16-byte chunks
-    // 4 (cq mod 2) .. + 3, chunk c stored at c xor (row mod 8) (the 128-byte
-    // swizzle).
-    const int32_t q0 = qt * kTile + 32 * cq;
-    const uint32_t prow = (cq >> 1) * kBox + row * 128;  // this thread's row of a P^T buffer
+    // q0 .. q0 + kCols - 1.  p = exp2(s sl2 - (m_q + log2 l_q)); valid where
+    // key <= q < n.  The row sum is added to the key's significance (one
+    // atomic per thread and tile), P^T (bf16) goes to shared memory once P V
+    // of the tile that last used the buffer has read it: the whole 128-byte
+    // key row `row` of query half cq, 16-byte chunk c stored at
+    // c xor (row mod 8) (the 128-byte swizzle).
+    const int32_t q0 = qt * kTile + kCols * cq;
+    const uint32_t prow = cq * kBox + row * 128;  // this thread's row of a P^T buffer
     const uint64_t s2 = f2_pack(sl2, sl2);
+    const float4 *nl4 = reinterpret_cast<const float4 *>(sm.nlse) + (kCols / 4) * cq;
     for (int32_t j = 0; j < nk && ok; ++j, ++g) {
       if (!(ok = wait(&sm.bar_s[g % kSBuf], (g / kSBuf) & 1u))) break;
       tc_fence_after();
-      float v[32];
-      tmem_ld32(lane_base + kTile * (g % kSBuf) + 32 * cq, v);
+      float v[kCols];
+      tmem_ld64(lane_base + kTile * (g % kSBuf) + kCols * cq, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.bar_sfree[g % kSBuf]);
-      uint64_t e[16];
+      const int32_t key = j * kTile + row;
+      const bool masked = j == qt || ragged;
+      uint32_t w[kCols / 2];
+      float rs = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 t = reinterpret_cast<const float4 *>(sm.nlse)[8 * cq + i];  // queries q0 + 4 i .. + 3
-        float x0, x1, x2, x3;
-        f2_unpack(f2_fma(f2_pack(v[4 * i], v[4 * i + 1]), s2, f2_pack(t.x, t.y)), x0, x1);
-        f2_unpack(f2_fma(f2_pack(v[4 * i + 2], v[4 * i + 3]), s2, f2_pack(t.z, t.w)), x2, x3);
-        e[2 * i] = f2_pack(ex2(x0), ex2(x1));
-        e[2 * i + 1] = f2_pack(ex2(x2), ex2(x3));
-      }
-      if (j == qt || ragged) {
-        const int32_t key = j * kTile + row;
-        const int32_t lo = key - q0, hi = n - q0;  // valid queries: lo <= i < hi
+      for (int c = 0; c < kCols / 32; ++c) {
+        uint64_t e[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 t = nl4[8 * c + i];  // queries q0 + 32 c + 4 i .. + 3
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(v[32 * c + 4 * i], v[32 * c + 4 * i + 1]), s2, f2_pack(t.x, t.y)), x0, x1);
+          f2_unpack(f2_fma(f2_pack(v[32 * c + 4 * i + 2], v[32 * c + 4 * i + 3]), s2, f2_pack(t.z, t.w)), x2, x3);
+          e[2 * i] = f2_pack(ex2(x0), ex2(x1));
+          e[2 * i + 1] = f2_pack(ex2(x2), ex2(x3));
+        }
+        if (masked) {
+          const int32_t lo = key - q0 - 32 * c, hi = n - q0 - 32 * c;  // valid queries: lo <= i < hi
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            f2_unpack(e[i], x0, x1);
+            x0 = (2 * i >= lo && 2 * i < hi) ? x0 : 0.0f;
+            x1 = (2 * i + 1 >= lo && 2 * i + 1 < hi) ? x1 : 0.0f;
+            e[i] = f2_pack(x0, x1);
+          }
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float x0, x1;
           f2_unpack(e[i], x0, x1);
-          x0 = (2 * i >= lo && 2 * i < hi) ? x0 : 0.0f;
-          x1 = (2 * i + 1 >= lo && 2 * i + 1 < hi) ? x1 : 0.0f;
-          e[i] = f2_pack(x0, x1);
+          w[16 * c + i] = bf16x2_rn(x0, x1);
         }
-      }
-      uint32_t w[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float x0, x1;
-        f2_unpack(e[i], x0, x1);
-        w[i] = bf16x2_rn(x0, x1);
-      }
-      {
         uint64_t t[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) t[i] = f2_add(e[i], e[i + 8]);
@@ -585,33 +618,32 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           for (int i = 0; i < wd; ++i) t[i] = f2_add(t[i], t[i + wd]);
         float lo_, hi_;
         f2_unpack(t[0], lo_, hi_);
-        const float rs = lo_ + hi_;
-        const int32_t key = j * kTile + row;
-        if (key < n && rs != 0.0f) atomicAdd(a.sig_sum + (row0 + key) * a.Hq + qh, rs);
+        rs += lo_ + hi_;
       }
+      if (key < n && rs != 0.0f) atomicAdd(a.sig_sum + (row0 + key) * a.Hq + qh, rs);
       // buffer j mod kPBuf is free once P V of tile j - kPBuf has read it
       if (j >= kPBuf && !(ok = wait(&sm.bar_o[j % kPBuf], ((j - kPBuf) / kPBuf) & 1u))) break;
       uint8_t *pb = sm.pt[j % kPBuf] + prow;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<uint4 *>(pb + 16 * ((4 * (cq & 1) + i) ^ (row & 7))) =
+      for (int i = 0; i < kCols / 8; ++i)
+        *reinterpret_cast<uint4 *>(pb + 16 * (i ^ (row & 7))) =
             make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.bar_pready[j % kPBuf]);
     }
 
-    // ---- outputs: this thread's 32 channels of its row of O (the loads are
-    // warp-collective, so every lane takes them; rows past the request store
-    // nothing)
+    // ---- outputs: this thread's kCols channels of its row of O (the loads
+    // are warp-collective, so every lane takes them; rows past the request
+    // store nothing)
     if (ok && wait(&sm.bar_done, 0)) {
       tc_fence_after();
-      float v[32];
-      tmem_ld32(lane_base + kColO + 32 * cq, v);
+      float v[kCols];
+      tmem_ld64(lane_base + kColO + kCols * cq, v);
       if (qrow < n) {
-        float *dst = a.out + ((row0 + qrow) * a.Hq + qh) * 128 + 32 * cq;
+        float *dst = a.out + ((row0 + qrow) * a.Hq + qh) * 128 + kCols * cq;
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
+        for (int i = 0; i < kCols; i += 4)
           *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
       }
     }
