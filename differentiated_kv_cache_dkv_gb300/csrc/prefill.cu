@@ -10,8 +10,11 @@
 // is also where sig_sum[j] = sum_{i >= j} p(i, j) and sig_cnt[j] = N - j are
 // produced; the compaction reads exactly these.
 //
-// One CTA per (128-query tile, request, layer x query head), one per SM:
-// 8 softmax warps, an S-issuing warp, a P V-issuing warp and a copy warp.
+// Persistent: one block per SM walks the work items, a 128-query tile of one
+// (request, layer x query head) each, longest first; every role keeps its
+// pipeline counters running from item to item, so the next item's copies and
+// S MMAs overlap the end of the current one.  A block has 8 softmax warps, an
+// S-issuing warp, a P V-issuing warp and a copy warp.
 // Key tiles are 128 keys; Q, K and V tiles are staged by TMA with the
 // 128-byte swizzle, 64 channels per box row, two boxes per 128-channel tile,
 // K and V through a ring of four tile slots.  Two passes, because a key's
@@ -77,13 +80,14 @@ struct __align__(1024) PrefillSmem {
   // (max, sum) of each row's column groups (float2 [kQuarters][128]).
   uint8_t pt[kPBuf][kTileBytes];
   float nlse[kTile];                 // per query: -(m + log2 l), its normaliser in log2 units
-  uint64_t bar_q;                    // Q landed
+  uint64_t bar_q, bar_qfree;         // the item's Q landed; the S MMAs reading it are done
   uint64_t full[kSlots], empty[kSlots];  // a ring slot landed / was read by its MMAs
   uint64_t bar_s[kSBuf];             // S (or S^T) of a tile computed into buffer b
   uint64_t bar_sfree[kSBuf];         // the softmax warps have read buffer b
   uint64_t bar_pready[kPBuf];        // P^T of a pass-2 tile is in shared-memory buffer b
-  uint64_t bar_o[kPBuf], bar_done;   // P V of a tile from buffer b done; every P V done
-  uint64_t bar_sdone;                // every S done
+  uint64_t bar_o[kPBuf], bar_done;   // P V of a tile from buffer b done; the item's P V done
+  uint64_t bar_ofree;                // the softmax warps have read the item's O
+  uint64_t bar_sdone, bar_pvdone;    // every S, every P V of the block done
   uint32_t tmem;                     // tensor-memory base address from tcgen05.alloc
   int32_t abort;                     // a bounded wait gave up: everyone winds down
   int64_t start;
@@ -199,22 +203,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&x)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
-}
-
 // 64 consecutive fp32 columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
   uint32_t r[64];
@@ -263,11 +251,6 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -348,30 +331,98 @@ __device__ __forceinline__ bool request_start(const PrefillArgs &a, int32_t r, i
   return *ok_sm != 0;
 }
 
+// One work item: a 128-query tile of one (layer, request, query head).
+struct PfItem {
+  int64_t row0;  // (layer, request) token row 0
+  int32_t qt, n, qh, h, nk;
+  bool ragged;   // rows past the request in this tile
+};
+
+// Item i of the longest-first order: the query tile counted from the end of
+// its request slowest, then the request, then layer x query head.  false
+// when the request has no such tile.
+__device__ __forceinline__ bool pf_item(const PrefillArgs &a, int64_t i, PfItem &it) {
+  const int64_t Z = static_cast<int64_t>(a.L) * a.Hq;
+  const int64_t per = static_cast<int64_t>(a.R) * Z;
+  const int32_t qt_rev = static_cast<int32_t>(i / per);
+  const int64_t rest = i - qt_rev * per;
+  const int32_t r = static_cast<int32_t>(rest / Z);
+  const int32_t z = static_cast<int32_t>(rest - static_cast<int64_t>(r) * Z);
+  const int32_t n = __ldg(a.lens + r);
+  const int32_t ntq = (n + kTile - 1) / kTile;
+  if (qt_rev >= ntq) return false;
+  int64_t start = 0;
+  for (int32_t q = 0; q < r; ++q) start += __ldg(a.lens + q);
+  const int32_t l = z / a.Hq;
+  it.qh = z - l * a.Hq;
+  it.h = it.qh / a.G;
+  it.n = n;
+  it.qt = ntq - 1 - qt_rev;
+  it.nk = it.qt + 1;
+  it.ragged = (it.qt + 1) * kTile > n;
+  it.row0 = static_cast<int64_t>(l) * a.T + start;
+  return true;
+}
+
+// Every length must lie in [0, max_len] and they must add up to T; checked
+// by warp 0 before anything is read or written (DKV_E_LENS otherwise).
+// Every thread of the block must call it.
+__device__ __forceinline__ bool lens_valid(const PrefillArgs &a, int32_t *ok_sm) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int64_t total = 0;
+    int bad = 0;
+    for (int32_t q = lane; q < a.R; q += 32) {
+      const int32_t n = __ldg(a.lens + q);
+      if (n < 0 || n > a.max_len) bad = 1;
+      total += n;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      total += __shfl_xor_sync(0xffffffffu, total, o);
+      bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    if (lane == 0) {
+      const bool ok = !bad && total == a.T;
+      *ok_sm = ok ? 1 : 0;
+      if (!ok) set_error(a.status, DKV_E_LENS);
+    }
+  }
+  __syncthreads();
+  return *ok_sm != 0;
+}
+
+// Named barrier of the softmax warps that also reduces a predicate: true in
+// every thread when it was true in any.
+__device__ __forceinline__ bool softmax_sync_or(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred q, o; setp.ne.u32 q, %1, 0; barrier.cta.red.or.pred o, 1, %2, q; selp.u32 %0, 1, 0, o; }"
+      : "=r"(r)
+      : "r"(p ? 1u : 0u), "n"(32 * kSoftmaxWarps)
+      : "memory");
+  return r != 0;
+}
+
+// Persistent: one block per SM walks the work items (pf_item) from blockIdx.x
+// in steps of the grid.  Every role walks the same items and keeps its
+// counters (S buffers, ring copies, P^T buffers, Q and O phases) running
+// across them, so the next item's copies and S MMAs overlap the end of this
+// one.
 __global__ void __launch_bounds__(kThreadsP, 1)
     k_prefill(PrefillArgs a, const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-              const __grid_constant__ CUtensorMap vmap) {
+              const __grid_constant__ CUtensorMap vmap, int64_t n_items) {
   extern __shared__ unsigned char smem_raw[];
   PrefillSmem &sm =
       *reinterpret_cast<PrefillSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int32_t r = blockIdx.y;
-  const int32_t l = static_cast<int32_t>(blockIdx.z / a.Hq), qh = static_cast<int32_t>(blockIdx.z % a.Hq);
-  const int32_t h = qh / a.G;
-  int64_t start = 0;
   // before any allocation: leaving early is safe
-  if (!request_start(a, r, &sm.start, &sm.lens_ok, start)) return;
-  const int32_t n = __ldg(a.lens + r);
-  const int32_t ntq = (n + kTile - 1) / kTile;
-  const int32_t qt = ntq - 1 - static_cast<int32_t>(blockIdx.x);  // longest rows first
-  if (qt < 0) return;
-  const int64_t row0 = static_cast<int64_t>(l) * a.T + start;    // (layer, request) token row 0
-  const int32_t nk = qt + 1;                                       // key tiles the causal rows reach
-  const bool ragged = (qt + 1) * kTile > n;                        // rows past the request in this tile
+  if (!lens_valid(a, &sm.lens_ok)) return;
   volatile int32_t *abort = &sm.abort;
 
   if (tid == 0) {
     mbar_init(&sm.bar_q, 1);
+    mbar_init(&sm.bar_qfree, 1);
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], 1);
@@ -385,7 +436,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       mbar_init(&sm.bar_o[i], 1);
     }
     mbar_init(&sm.bar_done, 1);
+    mbar_init(&sm.bar_ofree, kSoftmaxWarps);
     mbar_init(&sm.bar_sdone, 1);
+    mbar_init(&sm.bar_pvdone, 1);
     sm.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -409,88 +462,116 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     }
     return false;
   };
-  // Tiles g = 0 .. 2 nk - 1: pass 1 (g < nk) key tile g, pass 2 key tile
-  // g - nk; tile g is computed into tensor-memory buffer g mod 3.  Copies
-  // L = 0 .. 3 nk - 1 go to ring slot L mod kSlots: pass 1 K(L); pass 2 K(j)
-  // at nk + 2 j and V(j) at nk + 2 j + 1.
-  const int32_t n_loads = 3 * nk;
+  // Within an item, tiles t = 0 .. 2 nk - 1: pass 1 (t < nk) key tile t,
+  // pass 2 key tile t - nk; the block-wide tile count g picks tensor-memory
+  // buffer g mod 3.  The item's copies go to ring slots by the block-wide
+  // copy count: pass 1 K(t), then pass 2 K(j) and V(j) in turn.
 
   if (warp == kLoadWarp) {
     // ================= copy warp: lane 0 issues; a slot is refilled once
-    // the MMAs that read it have completed
+    // the MMAs that read it have completed, the Q tile once the last S^T of
+    // the previous item has
     if (lane == 0) {
-      load_tile(sm.q, &qmap, qh, static_cast<int>(row0 + qt * kTile), &sm.bar_q);
-      int32_t L = 0;
-      for (; L < n_loads; ++L) {
-        const int s = L % kSlots;
-        if (L >= kSlots && !wait(&sm.empty[s], ((L / kSlots) - 1) & 1u)) break;
-        const bool is_v = L >= nk && ((L - nk) & 1);
-        const int32_t j = L < nk ? L : (L - nk) >> 1;
-        load_tile(sm.ring[s], is_v ? &vmap : &kmap, h, static_cast<int>(row0 + j * kTile), &sm.full[s]);
+      int32_t L = 0, nq = 0;
+      bool ok = true;
+      for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        PfItem it;
+        if (!pf_item(a, i, it)) continue;
+        if (nq > 0 && !(ok = wait(&sm.bar_qfree, (nq - 1) & 1u))) break;
+        load_tile(sm.q, &qmap, it.qh, static_cast<int>(it.row0 + it.qt * kTile), &sm.bar_q);
+        ++nq;
+        for (int32_t p = 0; p < 3 * it.nk; ++p) {
+          const int s = L % kSlots;
+          if (L >= kSlots && !(ok = wait(&sm.empty[s], ((L / kSlots) - 1) & 1u))) break;
+          const bool is_v = p >= it.nk && ((p - it.nk) & 1);
+          const int32_t j = p < it.nk ? p : (p - it.nk) >> 1;
+          load_tile(sm.ring[s], is_v ? &vmap : &kmap, it.h, static_cast<int>(it.row0 + j * kTile), &sm.full[s]);
+          ++L;
+        }
       }
-      // every copy issued has landed before the CTA leaves (bounded)
-      mbar_wait(&sm.bar_q, 0, nullptr);
-      for (int32_t i = max(0, L - kSlots); i < L; ++i) mbar_wait(&sm.full[i % kSlots], (i / kSlots) & 1u, nullptr);
+      // every copy issued has landed before the block leaves (bounded)
+      if (nq > 0) mbar_wait(&sm.bar_q, (nq - 1) & 1u, nullptr);
+      for (int32_t c = max(0, L - kSlots); c < L; ++c) mbar_wait(&sm.full[c % kSlots], (c / kSlots) & 1u, nullptr);
     }
   } else if (warp == kSWarp || warp == kPvWarp) {
     // ================= MMA warps: lane 0 waits and issues.  The S warp runs
-    // S (pass 1) and S^T (pass 2) of tile g into buffer g mod 3 as soon as
-    // the softmax warps have read tile g - 3 and the K tile has landed; the
-    // P V warp runs O += P V of each pass-2 tile once its P^T is in shared
-    // memory.
+    // S (pass 1) and S^T (pass 2) of each tile as soon as its buffer has been
+    // read and its K tile has landed, then hands the Q tile back; the P V
+    // warp runs O += P V of each pass-2 tile once its P^T is in shared
+    // memory (and, for an item's first, once O of the previous item has been
+    // read), then marks the item's O complete.
     const bool leader = lane == 0;
     constexpr uint32_t kSlotStep = kTileBytes >> 4;
-    bool ok = true;
-    if (warp == kSWarp) {
-      if (leader) {
+    if (leader) {
+      int32_t L = 0, k = 0;
+      bool ok = true;
+      if (warp == kSWarp) {
         constexpr uint32_t idesc_s = idesc_bf16(kTile, kTile, false, false);
         // descriptors at the operands' bases; a K-step adds its byte offset / 16
         const uint64_t dq = sw128_desc(saddr(sm.q), 16, 1024);
         const uint64_t dk = sw128_desc(saddr(sm.ring[0]), 16, 1024);  // K-major (K tiles)
-        ok = wait(&sm.bar_q, 0);
-        for (int32_t g = 0; g < 2 * nk && ok; ++g) {
-          const int b = g % kSBuf;
-          if (g >= kSBuf && !(ok = wait(&sm.bar_sfree[b], ((g / kSBuf) - 1) & 1u))) break;
-          const bool pass2 = g >= nk;
-          const int32_t Lk = pass2 ? nk + 2 * (g - nk) : g;
-          if (!(ok = wait(&sm.full[Lk % kSlots], (Lk / kSlots) & 1u))) break;
-          tc_fence_after();
-          const uint64_t dks = dk + (Lk % kSlots) * kSlotStep;
-          const uint64_t da = pass2 ? dks : dq, db = pass2 ? dq : dks;  // S = Q K^T, S^T = K Q^T
+        int32_t g = 0;
+        for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+          PfItem it;
+          if (!pf_item(a, i, it)) continue;
+          if (!(ok = wait(&sm.bar_q, k & 1u))) break;
+          for (int32_t t = 0; t < 2 * it.nk; ++t, ++g) {
+            const int b = g % kSBuf;
+            if (g >= kSBuf && !(ok = wait(&sm.bar_sfree[b], ((g / kSBuf) - 1) & 1u))) break;
+            const bool pass2 = t >= it.nk;
+            const int32_t Lk = L + (pass2 ? it.nk + 2 * (t - it.nk) : t);
+            if (!(ok = wait(&sm.full[Lk % kSlots], (Lk / kSlots) & 1u))) break;
+            tc_fence_after();
+            const uint64_t dks = dk + (Lk % kSlots) * kSlotStep;
+            const uint64_t da = pass2 ? dks : dq, db = pass2 ? dq : dks;  // S = Q K^T, S^T = K Q^T
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // 16 channels a step: 32 bytes along the swizzled rows, then the next box
-            const uint32_t o = ((kk >> 2) * kBox + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + kTile * b, da + o, db + o, idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {  // 16 channels a step: 32 bytes along the swizzled rows, then the next box
+              const uint32_t o = ((kk >> 2) * kBox + (kk & 3) * 32) >> 4;
+              mma_ss(tmem + kTile * b, da + o, db + o, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&sm.bar_s[b]);
+            mma_commit(&sm.empty[Lk % kSlots]);
           }
-          mma_commit(&sm.bar_s[b]);
-          mma_commit(&sm.empty[Lk % kSlots]);
+          if (!ok) break;
+          mma_commit(&sm.bar_qfree);  // the Q tile is free once these MMAs complete
+          L += 3 * it.nk;
+          ++k;
         }
         // every MMA of this warp done (also after an abort)
         mma_commit(&sm.bar_sdone);
         mbar_wait(&sm.bar_sdone, 0, nullptr);
-      }
-    } else {
-      constexpr uint32_t idesc_o = idesc_bf16(kTile, 128, true, true);
-      const uint64_t dv = sw128_desc(saddr(sm.ring[0]), kBox, 1024);  // MN-major (V tiles): boxes kBox apart
-      const uint64_t dp = sw128_desc(saddr(sm.pt[0]), kBox, 1024);    // MN-major (P^T): query halves kBox apart
-      if (leader) {
-        for (int32_t j = 0; j < nk && ok; ++j) {
-          const int32_t Lv = nk + 2 * j + 1;
-          if (!(ok = wait(&sm.bar_pready[j % kPBuf], (j / kPBuf) & 1u) && wait(&sm.full[Lv % kSlots], (Lv / kSlots) & 1u)))
-            break;
-          tc_fence_after();
-          const uint64_t dvs = dv + (Lv % kSlots) * kSlotStep;
-          const uint64_t dps = dp + (j % kPBuf) * kSlotStep;
+      } else {
+        constexpr uint32_t idesc_o = idesc_bf16(kTile, 128, true, true);
+        const uint64_t dv = sw128_desc(saddr(sm.ring[0]), kBox, 1024);  // MN-major (V tiles): boxes kBox apart
+        const uint64_t dp = sw128_desc(saddr(sm.pt[0]), kBox, 1024);    // MN-major (P^T): query halves kBox apart
+        int32_t jj = 0;
+        for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+          PfItem it;
+          if (!pf_item(a, i, it)) continue;
+          for (int32_t j = 0; j < it.nk; ++j, ++jj) {
+            const int32_t Lv = L + it.nk + 2 * j + 1;
+            if (j == 0 && k > 0 && !(ok = wait(&sm.bar_ofree, (k - 1) & 1u))) break;
+            if (!(ok = wait(&sm.bar_pready[jj % kPBuf], (jj / kPBuf) & 1u) &&
+                       wait(&sm.full[Lv % kSlots], (Lv / kSlots) & 1u)))
+              break;
+            tc_fence_after();
+            const uint64_t dvs = dv + (Lv % kSlots) * kSlotStep;
+            const uint64_t dps = dp + (jj % kPBuf) * kSlotStep;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // 16 keys a step: 16 rows (2048 bytes) of P^T and of V
-            mma_ss(tmem + kColO, dps + ((kk * 2048) >> 4), dvs + ((kk * 2048) >> 4), idesc_o,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&sm.bar_o[j % kPBuf]);
-          mma_commit(&sm.empty[Lv % kSlots]);
+            for (int kk = 0; kk < 8; ++kk)  // 16 keys a step: 16 rows (2048 bytes) of P^T and of V
+              mma_ss(tmem + kColO, dps + ((kk * 2048) >> 4), dvs + ((kk * 2048) >> 4), idesc_o,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&sm.bar_o[jj % kPBuf]);
+            mma_commit(&sm.empty[Lv % kSlots]);
+          }
+          if (!ok) break;
+          mma_commit(&sm.bar_done);  // the item's O is complete
+          L += 3 * it.nk;
+          ++k;
         }
         // every MMA of this warp done (also after an abort)
-        mma_commit(&sm.bar_done);
-        mbar_wait(&sm.bar_done, 0, nullptr);
+        mma_commit(&sm.bar_pvdone);
+        mbar_wait(&sm.bar_pvdone, 0, nullptr);
       }
     }
   } else {
@@ -498,159 +579,170 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     // and columns kCols (w div 4) .. + kCols - 1 of each tile
     const int rq = warp & 3, cq = warp >> 2;
     const int row = 32 * rq + lane;  // pass 1: query row; pass 2: key row of the tile
-    const int32_t qrow = qt * kTile + row;
-    // pass 1 masks: a row past the request masks every key (qlim = -1);
-    // masks are applied per element only in the diagonal tile and in a tile
-    // with such rows
-    const int32_t qlim = qrow < n ? qrow : -1;
     const float sl2 = a.scale * 1.44269504088896340736f;  // logits in log2 units
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * rq) << 16);
-    bool ok = true;
-    int32_t g = 0;
-
-    // ---- pass 1: row maximum and sum over this thread's columns (log2
-    // units); the buffer is handed back as soon as it is read
-    float m = -INFINITY, lsum = 0.0f;
-    for (int32_t j = 0; j < nk; ++j, ++g) {
-      if (!(ok = wait(&sm.bar_s[g % kSBuf], (g / kSBuf) & 1u))) break;
-      tc_fence_after();
-      float v[kCols];
-      tmem_ld64(lane_base + kTile * (g % kSBuf) + kCols * cq, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.bar_sfree[g % kSBuf]);
-      if (j == qt || ragged) {
-        const int32_t key0 = j * kTile + kCols * cq;
-#pragma unroll
-        for (int i = 0; i < kCols; ++i) v[i] = key0 + i <= qlim ? v[i] : -INFINITY;
-      }
-      float(&v0)[32] = *reinterpret_cast<float(*)[32]>(&v[0]);
-      float(&v1)[32] = *reinterpret_cast<float(*)[32]>(&v[32]);
-      const float mn = fmaxf(m, fmaxf(max32(v0), max32(v1)) * sl2);  // scale > 0: the maximum commutes with it
-      if (mn != -INFINITY) {
-        const float t = exp2_sum32(v0, sl2, mn) + exp2_sum32(v1, sl2, mn);
-        lsum = lsum * ex2(m - mn) + t;  // ex2(-inf) = 0 on the first tile
-        m = mn;
-      }
-    }
-    // the column groups of a row meet: m = max, l = sum of rescaled sums;
-    // then -(m + log2 l) of every row is published for pass 2 (a row past
-    // the request has l = 0 and gets -inf: its probabilities are 0)
-    float2(&stat)[kQuarters][kTile] = *reinterpret_cast<float2(*)[kQuarters][kTile]>(sm.pt[0]);
-    stat[cq][row] = make_float2(m, lsum);
-    softmax_sync();
-    if (cq == 0) {
-      float2 st[kQuarters];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kQuarters; ++c) {
-        st[c] = stat[c][row];
-        mx = fmaxf(mx, st[c].x);
-      }
-      float ls = 0.0f;
-      if (mx != -INFINITY) {
-#pragma unroll
-        for (int c = 0; c < kQuarters; ++c) ls += st[c].y * ex2(st[c].x - mx);
-      }
-      sm.nlse[row] = ls > 0.0f ? -(mx + log2f(ls)) : -INFINITY;  // a row past the request: p = 0
-    }
-    softmax_sync();
-    ok = ok && *abort == 0;
-
-    // ---- pass 2: S^T of key tile j: this thread's key row, queries
-    // q0 .. q0 + kCols - 1.  p = exp2(s sl2 - (m_q + log2 l_q)); valid where
-    // key <= q < n.  The row sum is added to the key's significance (one
-    // atomic per thread and tile), P^T (bf16) goes to shared memory once P V
-    // of the tile that last used the buffer has read it: the whole 128-byte
-    // key row `row` of query half cq, 16-byte chunk c stored at
-    // c xor (row mod 8) (the 128-byte swizzle).
-    const int32_t q0 = qt * kTile + kCols * cq;
-    const uint32_t prow = cq * kBox + row * 128;  // this thread's row of a P^T buffer
     const uint64_t s2 = f2_pack(sl2, sl2);
     const float4 *nl4 = reinterpret_cast<const float4 *>(sm.nlse) + (kCols / 4) * cq;
-    for (int32_t j = 0; j < nk && ok; ++j, ++g) {
-      if (!(ok = wait(&sm.bar_s[g % kSBuf], (g / kSBuf) & 1u))) break;
-      tc_fence_after();
-      float v[kCols];
-      tmem_ld64(lane_base + kTile * (g % kSBuf) + kCols * cq, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.bar_sfree[g % kSBuf]);
-      const int32_t key = j * kTile + row;
-      const bool masked = j == qt || ragged;
-      uint32_t w[kCols / 2];
-      float rs = 0.0f;
-#pragma unroll
-      for (int c = 0; c < kCols / 32; ++c) {
-        uint64_t e[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 t = nl4[8 * c + i];  // queries q0 + 32 c + 4 i .. + 3
-          float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(v[32 * c + 4 * i], v[32 * c + 4 * i + 1]), s2, f2_pack(t.x, t.y)), x0, x1);
-          f2_unpack(f2_fma(f2_pack(v[32 * c + 4 * i + 2], v[32 * c + 4 * i + 3]), s2, f2_pack(t.z, t.w)), x2, x3);
-          e[2 * i] = f2_pack(ex2(x0), ex2(x1));
-          e[2 * i + 1] = f2_pack(ex2(x2), ex2(x3));
-        }
-        if (masked) {
-          const int32_t lo = key - q0 - 32 * c, hi = n - q0 - 32 * c;  // valid queries: lo <= i < hi
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float x0, x1;
-            f2_unpack(e[i], x0, x1);
-            x0 = (2 * i >= lo && 2 * i < hi) ? x0 : 0.0f;
-            x1 = (2 * i + 1 >= lo && 2 * i + 1 < hi) ? x1 : 0.0f;
-            e[i] = f2_pack(x0, x1);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float x0, x1;
-          f2_unpack(e[i], x0, x1);
-          w[16 * c + i] = bf16x2_rn(x0, x1);
-        }
-        uint64_t t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = f2_add(e[i], e[i + 8]);
-#pragma unroll
-        for (int wd = 4; wd >= 1; wd >>= 1)
-#pragma unroll
-          for (int i = 0; i < wd; ++i) t[i] = f2_add(t[i], t[i + wd]);
-        float lo_, hi_;
-        f2_unpack(t[0], lo_, hi_);
-        rs += lo_ + hi_;
-      }
-      if (key < n && rs != 0.0f) atomicAdd(a.sig_sum + (row0 + key) * a.Hq + qh, rs);
-      // buffer j mod kPBuf is free once P V of tile j - kPBuf has read it
-      if (j >= kPBuf && !(ok = wait(&sm.bar_o[j % kPBuf], ((j - kPBuf) / kPBuf) & 1u))) break;
-      uint8_t *pb = sm.pt[j % kPBuf] + prow;
-#pragma unroll
-      for (int i = 0; i < kCols / 8; ++i)
-        *reinterpret_cast<uint4 *>(pb + 16 * (i ^ (row & 7))) =
-            make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.bar_pready[j % kPBuf]);
-    }
+    const uint32_t prow = cq * kBox + row * 128;  // this thread's row of a P^T buffer
+    bool ok = true;
+    int32_t g = 0, jj = 0, k = 0;
+    for (int64_t i = blockIdx.x; i < n_items; i += gridDim.x) {
+      PfItem it;
+      if (!pf_item(a, i, it)) continue;
+      const int32_t qt = it.qt, n = it.n, nk = it.nk;
+      const bool ragged = it.ragged;
+      const int32_t qrow = qt * kTile + row;
+      // pass 1 masks: a row past the request masks every key (qlim = -1);
+      // masks are applied per element only in the diagonal tile and in a
+      // tile with such rows
+      const int32_t qlim = qrow < n ? qrow : -1;
 
-    // ---- outputs: this thread's kCols channels of its row of O (the loads
-    // are warp-collective, so every lane takes them; rows past the request
-    // store nothing)
-    if (ok && wait(&sm.bar_done, 0)) {
-      tc_fence_after();
-      float v[kCols];
-      tmem_ld64(lane_base + kColO + kCols * cq, v);
-      if (qrow < n) {
-        float *dst = a.out + ((row0 + qrow) * a.Hq + qh) * 128 + kCols * cq;
+      // ---- pass 1: row maximum and sum over this thread's columns (log2
+      // units); the buffer is handed back as soon as it is read
+      float m = -INFINITY, lsum = 0.0f;
+      for (int32_t j = 0; j < nk && ok; ++j, ++g) {
+        if (!(ok = wait(&sm.bar_s[g % kSBuf], (g / kSBuf) & 1u))) break;
+        tc_fence_after();
+        float v[kCols];
+        tmem_ld64(lane_base + kTile * (g % kSBuf) + kCols * cq, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.bar_sfree[g % kSBuf]);
+        if (j == qt || ragged) {
+          const int32_t key0 = j * kTile + kCols * cq;
 #pragma unroll
-        for (int i = 0; i < kCols; i += 4)
-          *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          for (int i2 = 0; i2 < kCols; ++i2) v[i2] = key0 + i2 <= qlim ? v[i2] : -INFINITY;
+        }
+        float(&v0)[32] = *reinterpret_cast<float(*)[32]>(&v[0]);
+        float(&v1)[32] = *reinterpret_cast<float(*)[32]>(&v[32]);
+        const float mn = fmaxf(m, fmaxf(max32(v0), max32(v1)) * sl2);  // scale > 0: the maximum commutes with it
+        if (mn != -INFINITY) {
+          const float t = exp2_sum32(v0, sl2, mn) + exp2_sum32(v1, sl2, mn);
+          lsum = lsum * ex2(m - mn) + t;  // ex2(-inf) = 0 on the first tile
+          m = mn;
+        }
       }
+      // the column groups of a row meet: m = max, l = sum of rescaled sums;
+      // then -(m + log2 l) of every row is published for pass 2 (a row past
+      // the request has l = 0 and gets -inf: its probabilities are 0).  The
+      // second barrier also decides, for every softmax warp alike, whether
+      // the block is winding down.
+      float2(&stat)[kQuarters][kTile] = *reinterpret_cast<float2(*)[kQuarters][kTile]>(sm.pt[0]);
+      stat[cq][row] = make_float2(m, lsum);
+      softmax_sync();
+      if (cq == 0) {
+        float2 st[kQuarters];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kQuarters; ++c) {
+          st[c] = stat[c][row];
+          mx = fmaxf(mx, st[c].x);
+        }
+        float ls = 0.0f;
+        if (mx != -INFINITY) {
+#pragma unroll
+          for (int c = 0; c < kQuarters; ++c) ls += st[c].y * ex2(st[c].x - mx);
+        }
+        sm.nlse[row] = ls > 0.0f ? -(mx + log2f(ls)) : -INFINITY;  // a row past the request: p = 0
+      }
+      if (softmax_sync_or(!ok || *abort != 0)) break;
+
+      // ---- pass 2: S^T of key tile j: this thread's key row, queries
+      // q0 .. q0 + kCols - 1.  p = exp2(s sl2 - (m_q + log2 l_q)); valid
+      // where key <= q < n.  The row sum is added to the key's significance
+      // (one atomic per thread and tile), P^T (bf16) goes to shared memory
+      // once P V of the tile that last used the buffer has read it: the
+      // whole 128-byte key row `row` of query half cq, 16-byte chunk c
+      // stored at c xor (row mod 8) (the 128-byte swizzle).
+      const int32_t q0 = qt * kTile + kCols * cq;
+      for (int32_t j = 0; j < nk && ok; ++j, ++g, ++jj) {
+        if (!(ok = wait(&sm.bar_s[g % kSBuf], (g / kSBuf) & 1u))) break;
+        tc_fence_after();
+        float v[kCols];
+        tmem_ld64(lane_base + kTile * (g % kSBuf) + kCols * cq, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.bar_sfree[g % kSBuf]);
+        const int32_t key = j * kTile + row;
+        const bool masked = j == qt || ragged;
+        uint32_t w[kCols / 2];
+        float rs = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kCols / 32; ++c) {
+          uint64_t e[16];
+#pragma unroll
+          for (int i2 = 0; i2 < 8; ++i2) {
+            const float4 t = nl4[8 * c + i2];  // queries q0 + 32 c + 4 i2 .. + 3
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(v[32 * c + 4 * i2], v[32 * c + 4 * i2 + 1]), s2, f2_pack(t.x, t.y)), x0, x1);
+            f2_unpack(f2_fma(f2_pack(v[32 * c + 4 * i2 + 2], v[32 * c + 4 * i2 + 3]), s2, f2_pack(t.z, t.w)), x2, x3);
+            e[2 * i2] = f2_pack(ex2(x0), ex2(x1));
+            e[2 * i2 + 1] = f2_pack(ex2(x2), ex2(x3));
+          }
+          if (masked) {
+            const int32_t lo = key - q0 - 32 * c, hi = n - q0 - 32 * c;  // valid queries: lo <= i < hi
+#pragma unroll
+            for (int i2 = 0; i2 < 16; ++i2) {
+              float x0, x1;
+              f2_unpack(e[i2], x0, x1);
+              x0 = (2 * i2 >= lo && 2 * i2 < hi) ? x0 : 0.0f;
+              x1 = (2 * i2 + 1 >= lo && 2 * i2 + 1 < hi) ? x1 : 0.0f;
+              e[i2] = f2_pack(x0, x1);
+            }
+          }
+#pragma unroll
+          for (int i2 = 0; i2 < 16; ++i2) {
+            float x0, x1;
+            f2_unpack(e[i2], x0, x1);
+            w[16 * c + i2] = bf16x2_rn(x0, x1);
+          }
+          uint64_t t[8];
+#pragma unroll
+          for (int i2 = 0; i2 < 8; ++i2) t[i2] = f2_add(e[i2], e[i2 + 8]);
+#pragma unroll
+          for (int wd = 4; wd >= 1; wd >>= 1)
+#pragma unroll
+            for (int i2 = 0; i2 < wd; ++i2) t[i2] = f2_add(t[i2], t[i2 + wd]);
+          float lo_, hi_;
+          f2_unpack(t[0], lo_, hi_);
+          rs += lo_ + hi_;
+        }
+        if (key < n && rs != 0.0f) atomicAdd(a.sig_sum + (it.row0 + key) * a.Hq + it.qh, rs);
+        // buffer jj mod kPBuf is free once P V of tile jj - kPBuf has read it
+        if (jj >= kPBuf && !(ok = wait(&sm.bar_o[jj % kPBuf], ((jj - kPBuf) / kPBuf) & 1u))) break;
+        uint8_t *pb = sm.pt[jj % kPBuf] + prow;
+#pragma unroll
+        for (int i2 = 0; i2 < kCols / 8; ++i2)
+          *reinterpret_cast<uint4 *>(pb + 16 * (i2 ^ (row & 7))) =
+              make_uint4(w[4 * i2], w[4 * i2 + 1], w[4 * i2 + 2], w[4 * i2 + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.bar_pready[jj % kPBuf]);
+      }
+
+      // ---- outputs: this thread's kCols channels of its row of O (the
+      // loads are warp-collective, so every lane takes them; rows past the
+      // request store nothing); then O is handed back for the next item
+      if (ok && (ok = wait(&sm.bar_done, k & 1u))) {
+        tc_fence_after();
+        float v[kCols];
+        tmem_ld64(lane_base + kColO + kCols * cq, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.bar_ofree);
+        if (qrow < n) {
+          float *dst = a.out + ((it.row0 + qrow) * a.Hq + it.qh) * 128 + kCols * cq;
+#pragma unroll
+          for (int i2 = 0; i2 < kCols; i2 += 4)
+            *reinterpret_cast<float4 *>(dst + i2) = make_float4(v[i2], v[i2 + 1], v[i2 + 2], v[i2 + 3]);
+        }
+      }
+      ++k;
     }
   }
 
   // ---- teardown: the copy and MMA warps have waited (bounded) for this
-  // CTA's own copies and MMAs; free the tensor memory
+  // block's own copies and MMAs; free the tensor memory
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -707,8 +799,14 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s) {
   if ((e = make_map(&vmap, a.v, rows, a.Hkv)) != cudaSuccess) return e;
   const int smem = static_cast<int>(kPrefillSmem);
   if ((e = cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
-  const dim3 grid((a.max_len + kTile - 1) / kTile, a.R, static_cast<unsigned>(a.L) * a.Hq);
-  k_prefill<<<grid, kThreadsP, smem, s>>>(a, qmap, kmap, vmap);
+  // persistent: one block per SM over every (query tile, request, layer x
+  // head) item, longest first
+  const int64_t n_items = static_cast<int64_t>((a.max_len + kTile - 1) / kTile) * a.R * a.L * a.Hq;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int grid = static_cast<int>(std::min<int64_t>(n_items, std::max(sms, 1)));
+  k_prefill<<<grid, kThreadsP, smem, s>>>(a, qmap, kmap, vmap, n_items);
   return cudaGetLastError();
 }
 
