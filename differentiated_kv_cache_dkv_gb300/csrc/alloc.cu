@@ -236,58 +236,63 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
     const int32_t d = inf.p_hi + p_lo;
     int64_t ring = head_mod + inf.off;
     if (ring >= a.F) ring -= a.F;
+    // id of the unit's page k (-1 past its d pages; -2 where the checked build
+    // finds the ring index or the id out of range: nothing is written for it)
+    auto page_id = [&](int32_t k) -> int32_t {
+      if (k >= d) return -1;
+      int64_t idx = ring + k;
+      if (idx >= a.F) idx -= a.F;
+      if (!in_range(idx, a.F, a.status)) return -2;
+      const int32_t id = __ldg(a.free_list + idx);
+      return in_range(id, a.F, a.status) ? id : -2;
+    };
+    // the last K8V4 and the last K4V2 page, when partly filled (their ids
+    // loaded now, beside the first group's)
+    const int64_t sh = inf.n_hi % P, sl = inf.n_lo % (2 * P);
+    const int32_t id_th = sh != 0 ? page_id(inf.p_hi - 1) : -1;
+    const int32_t id_tl = sl != 0 ? page_id(d - 1) : -1;
+    // forward entries in groups of 32, one per lane; each group's ids are
+    // loaded before the previous group's stores, so the loads overlap
     int32_t *fw = a.fwd + u * a.pmax;
-    for (int k = lane; k < a.pmax; k += 32) {
-      int32_t id = -1;
-      if (k < d) {
-        int64_t idx = ring + k;
-        if (idx >= a.F) idx -= a.F;
-        if (!in_range(idx, a.F, a.status)) continue;
-        id = a.free_list[idx];
-        if (!in_range(id, a.F, a.status)) continue;
+    int32_t id = page_id(lane);
+    for (int32_t k0 = 0; k0 < a.pmax; k0 += 32) {  // d <= pmax
+      const int32_t k = k0 + lane;
+      const int32_t id_next = page_id(k + 32);
+      if (k < a.pmax && id != -2) fw[k] = id;
+      if (id >= 0) {
         a.rev_unit[id] = static_cast<int32_t>(a.unit_base + u);
         a.rev_idx[id] = k;
         a.page_cls[id] = k < inf.p_hi ? DKV_CLASS_K8V4 : DKV_CLASS_K4V2;
       }
-      fw[k] = id;
-    }
-    // a high page has no slots P..2P-1: their metadata (8P bytes: P/2 chunks
-    // of 16) and positions (4P bytes: P/2 chunks of 8; P is even) are
-    // cleared, the chunks spread over the lanes so that consecutive lanes
-    // write consecutive chunks of one page
-    {
-      const int64_t cm = P / 2, cp = P / 2;  // chunks of metadata, of positions
-      const int64_t per = cm + cp;
-      for (int64_t e = lane; e < inf.p_hi * per; e += 32) {
-        const int64_t k = e / per, c = e - k * per;
-        int64_t idx = ring + k;
-        if (idx >= a.F) idx -= a.F;
-        if (!in_range(idx, a.F, a.status)) continue;
-        const int64_t id = a.free_list[idx];
-        if (!in_range(id, a.F, a.status)) continue;
-        uint8_t *pg = a.pages + id * page_bytes;
-        if (c < cm) reinterpret_cast<uint4 *>(pg + g.meta + 8 * P)[c] = make_uint4(0u, 0u, 0u, 0u);
-        else reinterpret_cast<int2 *>(pg + g.pos + 4 * P)[c - cm] = make_int2(-1, -1);
+      // a high page has no slots P..2P-1: their metadata (8P bytes: P/2
+      // chunks of 16) and positions (4P bytes: P/2 chunks of 8; P is even)
+      // are cleared, consecutive lanes writing consecutive chunks of one page
+      // whose id comes from the lane that loaded it
+      const int32_t per = static_cast<int32_t>(P);  // chunks per page
+      const int32_t ne = max(min(inf.p_hi - k0, 32), 0) * per;
+      for (int32_t e0 = 0; e0 < ne; e0 += 32) {  // warp-uniform trip count
+        const int32_t e = e0 + lane;
+        const int32_t pid = __shfl_sync(0xffffffffu, id, min(e / per, 31));
+        if (e < ne && pid >= 0) {
+          uint8_t *pg = a.pages + static_cast<int64_t>(pid) * page_bytes;
+          const int32_t c = e % per;
+          if (c < per / 2) reinterpret_cast<uint4 *>(pg + g.meta + 8 * P)[c] = make_uint4(0u, 0u, 0u, 0u);
+          else reinterpret_cast<int2 *>(pg + g.pos + 4 * P)[c - per / 2] = make_int2(-1, -1);
+        }
       }
+      id = id_next;
     }
     if (lane == 0) reinterpret_cast<int4 *>(a.unit_hdr)[u] = make_int4(inf.n_hi, inf.n_lo, inf.p_hi, p_lo);
     // tails of the last K8V4 and the last K4V2 page
-    const int64_t sh = inf.n_hi % P;
-    int64_t ih = ring + inf.p_hi - 1, il = ring + d - 1;
-    if (ih >= a.F) ih -= a.F;
-    if (il >= a.F) il -= a.F;
-    if (sh != 0 && in_range(ih, a.F, a.status) && in_range(a.free_list[ih], a.F, a.status)) {
-      const int64_t idx = ih;
-      uint8_t *pg = a.pages + static_cast<int64_t>(a.free_list[idx]) * page_bytes;
+    if (id_th >= 0) {
+      uint8_t *pg = a.pages + static_cast<int64_t>(id_th) * page_bytes;
       fill_words(pg + 16 * g.kh * sh, 4 * g.kh * (P - sh), 0u, lane);
       fill_words(pg + g.vbase + 16 * g.vh * sh, 4 * g.vh * (P - sh), 0u, lane);
       fill_words(pg + g.meta + 8 * sh, 2 * (P - sh), 0u, lane);
       fill_words(pg + g.pos + 4 * sh, P - sh, 0xffffffffu, lane);
     }
-    const int64_t sl = inf.n_lo % (2 * P);
-    if (sl != 0 && in_range(il, a.F, a.status) && in_range(a.free_list[il], a.F, a.status)) {
-      const int64_t idx = il;
-      uint8_t *pg = a.pages + static_cast<int64_t>(a.free_list[idx]) * page_bytes;
+    if (id_tl >= 0) {
+      uint8_t *pg = a.pages + static_cast<int64_t>(id_tl) * page_bytes;
       fill_words(pg + 8 * g.kh * sl, 2 * g.kh * (2 * P - sl), 0u, lane);
       fill_words(pg + g.vbase + 8 * g.vh * sl, 2 * g.vh * (2 * P - sl), 0u, lane);
       fill_words(pg + g.meta + 8 * sl, 2 * (2 * P - sl), 0u, lane);

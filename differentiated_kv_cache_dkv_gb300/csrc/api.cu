@@ -202,7 +202,7 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
   a.ws = reinterpret_cast<dkv::WsHeader *>(ws);
   a.tok_off = reinterpret_cast<int64_t *>(ws + lay.tok_off);
   a.tile_off = reinterpret_cast<int32_t *>(ws + lay.tile_off);
-  a.tile_req = reinterpret_cast<int32_t *>(ws + lay.tile_req);
+  a.tile_info = reinterpret_cast<dkv::TileInfo *>(ws + lay.tile_info);
   a.part = reinterpret_cast<uint64_t *>(ws + lay.part);
   a.unit = reinterpret_cast<dkv::UnitInfo *>(ws + lay.unit);
   a.mask = reinterpret_cast<uint32_t *>(ws + lay.mask);
@@ -227,7 +227,7 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
   mark(0);
   if (const int32_t rc = cuda_status(dkv::launch_prep(a, s))) return rc;
   mark(1);
-  if (const int32_t rc = cuda_status(dkv::launch_classify(a, std::max(classify_grid, 1), s))) return rc;
+  if (const int32_t rc = cuda_status(dkv::launch_classify(a, std::max(classify_grid, 1), sms, s))) return rc;
   mark(2);
   if (const int32_t rc = cuda_status(dkv::launch_scan(a, lay.npart, s))) return rc;
   mark(3);

@@ -1,5 +1,6 @@
-// classify.cu -- request prefix sums (k_prep) and the significance reduce +
-// three-tier classification (k_classify).
+// classify.cu -- request prefix sums and per-tile records (k_prep) and the
+// significance reduce + three-tier classification (k_classify_rows for the
+// common head shapes, k_classify otherwise).
 //
 // DiffKV (arXiv 2412.03131), Pith review: a token's significance is the
 // average attention it receives from subsequent tokens, max-aggregated over
@@ -13,6 +14,9 @@
 // sum (and of the minimum sum for a negative count), so each (token, KV head)
 // costs one IEEE division instead of G with bit-identical results.
 #include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
 
 #include "dkv_internal.cuh"
 
@@ -86,10 +90,21 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(CompactArgs a, int32_t np
     if (r < a.R) {
       a.tok_off[r] = before_tok + it - n;
       a.tile_off[r] = before_tile + il - nt;
-      // request of each of its tiles (bounded by the workspace's room)
+      // the request's tiles (bounded by the workspace's room): first token,
+      // size, and the thresholds alpha / N, each an IEEE division done once
       const int64_t room = a.T / kTileTokens + a.R;
-      for (int32_t x = 0; x < nt; ++x)
-        if (before_tile + il - nt + x < room) a.tile_req[before_tile + il - nt + x] = static_cast<int32_t>(r);
+      TileInfo ti;
+      ti.N = static_cast<int32_t>(n);
+      ti.thr_h = __fdiv_rn(a.alpha_h, static_cast<float>(n));
+      ti.thr_l = __fdiv_rn(a.alpha_l, static_cast<float>(n));
+      ti.pad[0] = ti.pad[1] = 0;
+      for (int32_t x = 0; x < nt; ++x) {
+        if (before_tile + il - nt + x >= room) break;
+        const int64_t done = static_cast<int64_t>(x) * kTileTokens;
+        ti.t0 = before_tok + it - n + done;
+        ti.cnt = static_cast<int32_t>(n - done < kTileTokens ? n - done : kTileTokens);
+        a.tile_info[before_tile + il - nt + x] = ti;
+      }
     }
     __syncthreads();
     if (tid == blockDim.x - 1) {
@@ -112,25 +127,72 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(CompactArgs a, int32_t np
   for (int32_t i = tid; i < npart; i += blockDim.x) a.part[i] = 0;
 }
 
-// One tile of a layer: where its scores start and how many tokens it holds.
+// One tile of a layer: where its scores start, how many tokens it holds and
+// its request's thresholds.
 struct ClassifyItem {
-  int64_t l, t0, N;
+  int64_t l, t0;
   int32_t rt, cnt;
+  float thr_h, thr_l;
 };
+
+__device__ __forceinline__ TileInfo load_tile_info(const TileInfo *p) {
+  const int4 x = __ldg(reinterpret_cast<const int4 *>(p));
+  const int4 y = __ldg(reinterpret_cast<const int4 *>(p) + 1);
+  TileInfo t;
+  t.t0 = static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(x.y)) << 32) | static_cast<uint32_t>(x.x));
+  t.cnt = x.z;
+  t.N = x.w;
+  t.thr_h = __int_as_float(y.x);
+  t.thr_l = __int_as_float(y.y);
+  t.pad[0] = t.pad[1] = 0;
+  return t;
+}
 
 __device__ __forceinline__ ClassifyItem classify_item(const CompactArgs &a, int64_t item, int32_t TR) {
   ClassifyItem it;
   it.l = item / TR;
   it.rt = static_cast<int32_t>(item - it.l * TR);
-  const int r = __ldg(a.tile_req + it.rt);
-  const int32_t tr0 = __ldg(a.tile_off + r);
-  const int32_t j = it.rt - tr0;
-  const int64_t tok0 = __ldg(a.tok_off + r);
-  it.N = __ldg(a.tok_off + r + 1) - tok0;
-  it.t0 = tok0 + static_cast<int64_t>(j) * kTileTokens;
-  const int64_t left = it.N - static_cast<int64_t>(j) * kTileTokens;
-  it.cnt = static_cast<int>(left < kTileTokens ? left : kTileTokens);
+  const TileInfo ti = load_tile_info(a.tile_info + it.rt);
+  it.t0 = ti.t0;
+  it.cnt = ti.cnt;
+  it.thr_h = ti.thr_h;
+  it.thr_l = ti.thr_l;
   return it;
+}
+
+// The class of one (token, KV head) from m, the largest summed score over
+// the head's query heads (the smallest when the count n is negative), and n
+// (non-zero).  Reciprocal test: with rc the hardware reciprocal of n (within
+// 1 ulp), y = RN(m * rc) is within 2^-22 (relative) of m / n, so
+// y >= thr (1 + 2^-19) proves RN(m / n) >= thr and y <= thr (1 - 2^-19)
+// proves RN(m / n) < thr (the margins, themselves rounded, stay far from
+// 2^-22); in between, and for thresholds below 2^-100 where a tiny quotient
+// could leave the relative bound, the IEEE division decides.  A NaN fails
+// every test and goes to the division: pruned.
+struct Thresholds {
+  float thr_h, thr_l, hi_h, lo_h, hi_l, lo_l;
+  bool exact_only;
+};
+
+__device__ __forceinline__ Thresholds thresholds(float thr_h, float thr_l) {
+  Thresholds t;
+  t.thr_h = thr_h;
+  t.thr_l = thr_l;
+  t.exact_only = !(thr_l >= 0x1p-100f);
+  t.hi_h = __fmul_rn(thr_h, 1.0f + 0x1p-19f);
+  t.lo_h = __fmul_rn(thr_h, 1.0f - 0x1p-19f);
+  t.hi_l = __fmul_rn(thr_l, 1.0f + 0x1p-19f);
+  t.lo_l = __fmul_rn(thr_l, 1.0f - 0x1p-19f);
+  return t;
+}
+
+__device__ __forceinline__ int classify_score(float m, float cf, float rc, const Thresholds &t) {
+  const float y = __fmul_rn(m, rc);
+  if (!t.exact_only && y >= t.hi_h) return DKV_CLASS_K8V4;
+  if (!t.exact_only && !(y > t.lo_h) && y >= t.hi_l) return DKV_CLASS_K4V2;
+  if (!t.exact_only && !(y > t.lo_h) && !(y > t.lo_l)) return DKV_CLASS_PRUNE;
+  const float s = __fdiv_rn(m, cf);
+  return s >= t.thr_h ? DKV_CLASS_K8V4 : (s >= t.thr_l ? DKV_CLASS_K4V2 : DKV_CLASS_PRUNE);
 }
 
 // Scores held in registers for the next tile (the first kPre float4 per
@@ -175,18 +237,7 @@ __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
   for (; item < items; item += gridDim.x) {
     if (!kVec) cur = classify_item(a, item, TR);
     const int cnt = cur.cnt;
-    const float thr_h = __fdiv_rn(a.alpha_h, static_cast<float>(cur.N));
-    const float thr_l = __fdiv_rn(a.alpha_l, static_cast<float>(cur.N));
-    // Reciprocal test: with rc the hardware reciprocal of n (within 1 ulp),
-    // y = RN(m * rc) is within 2^-22 (relative) of m / n, so y >= thr (1 + 2^-19)
-    // proves RN(m / n) >= thr and y <= thr (1 - 2^-19) proves RN(m / n) < thr
-    // (the margins, themselves rounded, stay far from 2^-22); in between, and
-    // for thresholds below 2^-100 where a tiny quotient could leave the
-    // relative bound, the IEEE division decides.  A NaN fails every test and
-    // goes to the division: pruned.
-    const bool exact_only = !(thr_l >= 0x1p-100f);
-    const float hi_h = __fmul_rn(thr_h, 1.0f + 0x1p-19f), lo_h = __fmul_rn(thr_h, 1.0f - 0x1p-19f);
-    const float hi_l = __fmul_rn(thr_l, 1.0f + 0x1p-19f), lo_l = __fmul_rn(thr_l, 1.0f - 0x1p-19f);
+    const Thresholds thr = thresholds(cur.thr_h, cur.thr_l);
 
     // stage the tile's summed scores [cnt][Hq] into rows padded to Hq + 1
     // floats, so the per-token reads below hit 32 different banks
@@ -253,17 +304,7 @@ __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
           const float cf = static_cast<float>(n);
           float rc;
           asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(cf));
-          const float y = __fmul_rn(m, rc);
-          if (!exact_only && y >= hi_h) {
-            c = DKV_CLASS_K8V4;
-          } else if (!exact_only && !(y > lo_h) && y >= hi_l) {
-            c = DKV_CLASS_K4V2;
-          } else if (!exact_only && !(y > lo_h) && !(y > lo_l)) {
-            c = DKV_CLASS_PRUNE;
-          } else {
-            const float s = __fdiv_rn(m, cf);
-            c = s >= thr_h ? DKV_CLASS_K8V4 : (s >= thr_l ? DKV_CLASS_K4V2 : DKV_CLASS_PRUNE);
-          }
+          c = classify_score(m, cf, rc, thr);
         }
         cls_s[k * a.Hkv + h] = static_cast<uint8_t>(c);
       }
@@ -290,6 +331,260 @@ __global__ void __launch_bounds__(kClassifyThreads) k_classify(CompactArgs a) {
   }
 }
 
+// The same classification with one thread per token, for the head shapes of
+// common models (Hq and G known at compile time).  A warp takes 32
+// consecutive tokens of one tile (a quarter), so one ballot per KV head is
+// one word of that unit tile's class mask, and streams its quarters through
+// a private ring of kRowStages shared-memory buffers: one lane starts a bulk
+// asynchronous copy of the quarter's summed scores (32 contiguous rows of Hq
+// floats) that completes on the stage's mbarrier, kRowStages quarters ahead
+// of their use.  Each lane then reads its own token's row from shared memory,
+// reduces it per KV head, classifies, and stores the token's Hkv class bytes
+// as words.  Rows of 8 or 16 float4 chunks would put a warp's reads of one
+// chunk in one bank group, so those lanes take the KV heads in a rotated
+// order (lane i starts at head i).
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+constexpr int kRowWarps = kClassifyThreads / 32;
+constexpr int64_t kRowWaitLimit = 1ll << 24;  // polls of one mbarrier before giving up
+
+__host__ __device__ constexpr int row_stages(int hq) { return kRowWarps * 3 * 128 * hq <= 100 * 1024 ? 3 : 2; }
+__host__ __device__ constexpr size_t rows_smem(int hq) {
+  return static_cast<size_t>(kRowWarps) * row_stages(hq) * (128 * hq + sizeof(uint64_t) + sizeof(TileInfo));
+}
+
+__device__ __forceinline__ bool row_wait(uint64_t *bar, uint32_t parity) {
+  const uint32_t addr = smem_u32(bar);
+  for (int64_t i = 0; i < kRowWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+template <int HQ, int G>
+__global__ void __launch_bounds__(kClassifyThreads) k_classify_rows(CompactArgs a) {
+  constexpr int HKV = HQ / G, NV = HQ / 4, NW = (HKV + 3) / 4, S = row_stages(HQ);
+  constexpr bool kRotate = NV % 8 == 0 && G % 4 == 0 && (HKV & (HKV - 1)) == 0;
+  static_assert(HQ % 4 == 0 && HQ % G == 0, "rows of whole 16-byte chunks, whole KV heads");
+  static_assert(HKV <= 16, "the 2-bit classes of every KV head in one word");
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float *buf = reinterpret_cast<float *>(smem) + static_cast<size_t>(warp) * S * 32 * HQ;  // [S][32][HQ]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(kRowWarps) * S * 128 * HQ) + warp * S;
+  TileInfo *tinf = reinterpret_cast<TileInfo *>(smem + static_cast<size_t>(kRowWarps) * S * (128 * HQ + 8)) +
+                   warp * S;
+  if (a.ws->err != 0) return;
+  if (lane == 0) {
+    for (int st = 0; st < S; ++st)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + st)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  const int32_t TR = a.ws->TR;
+  const int64_t items = static_cast<int64_t>(a.L) * TR * kMaskWords;  // (layer, tile, quarter)
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kRowWarps;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kRowWarps + warp;
+  const int64_t nmine = first < items ? (items - first + nw - 1) / nw : 0;
+  if (nmine == 0) return;
+  // The warp's items first, first + nw, ... as (layer, tile quarter) pairs,
+  // stepped without a division per item: three cursors (the quarter in use,
+  // the next to copy, the one after it, whose tile record is loaded early).
+  const int32_t nq = TR * kMaskWords;  // quarters per layer
+  const int64_t dl = nw / nq;
+  const int32_t dq = static_cast<int32_t>(nw - dl * nq);
+  struct Cursor {
+    int64_t l;
+    int32_t tq;  // rt * kMaskWords + q
+  };
+  auto step = [&](Cursor &c) {
+    c.l += dl;
+    c.tq += dq;
+    if (c.tq >= nq) {
+      c.tq -= nq;
+      ++c.l;
+    }
+  };
+  Cursor use{first / nq, static_cast<int32_t>(first % nq)};
+  Cursor put = use, ahead_c = use;
+  // quarter c of this warp into stage st: lane 0 records its tile and starts
+  // the copy (a bare arrive when the quarter lies past the tile's end); every
+  // lane loads its token's count
+  int32_t cn[S];
+  auto issue = [&](const Cursor &c, int st, const TileInfo &ti) -> int32_t {
+    const int q = c.tq % kMaskWords;
+    const int nvalid = min(max(ti.cnt - 32 * q, 0), 32);
+    if (lane == 0) {
+      tinf[st] = ti;
+      const uint32_t b = smem_u32(bars + st);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (nvalid > 0) {
+        const uint32_t bytes = static_cast<uint32_t>(nvalid) * HQ * 4u;
+        const float *src = a.sig_sum + (c.l * a.T + ti.t0 + 32 * q) * HQ;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         smem_u32(buf + static_cast<size_t>(st) * 32 * HQ)),
+                     "l"(src), "r"(bytes), "r"(b)
+                     : "memory");
+      } else {
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
+      }
+    }
+    return lane < nvalid ? __ldg(a.sig_cnt + ti.t0 + 32 * q + lane) : 0;
+  };
+#pragma unroll
+  for (int st = 0; st < S; ++st) {
+    cn[st] = 0;
+    if (st < nmine) {
+      cn[st] = issue(put, st, load_tile_info(a.tile_info + put.tq / kMaskWords));
+      step(put);
+    }
+  }
+  ahead_c = put;
+  TileInfo ahead = S < nmine ? load_tile_info(a.tile_info + ahead_c.tq / kMaskWords) : TileInfo{};
+  __syncwarp();
+
+  const bool words = HKV % 4 == 0 && (reinterpret_cast<uintptr_t>(a.classes) & 3) == 0;
+  int64_t m = 0;
+  bool ok = true;
+  for (; m < nmine; ++m) {
+    const int st = static_cast<int>(m % S);
+    if (!__all_sync(0xffffffffu, row_wait(bars + st, static_cast<uint32_t>((m / S) & 1)))) {
+      ok = false;
+      break;
+    }
+    const int64_t l = use.l;
+    const int q = use.tq % kMaskWords;
+    const int32_t rt = use.tq / kMaskWords;
+    step(use);
+    const TileInfo ti = tinf[st];
+    const int32_t n = cn[0];
+#pragma unroll
+    for (int i = 0; i + 1 < S; ++i) cn[i] = cn[i + 1];
+    const int k = 32 * q + lane;
+    const bool valid = k < ti.cnt;
+    const Thresholds thr = thresholds(ti.thr_h, ti.thr_l);
+    const float cf = static_cast<float>(n);
+    float rc;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(cf));
+    const float *rowp = buf + static_cast<size_t>(st) * 32 * HQ + lane * HQ;
+    auto classify_head = [&](const float *v) -> int {
+      if (n == 0) return DKV_CLASS_K8V4;  // not yet observed: keep at high precision
+      float mx = v[0];
+      if (n > 0) {
+#pragma unroll
+        for (int g = 1; g < G; ++g) mx = fmaxf(mx, v[g]);
+      } else {
+#pragma unroll
+        for (int g = 1; g < G; ++g) mx = fminf(mx, v[g]);
+      }
+      return classify_score(mx, cf, rc, thr);
+    };
+    uint32_t cls2 = 0;  // 2-bit class of every KV head
+    if (valid) {
+      if (kRotate) {
+#pragma unroll
+        for (int s = 0; s < HKV; ++s) {
+          const int hh = (s + lane) & (HKV - 1);
+          float v[G];
+#pragma unroll
+          for (int j = 0; j < G / 4; ++j) {
+            const float4 x4 = reinterpret_cast<const float4 *>(rowp + hh * G)[j];
+            v[4 * j] = x4.x;
+            v[4 * j + 1] = x4.y;
+            v[4 * j + 2] = x4.z;
+            v[4 * j + 3] = x4.w;
+          }
+          cls2 |= static_cast<uint32_t>(classify_head(v)) << (2 * hh);
+        }
+      } else {
+        float x[HQ];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          const float4 x4 = reinterpret_cast<const float4 *>(rowp)[j];
+          x[4 * j] = x4.x;
+          x[4 * j + 1] = x4.y;
+          x[4 * j + 2] = x4.z;
+          x[4 * j + 3] = x4.w;
+        }
+#pragma unroll
+        for (int h = 0; h < HKV; ++h) cls2 |= static_cast<uint32_t>(classify_head(x + h * G)) << (2 * h);
+      }
+    }
+    __syncwarp();  // every lane is done with the stage: refill it
+    if (m + S < nmine) {
+      cn[S - 1] = issue(put, st, ahead);
+      step(put);
+      step(ahead_c);
+      if (m + S + 1 < nmine) ahead = load_tile_info(a.tile_info + ahead_c.tq / kMaskWords);
+    }
+    uint32_t mh = 0, ml = 0;  // lane h < HKV: word q of head h's masks
+    uint32_t cw[NW];
+#pragma unroll
+    for (int w = 0; w < NW; ++w) cw[w] = 0;
+#pragma unroll
+    for (int h = 0; h < HKV; ++h) {
+      const uint32_t c = (cls2 >> (2 * h)) & 3u;  // PRUNE (0) for the lanes past the tile's end
+      const uint32_t hi = __ballot_sync(0xffffffffu, c == DKV_CLASS_K8V4);
+      const uint32_t lo = __ballot_sync(0xffffffffu, c == DKV_CLASS_K4V2);
+      if (lane == h) {
+        mh = hi;
+        ml = lo;
+      }
+      cw[h / 4] |= c << (8 * (h % 4));
+    }
+    if (lane < HKV) {
+      uint32_t *mk = a.mask + ((l * HKV + lane) * TR + rt) * (2 * kMaskWords);
+      mk[q] = mh;
+      mk[kMaskWords + q] = ml;
+    }
+    if (valid) {
+      uint8_t *dst = a.classes + (l * a.T + ti.t0 + k) * HKV;
+      if (words && NW == 2 && (reinterpret_cast<uintptr_t>(a.classes) & 7) == 0) {
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(cw[0], cw[NW - 1]);
+      } else if (words) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) reinterpret_cast<uint32_t *>(dst)[w] = cw[w];
+      } else {
+#pragma unroll
+        for (int h = 0; h < HKV; ++h) dst[h] = static_cast<uint8_t>(cw[h / 4] >> (8 * (h % 4)));
+      }
+    }
+  }
+  if (!ok) {  // a copy never completed: record it, wait (bounded) for the ones in flight, stop
+    if (lane == 0) set_error(&a.ws->err, DKV_E_TIMEOUT);
+    for (int64_t r = m; r < min(nmine, m + S); ++r) row_wait(bars + r % S, static_cast<uint32_t>((r / S) & 1));
+  }
+}
+
+template <int HQ, int G>
+cudaError_t launch_rows(const CompactArgs &a, int sms, cudaStream_t s) {
+  static std::atomic<int> bps{0};  // resident blocks per SM, queried once
+  constexpr size_t smem = rows_smem(HQ);
+  if (bps.load() == 0) {
+    cudaError_t e = cudaFuncSetAttribute(k_classify_rows<HQ, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_classify_rows<HQ, G>, kClassifyThreads, smem);
+    if (e != cudaSuccess) return e;
+    bps.store(n > 0 ? n : 1);
+  }
+  const int64_t items = static_cast<int64_t>(a.L) * (a.T / kTileTokens + a.R) * kMaskWords;
+  const int64_t want = (items + kRowWarps - 1) / kRowWarps;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * bps.load())));
+  k_classify_rows<HQ, G><<<grid, kClassifyThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 size_t classify_smem(int Hq, int Hkv) {
   return sizeof(float) * kTileTokens * (Hq + 1) + sizeof(int32_t) * kTileTokens + kTileTokens * Hkv;
 }
@@ -302,17 +597,27 @@ cudaError_t launch_prep(const CompactArgs &a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_classify(const CompactArgs &a, int grid, cudaStream_t s) {
-  const size_t smem = classify_smem(a.Hq, a.Hkv);
-  const bool vec = (a.Hq % 4) == 0;
-  if (smem > 48 * 1024) {
-    const int limit = static_cast<int>(smem);
-    cudaError_t e = vec ? cudaFuncSetAttribute(k_classify<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit)
-                        : cudaFuncSetAttribute(k_classify<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
-    if (e != cudaSuccess) return e;
+cudaError_t launch_classify(const CompactArgs &a, int grid, int sms, cudaStream_t s) {
+  // the head shapes with a per-token kernel: (Hq, G) of Llama-3 8B / 70B,
+  // Qwen2.5 7B / 32B, and a small grouped shape
+  const int hq = a.Hq, g = a.G;
+  if (hq == 32 && g == 4) return launch_rows<32, 4>(a, sms, s);
+  if (hq == 64 && g == 8) return launch_rows<64, 8>(a, sms, s);
+  if (hq == 28 && g == 7) return launch_rows<28, 7>(a, sms, s);
+  if (hq == 40 && g == 5) return launch_rows<40, 5>(a, sms, s);
+  if (hq == 12 && g == 4) return launch_rows<12, 4>(a, sms, s);
+  {
+    const size_t smem = classify_smem(a.Hq, a.Hkv);
+    const bool vec = (a.Hq % 4) == 0;
+    if (smem > 48 * 1024) {
+      const int limit = static_cast<int>(smem);
+      cudaError_t e = vec ? cudaFuncSetAttribute(k_classify<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit)
+                          : cudaFuncSetAttribute(k_classify<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+      if (e != cudaSuccess) return e;
+    }
+    if (vec) k_classify<true><<<grid, kClassifyThreads, smem, s>>>(a);
+    else k_classify<false><<<grid, kClassifyThreads, smem, s>>>(a);
   }
-  if (vec) k_classify<true><<<grid, kClassifyThreads, smem, s>>>(a);
-  else k_classify<false><<<grid, kClassifyThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 

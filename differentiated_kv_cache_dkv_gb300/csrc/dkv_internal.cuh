@@ -6,7 +6,8 @@
 //             numbers the (request, tile) pairs, TR = sum_r ceil(N_r / tile).
 //             A "unit tile" is a tile of one unit, numbered
 //             tau = (l * Hkv + h) * TR + rt, so a unit's tiles are contiguous
-//             and tile_req[rt] = r decodes tau without a search.
+//             and tile_info[rt] (first token, size, request length and
+//             thresholds) decodes tau without a search.
 //
 // Kernels, in stream order (all bounded, none traps):
 //   k_prep      1 block: request prefix sums, length validation, resets
@@ -96,11 +97,21 @@ struct __align__(16) TileDesc {
   int32_t pad;
 };
 
+// One (request, tile) pair, written by k_prep: what the classification of
+// its tokens needs, in one 32-byte record.
+struct __align__(16) TileInfo {
+  int64_t t0;          // first token of the tile in the layer's token order
+  int32_t cnt;         // tokens in the tile (1 .. kTileTokens)
+  int32_t N;           // tokens of its request
+  float thr_h, thr_l;  // alpha_h / N and alpha_l / N, each rounded once
+  int32_t pad[2];
+};
+
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
   size_t tok_off;    // int64 [R + 1]
   size_t tile_off;   // int32 [R + 1]
-  size_t tile_req;   // int32 [tr_max]: request of each (request, tile) pair
+  size_t tile_info;  // TileInfo [tr_max]: one per (request, tile) pair
   size_t part;       // uint64 [npart]
   size_t unit;       // UnitInfo [U]
   size_t mask;       // uint32 [NT][2 * kMaskWords]: K8V4 words then K4V2 words
@@ -121,7 +132,7 @@ inline WsLayout ws_layout(int64_t L, int64_t R, int64_t Hkv, int64_t T) {
   size_t o = align256(sizeof(WsHeader));
   w.tok_off = o;  o = align256(o + sizeof(int64_t) * (R + 1));
   w.tile_off = o; o = align256(o + sizeof(int32_t) * (R + 1));
-  w.tile_req = o; o = align256(o + sizeof(int32_t) * tr_max);
+  w.tile_info = o; o = align256(o + sizeof(TileInfo) * tr_max);
   w.part = o;     o = align256(o + sizeof(uint64_t) * w.npart);
   w.unit = o;     o = align256(o + sizeof(UnitInfo) * U);
   w.mask = o;     o = align256(o + sizeof(uint32_t) * 2 * kMaskWords * w.nt_max);
@@ -151,7 +162,7 @@ struct CompactArgs {
   WsHeader *ws;
   int64_t *tok_off;
   int32_t *tile_off;
-  int32_t *tile_req;
+  TileInfo *tile_info;
   uint64_t *part;
   UnitInfo *unit;
   uint32_t *mask;
@@ -353,7 +364,7 @@ struct PrefillArgs {
 // Launchers (defined in the kernel translation units).
 namespace dkv {
 cudaError_t launch_prep(const CompactArgs &a, cudaStream_t s);
-cudaError_t launch_classify(const CompactArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_classify(const CompactArgs &a, int grid, int sms, cudaStream_t s);
 cudaError_t launch_scan(const CompactArgs &a, int npart, cudaStream_t s);
 cudaError_t launch_pack(const CompactArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_commit(const CompactArgs &a, int grid, cudaStream_t s);
