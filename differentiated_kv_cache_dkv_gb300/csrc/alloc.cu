@@ -24,7 +24,7 @@ namespace dkv {
 
 namespace {
 
-constexpr int kScanThreads = 256;
+constexpr int kScanThreads = 1024;  // one warp per unit of the partition
 constexpr int kCommitThreads = 256;
 
 __device__ __forceinline__ void st_release(uint64_t *p, uint64_t v) {

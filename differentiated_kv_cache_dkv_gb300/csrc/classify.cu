@@ -90,21 +90,6 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(CompactArgs a, int32_t np
     if (r < a.R) {
       a.tok_off[r] = before_tok + it - n;
       a.tile_off[r] = before_tile + il - nt;
-      // the request's tiles (bounded by the workspace's room): first token,
-      // size, and the thresholds alpha / N, each an IEEE division done once
-      const int64_t room = a.T / kTileTokens + a.R;
-      TileInfo ti;
-      ti.N = static_cast<int32_t>(n);
-      ti.thr_h = __fdiv_rn(a.alpha_h, static_cast<float>(n));
-      ti.thr_l = __fdiv_rn(a.alpha_l, static_cast<float>(n));
-      ti.pad[0] = ti.pad[1] = 0;
-      for (int32_t x = 0; x < nt; ++x) {
-        if (before_tile + il - nt + x >= room) break;
-        const int64_t done = static_cast<int64_t>(x) * kTileTokens;
-        ti.t0 = before_tok + it - n + done;
-        ti.cnt = static_cast<int32_t>(n - done < kTileTokens ? n - done : kTileTokens);
-        a.tile_info[before_tile + il - nt + x] = ti;
-      }
     }
     __syncthreads();
     if (tid == blockDim.x - 1) {
@@ -112,6 +97,31 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(CompactArgs a, int32_t np
       carry_tile = before_tile + il;
     }
     __syncthreads();
+  }
+  // every tile's record (bounded by the workspace's room), one thread per
+  // tile: its request by bisection of the tile offsets written above, first
+  // token, size, and the thresholds alpha / N, each an IEEE division
+  {
+    const int64_t room = a.T / kTileTokens + a.R;
+    const int64_t ntiles = carry_tile < room ? carry_tile : room;
+    for (int64_t x = tid; x < ntiles; x += blockDim.x) {
+      int lo = 0, hi = a.R - 1;  // the last request whose first tile is <= x
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.tile_off[mid] <= x) lo = mid; else hi = mid - 1;
+      }
+      const int64_t tok0 = a.tok_off[lo];
+      const int64_t n = static_cast<int64_t>(a.lens[lo]) < 0 ? 0 : a.lens[lo];
+      const int64_t done = (x - a.tile_off[lo]) * kTileTokens;
+      TileInfo ti;
+      ti.t0 = tok0 + done;
+      ti.cnt = static_cast<int32_t>(n - done < kTileTokens ? n - done : kTileTokens);
+      ti.N = static_cast<int32_t>(n);
+      ti.thr_h = __fdiv_rn(a.alpha_h, static_cast<float>(n));
+      ti.thr_l = __fdiv_rn(a.alpha_l, static_cast<float>(n));
+      ti.pad[0] = ti.pad[1] = 0;
+      a.tile_info[x] = ti;
+    }
   }
   if (tid == 0) {
     a.tok_off[a.R] = carry_tok;

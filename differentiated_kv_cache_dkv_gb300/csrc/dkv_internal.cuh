@@ -58,7 +58,7 @@ __host__ __device__ inline PageGeom page_geom(int scheme, int32_t P) {
 
 constexpr int kTileTokens = 128;                 // tokens per tile
 constexpr int kMaskWords = kTileTokens / 32;     // 32-bit words per class mask
-constexpr int kScanUnits = 128;                  // units per scan partition
+constexpr int kScanUnits = 32;                   // units per scan partition
 constexpr int kMaxHq = 128;                      // query heads supported
 
 // Call-local state at the start of the workspace.
