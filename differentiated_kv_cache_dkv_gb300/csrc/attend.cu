@@ -682,39 +682,59 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
     }
   }
 
-  // ---- significance: add each token's probability to its row.  Thread
-  // (t0, g) = (tid / G, tid % G) takes head g of tokens t0, t0 + T, ...
-  // (T = threads / G), so a warp's stores are consecutive; eight in flight.
+  // ---- significance: add each token's probability to its row.
   if (a.sig_sum != nullptr && !failed) {
-    constexpr int kB = 8;
     const int64_t row0 = (static_cast<int64_t>(a.layer0 + li) * a.R + r) * a.cap;
     const int32_t nloc = c1 - c0;
-    const int T = kAttendThreads / G;
-    const int t0 = threadIdx.x / G, g = threadIdx.x - t0 * G;
-    const float lsum = gL[g < G ? g : 0];
-    const float linv = lsum > 0.0f ? 1.0f / lsum : 0.0f, mg = gM[g < G ? g : 0];
-    if (t0 < T) {
-      for (int tb = t0; tb < nloc; tb += kB * T) {
-        float *dst[kB];
-        float old[kB];
+    // one block owns each (position, head) of the call, so an add in the
+    // memory system (no value returned: nothing waits on it) equals the
+    // read-add-write; the new token's row is set, not added to
+    if (G == 4 && (reinterpret_cast<uintptr_t>(a.sig_sum) & 15) == 0) {
+      // a token's four heads are 16 contiguous bytes: one vector add
+      float mg[4], linv[4];
 #pragma unroll
-        for (int i = 0; i < kB; ++i) {
-          const int t = tb + i * T;
-          dst[i] = nullptr;
-          old[i] = 0.0f;
-          if (t >= nloc) continue;
+      for (int g = 0; g < 4; ++g) {
+        mg[g] = gM[g];
+        linv[g] = gL[g] > 0.0f ? 1.0f / gL[g] : 0.0f;
+      }
+      for (int t = threadIdx.x; t < nloc; t += kAttendThreads) {
+        const int32_t pos = ps[t];
+        if (pos == -1) continue;  // a token whose page id was rejected
+        if (pos < 0 || pos >= a.cap) {
+          set_error(a.status, DKV_E_INTERNAL);
+          continue;
+        }
+        float *dst = a.sig_sum + (row0 + pos) * a.Hq + static_cast<int64_t>(h) * 4;
+        const float4 l4 = *reinterpret_cast<const float4 *>(lg + t * 4);
+        const float p0 = __expf(l4.x - mg[0]) * linv[0], p1 = __expf(l4.y - mg[1]) * linv[1];
+        const float p2 = __expf(l4.z - mg[2]) * linv[2], p3 = __expf(l4.w - mg[3]) * linv[3];
+        if (c0 + t < n_held)
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(p0), "f"(p1), "f"(p2),
+                       "f"(p3)
+                       : "memory");
+        else
+          *reinterpret_cast<float4 *>(dst) = make_float4(p0, p1, p2, p3);
+      }
+    } else {
+      // thread (t0, g) = (tid / G, tid % G) takes head g of tokens t0,
+      // t0 + T, ... (T = threads / G), so a warp's adds are consecutive
+      const int T = kAttendThreads / G;
+      const int t0 = threadIdx.x / G, g = threadIdx.x - t0 * G;
+      const float lsum = gL[g < G ? g : 0];
+      const float linv = lsum > 0.0f ? 1.0f / lsum : 0.0f, mg = gM[g < G ? g : 0];
+      if (t0 < T) {
+        for (int t = t0; t < nloc; t += T) {
           const int32_t pos = ps[t];
-          if (pos == -1) continue;  // a token whose page id was rejected
+          if (pos == -1) continue;
           if (pos < 0 || pos >= a.cap) {
             set_error(a.status, DKV_E_INTERNAL);
             continue;
           }
-          dst[i] = a.sig_sum + (row0 + pos) * a.Hq + static_cast<int64_t>(h) * G + g;
-          if (c0 + t < n_held) old[i] = __ldcg(dst[i]);  // the new token's row is set, not added to
+          float *dst = a.sig_sum + (row0 + pos) * a.Hq + static_cast<int64_t>(h) * G + g;
+          const float pv = __expf(lg[t * G + g] - mg) * linv;
+          if (c0 + t < n_held) atomicAdd(dst, pv);
+          else *dst = pv;
         }
-#pragma unroll
-        for (int i = 0; i < kB; ++i)
-          if (dst[i] != nullptr) *dst[i] = fmaf(__expf(lg[(tb + i * T) * G + g] - mg), linv, old[i]);
       }
     }
   }
