@@ -264,53 +264,67 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
   // 4j + g/2, part g & 1, channels 32t .. 32t + 31 (both orders above).  As a
   // D operand it holds head 4j + t: its scale and channel sum.
   const int64_t qrow = (static_cast<int64_t>(li) * a.R + r) * a.Hq + static_cast<int64_t>(h) * G;
-  uint32_t bh[NT][8][2], bl[NT][8][2];
+  // the same for every warp of the block: warp 0 forms them into shared
+  // memory (lane-major, so each lane's 8-byte read is conflict-free)
+  __shared__ uint2 frag_h[NT][8][32], frag_l[NT][8][32];  // K8V4 / K4V2 channel orders
+  __shared__ float frag_sum[NT][4], frag_inv[NT][4];      // per D-operand head 4j + t
+  if (warp == 0) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int hb = 4 * j + (gq >> 1), part = gq & 1;
+      float qv[32];
+      float mx = 0.0f, sm = 0.0f;
+      if (hb < G) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.q + (qrow + hb) * 128 + 32 * tq);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = __ldg(src + k);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) qv[8 * k + e] = bf16_at(w, e);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) qv[e] = 0.0f;
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        mx = fmaxf(mx, fabsf(qv[e]));
+        sm += qv[e];
+      }
+#pragma unroll
+      for (int off = 1; off < 4; off <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+        sm += __shfl_xor_sync(kFull, sm, off);
+      }
+      // head scale: max |q| into [2^14, 2^15)
+      const int ex = mx > 0.0f ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xff) - 127 : 0;
+      const int ke = min(max(14 - ex, -100), 100);
+      const float sc = pow2f(ke);
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) {
+        const float *x = qv + 4 * kc;  // channels 32t + 4kc + {0, 1, 2, 3}
+        frag_h[j][kc][lane] = make_uint2(pack2(f16part(x[0] * sc, part), f16part(x[1] * sc, part)),
+                                         pack2(f16part(x[2] * sc, part), f16part(x[3] * sc, part)));
+        frag_l[j][kc][lane] = make_uint2(pack2(f16part(x[0] * sc, part), f16part(x[2] * sc, part)),
+                                         pack2(f16part(x[1] * sc * 0.0625f, part), f16part(x[3] * sc * 0.0625f, part)));
+      }
+      // the D-operand head 4j + t is the B-operand head of lane 8t
+      const float qs = __shfl_sync(kFull, sm, 8 * tq);
+      const float qi = pow2f(-__shfl_sync(kFull, ke, 8 * tq)) * 16777216.0f;  // undoes 2^ke and the codes' 2^-24
+      if (gq == 0) {
+        frag_sum[j][tq] = qs;
+        frag_inv[j][tq] = qi;
+      }
+    }
+  }
+  __syncthreads();  // fw, barriers, query fragments
   float qsum[NT], qinv[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    const int hb = 4 * j + (gq >> 1), part = gq & 1;
-    float qv[32];
-    float mx = 0.0f, sm = 0.0f;
-    if (hb < G) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(a.q + (qrow + hb) * 128 + 32 * tq);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 v = __ldg(src + k);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qv[8 * k + e] = bf16_at(w, e);
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) qv[e] = 0.0f;
-    }
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      mx = fmaxf(mx, fabsf(qv[e]));
-      sm += qv[e];
-    }
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-      sm += __shfl_xor_sync(kFull, sm, off);
-    }
-    // head scale: max |q| into [2^14, 2^15)
-    const int ex = mx > 0.0f ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xff) - 127 : 0;
-    const int ke = min(max(14 - ex, -100), 100);
-    const float sc = pow2f(ke);
-#pragma unroll
-    for (int kc = 0; kc < 8; ++kc) {
-      const float *x = qv + 4 * kc;  // channels 32t + 4kc + {0, 1, 2, 3}
-      bh[j][kc][0] = pack2(f16part(x[0] * sc, part), f16part(x[1] * sc, part));
-      bh[j][kc][1] = pack2(f16part(x[2] * sc, part), f16part(x[3] * sc, part));
-      bl[j][kc][0] = pack2(f16part(x[0] * sc, part), f16part(x[2] * sc, part));
-      bl[j][kc][1] = pack2(f16part(x[1] * sc * 0.0625f, part), f16part(x[3] * sc * 0.0625f, part));
-    }
-    // the D-operand head 4j + t is the B-operand head of lane 8t
-    qsum[j] = __shfl_sync(kFull, sm, 8 * tq);
-    qinv[j] = pow2f(-__shfl_sync(kFull, ke, 8 * tq)) * 16777216.0f;  // undoes 2^ke and the 2^-24 of the codes
+    qsum[j] = frag_sum[j][tq];
+    qinv[j] = frag_inv[j][tq];
   }
-  __syncthreads();  // fw, barriers initialised
 
   // page item q of this block: kind, page id, first token index, used slots
   auto item = [&](int32_t q, int &kind, int32_t &pid, int32_t &tok0, int32_t &ntok) {
@@ -402,7 +416,10 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
             const uint32_t a0 = __byte_perm(x0[kc], 0, 0x4140), a2 = __byte_perm(x0[kc], 0, 0x4342);
             const uint32_t a1 = __byte_perm(x1[kc], 0, 0x4140), a3 = __byte_perm(x1[kc], 0, 0x4342);
 #pragma unroll
-            for (int j = 0; j < NT; ++j) mma((kc & 1) ? c2[j] : c[j], a0, a1, a2, a3, bh[j][kc][0], bh[j][kc][1]);
+            for (int j = 0; j < NT; ++j) {
+              const uint2 f = frag_h[j][kc][lane];
+              mma((kc & 1) ? c2[j] : c[j], a0, a1, a2, a3, f.x, f.y);
+            }
           }
         } else {
           const uint4 y0 = *reinterpret_cast<const uint4 *>(pg + r0 * 64 + 16 * tq);
@@ -415,7 +432,10 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
             const uint32_t a0 = e0 & 0x000F000Fu, a2 = e0 & 0x00F000F0u;
             const uint32_t a1 = e1 & 0x000F000Fu, a3 = e1 & 0x00F000F0u;
 #pragma unroll
-            for (int j = 0; j < NT; ++j) mma((kc & 1) ? c2[j] : c[j], a0, a1, a2, a3, bl[j][kc][0], bl[j][kc][1]);
+            for (int j = 0; j < NT; ++j) {
+              const uint2 f = frag_l[j][kc][lane];
+              mma((kc & 1) ? c2[j] : c[j], a0, a1, a2, a3, f.x, f.y);
+            }
           }
         }
 #pragma unroll
