@@ -236,11 +236,11 @@ __device__ __forceinline__ void quant16(const uint4 &a, const uint4 &b, float z,
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     fast_pair(w[i], z, rr, mm, q.b[2 * i], q.b[2 * i + 1]);
-    // zero iff either channel's 13 fraction bits are all zero (the product
-    // of two 13-bit values fits 26 bits)
-    flag = min(flag, (q.b[2 * i] & 8191u) * (q.b[2 * i + 1] & 8191u));
+    // the two channels' 13 fraction bits side by side in 16-bit halves: a
+    // half of the running minimum becomes zero once a fraction is zero
+    flag = __vminu2(flag, __byte_perm(q.b[2 * i], q.b[2 * i + 1], 0x5410) & 0x1fff1fffu);
   }
-  if (flag == 0u || r < 0.0f) {
+  if ((flag & 0xffffu) == 0u || (flag >> 16) == 0u || r < 0.0f) {
     const uint4 e = exact16(a, b, z, r, s, n);
     const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
@@ -260,6 +260,12 @@ __device__ __forceinline__ uint32_t pack_codes(const Bits16 &q, int first) {
     w |= x & (((1u << kWidth) - 1u) << (kWidth * i));
   }
   return w;
+}
+
+// Four 8-bit codes (bits 13..20 of each y) into one word by byte permutes.
+__device__ __forceinline__ uint32_t pack8x4(const Bits16 &q, int first) {
+  const uint32_t c0 = q.b[first] >> 13, c1 = q.b[first + 1] >> 13, c2 = q.b[first + 2] >> 13, c3 = q.b[first + 3] >> 13;
+  return __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040), 0x5410);
 }
 
 // Quantise a lane's 32 K and 32 V channels of one row and store their packed
@@ -290,8 +296,8 @@ __device__ __forceinline__ void store_row(uint8_t *pg, int32_t P, int32_t slot_,
     quant16(a, b, z, r, s, static_cast<float>((1 << width) - 1), q);
     uint8_t *d = isv ? vd : kd;
     if (width == 8) {
-      *reinterpret_cast<uint2 *>(d + 8 * c) = make_uint2(pack_codes<8, 4>(q, 0), pack_codes<8, 4>(q, 4));
-      *reinterpret_cast<uint2 *>(d + 8 * c2) = make_uint2(pack_codes<8, 4>(q, 8), pack_codes<8, 4>(q, 12));
+      *reinterpret_cast<uint2 *>(d + 8 * c) = make_uint2(pack8x4(q, 0), pack8x4(q, 4));
+      *reinterpret_cast<uint2 *>(d + 8 * c2) = make_uint2(pack8x4(q, 8), pack8x4(q, 12));
     } else if (width == 4) {
       *reinterpret_cast<uint32_t *>(d + 4 * c) = pack_codes<4, 8>(q, 0);
       *reinterpret_cast<uint32_t *>(d + 4 * c2) = pack_codes<4, 8>(q, 8);
