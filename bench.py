@@ -520,7 +520,10 @@ def run_native_decode(a):
 
     prof = libdkv.Profiler(a.steps)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
-    live_rows, new_rows, scored = 0, 0, 0
+    # the step's row counts, summed on the device so that the timed loop never
+    # waits on the host (a read-back here would leave the GPU idle before
+    # every step's first launch)
+    cnt_t = torch.zeros(3, dtype=torch.int64, device=dev)  # live rows, new rows, scored tokens
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -529,15 +532,15 @@ def run_native_decode(a):
     torch.cuda.synchronize()
     for i in range(a.steps):
         upd, d = inputs(step_no)
-        live_rows += int((ctx["ctx_lens"] + upd["new_lens"]).sum()) * w.L * w.Hkv
-        new_rows += int(upd["new_lens"].sum()) * w.L * w.Hkv
+        cnt_t[0] += (ctx["ctx_lens"] + upd["new_lens"]).sum()
+        cnt_t[1] += upd["new_lens"].sum()
         # tokens whose significance the step reads: outside the window (mode
         # 0), or the one leaving it (mode 1), plus a classified new token
         nl = ctx["ctx_lens"] + upd["new_lens"]
         if a.decode_mode == 0:
-            scored += int((nl - a.window).clamp(min=0).sum())
+            cnt_t[2] += (nl - a.window).clamp(min=0).sum()
         else:
-            scored += int(((ctx["ctx_lens"] - a.window >= 0) & (upd["new_lens"] > 0)).sum())
+            cnt_t[2] += ((ctx["ctx_lens"] - a.window >= 0) & (upd["new_lens"] > 0)).sum()
         evs[i][0].record(stream)
         dec.step(d, w.alpha_h, w.alpha_l, profiler=prof)
         evs[i][1].record(stream)
@@ -549,6 +552,9 @@ def run_native_decode(a):
     clk = clocks.stop()
     st = libdkv.dkv_get_status(dec.pool)
     assert st == libdkv.DKV_OK, libdkv.status_string(st)
+    live_rows = int(cnt_t[0]) * w.L * w.Hkv
+    new_rows = int(cnt_t[1]) * w.L * w.Hkv
+    scored = int(cnt_t[2])
     ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
     kt = prof.read()
     prof.close()

@@ -326,16 +326,16 @@ def decode_update_inputs(w: Workload, ctx: dict, step: int, seed: int | None = N
         upd = torch.where(u < p_prune, torch.zeros_like(s),
                           torch.where(u < p_prune + p_demote, mid * cntf, s + s / cntf))
         s.copy_(torch.where(live[:, :, None, None], upd, s))
-    tok = torch.nonzero(live.reshape(-1)).squeeze(1)
-    cnt[tok] += 1
-    # the new token of every request
+    cnt += live.reshape(-1).to(cnt.dtype)
+    # the new token of every request (no host round trip: a full request's
+    # slot index points at its last position, which keeps its values)
     g = _gen(seed * 1000003 + 900000 + step, device)
     room = clen < cap                                   # a full request takes no new token
-    newpos = (torch.arange(R, device=device) * cap + clen)[room]
+    newpos = torch.arange(R, device=device) * cap + clen.clamp(max=cap - 1)
     z = torch.randn((L, R, Hq), generator=g, device=device, dtype=torch.float64)
     wt = torch.exp(w.sigma * z - w.sigma ** 2 / 2) / (clen + 1).to(torch.float64)[None, :, None]
-    sig[:, newpos] = wt[:, room].to(torch.float32)
-    cnt[newpos] = 1
+    sig[:, newpos] = torch.where(room[None, :, None], wt.to(torch.float32), sig[:, newpos])
+    cnt[newpos] = torch.where(room, torch.ones_like(cnt[newpos]), cnt[newpos])
     kv = Workload(w.name, L=1, Hq=Hq, Hkv=Hkv, lens=[R], P=w.P, alpha_h=w.alpha_h, alpha_l=w.alpha_l,
                   n_outlier=w.n_outlier, outlier_scale=w.outlier_scale)
     k_new = torch.stack([make_kv_layer(kv, seed + 77 * step + 1, l, 0, device) for l in range(L)])
