@@ -218,6 +218,8 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
   float *bF = gL + kAttendMaxG;  // [8 blocks][8 heads]: exp(block max - cluster max)
 
   __shared__ int failed;  // a warp gave up on a copy: the significance update is skipped
+  __shared__ float nlg_s[kAttendMaxG];  // the new token's logit per query head
+  __shared__ float vnew_s[128];         // and its V row
   if (threadIdx.x == 0) failed = 0;
   if (lane == 0) {
     for (int s = 0; s < kNS; ++s) bar_init(bars + s);
@@ -589,6 +591,34 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
     for (int32_t q = n; q < min(nmine, n + kNS); ++q) bar_wait(bars + q % kNS, (q / kNS) & 1);
   }
 
+  // ---- the step's new token, when this block holds it: its logits and its V
+  // row, formed by the last warp as soon as its own pages are done (others may
+  // still be streaming), so the merge below finds them in shared memory
+  const bool own_new = has_new && n_held >= c0 && n_held < c1;
+  const int64_t new_row = ((static_cast<int64_t>(li) * a.R + r) * a.Hkv + h) * 128;
+  if (own_new && warp == kWarps - 1) {
+    constexpr int kG = 4 * NT;  // query heads a block can hold
+    const uint2 kk = __ldg(reinterpret_cast<const uint2 *>(a.k_new + new_row) + lane);  // channels 4 lane ..
+    const uint2 vv = __ldg(reinterpret_cast<const uint2 *>(a.v_new + new_row) + lane);
+    uint2 qq[kG];
+#pragma unroll
+    for (int g = 0; g < kG; ++g)
+      qq[g] = g < G ? __ldg(reinterpret_cast<const uint2 *>(a.q + (qrow + g) * 128) + lane) : make_uint2(0u, 0u);
+    const uint32_t kw[2] = {kk.x, kk.y}, vw[2] = {vv.x, vv.y};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) vnew_s[4 * lane + e] = bf16_at(vw, e);
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      const uint32_t qw[2] = {qq[g].x, qq[g].y};
+      float d = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d = fmaf(bf16_at(qw, e), bf16_at(kw, e), d);
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) d += __shfl_xor_sync(kFull, d, off);
+      if (lane == 0 && g < G) nlg_s[g] = a.scale * d;
+    }
+  }
+
   // ---- merge the warp's lanes (same head: lanes of equal t), then the block's warps
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
@@ -636,41 +666,26 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
   }
 
   // ---- the new token (last in the unit's order): one more term of the block's merge
-  if (has_new && n_held >= c0 && n_held < c1) {
-    const int64_t new_row = ((static_cast<int64_t>(li) * a.R + r) * a.Hkv + h) * 128;
+  if (own_new) {
     __syncthreads();
-    if (warp == 0) {
-      uint32_t kw[2];
-      const uint2 kk = __ldg(reinterpret_cast<const uint2 *>(a.k_new + new_row) + lane);  // channels 4 lane ..
-      kw[0] = kk.x;
-      kw[1] = kk.y;
+    if (threadIdx.x == 0) {
       for (int g = 0; g < G; ++g) {
-        const uint2 qq = __ldg(reinterpret_cast<const uint2 *>(a.q + (qrow + g) * 128) + lane);
-        const uint32_t qw[2] = {qq.x, qq.y};
-        float d = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) d = fmaf(bf16_at(qw, e), bf16_at(kw, e), d);
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) d += __shfl_xor_sync(kFull, d, off);
-        if (lane == 0) {
-          const float x = a.scale * d;
-          lg[(n_held - c0) * G + g] = x;
-          const float mx = fmaxf(bM[g], x);
-          const float fo = bM[g] == -INFINITY ? 0.0f : expf(bM[g] - mx);
-          const float fn = expf(x - mx);
-          bL[g] = bL[g] * fo + fn;
-          bM[g] = mx;
-          wm[g] = fo;  // reused: factors for the outputs below
-          wl[g] = fn;
-        }
+        const float x = nlg_s[g];
+        lg[(n_held - c0) * G + g] = x;
+        const float mx = fmaxf(bM[g], x);
+        const float fo = bM[g] == -INFINITY ? 0.0f : expf(bM[g] - mx);
+        const float fn = expf(x - mx);
+        bL[g] = bL[g] * fo + fn;
+        bM[g] = mx;
+        wm[g] = fo;  // reused: factors for the outputs below
+        wl[g] = fn;
       }
-      if (lane == 0) ps[n_held - c0] = ctx;
+      ps[n_held - c0] = ctx;
     }
     __syncthreads();
     for (int e = threadIdx.x; e < G * 128; e += kAttendThreads) {
       const int g = e >> 7, d = e & 127;
-      const uint16_t vb = a.v_new[new_row + d];
-      red[e] = fmaf(wl[g], __uint_as_float(static_cast<uint32_t>(vb) << 16), red[e] * wm[g]);
+      red[e] = fmaf(wl[g], vnew_s[d], red[e] * wm[g]);
     }
   }
   cluster.sync();  // 1: every block's (max, sum, output) is final
