@@ -690,17 +690,33 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
   }
   cluster.sync();  // 1: every block's (max, sum, output) is final
 
-  // ---- merge the cluster's blocks
+  // ---- merge the cluster's blocks.  The remote reads of every rank are
+  // issued together (S <= 8, unrolled), so the merge waits for one
+  // distributed-shared-memory round trip, not one per rank.
   if (threadIdx.x < G) {
     const int g = threadIdx.x;
+    float mq[8], lq[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      mq[q] = -INFINITY;
+      lq[q] = 0.0f;
+      if (q < S) {
+        mq[q] = cluster.map_shared_rank(bM, q)[g];
+        lq[q] = cluster.map_shared_rank(bL, q)[g];
+      }
+    }
     float mx = -INFINITY;
-    for (int q = 0; q < S; ++q) mx = fmaxf(mx, cluster.map_shared_rank(bM, q)[g]);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < S) mx = fmaxf(mx, mq[q]);
     float sum = 0.0f;
-    for (int q = 0; q < S; ++q) {
-      const float mq = cluster.map_shared_rank(bM, q)[g];
-      const float f = mq > -INFINITY ? expf(mq - mx) : 0.0f;
-      sum = fmaf(cluster.map_shared_rank(bL, q)[g], f, sum);
-      bF[q * kAttendMaxG + g] = f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (q < S) {
+        const float f = mq[q] > -INFINITY ? expf(mq[q] - mx) : 0.0f;
+        sum = fmaf(lq[q], f, sum);
+        bF[q * kAttendMaxG + g] = f;
+      }
     }
     gM[g] = mx;
     gL[g] = sum;
@@ -710,8 +726,13 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
     float *out = a.out + qrow * 128;
     for (int e = threadIdx.x; e < G * 128; e += kAttendThreads) {
       const int g = e >> 7;
+      float part[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) part[q] = q < S ? cluster.map_shared_rank(red, q)[e] : 0.0f;
       float sum = 0.0f;
-      for (int q = 0; q < S; ++q) sum = fmaf(cluster.map_shared_rank(red, q)[e], bF[q * kAttendMaxG + g], sum);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < S) sum = fmaf(part[q], bF[q * kAttendMaxG + g], sum);
       const float lsum = gL[g];
       out[e] = lsum > 0.0f ? __fdiv_rn(sum, lsum) : 0.0f;
     }
