@@ -22,8 +22,8 @@
 //     lazily when it grows by more than 8), and
 //   - accumulates the weighted values on the tensor cores (codes x p s_v).
 // The warps of a block, then the blocks of the cluster (distributed shared
-// memory), merge (max, sum, output); rank 0 writes the outputs and every block
-// adds its tokens' probabilities to their significance rows.
+// memory), merge (max, sum, output); each rank writes a share of the outputs,
+// and every block adds its tokens' probabilities to their significance rows.
 //
 // Arithmetic: with codes c, scale s and zero z of a row,
 //   q . k   = s (q . c) + z (sum of q),
@@ -722,9 +722,11 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
     gL[g] = sum;
   }
   __syncthreads();
-  if (rank == 0) {
+  {  // every rank writes its share of the outputs
     float *out = a.out + qrow * 128;
-    for (int e = threadIdx.x; e < G * 128; e += kAttendThreads) {
+    const int per = (G * 128 + S - 1) / S;
+    const int e1 = min(G * 128, (rank + 1) * per);
+    for (int e = rank * per + threadIdx.x; e < e1; e += kAttendThreads) {
       const int g = e >> 7;
       float part[8];
 #pragma unroll
