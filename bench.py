@@ -752,8 +752,9 @@ def run_native_attention(a):
     # new tokens' K and V; queries and outputs; the forward rows and headers
     # read; each attended position's G significance sums read and written
     pages_used = int(hdr[:, 2].sum() + hdr[:, 3].sum())
-    alg = (n_hi * (128 + 64 + 8 + 4) + n_lo * (64 + 32 + 8 + 4) + n_new * 512 + w.L * w.R * w.Hq * (256 + 512)
-           + pages_used * 4 + w.U * 16 + rows * G * 8)
+    kv = scheme_bits(w.scheme)  # K + V bits of the high class; the low class has half
+    alg = (n_hi * (16 * kv + 12) + n_lo * (8 * kv + 12) + n_new * 512
+           + w.L * w.R * w.Hq * (256 + 512) + pages_used * 4 + w.U * 16 + rows * G * 8)
 
     def call():
         dec.attend(q, ctx["ctx_lens"], out, ATTN_SCALE, k_new=k_new, v_new=v_new, new_lens=new_lens, sig_sum=sig)

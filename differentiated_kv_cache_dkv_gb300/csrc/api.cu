@@ -319,7 +319,6 @@ int32_t dkv_decode_attention(const dkv_attn_batch *b, const dkv_pool *pool, cons
   if (!b || !valid_pool(pool) || !t || !t->fwd || !t->unit_hdr || !aligned(t->unit_hdr, 16) ||
       !aligned(t->fwd, 4) || t->pmax < 2)
     return DKV_E_INVAL;
-  if (pool->scheme != DKV_SCHEME_K8V4_K4V2) return DKV_E_INVAL;  // the attention kernel reads K8V4/K4V2 pages
   if (b->L < 1 || b->R < 0 || b->Hkv < 1 || b->Hq < b->Hkv || b->Hq % b->Hkv != 0 ||
       b->Hq / b->Hkv > dkv::kAttendMaxG || b->cap < 1 || b->layer0 < 0 || b->n_layers < 0 ||
       b->layer0 + static_cast<int64_t>(b->n_layers) > b->L || !std::isfinite(b->scale))
@@ -350,6 +349,7 @@ int32_t dkv_decode_attention(const dkv_attn_batch *b, const dkv_pool *pool, cons
   dkv::AttnArgs a{};
   a.L = b->L; a.R = b->R; a.Hq = b->Hq; a.Hkv = b->Hkv; a.G = G; a.P = pool->P; a.pmax = t->pmax;
   a.cap = b->cap; a.layer0 = b->layer0; a.n_layers = b->n_layers; a.cmax = cmax;
+  a.scheme = pool->scheme;
   a.F = pool->F; a.units = units; a.scale = b->scale;
   a.q = static_cast<const uint16_t *>(b->q);
   a.k_new = static_cast<const uint16_t *>(b->k_new);

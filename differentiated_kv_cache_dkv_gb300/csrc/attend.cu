@@ -42,6 +42,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "dkv_internal.cuh"
 
@@ -84,30 +85,42 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // One lane: expect `bytes` on `bar` and start the copies of a page's used
-// regions into `dst` (K8V4: codes + metadata [0, 200P) and positions; K4V2:
-// the whole page).  Sizes and addresses are multiples of 16 bytes.
+// regions into `dst`: a high-class page its codes and the metadata of its P
+// slots, then its positions; a low-class page the whole page.  For scheme SC
+// the codes take 16 (kh + vh) P bytes (K8V4/K4V2: [0, 192P)).  Sizes and
+// addresses are multiples of 16 bytes.
+template <int SC>
 __device__ __forceinline__ void fetch_page(uint8_t *dst, const uint8_t *src, int kind, int P, uint64_t *bar) {
+  constexpr uint32_t KH = scheme_kh(SC), VH = scheme_vh(SC);
+  const uint32_t meta = 16u * (KH + VH) * P, pos = meta + 16u * P;
   const uint32_t b = saddr(bar);
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   if (kind == 1) {
-    const uint32_t n0 = 200u * P, n1 = (4u * P + 15u) & ~15u;
+    const uint32_t n0 = meta + 8u * P, n1 = (4u * P + 15u) & ~15u;
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(n0 + n1) : "memory");
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      saddr(dst)),
                  "l"(src), "r"(n0), "r"(b)
                  : "memory");
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     saddr(dst + 208 * P)),
-                 "l"(src + 208 * P), "r"(n1), "r"(b)
+                     saddr(dst + pos)),
+                 "l"(src + pos), "r"(n1), "r"(b)
                  : "memory");
   } else {
-    const uint32_t n = 216u * P;
+    const uint32_t n = meta + 24u * P;
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(n) : "memory");
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      saddr(dst)),
                  "l"(src), "r"(n), "r"(b)
                  : "memory");
   }
+}
+
+// Code i (of W bits) of a little-endian run of words; i a constant after
+// unrolling, so the word and the shift are too.
+template <int W>
+__device__ __forceinline__ uint32_t code_at_w(const uint32_t *x, int i) {
+  return (x[(i * W) >> 5] >> ((i * W) & 31)) & ((1u << W) - 1u);
 }
 
 // ---------------------------------------------------------- tensor cores --
@@ -173,6 +186,9 @@ __device__ __forceinline__ uint32_t sel_pair(int b) { return b | (b << 4) | ((4 
 //            consecutive channels 16 g ..): K8V4 low / high nibble of byte
 //            mt of the lane's 8 bytes, K4V2 crumbs 2 (mt & 1), +1 of byte
 //            mt / 2 of its 4 bytes.
+// The other bit-width schemes (K8V2/K4V1, K4V8/K2V4) take one code per
+// half by shift and mask, in the K8V4 channel order for the logits and the
+// value order above for the outputs, at their own widths (1, 2, 4 or 8 bits).
 // fp32 inputs become two fp16 parts (nearest, then the remainder) in two
 // columns, so the products carry 22 bits of them; query heads are scaled by
 // a power of two into fp16 range, and the weights p s_v by the power of two
@@ -186,8 +202,10 @@ __device__ __forceinline__ T unrot(const T (&z)[4], int t, int i) {
   return k == 0 ? z[0] : (k == 1 ? z[1] : (k == 2 ? z[2] : z[3]));
 }
 
-template <int NT>  // n-tiles of four query heads (G <= 4 NT)
+// NT: n-tiles of four query heads (G <= 4 NT); SC: the pool's bit-width scheme
+template <int NT, int SC>
 __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_sm(4 * NT)) k_attend(AttnArgs a) {
+  constexpr int KH = scheme_kh(SC), VH = scheme_vh(SC);  // high-class K and V widths (the low class: half)
   constexpr int kWarps = attend_warps(4 * NT);
   constexpr int kAttendThreads = 32 * kWarps;
   cg::cluster_group cluster = cg::this_cluster();
@@ -204,7 +222,10 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
 
   extern __shared__ __align__(128) uint8_t smem[];
   const AttnLayout lay = attend_layout(a.cmax, G, a.pmax, P);
-  const int32_t pbytes = 216 * P;
+  const int32_t pbytes = 216 * P;  // a ring slot: the largest page of any scheme
+  // the scheme's page: K codes [0, vbase), V codes [vbase, moff), metadata, positions
+  const int32_t vbase = 16 * KH * P, moff = 16 * (KH + VH) * P, poff = moff + 16 * P;
+  const int64_t gbytes = moff + 24 * static_cast<int64_t>(P);
   uint8_t *stage = smem + lay.stage + static_cast<size_t>(warp) * kNS * pbytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bar) + warp * kNS;
   float *lg = reinterpret_cast<float *>(smem + lay.lg);
@@ -369,7 +390,7 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
     int32_t pid, tok0, ntok;
     item(warp + n * kWarps, kind, pid, tok0, ntok);
     uint64_t *bar = bars + n % kNS;
-    if (pid >= 0) fetch_page(stage + (n % kNS) * pbytes, a.pages + static_cast<int64_t>(pid) * pbytes, kind, P, bar);
+    if (pid >= 0) fetch_page<SC>(stage + (n % kNS) * pbytes, a.pages + pid * gbytes, kind, P, bar);
     else bar_arrive(bar);
   };
   if (lane == 0) {
@@ -406,7 +427,33 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
         for (int j = 0; j < NT; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) c[j][e] = c2[j][e] = 0.0f;
-        if (kind == 1) {
+        // other schemes: each code extracted by shift and mask in the K8V4
+        // channel order (lane t: channels 32t + 4kc + {0..3} of step kc)
+        auto qk_generic = [&](auto wtag) {
+          constexpr int W = decltype(wtag)::value;  // K bits
+          uint32_t x0[W], x1[W];                    // the lane's 32 channels: 4W bytes of each row
+#pragma unroll
+          for (int i = 0; i < W; ++i) {
+            x0[i] = reinterpret_cast<const uint32_t *>(pg + r0 * 16 * W + 4 * W * tq)[i];
+            x1[i] = reinterpret_cast<const uint32_t *>(pg + r1 * 16 * W + 4 * W * tq)[i];
+          }
+#pragma unroll
+          for (int kc = 0; kc < 8; ++kc) {
+            const uint32_t a0 = code_at_w<W>(x0, 4 * kc) | (code_at_w<W>(x0, 4 * kc + 1) << 16);
+            const uint32_t a2 = code_at_w<W>(x0, 4 * kc + 2) | (code_at_w<W>(x0, 4 * kc + 3) << 16);
+            const uint32_t a1 = code_at_w<W>(x1, 4 * kc) | (code_at_w<W>(x1, 4 * kc + 1) << 16);
+            const uint32_t a3 = code_at_w<W>(x1, 4 * kc + 2) | (code_at_w<W>(x1, 4 * kc + 3) << 16);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              const uint2 f = frag_h[j][kc][lane];
+              mma((kc & 1) ? c2[j] : c[j], a0, a1, a2, a3, f.x, f.y);
+            }
+          }
+        };
+        if constexpr (SC != 0) {
+          if (kind == 1) qk_generic(std::integral_constant<int, KH>{});
+          else qk_generic(std::integral_constant<int, KH / 2>{});
+        } else if (kind == 1) {
           uint32_t x0[8], x1[8];
           const uint4 *k0 = reinterpret_cast<const uint4 *>(pg + r0 * 128 + 32 * tq);
           const uint4 *k1 = reinterpret_cast<const uint4 *>(pg + r1 * 128 + 32 * tq);
@@ -444,13 +491,13 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
         for (int j = 0; j < NT; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) c[j][e] += c2[j][e];
-        const uint2 mt0 = *reinterpret_cast<const uint2 *>(pg + 192 * P + 8 * r0);
-        const uint2 mt1 = *reinterpret_cast<const uint2 *>(pg + 192 * P + 8 * r1);
+        const uint2 mt0 = *reinterpret_cast<const uint2 *>(pg + moff + 8 * r0);
+        const uint2 mt1 = *reinterpret_cast<const uint2 *>(pg + moff + 8 * r1);
         const float ks0 = half_lo(mt0.x), kz0 = half_hi(mt0.x), sv0 = half_lo(mt0.y), zv0 = half_hi(mt0.y);
         const float ks1 = half_lo(mt1.x), kz1 = half_hi(mt1.x), sv1 = half_lo(mt1.y), zv1 = half_hi(mt1.y);
         if (tq == 0) {
-          if (v0) ps[tok0 + s0 - c0] = *reinterpret_cast<const int32_t *>(pg + 208 * P + 4 * r0);
-          if (v1) ps[tok0 + s1 - c0] = *reinterpret_cast<const int32_t *>(pg + 208 * P + 4 * r1);
+          if (v0) ps[tok0 + s0 - c0] = *reinterpret_cast<const int32_t *>(pg + poff + 4 * r0);
+          if (v1) ps[tok0 + s1 - c0] = *reinterpret_cast<const int32_t *>(pg + poff + 4 * r1);
         }
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
@@ -547,8 +594,37 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
         int32_t rr[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) rr[i] = min(sb + tq + 4 * i, ntok - 1);
-        if (kind == 1) {
-          const uint8_t *vb8 = pg + 128 * P + 8 * gq;
+        // other schemes: lane g's 16 channels 16g .. of each of its 4 slots are
+        // 2W bytes; each code extracted by shift and mask
+        auto pv_generic = [&](auto wtag) {
+          constexpr int W = decltype(wtag)::value;  // V bits
+          constexpr int NZ = W >= 2 ? W / 2 : 1;     // words of 16 channels
+          uint32_t z[4][NZ];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint8_t *src = pg + vbase + rr[i] * 16 * W + 2 * W * gq;
+            if (W == 1) {
+              z[i][0] = *reinterpret_cast<const uint16_t *>(src);
+            } else {
+#pragma unroll
+              for (int q = 0; q < NZ; ++q) z[i][q] = reinterpret_cast<const uint32_t *>(src)[q];
+            }
+          }
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const uint32_t a0 = code_at_w<W>(z[0], 2 * mt) | (code_at_w<W>(z[1], 2 * mt) << 16);
+            const uint32_t a1 = code_at_w<W>(z[0], 2 * mt + 1) | (code_at_w<W>(z[1], 2 * mt + 1) << 16);
+            const uint32_t a2 = code_at_w<W>(z[2], 2 * mt) | (code_at_w<W>(z[3], 2 * mt) << 16);
+            const uint32_t a3 = code_at_w<W>(z[2], 2 * mt + 1) | (code_at_w<W>(z[3], 2 * mt + 1) << 16);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) mma(cv[j][mt], a0, a1, a2, a3, b[j][0], b[j][1]);
+          }
+        };
+        if constexpr (SC != 0) {
+          if (kind == 1) pv_generic(std::integral_constant<int, VH>{});
+          else pv_generic(std::integral_constant<int, VH / 2>{});
+        } else if (kind == 1) {
+          const uint8_t *vb8 = pg + vbase + 8 * gq;
           uint2 z[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) z[i] = *reinterpret_cast<const uint2 *>(vb8 + rr[i] * 64);
@@ -563,7 +639,7 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
             for (int j = 0; j < NT; ++j) mma(cv[j][mt], a0, a1, a2, a3, b[j][0], b[j][1]);
           }
         } else {
-          const uint8_t *vb8 = pg + 128 * P + 4 * gq;
+          const uint8_t *vb8 = pg + vbase + 4 * gq;
           uint32_t z[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) z[i] = *reinterpret_cast<const uint32_t *>(vb8 + rr[i] * 32);
@@ -799,10 +875,10 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
   cluster.sync();  // 2: no block leaves while another may still read its shared memory
 }
 
-template <int NT>
+template <int NT, int SC>
 cudaError_t launch_nt(const AttnArgs &a, int32_t S, size_t smem, cudaStream_t s) {
   if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(k_attend<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(k_attend<NT, SC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
@@ -818,7 +894,7 @@ cudaError_t launch_nt(const AttnArgs &a, int32_t S, size_t smem, cudaStream_t s)
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_attend<NT>, a);
+  return cudaLaunchKernelEx(&cfg, k_attend<NT, SC>, a);
 }
 
 }  // namespace
@@ -827,7 +903,9 @@ cudaError_t launch_attend(const AttnArgs &a, int32_t S, cudaStream_t s) {
   if (a.units == 0) return cudaSuccess;
   const size_t smem = attend_layout(a.cmax, a.G, a.pmax, a.P).bytes;
   if (a.G < 1 || a.G > 8) return cudaErrorInvalidValue;
-  return a.G <= 4 ? launch_nt<1>(a, S, smem, s) : launch_nt<2>(a, S, smem, s);
+  if (a.scheme == 1) return a.G <= 4 ? launch_nt<1, 1>(a, S, smem, s) : launch_nt<2, 1>(a, S, smem, s);
+  if (a.scheme == 2) return a.G <= 4 ? launch_nt<1, 2>(a, S, smem, s) : launch_nt<2, 2>(a, S, smem, s);
+  return a.G <= 4 ? launch_nt<1, 0>(a, S, smem, s) : launch_nt<2, 0>(a, S, smem, s);
 }
 
 }  // namespace dkv

@@ -308,6 +308,7 @@ __host__ __device__ constexpr int attend_blocks_per_sm(int G) { return G <= 4 ? 
 
 struct AttnArgs {
   int32_t L, R, Hq, Hkv, G, P, pmax, cap, layer0, n_layers;
+  int32_t scheme;               // the pool's bit-width scheme
   int32_t cmax;                 // tokens one block of a cluster holds at most
   int64_t F, units;             // units = n_layers * R * Hkv
   float scale;

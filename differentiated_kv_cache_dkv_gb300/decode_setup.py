@@ -56,7 +56,8 @@ def decode_setup(w, dev, seed: int, total_steps: int, window: int = 0, mode: int
     the pages it takes, the second starts the ring DECODE_SLACK pages before
     its end."""
     cap = decode_cap(w, total_steps)
-    dec = libdkv.Decoder(w.L, w.R, w.Hq, w.Hkv, cap, w.P, w.pool_pages, device=dev, window=window, mode=mode)
+    dec = libdkv.Decoder(w.L, w.R, w.Hq, w.Hkv, cap, w.P, w.pool_pages, device=dev, window=window, mode=mode,
+                         scheme=w.scheme)
     decode_prefill(w, dec, dev, seed, cap)
     used = int(dec.pool.cursors[0])
     F = dec.pool.F

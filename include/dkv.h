@@ -300,7 +300,8 @@ int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dk
  * attention reads the mixed-precision unified pages.  The pages do not print
  * that kernel; this is plain scaled dot-product attention.  For query head q
  * of request r in layer l (unit (l, r, q / G), G = Hq / Hkv) the attended
- * tokens are every used slot of the unit's K8V4 and K4V2 lists, with K and V
+ * tokens are every used slot of the unit's high- and low-class lists (the
+ * pool's bit-width scheme: K8V4/K4V2, K8V2/K4V1 or K4V8/K2V4), with K and V
  * the dequantised values fma(code, scale, zero) that dkv_dequant_page gives,
  * plus the step's new token (its bf16 K and V, position ctx_lens[r]) when
  * k_new is given and new_lens[r] = 1:
@@ -328,9 +329,7 @@ typedef struct dkv_attn_batch {
 } dkv_attn_batch;
 
 /* Decode attention (above), asynchronous; allocates nothing.  The pool and
- * tables are read only.  Synchronous DKV_E_INVAL: a pool whose scheme is not
- * DKV_SCHEME_K8V4_K4V2 (the kernel reads 8/4-bit K and 4/2-bit V), a bad
- * shape or pointer,
+ * tables are read only.  Synchronous DKV_E_INVAL: a bad shape or pointer,
  * G outside 1..8, or a shape whose per-block shared memory does not fit 220 KB
  * even with a cluster of 8 blocks per unit (a block holds 2 page buffers of
  * 216 P bytes per warp, 6 warps for G <= 4 and 8 above, plus its share of the

@@ -6,27 +6,31 @@ from __future__ import annotations
 
 import numpy as np
 
-from tests.oracle_helpers import unpack
+from tests.oracle_helpers import Layout, unpack
 
 U = 2.0 ** -24  # fp32 unit roundoff
 
 
-def unit_tokens(pages: np.ndarray, fwd_row: np.ndarray, hdr, P: int):
-    """Held tokens of a unit in list order (K8V4 list, then K4V2 list):
+def unit_tokens(pages: np.ndarray, fwd_row: np.ndarray, hdr, P: int, scheme: int = 0):
+    """Held tokens of a unit in list order (high list, then low list):
     (K codes [n,128], V codes [n,128], k_s, k_z, v_s, v_z [n] float64,
-    positions [n] int64).  `pages` is indexable by the forward row's ids."""
+    positions [n] int64).  `pages` is indexable by the forward row's ids; the
+    page layout and code widths are those of the bit-width scheme."""
+    lay = Layout(P, scheme)
     n_hi, n_lo, p_hi, p_lo = (int(x) for x in hdr)
     parts = []
-    for n, ids, per, kb, vb in ((n_hi, fwd_row[:p_hi], P, 8, 4), (n_lo, fwd_row[p_hi:p_hi + p_lo], 2 * P, 4, 2)):
+    for n, ids, per, high in ((n_hi, fwd_row[:p_hi], P, True), (n_lo, fwd_row[p_hi:p_hi + p_lo], 2 * P, False)):
         if n == 0:
             continue
-        pg = np.stack([pages[int(i)] for i in ids])                     # [pages, 216P]
+        kb, vb = lay.kbits(high), lay.vbits(high)
+        pg = np.stack([pages[int(i)] for i in ids])                     # [pages, page bytes]
         kbytes = 16 * kb
         vbytes = 16 * vb
+        vbase = lay.v_off(high, 0)
         kc = pg[:, :per * kbytes].reshape(-1, kbytes)[:n]
-        vc = pg[:, 128 * P:128 * P + per * vbytes].reshape(-1, vbytes)[:n]
-        meta = pg[:, 192 * P:192 * P + 8 * per].reshape(-1, 8)[:n].copy().view(np.uint16)
-        pos = pg[:, 208 * P:208 * P + 4 * per].reshape(-1, 4)[:n].copy().view(np.int32)[:, 0]
+        vc = pg[:, vbase:vbase + per * vbytes].reshape(-1, vbytes)[:n]
+        meta = pg[:, lay.meta:lay.meta + 8 * per].reshape(-1, 8)[:n].copy().view(np.uint16)
+        pos = pg[:, lay.pos:lay.pos + 4 * per].reshape(-1, 4)[:n].copy().view(np.int32)[:, 0]
         kq = unpack(kc.reshape(-1), kb).reshape(n, 128)
         vq = unpack(vc.reshape(-1), vb).reshape(n, 128)
         m = meta.view(np.float16).astype(np.float64)

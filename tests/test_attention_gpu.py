@@ -80,7 +80,7 @@ def _check(hd, dec, layer0, n_layers, with_new, scale=0.08838834764831845, seed=
             has_new = with_new and int(nl[r]) == 1
             for h in range(w.Hkv):
                 u = (l * w.R + r) * w.Hkv + h
-                toks = unit_tokens(hd.pool.pages, hd.tab.fwd[u], hd.tab.unit_hdr[u], w.P)
+                toks = unit_tokens(hd.pool.pages, hd.tab.fwd[u], hd.tab.unit_hdr[u], w.P, w.scheme)
                 pos = list(toks[6])
                 if has_new:
                     pos.append(int(ctx[r]))
@@ -129,6 +129,23 @@ def test_attention_small_ragged(with_new):
 ])
 def test_attention_shapes(shape):
     w = W.small("atts", **shape)
+    cap = (max(w.lens) + 16 + 15) // 16 * 16
+    hd, dec = _state(w, cap=cap, steps=3)
+    _check(hd, dec, 0, w.L, True)
+
+
+@pytest.mark.parametrize("scheme", [1, 2], ids=["k8v2-k4v1", "k4v8-k2v4"])
+@pytest.mark.parametrize("shape", [
+    dict(lens=[300, 7, 517, 0, 129]),                            # G = 3, 2 layers
+    dict(Hq=8, Hkv=2, P=16, lens=[2100, 300, 2], L=1),           # G = 4
+    dict(Hq=16, Hkv=2, P=16, lens=[1500, 64], L=1),              # G = 8
+    dict(Hq=4, Hkv=4, P=2, lens=[90, 91, 1], L=1),               # G = 1, tiny pages
+], ids=["g3", "g4", "g8", "g1-p2"])
+def test_attention_other_schemes(scheme, shape):
+    """The bit-width schemes beside K8V4/K4V2: pages of K8V2/K4V1 (1-bit low
+    values) and K4V8/K2V4 (2-bit low keys, 8-bit high values), after
+    generation steps with churn, with the new token."""
+    w = W.small("attsc", scheme=scheme, **shape)
     cap = (max(w.lens) + 16 + 15) // 16 * 16
     hd, dec = _state(w, cap=cap, steps=3)
     _check(hd, dec, 0, w.L, True)

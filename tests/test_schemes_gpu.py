@@ -120,14 +120,3 @@ def test_edge_rows_requantise_bit_exact(scheme):
         compare(g, hd, f"step {step}:")
         check_slot_index(g, hd)
     check_state(w, cap, hd.pool, hd.tab.fwd, hd.tab.unit_hdr, hd.classes, hd.ctx_lens)
-
-
-def test_decode_attention_refuses_other_schemes():
-    w = W.small("sch_att", lens=[40, 9], L=1, Hq=4, Hkv=2, scheme=1)
-    hd = HostDecode(w, 64, inp=W.make_inputs(w, 3))
-    dec = gpu_decoder(hd, W.make_inputs(w, 3))
-    q = torch.zeros((1, w.R, w.Hq, 128), dtype=torch.bfloat16, device="cuda")
-    out = torch.empty((1, w.R, w.Hq, 128), dtype=torch.float32, device="cuda")
-    with pytest.raises(libdkv.DkvError) as e:
-        dec.attend(q, hd.ctx["ctx_lens"].cuda(), out, 0.088)
-    assert e.value.code == libdkv.DKV_E_INVAL
