@@ -450,10 +450,9 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
             }
           }
         };
-        if constexpr (SC != 0) {
-          if (kind == 1) qk_generic(std::integral_constant<int, KH>{});
-          else qk_generic(std::integral_constant<int, KH / 2>{});
-        } else if (kind == 1) {
+        // 8-bit and 4-bit keys take the byte-permute extraction (either class
+        // of any scheme), other widths the generic one
+        auto qk_k8 = [&]() {
           uint32_t x0[8], x1[8];
           const uint4 *k0 = reinterpret_cast<const uint4 *>(pg + r0 * 128 + 32 * tq);
           const uint4 *k1 = reinterpret_cast<const uint4 *>(pg + r1 * 128 + 32 * tq);
@@ -470,7 +469,8 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
               mma((kc & 1) ? c2[j] : c[j], a0, a1, a2, a3, f.x, f.y);
             }
           }
-        } else {
+        };
+        auto qk_k4 = [&]() {
           const uint4 y0 = *reinterpret_cast<const uint4 *>(pg + r0 * 64 + 16 * tq);
           const uint4 y1 = *reinterpret_cast<const uint4 *>(pg + r1 * 64 + 16 * tq);
           const uint32_t x0[4] = {y0.x, y0.y, y0.z, y0.w}, x1[4] = {y1.x, y1.y, y1.z, y1.w};
@@ -486,7 +486,15 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
               mma((kc & 1) ? c2[j] : c[j], a0, a1, a2, a3, f.x, f.y);
             }
           }
-        }
+        };
+        auto qk_width = [&](auto wtag) {
+          constexpr int W = decltype(wtag)::value;
+          if constexpr (W == 8) qk_k8();
+          else if constexpr (W == 4) qk_k4();
+          else qk_generic(wtag);
+        };
+        if (kind == 1) qk_width(std::integral_constant<int, KH>{});
+        else qk_width(std::integral_constant<int, KH / 2>{});
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -620,10 +628,9 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
             for (int j = 0; j < NT; ++j) mma(cv[j][mt], a0, a1, a2, a3, b[j][0], b[j][1]);
           }
         };
-        if constexpr (SC != 0) {
-          if (kind == 1) pv_generic(std::integral_constant<int, VH>{});
-          else pv_generic(std::integral_constant<int, VH / 2>{});
-        } else if (kind == 1) {
+        // 4-bit and 2-bit values take the byte-permute extraction (either
+        // class of any scheme), other widths the generic one
+        auto pv_v4 = [&]() {
           const uint8_t *vb8 = pg + vbase + 8 * gq;
           uint2 z[4];
 #pragma unroll
@@ -638,7 +645,8 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
 #pragma unroll
             for (int j = 0; j < NT; ++j) mma(cv[j][mt], a0, a1, a2, a3, b[j][0], b[j][1]);
           }
-        } else {
+        };
+        auto pv_v2 = [&]() {
           const uint8_t *vb8 = pg + vbase + 4 * gq;
           uint32_t z[4];
 #pragma unroll
@@ -653,7 +661,15 @@ __global__ void __launch_bounds__(32 * attend_warps(4 * NT), attend_blocks_per_s
 #pragma unroll
             for (int j = 0; j < NT; ++j) mma(cv[j][mt], a0, a1, a2, a3, b[j][0], b[j][1]);
           }
-        }
+        };
+        auto pv_width = [&](auto wtag) {
+          constexpr int W = decltype(wtag)::value;
+          if constexpr (W == 4) pv_v4();
+          else if constexpr (W == 2) pv_v2();
+          else pv_generic(wtag);
+        };
+        if (kind == 1) pv_width(std::integral_constant<int, VH>{});
+        else pv_width(std::integral_constant<int, VH / 2>{});
       }
     }
     __syncwarp();  // every lane is done with stage s
