@@ -99,7 +99,7 @@ dkv::DecodeArgs decode_args(const dkv_decode_batch *b, const dkv_pool *pool, con
   a.pg = dkv::page_geom(pool->scheme, pool->P);
   a.L = b->L; a.R = b->R; a.Hq = b->Hq; a.Hkv = b->Hkv; a.G = b->Hq / b->Hkv;
   a.P = pool->P; a.pmax = t->pmax; a.cap = b->cap;
-  a.window = b->window; a.mode = b->mode;
+  a.window = b->window; a.mode = b->mode; a.rchunk = dkv::kReclassChunk;
   a.F = pool->F; a.U = static_cast<int64_t>(b->L) * b->R * b->Hkv; a.unit_base = b->unit_base;
   a.k_new = static_cast<const uint16_t *>(b->k_new); a.v_new = static_cast<const uint16_t *>(b->v_new);
   a.sig_sum = b->sig_sum; a.sig_cnt = b->sig_cnt; a.ctx_lens = b->ctx_lens; a.new_lens = b->new_lens;
@@ -281,6 +281,7 @@ int32_t dkv_decode_step(const dkv_decode_batch *b, const dkv_params *p, const dk
   a.spin_limit = p->spin_limit < 0 ? (1 << 22) : p->spin_limit;
   a.alpha_h = p->alpha_h;
   a.alpha_l = p->alpha_l;
+  a.rchunk = dkv::reclass_chunk(static_cast<int64_t>(b->L) * b->R, b->cap, sms);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   a.ws = reinterpret_cast<dkv::DecWsHeader *>(ws);
   a.ucnt = reinterpret_cast<int4 *>(ws + lay.ucnt);

@@ -86,6 +86,15 @@ __device__ __forceinline__ bool words_out_of_range(uint4 v) {
 
 // ---------------------------------------------------------------- k_reclass --
 
+// Starts the copy of [p, p + bytes) from HBM into L2 (whole 16-byte pieces
+// inside the range); nothing waits on it, the loads that follow hit L2.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint64_t bytes) {
+  const uintptr_t b = reinterpret_cast<uintptr_t>(p);
+  const uintptr_t e = (b + bytes) & ~static_cast<uintptr_t>(15);
+  const uintptr_t st = (b + 15) & ~static_cast<uintptr_t>(15);
+  if (e > st) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(st), "r"(static_cast<uint32_t>(e - st)));
+}
+
 // The new token's class mark, its saved prior byte and class, and the range
 // check of a kept new token's K and V.  Once per unit, so out of line.
 __device__ __noinline__ void new_token(const DecodeArgs &a, uint8_t *c, int64_t u, uint32_t prior, uint32_t cn) {
@@ -132,7 +141,7 @@ __global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
   __shared__ uint32_t mk_s[kMarkList];  // this block's changes, listed for the apply kernel
   __shared__ int32_t mk_n, mk_base;
   const int32_t r = blockIdx.y, l = blockIdx.z;
-  const int32_t i0 = blockIdx.x * kReclassChunk;
+  const int32_t i0 = static_cast<int32_t>(blockIdx.x) << (31 - __clz(a.rchunk));  // rchunk: a power of two
   const int32_t ctx = __ldg(a.ctx_lens + r), nw = __ldg(a.new_lens + r);
   if (lens_bad(a, ctx, nw)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) set_error(&a.ws->err, DKV_E_LENS);
@@ -144,10 +153,17 @@ __global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
   }
   const int32_t N = ctx + nw;
   if (i0 >= N) return;
-  const int32_t i1 = min(N, i0 + kReclassChunk);
+  const int32_t i1 = min(N, i0 + a.rchunk);
   // With a recent window the scored rows end where it starts (N - W; the
   // held rows in it keep their class, the new token enters as K8V4 below)
   const int32_t is = a.window >= 1 ? max(i0, min(i1, N - a.window)) : i1;
+  // The block's significance rows are one contiguous range: one bulk
+  // prefetch into L2 keeps HBM busy with far more bytes in flight than the
+  // threads' own loads (2 rows each at 32 registers) hold.  Issued here,
+  // before the loop's registers are live, it costs the loop none.
+  if (threadIdx.x == 0 && is > i0)
+    prefetch_l2(a.sig_sum + ((static_cast<int64_t>(l) * a.R + r) * a.cap + i0) * a.Hq,
+                static_cast<uint64_t>(is - i0) * a.Hq * 4u);
   const int Hkv = a.Hkv, G = a.G;
   for (int t = threadIdx.x; t < Hkv * 3; t += blockDim.x) ev_s[t] = 0;
   if (threadIdx.x == 0) mk_n = 0;
@@ -1240,7 +1256,7 @@ size_t apply_smem(int32_t hpc, int32_t words, int32_t pmax) {
 
 cudaError_t launch_reclass(const DecodeArgs &a, cudaStream_t s) {
   // with a recent window one more block per (layer, request) takes the new token
-  const dim3 grid((a.cap + kReclassChunk - 1) / kReclassChunk + (a.window >= 1 ? 1 : 0), a.R, a.L);
+  const dim3 grid((a.cap + a.rchunk - 1) / a.rchunk + (a.window >= 1 ? 1 : 0), a.R, a.L);
   if (a.G == 4) k_reclass<1><<<grid, kReclassThreads, 0, s>>>(a);
   else if (a.G == 8) k_reclass<2><<<grid, kReclassThreads, 0, s>>>(a);
   else k_reclass<0><<<grid, kReclassThreads, 0, s>>>(a);

@@ -199,7 +199,17 @@ __device__ __forceinline__ int find_segment(const int32_t *a, int n, int64_t x, 
 
 // ---------------------------------------------------------------- decode --
 
-constexpr int kReclassChunk = 2048;   // positions per reclassification block
+constexpr int kReclassChunk = 4096;   // most positions per reclassification block
+
+// Positions per reclassification block: the longest of 4096, 2048, 1024, 512
+// that still makes two waves of blocks (4 resident per SM) over the L R
+// (layer, request) pairs.  Longer blocks amortise their set-up and L2
+// prefetch; shorter ones keep a small batch spread over every SM.
+inline int32_t reclass_chunk(int64_t lr, int32_t cap, int sms) {
+  int32_t c = kReclassChunk;
+  while (c > 512 && lr * ((cap + c - 1) / c) < 8ll * sms) c >>= 1;
+  return c;
+}
 constexpr int kMaxApplyWarps = 8;     // units (KV heads) per apply block, one warp each
 
 struct DecWsHeader {
@@ -271,6 +281,7 @@ struct DecodeArgs {
   PageGeom pg;                    // page layout of the pool's scheme
   int32_t L, R, Hq, Hkv, G, P, pmax, cap, spin_limit;
   int32_t window, mode;
+  int32_t rchunk;  // positions per reclassification block
   int64_t F, U, unit_base;
   float alpha_h, alpha_l;
   const uint16_t *k_new, *v_new;
