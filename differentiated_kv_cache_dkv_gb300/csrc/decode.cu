@@ -663,9 +663,10 @@ __device__ void hole_fill(const DecodeArgs &a, const UnitView &v, bool hi, const
 // RN(x - z): y lies on a grid of 2^-13 and bits(y) >> 13 holds floor(t + 0.5)
 // for t = y - 1536.5.  |d * RN(1/s) - d / s| <= 2^-16 for codes below 256, far
 // inside half the grid step, so when y is not an integer (t not a
-// half-integer) floor(t + 0.5) is the rounded quotient of the definition;
-// an integer y (low 13 bits zero) is re-evaluated with the IEEE division, as
-// is every element of a row whose codes would need clamping.
+// half-integer) floor(t + 0.5) is the rounded quotient of the definition.
+// A lane holding an integer y (low 13 bits zero) re-evaluates all its
+// elements with the IEEE division, as does every lane of a row whose codes
+// would need clamping.
 template <int kPer, int kGroup>
 __device__ __forceinline__ void quant_vals(const float (&x)[kPer], int nmax, uint32_t (&q)[kPer], uint16_t &s16o,
                                            uint16_t &z16o) {
@@ -699,13 +700,22 @@ __device__ __forceinline__ void quant_vals(const float (&x)[kPer], int nmax, uin
   }
   const float r = __frcp_rn(s);
   const bool clamp_row = __fmul_rn(__fsub_rn(mn, z), r) < -0.25f || __fmul_rn(__fsub_rn(mx, z), r) > nf + 0.25f;
+  // fast codes first, with the smallest fraction field seen; one branch for
+  // the lane's codes: where any fraction is zero (a code that may differ from
+  // the definition) or the row clamps, every code is taken by the division
+  // (equal to the fast code wherever that one is right)
+  uint32_t frac = clamp_row ? 0u : 8191u;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const float d = __fsub_rn(x[i], z);
     const uint32_t bits = __float_as_uint(__fmaf_rn(d, r, 1536.5f));
     q[i] = (bits >> 13) & 255u;
-    if (clamp_row || (bits & 8191u) == 0u)
-      q[i] = static_cast<uint32_t>(fminf(fmaxf(rintf(__fdiv_rn(d, s)), 0.0f), nf));
+    frac = min(frac, bits & 8191u);
+  }
+  if (frac == 0u) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      q[i] = static_cast<uint32_t>(fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(x[i], z), s)), 0.0f), nf));
   }
 }
 
@@ -1175,7 +1185,7 @@ __global__ void __launch_bounds__(32 * kMaxApplyWarps, 3) k_apply(DecodeArgs a, 
 // hole-fill has emptied the destination slots and whose page clears came
 // first; a failed call staged nothing.
 template <int S>
-__global__ void __launch_bounds__(256) k_demote(DecodeArgs a) {
+__global__ void __launch_bounds__(256, 4) k_demote(DecodeArgs a) {
   if (*reinterpret_cast<volatile int32_t *>(&a.ws->err) != 0) return;
   const int64_t n = min(static_cast<int64_t>(a.ws->job_n), a.njobs);
   const int lane = threadIdx.x & 31, grp = lane >> 3, t = lane & 7;
