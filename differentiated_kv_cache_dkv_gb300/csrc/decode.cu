@@ -135,8 +135,10 @@ __device__ __noinline__ void window_new_token(const DecodeArgs &a, int32_t r, in
   }
 }
 
+// 4 blocks of 512 per SM (32 registers); the paired-row loop of G = 4 runs
+// at 3 (40 registers: at 32 it spills)
 template <int kV4>  // float4 loads per row (G / 4); 0 = scalar loads
-__global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
+__global__ void __launch_bounds__(kReclassThreads, kV4 == 1 ? 3 : 4) k_reclass(DecodeArgs a) {
   __shared__ int32_t ev_s[kMaxHq * 3];  // per head: demoted, K8V4 pruned, K4V2 pruned
   __shared__ uint32_t mk_s[kMarkList];  // this block's changes, listed for the apply kernel
   __shared__ int32_t mk_n, mk_base;
@@ -188,6 +190,76 @@ __global__ void __launch_bounds__(kReclassThreads, 4) k_reclass(DecodeArgs a) {
   const int32_t *cnt = a.sig_cnt + tok0;
   const int nrows = (is - i0) * Hkv;
   const int64_t u0 = (static_cast<int64_t>(l) * a.R + r) * Hkv;
+  if (kV4 == 1 && sh >= 1) {
+    // G = 4 and an even power-of-two Hkv: a thread takes the two rows of one
+    // token and head pair (32 contiguous bytes of sums, 2 class bytes),
+    // sharing the token's count, reciprocal and new-token test
+    // the reciprocal test's bounds, opened to +-inf when only the division
+    // decides: then the first test passes only y = +inf and the third only
+    // y = -inf or NaN, where the division gives the same class
+    const float fhh = exact_only ? INFINITY : hi_h, fhl = exact_only ? -INFINITY : lo_h;
+    const float flh = exact_only ? INFINITY : hi_l, fll = exact_only ? -INFINITY : lo_l;
+    auto decide = [&](float mm, float cf, float rc) -> uint32_t {
+      const float yv = __fmul_rn(mm, rc);
+      if (yv >= fhh) return DKV_CLASS_K8V4;
+      if (!(yv > fhl) && yv >= flh) return DKV_CLASS_K4V2;
+      if (!(yv > fhl) && !(yv > fll)) return DKV_CLASS_PRUNE;
+      const float sq = __fdiv_rn(mm, cf);
+      return sq >= thr_h ? DKV_CLASS_K8V4 : (sq >= thr_l ? DKV_CLASS_K4V2 : DKV_CLASS_PRUNE);
+    };
+    auto update = [&](int j, int ii, bool is_new, uint32_t o, uint32_t cn) {
+      const int h = j - (ii << sh);
+      if (!is_new) {
+        if (o == DKV_CLASS_PRUNE) return;  // min(0, x) = 0: nothing can change
+        if (o > DKV_CLASS_K8V4) {
+          set_error(&a.ws->err, DKV_E_INTERNAL);
+          return;
+        }
+        if (cn < o) {
+          cls[j] = static_cast<uint8_t>(0x80u | (o << 2) | cn);
+          atomicAdd(&ev_s[h * 3 + (o == DKV_CLASS_K4V2 ? 2 : (cn == DKV_CLASS_K4V2 ? 0 : 1))], 1);
+          const int32_t q = atomicAdd(&mk_n, 1);
+          if (q < kMarkList) mk_s[q] = (static_cast<uint32_t>(i0 + ii) << 11) | (h << 4) | (o << 2) | cn;
+        }
+      } else {  // the new token (position ctx)
+        new_token(a, cls + j, u0 + h, o, cn);
+        const int32_t q = atomicAdd(&mk_n, 1);
+        if (q < kMarkList) mk_s[q] = (static_cast<uint32_t>(i0 + ii) << 11) | (h << 4) | (3u << 2) | cn;
+      }
+    };
+    const float4 *sp = reinterpret_cast<const float4 *>(sig);
+    const int npairs = nrows >> 1;
+    for (int jp = threadIdx.x; jp < npairs; jp += kReclassThreads) {
+      const int j = 2 * jp;
+      const int ii = j >> sh;
+      const int32_t cc = __ldg(cnt + ii);
+      const uint32_t o2 = *reinterpret_cast<const uint16_t *>(cls + j);
+      const float4 x = __ldcs(sp + j), y = __ldcs(sp + j + 1);
+      const bool is_new = i0 + ii >= ctx;
+      const uint32_t o0 = o2 & 0xffu, o1 = o2 >> 8;
+      if (!is_new && o0 == DKV_CLASS_PRUNE && o1 == DKV_CLASS_PRUNE) continue;
+      // max over the group of the rounded quotients == rounded quotient of
+      // the max sum (min for a negative count): division is monotone
+      float m0, m1;
+      if (cc > 0) {
+        m0 = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+        m1 = fmaxf(fmaxf(y.x, y.y), fmaxf(y.z, y.w));
+      } else {
+        m0 = fminf(fminf(x.x, x.y), fminf(x.z, x.w));
+        m1 = fminf(fminf(y.x, y.y), fminf(y.z, y.w));
+      }
+      uint32_t cn0 = DKV_CLASS_K8V4, cn1 = DKV_CLASS_K8V4;  // a count of 0: not yet observed
+      if (cc != 0) {
+        const float cf = static_cast<float>(cc);
+        float rc;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(cf));
+        cn0 = decide(m0, cf, rc);
+        cn1 = decide(m1, cf, rc);
+      }
+      update(j, ii, is_new, o0, cn0);
+      update(j + 1, ii, is_new, o1, cn1);
+    }
+  } else
   for (int jb = 0; jb < nrows; jb += kReclassRows * kReclassThreads) {
     float m[kReclassRows];
     int32_t c[kReclassRows];
