@@ -96,10 +96,10 @@ SCHEME_NAMES = {0: "K8V4/K4V2", 1: "K8V2/K4V1", 2: "K4V8/K2V4"}
 PACK_TRAFFIC = {"workload": "llama", "source_sha1": "8053ae355a66", "bytes": 16 * (537.714944 + 130.876928) * 1e6}
 
 # DRAM traffic of k_reclass per algorithmic byte, from one ncu capture on 4
-# layers x 64 requests of the decode workload (180.2 MB for 176.2 MB; traffic
+# layers x 64 requests of the decode workload (180.6 MB for 176.2 MB; traffic
 # grows with the live rows) (profiles/decode_step.md); valid only for the
 # kernel source it was measured on.
-RECLASS_TRAFFIC = {"workload": "decode", "source_sha1": "b772ffd268e6", "per_byte": (177.175808 + 3.048448) / 176.177616}
+RECLASS_TRAFFIC = {"workload": "decode", "source_sha1": "cb145cbff917", "per_byte": (177.17376 + 3.397632) / 176.177616}
 
 
 def _source_sha(name: str):
