@@ -417,7 +417,7 @@ def run_native(a):
             "classes": {"k8v4": n_hi / rows, "k4v2": n_lo / rows, "pruned": n_pruned / rows},
             "pages_per_step": pages,
             "payload_fraction": ((scheme_bits(w.scheme)) * (n_hi + 0.5 * n_lo)) / (32 * rows),
-            "gpu_launches": a.steps * (1 + libdkv.DKV_PROFILE_KERNELS),
+            "gpu_launches": a.steps * (2 + libdkv.DKV_PROFILE_KERNELS),  # pool reset, 5 kernels, k_clear_hi
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,

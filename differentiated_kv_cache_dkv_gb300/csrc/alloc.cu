@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kScanThreads = 1024;  // one warp per unit of the partition
 constexpr int kCommitThreads = 256;
+constexpr int kClearThreads = 128;
 
 __device__ __forceinline__ void st_release(uint64_t *p, uint64_t v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -212,11 +213,55 @@ __device__ __forceinline__ void fill_words(uint8_t *p, int64_t nwords, uint32_t 
   for (int64_t i = lane; i < nwords; i += 32) w[i] = value;
 }
 
+// The unused slots P..2P-1 of every new high page: their metadata (8P bytes:
+// P/2 chunks of 16) and positions (4P bytes: P/2 chunks of 8; P is even) are
+// cleared (zero, position -1).  It needs only the scan's placement, so it
+// runs beside k_pack on a second stream, at 32 registers and no shared memory
+// so that its blocks fit an SM beside a k_pack block.  One warp per unit;
+// consecutive lanes write consecutive chunks of one page whose id comes from
+// the lane that loaded it.  A call the scan failed writes nothing; one that
+// fails later (in k_pack) has only written pages that stay free.
+__global__ void __launch_bounds__(kClearThreads, 16) k_clear_hi(CompactArgs a) {
+  if (a.ws->err != 0) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t head_mod = a.ws->head_mod;
+  const int32_t per = a.P;  // chunks per page
+  const PageGeom &g = a.pg;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kClearThreads / 32);
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * (kClearThreads / 32) + (threadIdx.x >> 5); u < a.U;
+       u += nwarps) {
+    const UnitInfo inf = a.unit[u];
+    int64_t ring = head_mod + inf.off;
+    if (ring >= a.F) ring -= a.F;
+    for (int32_t k0 = 0; k0 < inf.p_hi; k0 += 32) {
+      int32_t id = -1;
+      if (k0 + lane < inf.p_hi) {
+        int64_t idx = ring + k0 + lane;
+        if (idx >= a.F) idx -= a.F;
+        if (in_range(idx, a.F, a.status)) {
+          id = __ldg(a.free_list + idx);
+          if (!in_range(id, a.F, a.status)) id = -1;
+        }
+      }
+      const int32_t ne = min(inf.p_hi - k0, 32) * per;
+      for (int32_t e0 = 0; e0 < ne; e0 += 32) {  // warp-uniform trip count
+        const int32_t e = e0 + lane;
+        const int32_t pid = __shfl_sync(0xffffffffu, id, min(e / per, 31));
+        if (e < ne && pid >= 0) {
+          uint8_t *pg = a.pages + static_cast<int64_t>(pid) * g.bytes;
+          const int32_t c = e % per;
+          if (c < per / 2) reinterpret_cast<uint4 *>(pg + g.meta + 8 * static_cast<int64_t>(per))[c] = make_uint4(0u, 0u, 0u, 0u);
+          else reinterpret_cast<int2 *>(pg + g.pos + 4 * static_cast<int64_t>(per))[c - per / 2] = make_int2(-1, -1);
+        }
+      }
+    }
+  }
+}
+
 // Commit of a successful call: forward and reverse tables, page classes,
-// unit headers, the head cursor; and the unused slots of the new pages (zero
-// codes and metadata, position -1): slots P..2P-1 of every high page and the
-// tail of each unit's last high and low page.  A failed call only records
-// its error in the pool's status word.
+// unit headers, the head cursor; and the tail of each unit's last high and
+// low page (zero codes and metadata, position -1).  A failed call only
+// records its error in the pool's status word.
 __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
   const int32_t err = a.ws->err;
   if (err != 0) {
@@ -264,22 +309,6 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
         a.rev_idx[id] = k;
         a.page_cls[id] = k < inf.p_hi ? DKV_CLASS_K8V4 : DKV_CLASS_K4V2;
       }
-      // a high page has no slots P..2P-1: their metadata (8P bytes: P/2
-      // chunks of 16) and positions (4P bytes: P/2 chunks of 8; P is even)
-      // are cleared, consecutive lanes writing consecutive chunks of one page
-      // whose id comes from the lane that loaded it
-      const int32_t per = static_cast<int32_t>(P);  // chunks per page
-      const int32_t ne = max(min(inf.p_hi - k0, 32), 0) * per;
-      for (int32_t e0 = 0; e0 < ne; e0 += 32) {  // warp-uniform trip count
-        const int32_t e = e0 + lane;
-        const int32_t pid = __shfl_sync(0xffffffffu, id, min(e / per, 31));
-        if (e < ne && pid >= 0) {
-          uint8_t *pg = a.pages + static_cast<int64_t>(pid) * page_bytes;
-          const int32_t c = e % per;
-          if (c < per / 2) reinterpret_cast<uint4 *>(pg + g.meta + 8 * P)[c] = make_uint4(0u, 0u, 0u, 0u);
-          else reinterpret_cast<int2 *>(pg + g.pos + 4 * P)[c - per / 2] = make_int2(-1, -1);
-        }
-      }
       id = id_next;
     }
     if (lane == 0) reinterpret_cast<int4 *>(a.unit_hdr)[u] = make_int4(inf.n_hi, inf.n_lo, inf.p_hi, p_lo);
@@ -306,6 +335,11 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(CompactArgs a) {
 
 cudaError_t launch_scan(const CompactArgs &a, int npart, cudaStream_t s) {
   k_scan<<<npart, kScanThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_clear_hi(const CompactArgs &a, int grid, cudaStream_t s) {
+  k_clear_hi<<<grid, kClearThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

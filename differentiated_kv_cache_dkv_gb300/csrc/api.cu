@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -31,6 +32,42 @@ bool device_info(int *sms, int *pack_bps) {
   *sms = g_sms[dev];
   *pack_bps = g_pack_bps[dev];
   return true;
+}
+
+// A second stream per device for work that runs beside k_pack, with the
+// events that fork it from the caller's stream and join it back.  The events
+// are shared, so a fork and its join are enqueued under the mutex.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[kMaxDevices];
+
+// The current device's side stream, created on first use; call with
+// g_side_mu held.
+cudaError_t side_stream(SideStream **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  SideStream &ss = g_side[dev];
+  if (!ss.s) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if ((e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&f, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&j, cudaEventDisableTiming)) != cudaSuccess) {
+      if (f) cudaEventDestroy(f);
+      cudaStreamDestroy(st);
+      return e;
+    }
+    ss.s = st;
+    ss.fork = f;
+    ss.join = j;
+  }
+  *out = &ss;
+  return cudaSuccess;
 }
 
 thread_local cudaError_t g_last_cuda = cudaSuccess;
@@ -231,8 +268,20 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
   mark(2);
   if (const int32_t rc = cuda_status(dkv::launch_scan(a, lay.npart, s))) return rc;
   mark(3);
-  if (const int32_t rc = cuda_status(dkv::launch_pack(a, pack_grid, s))) return rc;
-  mark(4);
+  {
+    // the unused halves of the new high pages are cleared on the side stream
+    // while k_pack runs (they need only the scan's placement)
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream *ss = nullptr;
+    if (const int32_t rc = cuda_status(side_stream(&ss))) return rc;
+    if (const int32_t rc = cuda_status(cudaEventRecord(ss->fork, s))) return rc;
+    if (const int32_t rc = cuda_status(cudaStreamWaitEvent(ss->s, ss->fork, 0))) return rc;
+    if (const int32_t rc = cuda_status(dkv::launch_clear_hi(a, sms, ss->s))) return rc;
+    if (const int32_t rc = cuda_status(cudaEventRecord(ss->join, ss->s))) return rc;
+    if (const int32_t rc = cuda_status(dkv::launch_pack(a, pack_grid, s))) return rc;
+    mark(4);
+    if (const int32_t rc = cuda_status(cudaStreamWaitEvent(s, ss->join, 0))) return rc;
+  }
   if (const int32_t rc = cuda_status(dkv::launch_commit(a, std::max(commit_grid, 1), s))) return rc;
   mark(5);
   return DKV_OK;

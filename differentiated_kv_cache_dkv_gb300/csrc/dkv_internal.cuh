@@ -380,6 +380,7 @@ cudaError_t launch_classify(const CompactArgs &a, int grid, int sms, cudaStream_
 cudaError_t launch_scan(const CompactArgs &a, int npart, cudaStream_t s);
 cudaError_t launch_pack(const CompactArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_commit(const CompactArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_clear_hi(const CompactArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_init_pool(const dkv_pool &p, cudaStream_t s);
 cudaError_t launch_dequant(const dkv_pool &p, const int32_t *ids, int32_t one_id, int32_t n,
                            float *k_out, float *v_out, int32_t *pos_out, cudaStream_t s);

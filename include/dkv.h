@@ -174,7 +174,15 @@ int32_t dkv_init_pool(const dkv_pool *pool, void *stream);
  * page ids taken from free-list slots [head + off_u, head + off_u + d_u) mod F
  * (off_u = exclusive prefix sum of d_u = ceil(n_k8v4 / P) + ceil(n_k4v2 / 2P)),
  * rev_unit / rev_idx / page_cls describe those pages, the pages hold the
- * packed tokens, and head advanced by sum(d_u). */
+ * packed tokens, and head advanced by sum(d_u).
+ * One part of the work, clearing the unused slot halves of the new K8V4
+ * pages, runs on a library-owned second stream of the current device: it is
+ * forked from `stream` after the page scan and joined back before the
+ * commit, so the call's effects are ordered on `stream` as if it ran there
+ * alone (under stream capture it becomes a fork and a join of the graph).
+ * The first call on a device creates that stream and two events; make it
+ * before any stream capture.  Calls from several host threads are safe (the
+ * fork and join are enqueued under a lock). */
 int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *pool,
                     const dkv_tables *t, void *workspace, size_t workspace_bytes,
                     void *stream);
@@ -190,7 +198,8 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
  * that device current; make that first call before any stream capture.  The
  * array is shared by all calls on a device and keeps the last call's contents
  * (nothing in it needs to start at zero): calls that overlap on the GPU race,
- * so order them on one stream.  Allocates nothing. */
+ * so order them on one stream.  Allocates no device memory (the first call
+ * on a device creates dkv_compact's second stream and its events). */
 #define DKV_NOALLOC_SCRATCH_BYTES (16u << 20)
 int32_t dkv_compact_noalloc(const dkv_batch *b, const dkv_params *p, const dkv_pool *pool,
                             const dkv_tables *t, void *stream);
