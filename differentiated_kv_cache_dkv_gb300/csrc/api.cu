@@ -1,6 +1,7 @@
 // api.cu -- the libdkv C ABI: argument validation, workspace layout, kernel
 // launches, status and profiling.  Every entry point is declared, with its
 // argument meaning, layout, ownership and error behaviour, in include/dkv.h.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -34,39 +35,75 @@ bool device_info(int *sms, int *pack_bps) {
   return true;
 }
 
-// A second stream per device for work that runs beside k_pack, with the
-// events that fork it from the caller's stream and join it back.  The events
-// are shared, so a fork and its join are enqueued under the mutex.
+// A second stream for work that runs beside k_pack, with the events that fork
+// it from the caller's stream and join it back, one set per CUDA context
+// (keyed by the context's unique id, which a context made after
+// cudaDeviceReset does not share, so no handle of a destroyed context is
+// reused).  The events are shared, so a fork and its join are enqueued under
+// the mutex.
 struct SideStream {
+  unsigned long long ctx = 0;
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
 std::mutex g_side_mu;
-SideStream g_side[kMaxDevices];
+std::vector<SideStream> g_side;
 
-// The current device's side stream, created on first use; call with
+// Unique id of the calling thread's current context (the runtime makes the
+// device's primary context current if there is none yet).  Call with
+// g_side_mu held (the entry points are cached in statics).
+cudaError_t current_context_id(unsigned long long *id) {
+  using GetCurrent = CUresult (*)(CUcontext *);
+  using GetId = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  if (!get_current || !get_id) {
+    void *f = nullptr, *g = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q1);
+    if (e != cudaSuccess) return e;
+    e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &g, 12000, cudaEnableDefault, &q2);
+    if (e != cudaSuccess) return e;
+    if (q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f || !g)
+      return cudaErrorNotSupported;
+    get_current = reinterpret_cast<GetCurrent>(f);
+    get_id = reinterpret_cast<GetId>(g);
+  }
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (!c) {  // no context current yet: the runtime makes the device's primary one current
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    if (get_current(&c) != CUDA_SUCCESS || !c) return cudaErrorDeviceUninitialized;
+  }
+  if (get_id(c, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
+
+// The current context's side stream, created on first use; call with
 // g_side_mu held.
 cudaError_t side_stream(SideStream **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  unsigned long long ctx = 0;
+  cudaError_t e = current_context_id(&ctx);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  SideStream &ss = g_side[dev];
-  if (!ss.s) {
-    cudaStream_t st = nullptr;
-    cudaEvent_t f = nullptr, j = nullptr;
-    if ((e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&f, cudaEventDisableTiming)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&j, cudaEventDisableTiming)) != cudaSuccess) {
-      if (f) cudaEventDestroy(f);
-      cudaStreamDestroy(st);
-      return e;
+  for (SideStream &ss : g_side)
+    if (ss.ctx == ctx) {
+      *out = &ss;
+      return cudaSuccess;
     }
-    ss.s = st;
-    ss.fork = f;
-    ss.join = j;
+  SideStream ss;
+  ss.ctx = ctx;
+  if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+  if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) {
+    if (ss.fork) cudaEventDestroy(ss.fork);
+    cudaStreamDestroy(ss.s);
+    return e;
   }
-  *out = &ss;
+  g_side.push_back(ss);
+  *out = &g_side.back();
   return cudaSuccess;
 }
 

@@ -180,9 +180,11 @@ int32_t dkv_init_pool(const dkv_pool *pool, void *stream);
  * forked from `stream` after the page scan and joined back before the
  * commit, so the call's effects are ordered on `stream` as if it ran there
  * alone (under stream capture it becomes a fork and a join of the graph).
- * The first call on a device creates that stream and two events; make it
- * before any stream capture.  Calls from several host threads are safe (the
- * fork and join are enqueued under a lock). */
+ * The first call in a CUDA context creates that stream and two events, kept
+ * for that context until process exit (a context made after cudaDeviceReset
+ * gets its own); make that first call before any stream capture.  Calls from
+ * several host threads are safe (the fork and join are enqueued under a
+ * lock). */
 int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *pool,
                     const dkv_tables *t, void *workspace, size_t workspace_bytes,
                     void *stream);
@@ -193,10 +195,10 @@ int32_t dkv_compact(const dkv_batch *b, const dkv_params *p, const dkv_pool *poo
  * DKV_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
  * process exit.  A batch whose dkv_workspace_size exceeds that limit is
  * rejected with DKV_E_INVAL before anything is enqueued (the Llama-3-8B-shaped
- * batch of 32 layers x 16 x 4096 tokens needs about 12.5 MiB).  The first call
- * on a device resolves the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  The
- * array is shared by all calls on a device and keeps the last call's contents
+ * batch of 32 layers x 16 x 4096 tokens needs about 12.5 MiB).  Every call
+ * resolves the array's device address in the current context
+ * (cudaGetSymbolAddress, which loads the library's module on first use); make
+ * the first call on a device before any stream capture.  The array is shared by all calls on a device and keeps the last call's contents
  * (nothing in it needs to start at zero): calls that overlap on the GPU race,
  * so order them on one stream.  Allocates no device memory (the first call
  * on a device creates dkv_compact's second stream and its events). */
