@@ -144,6 +144,9 @@ def test_decode_small_ragged_with_wrap():
     dict(Hq=28, Hkv=4, P=32, lens=[1000, 33, 700], alpha_h=1.5, alpha_l=0.3, sigma=2.5),  # G = 7, scalar loads
     dict(Hq=16, Hkv=2, P=16, lens=[2100, 64], L=1),                                     # G = 8, two float4
     dict(Hq=4, Hkv=4, P=2, lens=[90, 91, 1], L=1),                                       # G = 1, tiny pages
+    dict(Hq=4, Hkv=1, P=16, lens=[700, 130], L=1),                                       # G = 4, one row a thread
+    dict(Hq=12, Hkv=3, P=16, lens=[400, 257, 1], L=1),                                   # G = 4, Hkv not 2^k
+    dict(Hq=32, Hkv=8, P=16, lens=[600, 70, 333], L=2),                                  # G = 4, head pairs
 ])
 def test_decode_shapes(shape):
     w = W.small("dec_shape", **shape)
