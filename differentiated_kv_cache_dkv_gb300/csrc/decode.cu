@@ -1028,10 +1028,12 @@ __device__ void apply_unit(const DecodeArgs &a, UnitView &v, uint32_t *rh, uint3
     if (id >= 0) clear_page(a, id, lane);
   }
   __syncwarp();
-  hole_fill<S>(a, v, false, rl, p.keep_lo, p.n_lo, buf, lane);   // K4V2 list
-  demote<S>(a, v, dem, buf, lane);                               // appended after its survivors
+  // a list that lost no token has no holes, and a unit that demoted none has
+  // nothing to stage: their bitmap scans are skipped (warp-uniform tests)
+  if (p.keep_lo < p.n_lo) hole_fill<S>(a, v, false, rl, p.keep_lo, p.n_lo, buf, lane);  // K4V2 list
+  if (p.dem > 0) demote<S>(a, v, dem, buf, lane);  // appended after its survivors
   __syncwarp();
-  hole_fill<S>(a, v, true, rh, p.keep_hi, p.n_hi, buf, lane);    // K8V4 list (demoted slots read)
+  if (p.keep_hi < p.n_hi) hole_fill<S>(a, v, true, rh, p.keep_hi, p.n_hi, buf, lane);  // K8V4 list (demoted slots read)
   if (p.new_cls != DKV_CLASS_PRUNE) append_new<S>(a, v, lane);
   __syncwarp();
   // vacated slots of the pages the lists keep
