@@ -1018,6 +1018,12 @@ __device__ void apply_unit(const DecodeArgs &a, UnitView &v, uint32_t *rh, uint3
   const DecPlan &p = v.p;
   const int32_t n2_hi = p.keep_hi + (p.new_cls == DKV_CLASS_K8V4);
   const int32_t n2_lo = p.keep_lo + p.dem + (p.new_cls == DKV_CLASS_K4V2);
+  // the new token's K and V rows, read at the append near the end: start
+  // their way into L2 now
+  if (lane == 0 && p.new_cls != DKV_CLASS_PRUNE) {
+    prefetch_l2(a.k_new + v.u * DKV_HEAD_DIM, 2 * DKV_HEAD_DIM);
+    prefetch_l2(a.v_new + v.u * DKV_HEAD_DIM, 2 * DKV_HEAD_DIM);
+  }
   // new pages start clear
   for (int32_t k = p.have_hi; k < p.need_hi; ++k) {
     const int32_t id = list_page(a, v, true, k);
@@ -1049,9 +1055,11 @@ __device__ void apply_unit(const DecodeArgs &a, UnitView &v, uint32_t *rh, uint3
       if (slot_addr(a, v, false, s, t)) clear_slot(t, k_units<S>(false), v_units<S>(false));
     }
   }
-  // tables: stage the kept K4V2 page ids, free the surplus, rewrite the row
+  // tables: stage the kept K4V2 page ids (only when the K8V4 page count
+  // changes, which moves them in the row), free the surplus, rewrite the row
   const int32_t keep_lo_pages = min(p.have_lo, p.need_lo);
-  for (int32_t k = lane; k < keep_lo_pages; k += 32) stage[k] = v.fw[p.have_hi + k];
+  if (p.need_hi != p.have_hi)
+    for (int32_t k = lane; k < keep_lo_pages; k += 32) stage[k] = v.fw[p.have_hi + k];
   int32_t fj = 0;
   const uint64_t tail = a.ws->tail + static_cast<uint64_t>(p.off_f);
   for (int32_t k = p.need_hi + lane; k < p.have_hi; k += 32) {
