@@ -98,17 +98,29 @@ PACK_TRAFFIC = {"workload": "llama", "source_sha1": "8053ae355a66", "bytes": 16 
 # DRAM traffic of k_reclass per algorithmic byte, from one ncu capture on 4
 # layers x 64 requests of the decode workload (180.6 MB for 176.2 MB; traffic
 # grows with the live rows) (profiles/decode_step.md); valid only for the
-# kernel source it was measured on.
-RECLASS_TRAFFIC = {"workload": "decode", "source_sha1": "cb145cbff917", "per_byte": (177.17376 + 3.397632) / 176.177616}
+# kernel source it was measured on.  That source is decode.cu up to the next
+# kernel's definition (k_candidate): k_reclass and every device helper it
+# calls precede it, so later edits to the apply kernels keep the figure.
+RECLASS_TRAFFIC = {"workload": "decode", "source_sha1": "a334c0a2478c", "upto": b"k_candidate(DecodeArgs a)",
+                   "per_byte": (177.17376 + 3.397632) / 176.177616}
 
 
-def _source_sha(name: str):
+def _source_sha(name: str, upto: bytes = None):
+    """First 12 hex digits of the SHA-1 of a csrc file, or of its lines before
+    the first line holding `upto` (None if the file or the marker is missing)."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "differentiated_kv_cache_dkv_gb300", "csrc", name), "rb") as f:
-            return hashlib.sha1(f.read()).hexdigest()[:12]
+            data = f.read()
     except OSError:
         return None
+    if upto is not None:
+        lines = data.split(b"\n")
+        cut = next((i for i, line in enumerate(lines) if upto in line), None)
+        if cut is None:
+            return None
+        data = b"\n".join(lines[:cut])
+    return hashlib.sha1(data).hexdigest()[:12]
 
 
 def _pack_traffic(workload: str):
@@ -118,7 +130,7 @@ def _pack_traffic(workload: str):
 
 
 def _reclass_traffic(workload: str, alg_bytes: float):
-    if workload != RECLASS_TRAFFIC["workload"] or _source_sha("decode.cu") != RECLASS_TRAFFIC["source_sha1"]:
+    if workload != RECLASS_TRAFFIC["workload"] or _source_sha("decode.cu", RECLASS_TRAFFIC["upto"]) != RECLASS_TRAFFIC["source_sha1"]:
         return None
     return RECLASS_TRAFFIC["per_byte"] * alg_bytes
 
