@@ -93,7 +93,7 @@ SCHEME_NAMES = {0: "K8V4/K4V2", 1: "K8V2/K4V1", 2: "K4V8/K2V4"}
 # ncu capture of the same kernel on 2 of its 32 layers scaled by the units
 # processed (profiles/k_pack_llama_prefill.md); valid only for the kernel
 # source it was measured on.
-PACK_TRAFFIC = {"workload": "llama", "source_sha1": "8053ae355a66", "bytes": 16 * (537.714944 + 130.876928) * 1e6}
+PACK_TRAFFIC = {"workload": "llama", "source_sha1": "99bd3387b01d", "bytes": 16 * (537.732608 + 130.183424) * 1e6}
 
 # DRAM traffic of k_reclass per algorithmic byte, from one ncu capture on 4
 # layers x 64 requests of the decode workload (180.6 MB for 176.2 MB; traffic

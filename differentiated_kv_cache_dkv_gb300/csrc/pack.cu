@@ -32,7 +32,7 @@
 //       stores the list of surviving rows (K8V4 first, ranks by popcount of
 //       the class bitmasks) with page id (from the circular free list), slot
 //       and position, and arrives on it.
-//   consumer warps (18) claim 8-row groups of a stage from a shared counter
+//   consumer warps (19) claim 8-row groups of a stage from a shared counter
 //       (low-class rows start at a multiple of 8, so a group is
 //       class-uniform: one pair of K / V widths of the pool's scheme),
 //       one row per 4-lane group: bf16x2 min / max reduced over the group,
@@ -45,7 +45,7 @@
 //       group, so the 8 rows a warp reads at once (256 bytes apart) fall on
 //       all 32 shared-memory banks.  A warp
 //       that finds no group left arrives on the stage's "empty" mbarrier and
-//       moves on; the stage is refilled once all 16 have left it.
+//       moves on; the stage is refilled once every consumer warp has left it.
 // Unused slots of the pages are filled by k_commit, which walks every page.
 // Every mbarrier wait is bounded by the global timer (about a second); on
 // expiry the CTA records DKV_E_TIMEOUT, drains its own copies in flight
@@ -64,9 +64,10 @@ namespace {
 
 constexpr int kStages = 3;
 constexpr int kProducerWarps = 1;
-// 18 consumer warps: the most whose registers (94 a thread) fit one block per
-// SM without spilling; 16 measured 1.4% slower on the Llama prefill, 20 spill.
-constexpr int kConsumerWarps = 18;
+// 19 consumer warps: the most whose registers (88 a thread) fit one block per
+// SM without spilling; 18 measured 1.2% slower on the Llama prefill (same GPU,
+// alternating runs), 16 slower still, and 20 spill.
+constexpr int kConsumerWarps = 19;
 constexpr int kPackThreads = 32 * (kConsumerWarps + kProducerWarps);
 constexpr uint64_t kWaitNs = 1000000000ull;  // an mbarrier wait gives up after about a second
 constexpr uint32_t kWaitPolls = 1u << 26;    // ... or after this many polls, whichever is first
